@@ -1,0 +1,161 @@
+"""CPU oracle of the Tensor-Train embedding bag -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its
+binding) never calls it and shares no code with it.
+
+The arithmetic lives in ``tt_oracle.c`` (plain fp64 C, one naive chained
+contraction per lookup, see its header for the definitions and the passages
+they follow).  This module only compiles it with gcc and marshals numpy arrays
+through ctypes.
+
+Pins (tests/test_oracle_pins.py): a hand-worked example (tests/golden/),
+exact reconstruction of a dense table through a TT-SVD, Kronecker rows for
+rank-1 cores, a materialised table + torch embedding_bag, multilinearity,
+the adjoint identity and torch autograd for the backward, and numpy
+lexsort/unique for the grouping.  No function here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tt_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libtt_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+TTO_OK, TTO_ERR_ARG, TTO_ERR_INDEX, TTO_ERR_OFFSETS, TTO_ERR_NOMEM = 0, -1, -2, -3, -4
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what} returned {code}")
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    """Compile tt_oracle.c into oracle/_build/libtt_oracle.so (gcc, -O2)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-o", tmp, _SRC])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            lib.tto_forward.argtypes = [P, P, P, P, P, P, P, I64, P, I64, P, ctypes.c_int]
+            lib.tto_forward.restype = ctypes.c_int
+            lib.tto_backward.argtypes = [P, P, P, P, P, P, P, P, I64, P, I64, P, P, P,
+                                         ctypes.c_int, I64, ctypes.c_int]
+            lib.tto_backward.restype = ctypes.c_int
+            lib.tto_sgd.argtypes = [P, P, I64, ctypes.c_double, P]
+            lib.tto_sgd.restype = None
+            lib.tto_group.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P]
+            lib.tto_group.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _shape_args(m, n, R):
+    m_a = np.ascontiguousarray(m, dtype=np.int64)
+    n_a = np.ascontiguousarray(n, dtype=np.int32)
+    R_a = np.ascontiguousarray(R, dtype=np.int32)
+    return m_a, n_a, R_a
+
+
+def _cores(cores):
+    return [np.ascontiguousarray(c, dtype=np.float32) for c in cores]
+
+
+def forward(cores, m, n, R, indices, offsets, threads: int = 1, strict: bool = True):
+    """fp64 pooled output [B][D] (naive chained contraction per lookup, then sum)."""
+    lib = _load()
+    G = _cores(cores)
+    m_a, n_a, R_a = _shape_args(m, n, R)
+    idx = np.ascontiguousarray(indices, dtype=np.int64)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    B = off.shape[0] - 1
+    D = int(n_a.prod())
+    out = np.zeros((max(B, 0), D), dtype=np.float64)
+    rc = lib.tto_forward(_p(G[0]), _p(G[1]), _p(G[2]), _p(m_a), _p(n_a), _p(R_a), _p(idx),
+                         idx.shape[0], _p(off), B, _p(out), int(threads))
+    if rc != TTO_OK and (strict or rc != TTO_ERR_INDEX):
+        raise OracleError(rc, "tto_forward")
+    return out
+
+
+def backward(grad_out, cores, m, n, R, indices, offsets, threads: int = 1,
+             filter_core: int = 0, filter_value: int = 0, strict: bool = True):
+    """fp64 core gradients [dG1, dG2, dG3] of <grad_out, out> (fresh zeros, then +=)."""
+    lib = _load()
+    G = _cores(cores)
+    m_a, n_a, R_a = _shape_args(m, n, R)
+    idx = np.ascontiguousarray(indices, dtype=np.int64)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    g = np.ascontiguousarray(grad_out, dtype=np.float32)
+    B = off.shape[0] - 1
+    dG = [np.zeros(c.shape, dtype=np.float64) for c in G]
+    rc = lib.tto_backward(_p(g), _p(G[0]), _p(G[1]), _p(G[2]), _p(m_a), _p(n_a), _p(R_a),
+                          _p(idx), idx.shape[0], _p(off), B, _p(dG[0]), _p(dG[1]), _p(dG[2]),
+                          int(filter_core), int(filter_value), int(threads))
+    if rc != TTO_OK and (strict or rc != TTO_ERR_INDEX):
+        raise OracleError(rc, "tto_backward")
+    return dG
+
+
+def sgd(core, dcore, lr: float):
+    """fp64 G - lr*dG."""
+    lib = _load()
+    G = np.ascontiguousarray(core, dtype=np.float32)
+    dG = np.ascontiguousarray(dcore, dtype=np.float64)
+    out = np.empty(G.shape, dtype=np.float64)
+    lib.tto_sgd(_p(G), _p(dG), G.size, float(lr), _p(out))
+    return out
+
+
+def group(indices, m):
+    """Grouping reference: stable sort by (i2, i1, i3) and unique runs (see tt_oracle.c)."""
+    lib = _load()
+    idx = np.ascontiguousarray(indices, dtype=np.int64)
+    nnz = idx.shape[0]
+    m_a = np.ascontiguousarray(m, dtype=np.int64)
+    cap = max(nnz, 1)
+    perm = np.empty(cap, np.int32)
+    row_start = np.empty(cap + 1, np.int32)
+    row_index = np.empty(cap, np.int64)
+    row_pair = np.empty(cap, np.int32)
+    pair_row_start = np.empty(cap + 1, np.int32)
+    pair_i1 = np.empty(cap, np.int32)
+    pair_i2 = np.empty(cap, np.int32)
+    uid = np.empty(cap, np.int32)
+    counts = np.zeros(3, np.int64)
+    rc = lib.tto_group(_p(idx), nnz, _p(m_a), _p(perm), _p(row_start), _p(row_index),
+                       _p(row_pair), _p(pair_row_start), _p(pair_i1), _p(pair_i2), _p(uid),
+                       _p(counts))
+    if rc not in (TTO_OK, TTO_ERR_INDEX):
+        raise OracleError(rc, "tto_group")
+    nv, ur, up = (int(v) for v in counts)
+    return dict(n_valid=nv, U_r=ur, U_12=up, perm=perm[:nv].copy(),
+                row_start=row_start[:ur + 1].copy(), row_index=row_index[:ur].copy(),
+                row_pair=row_pair[:ur].copy(), pair_row_start=pair_row_start[:up + 1].copy(),
+                pair_i1=pair_i1[:up].copy(), pair_i2=pair_i2[:up].copy(),
+                uid=uid[:nnz].copy(), status=rc)
