@@ -1,0 +1,144 @@
+/*
+ * tt_emb.h -- C ABI of the GB300 Tensor-Train embedding bag.
+ *
+ * The operation (FlowTT: Exploiting Computation Flow Reuse in Irregular
+ * Tensor-Train Embedding, summary card, problem statement; TT-Rec: Tensor
+ * Train Compression for Deep Learning Recommendation Models, abstract):
+ * a table of M = m1*m2*m3 rows of width D = n1*n2*n3 is held as three TT
+ * cores; looking up row r contracts the chain of cores selected by the
+ * mixed-radix digits of r, and the looked-up rows are sum-pooled per bag.
+ *
+ *   core k:   float32, contiguous [m_k][R_{k-1}][n_k][R_k], R_0 = R_3 = 1
+ *   row r:    r = (i1*m2 + i2)*m3 + i3 (i1 most significant)
+ *   row(r)[j] = sum_{a,b} G1[i1][0][j1][a] * G2[i2][a][j2][b] * G3[i3][b][j3][0],
+ *             j = (j1*n2 + j2)*n3 + j3
+ *   bags:     CSR; offsets has num_bags+1 int64 entries, offsets[0] = 0,
+ *             offsets[num_bags] = nnz, non-decreasing; bag b holds lookups
+ *             offsets[b] .. offsets[b+1]-1 of `indices` (int64 row numbers)
+ *   out[b]    = sum over the bag's lookups of row(indices[l]); empty bag -> 0
+ *
+ * How it is computed (FlowTT, summary card, key innovations; FlowTT
+ * abstract): lookups are grouped by their (i1, i2) prefix on the device
+ * (radix sort + run segmentation), the prefix partial P2 = G1[i1].G2[i2] is
+ * formed once per unique prefix and kept on chip, each unique row is formed
+ * once from it, and rows are pooled per bag.  Persistent CTAs take work
+ * chunks from an atomic queue so that Zipf-skewed prefixes do not stall the
+ * grid.
+ *
+ * Conventions for every entry point:
+ *  - All array arguments are DEVICE pointers owned by the caller (CUDA
+ *    global memory of the current device).  The library allocates nothing
+ *    and keeps no state between calls beyond the caller's workspace.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call only enqueues work on it and returns; none synchronises except
+ *    tt_emb_get_error.
+ *  - Shape arguments (m, n, R) are HOST arrays: m[3] int64, n[3] int32,
+ *    R[4] int32.
+ *  - Returns TT_EMB_OK (0) or a negative TT_EMB_ERR_* code.  Argument errors
+ *    are detected on the host before anything is enqueued.  Errors found by
+ *    the kernels (an index outside [0, M), bad offsets, a capped wait that
+ *    gave up) never trap: they set a status word in the workspace, the
+ *    offending lookups contribute nothing, and tt_emb_get_error reports them.
+ *
+ * Limits: M <= 2^32 - 2, nnz < 2^30, num_bags < 2^31, every m_k < 2^31,
+ * and R1*n2*R2 + n1*R1 + 2*n1*n2*R2 <= 53248 (the G2 slice and one prefix
+ * partial must fit in shared memory); larger shapes return
+ * TT_EMB_ERR_UNSUPPORTED.  Cores, out, grad_out and workspace must be
+ * 16-byte aligned (workspace: 256-byte).
+ */
+#ifndef TT_EMB_H
+#define TT_EMB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TT_EMB_OK 0
+#define TT_EMB_ERR_ARG (-1)          /* null pointer, bad dims, R[0] != 1, misalignment ...  */
+#define TT_EMB_ERR_WORKSPACE (-2)    /* ws_bytes smaller than tt_emb_workspace_bytes         */
+#define TT_EMB_ERR_CUDA (-3)         /* a launch or runtime call failed                      */
+#define TT_EMB_ERR_INDEX (-4)        /* device: an index outside [0, M)                      */
+#define TT_EMB_ERR_OFFSETS (-5)      /* device: offsets not CSR (see above)                  */
+#define TT_EMB_ERR_TIMEOUT (-6)      /* device: a capped inter-CTA wait gave up              */
+#define TT_EMB_ERR_UNSUPPORTED (-7)  /* shape beyond the limits above                        */
+
+/* Bytes of workspace that forward/backward/group need for this shape and
+ * batch.  The workspace holds the prefix grouping (sorted lookups, unique
+ * rows, unique prefixes, work chunks), the unique-row buffer and a status
+ * word.  Host-only; touches no device memory. */
+int tt_emb_workspace_bytes(const int64_t m[3], const int32_t n[3], const int32_t R[4],
+                           int64_t nnz, int64_t num_bags, size_t* bytes);
+
+/* Prefix grouping only (index decomposition, radix sort by (i2, i1, i3),
+ * unique rows / unique (i1,i2) prefixes, work chunks), written into the
+ * workspace.  FlowTT summary card, key innovations ("prefix-based index
+ * grouping").  tt_emb_forward calls this itself. */
+int tt_emb_group(const int64_t m[3], const int32_t n[3], const int32_t R[4],
+                 const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                 int64_t num_bags, void* workspace, size_t ws_bytes, void* stream);
+
+/* Forward TT embedding bag.  cores[k] as above; out is float32 [num_bags][D]
+ * row-major and is overwritten (every bag, empty ones with zeros).  The
+ * grouping it builds stays in the workspace for a later
+ * tt_emb_backward(..., reuse_grouping = 1). */
+int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_t n[3],
+                   const int32_t R[4], const int64_t* indices, int64_t nnz,
+                   const int64_t* offsets, int64_t num_bags, float* out, void* workspace,
+                   size_t ws_bytes, void* stream);
+
+/* Backward into the cores: core_grads[k] (same layout as cores[k]) are
+ * ACCUMULATED (+=) with d<grad_out, out>/dG_k; the caller zeroes them.
+ * grad_out is float32 [num_bags][D].  With reuse_grouping != 0 the grouping
+ * left in the workspace by the last tt_emb_forward / tt_emb_group on the SAME
+ * indices, offsets and shape is reused (the caller guarantees that);
+ * otherwise it is rebuilt.  The accumulation uses float atomics, so the
+ * summation order (and the last bits) may differ from call to call. */
+int tt_emb_backward(const float* grad_out, const float* const cores[3], const int64_t m[3],
+                    const int32_t n[3], const int32_t R[4], const int64_t* indices, int64_t nnz,
+                    const int64_t* offsets, int64_t num_bags, float* const core_grads[3],
+                    void* workspace, size_t ws_bytes, int reuse_grouping, void* stream);
+
+/* Plain SGD on the three cores: G_k <- G_k - lr * dG_k (element-wise, fp32). */
+int tt_emb_sgd(float* const cores[3], const float* const core_grads[3], const int64_t m[3],
+               const int32_t n[3], const int32_t R[4], float lr, void* stream);
+
+/* Synchronises `stream`, then reads the workspace status word written by the
+ * kernels of the calls enqueued so far.  *device_status receives the raw
+ * bit set (1 = index out of range, 2 = bad offsets, 4 = timeout).  Returns
+ * TT_EMB_OK or the code of the most severe condition found
+ * (TIMEOUT > OFFSETS > INDEX), or TT_EMB_ERR_CUDA. */
+int tt_emb_get_error(const void* workspace, void* stream, int* device_status);
+
+/* Device pointers into a workspace holding a grouping (pure pointer
+ * arithmetic; reads no device memory).  For inspection and tests. */
+typedef struct {
+  const int32_t* counts;          /* [0] valid lookups, [1] U_r unique rows, [2] U_12 unique
+                                     (i1,i2) prefixes, [3] work chunks, [4] status bits     */
+  const int32_t* perm;            /* [nnz]   lookup positions sorted by (i2,i1,i3, position);
+                                              out-of-range lookups last                     */
+  const int32_t* row_start;       /* [U_r+1] first sorted position of each unique row         */
+  const int32_t* row_i3;          /* [U_r]   i3 digit of each unique row                       */
+  const int32_t* row_pair;        /* [U_r]   unique prefix of each unique row                  */
+  const int32_t* pair_row_start;  /* [U_12+1] first unique row of each unique prefix           */
+  const int32_t* pair_i1;         /* [U_12]                                                     */
+  const int32_t* pair_i2;         /* [U_12]                                                     */
+  const int32_t* uid;             /* [nnz]   unique row of each lookup, -1 if out of range      */
+  const int32_t* bag_of;          /* [nnz]   bag of each lookup                                */
+  const int32_t* chunk_start;     /* [chunks+1] first unique row of each work chunk             */
+  const float* rowbuf;            /* [U_r][D] unique rows (after a forward)                    */
+} tt_emb_grouping;
+
+int tt_emb_grouping_view(const int64_t m[3], const int32_t n[3], const int32_t R[4],
+                         int64_t nnz, int64_t num_bags, const void* workspace,
+                         tt_emb_grouping* view);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int tt_emb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TT_EMB_H */

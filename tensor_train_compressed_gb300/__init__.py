@@ -1,0 +1,108 @@
+"""GB300-native Tensor-Train embedding bag (forward, backward, SGD).
+
+The compute runs in libtt_emb.so (hand-written CUDA for sm_103a behind the C
+ABI of include/tt_emb.h).  This package is the thin Python side: the ctypes
+binding with the C names (``tt_emb_*``), a small owner object for cores and
+workspace, and the seeded input recipe (``inputs``).  PyTorch supplies device
+memory and streams only.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from ._binding import (EXPORTED, TTEmbError, library_path, lib, tt_emb_backward,
+                       tt_emb_forward, tt_emb_get_error, tt_emb_group, tt_emb_grouping_view,
+                       tt_emb_sgd, tt_emb_version, tt_emb_workspace_bytes)
+from ._binding import (TT_EMB_ERR_ARG, TT_EMB_ERR_CUDA, TT_EMB_ERR_INDEX, TT_EMB_ERR_OFFSETS,
+                       TT_EMB_ERR_TIMEOUT, TT_EMB_ERR_UNSUPPORTED, TT_EMB_ERR_WORKSPACE, TT_EMB_OK)
+
+__all__ = ["TTEmbeddingBag", "TTEmbError", "tt_emb_forward", "tt_emb_backward", "tt_emb_sgd",
+           "tt_emb_group", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_workspace_bytes",
+           "tt_emb_version", "read_grouping", "lib", "library_path", "EXPORTED"]
+
+
+def read_grouping(m, n, R, nnz: int, num_bags: int, workspace: torch.Tensor) -> dict:
+    """Copy the grouping held in ``workspace`` to host numpy arrays (inspection/tests)."""
+    view = tt_emb_grouping_view(m, n, R, nnz, num_bags, workspace)
+    base = workspace.data_ptr()
+
+    def arr(name, count, dtype=torch.int32):
+        off = view[name] - base
+        esz = torch.tensor([], dtype=dtype).element_size()
+        return workspace[off:off + count * esz].view(dtype).cpu().numpy()
+
+    counts = arr("counts", 5)
+    nv, ur, up, nc = (int(v) for v in counts[:4])
+    D = int(n[0] * n[1] * n[2])
+    return dict(n_valid=nv, U_r=ur, U_12=up, n_chunks=nc, status=int(counts[4]),
+                perm=arr("perm", nnz), row_start=arr("row_start", ur + 1),
+                row_i3=arr("row_i3", ur), row_pair=arr("row_pair", ur),
+                pair_row_start=arr("pair_row_start", up + 1), pair_i1=arr("pair_i1", up),
+                pair_i2=arr("pair_i2", up), uid=arr("uid", nnz), bag_of=arr("bag_of", nnz),
+                chunk_start=arr("chunk_start", nc + 1),
+                rowbuf=arr("rowbuf", ur * D, torch.float32).reshape(ur, D))
+
+
+class TTEmbeddingBag:
+    """A TT-compressed embedding table with sum pooling, resident on one GPU.
+
+    ``cores`` are float32 arrays [m_k][R_{k-1}][n_k][R_k].  ``forward`` takes
+    int64 indices and CSR offsets (host or device tensors / numpy arrays; host
+    inputs are copied in on the current stream) and returns the pooled
+    float32 [num_bags][D] output on the device.
+    """
+
+    def __init__(self, cores, m, n, R, device="cuda"):
+        self.m, self.n, self.R = tuple(int(v) for v in m), tuple(int(v) for v in n), \
+            tuple(int(v) for v in R)
+        self.D = self.n[0] * self.n[1] * self.n[2]
+        self.device = torch.device(device)
+        self.cores = [torch.as_tensor(np.ascontiguousarray(c, np.float32) if not
+                                      isinstance(c, torch.Tensor) else c)
+                      .to(self.device, torch.float32).contiguous() for c in cores]
+        self.grads = [torch.zeros_like(c) for c in self.cores]
+        self.workspace = torch.empty(0, dtype=torch.uint8, device=self.device)
+        self._batch = None
+
+    def _ensure_ws(self, nnz, num_bags):
+        need = tt_emb_workspace_bytes(self.m, self.n, self.R, nnz, num_bags)
+        if self.workspace.numel() < need:
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+
+    def _to_dev(self, x):
+        t = torch.as_tensor(x)
+        return t.to(self.device, torch.int64, non_blocking=True).contiguous()
+
+    def forward(self, indices, offsets, out=None, stream=None):
+        idx, off = self._to_dev(indices), self._to_dev(offsets)
+        B = off.numel() - 1
+        self._ensure_ws(idx.numel(), B)
+        if out is None:
+            out = torch.empty((B, self.D), dtype=torch.float32, device=self.device)
+        tt_emb_forward(self.cores, self.m, self.n, self.R, idx, off, out, self.workspace, stream)
+        self._batch = (idx, off)
+        return out
+
+    def backward(self, grad_out, stream=None):
+        """Accumulate d<grad_out, out>/dG into self.grads, reusing the last forward's grouping."""
+        if self._batch is None:
+            raise RuntimeError("backward needs a forward on the same batch first")
+        idx, off = self._batch
+        g = torch.as_tensor(grad_out).to(self.device, torch.float32, non_blocking=True)
+        tt_emb_backward(g.contiguous(), self.cores, self.m, self.n, self.R, idx, off, self.grads,
+                        self.workspace, reuse_grouping=True, stream=stream)
+        return self.grads
+
+    def zero_grad(self):
+        for g in self.grads:
+            g.zero_()
+
+    def sgd_step(self, lr: float, stream=None):
+        tt_emb_sgd(self.cores, self.grads, self.m, self.n, self.R, lr, stream)
+
+    def check(self, stream=None):
+        """Raise TTEmbError if a kernel flagged bad input (synchronises)."""
+        rc, bits = tt_emb_get_error(self.workspace, stream)
+        if rc != TT_EMB_OK:
+            raise TTEmbError(rc, f"device status bits {bits}")

@@ -1,0 +1,164 @@
+"""ctypes binding of libtt_emb.so: argument marshalling only.
+
+Every function has the name and the argument order of its C entry point
+(include/tt_emb.h).  Array arguments are CUDA torch tensors; the binding
+checks dtype, device and contiguity, passes raw pointers and the current
+CUDA stream, and turns a negative return code into TTEmbError.  All work runs
+in the library's kernels; there is no fallback of any kind, and a missing
+library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+TT_EMB_OK = 0
+TT_EMB_ERR_ARG = -1
+TT_EMB_ERR_WORKSPACE = -2
+TT_EMB_ERR_CUDA = -3
+TT_EMB_ERR_INDEX = -4
+TT_EMB_ERR_OFFSETS = -5
+TT_EMB_ERR_TIMEOUT = -6
+TT_EMB_ERR_UNSUPPORTED = -7
+_NAMES = {v: k for k, v in list(globals().items()) if k.startswith("TT_EMB_")}
+
+EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
+            "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_version")
+
+
+class TTEmbError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {_NAMES.get(code, code)}")
+        self.code = code
+
+
+class Grouping(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in (
+        "counts", "perm", "row_start", "row_i3", "row_pair", "pair_row_start", "pair_i1",
+        "pair_i2", "uid", "bag_of", "chunk_start", "rowbuf")]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libtt_emb.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "tensor_train_compressed_gb300.build.build() (nvcc, sm_103a)")
+        L = ctypes.CDLL(path)
+        P, I64, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+        L.tt_emb_workspace_bytes.argtypes = [P, P, P, I64, I64, ctypes.POINTER(SZ)]
+        L.tt_emb_group.argtypes = [P, P, P, P, I64, P, I64, P, SZ, P]
+        L.tt_emb_forward.argtypes = [P, P, P, P, P, I64, P, I64, P, P, SZ, P]
+        L.tt_emb_backward.argtypes = [P, P, P, P, P, P, I64, P, I64, P, P, SZ, ctypes.c_int, P]
+        L.tt_emb_sgd.argtypes = [P, P, P, P, P, ctypes.c_float, P]
+        L.tt_emb_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
+        L.tt_emb_grouping_view.argtypes = [P, P, P, I64, I64, P, ctypes.POINTER(Grouping)]
+        for name in EXPORTED:
+            getattr(L, name).restype = ctypes.c_int
+        L.tt_emb_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != TT_EMB_OK:
+        raise TTEmbError(rc, what)
+
+
+def _shape(m, n, R):
+    return ((ctypes.c_int64 * 3)(*[int(v) for v in m]), (ctypes.c_int32 * 3)(*[int(v) for v in n]),
+            (ctypes.c_int32 * 4)(*[int(v) for v in R]))
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ptrs3(ts, name):
+    return (ctypes.c_void_p * 3)(*[_dev(t, torch.float32, f"{name}[{k}]").value
+                                   for k, t in enumerate(ts)])
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def tt_emb_workspace_bytes(m, n, R, nnz: int, num_bags: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().tt_emb_workspace_bytes(*_shape(m, n, R), int(nnz), int(num_bags),
+                                        ctypes.byref(out)), "tt_emb_workspace_bytes")
+    return int(out.value)
+
+
+def tt_emb_group(m, n, R, indices, offsets, workspace, stream=None):
+    _check(lib().tt_emb_group(*_shape(m, n, R), _dev(indices, torch.int64, "indices"),
+                              indices.numel(), _dev(offsets, torch.int64, "offsets"),
+                              offsets.numel() - 1, _dev(workspace, torch.uint8, "workspace"),
+                              workspace.numel(), _stream(stream)), "tt_emb_group")
+
+
+def tt_emb_forward(cores, m, n, R, indices, offsets, out, workspace, stream=None):
+    _check(lib().tt_emb_forward(_ptrs3(cores, "cores"), *_shape(m, n, R),
+                                _dev(indices, torch.int64, "indices"), indices.numel(),
+                                _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
+                                _dev(out, torch.float32, "out"),
+                                _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                _stream(stream)), "tt_emb_forward")
+
+
+def tt_emb_backward(grad_out, cores, m, n, R, indices, offsets, core_grads, workspace,
+                    reuse_grouping: bool = True, stream=None):
+    _check(lib().tt_emb_backward(_dev(grad_out, torch.float32, "grad_out"),
+                                 _ptrs3(cores, "cores"), *_shape(m, n, R),
+                                 _dev(indices, torch.int64, "indices"), indices.numel(),
+                                 _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
+                                 _ptrs3(core_grads, "core_grads"),
+                                 _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                 int(bool(reuse_grouping)), _stream(stream)), "tt_emb_backward")
+
+
+def tt_emb_sgd(cores, core_grads, m, n, R, lr: float, stream=None):
+    _check(lib().tt_emb_sgd(_ptrs3(cores, "cores"), _ptrs3(core_grads, "core_grads"),
+                            *_shape(m, n, R), ctypes.c_float(lr), _stream(stream)), "tt_emb_sgd")
+
+
+def tt_emb_get_error(workspace, stream=None) -> tuple[int, int]:
+    """(return code, raw device status bits); synchronises the stream."""
+    st = ctypes.c_int(0)
+    rc = lib().tt_emb_get_error(_dev(workspace, torch.uint8, "workspace"), _stream(stream),
+                                ctypes.byref(st))
+    return int(rc), int(st.value)
+
+
+def tt_emb_grouping_view(m, n, R, nnz: int, num_bags: int, workspace) -> dict:
+    """Device addresses of the grouping arrays inside a workspace."""
+    g = Grouping()
+    _check(lib().tt_emb_grouping_view(*_shape(m, n, R), int(nnz), int(num_bags),
+                                      _dev(workspace, torch.uint8, "workspace"), ctypes.byref(g)),
+           "tt_emb_grouping_view")
+    return {name: getattr(g, name) for name, _ in Grouping._fields_}
+
+
+def tt_emb_version() -> int:
+    return int(lib().tt_emb_version())

@@ -1,0 +1,281 @@
+// C ABI of the TT embedding-bag library: argument checks, workspace layout and
+// the order of launches.  The declarations and their contracts are in
+// include/tt_emb.h.
+#include <string.h>
+
+#include "tt_internal.cuh"
+
+namespace tt {
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (cached[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+      v = 152;
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
+int shape_from_args(const int64_t m[3], const int32_t n[3], const int32_t R[4], Shape* s) {
+  if (!m || !n || !R || !s) return TT_EMB_ERR_ARG;
+  if (R[0] != 1 || R[3] != 1 || R[1] < 1 || R[2] < 1) return TT_EMB_ERR_ARG;
+  for (int k = 0; k < 3; ++k) {
+    if (m[k] < 1 || m[k] >= (1ll << 31)) return TT_EMB_ERR_ARG;
+    if (n[k] < 1) return TT_EMB_ERR_ARG;
+  }
+  const unsigned __int128 M = (unsigned __int128)m[0] * (unsigned __int128)m[1] * m[2];
+  if (M > (unsigned __int128)0xfffffffeull) return TT_EMB_ERR_UNSUPPORTED;
+  const int64_t D = (int64_t)n[0] * n[1] * n[2];
+  if (D > (1 << 20)) return TT_EMB_ERR_UNSUPPORTED;
+  s->m1 = m[0];
+  s->m2 = m[1];
+  s->m3 = m[2];
+  s->M = (int64_t)M;
+  s->n1 = n[0];
+  s->n2 = n[1];
+  s->n3 = n[2];
+  s->R1 = R[1];
+  s->R2 = R[2];
+  s->D = (int)D;
+  const int64_t g2n = (int64_t)s->R1 * s->n2 * s->R2;
+  const int64_t p2n = (int64_t)s->n1 * s->n2 * s->R2;
+  if (g2n + (int64_t)s->n1 * s->R1 + 2 * p2n > kMaxSmemFloats) return TT_EMB_ERR_UNSUPPORTED;
+  return TT_EMB_OK;
+}
+
+Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
+  (void)num_bags;
+  Layout L;
+  memset(&L, 0, sizeof(L));
+  int kb = 1;
+  while (kb < 32 && (((uint64_t)1 << kb) - 1) < (uint64_t)s.M) ++kb;
+  L.key_bits = kb;
+  L.passes = (kb + kRadixBits - 1) / kRadixBits;
+  const int64_t n = nnz > 0 ? nnz : 1;
+  L.n_sort_tiles = (int)ceil_div(n, kSortTile);
+  L.n_scan_tiles = (int)ceil_div(n, kScanTile);
+  L.rowbuf_rows = nnz < s.M ? nnz : s.M;
+  if (L.rowbuf_rows < 1) L.rowbuf_rows = 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.ctl = take(sizeof(Ctl));
+  L.hist = take(sizeof(uint32_t) * kMaxPasses * kRadix);
+  L.sort_status = take(sizeof(uint32_t) * kMaxPasses * (size_t)L.n_sort_tiles * kRadix);
+  L.keysA = take(sizeof(uint64_t) * (size_t)n);
+  L.keysB = take(sizeof(uint64_t) * (size_t)n);
+  L.bag_of = take(sizeof(int32_t) * (size_t)n);
+  L.uid = take(sizeof(int32_t) * (size_t)n);
+  L.perm = take(sizeof(int32_t) * (size_t)n);
+  L.row_start = take(sizeof(int32_t) * ((size_t)n + 1));
+  L.row_i3 = take(sizeof(int32_t) * (size_t)n);
+  L.row_pair = take(sizeof(int32_t) * (size_t)n);
+  L.pair_row_start = take(sizeof(int32_t) * ((size_t)n + 1));
+  L.pair_i1 = take(sizeof(int32_t) * (size_t)n);
+  L.pair_i2 = take(sizeof(int32_t) * (size_t)n);
+  L.seg_status = take(sizeof(unsigned long long) * (size_t)L.n_scan_tiles);
+  L.chunk_start = take(sizeof(int32_t) * ((size_t)n + 1));
+  L.chunk_status = take(sizeof(uint32_t) * (size_t)L.n_scan_tiles);
+  L.rowbuf = take(sizeof(float) * (size_t)L.rowbuf_rows * (size_t)s.D);
+  L.total = off;
+  return L;
+}
+
+WS make_ws(void* base, const Layout& L) {
+  char* b = static_cast<char*>(base);
+  WS w;
+  w.ctl = reinterpret_cast<Ctl*>(b + L.ctl);
+  w.hist = reinterpret_cast<uint32_t*>(b + L.hist);
+  w.sort_status = reinterpret_cast<uint32_t*>(b + L.sort_status);
+  w.keysA = reinterpret_cast<uint64_t*>(b + L.keysA);
+  w.keysB = reinterpret_cast<uint64_t*>(b + L.keysB);
+  w.bag_of = reinterpret_cast<int32_t*>(b + L.bag_of);
+  w.uid = reinterpret_cast<int32_t*>(b + L.uid);
+  w.perm = reinterpret_cast<int32_t*>(b + L.perm);
+  w.row_start = reinterpret_cast<int32_t*>(b + L.row_start);
+  w.row_i3 = reinterpret_cast<int32_t*>(b + L.row_i3);
+  w.row_pair = reinterpret_cast<int32_t*>(b + L.row_pair);
+  w.pair_row_start = reinterpret_cast<int32_t*>(b + L.pair_row_start);
+  w.pair_i1 = reinterpret_cast<int32_t*>(b + L.pair_i1);
+  w.pair_i2 = reinterpret_cast<int32_t*>(b + L.pair_i2);
+  w.seg_status = reinterpret_cast<unsigned long long*>(b + L.seg_status);
+  w.chunk_start = reinterpret_cast<int32_t*>(b + L.chunk_start);
+  w.chunk_status = reinterpret_cast<uint32_t*>(b + L.chunk_status);
+  w.rowbuf = reinterpret_cast<float*>(b + L.rowbuf);
+  return w;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Common checks of the batch arguments.
+static int check_batch(const Shape& s, const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                       int64_t num_bags, const void* workspace, size_t ws_bytes, Layout* L) {
+  (void)s;
+  if (nnz < 0 || nnz >= (1ll << 30) || num_bags < 0 || num_bags >= (1ll << 31)) return TT_EMB_ERR_ARG;
+  if (nnz > 0 && num_bags == 0) return TT_EMB_ERR_ARG;   // offsets[0] = 0 != offsets[B] = nnz
+  if (nnz > 0 && !indices) return TT_EMB_ERR_ARG;
+  if (!offsets || !workspace) return TT_EMB_ERR_ARG;
+  if (!aligned(workspace, 256)) return TT_EMB_ERR_ARG;
+  *L = make_layout(s, nnz, num_bags);
+  if (ws_bytes < L->total) return TT_EMB_ERR_WORKSPACE;
+  return TT_EMB_OK;
+}
+
+static int check_cores(const float* const cores[3]) {
+  if (!cores) return TT_EMB_ERR_ARG;
+  for (int k = 0; k < 3; ++k)
+    if (!cores[k] || !aligned(cores[k], 16)) return TT_EMB_ERR_ARG;
+  return TT_EMB_OK;
+}
+
+}  // namespace tt
+
+using namespace tt;
+
+extern "C" {
+
+int tt_emb_version(void) { return 100; }
+
+int tt_emb_workspace_bytes(const int64_t m[3], const int32_t n[3], const int32_t R[4], int64_t nnz,
+                           int64_t num_bags, size_t* bytes) {
+  Shape s;
+  int rc = shape_from_args(m, n, R, &s);
+  if (rc) return rc;
+  if (!bytes || nnz < 0 || nnz >= (1ll << 30) || num_bags < 0) return TT_EMB_ERR_ARG;
+  *bytes = make_layout(s, nnz, num_bags).total;
+  return TT_EMB_OK;
+}
+
+int tt_emb_group(const int64_t m[3], const int32_t n[3], const int32_t R[4], const int64_t* indices,
+                 int64_t nnz, const int64_t* offsets, int64_t num_bags, void* workspace,
+                 size_t ws_bytes, void* stream) {
+  Shape s;
+  int rc = shape_from_args(m, n, R, &s);
+  if (rc) return rc;
+  Layout L;
+  rc = check_batch(s, indices, nnz, offsets, num_bags, workspace, ws_bytes, &L);
+  if (rc) return rc;
+  int CP, CR;
+  rc = forward_chunk_params(s, &CP, &CR);
+  if (rc) return rc;
+  return launch_group(s, L, make_ws(workspace, L), indices, nnz, offsets, num_bags, CP, CR,
+                      (cudaStream_t)stream);
+}
+
+int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_t n[3],
+                   const int32_t R[4], const int64_t* indices, int64_t nnz,
+                   const int64_t* offsets, int64_t num_bags, float* out, void* workspace,
+                   size_t ws_bytes, void* stream) {
+  Shape s;
+  int rc = shape_from_args(m, n, R, &s);
+  if (rc) return rc;
+  rc = check_cores(cores);
+  if (rc) return rc;
+  Layout L;
+  rc = check_batch(s, indices, nnz, offsets, num_bags, workspace, ws_bytes, &L);
+  if (rc) return rc;
+  if (num_bags > 0 && (!out || !aligned(out, 16))) return TT_EMB_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const WS w = make_ws(workspace, L);
+  int CP, CR;
+  rc = forward_chunk_params(s, &CP, &CR);
+  if (rc) return rc;
+  rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, st);
+  if (rc) return rc;
+  if (nnz == 0) {
+    if (num_bags > 0 &&
+        cudaMemsetAsync(out, 0, sizeof(float) * (size_t)num_bags * s.D, st) != cudaSuccess)
+      return TT_EMB_ERR_CUDA;
+    return TT_EMB_OK;
+  }
+  return launch_forward(s, L, w, cores, offsets, nnz, num_bags, out, st);
+}
+
+int tt_emb_backward(const float* grad_out, const float* const cores[3], const int64_t m[3],
+                    const int32_t n[3], const int32_t R[4], const int64_t* indices, int64_t nnz,
+                    const int64_t* offsets, int64_t num_bags, float* const core_grads[3],
+                    void* workspace, size_t ws_bytes, int reuse_grouping, void* stream) {
+  Shape s;
+  int rc = shape_from_args(m, n, R, &s);
+  if (rc) return rc;
+  rc = check_cores(cores);
+  if (rc) return rc;
+  rc = check_cores(core_grads);
+  if (rc) return rc;
+  Layout L;
+  rc = check_batch(s, indices, nnz, offsets, num_bags, workspace, ws_bytes, &L);
+  if (rc) return rc;
+  if (num_bags > 0 && (!grad_out || !aligned(grad_out, 16))) return TT_EMB_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const WS w = make_ws(workspace, L);
+  if (!reuse_grouping) {
+    int CP, CR;
+    rc = forward_chunk_params(s, &CP, &CR);
+    if (rc) return rc;
+    rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, st);
+    if (rc) return rc;
+  }
+  return launch_backward(s, L, w, grad_out, cores, nnz, num_bags, core_grads, st);
+}
+
+int tt_emb_sgd(float* const cores[3], const float* const core_grads[3], const int64_t m[3],
+               const int32_t n[3], const int32_t R[4], float lr, void* stream) {
+  Shape s;
+  int rc = shape_from_args(m, n, R, &s);
+  if (rc) return rc;
+  rc = check_cores(cores);
+  if (rc) return rc;
+  rc = check_cores(core_grads);
+  if (rc) return rc;
+  return launch_sgd(cores, core_grads, s, lr, (cudaStream_t)stream);
+}
+
+int tt_emb_get_error(const void* workspace, void* stream, int* device_status) {
+  if (!workspace || !device_status) return TT_EMB_ERR_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return TT_EMB_ERR_CUDA;
+  uint32_t st = 0;
+  const Ctl* c = static_cast<const Ctl*>(workspace);
+  if (cudaMemcpy(&st, &c->status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return TT_EMB_ERR_CUDA;
+  *device_status = (int)st;
+  if (st & kStTimeout) return TT_EMB_ERR_TIMEOUT;
+  if (st & kStOffsets) return TT_EMB_ERR_OFFSETS;
+  if (st & kStIndex) return TT_EMB_ERR_INDEX;
+  return TT_EMB_OK;
+}
+
+int tt_emb_grouping_view(const int64_t m[3], const int32_t n[3], const int32_t R[4], int64_t nnz,
+                         int64_t num_bags, const void* workspace, tt_emb_grouping* view) {
+  Shape s;
+  int rc = shape_from_args(m, n, R, &s);
+  if (rc) return rc;
+  if (!workspace || !view || nnz < 0 || nnz >= (1ll << 30)) return TT_EMB_ERR_ARG;
+  const Layout L = make_layout(s, nnz, num_bags);
+  const WS w = make_ws(const_cast<void*>(workspace), L);
+  view->counts = reinterpret_cast<const int32_t*>(w.ctl);
+  view->perm = w.perm;
+  view->row_start = w.row_start;
+  view->row_i3 = w.row_i3;
+  view->row_pair = w.row_pair;
+  view->pair_row_start = w.pair_row_start;
+  view->pair_i1 = w.pair_i1;
+  view->pair_i2 = w.pair_i2;
+  view->uid = w.uid;
+  view->bag_of = w.bag_of;
+  view->chunk_start = w.chunk_start;
+  view->rowbuf = w.rowbuf;
+  return TT_EMB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,191 @@
+// Forward TT embedding bag: prefix partials, unique rows, bag pooling.
+//
+// FlowTT (summary card, key innovations and approach; abstract): each shared
+// prefix of the contraction chain is formed once and kept on chip while every
+// row that extends it is formed.  Per work chunk (a run of unique (i1, i2)
+// prefixes with the same i2, or a piece of one large prefix):
+//
+//   stage 2   P2[p] = G1[i1_p] . G2[i2]     (n1 x R1).(R1 x n2*R2), in shared memory
+//   stage 3   row[x] = P2[p(x)] . G3[i3_x]  (n1*n2 x R2).(R2 x n3) = D values
+//
+// Rows go to a unique-row buffer in the workspace (L2-resident at the sizes
+// used here); k_pool then sums each bag's rows with coalesced float4 loads
+// and stores (sum pooling of the TT-EmbeddingBag, TT-Rec abstract).
+// Persistent CTAs take chunks from an atomic counter (dynamic load
+// balancing under Zipf skew, FlowTT summary card, key innovations).
+#include "tt_internal.cuh"
+
+namespace tt {
+
+struct FwdArgs {
+  Shape s;
+  WS w;
+  const float* G1;
+  const float* G2;
+  const float* G3;
+};
+
+// Shape-generic chunk kernel (any shape within the shared-memory limit).
+__global__ void __launch_bounds__(256) k_fwd_generic(FwdArgs a) {
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
+  __shared__ int c_sh;
+  const Shape& s = a.s;
+  const int tid = threadIdx.x;
+  const int g2n = s.R1 * s.n2 * s.R2;
+  const int p1n = s.n1 * s.R1;
+  const int n2R2 = s.n2 * s.R2;
+  const int p2n = s.n1 * n2R2;
+  const int n3 = s.n3, R1 = s.R1, R2 = s.R2, D = s.D;
+  float* G2s = sm;
+  const int n_chunks = a.w.ctl->n_chunks;
+  for (;;) {
+    if (tid == 0) c_sh = (int)atomicAdd(&a.w.ctl->fwd_chunk_ctr, 1u);
+    __syncthreads();
+    const int c = c_sh;
+    if (c >= n_chunks) break;
+    const int x0 = a.w.chunk_start[c], x1 = a.w.chunk_start[c + 1];
+    const int p0 = a.w.row_pair[x0], p1 = a.w.row_pair[x1 - 1];
+    const int np = p1 - p0 + 1;
+    float* P1s = G2s + g2n;
+    float* P2s = P1s + np * p1n;
+    const int i2 = a.w.pair_i2[p0];
+    const float* g2 = a.G2 + (size_t)i2 * g2n;
+    for (int e = tid; e < g2n; e += blockDim.x) G2s[e] = __ldg(g2 + e);
+    for (int e = tid; e < np * p1n; e += blockDim.x) {
+      const int p = e / p1n;
+      P1s[e] = __ldg(a.G1 + (size_t)a.w.pair_i1[p0 + p] * p1n + (e - p * p1n));
+    }
+    __syncthreads();
+    for (int e = tid; e < np * p2n; e += blockDim.x) {
+      const int p = e / p2n, rem = e - p * p2n;
+      const int j1 = rem / n2R2, j2b = rem - j1 * n2R2;
+      const float* pa = P1s + p * p1n + j1 * R1;
+      float acc = 0.f;
+      for (int aa = 0; aa < R1; ++aa) acc = fmaf(pa[aa], G2s[aa * n2R2 + j2b], acc);
+      P2s[e] = acc;
+    }
+    __syncthreads();
+    const int nx = x1 - x0;
+    for (int e = tid; e < nx * D; e += blockDim.x) {
+      const int xi = e / D, j = e - xi * D;
+      const int x = x0 + xi;
+      const int j12 = j / n3, j3 = j - j12 * n3;
+      const float* pp = P2s + (a.w.row_pair[x] - p0) * p2n + j12 * R2;
+      const float* g3 = a.G3 + (size_t)a.w.row_i3[x] * R2 * n3 + j3;
+      float acc = 0.f;
+      for (int b = 0; b < R2; ++b) acc = fmaf(pp[b], __ldg(g3 + b * n3), acc);
+      a.w.rowbuf[(size_t)x * D + j] = acc;
+    }
+    __syncthreads();
+  }
+}
+
+// out[b] = sum of the unique rows of bag b's lookups; one warp per bag.
+__global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offsets, int64_t B,
+                                              int64_t nnz, const int32_t* __restrict__ uid,
+                                              const float* __restrict__ rowbuf, int D,
+                                              float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < B; b += warps) {
+    int64_t l0 = offsets[b], l1 = offsets[b + 1];
+    l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
+    l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
+    if ((D & 3) == 0) {
+      const int D4 = D >> 2;
+      const float4* rb = reinterpret_cast<const float4*>(rowbuf);
+      float4* o = reinterpret_cast<float4*>(out + b * (int64_t)D);
+      for (int c = lane; c < D4; c += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int64_t l = l0;
+        for (; l + 4 <= l1; l += 4) {
+          const int u0 = uid[l], u1 = uid[l + 1], u2 = uid[l + 2], u3 = uid[l + 3];
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 v0 = u0 >= 0 ? rb[(int64_t)u0 * D4 + c] : z;
+          const float4 v1 = u1 >= 0 ? rb[(int64_t)u1 * D4 + c] : z;
+          const float4 v2 = u2 >= 0 ? rb[(int64_t)u2 * D4 + c] : z;
+          const float4 v3 = u3 >= 0 ? rb[(int64_t)u3 * D4 + c] : z;
+          acc.x += v0.x; acc.y += v0.y; acc.z += v0.z; acc.w += v0.w;
+          acc.x += v1.x; acc.y += v1.y; acc.z += v1.z; acc.w += v1.w;
+          acc.x += v2.x; acc.y += v2.y; acc.z += v2.z; acc.w += v2.w;
+          acc.x += v3.x; acc.y += v3.y; acc.z += v3.z; acc.w += v3.w;
+        }
+        for (; l < l1; ++l) {
+          const int u = uid[l];
+          if (u >= 0) {
+            const float4 v = rb[(int64_t)u * D4 + c];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+          }
+        }
+        o[c] = acc;
+      }
+    } else {
+      for (int j = lane; j < D; j += 32) {
+        float acc = 0.f;
+        for (int64_t l = l0; l < l1; ++l) {
+          const int u = uid[l];
+          if (u >= 0) acc += rowbuf[(int64_t)u * D + j];
+        }
+        out[b * (int64_t)D + j] = acc;
+      }
+    }
+  }
+}
+
+static size_t fwd_generic_smem(const Shape& s, int CP) {
+  return sizeof(float) * ((size_t)s.R1 * s.n2 * s.R2 +
+                          (size_t)CP * (s.n1 * s.R1 + s.n1 * s.n2 * s.R2));
+}
+
+int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chunk) {
+  const int64_t g2n = (int64_t)s.R1 * s.n2 * s.R2;
+  const int64_t per = (int64_t)s.n1 * s.R1 + (int64_t)s.n1 * s.n2 * s.R2;
+  if (g2n + per + (int64_t)s.n1 * s.n2 * s.R2 > kMaxSmemFloats) return TT_EMB_ERR_UNSUPPORTED;
+  int64_t cp = (kMaxSmemFloats - g2n) / per;
+  if (cp > 16) cp = 16;
+  if (cp < 1) cp = 1;
+  *pairs_per_chunk = (int)cp;
+  *rows_per_chunk = 32;
+  return TT_EMB_OK;
+}
+
+static int persistent_grid(const void* fn, int threads, size_t smem) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  return per_sm * sm_count();
+}
+
+int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* const cores[3],
+                   const int64_t* offsets, int64_t nnz, int64_t num_bags, float* out,
+                   cudaStream_t st) {
+  (void)L;
+  int CP = 0, CR = 0;
+  int rc = forward_chunk_params(s, &CP, &CR);
+  if (rc) return rc;
+  FwdArgs fa;
+  fa.s = s;
+  fa.w = w;
+  fa.G1 = cores[0];
+  fa.G2 = cores[1];
+  fa.G3 = cores[2];
+  const size_t smem = fwd_generic_smem(s, CP);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(k_fwd_generic, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kMaxSmemFloats * (int)sizeof(float));
+    attr_set = true;
+  }
+  k_fwd_generic<<<persistent_grid((const void*)k_fwd_generic, 256, smem), 256, smem, st>>>(fa);
+  if (num_bags > 0) {
+    int grid = (int)ceil_div(num_bags, 8);
+    const int cap = sm_count() * 16;
+    if (grid > cap) grid = cap;
+    k_pool<<<grid, 256, 0, st>>>(offsets, num_bags, nnz, w.uid, w.rowbuf, s.D, out);
+  }
+  return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
+}
+
+}  // namespace tt

@@ -1,0 +1,104 @@
+"""The C-ABI library loads and exports every entry point its header declares (no GPU).
+
+Only host-side argument checks are exercised here: each call below returns
+before anything is enqueued on a device.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import tensor_train_compressed_gb300 as tte
+from tensor_train_compressed_gb300 import _binding as B
+from tensor_train_compressed_gb300 import build as tbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    tbuild.build()
+    return tte.lib()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names |= set(re.findall(r"^\s*int\s+(tt_emb_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_header_symbols_exported(L):
+    names = _declared()
+    assert {"tt_emb_forward", "tt_emb_backward", "tt_emb_sgd", "tt_emb_workspace_bytes"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(B.EXPORTED) >= names
+
+
+def test_version(L):
+    assert tte.tt_emb_version() >= 100
+
+
+def test_workspace_bytes_and_shape_errors(L):
+    b = tte.tt_emb_workspace_bytes((200, 240, 250), (4, 8, 4), (1, 32, 32, 1), 655360, 32768)
+    # the unique-row buffer dominates: min(nnz, M) rows of D floats
+    assert b >= 655360 * 128 * 4
+    small = tte.tt_emb_workspace_bytes((10, 10, 10), (2, 4, 2), (1, 4, 4, 1), 100, 10)
+    assert small >= 100 * 16 * 4 and small < b
+    with pytest.raises(tte.TTEmbError) as e:
+        tte.tt_emb_workspace_bytes((10, 10, 10), (2, 4, 2), (2, 4, 4, 1), 100, 10)
+    assert e.value.code == tte.TT_EMB_ERR_ARG
+    with pytest.raises(tte.TTEmbError) as e:   # G2 slice beyond shared memory
+        tte.tt_emb_workspace_bytes((10, 10, 10), (4, 16, 4), (1, 128, 128, 1), 100, 10)
+    assert e.value.code == tte.TT_EMB_ERR_UNSUPPORTED
+    with pytest.raises(tte.TTEmbError) as e:   # M beyond 2^32 - 2
+        tte.tt_emb_workspace_bytes((70000, 70000, 2), (2, 2, 2), (1, 2, 2, 1), 100, 10)
+    assert e.value.code == tte.TT_EMB_ERR_UNSUPPORTED
+
+
+def _shape(m, n, R):
+    return B._shape(m, n, R)
+
+
+def test_forward_host_side_argument_checks(L):
+    """Null, misaligned and undersized arguments are refused before any launch."""
+    m, n, R = (10, 10, 10), (2, 4, 2), (1, 4, 4, 1)
+    fake = 1 << 20                       # never dereferenced: the checks fail first
+    cores = (ctypes.c_void_p * 3)(fake, fake, fake)
+    P = ctypes.c_void_p
+    need = tte.tt_emb_workspace_bytes(m, n, R, 100, 10)
+    rc = L.tt_emb_forward(cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, P(fake), P(fake),
+                          need - 1, None)
+    assert rc == tte.TT_EMB_ERR_WORKSPACE
+    rc = L.tt_emb_forward(cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, P(fake),
+                          P(fake + 8), need, None)
+    assert rc == tte.TT_EMB_ERR_ARG      # workspace not 256-byte aligned
+    rc = L.tt_emb_forward(cores, *_shape(m, n, R), None, 100, P(fake), 10, P(fake), P(fake),
+                          need, None)
+    assert rc == tte.TT_EMB_ERR_ARG      # null indices
+    rc = L.tt_emb_forward(cores, *_shape(m, n, R), P(fake), 100, P(fake), 0, P(fake), P(fake),
+                          need, None)
+    assert rc == tte.TT_EMB_ERR_ARG      # lookups without bags
+    bad = (ctypes.c_void_p * 3)(fake, fake + 4, fake)
+    rc = L.tt_emb_forward(bad, *_shape(m, n, R), P(fake), 100, P(fake), 10, P(fake), P(fake),
+                          need, None)
+    assert rc == tte.TT_EMB_ERR_ARG      # core not 16-byte aligned
+    rc = L.tt_emb_backward(P(fake), cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, None,
+                           P(fake), need, 1, None)
+    assert rc == tte.TT_EMB_ERR_ARG      # null core_grads
+    rc = L.tt_emb_sgd(cores, None, *_shape(m, n, R), ctypes.c_float(0.1), None)
+    assert rc == tte.TT_EMB_ERR_ARG
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The package never imports the oracle."""
+    pkg = os.path.join(ROOT, "tensor_train_compressed_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*.*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h")):
+            src = open(path).read()
+            assert "import oracle" not in src and "from oracle" not in src, path
+            assert "tt_oracle" not in src, path

@@ -1,0 +1,289 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars: the grouping is bit-exact; the fp32 forward is within
+1e-4 * max|ref| over the whole output; fp32 core gradients (float atomics)
+within 1e-3 * max|ref| per core; SGD within 0.01 * 1e-3 * max|dG_ref| plus
+fp32 rounding of the cores.  Full-size configurations are checked on sampled
+bags (forward) and on sampled core slices (backward), computed one by one by
+the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tensor_train_compressed_gb300 as tte
+from tensor_train_compressed_gb300.inputs import make_custom, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+FWD_TOL = 1e-4
+BWD_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from tensor_train_compressed_gb300 import build
+    build.build()
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _gpu_forward(x, ws=None):
+    cores = [_dev(c) for c in x.cores]
+    idx, off = _dev(x.indices.astype(np.int64)), _dev(x.offsets.astype(np.int64))
+    B = x.num_bags
+    need = tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, B)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = torch.full((B, x.D), float("nan"), dtype=torch.float32, device="cuda")
+    tte.tt_emb_forward(cores, x.m, x.n, x.R, idx, off, out, ws)
+    rc, bits = tte.tt_emb_get_error(ws)
+    return out.cpu().numpy(), rc, bits, dict(cores=cores, idx=idx, off=off, ws=ws)
+
+
+def _gpu_backward(x, st):
+    grads = [torch.zeros_like(c) for c in st["cores"]]
+    tte.tt_emb_backward(_dev(x.grad_out), st["cores"], x.m, x.n, x.R, st["idx"], st["off"],
+                        grads, st["ws"], reuse_grouping=True)
+    rc, bits = tte.tt_emb_get_error(st["ws"])
+    assert rc == tte.TT_EMB_OK, bits
+    return [g.cpu().numpy() for g in grads]
+
+
+def _rel_err(a, ref):
+    return float(np.abs(a.astype(np.float64) - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def _check_grouping(x, ws):
+    ref = oracle.group(x.indices, x.m)
+    g = tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, ws)
+    assert g["n_valid"] == ref["n_valid"] and g["U_r"] == ref["U_r"] and g["U_12"] == ref["U_12"]
+    nv = ref["n_valid"]
+    assert np.array_equal(g["perm"][:nv], ref["perm"])
+    assert np.array_equal(g["row_start"], ref["row_start"])
+    assert np.array_equal(g["row_pair"], ref["row_pair"])
+    assert np.array_equal(g["pair_row_start"], ref["pair_row_start"])
+    assert np.array_equal(g["pair_i1"], ref["pair_i1"])
+    assert np.array_equal(g["pair_i2"], ref["pair_i2"])
+    assert np.array_equal(g["uid"], ref["uid"])
+    m2, m3 = x.m[1], x.m[2]
+    rows = (g["pair_i1"][g["row_pair"]].astype(np.int64) * m2 + g["pair_i2"][g["row_pair"]]) * m3 \
+        + g["row_i3"]
+    assert np.array_equal(rows, ref["row_index"])
+    # bag of every lookup
+    lens = np.diff(x.offsets)
+    assert np.array_equal(g["bag_of"], np.repeat(np.arange(x.num_bags), lens))
+    # chunks partition the unique rows, each chunk's prefixes share one i2
+    cs = g["chunk_start"]
+    assert cs[0] == 0 and cs[-1] == g["U_r"] and np.all(np.diff(cs) > 0)
+    for c in range(g["n_chunks"]):
+        p = g["row_pair"][cs[c]:cs[c + 1]]
+        assert np.unique(g["pair_i2"][p]).size == 1
+    return g
+
+
+def _sample_bags(x, bags):
+    idx = np.concatenate([x.indices[x.offsets[b]:x.offsets[b + 1]] for b in bags])
+    off = np.concatenate([[0], np.cumsum([x.offsets[b + 1] - x.offsets[b] for b in bags])])
+    return idx, off
+
+
+# ------------------------------------------------------------------ grouping + forward
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_forward_small_configs_full(cfg):
+    x = make_inputs(cfg)
+    out, rc, _, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    assert _rel_err(out, ref) <= FWD_TOL
+    _check_grouping(x, st["ws"])
+
+
+def test_config1_against_materialised_table():
+    x = make_inputs(1)
+    out, rc, _, _ = _gpu_forward(x)
+    G1, G2, G3 = (c.astype(np.float64) for c in x.cores)
+    T = np.einsum("xpa,yaqb,zbr->xyzpqr", G1[:, 0], G2, G3[:, :, :, 0]).reshape(1000, 16)
+    ref = np.stack([T[x.indices[x.offsets[b]:x.offsets[b + 1]]].sum(0) for b in range(64)])
+    assert _rel_err(out, ref) <= FWD_TOL
+
+
+@pytest.mark.parametrize("cfg,bags", [(3, 3000), (5, 3000), (4, 3000)])
+def test_forward_reduced_configs_full_compare(cfg, bags):
+    """Config shapes and index distributions, fewer bags: every output compared."""
+    x = make_inputs(cfg, table=3 if cfg == 4 else 0, num_bags=bags)
+    out, rc, _, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    assert _rel_err(out, ref) <= FWD_TOL
+    _check_grouping(x, st["ws"])
+
+
+@pytest.mark.parametrize("cfg,table", [(3, 0), (5, 0), (4, 0), (4, 7)])
+def test_forward_full_size_sampled(cfg, table):
+    x = make_inputs(cfg, table=table)
+    out, rc, _, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK
+    rng = np.random.default_rng(100 + cfg)
+    bags = np.sort(rng.choice(x.num_bags, size=300, replace=False))
+    idx, off = _sample_bags(x, bags)
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, idx, off, threads=8)
+    # the tolerance is relative to the largest pooled value of the full output
+    scale = max(np.abs(out).max(), np.abs(ref).max())
+    assert np.abs(out[bags] - ref).max() <= FWD_TOL * scale
+    assert np.isfinite(out).all()
+    g = tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, st["ws"])
+    ur = np.unique(x.indices).size
+    assert g["U_r"] == ur and g["n_valid"] == x.nnz
+
+
+def test_forward_is_deterministic():
+    x = make_inputs(3, num_bags=2000)
+    a, _, _, st = _gpu_forward(x)
+    b, _, _, _ = _gpu_forward(x, ws=st["ws"])
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ edge cases
+
+
+@pytest.mark.parametrize("shape", [((3, 4, 5), (2, 3, 2), (1, 3, 2, 1)),
+                                   ((7, 1, 9), (3, 1, 5), (1, 5, 2, 1)),
+                                   ((1, 1, 1), (1, 1, 1), (1, 1, 1, 1)),
+                                   ((5, 6, 7), (4, 8, 4), (1, 32, 32, 1)),
+                                   ((13, 11, 17), (4, 4, 4), (1, 16, 16, 1)),
+                                   ((9, 8, 7), (4, 8, 4), (1, 64, 64, 1))])
+def test_edge_shapes_ragged_and_empty_bags(shape):
+    m, n, R = shape
+    x = make_custom(m, n, R, num_bags=2500, max_len=7, seed=42, empty_frac=0.15)
+    out, rc, _, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK
+    ref = oracle.forward(x.cores, m, n, R, x.indices, x.offsets, threads=8)
+    assert _rel_err(out, ref) <= FWD_TOL
+    assert not out[np.diff(x.offsets) == 0].any()
+    _check_grouping(x, st["ws"])
+    dG = _gpu_backward(x, st)
+    dref = oracle.backward(x.grad_out, x.cores, m, n, R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(dG[k], dref[k]) <= BWD_TOL, k
+
+
+def test_no_lookups_and_all_empty_bags():
+    x = make_custom((3, 4, 5), (2, 3, 2), (1, 3, 2, 1), num_bags=17, max_len=0, seed=1)
+    assert x.nnz == 0
+    out, rc, _, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK and not out.any() and out.shape == (17, 12)
+    dG = _gpu_backward(x, st)
+    assert not any(g.any() for g in dG)
+
+
+def test_out_of_range_indices_are_reported_and_skipped():
+    x = make_custom((3, 4, 5), (2, 3, 2), (1, 3, 2, 1), num_bags=300, max_len=6, seed=5)
+    bad = x.indices.copy()
+    bad[::11] = 60
+    bad[5] = -3
+    x.indices = bad
+    out, rc, bits, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_ERR_INDEX and bits & 1
+    keep = (bad >= 0) & (bad < 60)
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, bad, x.offsets, strict=False)
+    assert _rel_err(out, ref) <= FWD_TOL
+    g = _check_grouping(x, st["ws"])
+    assert g["n_valid"] == keep.sum()
+
+
+def test_bad_offsets_are_reported():
+    x = make_custom((3, 4, 5), (2, 3, 2), (1, 3, 2, 1), num_bags=50, max_len=4, seed=6)
+    off = x.offsets.copy()
+    off[10] = off[12] + 1          # not monotone
+    x.offsets = off
+    _, rc, bits, _ = _gpu_forward(x)
+    assert rc == tte.TT_EMB_ERR_OFFSETS and bits & 2
+
+
+def test_single_hot_row_and_all_same_prefix():
+    """Every lookup on one row (a 40k-lookup run) and one prefix with many rows."""
+    m, n, R = (4, 5, 300), (4, 8, 4), (1, 32, 32, 1)
+    x = make_custom(m, n, R, num_bags=2000, max_len=40, seed=9)
+    x.indices[:] = 7
+    x.indices[::3] = np.arange(x.indices[::3].size) % 300 + 600   # prefix (0, 2), all i3
+    out, rc, _, st = _gpu_forward(x)
+    ref = oracle.forward(x.cores, m, n, R, x.indices, x.offsets, threads=8)
+    assert rc == tte.TT_EMB_OK and _rel_err(out, ref) <= FWD_TOL
+    _check_grouping(x, st["ws"])
+    dG = _gpu_backward(x, st)
+    dref = oracle.backward(x.grad_out, x.cores, m, n, R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(dG[k], dref[k]) <= BWD_TOL, k
+
+
+# ------------------------------------------------------------------ backward + SGD
+
+
+def test_backward_config5_reduced_full_compare_and_sgd():
+    x = make_inputs(5, num_bags=1500)
+    _, rc, _, st = _gpu_forward(x)
+    dG = _gpu_backward(x, st)
+    dref = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(dG[k], dref[k]) <= BWD_TOL, k
+    grads = [_dev(g) for g in dG]
+    tte.tt_emb_sgd(st["cores"], grads, x.m, x.n, x.R, 0.01)
+    for k in range(3):
+        upd = st["cores"][k].cpu().numpy().astype(np.float64)
+        ref = oracle.sgd(x.cores[k], dref[k], 0.01)
+        tol = 0.01 * BWD_TOL * np.abs(dref[k]).max() + 2e-7 * np.abs(ref).max()
+        assert np.abs(upd - ref).max() <= tol, k
+
+
+@pytest.mark.parametrize("cfg", [5, 3])
+def test_backward_full_size_sampled_slices(cfg):
+    x = make_inputs(cfg, with_grad=True)
+    _, rc, _, st = _gpu_forward(x)
+    dG = _gpu_backward(x, st)
+    r = x.indices
+    i1, i2, i3 = r // (x.m[1] * x.m[2]), (r // x.m[2]) % x.m[1], r % x.m[2]
+    picks = [(1, int(i1[7])), (1, int(np.max(i1))), (2, int(i2[3])), (2, int(i2[1000])),
+             (3, int(i3[0])), (3, int(i3[555]))]
+    for core, v in picks:
+        ref = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets,
+                              threads=8, filter_core=core, filter_value=v)[core - 1][v]
+        got = dG[core - 1][v]
+        assert _rel_err(got, ref) <= BWD_TOL, (core, v)
+    for k in range(3):
+        assert np.isfinite(dG[k]).all()
+
+
+def test_backward_rebuilds_grouping_when_not_reused():
+    x = make_inputs(5, num_bags=800)
+    cores = [_dev(c) for c in x.cores]
+    idx, off = _dev(x.indices), _dev(x.offsets)
+    ws = torch.empty(tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags),
+                     dtype=torch.uint8, device="cuda")
+    grads = [torch.zeros_like(c) for c in cores]
+    tte.tt_emb_backward(_dev(x.grad_out), cores, x.m, x.n, x.R, idx, off, grads, ws,
+                        reuse_grouping=False)
+    dref = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(grads[k].cpu().numpy(), dref[k]) <= BWD_TOL
+
+
+def test_owner_object_host_inputs():
+    x = make_inputs(5, num_bags=500)
+    emb = tte.TTEmbeddingBag(x.cores, x.m, x.n, x.R)
+    out = emb.forward(torch.from_numpy(x.indices).pin_memory(),
+                      torch.from_numpy(x.offsets).pin_memory())
+    emb.backward(torch.from_numpy(x.grad_out))
+    emb.check()
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    assert _rel_err(out.cpu().numpy(), ref) <= FWD_TOL
+    dref = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(emb.grads[k].cpu().numpy(), dref[k]) <= BWD_TOL
