@@ -1,0 +1,525 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 TT embedding bag.
+
+One step = one pass of the whole hot path over one batch: prefix grouping,
+forward contraction, bag pooling, backward into the cores and the SGD update,
+on the 48M-row training workload (360x360x370 rows, D = 128 = 4x8x4,
+R1 = R2 = 32, 32768 bags of U{10..30} Zipf(1.2) lookups, lr 0.01).  The
+12M-row forward workload (200x240x250 rows, 32768 bags of 20 Zipf(1.2)
+lookups) is timed beside it and reported under "forward".
+
+Timing: every step is captured once as a CUDA graph and replayed; each timed
+replay is bracketed by CUDA events on its stream; between timed replays a
+512 MB buffer is written (L2 flush) and the cores are restored from a copy
+(both outside the events).  Per-kernel durations come from the library's own
+launch events (tt_emb_profile_*), recorded in a separately captured graph.
+`--impl reference` times the fp64 CPU oracle on a sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TT embedding-bag lookups/s at batch 32768 (fwd, fwd+bwd); % of roofline"
+TRAIN_CFG, FWD_CFG = 5, 3
+LR = 0.01
+FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    """Measured HBM bandwidth and SM clock of this machine, else the recipe's fallback."""
+    p = {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        p.update(hbm_gbs=float(d.get("hbm_gbs", p["hbm_gbs"])),
+                 sm_max_mhz=float(d.get("sm_max_mhz", p["sm_max_mhz"])), source="measured")
+    return p
+
+
+def fp32_peak_tflops(sm_count: int, mhz: float) -> float:
+    """FP32 FMA peak: SMs x 128 FP32 lanes x 2 FLOP x clock."""
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def algorithmic(x, U_12: int, U_r: int) -> dict:
+    """Algorithmic FLOPs and bytes of one batch (each unique prefix and row once)."""
+    n1, n2, n3 = x.n
+    R1, R2 = x.R[1], x.R[2]
+    D, nnz, B = x.D, x.nnz, x.num_bags
+    f2 = 2 * n1 * R1 * n2 * R2
+    f3 = 2 * D * R2
+    return dict(
+        f2=f2, f3=f3, U_12=U_12, U_r=U_r, nnz=nnz, B=B,
+        fwd_contract=U_12 * f2 + U_r * f3,
+        pool=nnz * D,
+        bwd_contract=3 * U_12 * f2 + 2 * U_r * f3,
+        s_gather=nnz * D,
+        fwd_bytes=8 * nnz + 8 * (B + 1) + 4 * B * D,
+    )
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+
+class Workload:
+    """Device-resident inputs of one workload plus its captured step graphs."""
+
+    def __init__(self, cfg: int, train: bool, torch, tte, stream):
+        from tensor_train_compressed_gb300.inputs import make_inputs
+        self.torch, self.tte, self.stream = torch, tte, stream
+        self.x = x = make_inputs(cfg, with_grad=train)
+        self.train = train
+        dev = torch.device("cuda")
+        self.cores0 = [torch.from_numpy(c).to(dev) for c in x.cores]
+        self.cores = [c.clone() for c in self.cores0]
+        self.grads = [torch.zeros_like(c) for c in self.cores]
+        self.idx = torch.from_numpy(x.indices).to(dev)
+        self.off = torch.from_numpy(x.offsets).to(dev)
+        self.out = torch.empty((x.num_bags, x.D), dtype=torch.float32, device=dev)
+        self.gout = torch.from_numpy(x.grad_out).to(dev) if train else None
+        ws = tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.ws_bytes = ws
+
+    def step(self):
+        t, x = self.tte, self.x
+        if self.train:
+            for g in self.grads:
+                g.zero_()
+        t.tt_emb_forward(self.cores, x.m, x.n, x.R, self.idx, self.off, self.out, self.ws)
+        if self.train:
+            t.tt_emb_backward(self.gout, self.cores, x.m, x.n, x.R, self.idx, self.off,
+                              self.grads, self.ws, reuse_grouping=True)
+            t.tt_emb_sgd(self.cores, self.grads, x.m, x.n, x.R, LR)
+
+    def restore(self):
+        for c, c0 in zip(self.cores, self.cores0):
+            c.copy_(c0)
+
+    def capture(self, profile: bool = False):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        if profile:
+            self.tte.tt_emb_profile_start()
+        with torch.cuda.graph(g, stream=self.stream, capture_error_mode="thread_local"):
+            self.step()
+        n = self.tte.tt_emb_profile_stop() if profile else 0
+        return g, n
+
+    def counts(self):
+        g = self.tte.read_grouping(self.x.m, self.x.n, self.x.R, self.x.nnz, self.x.num_bags,
+                                   self.ws)
+        return g["U_12"], g["U_r"], g["n_valid"], g["status"]
+
+
+def time_replays(torch, wl, graph, steps, flush, profile_n=0):
+    """Per-replay device ms (events on the replay stream); flush + restore outside the events."""
+    tte = wl.tte
+    s = wl.stream
+    times, per_kernel = [], {}
+    for _ in range(steps):
+        with torch.cuda.stream(s):
+            flush.zero_()
+            wl.restore()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            graph.replay()
+            e1.record(s)
+        s.synchronize()
+        times.append(e0.elapsed_time(e1))
+        for i in range(profile_n):
+            name, ms = tte.tt_emb_profile_read(i)
+            d = per_kernel.setdefault(name, [0.0, 0])
+            d[0] += ms
+            d[1] += 1
+    return times, per_kernel
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import tensor_train_compressed_gb300 as tte
+    from tensor_train_compressed_gb300 import build as tbuild
+
+    tbuild.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    props = torch.cuda.get_device_properties(local)
+    uuid = str(getattr(props, "uuid", ""))
+    gpu_id = uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local))
+    pk = peaks()
+    p_fp32 = fp32_peak_tflops(props.multi_processor_count, pk["sm_max_mhz"])
+    stream = torch.cuda.Stream()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    result = {}
+    for name, cfg, train in (("train", TRAIN_CFG, True), ("forward", FWD_CFG, False)):
+        wl = Workload(cfg, train, torch, tte, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):          # eager warm-up (also settles the library's caches)
+                wl.restore()
+                wl.step()
+        stream.synchronize()
+        rc, bits = tte.tt_emb_get_error(wl.ws, stream)
+        if rc != 0:
+            raise RuntimeError(f"device status {bits} on workload {name}")
+        U_12, U_r, nv, _ = wl.counts()
+        alg = algorithmic(wl.x, U_12, U_r)
+        with torch.cuda.stream(stream):   # creates the timing events before any capture
+            tte.tt_emb_profile_start()
+            wl.restore()
+            wl.step()
+            tte.tt_emb_profile_stop()
+        stream.synchronize()
+        graph, _ = wl.capture()
+        pgraph, n_launch = wl.capture(profile=True)
+        time_replays(torch, wl, graph, max(args.warmup, 3), flush)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(gpu_id)
+        clocks.start()
+        t0 = time.perf_counter()
+        times, _ = time_replays(torch, wl, graph, args.steps, flush)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        clk = clocks.stop()
+        if dist is not None:
+            dist.barrier()
+        _, kern = time_replays(torch, wl, pgraph, max(3, min(args.steps, 10)), flush, n_launch)
+        ms = float(np.mean(times))
+        result[name] = dict(wl=wl, alg=alg, ms=ms, times=times, wall=wall, clocks=clk,
+                            kern=kern, n_launch=n_launch, n_valid=nv)
+
+    # ---- end to end through the public API from pinned host buffers (training step)
+    wl = result["train"]["wl"]
+    x = wl.x
+    idx_h = torch.from_numpy(x.indices).pin_memory()
+    off_h = torch.from_numpy(x.offsets).pin_memory()
+    g_h = torch.from_numpy(x.grad_out).pin_memory()
+    out_h = torch.empty((x.num_bags, x.D), dtype=torch.float32).pin_memory()
+    idx_d, off_d, g_d = torch.empty_like(wl.idx), torch.empty_like(wl.off), torch.empty_like(wl.gout)
+    e2e_times = []
+    for it in range(max(args.warmup, 3) + args.steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            wl.restore()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            idx_d.copy_(idx_h, non_blocking=True)
+            off_d.copy_(off_h, non_blocking=True)
+            g_d.copy_(g_h, non_blocking=True)
+            for gr in wl.grads:
+                gr.zero_()
+            tte.tt_emb_forward(wl.cores, x.m, x.n, x.R, idx_d, off_d, wl.out, wl.ws)
+            tte.tt_emb_backward(g_d, wl.cores, x.m, x.n, x.R, idx_d, off_d, wl.grads, wl.ws,
+                                reuse_grouping=True)
+            tte.tt_emb_sgd(wl.cores, wl.grads, x.m, x.n, x.R, LR)
+            out_h.copy_(wl.out, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        if it >= max(args.warmup, 3):
+            e2e_times.append(e0.elapsed_time(e1))
+    h2d = idx_h.numel() * 8 + off_h.numel() * 8 + g_h.numel() * 4
+    d2h = out_h.numel() * 4
+
+    # ---- max over ranks
+    def rank_max(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    tr, fw = result["train"], result["forward"]
+    ms_train = rank_max(tr["ms"])
+    ms_fwd = rank_max(fw["ms"])
+    ms_e2e = rank_max(float(np.mean(e2e_times)))
+    if rank != 0:
+        return None
+
+    def per_step_kernel_ms(r):
+        steps = max(1, min(len(r["times"]), 10))
+        reps = max(3, min(args.steps, 10))
+        return {k: v[0] / reps for k, v in r["kern"].items()}, steps
+
+    def roofline_of(r, which):
+        """Dominant kernel of the step, its algorithmic FLOPs per launch and its live duration."""
+        kms, _ = per_step_kernel_ms(r)
+        dom = max(kms, key=kms.get)
+        a = r["alg"]
+        launches_per_step = {k: v[1] for k, v in r["kern"].items()}
+        reps = max(3, min(args.steps, 10))
+        flops = {"k_fwd_generic": a["fwd_contract"], "k_fwd_tiled": a["fwd_contract"],
+                 "k_bwd_generic": a["bwd_contract"], "k_bwd_tiled": a["bwd_contract"],
+                 "k_pool": a["pool"], "k_s_gather": a["s_gather"]}
+        per_launch_ms = kms[dom] / max(1, launches_per_step[dom] / reps)
+        out = {"kernel": dom, "share": round(kms[dom] / sum(kms.values()), 4)}
+        if dom in flops:
+            ach = flops[dom] / (per_launch_ms * 1e-3) / 1e12
+            out.update(bound="alu", achieved=round(ach, 3), peak=round(p_fp32, 2),
+                       unit="TFLOP/s", frac=round(ach / p_fp32, 4), traffic=None,
+                       algorithmic_flop_per_launch=flops[dom],
+                       avg_launch_ms=round(per_launch_ms, 5),
+                       peak_source=f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x "
+                                   f"{pk['sm_max_mhz']:.0f} MHz")
+        else:
+            out.update(bound="hbm", achieved=None, peak=pk["hbm_gbs"], unit="GB/s", frac=None,
+                       traffic=None, avg_launch_ms=round(per_launch_ms, 5))
+        return out, {k: round(v, 5) for k, v in sorted(kms.items(), key=lambda kv: -kv[1])}
+
+    roof_tr, kms_tr = roofline_of(tr, "train")
+    roof_fw, kms_fw = roofline_of(fw, "forward")
+    a = fw["alg"]
+    F_fwd = a["fwd_contract"] + a["pool"]
+    t_roof = max(F_fwd / (p_fp32 * 1e12), a["fwd_bytes"] / (pk["hbm_gbs"] * 1e9))
+    fwd_call = {"T_roof_us": round(t_roof * 1e6, 3), "T_call_us": round(ms_fwd * 1e3, 3),
+                "frac": round(t_roof / (ms_fwd * 1e-3), 4),
+                "F_unique_flop": F_fwd, "bytes": a["fwd_bytes"]}
+    at = tr["alg"]
+    nnz_tr = tr["wl"].x.nnz
+    value = nnz_tr * world / (ms_train * 1e-3)
+    cpu = cpu_baseline(args) if (world == 1 and not args.no_cpu_baseline) else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "lookups/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_train, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded cores, Zipf indices, Gaussian grad_out)",
+        "config": {
+            "workload": "training step: 47,952,000 rows = 360x360x370, D=128=4x8x4, "
+                        "R1=R2=32, 32768 bags of U{10..30} Zipf(1.2) lookups, "
+                        "forward + backward + SGD(lr=0.01)",
+            "global_batch": 32768 * world, "lookups_per_gpu": nnz_tr,
+            "unique_rows": at["U_r"], "unique_prefixes": at["U_12"],
+            "parallelism": f"replicas x{world}",
+            "l2": "flushed between timed steps (512 MB write outside the timed events)",
+            "timing": "one CUDA graph replay per step, CUDA events on its stream",
+        },
+        "bags_per_s": round(32768 * world / (ms_train * 1e-3), 1),
+        "roofline": roof_tr,
+        "kernels_ms_per_step": kms_tr,
+        "forward": {
+            "workload": "12,000,000 rows = 200x240x250, D=128=4x8x4, R1=R2=32, 32768 bags x "
+                        "20 Zipf(1.2) lookups, forward only",
+            "lookups_per_s": round(fw["wl"].x.nnz * world / (ms_fwd * 1e-3), 1),
+            "bags_per_s": round(32768 * world / (ms_fwd * 1e-3), 1),
+            "ms_per_call": round(ms_fwd, 5),
+            "unique_rows": a["U_r"], "unique_prefixes": a["U_12"],
+            "roofline_call": fwd_call,
+            "roofline": roof_fw,
+            "kernels_ms_per_call": kms_fw,
+            "clocks": fw["clocks"],
+        },
+        "e2e": {"value": round(nnz_tr * world / (ms_e2e * 1e-3), 1), "unit": "lookups/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e, 5),
+                "path": "pinned host indices/offsets/grad_out -> device, tt_emb_forward, "
+                        "tt_emb_backward, tt_emb_sgd, pooled output -> pinned host"},
+        "gpu_launches": tr["n_launch"] * args.steps,
+        "clocks": tr["clocks"],
+        "workspace_bytes": tr["wl"].ws_bytes,
+        "wall_s_timed_region": round(tr["wall"], 4),
+        "peaks": pk,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+
+def _oracle_sample(bags: int):
+    from tensor_train_compressed_gb300.inputs import make_inputs
+    x = make_inputs(TRAIN_CFG, with_grad=True)
+    sel = np.arange(bags)
+    idx = x.indices[:x.offsets[bags]]
+    off = x.offsets[:bags + 1]
+    return x, idx, off, x.grad_out[sel]
+
+
+def oracle_step(x, idx, off, g, threads):
+    import oracle
+    oracle.forward(x.cores, x.m, x.n, x.R, idx, off, threads=threads)
+    dG = oracle.backward(g, x.cores, x.m, x.n, x.R, idx, off, threads=threads)
+    for k in range(3):
+        oracle.sgd(x.cores[k], dG[k], LR)
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(args, target_s: float = 10.0) -> dict:
+    """The oracle, as it stands, on a bounded sample of the training workload."""
+    import oracle
+    oracle.build()
+    threads = cpu_threads()
+    bags = 2048
+    x, idx, off, g = _oracle_sample(bags)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_step(x, idx, off, g, threads)
+        n += 1
+        if time.perf_counter() - t0 >= target_s or n >= 50:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(len(idx) / dt, 1), "unit": "lookups/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"first {bags} bags ({len(idx)} lookups) of the training workload, "
+                      f"fp64 forward + backward + SGD, {n} repetitions"}
+
+
+def run_reference(args):
+    import oracle
+    oracle.build()
+    threads = cpu_threads()
+    bags = 1024
+    x, idx, off, g = _oracle_sample(bags)
+    for _ in range(args.warmup):
+        oracle_step(x, idx, off, g, threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(x, idx, off, g, threads)
+        times.append(time.perf_counter() - t0)
+    ms = float(np.mean(times)) * 1e3
+    value = len(idx) / (ms * 1e-3)
+    sample = (f"first {bags} bags ({len(idx)} lookups) of the training workload per step, "
+              "fp64 forward + backward + SGD")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "lookups/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "training step: 47,952,000 rows = 360x360x370, D=128=4x8x4, "
+                               "R1=R2=32, U{10..30} Zipf(1.2) bags, forward + backward + SGD",
+                   "sample_bags_per_step": bags},
+        "cpu_baseline": {"value": round(value, 1), "unit": "lookups/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": "lookups/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist_mod.init_process_group("gloo")
+        dist = dist_mod
+    line = run_ours(args, rank, world, dist)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

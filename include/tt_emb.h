@@ -135,6 +135,17 @@ int tt_emb_grouping_view(const int64_t m[3], const int32_t n[3], const int32_t R
                          int64_t nnz, int64_t num_bags, const void* workspace,
                          tt_emb_grouping* view);
 
+/* Opt-in launch timing (process-wide host state, off by default, not
+ * thread-safe).  After tt_emb_profile_start, every kernel launch of the
+ * library is bracketed by two CUDA events recorded on its stream (inside a
+ * stream capture they become event nodes of the graph).
+ * tt_emb_profile_stop ends recording and returns the number of launches
+ * recorded.  tt_emb_profile_read(i, ...) synchronises the i-th record's end
+ * event and returns the kernel's name and its device duration in ms. */
+int tt_emb_profile_start(void);
+int tt_emb_profile_stop(void);
+int tt_emb_profile_read(int i, char* name, int name_len, float* ms);
+
 /* Library version (major*10000 + minor*100 + patch). */
 int tt_emb_version(void);
 

@@ -27,7 +27,8 @@ TT_EMB_ERR_UNSUPPORTED = -7
 _NAMES = {v: k for k, v in list(globals().items()) if k.startswith("TT_EMB_")}
 
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
-            "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_version")
+            "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_profile_start",
+            "tt_emb_profile_stop", "tt_emb_profile_read", "tt_emb_version")
 
 
 class TTEmbError(RuntimeError):
@@ -66,6 +67,10 @@ def lib():
         L.tt_emb_sgd.argtypes = [P, P, P, P, P, ctypes.c_float, P]
         L.tt_emb_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
         L.tt_emb_grouping_view.argtypes = [P, P, P, I64, I64, P, ctypes.POINTER(Grouping)]
+        L.tt_emb_profile_start.argtypes = []
+        L.tt_emb_profile_stop.argtypes = []
+        L.tt_emb_profile_read.argtypes = [ctypes.c_int, ctypes.c_char_p, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_float)]
         for name in EXPORTED:
             getattr(L, name).restype = ctypes.c_int
         L.tt_emb_version.argtypes = []
@@ -158,6 +163,22 @@ def tt_emb_grouping_view(m, n, R, nnz: int, num_bags: int, workspace) -> dict:
                                       _dev(workspace, torch.uint8, "workspace"), ctypes.byref(g)),
            "tt_emb_grouping_view")
     return {name: getattr(g, name) for name, _ in Grouping._fields_}
+
+
+def tt_emb_profile_start():
+    _check(lib().tt_emb_profile_start(), "tt_emb_profile_start")
+
+
+def tt_emb_profile_stop() -> int:
+    return int(lib().tt_emb_profile_stop())
+
+
+def tt_emb_profile_read(i: int) -> tuple[str, float]:
+    """(kernel name, device ms) of the i-th recorded launch (synchronises its end event)."""
+    buf = ctypes.create_string_buffer(64)
+    ms = ctypes.c_float(0.0)
+    _check(lib().tt_emb_profile_read(int(i), buf, 64, ctypes.byref(ms)), "tt_emb_profile_read")
+    return buf.value.decode(), float(ms.value)
 
 
 def tt_emb_version() -> int:

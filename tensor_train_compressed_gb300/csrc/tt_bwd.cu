@@ -231,9 +231,9 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   int grid = (int)ceil_div(L.rowbuf_rows, 8);
   if (grid > sms * 16) grid = sms * 16;
   if (grid < 1) grid = 1;
-  k_s_zero<<<grid, 256, 0, st>>>(w, s.D);
+  TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D)));
   const int64_t slices = ceil_div(nnz, kSSlice);
-  k_s_gather<<<(int)ceil_div(slices, 8), 256, 0, st>>>(w, grad_out, num_bags, s.D);
+  TT_TIMED("k_s_gather", st, (k_s_gather<<<(int)ceil_div(slices, 8), 256, 0, st>>>(w, grad_out, num_bags, s.D)));
 
   BwdArgs ba;
   ba.s = s;
@@ -254,7 +254,7 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
                          kMaxSmemFloats * (int)sizeof(float));
     attr_set = true;
   }
-  k_bwd_generic<<<persistent_grid_bwd((const void*)k_bwd_generic, 256, smem), 256, smem, st>>>(ba);
+  TT_TIMED("k_bwd_generic", st, (k_bwd_generic<<<persistent_grid_bwd((const void*)k_bwd_generic, 256, smem), 256, smem, st>>>(ba)));
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }
 
@@ -265,7 +265,7 @@ int launch_sgd(float* const cores[3], const float* const grads[3], const Shape& 
     int grid = (int)ceil_div(ceil_div(counts[k], 4), 256);
     if (grid > sm_count() * 8) grid = sm_count() * 8;
     if (grid < 1) grid = 1;
-    k_sgd<<<grid, 256, 0, st>>>(cores[k], grads[k], counts[k], lr);
+    TT_TIMED("k_sgd", st, (k_sgd<<<grid, 256, 0, st>>>(cores[k], grads[k], counts[k], lr)));
   }
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }

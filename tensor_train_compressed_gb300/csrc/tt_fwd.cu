@@ -178,12 +178,12 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
                          kMaxSmemFloats * (int)sizeof(float));
     attr_set = true;
   }
-  k_fwd_generic<<<persistent_grid((const void*)k_fwd_generic, 256, smem), 256, smem, st>>>(fa);
+  TT_TIMED("k_fwd_generic", st, (k_fwd_generic<<<persistent_grid((const void*)k_fwd_generic, 256, smem), 256, smem, st>>>(fa)));
   if (num_bags > 0) {
     int grid = (int)ceil_div(num_bags, 8);
     const int cap = sm_count() * 16;
     if (grid > cap) grid = cap;
-    k_pool<<<grid, 256, 0, st>>>(offsets, num_bags, nnz, w.uid, w.rowbuf, s.D, out);
+    TT_TIMED("k_pool", st, (k_pool<<<grid, 256, 0, st>>>(offsets, num_bags, nnz, w.uid, w.rowbuf, s.D, out)));
   }
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }

@@ -437,7 +437,7 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
   const int cap = sm_count() * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  k_prepare<<<grid, 256, 0, st>>>(pa);
+  TT_TIMED("k_prepare", st, (k_prepare<<<grid, 256, 0, st>>>(pa)));
 
   const uint64_t* in = nullptr;
   for (int p = 0; p < L.passes; ++p) {
@@ -451,7 +451,7 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
     sa.pass = p;
     sa.n_tiles = L.n_sort_tiles;
     sa.w = w;
-    k_scatter<<<L.n_sort_tiles, kSortThreads, 0, st>>>(sa);
+    TT_TIMED("k_scatter", st, (k_scatter<<<L.n_sort_tiles, kSortThreads, 0, st>>>(sa)));
     in = sa.out;
   }
   SegArgs ga;
@@ -459,13 +459,13 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
   ga.nnz = nnz;
   ga.s = s;
   ga.w = w;
-  k_segment<<<L.n_scan_tiles, kScanThreads, 0, st>>>(ga);
+  TT_TIMED("k_segment", st, (k_segment<<<L.n_scan_tiles, kScanThreads, 0, st>>>(ga)));
 
   ChunkArgs ca;
   ca.w = w;
   ca.pairs_per_chunk = pairs_per_chunk;
   ca.rows_per_chunk = rows_per_chunk;
-  k_chunks<<<L.n_scan_tiles, kScanThreads, 0, st>>>(ca);
+  TT_TIMED("k_chunks", st, (k_chunks<<<L.n_scan_tiles, kScanThreads, 0, st>>>(ca)));
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }
 

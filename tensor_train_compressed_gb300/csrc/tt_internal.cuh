@@ -153,6 +153,17 @@ __device__ __forceinline__ uint32_t block_exclusive_scan_256(uint32_t v, uint32_
 
 // ---------------------------------------------------------------- host side
 
+// opt-in launch timing (tt_prof.cu)
+extern bool g_prof_on;
+void prof_begin(const char* name, cudaStream_t st);
+void prof_end(cudaStream_t st);
+#define TT_TIMED(name, st, launch) \
+  do {                             \
+    ::tt::prof_begin(name, st);    \
+    launch;                        \
+    ::tt::prof_end(st);            \
+  } while (0)
+
 int64_t ceil_div(int64_t a, int64_t b);
 Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags);
 WS make_ws(void* base, const Layout& L);
