@@ -23,6 +23,16 @@ std::vector<Rec> g_recs;
 size_t g_next = 0;
 int g_open = -1;
 
+// Inside a stream capture a plain record only orders the graph; the external
+// flag makes it an event node that takes a timestamp on every replay.
+void record(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, st);
+}
+
 int take_event() {
   if (g_next == g_pool.size()) {
     cudaEvent_t e;
@@ -37,7 +47,7 @@ void prof_begin(const char* name, cudaStream_t st) {
   if (!g_prof_on) return;
   const int a = take_event();
   if (a < 0) return;
-  cudaEventRecord(g_pool[a], st);
+  record(g_pool[a], st);
   g_recs.push_back(Rec{name, a, -1});
   g_open = (int)g_recs.size() - 1;
 }
@@ -46,7 +56,7 @@ void prof_end(cudaStream_t st) {
   if (!g_prof_on || g_open < 0) return;
   const int b = take_event();
   if (b >= 0) {
-    cudaEventRecord(g_pool[b], st);
+    record(g_pool[b], st);
     g_recs[g_open].b = b;
   }
   g_open = -1;
