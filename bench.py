@@ -128,6 +128,21 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def rank_max(dist, v: float) -> float:
+    """Max of a per-rank time over all ranks (the slowest replica sets the step time)."""
+    if dist is None:
+        return float(v)
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_throughput(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job units/s: every rank processes its own batch in the max-over-ranks time."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 
@@ -295,18 +310,10 @@ def run_ours(args, rank, world, dist):
     h2d = idx_h.numel() * 8 + off_h.numel() * 8 + g_h.numel() * 4
     d2h = out_h.numel() * 4
 
-    # ---- max over ranks
-    def rank_max(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     tr, fw = result["train"], result["forward"]
-    ms_train = rank_max(tr["ms"])
-    ms_fwd = rank_max(fw["ms"])
-    ms_e2e = rank_max(float(np.mean(e2e_times)))
+    ms_train = rank_max(dist, tr["ms"])
+    ms_fwd = rank_max(dist, fw["ms"])
+    ms_e2e = rank_max(dist, float(np.mean(e2e_times)))
     if rank != 0:
         return None
 
@@ -350,7 +357,7 @@ def run_ours(args, rank, world, dist):
                 "F_unique_flop": F_fwd, "bytes": a["fwd_bytes"]}
     at = tr["alg"]
     nnz_tr = tr["wl"].x.nnz
-    value = nnz_tr * world / (ms_train * 1e-3)
+    value = weak_throughput(nnz_tr, world, ms_train)
     cpu = cpu_baseline(args) if (world == 1 and not args.no_cpu_baseline) else None
     line = {
         "metric": METRIC,
