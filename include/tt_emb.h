@@ -126,7 +126,7 @@ typedef struct {
   const int32_t* pair_i1;         /* [U_12]                                                     */
   const int32_t* pair_i2;         /* [U_12]                                                     */
   const int32_t* uid;             /* [nnz]   unique row of each lookup, -1 if out of range      */
-  const int32_t* bag_of;          /* [nnz]   bag of each lookup                                */
+  const int32_t* bag_of;          /* [nnz]   bag of each lookup (written by tt_emb_backward)   */
   const int32_t* chunk_start;     /* [chunks+1] first unique row of each work chunk             */
   const float* rowbuf;            /* [U_r][D] unique rows (after a forward)                    */
 } tt_emb_grouping;

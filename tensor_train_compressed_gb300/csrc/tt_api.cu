@@ -226,7 +226,7 @@ int tt_emb_backward(const float* grad_out, const float* const cores[3], const in
     rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, st);
     if (rc) return rc;
   }
-  return launch_backward(s, L, w, grad_out, cores, nnz, num_bags, core_grads, st);
+  return launch_backward(s, L, w, grad_out, cores, offsets, nnz, num_bags, core_grads, st);
 }
 
 int tt_emb_sgd(float* const cores[3], const float* const core_grads[3], const int64_t m[3],

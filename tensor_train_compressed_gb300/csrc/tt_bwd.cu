@@ -15,22 +15,32 @@
 // boundary is accumulated with atomics into a zeroed row, all others are
 // stored once.  Core gradients are accumulated with float atomics.
 #include "tt_internal.cuh"
+#include "tt_tile.cuh"
 
 namespace tt {
 
-// Zero the S rows that more than one gather slice will add into, and reset
-// the backward chunk counter.
-__global__ void __launch_bounds__(256) k_s_zero(WS w, int D) {
+// Zero the S rows that more than one gather slice will add into, write the bag
+// of every lookup (CSR offsets, one warp per bag, clamped so that bad offsets
+// stay in bounds) and reset the backward chunk counter.
+__global__ void __launch_bounds__(256) k_s_zero(WS w, int D, const int64_t* __restrict__ offsets,
+                                                int64_t B, int64_t nnz) {
   if (blockIdx.x == 0 && threadIdx.x == 0) w.ctl->bwd_chunk_ctr = 0;
   const int U = w.ctl->U_r;
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < U; u += warps) {
+  const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (int64_t u = gw; u < U; u += warps) {
     const int32_t s0 = w.row_start[u], s1 = w.row_start[u + 1];
     if (s0 / kSSlice != (s1 - 1) / kSSlice) {
       float* r = w.rowbuf + u * (int64_t)D;
       for (int j = lane; j < D; j += 32) r[j] = 0.f;
     }
+  }
+  for (int64_t b = gw; b < B; b += warps) {
+    int64_t l0 = offsets[b], l1 = offsets[b + 1];
+    l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
+    l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
+    for (int64_t l = l0 + lane; l < l1; l += 32) w.bag_of[l] = (int32_t)b;
   }
 }
 
@@ -40,15 +50,8 @@ __device__ __forceinline__ void s_flush(const WS& w, int32_t u, int64_t k0, int 
   const bool shared_row = s0 < k0 || s1 > k0 + kSSlice;
   if (vec) {
     float4* dst = reinterpret_cast<float4*>(w.rowbuf + u * (int64_t)D) + c;
-    if (shared_row) {
-      float* d = reinterpret_cast<float*>(dst);
-      atomicAdd(d + 0, acc.x);
-      atomicAdd(d + 1, acc.y);
-      atomicAdd(d + 2, acc.z);
-      atomicAdd(d + 3, acc.w);
-    } else {
-      *dst = acc;
-    }
+    if (shared_row) atomicAdd(dst, acc);
+    else *dst = acc;
   } else {
     float* dst = w.rowbuf + u * (int64_t)D + c;
     if (shared_row) atomicAdd(dst, accs);
@@ -56,7 +59,9 @@ __device__ __forceinline__ void s_flush(const WS& w, int32_t u, int64_t k0, int 
   }
 }
 
-// S[x] for every unique row: one warp per slice of kSSlice sorted lookups.
+// S[x] for every unique row: one warp per slice of kSSlice sorted lookups.  The
+// lanes first fetch the slice's (unique row, bag) pairs in parallel; then the
+// output-gradient rows are summed with several loads in flight.
 __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict__ grad_out,
                                                   int64_t B, int D) {
   const int lane = threadIdx.x & 31;
@@ -64,31 +69,65 @@ __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict_
   const int64_t k0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kSSlice;
   if (k0 >= nv) return;
   const int64_t k1 = k0 + kSSlice < nv ? k0 + kSSlice : nv;
+  int32_t um[kSSlice / 32], bm[kSSlice / 32];
+#pragma unroll
+  for (int h = 0; h < kSSlice / 32; ++h) {
+    const int64_t k = k0 + h * 32 + lane;
+    um[h] = -1;
+    bm[h] = 0;
+    if (k < k1) {
+      const int32_t l = w.perm[k];
+      um[h] = w.uid[l];
+      int32_t b = w.bag_of[l];
+      bm[h] = b < 0 ? 0 : (b >= B ? (int32_t)(B - 1) : b);
+    }
+  }
+  const int n = (int)(k1 - k0);
   const bool vec = (D & 3) == 0;
   const int cols = vec ? (D >> 2) : D;
-  for (int c = lane; c < cols; c += 32) {
+  for (int c = lane; c < cols + ((32 - cols % 32) % 32); c += 32) {
+    const bool live = c < cols;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float accs = 0.f;
     int32_t cur = -1;
-    for (int64_t k = k0; k < k1; ++k) {
-      const int32_t l = w.perm[k];
-      const int32_t u = w.uid[l];
-      int32_t b = w.bag_of[l];
-      b = b < 0 ? 0 : (b >= B ? (int32_t)(B - 1) : b);
-      if (u != cur) {
-        if (cur >= 0) s_flush(w, cur, k0, c, D, acc, vec, accs);
-        acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        accs = 0.f;
-        cur = u;
+    for (int j0 = 0; j0 < n; j0 += 4) {
+      int32_t uj[4], bj[4];
+      float4 g[4];
+      float gs[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int j = j0 + t;
+        const int h = (j >> 5) & (kSSlice / 32 - 1);
+        int32_t us = -1, bs = 0;
+#pragma unroll
+        for (int hh = 0; hh < kSSlice / 32; ++hh) {
+          const int32_t uu = __shfl_sync(0xffffffffu, um[hh], j & 31);
+          const int32_t bb = __shfl_sync(0xffffffffu, bm[hh], j & 31);
+          if (hh == h) { us = uu; bs = bb; }
+        }
+        uj[t] = j < n ? us : -2;
+        bj[t] = bs;
+        g[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        gs[t] = 0.f;
+        if (live && j < n) {
+          if (vec) g[t] = reinterpret_cast<const float4*>(grad_out + bj[t] * (int64_t)D)[c];
+          else gs[t] = grad_out[bj[t] * (int64_t)D + c];
+        }
       }
-      if (vec) {
-        const float4 g = reinterpret_cast<const float4*>(grad_out + b * (int64_t)D)[c];
-        acc.x += g.x; acc.y += g.y; acc.z += g.z; acc.w += g.w;
-      } else {
-        accs += grad_out[b * (int64_t)D + c];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (uj[t] == -2) break;
+        if (uj[t] != cur) {
+          if (cur >= 0 && live) s_flush(w, cur, k0, c, D, acc, vec, accs);
+          acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          accs = 0.f;
+          cur = uj[t];
+        }
+        acc.x += g[t].x; acc.y += g[t].y; acc.z += g[t].z; acc.w += g[t].w;
+        accs += gs[t];
       }
     }
-    if (cur >= 0) s_flush(w, cur, k0, c, D, acc, vec, accs);
+    if (cur >= 0 && live) s_flush(w, cur, k0, c, D, acc, vec, accs);
   }
 }
 
@@ -197,6 +236,287 @@ __global__ void __launch_bounds__(256) k_bwd_generic(BwdArgs a) {
   (void)n2;
 }
 
+// ---------------------------------------------------------------------------
+// Register-tiled backward chunk kernel (n1 = n3 = 4, R1 = R2 = R).  A chunk that
+// starts a hot prefix takes ALL of that prefix's rows (its dP2 is summed in
+// shared memory before dG2/dG1 are formed once); the chunks holding the later
+// pieces of that prefix are skipped.  Shared memory:
+//   G2s [R][N2*R], P1t [CP][R][4], P2 and dP2 [CP][4*N2][R+4] (+4 per prefix),
+//   S [32][D+4] (gathered output gradients of a batch of rows),
+//   G3t [32][4*R+4] (G3 slices of the batch, transposed to [j3][b]).
+template <int N2, int R, int CP>
+struct BwdCfg {
+  using T = TileCfg<N2, R, CP>;
+  static constexpr int RB = 32;
+  static constexpr int SS = T::D + 4;
+  static constexpr int G3TS = 4 * R + 4;
+  static constexpr int F_S = RB * SS;
+  static constexpr int F_G3 = RB * G3TS;
+  static constexpr int SMEM = 4 * (T::F_G2 + T::F_P1 + 2 * T::F_P2 + F_S + F_G3) + 8 * RB;
+  static constexpr int TILES = T::NB * (R / 4);          // (j12 block, b block) tiles of dP2
+  static constexpr int RG = 256 / TILES;                  // row groups in the dP2 phase
+  static_assert(256 % TILES == 0 && RB % RG == 0, "dP2 phase mapping");
+  static_assert(T::NC % 128 == 0, "dG2 phase mapping");
+};
+
+template <int N2, int R, int CP>
+__global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
+  using C = BwdCfg<N2, R, CP>;
+  using T = typename C::T;
+  constexpr int NC = T::NC, P2S = T::P2S, P2P = T::P2P, D = T::D;
+  extern __shared__ float4 sm4[];
+  float* G2s = reinterpret_cast<float*>(sm4);
+  float* P1t = G2s + T::F_G2;
+  float* P2 = P1t + T::F_P1;
+  float* dP2 = P2 + T::F_P2;
+  float* Ss = dP2 + T::F_P2;
+  float* G3t = Ss + C::F_S;
+  int* rowp = reinterpret_cast<int*>(G3t + C::F_G3);
+  int* rowi3 = rowp + C::RB;
+  __shared__ int c_sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_chunks = a.w.ctl->n_chunks;
+  for (;;) {
+    if (tid == 0) c_sh = (int)atomicAdd(&a.w.ctl->bwd_chunk_ctr, 1u);
+    __syncthreads();
+    const int c = c_sh;
+    if (c >= n_chunks) break;
+    const int x0 = a.w.chunk_start[c];
+    const int p0 = a.w.row_pair[x0];
+    const int pr0 = a.w.pair_row_start[p0];
+    if (x0 != pr0) {          // a later piece of a hot prefix: its first chunk does it all
+      __syncthreads();
+      continue;
+    }
+    int x1 = a.w.chunk_start[c + 1];
+    const int p1 = a.w.row_pair[x1 - 1];
+    if (p1 == p0) x1 = a.w.pair_row_start[p0 + 1];   // whole prefix
+    const int np = p1 - p0 + 1;
+    const int i2 = a.w.pair_i2[p0];
+    tiled_load_g2_p1<T>(a.G1, a.G2, a.w.pair_i1, i2, p0, np, G2s, P1t);
+    for (int e = tid; e < np * P2P; e += 256) dP2[e] = 0.f;
+    __syncthreads();
+    tiled_stage2_any<T>(G2s, P1t, P2, np);
+
+    for (int xb = x0; xb < x1; xb += C::RB) {
+      const int nb = min(C::RB, x1 - xb);
+      __syncthreads();
+      if (tid < nb) {
+        rowp[tid] = a.w.row_pair[xb + tid] - p0;
+        rowi3[tid] = a.w.row_i3[xb + tid];
+      }
+      // S rows of the batch
+      for (int e = tid; e < nb * (D / 4); e += 256) {
+        const int r = e / (D / 4), q = e - r * (D / 4);
+        const float4 v = reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)(xb + r) * D)[q];
+        *reinterpret_cast<float4*>(Ss + r * C::SS + 4 * q) = v;
+      }
+      // G3 slices, transposed to [j3][b]
+      for (int e = tid; e < nb * R; e += 256) {
+        const int r = e / R, b = e - r * R;
+        const float4 v = __ldg(reinterpret_cast<const float4*>(
+            a.G3 + ((size_t)a.w.row_i3[xb + r] * R + b) * 4));
+        float* g = G3t + r * C::G3TS + b;
+        g[0] = v.x;
+        g[R] = v.y;
+        g[2 * R] = v.z;
+        g[3 * R] = v.w;
+      }
+      __syncthreads();
+      // dG3[i3][b][j3] += sum_j12 P2[j12][b] S[j12][j3]: lane = row, warp = block of 4 b
+      if (lane < nb) {
+        const int r = lane;
+        const float* ss = Ss + r * C::SS;
+        for (int bb = warp; bb < R / 4; bb += 8) {
+          const float* pp = P2 + rowp[r] * P2P + 4 * bb;
+          float acc[4][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 8
+          for (int j12 = 0; j12 < 4 * N2; ++j12) {
+            const float4 pv = *reinterpret_cast<const float4*>(pp + j12 * P2S);
+            const float4 sv = *reinterpret_cast<const float4*>(ss + 4 * j12);
+            const float pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[i][0] = fmaf(pw[i], sv.x, acc[i][0]);
+              acc[i][1] = fmaf(pw[i], sv.y, acc[i][1]);
+              acc[i][2] = fmaf(pw[i], sv.z, acc[i][2]);
+              acc[i][3] = fmaf(pw[i], sv.w, acc[i][3]);
+            }
+          }
+          float4* dst = reinterpret_cast<float4*>(a.dG3 + ((size_t)rowi3[r] * R + 4 * bb) * 4);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            atomicAdd(dst + i, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+        }
+      }
+      // dP2[p][j12][b] += sum_j3 S[j12][j3] G3[b][j3]: tile (4 j12 x 4 b) per thread,
+      // row groups walk their rows and flush at every change of prefix
+      {
+        const int tile = tid % C::TILES, rg = tid / C::TILES;
+        const int jb = tile / (R / 4), bq = tile - jb * (R / 4);
+        constexpr int RPG = C::RB / C::RG;
+        const int r0 = rg * RPG, r1 = min(r0 + RPG, nb);
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        int cur = -1;
+        for (int r = r0; r < r1; ++r) {
+          const int pl = rowp[r];
+          if (pl != cur) {
+            if (cur >= 0) {
+              float* d = dP2 + cur * P2P + (4 * jb) * P2S + 4 * bq;
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  atomicAdd(d + i * P2S + j, acc[i][j]);
+                  acc[i][j] = 0.f;
+                }
+            }
+            cur = pl;
+          }
+          float4 sv[4], gv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            sv[i] = *reinterpret_cast<const float4*>(Ss + r * C::SS + (4 * jb + i) * 4);
+#pragma unroll
+          for (int j3 = 0; j3 < 4; ++j3)
+            gv[j3] = *reinterpret_cast<const float4*>(G3t + r * C::G3TS + j3 * R + 4 * bq);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float s4[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};
+#pragma unroll
+            for (int j3 = 0; j3 < 4; ++j3) {
+              acc[i][0] = fmaf(s4[j3], gv[j3].x, acc[i][0]);
+              acc[i][1] = fmaf(s4[j3], gv[j3].y, acc[i][1]);
+              acc[i][2] = fmaf(s4[j3], gv[j3].z, acc[i][2]);
+              acc[i][3] = fmaf(s4[j3], gv[j3].w, acc[i][3]);
+            }
+          }
+        }
+        if (cur >= 0) {
+          float* d = dP2 + cur * P2P + (4 * jb) * P2S + 4 * bq;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) atomicAdd(d + i * P2S + j, acc[i][j]);
+        }
+      }
+    }
+    __syncthreads();
+    // dG2[i2][a][n] += sum_{p, j1} P1[p][j1][a] dP2[p][j1][n]: warp = block of 4 a,
+    // lane = 4-column groups at stride 128
+    {
+      constexpr int Q = NC / 128;
+      for (int ab = warp; ab < R / 4; ab += 8) {
+        float acc[4][4 * Q];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4 * Q; ++j) acc[i][j] = 0.f;
+        for (int p = 0; p < np; ++p) {
+          float4 av[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            av[i] = *reinterpret_cast<const float4*>(P1t + p * (R * 4) + (4 * ab + i) * 4);
+#pragma unroll
+          for (int j1 = 0; j1 < 4; ++j1) {
+            float bv[4 * Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+              const int n = q * 128 + 4 * lane;
+              const int j2 = n / R, b = n - j2 * R;
+              const float4 v = *reinterpret_cast<const float4*>(
+                  dP2 + p * P2P + (j1 * N2 + j2) * P2S + b);
+              bv[4 * q] = v.x; bv[4 * q + 1] = v.y; bv[4 * q + 2] = v.z; bv[4 * q + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float aw = j1 == 0 ? av[i].x : (j1 == 1 ? av[i].y : (j1 == 2 ? av[i].z : av[i].w));
+#pragma unroll
+              for (int j = 0; j < 4 * Q; ++j) acc[i][j] = fmaf(aw, bv[j], acc[i][j]);
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int q = 0; q < Q; ++q) {
+            float4* dst = reinterpret_cast<float4*>(
+                a.dG2 + (size_t)i2 * T::F_G2 + (size_t)(4 * ab + i) * NC + q * 128 + 4 * lane);
+            atomicAdd(dst, make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2],
+                                       acc[i][4 * q + 3]));
+          }
+      }
+    }
+    // dG1[i1_p][j1][a] += sum_n dP2[p][j1][n] G2[a][n]: item = (prefix, 4 a, n-slice);
+    // the 8 n-slices of an item sit in 8 adjacent lanes and are summed by shuffles
+    {
+      constexpr int AQ = R / 4;
+      const int items = np * AQ * 8;
+      for (int base = 0; base < items; base += 256) {
+        const int item = base + tid;
+        const bool valid = item < items;
+        const int ns = item & 7, g = item >> 3;
+        const int p = g / AQ, aq = g - p * AQ;
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        if (valid) {
+          for (int s = 0; s < NC / 32; ++s) {
+            const int n = 32 * s + 4 * ns;
+            const int j2 = n / R, b = n - j2 * R;
+            float4 dv[4], gv[4];
+#pragma unroll
+            for (int j1 = 0; j1 < 4; ++j1)
+              dv[j1] = *reinterpret_cast<const float4*>(dP2 + p * P2P + (j1 * N2 + j2) * P2S + b);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              gv[i] = *reinterpret_cast<const float4*>(G2s + (4 * aq + i) * NC + n);
+#pragma unroll
+            for (int j1 = 0; j1 < 4; ++j1)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                float v = acc[j1][i];
+                v = fmaf(dv[j1].x, gv[i].x, v);
+                v = fmaf(dv[j1].y, gv[i].y, v);
+                v = fmaf(dv[j1].z, gv[i].z, v);
+                v = fmaf(dv[j1].w, gv[i].w, v);
+                acc[j1][i] = v;
+              }
+          }
+        }
+#pragma unroll
+        for (int j1 = 0; j1 < 4; ++j1)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float v = acc[j1][i];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            acc[j1][i] = v;
+          }
+        if (valid && ns == 0) {
+          const int i1 = a.w.pair_i1[p0 + p];
+#pragma unroll
+          for (int j1 = 0; j1 < 4; ++j1)
+            atomicAdd(reinterpret_cast<float4*>(a.dG1 + ((size_t)i1 * 4 + j1) * R + 4 * aq),
+                      make_float4(acc[j1][0], acc[j1][1], acc[j1][2], acc[j1][3]));
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void k_sgd(float* __restrict__ G, const float* __restrict__ dG, int64_t count, float lr) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t n4 = count >> 2;
@@ -224,14 +544,14 @@ static int persistent_grid_bwd(const void* fn, int threads, size_t smem) {
 }
 
 int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out,
-                    const float* const cores[3], int64_t nnz, int64_t num_bags,
-                    float* const core_grads[3], cudaStream_t st) {
+                    const float* const cores[3], const int64_t* offsets, int64_t nnz,
+                    int64_t num_bags, float* const core_grads[3], cudaStream_t st) {
   if (nnz == 0) return TT_EMB_OK;
   const int sms = sm_count();
-  int grid = (int)ceil_div(L.rowbuf_rows, 8);
+  int grid = (int)ceil_div(L.rowbuf_rows > num_bags ? L.rowbuf_rows : num_bags, 8);
   if (grid > sms * 16) grid = sms * 16;
   if (grid < 1) grid = 1;
-  TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D)));
+  TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D, offsets, num_bags, nnz)));
   const int64_t slices = ceil_div(nnz, kSSlice);
   TT_TIMED("k_s_gather", st, (k_s_gather<<<(int)ceil_div(slices, 8), 256, 0, st>>>(w, grad_out, num_bags, s.D)));
 
@@ -244,17 +564,28 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   ba.dG1 = core_grads[0];
   ba.dG2 = core_grads[1];
   ba.dG3 = core_grads[2];
-  const size_t g2n = (size_t)s.R1 * s.n2 * s.R2;
-  const size_t base = g2n + (size_t)s.n1 * s.R1 + 2 * (size_t)s.n1 * s.n2 * s.R2;
-  ba.dG2_in_smem = (base + g2n) <= (size_t)kMaxSmemFloats;
-  const size_t smem = sizeof(float) * (base + (ba.dG2_in_smem ? g2n : 0));
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(k_bwd_generic, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kMaxSmemFloats * (int)sizeof(float));
-    attr_set = true;
+  if (s.n1 == 4 && s.n3 == 4 && s.n2 == 8 && s.R1 == 32 && s.R2 == 32) {
+    using C = BwdCfg<8, 32, kCP_8_32>;
+    static int grid = 0;
+    if (grid == 0) {
+      cudaFuncSetAttribute(k_bwd_tiled<8, 32, kCP_8_32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM);
+      grid = persistent_grid_bwd((const void*)k_bwd_tiled<8, 32, kCP_8_32>, 256, C::SMEM);
+    }
+    TT_TIMED("k_bwd_tiled", st, (k_bwd_tiled<8, 32, kCP_8_32><<<grid, 256, C::SMEM, st>>>(ba)));
+  } else {
+    const size_t g2n = (size_t)s.R1 * s.n2 * s.R2;
+    const size_t base = g2n + (size_t)s.n1 * s.R1 + 2 * (size_t)s.n1 * s.n2 * s.R2;
+    ba.dG2_in_smem = (base + g2n) <= (size_t)kMaxSmemFloats;
+    const size_t smem = sizeof(float) * (base + (ba.dG2_in_smem ? g2n : 0));
+    static int grid = 0;
+    if (grid == 0) {
+      cudaFuncSetAttribute(k_bwd_generic, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmemFloats * (int)sizeof(float));
+      grid = persistent_grid_bwd((const void*)k_bwd_generic, 256, kMaxSmemFloats * sizeof(float));
+    }
+    TT_TIMED("k_bwd_generic", st, (k_bwd_generic<<<grid, 256, smem, st>>>(ba)));
   }
-  TT_TIMED("k_bwd_generic", st, (k_bwd_generic<<<persistent_grid_bwd((const void*)k_bwd_generic, 256, smem), 256, smem, st>>>(ba)));
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }
 

@@ -14,6 +14,7 @@
 // Persistent CTAs take chunks from an atomic counter (dynamic load
 // balancing under Zipf skew, FlowTT summary card, key innovations).
 #include "tt_internal.cuh"
+#include "tt_tile.cuh"
 
 namespace tt {
 
@@ -81,101 +82,6 @@ __global__ void __launch_bounds__(256) k_fwd_generic(FwdArgs a) {
   }
 }
 
-// ---------------------------------------------------------------------------
-// Register-tiled chunk kernel for n1 = n3 = 4 and R1 = R2 = R (the shapes of the
-// benchmark tables).  Shared memory per CTA:
-//   G2s  [R][N2*R]          the chunk's G2 slice (all its prefixes share i2)
-//   P1t  [CP][R][4]         G1[i1_p] transposed, a-major
-//   P2   [CP][4*N2][R+4]    prefix partials, rows padded by 4 floats and the
-//                           per-prefix block by 4 more, so that the 128-bit
-//                           loads of stage 3 are free of bank conflicts
-//   G3s  [RB][R*4+4]        G3 slices of a batch of RB rows, padded likewise
-// Stage 2 is a (4*np) x (N2*R) x R GEMM: each thread owns the 4 j1 rows of one
-// prefix and C columns (C chosen from np so that ~256 threads are busy).
-// Stage 3 gives each warp one block of 4 j12 values and each lane one row.
-template <int N2, int R, int CP>
-struct TileCfg {
-  static constexpr int N1 = 4, N3 = 4, kN2 = N2, kR = R;
-  static constexpr int NC = N2 * R;                 // stage-2 columns (j2, b)
-  static constexpr int NB = N1 * N2 / 4;            // j12 blocks of 4
-  static constexpr int P2S = R + 4;                 // padded P2 row stride
-  static constexpr int P2P = N1 * N2 * P2S + 4;     // padded P2 block per prefix
-  static constexpr int RB = 32 * (8 / NB);          // rows per stage-3 batch
-  static constexpr int G3S = R * N3 + 4;            // padded G3 row stride
-  static constexpr int D = N1 * N2 * N3;
-  static constexpr int F_G2 = R * NC;
-  static constexpr int F_P1 = CP * R * N1;
-  static constexpr int F_P2 = CP * P2P;
-  static constexpr int F_G3 = RB * G3S;
-  static constexpr int SMEM = 4 * (F_G2 + F_P1 + F_P2 + F_G3);
-  static constexpr int MIN_BLOCKS = SMEM <= 110 * 1024 ? 2 : 1;
-  static_assert(NB == 4 || NB == 8, "j12 blocks must fill 8 warps");
-  static_assert(R % 4 == 0, "R must be a multiple of 4");
-};
-
-template <class T, int C>
-__device__ __forceinline__ void tiled_stage2(const float* __restrict__ G2s,
-                                             const float* __restrict__ P1t,
-                                             float* __restrict__ P2, int np) {
-  constexpr int R = T::kR;
-  constexpr int NC = T::NC;
-  constexpr int G = NC / C;                 // column groups per prefix
-  for (int item = threadIdx.x; item < np * G; item += blockDim.x) {
-    const int p = item / G, cg = item - p * G;
-    float acc[4][C];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int c = 0; c < C; ++c) acc[i][c] = 0.f;
-    const float* ap = P1t + p * (R * 4);
-#pragma unroll 8
-    for (int k = 0; k < R; ++k) {
-      const float4 av = *reinterpret_cast<const float4*>(ap + k * 4);
-      float bv[C];
-      const float* brow = G2s + k * NC;
-      if constexpr (C >= 4) {
-#pragma unroll
-        for (int q = 0; q < C / 4; ++q) {
-          const float4 v = *reinterpret_cast<const float4*>(brow + q * (NC * 4 / C) + 4 * cg);
-          bv[4 * q] = v.x; bv[4 * q + 1] = v.y; bv[4 * q + 2] = v.z; bv[4 * q + 3] = v.w;
-        }
-      } else if constexpr (C == 2) {
-        const float2 v = *reinterpret_cast<const float2*>(brow + 2 * cg);
-        bv[0] = v.x; bv[1] = v.y;
-      } else {
-        bv[0] = brow[cg];
-      }
-#pragma unroll
-      for (int c = 0; c < C; ++c) {
-        acc[0][c] = fmaf(av.x, bv[c], acc[0][c]);
-        acc[1][c] = fmaf(av.y, bv[c], acc[1][c]);
-        acc[2][c] = fmaf(av.z, bv[c], acc[2][c]);
-        acc[3][c] = fmaf(av.w, bv[c], acc[3][c]);
-      }
-    }
-    float* pp = P2 + p * T::P2P;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if constexpr (C >= 4) {
-#pragma unroll
-        for (int q = 0; q < C / 4; ++q) {
-          const int n = q * (NC * 4 / C) + 4 * cg;    // 4 consecutive columns, same j2
-          const int j2 = n / R, b = n - j2 * R;
-          *reinterpret_cast<float4*>(pp + (i * T::kN2 + j2) * T::P2S + b) =
-              make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-          const int n = C * cg + c;
-          const int j2 = n / R, b = n - j2 * R;
-          pp[(i * T::kN2 + j2) * T::P2S + b] = acc[i][c];
-        }
-      }
-    }
-  }
-}
-
 template <int N2, int R, int CP>
 __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_tiled(FwdArgs a) {
   using T = TileCfg<N2, R, CP>;
@@ -196,27 +102,9 @@ __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_til
     const int p0 = a.w.row_pair[x0], p1 = a.w.row_pair[x1 - 1];
     const int np = p1 - p0 + 1;
     const int i2 = a.w.pair_i2[p0];
-    {
-      const float4* g2 = reinterpret_cast<const float4*>(a.G2 + (size_t)i2 * T::F_G2);
-      float4* d = reinterpret_cast<float4*>(G2s);
-#pragma unroll 4
-      for (int e = tid; e < T::F_G2 / 4; e += 256) d[e] = __ldg(g2 + e);
-    }
-    for (int e = tid; e < np * R * 4; e += 256) {
-      const int p = e / (R * 4), rem = e - p * (R * 4);
-      const int j1 = rem / R, k = rem - j1 * R;         // coalesced read of G1[i1][0][j1][k]
-      P1t[p * (R * 4) + k * 4 + j1] = __ldg(a.G1 + (size_t)a.w.pair_i1[p0 + p] * (R * 4) + rem);
-    }
+    tiled_load_g2_p1<T>(a.G1, a.G2, a.w.pair_i1, i2, p0, np, G2s, P1t);
     __syncthreads();
-    // stage 2: C = columns per thread, so that np * NC / C ~ 256 items
-    {
-      const int need = (np * T::NC + 255) / 256;
-      if (need <= 1) tiled_stage2<T, 1>(G2s, P1t, P2, np);
-      else if (need <= 2) tiled_stage2<T, 2>(G2s, P1t, P2, np);
-      else if (need <= 4) tiled_stage2<T, 4>(G2s, P1t, P2, np);
-      else if (need <= 8) tiled_stage2<T, 8>(G2s, P1t, P2, np);
-      else tiled_stage2<T, 16>(G2s, P1t, P2, np);
-    }
+    tiled_stage2_any<T>(G2s, P1t, P2, np);
     // stage 3 in batches of RB rows
     const int blk = warp % T::NB, rgrp = warp / T::NB;
     for (int xb = x0; xb < x1; xb += T::RB) {
@@ -335,8 +223,6 @@ static FwdKind fwd_kind(const Shape& s) {
   if (s.n2 == 4 && s.R1 == 16) return kFwdTiled_4_16;
   return kFwdGeneric;
 }
-
-constexpr int kCP_8_32 = 12, kCP_8_64 = 4, kCP_4_16 = 16;
 
 int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chunk) {
   const int64_t g2n = (int64_t)s.R1 * s.n2 * s.R2;

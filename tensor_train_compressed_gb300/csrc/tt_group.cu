@@ -4,8 +4,8 @@
 // share high-order TT-core indices so that every shared partial product is
 // formed once.  Here that grouping is:
 //
-//   1. k_prepare   index decomposition + range check, bag of each lookup,
-//                  offsets check, digit histograms of the grouping key
+//   1. k_prepare   index decomposition + range check, offsets check, digit
+//                  histograms of the grouping key
 //   2. k_scatter   one LSD radix pass per 8-bit digit (onesweep style:
 //                  tiles ranked in shared memory, tile prefixes chained by
 //                  decoupled look-back), sorting (key << 32 | position)
@@ -59,14 +59,6 @@ __global__ void __launch_bounds__(256) k_prepare(PrepArgs a) {
       const int64_t r = a.indices[l];
       if (r >= 0 && r < a.s.M) key = group_key(r, a.s);
       else bad_index = true;
-      // bag of lookup l: the largest b with offsets[b] <= l (clamped to [0, B-1])
-      int64_t lo = 0, hi = a.B - 1;
-      while (lo < hi) {
-        const int64_t mid = (lo + hi + 1) >> 1;
-        if (a.offsets[mid] <= l) lo = mid;
-        else hi = mid - 1;
-      }
-      a.w.bag_of[l] = (int32_t)lo;
     }
     for (int p = 0; p < a.passes; ++p) {
       const uint32_t d = live ? ((key >> (kRadixBits * p)) & (kRadix - 1)) : 0xffffffffu;

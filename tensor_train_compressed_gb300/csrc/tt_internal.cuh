@@ -181,8 +181,8 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
 int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chunk);
 // backward (tt_bwd.cu)
 int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out,
-                    const float* const cores[3], int64_t nnz, int64_t num_bags,
-                    float* const core_grads[3], cudaStream_t st);
+                    const float* const cores[3], const int64_t* offsets, int64_t nnz,
+                    int64_t num_bags, float* const core_grads[3], cudaStream_t st);
 int launch_sgd(float* const cores[3], const float* const grads[3], const Shape& s, float lr,
                cudaStream_t st);
 

@@ -52,6 +52,9 @@ def _gpu_backward(x, st):
                         grads, st["ws"], reuse_grouping=True)
     rc, bits = tte.tt_emb_get_error(st["ws"])
     assert rc == tte.TT_EMB_OK, bits
+    # the backward writes the bag of every lookup into the workspace
+    g = tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, st["ws"])
+    assert np.array_equal(g["bag_of"], np.repeat(np.arange(x.num_bags), np.diff(x.offsets)))
     return [g.cpu().numpy() for g in grads]
 
 
@@ -75,9 +78,6 @@ def _check_grouping(x, ws):
     rows = (g["pair_i1"][g["row_pair"]].astype(np.int64) * m2 + g["pair_i2"][g["row_pair"]]) * m3 \
         + g["row_i3"]
     assert np.array_equal(rows, ref["row_index"])
-    # bag of every lookup
-    lens = np.diff(x.offsets)
-    assert np.array_equal(g["bag_of"], np.repeat(np.arange(x.num_bags), lens))
     # chunks partition the unique rows, each chunk's prefixes share one i2
     cs = g["chunk_start"]
     assert cs[0] == 0 and cs[-1] == g["U_r"] and np.all(np.diff(cs) > 0)
