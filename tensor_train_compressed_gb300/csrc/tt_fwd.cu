@@ -156,53 +156,54 @@ __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_til
   }
 }
 
-// out[b] = sum of the unique rows of bag b's lookups; one warp per bag.
+// out[b] = sum of the unique rows of bag b's lookups; one warp per bag.  The
+// lanes fetch up to 32 of the bag's unique-row ids at once; each lane then sums
+// its float4 column of those rows with 8 loads in flight.
 __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offsets, int64_t B,
                                               int64_t nnz, const int32_t* __restrict__ uid,
                                               const float* __restrict__ rowbuf, int D,
                                               float* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const bool vec = (D & 3) == 0;
+  const int cols = vec ? (D >> 2) : D;
+  const int cols_pad = cols + ((32 - cols % 32) % 32);   // uniform trip count for the shuffles
+  const float4* rb4 = reinterpret_cast<const float4*>(rowbuf);
   for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < B; b += warps) {
     int64_t l0 = offsets[b], l1 = offsets[b + 1];
     l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
     l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
-    if ((D & 3) == 0) {
-      const int D4 = D >> 2;
-      const float4* rb = reinterpret_cast<const float4*>(rowbuf);
-      float4* o = reinterpret_cast<float4*>(out + b * (int64_t)D);
-      for (int c = lane; c < D4; c += 32) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        int64_t l = l0;
-        for (; l + 4 <= l1; l += 4) {
-          const int u0 = uid[l], u1 = uid[l + 1], u2 = uid[l + 2], u3 = uid[l + 3];
-          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-          const float4 v0 = u0 >= 0 ? rb[(int64_t)u0 * D4 + c] : z;
-          const float4 v1 = u1 >= 0 ? rb[(int64_t)u1 * D4 + c] : z;
-          const float4 v2 = u2 >= 0 ? rb[(int64_t)u2 * D4 + c] : z;
-          const float4 v3 = u3 >= 0 ? rb[(int64_t)u3 * D4 + c] : z;
-          acc.x += v0.x; acc.y += v0.y; acc.z += v0.z; acc.w += v0.w;
-          acc.x += v1.x; acc.y += v1.y; acc.z += v1.z; acc.w += v1.w;
-          acc.x += v2.x; acc.y += v2.y; acc.z += v2.z; acc.w += v2.w;
-          acc.x += v3.x; acc.y += v3.y; acc.z += v3.z; acc.w += v3.w;
-        }
-        for (; l < l1; ++l) {
-          const int u = uid[l];
-          if (u >= 0) {
-            const float4 v = rb[(int64_t)u * D4 + c];
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    for (int c = lane; c < cols_pad; c += 32) {
+      const bool live = c < cols;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float accs = 0.f;
+      for (int64_t lb = l0; lb < l1; lb += 32) {
+        const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
+        const int32_t my_u = lane < cnt ? uid[lb + lane] : -1;
+        for (int j0 = 0; j0 < cnt; j0 += 8) {
+          float4 v[8];
+          float vs[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int32_t u = __shfl_sync(0xffffffffu, my_u, (j0 + t) & 31);
+            const bool use = live && (j0 + t) < cnt && u >= 0;
+            v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+            vs[t] = 0.f;
+            if (use) {
+              if (vec) v[t] = rb4[(int64_t)u * cols + c];
+              else vs[t] = rowbuf[(int64_t)u * D + c];
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            acc.x += v[t].x; acc.y += v[t].y; acc.z += v[t].z; acc.w += v[t].w;
+            accs += vs[t];
           }
         }
-        o[c] = acc;
       }
-    } else {
-      for (int j = lane; j < D; j += 32) {
-        float acc = 0.f;
-        for (int64_t l = l0; l < l1; ++l) {
-          const int u = uid[l];
-          if (u >= 0) acc += rowbuf[(int64_t)u * D + j];
-        }
-        out[b * (int64_t)D + j] = acc;
+      if (live) {
+        if (vec) reinterpret_cast<float4*>(out + b * (int64_t)D)[c] = acc;
+        else out[b * (int64_t)D + c] = accs;
       }
     }
   }

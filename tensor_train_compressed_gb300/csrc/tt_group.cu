@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kScanThreads) k_segment(SegArgs a) {
   const uint32_t tile = tile_sh;
   const int64_t k0 = (int64_t)tile * kScanTile + (int64_t)tid * kScanItems;
   const uint64_t M = (uint64_t)a.s.M;
-  const uint64_t m3 = (uint64_t)a.s.m3;
+  const uint32_t m3 = (uint32_t)a.s.m3;
 
   uint64_t w[kScanItems];
   uint32_t rflag = 0, pflag = 0;
@@ -233,42 +233,17 @@ __global__ void __launch_bounds__(kScanThreads) k_segment(SegArgs a) {
       const uint64_t pk = prev >> 32;
       const bool first = (k == 0);
       if (first || key != pk) rflag |= 1u << i;
-      if (first || key / m3 != pk / m3) pflag |= 1u << i;
+      if (first || (uint32_t)key / m3 != (uint32_t)pk / m3) pflag |= 1u << i;
     }
     prev = wv;
   }
   const uint32_t cnt = (uint32_t)__popc(rflag) | ((uint32_t)__popc(pflag) << 16);
   uint32_t tot;
   const uint32_t excl = block_exclusive_scan_256(cnt, &tot, scan8);
-  if (tid == 0) {
-    const unsigned long long agg_r = tot & 0xffffu, agg_p = tot >> 16;
-    unsigned long long* st = a.w.seg_status;
-    const unsigned long long kF1 = 1ull << 62, kF2 = 2ull << 62, kM31 = (1ull << 31) - 1;
-    unsigned long long er = 0, ep = 0;
-    if (tile == 0) {
-      st_relaxed_u64(st, kF2 | (agg_r << 31) | agg_p);
-    } else {
-      st_relaxed_u64(st + tile, kF1 | (agg_r << 31) | agg_p);
-      int64_t j = (int64_t)tile - 1;
-      long long spins = 0;
-      while (j >= 0) {
-        const unsigned long long v = ld_relaxed_u64(st + j);
-        const unsigned long long f = v >> 62;
-        if (f == 0) {
-          if (++spins > kSpinCap) {
-            set_status(a.w.ctl, kStTimeout);
-            break;
-          }
-          continue;
-        }
-        er += (v >> 31) & kM31;
-        ep += v & kM31;
-        if (f == 2) break;
-        --j;
-      }
-      st_relaxed_u64(st + tile, kF2 | (((er + agg_r) & kM31) << 31) | ((ep + agg_p) & kM31));
-    }
-    prefix_sh = (er << 31) | ep;
+  if (tid < 32) {
+    const unsigned long long agg = ((unsigned long long)(tot & 0xffffu) << 31) | (tot >> 16);
+    const unsigned long long e = warp_lookback<unsigned long long>(a.w.seg_status, tile, agg, a.w.ctl);
+    if (tid == 0) prefix_sh = e;
   }
   __syncthreads();
   int32_t rr = (int32_t)((prefix_sh >> 31) & ((1ull << 31) - 1)) + (int32_t)(excl & 0xffffu);
@@ -292,16 +267,17 @@ __global__ void __launch_bounds__(kScanThreads) k_segment(SegArgs a) {
       }
       continue;
     }
+    const uint32_t q = (uint32_t)key / m3;
     if (pflag & (1u << i)) {
-      const uint64_t q = key / m3;
+      const uint32_t q2 = q / (uint32_t)a.s.m1;
       a.w.pair_row_start[pp] = rr;
-      a.w.pair_i1[pp] = (int32_t)(q % (uint64_t)a.s.m1);
-      a.w.pair_i2[pp] = (int32_t)(q / (uint64_t)a.s.m1);
+      a.w.pair_i1[pp] = (int32_t)(q - q2 * (uint32_t)a.s.m1);
+      a.w.pair_i2[pp] = (int32_t)q2;
       ++pp;
     }
     if (rflag & (1u << i)) {
       a.w.row_start[rr] = (int32_t)k;
-      a.w.row_i3[rr] = (int32_t)(key % m3);
+      a.w.row_i3[rr] = (int32_t)((uint32_t)key - q * m3);
       a.w.row_pair[rr] = pp - 1;
       ++rr;
     }
@@ -360,32 +336,9 @@ __global__ void __launch_bounds__(kScanThreads) k_chunks(ChunkArgs a) {
   }
   uint32_t tot;
   const uint32_t excl = block_exclusive_scan_256((uint32_t)__popc(flags), &tot, scan8);
-  if (tid == 0) {
-    uint32_t* st = a.w.chunk_status;
-    uint32_t e = 0;
-    if (tile == 0) {
-      st_relaxed_u32(st, kFlagIncl | tot);
-    } else {
-      st_relaxed_u32(st + tile, kFlagAgg | tot);
-      int64_t j = (int64_t)tile - 1;
-      long long spins = 0;
-      while (j >= 0) {
-        const uint32_t v = ld_relaxed_u32(st + j);
-        const uint32_t f = v & kFlagMask;
-        if (f == 0) {
-          if (++spins > kSpinCap) {
-            set_status(a.w.ctl, kStTimeout);
-            break;
-          }
-          continue;
-        }
-        e += v & kValMask;
-        if (f == kFlagIncl) break;
-        --j;
-      }
-      st_relaxed_u32(st + tile, kFlagIncl | ((e + tot) & kValMask));
-    }
-    prefix_sh = e;
+  if (tid < 32) {
+    const uint32_t e = warp_lookback<uint32_t>(a.w.chunk_status, tile, tot, a.w.ctl);
+    if (tid == 0) prefix_sh = e;
   }
   __syncthreads();
   int32_t c = (int32_t)(prefix_sh + excl);

@@ -117,14 +117,75 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 
 __device__ __forceinline__ void set_status(Ctl* ctl, uint32_t bit) { atomicOr(&ctl->status, bit); }
 
-// Grouping key of a row index: (i2, i1, i3) with i3 least significant, so that
-// unique (i1, i2) prefixes come out grouped by the G2 slice they read.
+// Grouping key of an in-range row index (r < M <= 2^32 - 2, so 32-bit
+// arithmetic is exact): (i2, i1, i3) with i3 least significant, so that unique
+// (i1, i2) prefixes come out grouped by the G2 slice they read.
 __device__ __forceinline__ uint32_t group_key(int64_t r, const Shape& s) {
-  int64_t i3 = r % s.m3;
-  int64_t q = r / s.m3;
-  int64_t i2 = q % s.m2;
-  int64_t i1 = q / s.m2;
-  return (uint32_t)((i2 * s.m1 + i1) * s.m3 + i3);
+  const uint32_t ru = (uint32_t)r, m1 = (uint32_t)s.m1, m2 = (uint32_t)s.m2, m3 = (uint32_t)s.m3;
+  const uint32_t q = ru / m3, i3 = ru - q * m3;
+  const uint32_t i1 = q / m2, i2 = q - i1 * m2;
+  return (i2 * m1 + i1) * m3 + i3;
+}
+
+// Decoupled look-back over the tiles before `tile`, done by one whole warp:
+// the lanes read 32 predecessor words at once, so the walk costs one round
+// trip per 32 tiles.  Words hold a 2-bit flag in the top bits (1 = tile
+// aggregate, 2 = inclusive prefix) and an additive value below; `agg` is this
+// tile's own aggregate, published first.  Returns the exclusive prefix; after
+// kSpinCap polls of a window with an unpublished tile it sets the timeout bit
+// and returns what it has.  Called by all 32 lanes of one warp.
+template <typename W>
+__device__ __forceinline__ W warp_lookback(W* st, uint32_t tile, W agg, Ctl* ctl) {
+  constexpr int kTop = sizeof(W) * 8 - 2;
+  const W kAgg = (W)1 << kTop, kIncl = (W)2 << kTop, kVal = ((W)1 << kTop) - 1;
+  const int lane = threadIdx.x & 31;
+  if (tile == 0) {
+    if (lane == 0) {
+      if constexpr (sizeof(W) == 8) st_relaxed_u64((unsigned long long*)st, kIncl | agg);
+      else st_relaxed_u32((uint32_t*)st, kIncl | agg);
+    }
+    return 0;
+  }
+  if (lane == 0) {
+    if constexpr (sizeof(W) == 8) st_relaxed_u64((unsigned long long*)(st + tile), kAgg | agg);
+    else st_relaxed_u32((uint32_t*)(st + tile), kAgg | agg);
+  }
+  W excl = 0;
+  int64_t top = (int64_t)tile - 1;
+  long long spins = 0;
+  while (top >= 0) {
+    const int64_t j = top - lane;
+    W v = kIncl;                       // before tile 0: an inclusive prefix of 0
+    if (j >= 0) {
+      if constexpr (sizeof(W) == 8) v = (W)ld_relaxed_u64((const unsigned long long*)(st + j));
+      else v = (W)ld_relaxed_u32((const uint32_t*)(st + j));
+    }
+    const W f = v >> kTop;
+    const uint32_t incl = __ballot_sync(0xffffffffu, f == 2);
+    const uint32_t none = __ballot_sync(0xffffffffu, f == 0);
+    const int first = incl ? __ffs(incl) - 1 : 31;
+    const uint32_t needed = first == 31 ? 0xffffffffu : ((2u << first) - 1u);
+    if (none & needed) {
+      if (++spins > kSpinCap) {
+        if (lane == 0) set_status(ctl, kStTimeout);
+        break;
+      }
+      continue;
+    }
+    W part = lane <= first ? (v & kVal) : (W)0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    excl += part;
+    if (incl) break;
+    top -= 32;
+  }
+  if (lane == 0) {
+    if constexpr (sizeof(W) == 8)
+      st_relaxed_u64((unsigned long long*)(st + tile), kIncl | ((excl + agg) & kVal));
+    else
+      st_relaxed_u32((uint32_t*)(st + tile), kIncl | ((excl + agg) & kVal));
+  }
+  return excl;
 }
 
 // Block-wide exclusive scan of one uint32 per thread (blockDim = 256).
