@@ -239,7 +239,10 @@ def run_ours(args, rank, world, dist):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
     result = {}
-    for name, cfg, train in (("train", TRAIN_CFG, True), ("forward", FWD_CFG, False)):
+    todo = (("train", TRAIN_CFG, True), ("forward", FWD_CFG, False))
+    if args.only:
+        todo = tuple(t for t in todo if t[0] == args.only)
+    for name, cfg, train in todo:
         wl = Workload(cfg, train, torch, tte, stream)
         with torch.cuda.stream(stream):
             for _ in range(2):          # eager warm-up (also settles the library's caches)
@@ -276,6 +279,16 @@ def run_ours(args, rank, world, dist):
         ms = float(np.mean(times))
         result[name] = dict(wl=wl, alg=alg, ms=ms, times=times, wall=wall, clocks=clk,
                             kern=kern, n_launch=n_launch, n_valid=nv)
+
+    if args.only:
+        # single-workload run (profiling driver): a short report, no e2e / baseline
+        r = result[args.only]
+        ms = rank_max(dist, r["ms"])
+        if rank == 0:
+            return {"only": args.only, "ms_per_step": round(ms, 5),
+                    "lookups_per_s": round(weak_throughput(r["wl"].x.nnz, world, ms), 1),
+                    "kernels": {k: round(v[0] / max(1, v[1]), 5) for k, v in r["kern"].items()}}
+        return None
 
     # ---- end to end through the public API from pinned host buffers (training step)
     wl = result["train"]["wl"]
@@ -503,6 +516,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["train", "forward"], default=None,
+                    help="time one workload only (short report; used to drive ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
