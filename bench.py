@@ -76,7 +76,14 @@ def algorithmic(x, U_12: int, U_r: int) -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    """SM clock and clock-event reasons sampled while the timed region runs.
+
+    Reads NVML through ctypes (read-only queries, ~1 ms polling, so even a
+    timed region of a few ms gets samples); falls back to `nvidia-smi -lms 200`.
+    """
+    # clocks-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -85,8 +92,44 @@ class ClockSampler:
         self.gpu = gpu
         self.proc = None
         self.lines = []
+        self.samples = []
+        self.max_mhz = None
+        self.nvml = None
+        self._stop = threading.Event()
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if not self.gpu.startswith("GPU-") or \
+                lib.nvmlDeviceGetHandleByUUID(self.gpu.encode(), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        self.nvml, self.h, self.ct = lib, h, ctypes
+        mx = ctypes.c_uint(0)
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+
+    def _poll(self):
+        ct, lib, h = self.ct, self.nvml, self.h
+        mhz, rs = ct.c_uint(0), ct.c_ulonglong(0)
+        get_r = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0 and \
+                    get_r(h, ct.byref(rs)) == 0:
+                self.samples.append((float(mhz.value), int(rs.value)))
+            time.sleep(0.001)
 
     def start(self):
+        try:
+            self._nvml_open()
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return
+        except (OSError, AttributeError):
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.Q}",
@@ -102,8 +145,16 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self) -> dict:
+        if self.nvml is not None:
+            self._stop.set()
+            self.t.join(timeout=2)
+            sm = [m for m, _ in self.samples]
+            reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items()
+                              if r & bit})
+            return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "samples": len(sm), "reasons": reasons, "source": "nvml"}
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -125,22 +176,7 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": float(np.median(sm)) if sm else None,
                 "sm_max_mhz": float(max(smax)) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
-
-
-def rank_max(dist, v: float) -> float:
-    """Max of a per-rank time over all ranks (the slowest replica sets the step time)."""
-    if dist is None:
-        return float(v)
-    import torch
-    t = torch.tensor([float(v)], dtype=torch.float64)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def weak_throughput(units_per_rank: int, world: int, ms_max: float) -> float:
-    """Whole-job units/s: every rank processes its own batch in the max-over-ranks time."""
-    return units_per_rank * world / (ms_max * 1e-3)
+                "samples": len(sm), "reasons": sorted(reasons), "source": "nvidia-smi"}
 
 
 # ----------------------------------------------------------------------------- GPU arm

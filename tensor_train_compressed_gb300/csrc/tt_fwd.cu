@@ -156,6 +156,163 @@ __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_til
   }
 }
 
+// ---------------------------------------------------------------------------
+// Warp-specialised chunk kernel (n1 = n3 = 4, R1 = R2 = R, G2 slice small enough
+// to double-buffer).  Warp 8 is a producer: it claims the next chunk, writes the
+// chunk's metadata and issues bulk copies (TMA, 1-D) of the G2 slice, the G1
+// rows and up to ROWMAX G3 rows into the free one of two stage buffers,
+// completing on that buffer's "full" mbarrier.  Warps 0-7 consume: stage 2
+// (P2 in shared memory), stage 3 (rows), then release the buffer through its
+// "empty" mbarrier.  Staging of chunk i+1 thus overlaps the math of chunk i.
+template <int N2, int R, int CP>
+struct WsCfg {
+  using T = TileCfg<N2, R, CP>;
+  static constexpr int ROWMAX = 64;
+  static constexpr int F_P1 = CP * 4 * R;            // G1 rows, natural [p][j1][a]
+  static constexpr int F_G3 = ROWMAX * T::G3S;
+  static constexpr int STAGE_F = T::F_G2 + F_P1 + F_G3;
+  struct Meta {
+    int x0, x1, p0, np, end, pad[3];
+    int rp[ROWMAX];                                   // prefix (chunk-local) of each staged row
+  };
+  static constexpr int SMEM = 4 * (2 * STAGE_F + T::F_P2) + 2 * (int)sizeof(Meta) + 4 * 8;
+  static_assert(T::NB == 8, "one compute warp per j12 block");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+template <class T, bool kGlobalG3>
+__device__ __forceinline__ void row_dot(const float* __restrict__ pp,
+                                        const float* __restrict__ gg, float acc[4][4]) {
+  constexpr int R = T::kR;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 2
+  for (int b = 0; b < R; b += 4) {
+    float4 pv[4], gv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pv[i] = *reinterpret_cast<const float4*>(pp + i * T::P2S + b);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if constexpr (kGlobalG3) gv[t] = __ldg(reinterpret_cast<const float4*>(gg + (b + t) * 4));
+      else gv[t] = *reinterpret_cast<const float4*>(gg + (b + t) * 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float pw[4] = {pv[i].x, pv[i].y, pv[i].z, pv[i].w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        acc[i][0] = fmaf(pw[t], gv[t].x, acc[i][0]);
+        acc[i][1] = fmaf(pw[t], gv[t].y, acc[i][1]);
+        acc[i][2] = fmaf(pw[t], gv[t].z, acc[i][2]);
+        acc[i][3] = fmaf(pw[t], gv[t].w, acc[i][3]);
+      }
+    }
+  }
+}
+
+template <int N2, int R, int CP>
+__global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
+  using W = WsCfg<N2, R, CP>;
+  using T = typename W::T;
+  using Meta = typename W::Meta;
+  extern __shared__ float4 sm4[];
+  float* base = reinterpret_cast<float*>(sm4);
+  float* P2 = base + 2 * W::STAGE_F;
+  Meta* meta = reinterpret_cast<Meta*>(P2 + T::F_P2);
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
+  uint64_t* empty = full + 2;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(&empty[0], 1);
+    mbar_init(&empty[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const int n_chunks = a.w.ctl->n_chunks;
+
+  if (warp == 8) {
+    // ---------------- producer
+    for (int it = 0;; ++it) {
+      const int s = it & 1;
+      const uint32_t use = (uint32_t)it >> 1;
+      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
+      int c = 0;
+      if (lane == 0) c = (int)atomicAdd(&a.w.ctl->fwd_chunk_ctr, 1u);
+      c = __shfl_sync(0xffffffffu, c, 0);
+      Meta& m = meta[s];
+      if (c >= n_chunks) {
+        if (lane == 0) {
+          m.end = 1;
+          mbar_arrive(&full[s]);
+        }
+        break;
+      }
+      const int x0 = a.w.chunk_start[c], x1 = a.w.chunk_start[c + 1];
+      const int p0 = a.w.row_pair[x0];
+      const int np = a.w.row_pair[x1 - 1] - p0 + 1;
+      const int i2 = a.w.pair_i2[p0];
+      const int nst = min(x1 - x0, W::ROWMAX);
+      float* G2s = base + s * W::STAGE_F;
+      float* P1n = G2s + T::F_G2;
+      float* G3s = P1n + W::F_P1;
+      for (int r = lane; r < nst; r += 32) m.rp[r] = a.w.row_pair[x0 + r] - p0;
+      __syncwarp();
+      if (lane == 0) {
+        m.x0 = x0;
+        m.x1 = x1;
+        m.p0 = p0;
+        m.np = np;
+        m.end = 0;
+        const uint32_t bytes = 4u * (T::F_G2 + np * 4 * R + nst * 4 * R);
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_g2s(G2s, a.G2 + (size_t)i2 * T::F_G2, 4u * T::F_G2, &full[s]);
+      }
+      __syncwarp();
+      for (int p = lane; p < np; p += 32)
+        bulk_g2s(P1n + p * 4 * R, a.G1 + (size_t)a.w.pair_i1[p0 + p] * 4 * R, 16u * R, &full[s]);
+      for (int r = lane; r < nst; r += 32)
+        bulk_g2s(G3s + r * T::G3S, a.G3 + (size_t)a.w.row_i3[x0 + r] * 4 * R, 16u * R, &full[s]);
+    }
+    return;
+  }
+
+  // ---------------- consumers (warps 0-7)
+  for (int it = 0;; ++it) {
+    const int s = it & 1;
+    if (!mbar_wait(&full[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
+    const Meta& m = meta[s];
+    if (m.end) break;
+    const int x0 = m.x0, x1 = m.x1, p0 = m.p0, np = m.np;
+    const float* G2s = base + s * W::STAGE_F;
+    const float* P1n = G2s + T::F_G2;
+    const float* G3s = P1n + W::F_P1;
+    stage2_natural<T>(G2s, P1n, P2, np);
+    named_sync(1, 256);
+    const int rows = x1 - x0;
+    const int blk = warp;
+    for (int r = lane; r < rows; r += 32) {
+      const int x = x0 + r;
+      float acc[4][4];
+      if (r < W::ROWMAX) {
+        const float* pp = P2 + m.rp[r] * T::P2P + (blk * 4) * T::P2S;
+        row_dot<T, false>(pp, G3s + r * T::G3S, acc);
+      } else {
+        const float* pp = P2 + (a.w.row_pair[x] - p0) * T::P2P + (blk * 4) * T::P2S;
+        row_dot<T, true>(pp, a.G3 + (size_t)a.w.row_i3[x] * 4 * R, acc);
+      }
+      float4* o = reinterpret_cast<float4*>(a.w.rowbuf + (size_t)x * T::D + blk * 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    }
+    named_sync(1, 256);
+    if (tid == 0) mbar_arrive(&empty[s]);
+  }
+}
+
 // out[b] = sum of the unique rows of bag b's lookups; one warp per bag.  The
 // lanes fetch up to 32 of the bag's unique-row ids at once; each lane then sums
 // its float4 column of those rows with 8 loads in flight.
@@ -252,6 +409,18 @@ static int persistent_grid(const void* fn, int threads, size_t smem) {
 }
 
 template <int N2, int R, int CP>
+static void launch_ws(const FwdArgs& fa, cudaStream_t st) {
+  using W = WsCfg<N2, R, CP>;
+  static int grid = 0;
+  if (grid == 0) {
+    cudaFuncSetAttribute(k_fwd_ws<N2, R, CP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         W::SMEM);
+    grid = persistent_grid((const void*)k_fwd_ws<N2, R, CP>, 288, W::SMEM);
+  }
+  TT_TIMED("k_fwd_ws", st, (k_fwd_ws<N2, R, CP><<<grid, 288, W::SMEM, st>>>(fa)));
+}
+
+template <int N2, int R, int CP>
 static void launch_tiled(const FwdArgs& fa, cudaStream_t st) {
   using T = TileCfg<N2, R, CP>;
   static int grid = 0;
@@ -277,7 +446,7 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
   fa.G2 = cores[1];
   fa.G3 = cores[2];
   switch (fwd_kind(s)) {
-    case kFwdTiled_8_32: launch_tiled<8, 32, kCP_8_32>(fa, st); break;
+    case kFwdTiled_8_32: launch_ws<8, 32, kCP_8_32>(fa, st); break;
     case kFwdTiled_8_64: launch_tiled<8, 64, kCP_8_64>(fa, st); break;
     case kFwdTiled_4_16: launch_tiled<4, 16, kCP_4_16>(fa, st); break;
     default: {

@@ -136,4 +136,171 @@ __device__ __forceinline__ void tiled_load_g2_p1(const float* __restrict__ G1,
   }
 }
 
+// ---------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA, 1-D) helpers.  Every wait is capped: after
+// kWaitCap polls it sets the timeout bit and gives up.
+constexpr long long kWaitCap = 1ll << 24;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Ctl* ctl) {
+  for (long long i = 0; i < kWaitCap; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  set_status(ctl, kStTimeout);
+  return false;
+}
+// global -> shared bulk copy completing on `bar` (16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Stage 2 for chunks of one or two prefixes, from G1 rows in their natural
+// [j1][a] layout: the R-long reduction is split over KQ lanes (8/16 lanes
+// apart, so the 128-bit G2 loads of a phase stay conflict-free) and summed by
+// shuffles.  KQ = 4 for one prefix, 2 for two: 256 threads either way.
+template <class T, int KQ>
+__device__ __forceinline__ void tiled_stage2_splitk(const float* __restrict__ G2s,
+                                                    const float* __restrict__ P1n,
+                                                    float* __restrict__ P2, int np, int nthreads) {
+  constexpr int R = T::kR, NC = T::NC, CPW = 32 / KQ;   // column groups per warp
+  constexpr int KS = R / KQ;
+  const int lane = threadIdx.x & 31;
+  const int kq = lane / CPW, cgl = lane - kq * CPW;
+  const int total = np * (NC / 4) * KQ;
+  for (int base = 0; base < total; base += nthreads) {
+    const int wi = (base + threadIdx.x) >> 5;          // warp-item
+    const int cgall = wi * CPW + cgl;                   // over all prefixes
+    const bool valid = base + (int)threadIdx.x < total;
+    const int p = cgall / (NC / 4), cg = cgall - p * (NC / 4);
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    if (valid) {
+      const float* ap = P1n + p * (4 * R);
+#pragma unroll 4
+      for (int k = kq * KS; k < (kq + 1) * KS; ++k) {
+        const float4 bv = *reinterpret_cast<const float4*>(G2s + k * NC + 4 * cg);
+        const float a0 = ap[k], a1 = ap[R + k], a2 = ap[2 * R + k], a3 = ap[3 * R + k];
+        acc[0][0] = fmaf(a0, bv.x, acc[0][0]); acc[0][1] = fmaf(a0, bv.y, acc[0][1]);
+        acc[0][2] = fmaf(a0, bv.z, acc[0][2]); acc[0][3] = fmaf(a0, bv.w, acc[0][3]);
+        acc[1][0] = fmaf(a1, bv.x, acc[1][0]); acc[1][1] = fmaf(a1, bv.y, acc[1][1]);
+        acc[1][2] = fmaf(a1, bv.z, acc[1][2]); acc[1][3] = fmaf(a1, bv.w, acc[1][3]);
+        acc[2][0] = fmaf(a2, bv.x, acc[2][0]); acc[2][1] = fmaf(a2, bv.y, acc[2][1]);
+        acc[2][2] = fmaf(a2, bv.z, acc[2][2]); acc[2][3] = fmaf(a2, bv.w, acc[2][3]);
+        acc[3][0] = fmaf(a3, bv.x, acc[3][0]); acc[3][1] = fmaf(a3, bv.y, acc[3][1]);
+        acc[3][2] = fmaf(a3, bv.z, acc[3][2]); acc[3][3] = fmaf(a3, bv.w, acc[3][3]);
+      }
+    }
+#pragma unroll
+    for (int o = CPW; o < 32; o <<= 1)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], o);
+    if (valid && kq == 0) {
+      const int n = 4 * cg, j2 = n / R, b = n - j2 * R;
+      float* pp = P2 + p * T::P2P + j2 * T::P2S + b;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(pp + i * T::kN2 * T::P2S) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    }
+  }
+}
+
+// Stage 2 for np >= 3 prefixes from G1 rows in their natural [j1][a] layout:
+// 4 j1 rows x C columns per thread (as tiled_stage2, A read with scalar loads).
+template <class T, int C>
+__device__ __forceinline__ void tiled_stage2_n(const float* __restrict__ G2s,
+                                               const float* __restrict__ P1n,
+                                               float* __restrict__ P2, int np, int nthreads) {
+  constexpr int R = T::kR, NC = T::NC, G = NC / C;
+  static_assert(C >= 4, "column groups of 4");
+  for (int item = threadIdx.x; item < np * G; item += nthreads) {
+    const int p = item / G, cg = item - p * G;
+    float acc[4][C];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < C; ++c) acc[i][c] = 0.f;
+    const float* ap = P1n + p * (4 * R);
+#pragma unroll 4
+    for (int k = 0; k < R; ++k) {
+      const float a0 = ap[k], a1 = ap[R + k], a2 = ap[2 * R + k], a3 = ap[3 * R + k];
+      const float* brow = G2s + k * NC;
+      float bv[C];
+#pragma unroll
+      for (int q = 0; q < C / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(brow + q * (NC * 4 / C) + 4 * cg);
+        bv[4 * q] = v.x; bv[4 * q + 1] = v.y; bv[4 * q + 2] = v.z; bv[4 * q + 3] = v.w;
+      }
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        acc[0][c] = fmaf(a0, bv[c], acc[0][c]);
+        acc[1][c] = fmaf(a1, bv[c], acc[1][c]);
+        acc[2][c] = fmaf(a2, bv[c], acc[2][c]);
+        acc[3][c] = fmaf(a3, bv[c], acc[3][c]);
+      }
+    }
+    float* pp = P2 + p * T::P2P;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int q = 0; q < C / 4; ++q) {
+        const int n = q * (NC * 4 / C) + 4 * cg;
+        const int j2 = n / R, b = n - j2 * R;
+        *reinterpret_cast<float4*>(pp + (i * T::kN2 + j2) * T::P2S + b) =
+            make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
+      }
+  }
+}
+
+template <class T>
+__device__ __forceinline__ void stage2_natural(const float* __restrict__ G2s,
+                                               const float* __restrict__ P1n,
+                                               float* __restrict__ P2, int np) {
+  const int need = (np * T::NC + 255) / 256;    // column groups of 4 per thread for ~256 items
+  if (np == 1) tiled_stage2_splitk<T, 4>(G2s, P1n, P2, np, 256);
+  else if (np == 2) tiled_stage2_splitk<T, 2>(G2s, P1n, P2, np, 256);
+  else if (need <= 4) tiled_stage2_n<T, 4>(G2s, P1n, P2, np, 256);
+  else if (need <= 8) tiled_stage2_n<T, 8>(G2s, P1n, P2, np, 256);
+  else tiled_stage2_n<T, 16>(G2s, P1n, P2, np, 256);
+}
+
 }  // namespace tt
