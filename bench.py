@@ -179,6 +179,21 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons), "source": "nvidia-smi"}
 
 
+def rank_max(dist, v: float) -> float:
+    """Max of a per-rank time over all ranks (the slowest replica sets the step time)."""
+    if dist is None:
+        return float(v)
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_throughput(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job units/s: every rank processes its own batch in the max-over-ranks time."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 
