@@ -146,6 +146,34 @@ int tt_emb_profile_start(void);
 int tt_emb_profile_stop(void);
 int tt_emb_profile_read(int i, char* name, int name_len, float* ms);
 
+/* Forward for callers that cannot allocate device memory.  (The paper has no
+ * counterpart of this entry point.)  Some callers cannot call cudaMalloc at
+ * all -- an allocator-less runtime that only hands out input and output
+ * buffers, a plugin whose host framework owns every device allocation, code
+ * that must not allocate once it is in steady state -- and so cannot provide
+ * the workspace tt_emb_forward needs.  This variant computes exactly what
+ * tt_emb_forward computes, with the same arguments minus the workspace: its
+ * scratch is one file-scope device array of TT_EMB_STATIC_WORKSPACE_BYTES
+ * (16 MiB) that every GPU loading this library holds until the process exits.
+ *  - Sizes whose tt_emb_workspace_bytes exceed that capacity return
+ *    TT_EMB_ERR_WORKSPACE before anything is enqueued (about 29k lookups at
+ *    D = 128).
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - Every call shares the one array, which keeps the last call's contents;
+ *    the call clears what must start at zero itself.  Calls whose work
+ *    overlaps on the GPU (other streams or threads) race on the array: the
+ *    caller must serialise them.
+ *  - It allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *    routine.  Argument errors are returned as usual; conditions found by
+ *    the kernels (an index outside [0, M), bad offsets) are handled as in
+ *    tt_emb_forward (the lookup contributes nothing) but their status word
+ *    lives in the shared array and is not reported. */
+#define TT_EMB_STATIC_WORKSPACE_BYTES (16u << 20)
+int tt_emb_forward_static(const float* const cores[3], const int64_t m[3], const int32_t n[3],
+                          const int32_t R[4], const int64_t* indices, int64_t nnz,
+                          const int64_t* offsets, int64_t num_bags, float* out, void* stream);
+
 /* Library version (major*10000 + minor*100 + patch). */
 int tt_emb_version(void);
 

@@ -28,7 +28,8 @@ _NAMES = {v: k for k, v in list(globals().items()) if k.startswith("TT_EMB_")}
 
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
             "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_profile_start",
-            "tt_emb_profile_stop", "tt_emb_profile_read", "tt_emb_version")
+            "tt_emb_profile_stop", "tt_emb_profile_read", "tt_emb_forward_static",
+            "tt_emb_version")
 
 
 class TTEmbError(RuntimeError):
@@ -67,6 +68,7 @@ def lib():
         L.tt_emb_sgd.argtypes = [P, P, P, P, P, ctypes.c_float, P]
         L.tt_emb_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
         L.tt_emb_grouping_view.argtypes = [P, P, P, I64, I64, P, ctypes.POINTER(Grouping)]
+        L.tt_emb_forward_static.argtypes = [P, P, P, P, P, I64, P, I64, P, P]
         L.tt_emb_profile_start.argtypes = []
         L.tt_emb_profile_stop.argtypes = []
         L.tt_emb_profile_read.argtypes = [ctypes.c_int, ctypes.c_char_p, ctypes.c_int,
@@ -163,6 +165,16 @@ def tt_emb_grouping_view(m, n, R, nnz: int, num_bags: int, workspace) -> dict:
                                       _dev(workspace, torch.uint8, "workspace"), ctypes.byref(g)),
            "tt_emb_grouping_view")
     return {name: getattr(g, name) for name, _ in Grouping._fields_}
+
+
+def tt_emb_forward_static(cores, m, n, R, indices, offsets, out, stream=None):
+    """Forward without a workspace argument: the library's own fixed-size device array is used
+    (for callers that cannot allocate; calls must not overlap on the GPU)."""
+    _check(lib().tt_emb_forward_static(_ptrs3(cores, "cores"), *_shape(m, n, R),
+                                       _dev(indices, torch.int64, "indices"), indices.numel(),
+                                       _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
+                                       _dev(out, torch.float32, "out"), _stream(stream)),
+           "tt_emb_forward_static")
 
 
 def tt_emb_profile_start():
