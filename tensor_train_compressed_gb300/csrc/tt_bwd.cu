@@ -60,8 +60,9 @@ __device__ __forceinline__ void s_flush(const WS& w, int32_t u, int64_t k0, int 
 }
 
 // S[x] for every unique row: one warp per slice of kSSlice sorted lookups.  The
-// lanes first fetch the slice's (unique row, bag) pairs in parallel; then the
-// output-gradient rows are summed with several loads in flight.
+// lanes fetch the slice's (unique row, bag) pairs in parallel, 32 at a time; the
+// output-gradient rows are then summed with 8 loads in flight, flushing at every
+// change of unique row.
 __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict__ grad_out,
                                                   int64_t B, int D) {
   const int lane = threadIdx.x & 31;
@@ -69,62 +70,53 @@ __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict_
   const int64_t k0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kSSlice;
   if (k0 >= nv) return;
   const int64_t k1 = k0 + kSSlice < nv ? k0 + kSSlice : nv;
-  int32_t um[kSSlice / 32], bm[kSSlice / 32];
-#pragma unroll
-  for (int h = 0; h < kSSlice / 32; ++h) {
-    const int64_t k = k0 + h * 32 + lane;
-    um[h] = -1;
-    bm[h] = 0;
-    if (k < k1) {
-      const int32_t l = w.perm[k];
-      um[h] = w.uid[l];
-      int32_t b = w.bag_of[l];
-      bm[h] = b < 0 ? 0 : (b >= B ? (int32_t)(B - 1) : b);
-    }
-  }
-  const int n = (int)(k1 - k0);
   const bool vec = (D & 3) == 0;
   const int cols = vec ? (D >> 2) : D;
-  for (int c = lane; c < cols + ((32 - cols % 32) % 32); c += 32) {
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < cols; c0 += 32) {
+    const int c = c0 + lane;
     const bool live = c < cols;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = z4;
     float accs = 0.f;
     int32_t cur = -1;
-    for (int j0 = 0; j0 < n; j0 += 4) {
-      int32_t uj[4], bj[4];
-      float4 g[4];
-      float gs[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int j = j0 + t;
-        const int h = (j >> 5) & (kSSlice / 32 - 1);
-        int32_t us = -1, bs = 0;
-#pragma unroll
-        for (int hh = 0; hh < kSSlice / 32; ++hh) {
-          const int32_t uu = __shfl_sync(0xffffffffu, um[hh], j & 31);
-          const int32_t bb = __shfl_sync(0xffffffffu, bm[hh], j & 31);
-          if (hh == h) { us = uu; bs = bb; }
-        }
-        uj[t] = j < n ? us : -2;
-        bj[t] = bs;
-        g[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-        gs[t] = 0.f;
-        if (live && j < n) {
-          if (vec) g[t] = reinterpret_cast<const float4*>(grad_out + bj[t] * (int64_t)D)[c];
-          else gs[t] = grad_out[bj[t] * (int64_t)D + c];
-        }
+    for (int64_t kb = k0; kb < k1; kb += 32) {
+      const int cnt = (int)(k1 - kb < 32 ? k1 - kb : 32);
+      int32_t my_u = -1, my_b = 0;
+      if (lane < cnt) {
+        const int32_t l = w.perm[kb + lane];
+        my_u = w.uid[l];
+        const int32_t bb = w.bag_of[l];
+        my_b = bb < 0 ? 0 : (bb >= B ? (int32_t)(B - 1) : bb);
       }
+      for (int j = 0; j < cnt; j += 8) {
+        int32_t uj[8];
+        float4 g[8];
+        float gs[8];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (uj[t] == -2) break;
-        if (uj[t] != cur) {
-          if (cur >= 0 && live) s_flush(w, cur, k0, c, D, acc, vec, accs);
-          acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          accs = 0.f;
-          cur = uj[t];
+        for (int t = 0; t < 8; ++t) {
+          const int jj = (j + t) & 31;
+          uj[t] = __shfl_sync(0xffffffffu, my_u, jj);
+          const int32_t bj = __shfl_sync(0xffffffffu, my_b, jj);
+          const bool use = live && (j + t) < cnt;
+          g[t] = z4;
+          gs[t] = 0.f;
+          if (use) {
+            if (vec) g[t] = __ldg(reinterpret_cast<const float4*>(grad_out + bj * (int64_t)D) + c);
+            else gs[t] = __ldg(grad_out + bj * (int64_t)D + c);
+          }
         }
-        acc.x += g[t].x; acc.y += g[t].y; acc.z += g[t].z; acc.w += g[t].w;
-        accs += gs[t];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (j + t >= cnt) break;
+          if (uj[t] != cur) {
+            if (cur >= 0 && live) s_flush(w, cur, k0, c, D, acc, vec, accs);
+            acc = z4;
+            accs = 0.f;
+            cur = uj[t];
+          }
+          acc.x += g[t].x; acc.y += g[t].y; acc.z += g[t].z; acc.w += g[t].w;
+          accs += gs[t];
+        }
       }
     }
     if (cur >= 0 && live) s_flush(w, cur, k0, c, D, acc, vec, accs);
@@ -237,98 +229,165 @@ __global__ void __launch_bounds__(256) k_bwd_generic(BwdArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Register-tiled backward chunk kernel (n1 = n3 = 4, R1 = R2 = R).  A chunk that
-// starts a hot prefix takes ALL of that prefix's rows (its dP2 is summed in
-// shared memory before dG2/dG1 are formed once); the chunks holding the later
-// pieces of that prefix are skipped.  Shared memory:
-//   G2s [R][N2*R], P1t [CP][R][4], P2 and dP2 [CP][4*N2][R+4] (+4 per prefix),
-//   S [32][D+4] (gathered output gradients of a batch of rows),
-//   G3t [32][4*R+4] (G3 slices of the batch, transposed to [j3][b]).
+// Warp-specialised backward chunk kernel (n1 = n3 = 4, R1 = R2 = R).  Warp 8 is a
+// producer: for the next chunk it writes the metadata and bulk-copies (TMA,
+// 1-D) the G2 slice, the G1 rows and the S and G3 rows of the first RB rows into
+// the free one of two stage buffers.  Warps 0-7 consume: P2 (stage 2), then per
+// batch of RB rows dG3 (float4 atomics) and dP2 (shared memory), then
+// dG2 = P1^T dP2 and dG1 = dP2 G2^T.  A chunk that starts a hot prefix takes all
+// of that prefix's rows (later batches are loaded by the consumers into the
+// already consumed row area); chunks holding its later pieces are skipped.
 template <int N2, int R, int CP>
-struct BwdCfg {
+struct BwsCfg {
   using T = TileCfg<N2, R, CP>;
   static constexpr int RB = 32;
-  static constexpr int SS = T::D + 4;
-  static constexpr int G3TS = 4 * R + 4;
-  static constexpr int F_S = RB * SS;
-  static constexpr int F_G3 = RB * G3TS;
-  static constexpr int SMEM = 4 * (T::F_G2 + T::F_P1 + 2 * T::F_P2 + F_S + F_G3) + 8 * RB;
-  static constexpr int TILES = T::NB * (R / 4);          // (j12 block, b block) tiles of dP2
-  static constexpr int RG = 256 / TILES;                  // row groups in the dP2 phase
-  static_assert(256 % TILES == 0 && RB % RG == 0, "dP2 phase mapping");
-  static_assert(T::NC % 128 == 0, "dG2 phase mapping");
+  static constexpr int SS = T::D + 4;                 // padded S row (floats)
+  static constexpr int GS = 4 * R + 4;                // padded G3 row, natural [b][j3]
+  static constexpr int F_P1 = CP * 4 * R;             // natural [p][j1][a]
+  static constexpr int STAGE_F = T::F_G2 + F_P1 + RB * (SS + GS);
+  struct Meta {
+    int x0, x1, p0, np, end, nst, pad[2];
+    int rp[RB];
+    int ri3[RB];
+  };
+  static constexpr int SMEM = 4 * (2 * STAGE_F + 2 * T::F_P2) + 2 * (int)sizeof(Meta) + 4 * 8;
+  static constexpr int TILES = T::NB * (R / 4);
+  static constexpr int RG = 256 / TILES;
+  static_assert(T::NB == 8 && 256 % TILES == 0 && RB % RG == 0, "mappings");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 template <int N2, int R, int CP>
-__global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
-  using C = BwdCfg<N2, R, CP>;
+__global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
+  using C = BwsCfg<N2, R, CP>;
   using T = typename C::T;
+  using Meta = typename C::Meta;
   constexpr int NC = T::NC, P2S = T::P2S, P2P = T::P2P, D = T::D;
   extern __shared__ float4 sm4[];
-  float* G2s = reinterpret_cast<float*>(sm4);
-  float* P1t = G2s + T::F_G2;
-  float* P2 = P1t + T::F_P1;
+  float* base = reinterpret_cast<float*>(sm4);
+  float* P2 = base + 2 * C::STAGE_F;
   float* dP2 = P2 + T::F_P2;
-  float* Ss = dP2 + T::F_P2;
-  float* G3t = Ss + C::F_S;
-  int* rowp = reinterpret_cast<int*>(G3t + C::F_G3);
-  int* rowi3 = rowp + C::RB;
-  __shared__ int c_sh;
+  Meta* meta = reinterpret_cast<Meta*>(dP2 + T::F_P2);
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
+  uint64_t* empty = full + 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(&empty[0], 1);
+    mbar_init(&empty[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
   const int n_chunks = a.w.ctl->n_chunks;
-  for (;;) {
-    if (tid == 0) c_sh = (int)atomicAdd(&a.w.ctl->bwd_chunk_ctr, 1u);
-    __syncthreads();
-    const int c = c_sh;
-    if (c >= n_chunks) break;
-    const int x0 = a.w.chunk_start[c];
-    const int p0 = a.w.row_pair[x0];
-    const int pr0 = a.w.pair_row_start[p0];
-    if (x0 != pr0) {          // a later piece of a hot prefix: its first chunk does it all
-      __syncthreads();
-      continue;
+
+  if (warp == 8) {
+    // ---------------- producer
+    int it = 0;
+    for (;;) {
+      int c = 0;
+      if (lane == 0) c = (int)atomicAdd(&a.w.ctl->bwd_chunk_ctr, 1u);
+      c = __shfl_sync(0xffffffffu, c, 0);
+      int x0 = 0, x1 = 0, p0 = 0, np = 0;
+      if (c < n_chunks) {
+        x0 = a.w.chunk_start[c];
+        p0 = a.w.row_pair[x0];
+        if (x0 != a.w.pair_row_start[p0]) continue;      // a later piece of a hot prefix
+        x1 = a.w.chunk_start[c + 1];
+        const int p1 = a.w.row_pair[x1 - 1];
+        if (p1 == p0) x1 = a.w.pair_row_start[p0 + 1];   // the whole prefix
+        np = p1 - p0 + 1;
+      }
+      const int s = it & 1;
+      const uint32_t use = (uint32_t)it >> 1;
+      ++it;
+      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
+      Meta& m = meta[s];
+      if (c >= n_chunks) {
+        if (lane == 0) {
+          m.end = 1;
+          mbar_arrive(&full[s]);
+        }
+        break;
+      }
+      const int i2 = a.w.pair_i2[p0];
+      const int nst = min(x1 - x0, C::RB);
+      float* G2s = base + s * C::STAGE_F;
+      float* P1n = G2s + T::F_G2;
+      float* Ss = P1n + C::F_P1;
+      float* G3s = Ss + C::RB * C::SS;
+      int my_i3 = 0;
+      if (lane < nst) {
+        m.rp[lane] = a.w.row_pair[x0 + lane] - p0;
+        my_i3 = a.w.row_i3[x0 + lane];
+        m.ri3[lane] = my_i3;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        m.x0 = x0;
+        m.x1 = x1;
+        m.p0 = p0;
+        m.np = np;
+        m.nst = nst;
+        m.end = 0;
+        const uint32_t bytes = 4u * (T::F_G2 + np * 4 * R + nst * (D + 4 * R));
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_g2s(G2s, a.G2 + (size_t)i2 * T::F_G2, 4u * T::F_G2, &full[s]);
+      }
+      __syncwarp();
+      if (lane < np)
+        bulk_g2s(P1n + lane * 4 * R, a.G1 + (size_t)a.w.pair_i1[p0 + lane] * 4 * R, 16u * R,
+                 &full[s]);
+      if (lane < nst) {
+        bulk_g2s(Ss + lane * C::SS, a.w.rowbuf + (size_t)(x0 + lane) * D, 4u * D, &full[s]);
+        bulk_g2s(G3s + lane * C::GS, a.G3 + (size_t)my_i3 * 4 * R, 16u * R, &full[s]);
+      }
     }
-    int x1 = a.w.chunk_start[c + 1];
-    const int p1 = a.w.row_pair[x1 - 1];
-    if (p1 == p0) x1 = a.w.pair_row_start[p0 + 1];   // whole prefix
-    const int np = p1 - p0 + 1;
-    const int i2 = a.w.pair_i2[p0];
-    tiled_load_g2_p1<T>(a.G1, a.G2, a.w.pair_i1, i2, p0, np, G2s, P1t);
+    return;
+  }
+
+  // ---------------- consumers (warps 0-7)
+  for (int it = 0;; ++it) {
+    const int s = it & 1;
+    if (!mbar_wait(&full[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
+    Meta& m = meta[s];
+    if (m.end) break;
+    const int x0 = m.x0, x1 = m.x1, p0 = m.p0, np = m.np;
+    const float* G2s = base + s * C::STAGE_F;
+    const float* P1n = G2s + T::F_G2;
+    float* Ss = const_cast<float*>(P1n) + C::F_P1;
+    float* G3s = Ss + C::RB * C::SS;
     for (int e = tid; e < np * P2P; e += 256) dP2[e] = 0.f;
-    __syncthreads();
-    tiled_stage2_any<T>(G2s, P1t, P2, np);
+    stage2_natural<T>(G2s, P1n, P2, np);
+    named_sync(1, 256);
 
     for (int xb = x0; xb < x1; xb += C::RB) {
       const int nb = min(C::RB, x1 - xb);
-      __syncthreads();
-      if (tid < nb) {
-        rowp[tid] = a.w.row_pair[xb + tid] - p0;
-        rowi3[tid] = a.w.row_i3[xb + tid];
+      if (xb != x0) {
+        // later batches of a hot prefix: the consumers load them into the row area
+        named_sync(1, 256);
+        if (tid < nb) {
+          m.rp[tid] = a.w.row_pair[xb + tid] - p0;
+          m.ri3[tid] = a.w.row_i3[xb + tid];
+        }
+        for (int e = tid; e < nb * (D / 4); e += 256) {
+          const int r = e / (D / 4), q = e - r * (D / 4);
+          *reinterpret_cast<float4*>(Ss + r * C::SS + 4 * q) =
+              reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)(xb + r) * D)[q];
+        }
+        for (int e = tid; e < nb * R; e += 256) {
+          const int r = e / R, q = e - r * R;
+          *reinterpret_cast<float4*>(G3s + r * C::GS + 4 * q) = __ldg(
+              reinterpret_cast<const float4*>(a.G3 + (size_t)a.w.row_i3[xb + r] * 4 * R) + q);
+        }
+        named_sync(1, 256);
       }
-      // S rows of the batch
-      for (int e = tid; e < nb * (D / 4); e += 256) {
-        const int r = e / (D / 4), q = e - r * (D / 4);
-        const float4 v = reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)(xb + r) * D)[q];
-        *reinterpret_cast<float4*>(Ss + r * C::SS + 4 * q) = v;
-      }
-      // G3 slices, transposed to [j3][b]
-      for (int e = tid; e < nb * R; e += 256) {
-        const int r = e / R, b = e - r * R;
-        const float4 v = __ldg(reinterpret_cast<const float4*>(
-            a.G3 + ((size_t)a.w.row_i3[xb + r] * R + b) * 4));
-        float* g = G3t + r * C::G3TS + b;
-        g[0] = v.x;
-        g[R] = v.y;
-        g[2 * R] = v.z;
-        g[3 * R] = v.w;
-      }
-      __syncthreads();
       // dG3[i3][b][j3] += sum_j12 P2[j12][b] S[j12][j3]: lane = row, warp = block of 4 b
       if (lane < nb) {
         const int r = lane;
         const float* ss = Ss + r * C::SS;
         for (int bb = warp; bb < R / 4; bb += 8) {
-          const float* pp = P2 + rowp[r] * P2P + 4 * bb;
+          const float* pp = P2 + m.rp[r] * P2P + 4 * bb;
           float acc[4][4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -347,7 +406,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
               acc[i][3] = fmaf(pw[i], sv.w, acc[i][3]);
             }
           }
-          float4* dst = reinterpret_cast<float4*>(a.dG3 + ((size_t)rowi3[r] * R + 4 * bb) * 4);
+          float4* dst = reinterpret_cast<float4*>(a.dG3 + ((size_t)m.ri3[r] * R + 4 * bb) * 4);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             atomicAdd(dst + i, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
@@ -367,7 +426,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
           for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
         int cur = -1;
         for (int r = r0; r < r1; ++r) {
-          const int pl = rowp[r];
+          const int pl = m.rp[r];
           if (pl != cur) {
             if (cur >= 0) {
               float* d = dP2 + cur * P2P + (4 * jb) * P2S + 4 * bq;
@@ -386,19 +445,19 @@ __global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
           for (int i = 0; i < 4; ++i)
             sv[i] = *reinterpret_cast<const float4*>(Ss + r * C::SS + (4 * jb + i) * 4);
 #pragma unroll
-          for (int j3 = 0; j3 < 4; ++j3)
-            gv[j3] = *reinterpret_cast<const float4*>(G3t + r * C::G3TS + j3 * R + 4 * bq);
+          for (int t = 0; t < 4; ++t)
+            gv[t] = *reinterpret_cast<const float4*>(G3s + r * C::GS + (4 * bq + t) * 4);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float s4[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};
+          for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j3 = 0; j3 < 4; ++j3) {
-              acc[i][0] = fmaf(s4[j3], gv[j3].x, acc[i][0]);
-              acc[i][1] = fmaf(s4[j3], gv[j3].y, acc[i][1]);
-              acc[i][2] = fmaf(s4[j3], gv[j3].z, acc[i][2]);
-              acc[i][3] = fmaf(s4[j3], gv[j3].w, acc[i][3]);
+            for (int t = 0; t < 4; ++t) {
+              float v = acc[i][t];
+              v = fmaf(sv[i].x, gv[t].x, v);
+              v = fmaf(sv[i].y, gv[t].y, v);
+              v = fmaf(sv[i].z, gv[t].z, v);
+              v = fmaf(sv[i].w, gv[t].w, v);
+              acc[i][t] = v;
             }
-          }
         }
         if (cur >= 0) {
           float* d = dP2 + cur * P2P + (4 * jb) * P2S + 4 * bq;
@@ -409,9 +468,10 @@ __global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
         }
       }
     }
-    __syncthreads();
+    named_sync(1, 256);
     // dG2[i2][a][n] += sum_{p, j1} P1[p][j1][a] dP2[p][j1][n]: warp = block of 4 a,
     // lane = 4-column groups at stride 128
+    const int i2 = a.w.pair_i2[p0];
     {
       constexpr int Q = NC / 128;
       for (int ab = warp; ab < R / 4; ab += 8) {
@@ -421,12 +481,10 @@ __global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
 #pragma unroll
           for (int j = 0; j < 4 * Q; ++j) acc[i][j] = 0.f;
         for (int p = 0; p < np; ++p) {
-          float4 av[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            av[i] = *reinterpret_cast<const float4*>(P1t + p * (R * 4) + (4 * ab + i) * 4);
 #pragma unroll
           for (int j1 = 0; j1 < 4; ++j1) {
+            const float4 a4 = *reinterpret_cast<const float4*>(P1n + p * 4 * R + j1 * R + 4 * ab);
+            const float aw[4] = {a4.x, a4.y, a4.z, a4.w};
             float bv[4 * Q];
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
@@ -437,11 +495,9 @@ __global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
               bv[4 * q] = v.x; bv[4 * q + 1] = v.y; bv[4 * q + 2] = v.z; bv[4 * q + 3] = v.w;
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float aw = j1 == 0 ? av[i].x : (j1 == 1 ? av[i].y : (j1 == 2 ? av[i].z : av[i].w));
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-              for (int j = 0; j < 4 * Q; ++j) acc[i][j] = fmaf(aw, bv[j], acc[i][j]);
-            }
+              for (int j = 0; j < 4 * Q; ++j) acc[i][j] = fmaf(aw[i], bv[j], acc[i][j]);
           }
         }
 #pragma unroll
@@ -460,8 +516,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
     {
       constexpr int AQ = R / 4;
       const int items = np * AQ * 8;
-      for (int base = 0; base < items; base += 256) {
-        const int item = base + tid;
+      for (int b0 = 0; b0 < items; b0 += 256) {
+        const int item = b0 + tid;
         const bool valid = item < items;
         const int ns = item & 7, g = item >> 3;
         const int p = g / AQ, aq = g - p * AQ;
@@ -471,8 +527,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
         if (valid) {
-          for (int s = 0; s < NC / 32; ++s) {
-            const int n = 32 * s + 4 * ns;
+          for (int sgrp = 0; sgrp < NC / 32; ++sgrp) {
+            const int n = 32 * sgrp + 4 * ns;
             const int j2 = n / R, b = n - j2 * R;
             float4 dv[4], gv[4];
 #pragma unroll
@@ -513,7 +569,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_tiled(BwdArgs a) {
         }
       }
     }
-    __syncthreads();
+    named_sync(1, 256);
+    if (tid == 0) mbar_arrive(&empty[s]);
   }
 }
 
@@ -565,14 +622,14 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   ba.dG2 = core_grads[1];
   ba.dG3 = core_grads[2];
   if (s.n1 == 4 && s.n3 == 4 && s.n2 == 8 && s.R1 == 32 && s.R2 == 32) {
-    using C = BwdCfg<8, 32, kCP_8_32>;
+    using C = BwsCfg<8, 32, kCP_8_32>;
     static int grid = 0;
     if (grid == 0) {
-      cudaFuncSetAttribute(k_bwd_tiled<8, 32, kCP_8_32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(k_bwd_ws<8, 32, kCP_8_32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM);
-      grid = persistent_grid_bwd((const void*)k_bwd_tiled<8, 32, kCP_8_32>, 256, C::SMEM);
+      grid = persistent_grid_bwd((const void*)k_bwd_ws<8, 32, kCP_8_32>, 288, C::SMEM);
     }
-    TT_TIMED("k_bwd_tiled", st, (k_bwd_tiled<8, 32, kCP_8_32><<<grid, 256, C::SMEM, st>>>(ba)));
+    TT_TIMED("k_bwd_ws", st, (k_bwd_ws<8, 32, kCP_8_32><<<grid, 288, C::SMEM, st>>>(ba)));
   } else {
     const size_t g2n = (size_t)s.R1 * s.n2 * s.R2;
     const size_t base = g2n + (size_t)s.n1 * s.R1 + 2 * (size_t)s.n1 * s.n2 * s.R2;

@@ -315,52 +315,58 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
 
 // out[b] = sum of the unique rows of bag b's lookups; one warp per bag.  The
 // lanes fetch up to 32 of the bag's unique-row ids at once; each lane then sums
-// its float4 column of those rows with 8 loads in flight.
+// its float4 column of those rows, 8 loads in flight.
+__device__ __forceinline__ void f4add(float4& a, const float4& b) {
+  a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+}
+
 __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offsets, int64_t B,
                                               int64_t nnz, const int32_t* __restrict__ uid,
                                               const float* __restrict__ rowbuf, int D,
                                               float* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const bool vec = (D & 3) == 0;
-  const int cols = vec ? (D >> 2) : D;
-  const int cols_pad = cols + ((32 - cols % 32) % 32);   // uniform trip count for the shuffles
-  const float4* rb4 = reinterpret_cast<const float4*>(rowbuf);
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < B; b += warps) {
     int64_t l0 = offsets[b], l1 = offsets[b + 1];
     l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
     l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
-    for (int c = lane; c < cols_pad; c += 32) {
-      const bool live = c < cols;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float accs = 0.f;
-      for (int64_t lb = l0; lb < l1; lb += 32) {
-        const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
-        const int32_t my_u = lane < cnt ? uid[lb + lane] : -1;
-        for (int j0 = 0; j0 < cnt; j0 += 8) {
-          float4 v[8];
-          float vs[8];
+    if ((D & 3) == 0) {
+      const int cols = D >> 2;
+      const float4* rb4 = reinterpret_cast<const float4*>(rowbuf);
+      for (int c0 = 0; c0 < cols; c0 += 32) {
+        const int c = c0 + lane;
+        const bool live = c < cols;
+        float4 acc = z4;
+        for (int64_t lb = l0; lb < l1; lb += 32) {
+          const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
+          const int32_t my_u = lane < cnt ? uid[lb + lane] : -1;
+          int j = 0;
+          for (; j + 8 <= cnt; j += 8) {
+            float4 v[8];
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const int32_t u = __shfl_sync(0xffffffffu, my_u, (j0 + t) & 31);
-            const bool use = live && (j0 + t) < cnt && u >= 0;
-            v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-            vs[t] = 0.f;
-            if (use) {
-              if (vec) v[t] = rb4[(int64_t)u * cols + c];
-              else vs[t] = rowbuf[(int64_t)u * D + c];
+            for (int t = 0; t < 8; ++t) {
+              const int32_t u = __shfl_sync(0xffffffffu, my_u, j + t);
+              v[t] = (live && u >= 0) ? rb4[(int64_t)u * cols + c] : z4;
             }
-          }
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            acc.x += v[t].x; acc.y += v[t].y; acc.z += v[t].z; acc.w += v[t].w;
-            accs += vs[t];
+            for (int t = 0; t < 8; ++t) f4add(acc, v[t]);
+          }
+          for (; j < cnt; ++j) {
+            const int32_t u = __shfl_sync(0xffffffffu, my_u, j);
+            if (live && u >= 0) f4add(acc, rb4[(int64_t)u * cols + c]);
           }
         }
+        if (live) reinterpret_cast<float4*>(out + b * (int64_t)D)[c] = acc;
       }
-      if (live) {
-        if (vec) reinterpret_cast<float4*>(out + b * (int64_t)D)[c] = acc;
-        else out[b * (int64_t)D + c] = accs;
+    } else {
+      for (int j = lane; j < D; j += 32) {
+        float acc = 0.f;
+        for (int64_t l = l0; l < l1; ++l) {
+          const int u = uid[l];
+          if (u >= 0) acc += rowbuf[(int64_t)u * D + j];
+        }
+        out[b * (int64_t)D + j] = acc;
       }
     }
   }

@@ -8,7 +8,7 @@ namespace tt {
 
 // Prefixes per chunk of the tiled kernels (shared by the grouping, the forward
 // and the backward: the backward sizes its shared memory for this many).
-constexpr int kCP_8_32 = 12, kCP_8_64 = 4, kCP_4_16 = 16;
+constexpr int kCP_8_32 = 8, kCP_8_64 = 4, kCP_4_16 = 16;
 
 // Register-tiled chunk kernel for n1 = n3 = 4 and R1 = R2 = R (the shapes of the
 // benchmark tables).  Shared memory per CTA:
