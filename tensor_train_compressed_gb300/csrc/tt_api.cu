@@ -71,7 +71,7 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
     return at;
   };
   L.ctl = take(sizeof(Ctl));
-  L.hist = take(sizeof(uint32_t) * kMaxPasses * kRadix);
+  L.hist = take(sizeof(uint32_t) * kHistCopies * kMaxPasses * kRadix);
   L.sort_status = take(sizeof(uint32_t) * kMaxPasses * (size_t)L.n_sort_tiles * kRadix);
   L.keysA = take(sizeof(uint64_t) * (size_t)n);
   L.keysB = take(sizeof(uint64_t) * (size_t)n);
@@ -86,6 +86,7 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
   L.pair_i2 = take(sizeof(int32_t) * (size_t)n);
   L.seg_status = take(sizeof(unsigned long long) * (size_t)L.n_scan_tiles);
   L.chunk_start = take(sizeof(int32_t) * ((size_t)n + 1));
+  L.chunk_desc = take(sizeof(int2) * ((size_t)n + 1));
   L.chunk_status = take(sizeof(uint32_t) * (size_t)L.n_scan_tiles);
   L.rowbuf = take(sizeof(float) * (size_t)L.rowbuf_rows * (size_t)s.D);
   L.total = off;
@@ -111,6 +112,7 @@ WS make_ws(void* base, const Layout& L) {
   w.pair_i2 = reinterpret_cast<int32_t*>(b + L.pair_i2);
   w.seg_status = reinterpret_cast<unsigned long long*>(b + L.seg_status);
   w.chunk_start = reinterpret_cast<int32_t*>(b + L.chunk_start);
+  w.chunk_desc = reinterpret_cast<int2*>(b + L.chunk_desc);
   w.chunk_status = reinterpret_cast<uint32_t*>(b + L.chunk_status);
   w.rowbuf = reinterpret_cast<float*>(b + L.rowbuf);
   return w;

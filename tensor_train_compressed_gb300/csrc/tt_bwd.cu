@@ -282,45 +282,51 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
   const int n_chunks = a.w.ctl->n_chunks;
 
   if (warp == 8) {
-    // ---------------- producer
-    int it = 0;
-    for (;;) {
-      int c = 0;
-      if (lane == 0) c = (int)atomicAdd(&a.w.ctl->bwd_chunk_ctr, 1u);
-      c = __shfl_sync(0xffffffffu, c, 0);
-      int x0 = 0, x1 = 0, p0 = 0, np = 0;
-      if (c < n_chunks) {
-        x0 = a.w.chunk_start[c];
-        p0 = a.w.row_pair[x0];
-        if (x0 != a.w.pair_row_start[p0]) continue;      // a later piece of a hot prefix
-        x1 = a.w.chunk_start[c + 1];
-        const int p1 = a.w.row_pair[x1 - 1];
-        if (p1 == p0) x1 = a.w.pair_row_start[p0 + 1];   // the whole prefix
-        np = p1 - p0 + 1;
+    // ---------------- producer: claims one chunk ahead (see the forward kernel);
+    // chunks holding a later piece of a hot prefix are skipped
+    auto next_chunk = [&](ChunkDesc& d) {
+      for (;;) {
+        const int c = claim_chunk(&a.w.ctl->bwd_chunk_ctr);
+        if (c >= n_chunks) return c;
+        d = load_chunk(a.w.chunk_desc, c);
+        if (d.whole) return c;
       }
+    };
+    ChunkDesc d{};
+    int c = next_chunk(d);
+    for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t use = (uint32_t)it >> 1;
-      ++it;
-      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
       Meta& m = meta[s];
       if (c >= n_chunks) {
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
         if (lane == 0) {
           m.end = 1;
           mbar_arrive(&full[s]);
         }
         break;
       }
-      const int i2 = a.w.pair_i2[p0];
+      const int x0 = d.x0, p0 = d.p0, p1 = d.p1;
+      const int x1 = p1 == p0 ? a.w.pair_row_start[p0 + 1] : d.x1;   // a whole hot prefix
+      const int np = p1 - p0 + 1;
       const int nst = min(x1 - x0, C::RB);
+      int rp = 0, g3 = 0, gi1 = 0;
+      if (lane < nst) {
+        rp = a.w.row_pair[x0 + lane] - p0;
+        g3 = a.w.row_i3[x0 + lane];
+      }
+      if (lane < np) gi1 = a.w.pair_i1[p0 + lane];
+      const int i2 = a.w.pair_i2[p0];
+      ChunkDesc dn{};
+      const int cn = next_chunk(dn);
+      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
       float* G2s = base + s * C::STAGE_F;
       float* P1n = G2s + T::F_G2;
       float* Ss = P1n + C::F_P1;
       float* G3s = Ss + C::RB * C::SS;
-      int my_i3 = 0;
       if (lane < nst) {
-        m.rp[lane] = a.w.row_pair[x0 + lane] - p0;
-        my_i3 = a.w.row_i3[x0 + lane];
-        m.ri3[lane] = my_i3;
+        m.rp[lane] = rp;
+        m.ri3[lane] = g3;
       }
       __syncwarp();
       if (lane == 0) {
@@ -335,13 +341,13 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
         bulk_g2s(G2s, a.G2 + (size_t)i2 * T::F_G2, 4u * T::F_G2, &full[s]);
       }
       __syncwarp();
-      if (lane < np)
-        bulk_g2s(P1n + lane * 4 * R, a.G1 + (size_t)a.w.pair_i1[p0 + lane] * 4 * R, 16u * R,
-                 &full[s]);
+      if (lane < np) bulk_g2s(P1n + lane * 4 * R, a.G1 + (size_t)gi1 * 4 * R, 16u * R, &full[s]);
       if (lane < nst) {
         bulk_g2s(Ss + lane * C::SS, a.w.rowbuf + (size_t)(x0 + lane) * D, 4u * D, &full[s]);
-        bulk_g2s(G3s + lane * C::GS, a.G3 + (size_t)my_i3 * 4 * R, 16u * R, &full[s]);
+        bulk_g2s(G3s + lane * C::GS, a.G3 + (size_t)g3 * 4 * R, 16u * R, &full[s]);
       }
+      c = cn;
+      d = dn;
     }
     return;
   }

@@ -177,6 +177,7 @@ struct WsCfg {
   };
   static constexpr int SMEM = 4 * (2 * STAGE_F + T::F_P2) + 2 * (int)sizeof(Meta) + 4 * 8;
   static_assert(T::NB == 8, "one compute warp per j12 block");
+  static_assert(ROWMAX <= 64 && CP <= 32, "the producer stages with two rows per lane");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -235,31 +236,48 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
   const int n_chunks = a.w.ctl->n_chunks;
 
   if (warp == 8) {
-    // ---------------- producer
+    // ---------------- producer: claims one chunk ahead, so that the claim and
+    // the descriptor load of chunk i+1 overlap the staging of chunk i
+    int c = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
+    ChunkDesc d{};
+    if (c < n_chunks) d = load_chunk(a.w.chunk_desc, c);
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t use = (uint32_t)it >> 1;
-      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
-      int c = 0;
-      if (lane == 0) c = (int)atomicAdd(&a.w.ctl->fwd_chunk_ctr, 1u);
-      c = __shfl_sync(0xffffffffu, c, 0);
       Meta& m = meta[s];
       if (c >= n_chunks) {
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
         if (lane == 0) {
           m.end = 1;
           mbar_arrive(&full[s]);
         }
         break;
       }
-      const int x0 = a.w.chunk_start[c], x1 = a.w.chunk_start[c + 1];
-      const int p0 = a.w.row_pair[x0];
-      const int np = a.w.row_pair[x1 - 1] - p0 + 1;
-      const int i2 = a.w.pair_i2[p0];
+      const int x0 = d.x0, x1 = d.x1, p0 = d.p0;
+      const int np = d.p1 - p0 + 1;
       const int nst = min(x1 - x0, W::ROWMAX);
+      // metadata of this chunk (loads in flight while the stage frees up)
+      int rp0 = 0, rp1 = 0, g30 = 0, g31 = 0, gi1 = 0;
+      if (lane < nst) {
+        rp0 = a.w.row_pair[x0 + lane] - p0;
+        g30 = a.w.row_i3[x0 + lane];
+      }
+      if (lane + 32 < nst) {
+        rp1 = a.w.row_pair[x0 + lane + 32] - p0;
+        g31 = a.w.row_i3[x0 + lane + 32];
+      }
+      if (lane < np) gi1 = a.w.pair_i1[p0 + lane];
+      const int i2 = a.w.pair_i2[p0];
+      // claim the next chunk and fetch its descriptor
+      const int cn = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
+      ChunkDesc dn{};
+      if (cn < n_chunks) dn = load_chunk(a.w.chunk_desc, cn);
+      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
       float* G2s = base + s * W::STAGE_F;
       float* P1n = G2s + T::F_G2;
       float* G3s = P1n + W::F_P1;
-      for (int r = lane; r < nst; r += 32) m.rp[r] = a.w.row_pair[x0 + r] - p0;
+      if (lane < nst) m.rp[lane] = rp0;
+      if (lane + 32 < nst) m.rp[lane + 32] = rp1;
       __syncwarp();
       if (lane == 0) {
         m.x0 = x0;
@@ -272,10 +290,12 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
         bulk_g2s(G2s, a.G2 + (size_t)i2 * T::F_G2, 4u * T::F_G2, &full[s]);
       }
       __syncwarp();
-      for (int p = lane; p < np; p += 32)
-        bulk_g2s(P1n + p * 4 * R, a.G1 + (size_t)a.w.pair_i1[p0 + p] * 4 * R, 16u * R, &full[s]);
-      for (int r = lane; r < nst; r += 32)
-        bulk_g2s(G3s + r * T::G3S, a.G3 + (size_t)a.w.row_i3[x0 + r] * 4 * R, 16u * R, &full[s]);
+      if (lane < np) bulk_g2s(P1n + lane * 4 * R, a.G1 + (size_t)gi1 * 4 * R, 16u * R, &full[s]);
+      if (lane < nst) bulk_g2s(G3s + lane * T::G3S, a.G3 + (size_t)g30 * 4 * R, 16u * R, &full[s]);
+      if (lane + 32 < nst)
+        bulk_g2s(G3s + (lane + 32) * T::G3S, a.G3 + (size_t)g31 * 4 * R, 16u * R, &full[s]);
+      c = cn;
+      d = dn;
     }
     return;
   }

@@ -85,8 +85,9 @@ __global__ void __launch_bounds__(256) k_prepare(PrepArgs a) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + tid; i < a.zero32b_words; i += stride) a.zero32b[i] = 0;
 
   __syncthreads();
+  uint32_t* h = a.w.hist + (size_t)(blockIdx.x % kHistCopies) * kMaxPasses * kRadix;
   for (int i = tid; i < a.passes * kRadix; i += blockDim.x)
-    if (sh[i]) atomicAdd(&a.w.hist[i], sh[i]);
+    if (sh[i]) atomicAdd(&h[i], sh[i]);
 }
 
 struct ScatterArgs {
@@ -110,7 +111,10 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter(ScatterArgs a) {
   if (tid == 0) tile_sh = atomicAdd(&a.w.ctl->sort_tile_ctr[a.pass], 1u);
   for (int i = tid; i < (kSortThreads / 32) * kRadix; i += kSortThreads) (&whist[0][0])[i] = 0;
   uint32_t total;
-  const uint32_t bucket = block_exclusive_scan_256(a.w.hist[a.pass * kRadix + tid], &total, scan8);
+  uint32_t hsum = 0;
+#pragma unroll
+  for (int c = 0; c < kHistCopies; ++c) hsum += a.w.hist[(c * kMaxPasses + a.pass) * kRadix + tid];
+  const uint32_t bucket = block_exclusive_scan_256(hsum, &total, scan8);
   __syncthreads();
   const uint32_t tile = tile_sh;
   const int64_t base = (int64_t)tile * kSortTile;
@@ -167,21 +171,31 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter(ScatterArgs a) {
       st_relaxed_u32(st, kFlagIncl | sum);
     } else {
       st_relaxed_u32(st + (size_t)tile * kRadix, kFlagAgg | sum);
+      // walk back 8 predecessor tiles per round trip
       int64_t j = (int64_t)tile - 1;
       long long spins = 0;
       while (j >= 0) {
-        const uint32_t v = ld_relaxed_u32(st + (size_t)j * kRadix);
-        const uint32_t f = v & kFlagMask;
-        if (f == 0) {
-          if (++spins > kSpinCap) {
-            set_status(a.w.ctl, kStTimeout);
+        uint32_t v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          v[k] = (j - k >= 0) ? ld_relaxed_u32(st + (size_t)(j - k) * kRadix) : kFlagIncl;
+        int k = 0;
+        bool done = false;
+        for (; k < 8; ++k) {
+          const uint32_t f = v[k] & kFlagMask;
+          if (f == 0) break;
+          excl += v[k] & kValMask;
+          if (f == kFlagIncl) {
+            done = true;
             break;
           }
-          continue;
         }
-        excl += v & kValMask;
-        if (f == kFlagIncl) break;
-        --j;
+        if (done) break;
+        j -= k;
+        if (k < 8 && ++spins > kSpinCap) {
+          set_status(a.w.ctl, kStTimeout);
+          break;
+        }
       }
       st_relaxed_u32(st + (size_t)tile * kRadix, kFlagIncl | ((excl + sum) & kValMask));
     }
@@ -323,6 +337,7 @@ __global__ void __launch_bounds__(kScanThreads) k_chunks(ChunkArgs a) {
     if (tile == 0 && tid == 0) {   // no unique row: no chunk
       a.w.ctl->n_chunks = 0;
       a.w.chunk_start[0] = 0;
+      a.w.chunk_desc[0] = make_int2(0, (int32_t)0x80000000);
     }
     return;
   }
@@ -346,10 +361,17 @@ __global__ void __launch_bounds__(kScanThreads) k_chunks(ChunkArgs a) {
   for (int i = 0; i < kScanItems; ++i) {
     const int64_t x = x0 + i;
     if (x >= U) break;
-    if (flags & (1u << i)) a.w.chunk_start[c++] = (int32_t)x;
+    if (flags & (1u << i)) {
+      const int32_t p = a.w.row_pair[x];
+      const bool first = a.w.pair_row_start[p] == (int32_t)x;
+      a.w.chunk_start[c] = (int32_t)x;
+      a.w.chunk_desc[c] = make_int2((int32_t)x, p | (first ? (int32_t)0x80000000 : 0));
+      ++c;
+    }
     if (x == U - 1) {
       a.w.ctl->n_chunks = c;
       a.w.chunk_start[c] = U;
+      a.w.chunk_desc[c] = make_int2(U, a.w.ctl->U_12 | (int32_t)0x80000000);
     }
   }
 }
@@ -379,7 +401,7 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
   pa.zero32b_words = (size_t)L.n_scan_tiles;
   const int64_t work = nnz > num_bags + 1 ? nnz : num_bags + 1;
   int grid = (int)ceil_div(work, 256);
-  const int cap = sm_count() * 8;
+  const int cap = sm_count() * 2;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   TT_TIMED("k_prepare", st, (k_prepare<<<grid, 256, 0, st>>>(pa)));

@@ -16,6 +16,7 @@ namespace tt {
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
 constexpr int kMaxPasses = 4;               // keys of up to 32 bits
+constexpr int kHistCopies = 8;              // digit histograms are striped over 8 copies
 constexpr int kSortThreads = 256;
 constexpr int kSortItems = 8;               // per thread
 constexpr int kSortTile = kSortThreads * kSortItems;
@@ -63,7 +64,7 @@ struct Shape {
 struct Layout {
   size_t ctl, hist, sort_status, keysA, keysB, bag_of, uid, perm;
   size_t row_start, row_i3, row_pair, pair_row_start, pair_i1, pair_i2;
-  size_t seg_status, chunk_start, chunk_status, rowbuf, total;
+  size_t seg_status, chunk_start, chunk_desc, chunk_status, rowbuf, total;
   int key_bits, passes, n_sort_tiles, n_scan_tiles;
   int64_t rowbuf_rows;
 };
@@ -71,7 +72,7 @@ struct Layout {
 // Device pointers into one workspace.
 struct WS {
   Ctl* ctl;
-  uint32_t* hist;          // [kMaxPasses][kRadix]
+  uint32_t* hist;          // [kHistCopies][kMaxPasses][kRadix]
   uint32_t* sort_status;   // [kMaxPasses][n_sort_tiles][kRadix]
   uint64_t* keysA;
   uint64_t* keysB;
@@ -86,6 +87,7 @@ struct WS {
   int32_t* pair_i2;
   unsigned long long* seg_status;   // [n_scan_tiles]
   int32_t* chunk_start;
+  int2* chunk_desc;                 // [chunks+1] {first row, prefix | starts-a-prefix << 31}
   uint32_t* chunk_status;           // [n_scan_tiles]
   float* rowbuf;                    // [rowbuf_rows][D]
 };

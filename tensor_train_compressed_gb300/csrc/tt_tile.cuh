@@ -184,6 +184,30 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// Decoded work-chunk descriptor: rows [x0, x1), prefixes [p0, p1]; `whole` is
+// set when the chunk starts at the first row of its first prefix.
+struct ChunkDesc {
+  int x0, x1, p0, p1;
+  bool whole;
+};
+__device__ __forceinline__ ChunkDesc load_chunk(const int2* __restrict__ desc, int c) {
+  const int2 a = desc[c], b = desc[c + 1];
+  ChunkDesc d;
+  d.x0 = a.x;
+  d.x1 = b.x;
+  d.p0 = a.y & 0x7fffffff;
+  d.whole = a.y < 0;
+  // the next chunk starts a new prefix, or continues (a piece of) this one
+  d.p1 = (b.y & 0x7fffffff) - (b.y < 0 ? 1 : 0);
+  return d;
+}
+// Lane 0 of the calling warp claims the next work chunk; broadcast to the warp.
+__device__ __forceinline__ int claim_chunk(uint32_t* ctr) {
+  int c = 0;
+  if ((threadIdx.x & 31) == 0) c = (int)atomicAdd(ctr, 1u);
+  return __shfl_sync(0xffffffffu, c, 0);
+}
+
 __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
