@@ -251,6 +251,7 @@ struct BwsCfg {
     int ri3[RB];
   };
   static constexpr int SMEM = 4 * (2 * STAGE_F + 2 * T::F_P2) + 2 * (int)sizeof(Meta) + 4 * 8;
+  static_assert(RB * R <= 4 * 256, "in-place G3 transpose: 4 float4 per thread");
   static constexpr int TILES = T::NB * (R / 4);
   static constexpr int RG = 256 / TILES;
   static_assert(T::NB == 8 && 256 % TILES == 0 && RB % RG == 0, "mappings");
@@ -267,6 +268,7 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
   float* base = reinterpret_cast<float*>(sm4);
   float* P2 = base + 2 * C::STAGE_F;
   float* dP2 = P2 + T::F_P2;
+  float* P1t = dP2;     // transposed G1 rows live in the dP2 area until stage 2 is done
   Meta* meta = reinterpret_cast<Meta*>(dP2 + T::F_P2);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
   uint64_t* empty = full + 2;
@@ -363,9 +365,8 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
     const float* P1n = G2s + T::F_G2;
     float* Ss = const_cast<float*>(P1n) + C::F_P1;
     float* G3s = Ss + C::RB * C::SS;
+    stage2_natural<T>(G2s, P1n, P1t, P2, np);
     for (int e = tid; e < np * P2P; e += 256) dP2[e] = 0.f;
-    stage2_natural<T>(G2s, P1n, P2, np);
-    named_sync(1, 256);
 
     for (int xb = x0; xb < x1; xb += C::RB) {
       const int nb = min(C::RB, x1 - xb);
@@ -381,10 +382,38 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
           *reinterpret_cast<float4*>(Ss + r * C::SS + 4 * q) =
               reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)(xb + r) * D)[q];
         }
+        // G3 rows straight into the transposed [j3][b] layout
         for (int e = tid; e < nb * R; e += 256) {
-          const int r = e / R, q = e - r * R;
-          *reinterpret_cast<float4*>(G3s + r * C::GS + 4 * q) = __ldg(
-              reinterpret_cast<const float4*>(a.G3 + (size_t)a.w.row_i3[xb + r] * 4 * R) + q);
+          const int r = e / R, b = e - r * R;
+          const float4 v = __ldg(
+              reinterpret_cast<const float4*>(a.G3 + (size_t)a.w.row_i3[xb + r] * 4 * R) + b);
+          float* g = G3s + r * C::GS + b;
+          g[0] = v.x;
+          g[R] = v.y;
+          g[2 * R] = v.z;
+          g[3 * R] = v.w;
+        }
+        named_sync(1, 256);
+      } else {
+        // the staged G3 rows, in place from [b][j3] to [j3][b] (so that the dP2 tiles read
+        // 4 consecutive b per 128-bit load)
+        float4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = tid + 256 * q;
+          if (e < nb * R) v[q] = *reinterpret_cast<const float4*>(G3s + (e / R) * C::GS + 4 * (e % R));
+        }
+        named_sync(1, 256);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = tid + 256 * q;
+          if (e < nb * R) {
+            float* g = G3s + (e / R) * C::GS + (e % R);
+            g[0] = v[q].x;
+            g[R] = v[q].y;
+            g[2 * R] = v[q].z;
+            g[3 * R] = v[q].w;
+          }
         }
         named_sync(1, 256);
       }
@@ -451,19 +480,19 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
           for (int i = 0; i < 4; ++i)
             sv[i] = *reinterpret_cast<const float4*>(Ss + r * C::SS + (4 * jb + i) * 4);
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            gv[t] = *reinterpret_cast<const float4*>(G3s + r * C::GS + (4 * bq + t) * 4);
+          for (int j3 = 0; j3 < 4; ++j3)
+            gv[j3] = *reinterpret_cast<const float4*>(G3s + r * C::GS + j3 * R + 4 * bq);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 4; ++i) {
+            const float s4[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              float v = acc[i][t];
-              v = fmaf(sv[i].x, gv[t].x, v);
-              v = fmaf(sv[i].y, gv[t].y, v);
-              v = fmaf(sv[i].z, gv[t].z, v);
-              v = fmaf(sv[i].w, gv[t].w, v);
-              acc[i][t] = v;
+            for (int j3 = 0; j3 < 4; ++j3) {
+              acc[i][0] = fmaf(s4[j3], gv[j3].x, acc[i][0]);
+              acc[i][1] = fmaf(s4[j3], gv[j3].y, acc[i][1]);
+              acc[i][2] = fmaf(s4[j3], gv[j3].z, acc[i][2]);
+              acc[i][3] = fmaf(s4[j3], gv[j3].w, acc[i][3]);
             }
+          }
         }
         if (cur >= 0) {
           float* d = dP2 + cur * P2P + (4 * jb) * P2S + 4 * bq;

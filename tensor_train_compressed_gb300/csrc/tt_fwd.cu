@@ -175,7 +175,7 @@ struct WsCfg {
     int x0, x1, p0, np, end, pad[3];
     int rp[ROWMAX];                                   // prefix (chunk-local) of each staged row
   };
-  static constexpr int SMEM = 4 * (2 * STAGE_F + T::F_P2) + 2 * (int)sizeof(Meta) + 4 * 8;
+  static constexpr int SMEM = 4 * (2 * STAGE_F + T::F_P2 + F_P1) + 2 * (int)sizeof(Meta) + 4 * 8;
   static_assert(T::NB == 8, "one compute warp per j12 block");
   static_assert(ROWMAX <= 64 && CP <= 32, "the producer stages with two rows per lane");
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
   extern __shared__ float4 sm4[];
   float* base = reinterpret_cast<float*>(sm4);
   float* P2 = base + 2 * W::STAGE_F;
-  Meta* meta = reinterpret_cast<Meta*>(P2 + T::F_P2);
+  float* P1t = P2 + T::F_P2;
+  Meta* meta = reinterpret_cast<Meta*>(P1t + W::F_P1);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
   uint64_t* empty = full + 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -310,8 +311,7 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
     const float* G2s = base + s * W::STAGE_F;
     const float* P1n = G2s + T::F_G2;
     const float* G3s = P1n + W::F_P1;
-    stage2_natural<T>(G2s, P1n, P2, np);
-    named_sync(1, 256);
+    stage2_natural<T>(G2s, P1n, P1t, P2, np);
     const int rows = x1 - x0;
     const int blk = warp;
     for (int r = lane; r < rows; r += 32) {

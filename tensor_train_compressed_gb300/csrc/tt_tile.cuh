@@ -315,16 +315,33 @@ __device__ __forceinline__ void tiled_stage2_n(const float* __restrict__ G2s,
   }
 }
 
+// Stage 2 from G1 rows in natural layout P1n; for np >= 3 they are first
+// transposed into P1t ([p][a][j1], 4*R*np floats) so that the A operand of a
+// k step is one 128-bit broadcast load.  Ends with the 256 compute threads
+// synchronised (named barrier 1).
 template <class T>
 __device__ __forceinline__ void stage2_natural(const float* __restrict__ G2s,
                                                const float* __restrict__ P1n,
+                                               float* __restrict__ P1t,
                                                float* __restrict__ P2, int np) {
+  constexpr int R = T::kR;
   const int need = (np * T::NC + 255) / 256;    // column groups of 4 per thread for ~256 items
-  if (np == 1) tiled_stage2_splitk<T, 4>(G2s, P1n, P2, np, 256);
-  else if (np == 2) tiled_stage2_splitk<T, 2>(G2s, P1n, P2, np, 256);
-  else if (need <= 4) tiled_stage2_n<T, 4>(G2s, P1n, P2, np, 256);
-  else if (need <= 8) tiled_stage2_n<T, 8>(G2s, P1n, P2, np, 256);
-  else tiled_stage2_n<T, 16>(G2s, P1n, P2, np, 256);
+  if (np == 1) {
+    tiled_stage2_splitk<T, 4>(G2s, P1n, P2, np, 256);
+  } else if (np == 2) {
+    tiled_stage2_splitk<T, 2>(G2s, P1n, P2, np, 256);
+  } else {
+    for (int e = threadIdx.x; e < np * 4 * R; e += 256) {
+      const int p = e / (4 * R), rem = e - p * (4 * R);
+      const int j1 = rem / R, k = rem - j1 * R;
+      P1t[p * 4 * R + k * 4 + j1] = P1n[e];
+    }
+    named_sync(1, 256);
+    if (need <= 4) tiled_stage2<T, 4>(G2s, P1t, P2, np);
+    else if (need <= 8) tiled_stage2<T, 8>(G2s, P1t, P2, np);
+    else tiled_stage2<T, 16>(G2s, P1t, P2, np);
+  }
+  named_sync(1, 256);
 }
 
 }  // namespace tt
