@@ -246,9 +246,10 @@ struct BwsCfg {
   static constexpr int F_P1 = CP * 4 * R;             // natural [p][j1][a]
   static constexpr int STAGE_F = T::F_G2 + F_P1 + RB * (SS + GS);
   struct Meta {
-    int x0, x1, p0, np, end, nst, pad[2];
+    int x0, x1, p0, np, end, nst, i2, pad;
     int rp[RB];
     int ri3[RB];
+    int pi1[CP + (CP & 1)];   // even count keeps the barriers that follow 8-byte aligned
   };
   static constexpr int SMEM = 4 * (2 * STAGE_F + 2 * T::F_P2) + 2 * (int)sizeof(Meta) + 4 * 8;
   static_assert(RB * R <= 4 * 256, "in-place G3 transpose: 4 float4 per thread");
@@ -257,6 +258,51 @@ struct BwsCfg {
   static_assert(T::NB == 8 && 256 % TILES == 0 && RB % RG == 0, "mappings");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
+
+template <class T, class C, int SPLIT>
+__device__ __forceinline__ void bwd_dg3(const float* __restrict__ P2, const float* __restrict__ Ss,
+                                        const int* __restrict__ rp, const int* __restrict__ ri3,
+                                        float* __restrict__ dG3, int nb, int warp, int lane) {
+  constexpr int R = T::kR, NJ = 4 * T::kN2 / SPLIT;
+  const int r = lane / SPLIT, q = lane % SPLIT;
+  for (int bb = warp; bb < R / 4; bb += 8) {
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    if (r < nb) {
+      const float* pp = P2 + rp[r] * T::P2P + 4 * bb;
+      const float* ss = Ss + r * C::SS;
+#pragma unroll 8
+      for (int j12 = q * NJ; j12 < (q + 1) * NJ; ++j12) {
+        const float4 pv = *reinterpret_cast<const float4*>(pp + j12 * T::P2S);
+        const float4 sv = *reinterpret_cast<const float4*>(ss + 4 * j12);
+        const float pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[i][0] = fmaf(pw[i], sv.x, acc[i][0]);
+          acc[i][1] = fmaf(pw[i], sv.y, acc[i][1]);
+          acc[i][2] = fmaf(pw[i], sv.z, acc[i][2]);
+          acc[i][3] = fmaf(pw[i], sv.w, acc[i][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < SPLIT; o <<= 1)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], o);
+    if (r < nb) {
+      float4* dst = reinterpret_cast<float4*>(dG3 + ((size_t)ri3[r] * R + 4 * bb) * 4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (i % SPLIT == q)
+          atomicAdd(dst + i, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+    }
+  }
+}
 
 template <int N2, int R, int CP>
 __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
@@ -330,6 +376,7 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
         m.rp[lane] = rp;
         m.ri3[lane] = g3;
       }
+      if (lane < np) m.pi1[lane] = gi1;
       __syncwarp();
       if (lane == 0) {
         m.x0 = x0;
@@ -337,6 +384,7 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
         m.p0 = p0;
         m.np = np;
         m.nst = nst;
+        m.i2 = i2;
         m.end = 0;
         const uint32_t bytes = 4u * (T::F_G2 + np * 4 * R + nst * (D + 4 * R));
         mbar_arrive_expect_tx(&full[s], bytes);
@@ -417,43 +465,17 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
         }
         named_sync(1, 256);
       }
-      // dG3[i3][b][j3] += sum_j12 P2[j12][b] S[j12][j3]: lane = row, warp = block of 4 b
-      if (lane < nb) {
-        const int r = lane;
-        const float* ss = Ss + r * C::SS;
-        for (int bb = warp; bb < R / 4; bb += 8) {
-          const float* pp = P2 + m.rp[r] * P2P + 4 * bb;
-          float acc[4][4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 8
-          for (int j12 = 0; j12 < 4 * N2; ++j12) {
-            const float4 pv = *reinterpret_cast<const float4*>(pp + j12 * P2S);
-            const float4 sv = *reinterpret_cast<const float4*>(ss + 4 * j12);
-            const float pw[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              acc[i][0] = fmaf(pw[i], sv.x, acc[i][0]);
-              acc[i][1] = fmaf(pw[i], sv.y, acc[i][1]);
-              acc[i][2] = fmaf(pw[i], sv.z, acc[i][2]);
-              acc[i][3] = fmaf(pw[i], sv.w, acc[i][3]);
-            }
-          }
-          float4* dst = reinterpret_cast<float4*>(a.dG3 + ((size_t)m.ri3[r] * R + 4 * bb) * 4);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            atomicAdd(dst + i, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
-        }
-      }
+      // dG3[i3][b][j3] += sum_j12 P2[j12][b] S[j12][j3]: warp = block of 4 b, lane = row
+      // (batches of <= 16 / <= 8 rows: 2 / 4 lanes per row split the j12 sum)
+      if (nb <= 8) bwd_dg3<T, C, 4>(P2, Ss, m.rp, m.ri3, a.dG3, nb, warp, lane);
+      else if (nb <= 16) bwd_dg3<T, C, 2>(P2, Ss, m.rp, m.ri3, a.dG3, nb, warp, lane);
+      else bwd_dg3<T, C, 1>(P2, Ss, m.rp, m.ri3, a.dG3, nb, warp, lane);
       // dP2[p][j12][b] += sum_j3 S[j12][j3] G3[b][j3]: tile (4 j12 x 4 b) per thread,
       // row groups walk their rows and flush at every change of prefix
       {
         const int tile = tid % C::TILES, rg = tid / C::TILES;
         const int jb = tile / (R / 4), bq = tile - jb * (R / 4);
-        constexpr int RPG = C::RB / C::RG;
-        const int r0 = rg * RPG, r1 = min(r0 + RPG, nb);
+        const int r0 = (rg * nb) / C::RG, r1 = ((rg + 1) * nb) / C::RG;
         float acc[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -506,7 +528,7 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
     named_sync(1, 256);
     // dG2[i2][a][n] += sum_{p, j1} P1[p][j1][a] dP2[p][j1][n]: warp = block of 4 a,
     // lane = 4-column groups at stride 128
-    const int i2 = a.w.pair_i2[p0];
+    const int i2 = m.i2;
     {
       constexpr int Q = NC / 128;
       for (int ab = warp; ab < R / 4; ab += 8) {
@@ -596,7 +618,7 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
             acc[j1][i] = v;
           }
         if (valid && ns == 0) {
-          const int i1 = a.w.pair_i1[p0 + p];
+          const int i1 = m.pi1[p];
 #pragma unroll
           for (int j1 = 0; j1 < 4; ++j1)
             atomicAdd(reinterpret_cast<float4*>(a.dG1 + ((size_t)i1 * 4 + j1) * R + 4 * aq),

@@ -181,16 +181,17 @@ struct WsCfg {
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-template <class T, bool kGlobalG3>
+// acc[i][j3] = sum over b in [b0, b0 + NBV) of P2[j12 = 4 blk + i][b] G3[b][j3]
+template <class T, bool kGlobalG3, int NBV = T::kR>
 __device__ __forceinline__ void row_dot(const float* __restrict__ pp,
-                                        const float* __restrict__ gg, float acc[4][4]) {
-  constexpr int R = T::kR;
+                                        const float* __restrict__ gg, float acc[4][4],
+                                        int b0 = 0) {
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 #pragma unroll 2
-  for (int b = 0; b < R; b += 4) {
+  for (int b = b0; b < b0 + NBV; b += 4) {
     float4 pv[4], gv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) pv[i] = *reinterpret_cast<const float4*>(pp + i * T::P2S + b);
@@ -210,6 +211,37 @@ __device__ __forceinline__ void row_dot(const float* __restrict__ pp,
         acc[i][3] = fmaf(pw[t], gv[t].w, acc[i][3]);
       }
     }
+  }
+}
+
+template <class T, int SPLIT>
+__device__ __forceinline__ void stage3_split(const float* __restrict__ P2,
+                                             const float* __restrict__ G3s,
+                                             const int* __restrict__ rp, float* __restrict__ rowbuf,
+                                             int x0, int rows, int blk, int lane) {
+  constexpr int NBV = T::kR / SPLIT;
+  const int r = lane / SPLIT, q = lane % SPLIT;
+  float acc[4][4];
+  if (r < rows) {
+    const float* pp = P2 + rp[r] * T::P2P + (blk * 4) * T::P2S;
+    row_dot<T, false, NBV>(pp, G3s + r * T::G3S, acc, q * NBV);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  }
+#pragma unroll
+  for (int o = 1; o < SPLIT; o <<= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], o);
+  if (r < rows) {
+    float4* out = reinterpret_cast<float4*>(rowbuf + (size_t)(x0 + r) * T::D + blk * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i % SPLIT == q) out[i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
   }
 }
 
@@ -314,6 +346,11 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
     stage2_natural<T>(G2s, P1n, P1t, P2, np);
     const int rows = x1 - x0;
     const int blk = warp;
+    if (rows <= 16) {
+      // few rows: SPLIT lanes share a row, each over R/SPLIT of the b sum
+      if (rows <= 8) stage3_split<T, 4>(P2, G3s, m.rp, a.w.rowbuf, x0, rows, blk, lane);
+      else stage3_split<T, 2>(P2, G3s, m.rp, a.w.rowbuf, x0, rows, blk, lane);
+    } else
     for (int r = lane; r < rows; r += 32) {
       const int x = x0 + r;
       float acc[4][4];
