@@ -218,15 +218,13 @@ class Workload:
         self.ws_bytes = ws
 
     def step(self):
+        """forward, backward into the (zero) core gradients, SGD that also resets them"""
         t, x = self.tte, self.x
-        if self.train:
-            for g in self.grads:
-                g.zero_()
         t.tt_emb_forward(self.cores, x.m, x.n, x.R, self.idx, self.off, self.out, self.ws)
         if self.train:
             t.tt_emb_backward(self.gout, self.cores, x.m, x.n, x.R, self.idx, self.off,
                               self.grads, self.ws, reuse_grouping=True)
-            t.tt_emb_sgd(self.cores, self.grads, x.m, x.n, x.R, LR)
+            t.tt_emb_sgd(self.cores, self.grads, x.m, x.n, x.R, LR, zero_grads=True)
 
     def restore(self):
         for c, c0 in zip(self.cores, self.cores0):
@@ -360,12 +358,10 @@ def run_ours(args, rank, world, dist):
             idx_d.copy_(idx_h, non_blocking=True)
             off_d.copy_(off_h, non_blocking=True)
             g_d.copy_(g_h, non_blocking=True)
-            for gr in wl.grads:
-                gr.zero_()
             tte.tt_emb_forward(wl.cores, x.m, x.n, x.R, idx_d, off_d, wl.out, wl.ws)
             tte.tt_emb_backward(g_d, wl.cores, x.m, x.n, x.R, idx_d, off_d, wl.grads, wl.ws,
                                 reuse_grouping=True)
-            tte.tt_emb_sgd(wl.cores, wl.grads, x.m, x.n, x.R, LR)
+            tte.tt_emb_sgd(wl.cores, wl.grads, x.m, x.n, x.R, LR, zero_grads=True)
             out_h.copy_(wl.out, non_blocking=True)
             e1.record(stream)
         stream.synchronize()

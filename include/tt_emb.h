@@ -101,9 +101,11 @@ int tt_emb_backward(const float* grad_out, const float* const cores[3], const in
                     const int64_t* offsets, int64_t num_bags, float* const core_grads[3],
                     void* workspace, size_t ws_bytes, int reuse_grouping, void* stream);
 
-/* Plain SGD on the three cores: G_k <- G_k - lr * dG_k (element-wise, fp32). */
-int tt_emb_sgd(float* const cores[3], const float* const core_grads[3], const int64_t m[3],
-               const int32_t n[3], const int32_t R[4], float lr, void* stream);
+/* Plain SGD on the three cores, one launch: G_k <- G_k - lr * dG_k
+ * (element-wise, fp32).  With zero_grads != 0 the same pass also resets every
+ * dG_k to zero, ready for the next accumulating tt_emb_backward. */
+int tt_emb_sgd(float* const cores[3], float* const core_grads[3], const int64_t m[3],
+               const int32_t n[3], const int32_t R[4], float lr, int zero_grads, void* stream);
 
 /* Synchronises `stream`, then reads the workspace status word written by the
  * kernels of the calls enqueued so far.  *device_status receives the raw

@@ -101,8 +101,9 @@ class TTEmbeddingBag:
         for g in self.grads:
             g.zero_()
 
-    def sgd_step(self, lr: float, stream=None):
-        tt_emb_sgd(self.cores, self.grads, self.m, self.n, self.R, lr, stream)
+    def sgd_step(self, lr: float, zero_grads: bool = False, stream=None):
+        """G <- G - lr * dG; with zero_grads the gradients are reset in the same pass."""
+        tt_emb_sgd(self.cores, self.grads, self.m, self.n, self.R, lr, zero_grads, stream)
 
     def check(self, stream=None):
         """Raise TTEmbError if a kernel flagged bad input (synchronises)."""

@@ -65,7 +65,7 @@ def lib():
         L.tt_emb_group.argtypes = [P, P, P, P, I64, P, I64, P, SZ, P]
         L.tt_emb_forward.argtypes = [P, P, P, P, P, I64, P, I64, P, P, SZ, P]
         L.tt_emb_backward.argtypes = [P, P, P, P, P, P, I64, P, I64, P, P, SZ, ctypes.c_int, P]
-        L.tt_emb_sgd.argtypes = [P, P, P, P, P, ctypes.c_float, P]
+        L.tt_emb_sgd.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, P]
         L.tt_emb_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
         L.tt_emb_grouping_view.argtypes = [P, P, P, I64, I64, P, ctypes.POINTER(Grouping)]
         L.tt_emb_forward_static.argtypes = [P, P, P, P, P, I64, P, I64, P, P]
@@ -145,9 +145,10 @@ def tt_emb_backward(grad_out, cores, m, n, R, indices, offsets, core_grads, work
                                  int(bool(reuse_grouping)), _stream(stream)), "tt_emb_backward")
 
 
-def tt_emb_sgd(cores, core_grads, m, n, R, lr: float, stream=None):
+def tt_emb_sgd(cores, core_grads, m, n, R, lr: float, zero_grads: bool = False, stream=None):
     _check(lib().tt_emb_sgd(_ptrs3(cores, "cores"), _ptrs3(core_grads, "core_grads"),
-                            *_shape(m, n, R), ctypes.c_float(lr), _stream(stream)), "tt_emb_sgd")
+                            *_shape(m, n, R), ctypes.c_float(lr), int(bool(zero_grads)),
+                            _stream(stream)), "tt_emb_sgd")
 
 
 def tt_emb_get_error(workspace, stream=None) -> tuple[int, int]:

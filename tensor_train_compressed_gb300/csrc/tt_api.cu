@@ -88,6 +88,7 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
   L.chunk_start = take(sizeof(int32_t) * ((size_t)n + 1));
   L.chunk_desc = take(sizeof(int2) * ((size_t)n + 1));
   L.chunk_status = take(sizeof(uint32_t) * (size_t)L.n_scan_tiles);
+  L.coop = take(coop_scratch_bytes());
   L.rowbuf = take(sizeof(float) * (size_t)L.rowbuf_rows * (size_t)s.D);
   L.total = off;
   return L;
@@ -114,6 +115,7 @@ WS make_ws(void* base, const Layout& L) {
   w.chunk_start = reinterpret_cast<int32_t*>(b + L.chunk_start);
   w.chunk_desc = reinterpret_cast<int2*>(b + L.chunk_desc);
   w.chunk_status = reinterpret_cast<uint32_t*>(b + L.chunk_status);
+  w.coop = b + L.coop;
   w.rowbuf = reinterpret_cast<float*>(b + L.rowbuf);
   return w;
 }
@@ -231,8 +233,8 @@ int tt_emb_backward(const float* grad_out, const float* const cores[3], const in
   return launch_backward(s, L, w, grad_out, cores, offsets, nnz, num_bags, core_grads, st);
 }
 
-int tt_emb_sgd(float* const cores[3], const float* const core_grads[3], const int64_t m[3],
-               const int32_t n[3], const int32_t R[4], float lr, void* stream) {
+int tt_emb_sgd(float* const cores[3], float* const core_grads[3], const int64_t m[3],
+               const int32_t n[3], const int32_t R[4], float lr, int zero_grads, void* stream) {
   Shape s;
   int rc = shape_from_args(m, n, R, &s);
   if (rc) return rc;
@@ -240,7 +242,7 @@ int tt_emb_sgd(float* const cores[3], const float* const core_grads[3], const in
   if (rc) return rc;
   rc = check_cores(core_grads);
   if (rc) return rc;
-  return launch_sgd(cores, core_grads, s, lr, (cudaStream_t)stream);
+  return launch_sgd(cores, core_grads, s, lr, zero_grads, (cudaStream_t)stream);
 }
 
 int tt_emb_get_error(const void* workspace, void* stream, int* device_status) {

@@ -631,22 +631,41 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
   }
 }
 
-__global__ void k_sgd(float* __restrict__ G, const float* __restrict__ dG, int64_t count, float lr) {
+// G_k <- G_k - lr * dG_k for the three cores in one launch (float4 where the
+// segment allows), optionally resetting dG_k to zero in the same pass.
+struct SgdArgs {
+  float* G[3];
+  float* dG[3];
+  int64_t count[3];
+  int64_t start[4];   // prefix of the float4 counts of the segments
+  float lr;
+  int zero;
+};
+
+__global__ void __launch_bounds__(256) k_sgd(SgdArgs a) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t n4 = count >> 2;
-  float4* G4 = reinterpret_cast<float4*>(G);
-  const float4* d4 = reinterpret_cast<const float4*>(dG);
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    float4 g = G4[i];
-    const float4 d = d4[i];
-    g.x = fmaf(-lr, d.x, g.x);
-    g.y = fmaf(-lr, d.y, g.y);
-    g.z = fmaf(-lr, d.z, g.z);
-    g.w = fmaf(-lr, d.w, g.w);
-    G4[i] = g;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.start[3]; i += stride) {
+    const int k = i < a.start[1] ? 0 : (i < a.start[2] ? 1 : 2);
+    const int64_t e = (i - a.start[k]) * 4;
+    float* G = a.G[k];
+    float* dG = a.dG[k];
+    const int64_t n = a.count[k];
+    if (e + 4 <= n) {
+      float4 g = *reinterpret_cast<float4*>(G + e);
+      const float4 d = *reinterpret_cast<const float4*>(dG + e);
+      g.x = fmaf(-a.lr, d.x, g.x);
+      g.y = fmaf(-a.lr, d.y, g.y);
+      g.z = fmaf(-a.lr, d.z, g.z);
+      g.w = fmaf(-a.lr, d.w, g.w);
+      *reinterpret_cast<float4*>(G + e) = g;
+      if (a.zero) *reinterpret_cast<float4*>(dG + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      for (int64_t t = e; t < n; ++t) {
+        G[t] = fmaf(-a.lr, dG[t], G[t]);
+        if (a.zero) dG[t] = 0.f;
+      }
+    }
   }
-  for (int64_t i = (n4 << 2) + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride)
-    G[i] = fmaf(-lr, dG[i], G[i]);
 }
 
 static int persistent_grid_bwd(const void* fn, int threads, size_t smem) {
@@ -703,15 +722,23 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }
 
-int launch_sgd(float* const cores[3], const float* const grads[3], const Shape& s, float lr,
-               cudaStream_t st) {
+int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, float lr,
+               int zero_grads, cudaStream_t st) {
+  SgdArgs a;
   const int64_t counts[3] = {s.m1 * s.n1 * s.R1, s.m2 * s.R1 * s.n2 * s.R2, s.m3 * s.R2 * s.n3};
+  a.start[0] = 0;
   for (int k = 0; k < 3; ++k) {
-    int grid = (int)ceil_div(ceil_div(counts[k], 4), 256);
-    if (grid > sm_count() * 8) grid = sm_count() * 8;
-    if (grid < 1) grid = 1;
-    TT_TIMED("k_sgd", st, (k_sgd<<<grid, 256, 0, st>>>(cores[k], grads[k], counts[k], lr)));
+    a.G[k] = cores[k];
+    a.dG[k] = grads[k];
+    a.count[k] = counts[k];
+    a.start[k + 1] = a.start[k] + ceil_div(counts[k], 4);
   }
+  a.lr = lr;
+  a.zero = zero_grads ? 1 : 0;
+  int grid = (int)ceil_div(a.start[3], 256);
+  if (grid > sm_count() * 8) grid = sm_count() * 8;
+  if (grid < 1) grid = 1;
+  TT_TIMED("k_sgd", st, (k_sgd<<<grid, 256, 0, st>>>(a)));
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }
 

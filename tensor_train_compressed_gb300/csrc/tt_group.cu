@@ -382,6 +382,11 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
   // control block + digit histograms start from zero
   if (cudaMemsetAsync(w.ctl, 0, L.sort_status - L.ctl, st) != cudaSuccess) return TT_EMB_ERR_CUDA;
   if (nnz == 0) return TT_EMB_OK;   // counts stay zero; row_start etc. are never read
+  {
+    const int rc = launch_group_coop(s, L, w, w.coop, indices, nnz, offsets, num_bags,
+                                     pairs_per_chunk, rows_per_chunk, st);
+    if (rc != TT_EMB_ERR_UNSUPPORTED) return rc;
+  }
   const uint32_t sentinel = L.key_bits >= 32 ? 0xffffffffu : ((1u << L.key_bits) - 1u);
 
   PrepArgs pa;

@@ -64,7 +64,7 @@ struct Shape {
 struct Layout {
   size_t ctl, hist, sort_status, keysA, keysB, bag_of, uid, perm;
   size_t row_start, row_i3, row_pair, pair_row_start, pair_i1, pair_i2;
-  size_t seg_status, chunk_start, chunk_desc, chunk_status, rowbuf, total;
+  size_t seg_status, chunk_start, chunk_desc, chunk_status, coop, rowbuf, total;
   int key_bits, passes, n_sort_tiles, n_scan_tiles;
   int64_t rowbuf_rows;
 };
@@ -89,6 +89,7 @@ struct WS {
   int32_t* chunk_start;
   int2* chunk_desc;                 // [chunks+1] {first row, prefix | starts-a-prefix << 31}
   uint32_t* chunk_status;           // [n_scan_tiles]
+  void* coop;                       // scratch of the cooperative grouping
   float* rowbuf;                    // [rowbuf_rows][D]
 };
 
@@ -233,6 +234,11 @@ WS make_ws(void* base, const Layout& L);
 int shape_from_args(const int64_t m[3], const int32_t n[3], const int32_t R[4], Shape* s);
 int sm_count();
 
+// grouping in one cooperative launch (tt_group_coop.cu)
+size_t coop_scratch_bytes();
+int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratch,
+                      const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                      int64_t num_bags, int pairs_per_chunk, int rows_per_chunk, cudaStream_t st);
 // grouping (tt_group.cu)
 int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
@@ -246,7 +252,7 @@ int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chu
 int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out,
                     const float* const cores[3], const int64_t* offsets, int64_t nnz,
                     int64_t num_bags, float* const core_grads[3], cudaStream_t st);
-int launch_sgd(float* const cores[3], const float* const grads[3], const Shape& s, float lr,
-               cudaStream_t st);
+int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, float lr,
+               int zero_grads, cudaStream_t st);
 
 }  // namespace tt

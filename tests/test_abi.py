@@ -90,7 +90,7 @@ def test_forward_host_side_argument_checks(L):
     rc = L.tt_emb_backward(P(fake), cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, None,
                            P(fake), need, 1, None)
     assert rc == tte.TT_EMB_ERR_ARG      # null core_grads
-    rc = L.tt_emb_sgd(cores, None, *_shape(m, n, R), ctypes.c_float(0.1), None)
+    rc = L.tt_emb_sgd(cores, None, *_shape(m, n, R), ctypes.c_float(0.1), 0, None)
     assert rc == tte.TT_EMB_ERR_ARG
 
 

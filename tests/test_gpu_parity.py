@@ -144,6 +144,21 @@ def test_forward_full_size_sampled(cfg, table):
     assert g["U_r"] == ur and g["n_valid"] == x.nnz
 
 
+def test_large_batch_uses_the_multi_kernel_grouping():
+    """1.3M lookups exceed the register-resident cooperative grouping: the multi-kernel
+    grouping path must give the same bit-exact grouping and forward."""
+    x = make_custom((5, 6, 7), (4, 8, 4), (1, 32, 32, 1), num_bags=70000, max_len=36, seed=19)
+    assert x.nnz > 1_300_000
+    out, rc, _, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK
+    _check_grouping(x, st["ws"])
+    rng = np.random.default_rng(5)
+    bags = np.sort(rng.choice(x.num_bags, size=400, replace=False))
+    idx, off = _sample_bags(x, bags)
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, idx, off, threads=8)
+    assert np.abs(out[bags] - ref).max() <= FWD_TOL * max(np.abs(out).max(), np.abs(ref).max())
+
+
 def test_forward_is_deterministic():
     x = make_inputs(3, num_bags=2000)
     a, _, _, st = _gpu_forward(x)
@@ -235,12 +250,28 @@ def test_backward_config5_reduced_full_compare_and_sgd():
     for k in range(3):
         assert _rel_err(dG[k], dref[k]) <= BWD_TOL, k
     grads = [_dev(g) for g in dG]
-    tte.tt_emb_sgd(st["cores"], grads, x.m, x.n, x.R, 0.01)
+    tte.tt_emb_sgd(st["cores"], grads, x.m, x.n, x.R, 0.01, zero_grads=True)
     for k in range(3):
         upd = st["cores"][k].cpu().numpy().astype(np.float64)
         ref = oracle.sgd(x.cores[k], dref[k], 0.01)
         tol = 0.01 * BWD_TOL * np.abs(dref[k]).max() + 2e-7 * np.abs(ref).max()
         assert np.abs(upd - ref).max() <= tol, k
+        assert not grads[k].any(), k          # reset in the same pass
+
+
+def test_sgd_ragged_segments_without_reset():
+    """Core sizes that are not multiples of 4 exercise the scalar tails of the fused update."""
+    m, n, R = (3, 5, 7), (3, 1, 3), (1, 3, 5, 1)
+    x = make_custom(m, n, R, num_bags=1, max_len=1, seed=3)
+    cores = [_dev(c) for c in x.cores]
+    rng = np.random.default_rng(4)
+    dG = [rng.standard_normal(c.shape).astype(np.float32) for c in x.cores]
+    grads = [_dev(g) for g in dG]
+    tte.tt_emb_sgd(cores, grads, m, n, R, 0.25)
+    for k in range(3):
+        ref = oracle.sgd(x.cores[k], dG[k].astype(np.float64), 0.25)
+        assert np.abs(cores[k].cpu().numpy() - ref).max() <= 2e-7 * max(1.0, np.abs(ref).max())
+        assert np.array_equal(grads[k].cpu().numpy(), dG[k])
 
 
 @pytest.mark.parametrize("cfg", [5, 3])
