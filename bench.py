@@ -394,7 +394,22 @@ def run_ours(args, rank, world, dist):
                  "k_bwd_ws": a["bwd_contract"], "k_pool": a["pool"], "k_s_gather": a["s_gather"]}
         per_launch_ms = kms[dom] / max(1, launches_per_step[dom] / reps)
         out = {"kernel": dom, "share": round(kms[dom] / sum(kms.values()), 4)}
-        if dom in flops:
+        # algorithmic bytes of the non-contraction kernels (DRAM-level minimum)
+        nnz, B, D = a["nnz"], a["B"], r["wl"].x.D
+        npass = 3 if r["wl"].x.m[0] * r["wl"].x.m[1] * r["wl"].x.m[2] < (1 << 24) else 4
+        nbytes = {
+            "k_group_coop": 8 * nnz + 8 * (B + 1) + 16 * nnz * npass + 8 * nnz
+                            + 12 * a["U_r"] + 12 * a["U_12"],
+            "k_pool": 4 * nnz + 8 * (B + 1) + 4 * nnz * D + 4 * B * D,
+            "k_s_gather": 12 * nnz + 4 * nnz * D + 4 * a["U_r"] * D,
+        }
+        if dom in nbytes and dom not in flops:
+            ach = nbytes[dom] / (per_launch_ms * 1e-3) / 1e9
+            out.update(bound="hbm", achieved=round(ach, 1), peak=pk["hbm_gbs"], unit="GB/s",
+                       frac=round(ach / pk["hbm_gbs"], 4), traffic=None,
+                       algorithmic_bytes_per_launch=nbytes[dom],
+                       avg_launch_ms=round(per_launch_ms, 5))
+        elif dom in flops:
             ach = flops[dom] / (per_launch_ms * 1e-3) / 1e12
             out.update(bound="alu", achieved=round(ach, 3), peak=round(p_fp32, 2),
                        unit="TFLOP/s", frac=round(ach / p_fp32, 4), traffic=None,

@@ -37,8 +37,9 @@ struct CoopArgs {
   int L;                  // sorted positions per CTA segment
   int CP, CR;             // chunking parameters
   WS w;
-  uint32_t* counts;       // [kMaxPasses][G][kRadix] per-CTA digit counts
-  int2* seg_counts;       // [G] (rows, prefixes) per CTA
+  uint32_t* counts;       // [kMaxPasses][kRadix][Gp] per-CTA digit counts, Gp = G rounded to 4
+  int Gp;
+  int4* seg_counts;       // [G] (rows, prefixes, valid lookups, 0) per CTA
   int* chunk_counts;      // [G] chunk starts per CTA
 };
 
@@ -100,28 +101,29 @@ __device__ __forceinline__ uint32_t coop_scan(uint32_t v, uint32_t* total, uint3
   return pre + x - v;
 }
 
-// Sum over CTAs cc < c (pre) and over all CTAs (tot) of a per-CTA int2 count.
-__device__ __forceinline__ void cta_prefix2(const int2* cnt, int G, int c, int2* pre, int2* tot,
-                                            uint32_t* sm) {
-  uint32_t pr = 0, pp = 0, tr = 0, tp = 0;
-  for (int cc = threadIdx.x; cc < G; cc += kCoopThreads) {
-    const int2 v = __ldcg(cnt + cc);
-    tr += (uint32_t)v.x;
-    tp += (uint32_t)v.y;
-    if (cc < c) {
-      pr += (uint32_t)v.x;
-      pp += (uint32_t)v.y;
-    }
+// Block-wide sums of four uint32 per thread (kCoopThreads threads).
+__device__ __forceinline__ uint4 coop_sum4(uint4 v, uint4* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+    v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
   }
-  uint32_t t;
-  coop_scan(pr, &t, sm);
-  pre->x = (int)t;
-  coop_scan(pp, &t, sm);
-  pre->y = (int)t;
-  coop_scan(tr, &t, sm);
-  tot->x = (int)t;
-  coop_scan(tp, &t, sm);
-  tot->y = (int)t;
+  if (lane == 0) sm[warp] = v;
+  __syncthreads();
+  uint4 t = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int w = 0; w < kCoopWarps; ++w) {
+    const uint4 u = sm[w];
+    t.x += u.x;
+    t.y += u.y;
+    t.z += u.z;
+    t.w += u.w;
+  }
+  __syncthreads();
+  return t;
 }
 
 template <int ITEMS>
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
   __shared__ uint32_t red[4][kRadix];              // partial (pre, tot) of the two halves
   __shared__ uint32_t scan_sm[kCoopWarps];
   __shared__ int2 wcnt[kCoopWarps];                 // per-warp (rows, prefixes)
+  __shared__ uint4 sum_sm[kCoopWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x, G = gridDim.x;
@@ -173,8 +176,11 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     if (bad_off) set_status(a.w.ctl, kStOffsets);
     __syncthreads();
     for (int d = tid; d < kRadix; d += kCoopThreads) {
-      a.counts[(size_t)c * kRadix + d] = cnt0[d];
-      for (int p = 1; p < a.passes; ++p) a.counts[((size_t)p * G + c) * kRadix + d] = 0;
+      a.counts[(size_t)d * a.Gp + c] = cnt0[d];
+      for (int p = 1; p < a.passes; ++p) a.counts[((size_t)p * kRadix + d) * a.Gp + c] = 0;
+      if (c == 0)   // the padding columns stay zero
+        for (int p = 0; p < a.passes; ++p)
+          for (int cc = G; cc < a.Gp; ++cc) a.counts[((size_t)p * kRadix + d) * a.Gp + cc] = 0;
     }
   }
   grid_barrier(a.w.ctl);
@@ -191,17 +197,19 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       }
     }
     for (int i = tid; i < kCoopWarps * kRadix; i += kCoopThreads) (&whist[0][0])[i] = 0;
-    // partial sums over the CTAs of this pass's counts: two threads per digit
+    // partial sums over the CTAs of this pass's counts: two threads per digit, 128-bit loads
     {
       const int d = tid & (kRadix - 1), h = tid >> 8;
-      const uint32_t* col = a.counts + (size_t)p * G * kRadix + d;
-      const int c0 = h ? G / 2 : 0, c1 = h ? G : G / 2;
+      const uint4* row = reinterpret_cast<const uint4*>(a.counts + ((size_t)p * kRadix + d) * a.Gp);
+      const int q4 = a.Gp / 4, q0 = h ? q4 / 2 : 0, q1 = h ? q4 : q4 / 2;
       uint32_t pre = 0, tot = 0;
 #pragma unroll 8
-      for (int cc = c0; cc < c1; ++cc) {
-        const uint32_t v = __ldcg(col + (size_t)cc * kRadix);
-        tot += v;
-        pre += cc < c ? v : 0u;
+      for (int q = q0; q < q1; ++q) {
+        const uint4 v = __ldcg(row + q);
+        const int cc = 4 * q;
+        tot += v.x + v.y + v.z + v.w;
+        pre += (cc < c ? v.x : 0u) + (cc + 1 < c ? v.y : 0u) + (cc + 2 < c ? v.z : 0u) +
+               (cc + 3 < c ? v.w : 0u);
       }
       red[2 * h][d] = pre;
       red[2 * h + 1][d] = tot;
@@ -246,7 +254,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     }
     // scatter; count the next pass's digits by destination CTA
     const bool more = p + 1 < a.passes;
-    uint32_t* next = a.counts + (size_t)(p + 1) * G * kRadix;
+    uint32_t* next = a.counts + (size_t)(p + 1) * kRadix * a.Gp;
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
       const int64_t i = seg0 + warp * kSpan + it * 32 + lane;
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
         const uint32_t key = live && pos < (uint64_t)a.nnz ? (dc << 8) | d2 : 0xffffffffu;
         const uint32_t peers = __match_any_sync(0xffffffffu, key);
         if (key != 0xffffffffu && lane == __ffs(peers) - 1)
-          atomicAdd(&next[(size_t)dc * kRadix + d2], __popc(peers));
+          atomicAdd(&next[(size_t)d2 * a.Gp + dc], __popc(peers));
       }
     }
     src = dst;
@@ -276,7 +284,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
   const uint32_t m3 = (uint32_t)a.s.m3;
   uint32_t rbits[ITEMS], pbits[ITEMS];
   {
-    uint32_t wr = 0, wp = 0;
+    uint32_t wr = 0, wp = 0, wv_cnt = 0;
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
       const int64_t i = seg0 + warp * kSpan + it * 32 + lane;
@@ -292,23 +300,37 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       pbits[it] = __ballot_sync(0xffffffffu, pf);
       wr += __popc(rbits[it]);
       wp += __popc(pbits[it]);
+      wv_cnt += __popc(__ballot_sync(0xffffffffu, valid));
     }
     if (lane == 0) wcnt[warp] = make_int2((int)wr, (int)wp);
-    __syncthreads();
-    if (tid == 0) {
-      int tr = 0, tp = 0;
-      for (int w = 0; w < kCoopWarps; ++w) {
-        tr += wcnt[w].x;
-        tp += wcnt[w].y;
-      }
-      a.seg_counts[c] = make_int2(tr, tp);
-    }
+    const uint4 t = coop_sum4(make_uint4(lane == 0 ? wr : 0u, lane == 0 ? wp : 0u,
+                                         lane == 0 ? wv_cnt : 0u, 0u), sum_sm);
+    if (tid == 0) a.seg_counts[c] = make_int4((int)t.x, (int)t.y, (int)t.z, 0);
   }
   grid_barrier(a.w.ctl);
   {
-    int2 pre, tot;
-    cta_prefix2(a.seg_counts, G, c, &pre, &tot, scan_sm);
-    int rr = pre.x, pp = pre.y;          // runs before this warp's first position
+    uint4 mine_pre = make_uint4(0, 0, 0, 0), mine_tot = make_uint4(0, 0, 0, 0);
+    for (int cc = tid; cc < G; cc += kCoopThreads) {
+      const int4 v = __ldcg(a.seg_counts + cc);
+      mine_tot.x += v.x;
+      mine_tot.y += v.y;
+      mine_tot.z += v.z;
+      if (cc < c) {
+        mine_pre.x += v.x;
+        mine_pre.y += v.y;
+      }
+    }
+    const uint4 pre = coop_sum4(mine_pre, sum_sm);
+    const uint4 tot = coop_sum4(mine_tot, sum_sm);
+    const int64_t nv = (int64_t)tot.z;     // valid lookups (they sort first)
+    if (c == 0 && tid == 0) {
+      a.w.ctl->n_valid = (int32_t)nv;
+      a.w.ctl->U_r = (int32_t)tot.x;
+      a.w.ctl->U_12 = (int32_t)tot.y;
+      a.w.row_start[tot.x] = (int32_t)nv;
+      a.w.pair_row_start[tot.y] = (int32_t)tot.x;
+    }
+    int rr = (int)pre.x, pp = (int)pre.y;   // runs before this warp's first position
     for (int w = 0; w < warp; ++w) {
       rr += wcnt[w].x;
       pp += wcnt[w].y;
@@ -328,13 +350,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
         if ((uint64_t)(uint32_t)l < (uint64_t)a.nnz) {
           if (key >= M) {
             a.w.uid[l] = -1;
-            if (i == 0) {            // no valid lookup at all
-              a.w.ctl->n_valid = 0;
-              a.w.ctl->U_r = 0;
-              a.w.ctl->U_12 = 0;
-              a.w.row_start[0] = 0;
-              a.w.pair_row_start[0] = 0;
-            }
           } else {
             const uint32_t q = (uint32_t)key / m3;
             if (pf) {
@@ -349,14 +364,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
               a.w.row_pair[ri - 1] = pi - 1;
             }
             a.w.uid[l] = ri - 1;
-            const bool last = (i + 1 == a.nnz) || (__ldcg(sorted + i + 1) >> 32) >= M;
-            if (last) {
-              a.w.ctl->n_valid = (int32_t)(i + 1);
-              a.w.ctl->U_r = ri;
-              a.w.ctl->U_12 = pi;
-              a.w.row_start[ri] = (int32_t)(i + 1);
-              a.w.pair_row_start[pi] = ri;
-            }
           }
         }
       }
@@ -371,68 +378,55 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     const int U = __ldcg(&a.w.ctl->U_r);
     const int Lr = (U + G - 1) / G;
     const int x0 = c * Lr, x1 = min(x0 + Lr, U);
-    // Lr <= L <= kCoopThreads * ITEMS, so ITEMS rounds of the block cover a segment
-    uint32_t fl[ITEMS];
-    uint32_t mine = 0;
+    // each thread owns Rt consecutive rows of the CTA's range (Lr <= L <= 512 * ITEMS)
+    const int Rt = (Lr + kCoopThreads - 1) / kCoopThreads;
+    const int xt = x0 + tid * Rt;
+    uint32_t fl = 0, mine = 0;
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
-      const int x = x0 + k * kCoopThreads + tid;
+      const int x = xt + k;
       bool f = false;
-      if (x < x1) {
+      if (k < Rt && x < x1) {
         const int32_t p = __ldcg(a.w.row_pair + x);
         const int32_t f0 = __ldcg(a.w.pair_row_start + p);
         const int32_t nr = __ldcg(a.w.pair_row_start + p + 1) - f0;
-        if (x != f0) {
-          f = ((x - f0) % a.CR) == 0;
-        } else if (p == 0) {
-          f = true;
-        } else {
-          const int32_t pf = __ldcg(a.w.pair_row_start + p - 1);
-          f = (p % a.CP) == 0 || __ldcg(a.w.pair_i2 + p) != __ldcg(a.w.pair_i2 + p - 1) || nr > a.CR ||
-              (f0 - pf) > a.CR;
-        }
+        const int32_t pf = p > 0 ? __ldcg(a.w.pair_row_start + p - 1) : 0;
+        const int32_t i2 = __ldcg(a.w.pair_i2 + p);
+        const int32_t i2p = p > 0 ? __ldcg(a.w.pair_i2 + p - 1) : -1;
+        if (x != f0) f = ((x - f0) % a.CR) == 0;
+        else f = p == 0 || (p % a.CP) == 0 || i2 != i2p || nr > a.CR || (f0 - pf) > a.CR;
       }
-      fl[k] = f ? 1u : 0u;
-      mine += fl[k];
+      fl |= (f ? 1u : 0u) << k;
     }
+    mine = __popc(fl);
     uint32_t tot;
-    coop_scan(mine, &tot, scan_sm);
+    const uint32_t ex = coop_scan(mine, &tot, scan_sm);
     if (tid == 0) a.chunk_counts[c] = (int)tot;
     grid_barrier(a.w.ctl);
-    int2 pre2, tot2;
-    {
-      // reuse the int2 prefix helper with a zero second component
-      uint32_t pr = 0, tt = 0;
-      for (int cc = tid; cc < G; cc += kCoopThreads) {
-        const uint32_t v = (uint32_t)__ldcg(a.chunk_counts + cc);
-        tt += v;
-        if (cc < c) pr += v;
-      }
-      uint32_t t;
-      coop_scan(pr, &t, scan_sm);
-      pre2.x = (int)t;
-      coop_scan(tt, &t, scan_sm);
-      tot2.x = (int)t;
+    uint4 pr = make_uint4(0, 0, 0, 0);
+    for (int cc = tid; cc < G; cc += kCoopThreads) {
+      const uint32_t v = (uint32_t)__ldcg(a.chunk_counts + cc);
+      pr.y += v;
+      if (cc < c) pr.x += v;
     }
-    int base = pre2.x;
+    const uint4 ps = coop_sum4(pr, sum_sm);
+    int ci = (int)(ps.x + ex);
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
-      uint32_t t;
-      const uint32_t ex = coop_scan(fl[k], &t, scan_sm);
-      const int x = x0 + k * kCoopThreads + tid;
-      if (fl[k]) {
-        const int ci = base + (int)ex;
+      if ((fl >> k) & 1u) {
+        const int x = xt + k;
         const int32_t p = __ldcg(a.w.row_pair + x);
         const bool first = __ldcg(a.w.pair_row_start + p) == x;
         a.w.chunk_start[ci] = x;
         a.w.chunk_desc[ci] = make_int2(x, p | (first ? (int32_t)0x80000000 : 0));
+        ++ci;
       }
-      base += (int)t;
     }
     if (c == 0 && tid == 0) {
-      a.w.ctl->n_chunks = tot2.x;
-      a.w.chunk_start[tot2.x] = U;
-      a.w.chunk_desc[tot2.x] = make_int2(U, __ldcg(&a.w.ctl->U_12) | (int32_t)0x80000000);
+      const int n = (int)ps.y;
+      a.w.ctl->n_chunks = n;
+      a.w.chunk_start[n] = U;
+      a.w.chunk_desc[n] = make_int2(U, __ldcg(&a.w.ctl->U_12) | (int32_t)0x80000000);
     }
   }
 }
@@ -475,7 +469,7 @@ int coop_grid() {
 }
 
 size_t coop_scratch_bytes() {
-  return sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * kRadix + sizeof(int2) * kCoopMaxGrid +
+  return sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * kRadix + sizeof(int4) * kCoopMaxGrid +
          sizeof(int) * kCoopMaxGrid;
 }
 
@@ -487,7 +481,7 @@ int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratc
                       int64_t num_bags, int pairs_per_chunk, int rows_per_chunk,
                       cudaStream_t st) {
   const int G = coop_grid();
-  if (G < 2 || nnz <= 0) return TT_EMB_ERR_UNSUPPORTED;
+  if (G < 4 || G > kCoopMaxGrid || nnz <= 0) return TT_EMB_ERR_UNSUPPORTED;
   const int64_t Lseg = ceil_div(nnz, G);
   if (Lseg > (int64_t)kCoopThreads * kCoopItemsMax) return TT_EMB_ERR_UNSUPPORTED;
   CoopArgs ca;
@@ -503,12 +497,14 @@ int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratc
   ca.CR = rows_per_chunk;
   ca.w = w;
   char* sc = static_cast<char*>(scratch);
+  ca.Gp = (G + 3) & ~3;
   ca.counts = reinterpret_cast<uint32_t*>(sc);
-  ca.seg_counts = reinterpret_cast<int2*>(sc + sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * kRadix);
+  ca.seg_counts = reinterpret_cast<int4*>(sc + sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * kRadix);
   ca.chunk_counts = reinterpret_cast<int*>(reinterpret_cast<char*>(ca.seg_counts) +
-                                           sizeof(int2) * kCoopMaxGrid);
+                                           sizeof(int4) * kCoopMaxGrid);
   if (Lseg <= kCoopThreads * 4) return launch_coop_items<4>(ca, G, st);
   if (Lseg <= kCoopThreads * 8) return launch_coop_items<8>(ca, G, st);
+  if (Lseg <= kCoopThreads * 12) return launch_coop_items<12>(ca, G, st);
   return launch_coop_items<16>(ca, G, st);
 }
 
