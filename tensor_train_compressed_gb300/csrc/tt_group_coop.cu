@@ -41,6 +41,7 @@ struct CoopArgs {
   int Gp;
   int4* seg_counts;       // [G] (rows, prefixes, valid lookups, 0) per CTA
   int* chunk_counts;      // [G] chunk starts per CTA
+  uint32_t* bar;          // grid barrier words (zeroed before the launch)
 };
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
@@ -53,11 +54,14 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
 }
 
 // Sense-reversal grid barrier over the CTAs of a cooperative launch (capped).
-__device__ __forceinline__ void grid_barrier(Ctl* ctl) {
+// The arrival counter and the generation word sit in different 128-byte lines
+// (bar[0] and bar[32]) and waiters poll with a short sleep, so that the polling
+// does not queue in front of the arrivals.
+__device__ __forceinline__ void grid_barrier(uint32_t* bar, Ctl* ctl) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t* count = &ctl->pad[0];
-    uint32_t* gen = &ctl->pad[1];
+    uint32_t* count = bar;
+    uint32_t* gen = bar + 32;
     const uint32_t g = ld_acquire_u32(gen);
     __threadfence();
     if (atomicAdd(count, 1u) == gridDim.x - 1) {
@@ -66,7 +70,10 @@ __device__ __forceinline__ void grid_barrier(Ctl* ctl) {
       st_release_u32(gen, g + 1);
     } else {
       long long spins = 0;
+      unsigned ns = 32;
       while (ld_acquire_u32(gen) == g) {
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
         if (++spins > kSpinCap) {
           set_status(ctl, kStTimeout);
           break;
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
           for (int cc = G; cc < a.Gp; ++cc) a.counts[((size_t)p * kRadix + d) * a.Gp + cc] = 0;
     }
   }
-  grid_barrier(a.w.ctl);
+  grid_barrier(a.bar, a.w.ctl);
 
   // ------------------------------------------------------------------ radix passes
   const uint64_t* src = nullptr;
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       }
     }
     src = dst;
-    grid_barrier(a.w.ctl);
+    grid_barrier(a.bar, a.w.ctl);
   }
 
   // ------------------------------------------------------------------ segmentation
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
                                          lane == 0 ? wv_cnt : 0u, 0u), sum_sm);
     if (tid == 0) a.seg_counts[c] = make_int4((int)t.x, (int)t.y, (int)t.z, 0);
   }
-  grid_barrier(a.w.ctl);
+  grid_barrier(a.bar, a.w.ctl);
   {
     uint4 mine_pre = make_uint4(0, 0, 0, 0), mine_tot = make_uint4(0, 0, 0, 0);
     for (int cc = tid; cc < G; cc += kCoopThreads) {
@@ -371,7 +378,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       pp += __popc(pbits[it]);
     }
   }
-  grid_barrier(a.w.ctl);
+  grid_barrier(a.bar, a.w.ctl);
 
   // ------------------------------------------------------------------ chunks
   {
@@ -402,7 +409,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     uint32_t tot;
     const uint32_t ex = coop_scan(mine, &tot, scan_sm);
     if (tid == 0) a.chunk_counts[c] = (int)tot;
-    grid_barrier(a.w.ctl);
+    grid_barrier(a.bar, a.w.ctl);
     uint4 pr = make_uint4(0, 0, 0, 0);
     for (int cc = tid; cc < G; cc += kCoopThreads) {
       const uint32_t v = (uint32_t)__ldcg(a.chunk_counts + cc);
@@ -498,6 +505,9 @@ int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratc
   ca.w = w;
   char* sc = static_cast<char*>(scratch);
   ca.Gp = (G + 3) & ~3;
+  // barrier words inside the control block (zeroed by the grouping's memset): the
+  // counter at byte 100, the generation at byte 228 of the 256-byte block
+  ca.bar = &w.ctl->pad[12];
   ca.counts = reinterpret_cast<uint32_t*>(sc);
   ca.seg_counts = reinterpret_cast<int4*>(sc + sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * kRadix);
   ca.chunk_counts = reinterpret_cast<int*>(reinterpret_cast<char*>(ca.seg_counts) +
