@@ -42,7 +42,14 @@ struct CoopArgs {
   int4* seg_counts;       // [G] (rows, prefixes, valid lookups, 0) per CTA
   int* chunk_counts;      // [G] chunk starts per CTA
   uint32_t* bar;          // grid barrier words (zeroed before the launch)
+  unsigned long long* trace;   // [16] phase timestamps of CTA 0 (ns, %globaltimer)
 };
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
@@ -53,27 +60,43 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Sense-reversal grid barrier over the CTAs of a cooperative launch (capped).
-// The arrival counter and the generation word sit in different 128-byte lines
-// (bar[0] and bar[32]) and waiters poll with a short sleep, so that the polling
-// does not queue in front of the arrivals.
+// Two-level grid barrier over the CTAs of a cooperative launch (capped).  CTAs
+// arrive on one of kBarGroups counters (c % kBarGroups); the last arrival of a
+// group arrives on the top counter, and the last top arrival bumps the
+// generation word that everybody polls (with a short sleep).  Every word sits
+// in its own 128-byte line (bar[32 k]), so no address takes more than about
+// G / kBarGroups serialized arrivals.  `bar` must be zero before the launch.
+constexpr int kBarGroups = 16;
+
 __device__ __forceinline__ void grid_barrier(uint32_t* bar, Ctl* ctl) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t* count = bar;
-    uint32_t* gen = bar + 32;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int grp = c % kBarGroups;
+    const int ngroups = G < kBarGroups ? G : kBarGroups;
+    const int gsize = G / kBarGroups + (grp < G % kBarGroups ? 1 : 0);
+    uint32_t* sub = bar + 32 * grp;
+    uint32_t* top = bar + 32 * kBarGroups;
+    uint32_t* gen = bar + 32 * (kBarGroups + 1);
     const uint32_t g = ld_acquire_u32(gen);
     __threadfence();
-    if (atomicAdd(count, 1u) == gridDim.x - 1) {
-      *count = 0;
+    bool released = false;
+    if (atomicAdd(sub, 1u) == (uint32_t)gsize - 1) {
+      *sub = 0;
       __threadfence();
-      st_release_u32(gen, g + 1);
-    } else {
+      if (atomicAdd(top, 1u) == (uint32_t)ngroups - 1) {
+        *top = 0;
+        __threadfence();
+        st_release_u32(gen, g + 1);
+        released = true;
+      }
+    }
+    if (!released) {
       long long spins = 0;
       unsigned ns = 32;
       while (ld_acquire_u32(gen) == g) {
         __nanosleep(ns);
-        if (ns < 256) ns <<= 1;
+        if (ns < 128) ns <<= 1;
         if (++spins > kSpinCap) {
           set_status(ctl, kStTimeout);
           break;
@@ -143,6 +166,12 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x, G = gridDim.x;
+  int tstep = 0;
+  auto stamp = [&]() {
+    if (c == 0 && tid == 0 && tstep < 16) a.trace[tstep] = global_ns();
+    ++tstep;
+  };
+  stamp();
   const int64_t seg0 = (int64_t)c * a.L;
   const int64_t seg1 = seg0 + a.L < a.nnz ? seg0 + a.L : a.nnz;
   constexpr int kSpan = 32 * ITEMS;                // positions per warp
@@ -151,9 +180,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
 
   // ------------------------------------------------------------------ phase 0
   {
-    uint32_t* cnt0 = &red[0][0];
-    for (int i = tid; i < kRadix; i += kCoopThreads) cnt0[i] = 0;
-    __syncthreads();
     bool bad = false;
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
@@ -167,9 +193,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
         wv = ((uint64_t)key << 32) | (uint64_t)(uint32_t)i;
       }
       word[it] = wv;
-      const uint32_t d = i < seg1 ? (uint32_t)(wv >> 32) & (kRadix - 1) : 0x100u;
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (i < seg1 && lane == __ffs(peers) - 1) atomicAdd(&cnt0[d], __popc(peers));
     }
     if (bad) set_status(a.w.ctl, kStIndex);
     bool bad_off = false;
@@ -181,18 +204,14 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       if (b < a.B && a.offsets[b + 1] < v) bad_off = true;
     }
     if (bad_off) set_status(a.w.ctl, kStOffsets);
-    __syncthreads();
-    for (int d = tid; d < kRadix; d += kCoopThreads) {
-      a.counts[(size_t)d * a.Gp + c] = cnt0[d];
-      for (int p = 1; p < a.passes; ++p) a.counts[((size_t)p * kRadix + d) * a.Gp + c] = 0;
-      if (c == 0)   // the padding columns stay zero
-        for (int p = 0; p < a.passes; ++p)
-          for (int cc = G; cc < a.Gp; ++cc) a.counts[((size_t)p * kRadix + d) * a.Gp + cc] = 0;
-    }
+    if (c == 0)   // the padding columns of the counts stay zero
+      for (int e = tid; e < a.passes * kRadix; e += kCoopThreads)
+        for (int cc = G; cc < a.Gp; ++cc) a.counts[(size_t)e * a.Gp + cc] = 0;
   }
-  grid_barrier(a.bar, a.w.ctl);
 
   // ------------------------------------------------------------------ radix passes
+  // per pass: stable rank within the CTA -> this CTA's digit counts -> barrier ->
+  // CTA prefix and digit totals from all CTAs' counts -> scatter -> barrier
   const uint64_t* src = nullptr;
   for (int p = 0; p < a.passes; ++p) {
     uint64_t* dst = (p & 1) ? a.w.keysB : a.w.keysA;
@@ -204,25 +223,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       }
     }
     for (int i = tid; i < kCoopWarps * kRadix; i += kCoopThreads) (&whist[0][0])[i] = 0;
-    // partial sums over the CTAs of this pass's counts: two threads per digit, 128-bit loads
-    {
-      const int d = tid & (kRadix - 1), h = tid >> 8;
-      const uint4* row = reinterpret_cast<const uint4*>(a.counts + ((size_t)p * kRadix + d) * a.Gp);
-      const int q4 = a.Gp / 4, q0 = h ? q4 / 2 : 0, q1 = h ? q4 : q4 / 2;
-      uint32_t pre = 0, tot = 0;
-#pragma unroll 8
-      for (int q = q0; q < q1; ++q) {
-        const uint4 v = __ldcg(row + q);
-        const int cc = 4 * q;
-        tot += v.x + v.y + v.z + v.w;
-        pre += (cc < c ? v.x : 0u) + (cc + 1 < c ? v.y : 0u) + (cc + 2 < c ? v.z : 0u) +
-               (cc + 3 < c ? v.w : 0u);
-      }
-      red[2 * h][d] = pre;
-      red[2 * h + 1][d] = tot;
-    }
     __syncthreads();
-    // stable rank of each item among its warp's items with the same digit
     const int shift = 32 + kRadixBits * p;
     uint32_t rank[ITEMS];
 #pragma unroll
@@ -242,6 +243,33 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       __syncwarp();
     }
     __syncthreads();
+    uint32_t* cnt = a.counts + (size_t)p * kRadix * a.Gp;
+    if (tid < kRadix) {
+      uint32_t n = 0;
+#pragma unroll
+      for (int w = 0; w < kCoopWarps; ++w) n += whist[w][tid];
+      cnt[(size_t)tid * a.Gp + c] = n;
+    }
+    grid_barrier(a.bar, a.w.ctl);
+    stamp();
+    // CTA prefix and total of every digit: two threads per digit, 128-bit loads
+    {
+      const int d = tid & (kRadix - 1), h = tid >> 8;
+      const uint4* row = reinterpret_cast<const uint4*>(cnt + (size_t)d * a.Gp);
+      const int q4 = a.Gp / 4, q0 = h ? q4 / 2 : 0, q1 = h ? q4 : q4 / 2;
+      uint32_t pre = 0, tot = 0;
+#pragma unroll 8
+      for (int q = q0; q < q1; ++q) {
+        const uint4 v = __ldcg(row + q);
+        const int cc = 4 * q;
+        tot += v.x + v.y + v.z + v.w;
+        pre += (cc < c ? v.x : 0u) + (cc + 1 < c ? v.y : 0u) + (cc + 2 < c ? v.z : 0u) +
+               (cc + 3 < c ? v.w : 0u);
+      }
+      red[2 * h][d] = pre;
+      red[2 * h + 1][d] = tot;
+    }
+    __syncthreads();
     // absolute start of every (warp, digit): bucket base + CTA prefix + warp prefix
     {
       const uint32_t tot_d = tid < kRadix ? red[1][tid] + red[3][tid] : 0u;
@@ -259,30 +287,18 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       }
       __syncthreads();
     }
-    // scatter; count the next pass's digits by destination CTA
-    const bool more = p + 1 < a.passes;
-    uint32_t* next = a.counts + (size_t)(p + 1) * kRadix * a.Gp;
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
       const int64_t i = seg0 + warp * kSpan + it * 32 + lane;
-      const bool live = i < seg1;
-      uint32_t pos = 0;
-      if (live) {
+      if (i < seg1) {
         const uint32_t d = (uint32_t)(word[it] >> shift) & (kRadix - 1);
-        pos = whist[warp][d] + rank[it];
+        const uint32_t pos = whist[warp][d] + rank[it];
         if (pos < (uint64_t)a.nnz) dst[pos] = word[it];
-      }
-      if (more) {
-        const uint32_t d2 = (uint32_t)(word[it] >> (shift + kRadixBits)) & (kRadix - 1);
-        const uint32_t dc = pos / (uint32_t)a.L;
-        const uint32_t key = live && pos < (uint64_t)a.nnz ? (dc << 8) | d2 : 0xffffffffu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, key);
-        if (key != 0xffffffffu && lane == __ffs(peers) - 1)
-          atomicAdd(&next[(size_t)d2 * a.Gp + dc], __popc(peers));
       }
     }
     src = dst;
     grid_barrier(a.bar, a.w.ctl);
+    stamp();
   }
 
   // ------------------------------------------------------------------ segmentation
@@ -315,6 +331,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     if (tid == 0) a.seg_counts[c] = make_int4((int)t.x, (int)t.y, (int)t.z, 0);
   }
   grid_barrier(a.bar, a.w.ctl);
+  stamp();
   {
     uint4 mine_pre = make_uint4(0, 0, 0, 0), mine_tot = make_uint4(0, 0, 0, 0);
     for (int cc = tid; cc < G; cc += kCoopThreads) {
@@ -379,6 +396,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     }
   }
   grid_barrier(a.bar, a.w.ctl);
+  stamp();
 
   // ------------------------------------------------------------------ chunks
   {
@@ -410,6 +428,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     const uint32_t ex = coop_scan(mine, &tot, scan_sm);
     if (tid == 0) a.chunk_counts[c] = (int)tot;
     grid_barrier(a.bar, a.w.ctl);
+  stamp();
     uint4 pr = make_uint4(0, 0, 0, 0);
     for (int cc = tid; cc < G; cc += kCoopThreads) {
       const uint32_t v = (uint32_t)__ldcg(a.chunk_counts + cc);
@@ -429,6 +448,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
         ++ci;
       }
     }
+    stamp();
     if (c == 0 && tid == 0) {
       const int n = (int)ps.y;
       a.w.ctl->n_chunks = n;
@@ -477,7 +497,7 @@ int coop_grid() {
 
 size_t coop_scratch_bytes() {
   return sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * kRadix + sizeof(int4) * kCoopMaxGrid +
-         sizeof(int) * kCoopMaxGrid;
+         sizeof(int) * kCoopMaxGrid + 16 * sizeof(unsigned long long);
 }
 
 // Runs the whole grouping as one cooperative launch if the batch fits the
@@ -505,13 +525,14 @@ int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratc
   ca.w = w;
   char* sc = static_cast<char*>(scratch);
   ca.Gp = (G + 3) & ~3;
-  // barrier words inside the control block (zeroed by the grouping's memset): the
-  // counter at byte 100, the generation at byte 228 of the 256-byte block
-  ca.bar = &w.ctl->pad[12];
+  // barrier words: the digit-histogram area, zeroed by the grouping's memset and
+  // otherwise unused on this path (18 words 128 bytes apart = 2.3 KB)
+  ca.bar = w.hist;
   ca.counts = reinterpret_cast<uint32_t*>(sc);
   ca.seg_counts = reinterpret_cast<int4*>(sc + sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * kRadix);
   ca.chunk_counts = reinterpret_cast<int*>(reinterpret_cast<char*>(ca.seg_counts) +
                                            sizeof(int4) * kCoopMaxGrid);
+  ca.trace = reinterpret_cast<unsigned long long*>(ca.chunk_counts + kCoopMaxGrid);
   if (Lseg <= kCoopThreads * 4) return launch_coop_items<4>(ca, G, st);
   if (Lseg <= kCoopThreads * 8) return launch_coop_items<8>(ca, G, st);
   if (Lseg <= kCoopThreads * 12) return launch_coop_items<12>(ca, G, st);

@@ -50,7 +50,7 @@ struct Ctl {
   uint32_t chunk_tile_ctr;
   uint32_t fwd_chunk_ctr;
   uint32_t bwd_chunk_ctr;
-  uint32_t pad[51];       // pad[12] and pad[44]: grid barrier of the cooperative grouping
+  uint32_t pad[51];
 };
 static_assert(sizeof(Ctl) == 256, "control block is 256 bytes");
 
