@@ -89,7 +89,8 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
   L.chunk_desc = take(sizeof(int2) * ((size_t)n + 1));
   L.chunk_status = take(sizeof(uint32_t) * (size_t)L.n_scan_tiles);
   L.coop = take(coop_scratch_bytes());
-  L.rowbuf = take(sizeof(float) * (size_t)L.rowbuf_rows * (size_t)s.D);
+  // one extra row, kept at zero, that out-of-range lookups point at while pooling
+  L.rowbuf = take(sizeof(float) * ((size_t)L.rowbuf_rows + 1) * (size_t)s.D);
   L.total = off;
   return L;
 }

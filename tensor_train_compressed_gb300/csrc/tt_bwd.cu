@@ -132,8 +132,17 @@ __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict_
 // k_s_zero) when the row also crosses the CTA's range.  D % 4 == 0.
 constexpr int kSCta = 8 * kSSlice;
 
+__device__ __forceinline__ void s_merge_flush(const WS& w, int32_t u, int64_t K0, const float4& m,
+                                              int lane) {
+  const int32_t s0 = w.row_start[u], s1 = w.row_start[u + 1];
+  float4* dst = reinterpret_cast<float4*>(w.rowbuf) + (int64_t)u * 32 + lane;
+  if (s0 < K0 || s1 > K0 + kSCta) atomicAdd(dst, m);
+  else *dst = m;
+}
+
+// D = 128: every lane owns one float4 column of the rows.
 __global__ void __launch_bounds__(256) k_s_gather_cta(WS w, const float* __restrict__ grad_out,
-                                                      int64_t B, int D) {
+                                                      int64_t B) {
   __shared__ float4 part[8][2][32];
   __shared__ int part_u[8][2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -143,98 +152,88 @@ __global__ void __launch_bounds__(256) k_s_gather_cta(WS w, const float* __restr
   const int64_t K1 = K0 + kSCta < nv ? K0 + kSCta : nv;
   const int64_t k0 = K0 + (int64_t)warp * kSSlice;
   const int64_t k1 = k0 + kSSlice < K1 ? k0 + kSSlice : K1;
-  const int cols = D >> 2;
+  const float4* g4 = reinterpret_cast<const float4*>(grad_out);
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < cols; c0 += 32) {
-    const int c = c0 + lane;
-    const bool live = c < cols;
-    float4 acc = z4;
-    int32_t cur = -1, first_u = -1;
-    bool first_open = true;                            // the warp's first run is still open
-    if (lane < 2) part_u[warp][lane] = -1;
-    for (int64_t kb = k0; kb < k1; kb += 32) {
-      const int cnt = (int)(k1 - kb < 32 ? k1 - kb : 32);
-      int32_t my_u = -1, my_b = 0;
-      if (lane < cnt) {
-        const int32_t l = w.perm[kb + lane];
-        my_u = w.uid[l];
-        const int32_t bb = w.bag_of[l];
-        my_b = bb < 0 ? 0 : (bb >= B ? (int32_t)(B - 1) : bb);
-      }
-      for (int j = 0; j < cnt; j += 8) {
-        int32_t uj[8];
-        float4 g[8];
+  float4 acc = z4;
+  int32_t cur = -1, first_u = -1;
+  bool first_open = true;                              // the warp's first run is still open
+  if (lane < 2) part_u[warp][lane] = -1;
+  auto close_run = [&]() {
+    if (cur < 0) return;
+    if (first_open) {                                  // the first run: keep for the merge
+      part[warp][0][lane] = acc;
+      first_u = cur;
+      first_open = false;
+    } else {                                           // a run inside the warp's range
+      reinterpret_cast<float4*>(w.rowbuf)[(int64_t)cur * 32 + lane] = acc;
+    }
+  };
+  for (int64_t kb = k0; kb < k1; kb += 32) {
+    const int cnt = (int)(k1 - kb < 32 ? k1 - kb : 32);
+    int32_t my_u = -1, my_b = 0;
+    if (lane < cnt) {
+      const int32_t l = w.perm[kb + lane];
+      my_u = w.uid[l];
+      const int32_t bb = w.bag_of[l];
+      my_b = bb < 0 ? 0 : (bb >= B ? (int32_t)(B - 1) : bb);
+    }
+    int j = 0;
+    for (; j + 8 <= cnt; j += 8) {
+      int32_t uj[8];
+      float4 g[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int jj = (j + t) & 31;
-          uj[t] = __shfl_sync(0xffffffffu, my_u, jj);
-          const int32_t bj = __shfl_sync(0xffffffffu, my_b, jj);
-          g[t] = (live && (j + t) < cnt)
-                     ? __ldg(reinterpret_cast<const float4*>(grad_out + bj * (int64_t)D) + c)
-                     : z4;
-        }
+      for (int t = 0; t < 8; ++t) {
+        uj[t] = __shfl_sync(0xffffffffu, my_u, j + t);
+        g[t] = __ldg(g4 + (int64_t)__shfl_sync(0xffffffffu, my_b, j + t) * 32 + lane);
+      }
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (j + t >= cnt) break;
-          if (uj[t] != cur) {
-            if (cur >= 0) {
-              if (first_open) {                        // the first run: keep for the merge
-                if (live) part[warp][0][lane] = acc;
-                first_u = cur;
-                first_open = false;
-              } else if (live) {                       // a run inside the warp's range
-                reinterpret_cast<float4*>(w.rowbuf + cur * (int64_t)D)[c] = acc;
-              }
-            }
-            acc = z4;
-            cur = uj[t];
-          }
-          acc.x += g[t].x; acc.y += g[t].y; acc.z += g[t].z; acc.w += g[t].w;
+      for (int t = 0; t < 8; ++t) {
+        if (uj[t] != cur) {
+          close_run();
+          acc = z4;
+          cur = uj[t];
         }
+        f4add(acc, g[t]);
       }
     }
-    // the last run (or the only one)
-    if (cur >= 0) {
-      if (first_open) {
-        if (live) part[warp][0][lane] = acc;
-        first_u = cur;
-      } else {
-        if (live) part[warp][1][lane] = acc;
-        if (lane == 0) part_u[warp][1] = cur;
+    for (; j < cnt; ++j) {
+      const int32_t u = __shfl_sync(0xffffffffu, my_u, j);
+      const float4 g = __ldg(g4 + (int64_t)__shfl_sync(0xffffffffu, my_b, j) * 32 + lane);
+      if (u != cur) {
+        close_run();
+        acc = z4;
+        cur = u;
       }
+      f4add(acc, g);
     }
-    if (lane == 0) part_u[warp][0] = first_u;
-    __syncthreads();
-    if (warp == 0) {
-      int32_t mu = -1;
-      float4 m = z4;
-      for (int ww = 0; ww < 8; ++ww)
-        for (int e = 0; e < 2; ++e) {
-          const int32_t u = part_u[ww][e];
-          if (u < 0) continue;
-          if (u != mu) {
-            if (mu >= 0 && live) {
-              const int32_t s0 = w.row_start[mu], s1 = w.row_start[mu + 1];
-              float4* dst = reinterpret_cast<float4*>(w.rowbuf + mu * (int64_t)D) + c;
-              if (s0 < K0 || s1 > K0 + kSCta) atomicAdd(dst, m);
-              else *dst = m;
-            }
-            mu = u;
-            m = z4;
-          }
-          if (live) {
-            const float4 v = part[ww][e][lane];
-            m.x += v.x; m.y += v.y; m.z += v.z; m.w += v.w;
-          }
+  }
+  // the last run (or the only one)
+  if (cur >= 0) {
+    if (first_open) {
+      part[warp][0][lane] = acc;
+      first_u = cur;
+    } else {
+      part[warp][1][lane] = acc;
+      if (lane == 0) part_u[warp][1] = cur;
+    }
+  }
+  if (lane == 0) part_u[warp][0] = first_u;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t mu = -1;
+    float4 m = z4;
+    for (int ww = 0; ww < 8; ++ww)
+      for (int e = 0; e < 2; ++e) {
+        const int32_t u = part_u[ww][e];
+        if (u < 0) continue;
+        if (u != mu) {
+          if (mu >= 0) s_merge_flush(w, mu, K0, m, lane);
+          mu = u;
+          m = z4;
         }
-      if (mu >= 0 && live) {
-        const int32_t s0 = w.row_start[mu], s1 = w.row_start[mu + 1];
-        float4* dst = reinterpret_cast<float4*>(w.rowbuf + mu * (int64_t)D) + c;
-        if (s0 < K0 || s1 > K0 + kSCta) atomicAdd(dst, m);
-        else *dst = m;
+        f4add(m, part[ww][e][lane]);
       }
-    }
-    __syncthreads();
+    if (mu >= 0) s_merge_flush(w, mu, K0, m, lane);
   }
 }
 
@@ -799,13 +798,13 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   int grid = (int)ceil_div(L.rowbuf_rows > num_bags ? L.rowbuf_rows : num_bags, 8);
   if (grid > sms * 16) grid = sms * 16;
   if (grid < 1) grid = 1;
-  const bool cta_gather = (s.D & 3) == 0;
+  const bool cta_gather = s.D == 128;
   TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D, offsets, num_bags, nnz,
                                                              cta_gather ? kSCta : kSSlice)));
   const int64_t slices = ceil_div(nnz, kSSlice);
   if (cta_gather) {
     TT_TIMED("k_s_gather", st, (k_s_gather_cta<<<(int)ceil_div(nnz, kSCta), 256, 0, st>>>(
-                                   w, grad_out, num_bags, s.D)));
+                                   w, grad_out, num_bags)));
   } else {
     TT_TIMED("k_s_gather", st, (k_s_gather<<<(int)ceil_div(slices, 8), 256, 0, st>>>(w, grad_out, num_bags, s.D)));
   }

@@ -373,9 +373,6 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
 // out[b] = sum of the unique rows of bag b's lookups; one warp per bag.  The
 // lanes fetch up to 32 of the bag's unique-row ids at once; each lane then sums
 // its float4 column of those rows, 8 loads in flight.
-__device__ __forceinline__ void f4add(float4& a, const float4& b) {
-  a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-}
 
 __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offsets, int64_t B,
                                               int64_t nnz, const int32_t* __restrict__ uid,
@@ -426,6 +423,38 @@ __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offset
         out[b * (int64_t)D + j] = acc;
       }
     }
+  }
+}
+
+// Pooling for D = 128: every lane owns one float4 column, so the inner loop
+// needs no column checks; lookups with an out-of-range index point at the zero
+// row `zrow`; full batches of 8 row loads run unpredicated.
+__global__ void __launch_bounds__(256) k_pool128(const int64_t* __restrict__ offsets, int64_t B,
+                                                 int64_t nnz, const int32_t* __restrict__ uid,
+                                                 const float4* __restrict__ rb4, int32_t zrow,
+                                                 float4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < B; b += warps) {
+    int64_t l0 = offsets[b], l1 = offsets[b + 1];
+    l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
+    l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t lb = l0; lb < l1; lb += 32) {
+      const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
+      int32_t my_u = lane < cnt ? uid[lb + lane] : zrow;
+      my_u = my_u < 0 ? zrow : my_u;
+      int j = 0;
+      for (; j + 8 <= cnt; j += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) v[t] = rb4[(int64_t)__shfl_sync(0xffffffffu, my_u, j + t) * 32 + lane];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) f4add(acc, v[t]);
+      }
+      for (; j < cnt; ++j) f4add(acc, rb4[(int64_t)__shfl_sync(0xffffffffu, my_u, j) * 32 + lane]);
+    }
+    out[b * 32 + lane] = acc;
   }
 }
 
@@ -498,7 +527,6 @@ static void launch_tiled(const FwdArgs& fa, cudaStream_t st) {
 int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* const cores[3],
                    const int64_t* offsets, int64_t nnz, int64_t num_bags, float* out,
                    cudaStream_t st) {
-  (void)L;
   int CP = 0, CR = 0;
   int rc = forward_chunk_params(s, &CP, &CR);
   if (rc) return rc;
@@ -527,7 +555,13 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
     int grid = (int)ceil_div(num_bags, 8);
     const int cap = sm_count() * 16;
     if (grid > cap) grid = cap;
-    TT_TIMED("k_pool", st, (k_pool<<<grid, 256, 0, st>>>(offsets, num_bags, nnz, w.uid, w.rowbuf, s.D, out)));
+    if (s.D == 128) {
+      TT_TIMED("k_pool", st, (k_pool128<<<grid, 256, 0, st>>>(
+                                 offsets, num_bags, nnz, w.uid, reinterpret_cast<const float4*>(w.rowbuf),
+                                 (int32_t)L.rowbuf_rows, reinterpret_cast<float4*>(out))));
+    } else {
+      TT_TIMED("k_pool", st, (k_pool<<<grid, 256, 0, st>>>(offsets, num_bags, nnz, w.uid, w.rowbuf, s.D, out)));
+    }
   }
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }

@@ -381,6 +381,10 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
                  int rows_per_chunk, cudaStream_t st) {
   // control block + digit histograms start from zero
   if (cudaMemsetAsync(w.ctl, 0, L.sort_status - L.ctl, st) != cudaSuccess) return TT_EMB_ERR_CUDA;
+  // the zero row after the unique rows (pooling points out-of-range lookups at it)
+  if (cudaMemsetAsync(w.rowbuf + (size_t)L.rowbuf_rows * s.D, 0, sizeof(float) * (size_t)s.D, st) !=
+      cudaSuccess)
+    return TT_EMB_ERR_CUDA;
   if (nnz == 0) return TT_EMB_OK;   // counts stay zero; row_start etc. are never read
   {
     const int rc = launch_group_coop(s, L, w, w.coop, indices, nnz, offsets, num_bags,

@@ -90,7 +90,7 @@ struct WS {
   int2* chunk_desc;                 // [chunks+1] {first row, prefix | starts-a-prefix << 31}
   uint32_t* chunk_status;           // [n_scan_tiles]
   void* coop;                       // scratch of the cooperative grouping
-  float* rowbuf;                    // [rowbuf_rows][D]
+  float* rowbuf;                    // [rowbuf_rows + 1][D]; the last row stays zero
 };
 
 // ---------------------------------------------------------------- device helpers
@@ -119,6 +119,13 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 __device__ __forceinline__ void set_status(Ctl* ctl, uint32_t bit) { atomicOr(&ctl->status, bit); }
+
+__device__ __forceinline__ void f4add(float4& a, const float4& b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
 
 // Grouping key of an in-range row index (r < M <= 2^32 - 2, so 32-bit
 // arithmetic is exact): (i2, i1, i3) with i3 least significant, so that unique
