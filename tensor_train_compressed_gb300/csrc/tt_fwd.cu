@@ -164,9 +164,10 @@ __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_til
 // completing on that buffer's "full" mbarrier.  Warps 0-7 consume: stage 2
 // (P2 in shared memory), stage 3 (rows), then release the buffer through its
 // "empty" mbarrier.  Staging of chunk i+1 thus overlaps the math of chunk i.
-template <int N2, int R, int CP>
+template <int N2, int R, int CP, int GROUPS = 1>
 struct WsCfg {
   using T = TileCfg<N2, R, CP>;
+  static constexpr int THREADS = GROUPS * 256 + 32;
   static constexpr int ROWMAX = 64;
   static constexpr int F_P1 = CP * 4 * R;            // G1 rows, natural [p][j1][a]
   static constexpr int F_G3 = ROWMAX * T::G3S;
@@ -175,8 +176,10 @@ struct WsCfg {
     int x0, x1, p0, np, end, pad[3];
     int rp[ROWMAX];                                   // prefix (chunk-local) of each staged row
   };
-  static constexpr int SMEM = 4 * (2 * STAGE_F + T::F_P2 + F_P1) + 2 * (int)sizeof(Meta) + 4 * 8;
+  static constexpr int SMEM =
+      4 * (2 * STAGE_F + GROUPS * (T::F_P2 + F_P1)) + 2 * (int)sizeof(Meta) + 4 * 8;
   static_assert(T::NB == 8, "one compute warp per j12 block");
+  static_assert(GROUPS == 1 || GROUPS == 2, "one or two consumer groups");
   static_assert(ROWMAX <= 64 && CP <= 32, "the producer stages with two rows per lane");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -245,16 +248,19 @@ __device__ __forceinline__ void stage3_split(const float* __restrict__ P2,
   }
 }
 
-template <int N2, int R, int CP>
-__global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
-  using W = WsCfg<N2, R, CP>;
+// With GROUPS = 2 there are two consumer groups of 8 warps: group g owns stage
+// buffer g (and its own P2), so the producer's stages alternate between the
+// groups and two chunks are in flight per SM.
+template <int N2, int R, int CP, int GROUPS>
+__global__ void __launch_bounds__(WsCfg<N2, R, CP, GROUPS>::THREADS, 1) k_fwd_ws(FwdArgs a) {
+  using W = WsCfg<N2, R, CP, GROUPS>;
   using T = typename W::T;
   using Meta = typename W::Meta;
   extern __shared__ float4 sm4[];
   float* base = reinterpret_cast<float*>(sm4);
-  float* P2 = base + 2 * W::STAGE_F;
-  float* P1t = P2 + T::F_P2;
-  Meta* meta = reinterpret_cast<Meta*>(P1t + W::F_P1);
+  float* P2all = base + 2 * W::STAGE_F;
+  float* P1tall = P2all + GROUPS * T::F_P2;
+  Meta* meta = reinterpret_cast<Meta*>(P1tall + GROUPS * W::F_P1);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
   uint64_t* empty = full + 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -268,9 +274,18 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
   __syncthreads();
   const int n_chunks = a.w.ctl->n_chunks;
 
-  if (warp == 8) {
+  if (warp == 8 * GROUPS) {
     // ---------------- producer: claims one chunk ahead, so that the claim and
     // the descriptor load of chunk i+1 overlap the staging of chunk i
+    auto end_stage = [&](int it) {          // end marker into the stage of iteration it
+      const int s = it & 1;
+      const uint32_t use = (uint32_t)it >> 1;
+      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) return;
+      if (lane == 0) {
+        meta[s].end = 1;
+        mbar_arrive(&full[s]);
+      }
+    };
     int c = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
     ChunkDesc d{};
     if (c < n_chunks) d = load_chunk(a.w.chunk_desc, c);
@@ -279,11 +294,8 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
       const uint32_t use = (uint32_t)it >> 1;
       Meta& m = meta[s];
       if (c >= n_chunks) {
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
-        if (lane == 0) {
-          m.end = 1;
-          mbar_arrive(&full[s]);
-        }
+        end_stage(it);
+        if (GROUPS == 2) end_stage(it + 1);   // the other group's stage too
         break;
       }
       const int x0 = d.x0, x1 = d.x1, p0 = d.p0;
@@ -333,40 +345,46 @@ __global__ void __launch_bounds__(288, 1) k_fwd_ws(FwdArgs a) {
     return;
   }
 
-  // ---------------- consumers (warps 0-7)
-  for (int it = 0;; ++it) {
-    const int s = it & 1;
-    if (!mbar_wait(&full[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
+  // ---------------- consumers: group g = warps 8g .. 8g+7
+  const int g = warp >> 3, ltid = tid - 256 * g, blk = warp & 7;
+  const int bar_id = 1 + g;
+  float* P2 = P2all + g * T::F_P2;
+  float* P1t = P1tall + g * W::F_P1;
+  for (int k = 0;; ++k) {
+    // GROUPS == 1: both stages in turn; GROUPS == 2: stage g only
+    const int s = GROUPS == 1 ? (k & 1) : g;
+    const uint32_t parity = GROUPS == 1 ? (((uint32_t)k >> 1) & 1) : ((uint32_t)k & 1);
+    if (!mbar_wait(&full[s], parity, a.w.ctl)) break;
     const Meta& m = meta[s];
     if (m.end) break;
     const int x0 = m.x0, x1 = m.x1, p0 = m.p0, np = m.np;
     const float* G2s = base + s * W::STAGE_F;
     const float* P1n = G2s + T::F_G2;
     const float* G3s = P1n + W::F_P1;
-    stage2_natural<T>(G2s, P1n, P1t, P2, np);
+    stage2_natural<T>(G2s, P1n, P1t, P2, np, ltid, bar_id);
     const int rows = x1 - x0;
-    const int blk = warp;
     if (rows <= 16) {
       // few rows: SPLIT lanes share a row, each over R/SPLIT of the b sum
       if (rows <= 8) stage3_split<T, 4>(P2, G3s, m.rp, a.w.rowbuf, x0, rows, blk, lane);
       else stage3_split<T, 2>(P2, G3s, m.rp, a.w.rowbuf, x0, rows, blk, lane);
-    } else
-    for (int r = lane; r < rows; r += 32) {
-      const int x = x0 + r;
-      float acc[4][4];
-      if (r < W::ROWMAX) {
-        const float* pp = P2 + m.rp[r] * T::P2P + (blk * 4) * T::P2S;
-        row_dot<T, false>(pp, G3s + r * T::G3S, acc);
-      } else {
-        const float* pp = P2 + (a.w.row_pair[x] - p0) * T::P2P + (blk * 4) * T::P2S;
-        row_dot<T, true>(pp, a.G3 + (size_t)a.w.row_i3[x] * 4 * R, acc);
-      }
-      float4* o = reinterpret_cast<float4*>(a.w.rowbuf + (size_t)x * T::D + blk * 16);
+    } else {
+      for (int r = lane; r < rows; r += 32) {
+        const int x = x0 + r;
+        float acc[4][4];
+        if (r < W::ROWMAX) {
+          const float* pp = P2 + m.rp[r] * T::P2P + (blk * 4) * T::P2S;
+          row_dot<T, false>(pp, G3s + r * T::G3S, acc);
+        } else {
+          const float* pp = P2 + (a.w.row_pair[x] - p0) * T::P2P + (blk * 4) * T::P2S;
+          row_dot<T, true>(pp, a.G3 + (size_t)a.w.row_i3[x] * 4 * R, acc);
+        }
+        float4* o = reinterpret_cast<float4*>(a.w.rowbuf + (size_t)x * T::D + blk * 16);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        for (int i = 0; i < 4; ++i) o[i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      }
     }
-    named_sync(1, 256);
-    if (tid == 0) mbar_arrive(&empty[s]);
+    named_sync(bar_id, 256);
+    if (ltid == 0) mbar_arrive(&empty[s]);
   }
 }
 
@@ -500,16 +518,16 @@ static int persistent_grid(const void* fn, int threads, size_t smem) {
   return per_sm * sm_count();
 }
 
-template <int N2, int R, int CP>
+template <int N2, int R, int CP, int GROUPS>
 static void launch_ws(const FwdArgs& fa, cudaStream_t st) {
-  using W = WsCfg<N2, R, CP>;
+  using W = WsCfg<N2, R, CP, GROUPS>;
   static int grid = 0;
   if (grid == 0) {
-    cudaFuncSetAttribute(k_fwd_ws<N2, R, CP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(k_fwd_ws<N2, R, CP, GROUPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          W::SMEM);
-    grid = persistent_grid((const void*)k_fwd_ws<N2, R, CP>, 288, W::SMEM);
+    grid = persistent_grid((const void*)k_fwd_ws<N2, R, CP, GROUPS>, W::THREADS, W::SMEM);
   }
-  TT_TIMED("k_fwd_ws", st, (k_fwd_ws<N2, R, CP><<<grid, 288, W::SMEM, st>>>(fa)));
+  TT_TIMED("k_fwd_ws", st, (k_fwd_ws<N2, R, CP, GROUPS><<<grid, W::THREADS, W::SMEM, st>>>(fa)));
 }
 
 template <int N2, int R, int CP>
@@ -537,7 +555,7 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
   fa.G2 = cores[1];
   fa.G3 = cores[2];
   switch (fwd_kind(s)) {
-    case kFwdTiled_8_32: launch_ws<8, 32, kCP_8_32>(fa, st); break;
+    case kFwdTiled_8_32: launch_ws<8, 32, kCP_8_32, 2>(fa, st); break;
     case kFwdTiled_8_64: launch_tiled<8, 64, kCP_8_64>(fa, st); break;
     case kFwdTiled_4_16: launch_tiled<4, 16, kCP_4_16>(fa, st); break;
     default: {

@@ -44,11 +44,14 @@ struct TileCfg {
 template <class T, int C>
 __device__ __forceinline__ void tiled_stage2(const float* __restrict__ G2s,
                                              const float* __restrict__ P1t,
-                                             float* __restrict__ P2, int np) {
+                                             float* __restrict__ P2, int np,
+                                             int ltid = -1, int nthreads = -1) {
+  if (ltid < 0) ltid = threadIdx.x;
+  if (nthreads < 0) nthreads = blockDim.x;
   constexpr int R = T::kR;
   constexpr int NC = T::NC;
   constexpr int G = NC / C;                 // column groups per prefix
-  for (int item = threadIdx.x; item < np * G; item += blockDim.x) {
+  for (int item = ltid; item < np * G; item += nthreads) {
     const int p = item / G, cg = item - p * G;
     float acc[4][C];
 #pragma unroll
@@ -219,16 +222,17 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 template <class T, int KQ>
 __device__ __forceinline__ void tiled_stage2_splitk(const float* __restrict__ G2s,
                                                     const float* __restrict__ P1n,
-                                                    float* __restrict__ P2, int np, int nthreads) {
+                                                    float* __restrict__ P2, int np, int nthreads,
+                                                    int ltid) {
   constexpr int R = T::kR, NC = T::NC, CPW = 32 / KQ;   // column groups per warp
   constexpr int KS = R / KQ;
   const int lane = threadIdx.x & 31;
   const int kq = lane / CPW, cgl = lane - kq * CPW;
   const int total = np * (NC / 4) * KQ;
   for (int base = 0; base < total; base += nthreads) {
-    const int wi = (base + threadIdx.x) >> 5;          // warp-item
+    const int wi = (base + ltid) >> 5;                 // warp-item
     const int cgall = wi * CPW + cgl;                   // over all prefixes
-    const bool valid = base + (int)threadIdx.x < total;
+    const bool valid = base + ltid < total;
     const int p = cgall / (NC / 4), cg = cgall - p * (NC / 4);
     float acc[4][4];
 #pragma unroll
@@ -268,53 +272,6 @@ __device__ __forceinline__ void tiled_stage2_splitk(const float* __restrict__ G2
   }
 }
 
-// Stage 2 for np >= 3 prefixes from G1 rows in their natural [j1][a] layout:
-// 4 j1 rows x C columns per thread (as tiled_stage2, A read with scalar loads).
-template <class T, int C>
-__device__ __forceinline__ void tiled_stage2_n(const float* __restrict__ G2s,
-                                               const float* __restrict__ P1n,
-                                               float* __restrict__ P2, int np, int nthreads) {
-  constexpr int R = T::kR, NC = T::NC, G = NC / C;
-  static_assert(C >= 4, "column groups of 4");
-  for (int item = threadIdx.x; item < np * G; item += nthreads) {
-    const int p = item / G, cg = item - p * G;
-    float acc[4][C];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int c = 0; c < C; ++c) acc[i][c] = 0.f;
-    const float* ap = P1n + p * (4 * R);
-#pragma unroll 4
-    for (int k = 0; k < R; ++k) {
-      const float a0 = ap[k], a1 = ap[R + k], a2 = ap[2 * R + k], a3 = ap[3 * R + k];
-      const float* brow = G2s + k * NC;
-      float bv[C];
-#pragma unroll
-      for (int q = 0; q < C / 4; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(brow + q * (NC * 4 / C) + 4 * cg);
-        bv[4 * q] = v.x; bv[4 * q + 1] = v.y; bv[4 * q + 2] = v.z; bv[4 * q + 3] = v.w;
-      }
-#pragma unroll
-      for (int c = 0; c < C; ++c) {
-        acc[0][c] = fmaf(a0, bv[c], acc[0][c]);
-        acc[1][c] = fmaf(a1, bv[c], acc[1][c]);
-        acc[2][c] = fmaf(a2, bv[c], acc[2][c]);
-        acc[3][c] = fmaf(a3, bv[c], acc[3][c]);
-      }
-    }
-    float* pp = P2 + p * T::P2P;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int q = 0; q < C / 4; ++q) {
-        const int n = q * (NC * 4 / C) + 4 * cg;
-        const int j2 = n / R, b = n - j2 * R;
-        *reinterpret_cast<float4*>(pp + (i * T::kN2 + j2) * T::P2S + b) =
-            make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
-      }
-  }
-}
-
 // Stage 2 from G1 rows in natural layout P1n; for np >= 3 they are first
 // transposed into P1t ([p][a][j1], 4*R*np floats) so that the A operand of a
 // k step is one 128-bit broadcast load.  Ends with the 256 compute threads
@@ -323,25 +280,28 @@ template <class T>
 __device__ __forceinline__ void stage2_natural(const float* __restrict__ G2s,
                                                const float* __restrict__ P1n,
                                                float* __restrict__ P1t,
-                                               float* __restrict__ P2, int np) {
+                                               float* __restrict__ P2, int np, int ltid = -1,
+                                               int bar_id = 1) {
   constexpr int R = T::kR;
+  if (ltid < 0) ltid = threadIdx.x;
   const int need = (np * T::NC + 255) / 256;    // column groups of 4 per thread for ~256 items
   if (np == 1) {
-    tiled_stage2_splitk<T, 4>(G2s, P1n, P2, np, 256);
+    tiled_stage2_splitk<T, 4>(G2s, P1n, P2, np, 256, ltid);
   } else if (np == 2) {
-    tiled_stage2_splitk<T, 2>(G2s, P1n, P2, np, 256);
+    tiled_stage2_splitk<T, 2>(G2s, P1n, P2, np, 256, ltid);
   } else {
-    for (int e = threadIdx.x; e < np * 4 * R; e += 256) {
+    for (int e = ltid; e < np * 4 * R; e += 256) {
       const int p = e / (4 * R), rem = e - p * (4 * R);
       const int j1 = rem / R, k = rem - j1 * R;
       P1t[p * 4 * R + k * 4 + j1] = P1n[e];
     }
-    named_sync(1, 256);
-    if (need <= 4) tiled_stage2<T, 4>(G2s, P1t, P2, np);
-    else if (need <= 8) tiled_stage2<T, 8>(G2s, P1t, P2, np);
-    else tiled_stage2<T, 16>(G2s, P1t, P2, np);
+    named_sync(bar_id, 256);
+    if (need <= 4) tiled_stage2<T, 4>(G2s, P1t, P2, np, ltid, 256);
+    else if (need <= 8) tiled_stage2<T, 8>(G2s, P1t, P2, np, ltid, 256);
+    else tiled_stage2<T, 16>(G2s, P1t, P2, np, ltid, 256);
   }
-  named_sync(1, 256);
+  named_sync(bar_id, 256);
 }
+
 
 }  // namespace tt
