@@ -555,7 +555,7 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
   fa.G2 = cores[1];
   fa.G3 = cores[2];
   switch (fwd_kind(s)) {
-    case kFwdTiled_8_32: launch_ws<8, 32, kCP_8_32, 2>(fa, st); break;
+    case kFwdTiled_8_32: launch_ws<8, 32, kCP_8_32, 1>(fa, st); break;
     case kFwdTiled_8_64: launch_tiled<8, 64, kCP_8_64>(fa, st); break;
     case kFwdTiled_4_16: launch_tiled<4, 16, kCP_4_16>(fa, st); break;
     default: {
