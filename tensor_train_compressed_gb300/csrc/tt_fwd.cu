@@ -15,6 +15,7 @@
 // balancing under Zipf skew, FlowTT summary card, key innovations).
 #include "tt_internal.cuh"
 #include "tt_tile.cuh"
+#include "tt_mma.cuh"
 
 namespace tt {
 
@@ -157,116 +158,182 @@ __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_til
 }
 
 // ---------------------------------------------------------------------------
-// Warp-specialised chunk kernel (n1 = n3 = 4, R1 = R2 = R, G2 slice small enough
-// to double-buffer).  Warp 8 is a producer: it claims the next chunk, writes the
-// chunk's metadata and issues bulk copies (TMA, 1-D) of the G2 slice, the G1
-// rows and up to ROWMAX G3 rows into the free one of two stage buffers,
-// completing on that buffer's "full" mbarrier.  Warps 0-7 consume: stage 2
-// (P2 in shared memory), stage 3 (rows), then release the buffer through its
-// "empty" mbarrier.  Staging of chunk i+1 thus overlaps the math of chunk i.
-template <int N2, int R, int CP, int GROUPS = 1>
-struct WsCfg {
-  using T = TileCfg<N2, R, CP>;
-  static constexpr int THREADS = GROUPS * 256 + 32;
-  static constexpr int ROWMAX = 64;
-  static constexpr int F_P1 = CP * 4 * R;            // G1 rows, natural [p][j1][a]
-  static constexpr int F_G3 = ROWMAX * T::G3S;
-  static constexpr int STAGE_F = T::F_G2 + F_P1 + F_G3;
+// Tensor-core chunk kernel for n1 = n3 = 4, n2 = 8, R1 = R2 = 32 (D = 128).
+// Warp 8 is a producer: it claims the next chunk, writes the chunk's metadata
+// (the list of row pairs) and stages the G2 slice, the G1 rows and up to ROWMAX
+// G3 rows into the free one of two stage buffers with 16-byte cp.async copies
+// (one 512-byte warp instruction per row slice, into padded rows), each lane
+// signalling the buffer's "full" mbarrier when its copies have landed.
+// Warps 0-7 consume with m16n8k8 TF32 tiles (three-term split, fp32 accuracy;
+// tt_mma.cuh):
+//   stage 2  P2 = [G1 rows of the chunk's prefixes] . G2[i2]   (4 np) x 256 x 32
+//   stage 3  for each pair of rows of one prefix:
+//            P2[p] . [G3[i3_a] | G3[i3_b]]                     32 x 8 x 32
+//            (a prefix with an odd row count pairs its last row with itself and
+//            drops the copy)
+// and release the buffer through its "empty" mbarrier, so that the staging of
+// chunk i+1 overlaps the math of chunk i.  All shared-memory strides are
+// padded so that every fragment load and store is free of bank conflicts.
+template <int CW>
+struct MmaFwd {
+  static constexpr int CP = kCP_8_32, R = 32, NC = 256, D = 128;
+  static constexpr int ROWMAX = 64;                  // G3 rows staged per chunk
+  static constexpr int MAXROWS = CP * 32;            // rows of one chunk (CP prefixes x 32)
+  static constexpr int MAXPAIRS = MAXROWS / 2 + CP;
+  static constexpr int G2S = NC + 8;                 // G2 row (r1) stride
+  static constexpr int P1S = R + 4;                  // G1 row ((p, j1)) stride
+  static constexpr int G3S = 4 * R + 16;             // staged G3 row stride
+  static constexpr int P2B = R + 4;                  // P2[p][j1][j2][r2]: j2 stride
+  static constexpr int P2A = 8 * P2B + 8;            //   j1 stride
+  static constexpr int P2P = 4 * P2A;                //   p stride
+  static constexpr int F_G2 = R * G2S, F_P1 = CP * 4 * P1S, F_G3 = (ROWMAX + 1) * G3S;
+  static constexpr int STAGE_F = F_G2 + F_P1 + F_G3;
+  static constexpr int F_P2 = CP * P2P;
   struct Meta {
-    int x0, x1, p0, np, end, pad[3];
-    int rp[ROWMAX];                                   // prefix (chunk-local) of each staged row
+    int x0, x1, p0, np, npairs, end, pad[2];
+    int pair[MAXPAIRS];   // first row | (second row valid) << 8 | chunk-local prefix << 9
   };
-  static constexpr int SMEM =
-      4 * (2 * STAGE_F + GROUPS * (T::F_P2 + F_P1)) + 2 * (int)sizeof(Meta) + 4 * 8;
-  static_assert(T::NB == 8, "one compute warp per j12 block");
-  static_assert(GROUPS == 1 || GROUPS == 2, "one or two consumer groups");
-  static_assert(ROWMAX <= 64 && CP <= 32, "the producer stages with two rows per lane");
+  static constexpr int NCW = NC / CW;                // stage-2 columns per consumer warp
+  static constexpr int THREADS = 32 * CW + 32;
+  static constexpr int SMEM = 4 * (2 * STAGE_F + F_P2) + 2 * (int)sizeof(Meta) + 4 * 8;
+  static_assert(CW == 8 || CW == 16, "8 or 16 consumer warps");
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(MAXROWS <= 256 && CP <= 8 && 4 * CP <= 32, "pair encoding and G1 staging");
 };
 
-// acc[i][j3] = sum over b in [b0, b0 + NBV) of P2[j12 = 4 blk + i][b] G3[b][j3]
-template <class T, bool kGlobalG3, int NBV = T::kR>
-__device__ __forceinline__ void row_dot(const float* __restrict__ pp,
-                                        const float* __restrict__ gg, float acc[4][4],
-                                        int b0 = 0) {
+// P2 rows (p, j1) = 16 MT tiles x 256 columns (j2, r2); consumer warp w owns
+// columns NCW w .. NCW (w+1) - 1.
+template <int CW, int MT>
+__device__ __forceinline__ void mma_fwd_stage2(const float* __restrict__ G2s,
+                                               const float* __restrict__ P1n,
+                                               float* __restrict__ P2, int warp, int lane) {
+  using C = MmaFwd<CW>;
+  constexpr int NT = C::NCW / 8;
+  const int g = lane >> 2, t = lane & 3;
+  float acc[MT][NT][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 2
-  for (int b = b0; b < b0 + NBV; b += 4) {
-    float4 pv[4], gv[4];
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pv[i] = *reinterpret_cast<const float4*>(pp + i * T::P2S + b);
+      for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
+  const int col0 = warp * C::NCW;
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      if constexpr (kGlobalG3) gv[t] = __ldg(reinterpret_cast<const float4*>(gg + (b + t) * 4));
-      else gv[t] = *reinterpret_cast<const float4*>(gg + (b + t) * 4);
+  for (int ks = 0; ks < 4; ++ks) {
+    FragA af[MT];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+      af[mt] = load_a(P1n + 16 * mt * C::P1S + 8 * ks, C::P1S, 8 * C::P1S, lane);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const FragB bf = load_b(G2s + 8 * ks * C::G2S + col0 + 8 * nt, C::G2S, lane);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma_3xtf32(acc[mt][nt], af[mt], bf);
     }
+  }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float pw[4] = {pv[i].x, pv[i].y, pv[i].z, pv[i].w};
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        acc[i][0] = fmaf(pw[t], gv[t].x, acc[i][0]);
-        acc[i][1] = fmaf(pw[t], gv[t].y, acc[i][1]);
-        acc[i][2] = fmaf(pw[t], gv[t].z, acc[i][2]);
-        acc[i][3] = fmaf(pw[t], gv[t].w, acc[i][3]);
+    for (int h = 0; h < 2; ++h) {
+      const int row = 16 * mt + g + 8 * h;          // (p, j1)
+      float* dst = P2 + (row >> 2) * C::P2P + (row & 3) * C::P2A + 2 * t;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n0 = col0 + 8 * nt;               // (j2, r2) = (n0 / 32, n0 % 32 + 2t)
+        *reinterpret_cast<float2*>(dst + (n0 >> 5) * C::P2B + (n0 & 31)) =
+            make_float2(acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
       }
     }
+}
+
+// Rows of the chunk, by pairs.  Consumer warp w takes m-tile w % 2 (j12 =
+// 16 (w % 2) .. +15) of a contiguous share of the pairs, so that consecutive
+// pairs of one prefix reuse the warp's split P2 fragments.
+template <int CW>
+__device__ __forceinline__ void mma_fwd_stage3(const typename MmaFwd<CW>::Meta& m,
+                                               const float* __restrict__ P2,
+                                               const float* __restrict__ G3s, const float* __restrict__ G3,
+                                               const int32_t* __restrict__ row_i3, float* __restrict__ rowbuf,
+                                               int warp, int lane) {
+  using C = MmaFwd<CW>;
+  constexpr int SH = CW / 2;                        // warps per m-tile
+  const int g = lane >> 2, t = lane & 3;
+  const int mt = warp & 1, share = warp >> 1;
+  const int npairs = m.npairs, x0 = m.x0;
+  const int q0 = npairs * share / SH, q1 = npairs * (share + 1) / SH;
+  int cur_p = -1;
+  FragA af[4];
+  for (int q = q0; q < q1; ++q) {
+    const int e = m.pair[q];
+    const int r0 = e & 255, has2 = (e >> 8) & 1, p = e >> 9;
+    if (p != cur_p) {
+      cur_p = p;
+      // A[j12][r2] = P2[p][j1 = 2 mt (+1 for rows 8..15)][j2 = row % 8][r2]
+      const float* pa = P2 + p * C::P2P + 2 * mt * C::P2A;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) af[ks] = load_a(pa + 8 * ks, C::P2B, C::P2A, lane);
+    }
+    // B[r2][(row of pair, j3)] = G3[i3_row][r2][j3]
+    const int rb = r0 + (has2 ? (g >> 2) : 0);
+    FragB bf[4];
+    if (r0 + 1 < C::ROWMAX) {
+      const float* gp = G3s + rb * C::G3S + (g & 3);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        bf[ks].v[0] = split_tf32(gp[(8 * ks + t) * 4]);
+        bf[ks].v[1] = split_tf32(gp[(8 * ks + t + 4) * 4]);
+      }
+    } else {
+      const float* gp = rb < C::ROWMAX ? G3s + rb * C::G3S
+                                       : G3 + (size_t)__ldg(row_i3 + x0 + rb) * (4 * C::R);
+      gp += g & 3;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        bf[ks].v[0] = split_tf32(gp[(8 * ks + t) * 4]);
+        bf[ks].v[1] = split_tf32(gp[(8 * ks + t + 4) * 4]);
+      }
+    }
+    // four accumulator chains: k parity x {hi.hi, the two small terms}
+    float big[2][4], small[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) big[h][i] = small[h][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const FragA& a = af[ks];
+      const FragB& b = bf[ks];
+      mma_tf32(small[ks & 1], a.v[0].lo, a.v[1].lo, a.v[2].lo, a.v[3].lo, b.v[0].hi, b.v[1].hi);
+      mma_tf32(big[ks & 1], a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].hi, b.v[1].hi);
+      mma_tf32(small[ks & 1], a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].lo, b.v[1].lo);
+    }
+    // C[j12][(row of pair, j3)]: this lane holds j3 = 2 (t % 2), +1 of row t / 2
+    if (t < 2 || has2) {
+      float* o = rowbuf + (size_t)(x0 + r0 + (t >> 1)) * C::D + (16 * mt + g) * 4 + 2 * (t & 1);
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = (small[0][i] + small[1][i]) + (big[0][i] + big[1][i]);
+      *reinterpret_cast<float2*>(o) = make_float2(v[0], v[1]);
+      *reinterpret_cast<float2*>(o + 32) = make_float2(v[2], v[3]);
+    }
   }
 }
 
-template <class T, int SPLIT>
-__device__ __forceinline__ void stage3_split(const float* __restrict__ P2,
-                                             const float* __restrict__ G3s,
-                                             const int* __restrict__ rp, float* __restrict__ rowbuf,
-                                             int x0, int rows, int blk, int lane) {
-  constexpr int NBV = T::kR / SPLIT;
-  const int r = lane / SPLIT, q = lane % SPLIT;
-  float acc[4][4];
-  if (r < rows) {
-    const float* pp = P2 + rp[r] * T::P2P + (blk * 4) * T::P2S;
-    row_dot<T, false, NBV>(pp, G3s + r * T::G3S, acc, q * NBV);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  }
-#pragma unroll
-  for (int o = 1; o < SPLIT; o <<= 1)
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], o);
-  if (r < rows) {
-    float4* out = reinterpret_cast<float4*>(rowbuf + (size_t)(x0 + r) * T::D + blk * 16);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (i % SPLIT == q) out[i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-  }
-}
-
-// With GROUPS = 2 there are two consumer groups of 8 warps: group g owns stage
-// buffer g (and its own P2), so the producer's stages alternate between the
-// groups and two chunks are in flight per SM.
-template <int N2, int R, int CP, int GROUPS>
-__global__ void __launch_bounds__(WsCfg<N2, R, CP, GROUPS>::THREADS, 1) k_fwd_ws(FwdArgs a) {
-  using W = WsCfg<N2, R, CP, GROUPS>;
-  using T = typename W::T;
-  using Meta = typename W::Meta;
+template <int CW>
+__global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
+  using C = MmaFwd<CW>;
+  using Meta = typename C::Meta;
   extern __shared__ float4 sm4[];
   float* base = reinterpret_cast<float*>(sm4);
-  float* P2all = base + 2 * W::STAGE_F;
-  float* P1tall = P2all + GROUPS * T::F_P2;
-  Meta* meta = reinterpret_cast<Meta*>(P1tall + GROUPS * W::F_P1);
+  float* P2 = base + 2 * C::STAGE_F;
+  Meta* meta = reinterpret_cast<Meta*>(P2 + C::F_P2);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
   uint64_t* empty = full + 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    // full: 32 producer lanes' copy arrivals + the producer's metadata arrival
+    mbar_init(&full[0], 33);
+    mbar_init(&full[1], 33);
     mbar_init(&empty[0], 1);
     mbar_init(&empty[1], 1);
     mbar_init_fence();
@@ -274,117 +341,144 @@ __global__ void __launch_bounds__(WsCfg<N2, R, CP, GROUPS>::THREADS, 1) k_fwd_ws
   __syncthreads();
   const int n_chunks = a.w.ctl->n_chunks;
 
-  if (warp == 8 * GROUPS) {
-    // ---------------- producer: claims one chunk ahead, so that the claim and
-    // the descriptor load of chunk i+1 overlap the staging of chunk i
-    auto end_stage = [&](int it) {          // end marker into the stage of iteration it
-      const int s = it & 1;
-      const uint32_t use = (uint32_t)it >> 1;
-      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) return;
-      if (lane == 0) {
-        meta[s].end = 1;
-        mbar_arrive(&full[s]);
-      }
+  if (warp == CW) {
+    // ---------------- producer.  Software-pipelined: while chunk i is staged,
+    // the metadata loads of chunk i+1 and the claim of chunk i+2 are in flight.
+    struct PMeta {
+      int x0, x1, p0, np, nst, i2;
+      int g30, g31;    // i3 of staged rows lane, lane + 32
+      int gi1, rs, re; // lane < np: i1 and chunk-local row range of prefix p0 + lane
     };
+    auto load_meta = [&](const ChunkDesc& d, PMeta& pm) {
+      pm.x0 = d.x0;
+      pm.x1 = d.x1;
+      pm.p0 = d.p0;
+      pm.np = d.p1 - d.p0 + 1;
+      const int rows = d.x1 - d.x0;
+      pm.nst = min(rows, C::ROWMAX);
+      pm.g30 = lane < pm.nst ? a.w.row_i3[d.x0 + lane] : 0;
+      pm.g31 = lane + 32 < pm.nst ? a.w.row_i3[d.x0 + lane + 32] : 0;
+      pm.gi1 = 0;
+      pm.rs = pm.re = rows;
+      if (lane < pm.np) {
+        pm.gi1 = a.w.pair_i1[d.p0 + lane];
+        pm.rs = max(a.w.pair_row_start[d.p0 + lane], d.x0) - d.x0;
+        pm.re = min(a.w.pair_row_start[d.p0 + lane + 1], d.x1) - d.x0;
+      }
+      pm.i2 = a.w.pair_i2[d.p0];
+    };
+    PMeta cur{}, nxt{};
     int c = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
-    ChunkDesc d{};
-    if (c < n_chunks) d = load_chunk(a.w.chunk_desc, c);
+    if (c < n_chunks) load_meta(load_chunk(a.w.chunk_desc, c), cur);
+    int cn = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
+    ChunkDesc dn{};
+    if (cn < n_chunks) dn = load_chunk(a.w.chunk_desc, cn);
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t use = (uint32_t)it >> 1;
       Meta& m = meta[s];
       if (c >= n_chunks) {
-        end_stage(it);
-        if (GROUPS == 2) end_stage(it + 1);   // the other group's stage too
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
+        if (lane == 0) m.end = 1;
+        __syncwarp();
+        cp_async_arrive_noinc(&full[s]);
+        if (lane == 0) mbar_arrive(&full[s]);
         break;
       }
-      const int x0 = d.x0, x1 = d.x1, p0 = d.p0;
-      const int np = d.p1 - p0 + 1;
-      const int nst = min(x1 - x0, W::ROWMAX);
-      // metadata of this chunk (loads in flight while the stage frees up)
-      int rp0 = 0, rp1 = 0, g30 = 0, g31 = 0, gi1 = 0;
-      if (lane < nst) {
-        rp0 = a.w.row_pair[x0 + lane] - p0;
-        g30 = a.w.row_i3[x0 + lane];
-      }
-      if (lane + 32 < nst) {
-        rp1 = a.w.row_pair[x0 + lane + 32] - p0;
-        g31 = a.w.row_i3[x0 + lane + 32];
-      }
-      if (lane < np) gi1 = a.w.pair_i1[p0 + lane];
-      const int i2 = a.w.pair_i2[p0];
-      // claim the next chunk and fetch its descriptor
-      const int cn = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
-      ChunkDesc dn{};
-      if (cn < n_chunks) dn = load_chunk(a.w.chunk_desc, cn);
+      if (cn < n_chunks) load_meta(dn, nxt);
+      const int cnn = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
-      float* G2s = base + s * W::STAGE_F;
-      float* P1n = G2s + T::F_G2;
-      float* G3s = P1n + W::F_P1;
-      if (lane < nst) m.rp[lane] = rp0;
-      if (lane + 32 < nst) m.rp[lane + 32] = rp1;
+      float* G2s = base + s * C::STAGE_F;
+      float* P1n = G2s + C::F_G2;
+      float* G3s = P1n + C::F_P1;
+      // G2[i2]: 32 rows of 64 16-byte pieces
+      const float* g2src = a.G2 + (size_t)cur.i2 * C::R * C::NC;
+#pragma unroll 8
+      for (int i = 0; i < C::R * C::NC / 128; ++i) {
+        const int e = i * 32 + lane, row = e >> 6, q = e & 63;
+        cp_async16(G2s + row * C::G2S + 4 * q, g2src + row * C::NC + 4 * q);
+      }
+      // G1[i1_p]: 4 rows of 8 pieces per prefix
+#pragma unroll
+      for (int pp = 0; pp < C::CP; ++pp) {
+        const int i1 = __shfl_sync(0xffffffffu, cur.gi1, pp);
+        const int j1 = lane >> 3, q = lane & 7;
+        if (pp < cur.np)
+          cp_async16(P1n + (4 * pp + j1) * C::P1S + 4 * q, a.G1 + ((size_t)i1 * 4 + j1) * C::R + 4 * q);
+      }
+      // G3[i3_x]: 32 pieces per row, 8 rows per batch of independent shuffles
+      for (int r0 = 0; r0 < cur.nst; r0 += 8) {
+        const int src = r0 < 32 ? cur.g30 : cur.g31;
+        int i3v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) i3v[u] = __shfl_sync(0xffffffffu, src, (r0 & 31) + u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (r0 + u < cur.nst)
+            cp_async16(G3s + (r0 + u) * C::G3S + 4 * lane, a.G3 + (size_t)i3v[u] * 4 * C::R + 4 * lane);
+      }
+      cp_async_arrive_noinc(&full[s]);
+      // pairs: a row starts a pair when its offset within its prefix is even;
+      // the list follows row order (prefix after prefix)
+      int rsq[C::CP];
+#pragma unroll
+      for (int j = 0; j < C::CP; ++j) rsq[j] = __shfl_sync(0xffffffffu, cur.rs, j);
+      const int rows = cur.x1 - cur.x0;
+      int npairs = 0;
+      for (int rb = 0; rb < rows; rb += 32) {
+        const int r = rb + lane;
+        int q = -1, qs = 0, qe = rows;
+#pragma unroll
+        for (int j = 0; j < C::CP; ++j) {
+          if (rsq[j] <= r) {
+            ++q;
+            qs = rsq[j];
+          } else {
+            qe = min(qe, rsq[j]);
+          }
+        }
+        const bool start = r < rows && ((r - qs) & 1) == 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, start);
+        if (start)
+          m.pair[npairs + __popc(bal & ((1u << lane) - 1u))] = r | ((r + 1 < qe) ? 256 : 0) | (q << 9);
+        npairs += __popc(bal);
+      }
       __syncwarp();
       if (lane == 0) {
-        m.x0 = x0;
-        m.x1 = x1;
-        m.p0 = p0;
-        m.np = np;
+        m.x0 = cur.x0;
+        m.x1 = cur.x1;
+        m.p0 = cur.p0;
+        m.np = cur.np;
+        m.npairs = npairs;
         m.end = 0;
-        const uint32_t bytes = 4u * (T::F_G2 + np * 4 * R + nst * 4 * R);
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(G2s, a.G2 + (size_t)i2 * T::F_G2, 4u * T::F_G2, &full[s]);
+        mbar_arrive(&full[s]);
       }
-      __syncwarp();
-      if (lane < np) bulk_g2s(P1n + lane * 4 * R, a.G1 + (size_t)gi1 * 4 * R, 16u * R, &full[s]);
-      if (lane < nst) bulk_g2s(G3s + lane * T::G3S, a.G3 + (size_t)g30 * 4 * R, 16u * R, &full[s]);
-      if (lane + 32 < nst)
-        bulk_g2s(G3s + (lane + 32) * T::G3S, a.G3 + (size_t)g31 * 4 * R, 16u * R, &full[s]);
+      ChunkDesc dnn{};
+      if (cnn < n_chunks) dnn = load_chunk(a.w.chunk_desc, cnn);
       c = cn;
-      d = dn;
+      cur = nxt;
+      cn = cnn;
+      dn = dnn;
     }
+    cp_async_wait_all();
     return;
   }
 
-  // ---------------- consumers: group g = warps 8g .. 8g+7
-  const int g = warp >> 3, ltid = tid - 256 * g, blk = warp & 7;
-  const int bar_id = 1 + g;
-  float* P2 = P2all + g * T::F_P2;
-  float* P1t = P1tall + g * W::F_P1;
+  // ---------------- consumers: warps 0 .. CW-1
   for (int k = 0;; ++k) {
-    // GROUPS == 1: both stages in turn; GROUPS == 2: stage g only
-    const int s = GROUPS == 1 ? (k & 1) : g;
-    const uint32_t parity = GROUPS == 1 ? (((uint32_t)k >> 1) & 1) : ((uint32_t)k & 1);
-    if (!mbar_wait(&full[s], parity, a.w.ctl)) break;
+    const int s = k & 1;
+    if (!mbar_wait(&full[s], ((uint32_t)k >> 1) & 1, a.w.ctl)) break;
     const Meta& m = meta[s];
     if (m.end) break;
-    const int x0 = m.x0, x1 = m.x1, p0 = m.p0, np = m.np;
-    const float* G2s = base + s * W::STAGE_F;
-    const float* P1n = G2s + T::F_G2;
-    const float* G3s = P1n + W::F_P1;
-    stage2_natural<T>(G2s, P1n, P1t, P2, np, ltid, bar_id);
-    const int rows = x1 - x0;
-    if (rows <= 16) {
-      // few rows: SPLIT lanes share a row, each over R/SPLIT of the b sum
-      if (rows <= 8) stage3_split<T, 4>(P2, G3s, m.rp, a.w.rowbuf, x0, rows, blk, lane);
-      else stage3_split<T, 2>(P2, G3s, m.rp, a.w.rowbuf, x0, rows, blk, lane);
-    } else {
-      for (int r = lane; r < rows; r += 32) {
-        const int x = x0 + r;
-        float acc[4][4];
-        if (r < W::ROWMAX) {
-          const float* pp = P2 + m.rp[r] * T::P2P + (blk * 4) * T::P2S;
-          row_dot<T, false>(pp, G3s + r * T::G3S, acc);
-        } else {
-          const float* pp = P2 + (a.w.row_pair[x] - p0) * T::P2P + (blk * 4) * T::P2S;
-          row_dot<T, true>(pp, a.G3 + (size_t)a.w.row_i3[x] * 4 * R, acc);
-        }
-        float4* o = reinterpret_cast<float4*>(a.w.rowbuf + (size_t)x * T::D + blk * 16);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-      }
-    }
-    named_sync(bar_id, 256);
-    if (ltid == 0) mbar_arrive(&empty[s]);
+    const float* G2s = base + s * C::STAGE_F;
+    const float* P1n = G2s + C::F_G2;
+    const float* G3s = P1n + C::F_P1;
+    if (m.np > 4) mma_fwd_stage2<CW, 2>(G2s, P1n, P2, warp, lane);
+    else mma_fwd_stage2<CW, 1>(G2s, P1n, P2, warp, lane);
+    named_sync(1, 32 * CW);
+    mma_fwd_stage3<CW>(m, P2, G3s, a.G3, a.w.row_i3, a.w.rowbuf, warp, lane);
+    named_sync(1, 32 * CW);
+    if (tid == 0) mbar_arrive(&empty[s]);
   }
 }
 
@@ -518,16 +612,15 @@ static int persistent_grid(const void* fn, int threads, size_t smem) {
   return per_sm * sm_count();
 }
 
-template <int N2, int R, int CP, int GROUPS>
-static void launch_ws(const FwdArgs& fa, cudaStream_t st) {
-  using W = WsCfg<N2, R, CP, GROUPS>;
+template <int CW>
+static void launch_fwd_mma(const FwdArgs& fa, cudaStream_t st) {
+  using C = MmaFwd<CW>;
   static int grid = 0;
   if (grid == 0) {
-    cudaFuncSetAttribute(k_fwd_ws<N2, R, CP, GROUPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         W::SMEM);
-    grid = persistent_grid((const void*)k_fwd_ws<N2, R, CP, GROUPS>, W::THREADS, W::SMEM);
+    cudaFuncSetAttribute(k_fwd_mma<CW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    grid = persistent_grid((const void*)k_fwd_mma<CW>, C::THREADS, C::SMEM);
   }
-  TT_TIMED("k_fwd_ws", st, (k_fwd_ws<N2, R, CP, GROUPS><<<grid, W::THREADS, W::SMEM, st>>>(fa)));
+  TT_TIMED("k_fwd_mma", st, (k_fwd_mma<CW><<<grid, C::THREADS, C::SMEM, st>>>(fa)));
 }
 
 template <int N2, int R, int CP>
@@ -555,7 +648,7 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
   fa.G2 = cores[1];
   fa.G3 = cores[2];
   switch (fwd_kind(s)) {
-    case kFwdTiled_8_32: launch_ws<8, 32, kCP_8_32, 1>(fa, st); break;
+    case kFwdTiled_8_32: launch_fwd_mma<16>(fa, st); break;
     case kFwdTiled_8_64: launch_tiled<8, 64, kCP_8_64>(fa, st); break;
     case kFwdTiled_4_16: launch_tiled<4, 16, kCP_4_16>(fa, st); break;
     default: {
