@@ -391,7 +391,7 @@ def run_ours(args, rank, world, dist):
         reps = max(3, min(args.steps, 10))
         flops = {"k_fwd_generic": a["fwd_contract"], "k_fwd_tiled": a["fwd_contract"],
                  "k_fwd_ws": a["fwd_contract"], "k_fwd_mma": a["fwd_contract"], "k_bwd_generic": a["bwd_contract"],
-                 "k_bwd_ws": a["bwd_contract"], "k_pool": a["pool"], "k_s_gather": a["s_gather"]}
+                 "k_bwd_ws": a["bwd_contract"], "k_bwd_mma": a["bwd_contract"], "k_pool": a["pool"], "k_s_gather": a["s_gather"]}
         per_launch_ms = kms[dom] / max(1, launches_per_step[dom] / reps)
         out = {"kernel": dom, "share": round(kms[dom] / sum(kms.values()), 4)}
         # algorithmic bytes of the non-contraction kernels (DRAM-level minimum)

@@ -16,6 +16,7 @@
 // stored once.  Core gradients are accumulated with float atomics.
 #include "tt_internal.cuh"
 #include "tt_tile.cuh"
+#include "tt_mma.cuh"
 
 namespace tt {
 
@@ -343,99 +344,314 @@ __global__ void __launch_bounds__(256) k_bwd_generic(BwdArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Warp-specialised backward chunk kernel (n1 = n3 = 4, R1 = R2 = R).  Warp 8 is a
-// producer: for the next chunk it writes the metadata and bulk-copies (TMA,
-// 1-D) the G2 slice, the G1 rows and the S and G3 rows of the first RB rows into
-// the free one of two stage buffers.  Warps 0-7 consume: P2 (stage 2), then per
-// batch of RB rows dG3 (float4 atomics) and dP2 (shared memory), then
-// dG2 = P1^T dP2 and dG1 = dP2 G2^T.  A chunk that starts a hot prefix takes all
-// of that prefix's rows (later batches are loaded by the consumers into the
-// already consumed row area); chunks holding its later pieces are skipped.
-template <int N2, int R, int CP>
-struct BwsCfg {
-  using T = TileCfg<N2, R, CP>;
-  static constexpr int RB = 32;
-  static constexpr int SS = T::D + 4;                 // padded S row (floats)
-  static constexpr int GS = 4 * R + 4;                // padded G3 row, natural [b][j3]
-  static constexpr int F_P1 = CP * 4 * R;             // natural [p][j1][a]
-  static constexpr int STAGE_F = T::F_G2 + F_P1 + RB * (SS + GS);
+// Tensor-core backward chunk kernel for n1 = n3 = 4, n2 = 8, R1 = R2 = 32 (D = 128).
+// Warp 8 is a producer: it claims the next chunk (skipping chunks that hold a
+// later piece of a hot prefix: the chunk that starts such a prefix takes all of
+// its rows, so that its prefix-level products are formed once), lists the row
+// pairs of the first batch and stages the G2 slice, the G1 rows and the first
+// batch's S and G3 rows with 16-byte cp.async copies (per-lane mbarrier
+// arrivals), double-buffered.  Warps 0-7 consume with m16n8k8 TF32 tiles
+// (three-term split, fp32 accuracy; tt_mma.cuh):
+//   (1) P2 = [G1 rows] . G2[i2]                     (4 np) x 256 x 32
+//   per batch of RB rows, by pairs of rows of one prefix:
+//   (2) dP2[p] += S[x] . G3[i3_x]^T                  32 x 32 x (4 per row)
+//   (3) dG3[i3_x] += P2[p]^T . S[x]                  32 x (4 per row) x 32
+//   then
+//   (4) dG2[i2] += [G1 rows]^T . dP2                 32 x 256 x (4 np)
+//   (5) dG1[i1_p] += dP2[p] . G2[i2]^T               (4 np) x 32 x 256
+// Core gradients are accumulated with vector float reductions.
+struct MmaBwd {
+  static constexpr int CP = kCP_8_32, R = 32, NC = 256, D = 128;
+  static constexpr int RB = 24;                     // rows per batch
+  static constexpr int MAXPAIRS = RB / 2 + CP;      // pairs of one batch
+  static constexpr int G2S = NC + 4;                // G2 row (r1) stride
+  static constexpr int P1S = R + 4;                 // G1 row ((p, j1)) stride
+  static constexpr int SS = D + 16;                 // S row stride (rows of a pair 16 banks apart)
+  static constexpr int GS = 4 * R + 16;             // G3 row stride
+  static constexpr int QB = R + 8;                  // P2 / dP2 [p][j1][j2][r2]: j2 stride
+  static constexpr int QA = 8 * QB + 8;             //   j1 stride
+  static constexpr int QP = 4 * QA + 4;             //   p stride
+  static constexpr int F_G2 = R * G2S, F_P1 = CP * 4 * P1S, F_S = (RB + 1) * SS, F_G3 = (RB + 1) * GS;
+  static constexpr int STAGE_F = F_G2 + F_P1 + F_S + F_G3;
+  static constexpr int F_Q = CP * QP;
   struct Meta {
-    int x0, x1, p0, np, end, nst, i2, pad;
-    int rp[RB];
-    int ri3[RB];
-    int pi1[CP + (CP & 1)];   // even count keeps the barriers that follow 8-byte aligned
+    int x0, x1, p0, np, i2, nb, npairs, end;
+    int rs[CP];          // chunk-local first row of each prefix
+    int pi1[CP];
+    int ri3[RB];         // i3 of the current batch's rows
+    int pair[MAXPAIRS];  // batch-local first row | (second row valid) << 8 | prefix << 9
   };
-  static constexpr int SMEM = 4 * (2 * STAGE_F + 2 * T::F_P2) + 2 * (int)sizeof(Meta) + 4 * 8;
-  static_assert(RB * R <= 4 * 256, "in-place G3 transpose: 4 float4 per thread");
-  static constexpr int TILES = T::NB * (R / 4);
-  static constexpr int RG = 256 / TILES;
-  static_assert(T::NB == 8 && 256 % TILES == 0 && RB % RG == 0, "mappings");
+  static constexpr int THREADS = 288;
+  static constexpr int SMEM = 4 * (2 * STAGE_F + 2 * F_Q) + 2 * (int)sizeof(Meta) + 4 * 8;
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(RB <= 32 && CP <= 8, "one row per producer lane; pair encoding");
 };
 
-template <class T, class C, int SPLIT>
-__device__ __forceinline__ void bwd_dg3(const float* __restrict__ P2, const float* __restrict__ Ss,
-                                        const int* __restrict__ rp, const int* __restrict__ ri3,
-                                        float* __restrict__ dG3, int nb, int warp, int lane) {
-  constexpr int R = T::kR, NJ = 4 * T::kN2 / SPLIT;
-  const int r = lane / SPLIT, q = lane % SPLIT;
-  for (int bb = warp; bb < R / 4; bb += 8) {
-    float acc[4][4];
+// Pairs of the rows [b0, b1) of a chunk, prefix by prefix (rsq[j]: chunk-local
+// first row of prefix j, `rows` for j >= np).  One warp; returns the count.
+__device__ __forceinline__ int bwd_pairs(int b0, int b1, int rows, const int* rsq, int* pair, int lane) {
+  int n = 0;
+  for (int rb = b0; rb < b1; rb += 32) {
+    const int r = rb + lane;
+    int q = -1, qs = 0, qe = rows;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    if (r < nb) {
-      const float* pp = P2 + rp[r] * T::P2P + 4 * bb;
-      const float* ss = Ss + r * C::SS;
-#pragma unroll 8
-      for (int j12 = q * NJ; j12 < (q + 1) * NJ; ++j12) {
-        const float4 pv = *reinterpret_cast<const float4*>(pp + j12 * T::P2S);
-        const float4 sv = *reinterpret_cast<const float4*>(ss + 4 * j12);
-        const float pw[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[i][0] = fmaf(pw[i], sv.x, acc[i][0]);
-          acc[i][1] = fmaf(pw[i], sv.y, acc[i][1]);
-          acc[i][2] = fmaf(pw[i], sv.z, acc[i][2]);
-          acc[i][3] = fmaf(pw[i], sv.w, acc[i][3]);
-        }
+    for (int j = 0; j < MmaBwd::CP; ++j) {
+      const int v = rsq[j];
+      if (v <= r) {
+        ++q;
+        qs = v;
+      } else {
+        qe = min(qe, v);
       }
     }
+    qs = max(qs, b0);
+    qe = min(qe, b1);
+    const bool start = r < b1 && ((r - qs) & 1) == 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, start);
+    if (start) pair[n + __popc(bal & ((1u << lane) - 1u))] = (r - b0) | ((r + 1 < qe) ? 256 : 0) | (q << 9);
+    n += __popc(bal);
+  }
+  return n;
+}
+
+// (1): P2 rows (p, j1) = 16 MT tiles x 256 columns; warp w owns j2 = w.
+template <int MT>
+__device__ __forceinline__ void mma_bwd_p2(const float* __restrict__ G2s, const float* __restrict__ P1n,
+                                           float* __restrict__ P2, int warp, int lane) {
+  using C = MmaBwd;
+  const int g = lane >> 2, t = lane & 3;
+  float acc[MT][4][4];
 #pragma unroll
-    for (int o = 1; o < SPLIT; o <<= 1)
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], o);
-    if (r < nb) {
-      float4* dst = reinterpret_cast<float4*>(dG3 + ((size_t)ri3[r] * R + 4 * bb) * 4);
+      for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (i % SPLIT == q)
-          atomicAdd(dst + i, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+  for (int ks = 0; ks < 4; ++ks) {
+    FragA af[MT];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) af[mt] = load_a(P1n + 16 * mt * C::P1S + 8 * ks, C::P1S, 8 * C::P1S, lane);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const FragB bf = load_b(G2s + 8 * ks * C::G2S + 32 * warp + 8 * nt, C::G2S, lane);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma_3xtf32(acc[mt][nt], af[mt], bf);
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = 16 * mt + g + 8 * h;
+      float* dst = P2 + (row >> 2) * C::QP + (row & 3) * C::QA + warp * C::QB + 2 * t;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+        *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
+    }
+}
+
+// dP2 accumulator of one warp: tile (j12 = 16 mt .. +15) x (r2 = 8 nt .. +7) of
+// the current prefix, two pair parities x {hi.hi, small terms}.
+struct DP2Acc {
+  float c[4][4];
+  int p;
+};
+
+__device__ __forceinline__ void dp2_flush(DP2Acc& acc, float* __restrict__ dP2, int mt, int nt, int lane) {
+  using C = MmaBwd;
+  const int g = lane >> 2, t = lane & 3;
+  if (acc.p >= 0) {
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (acc.c[1][i] + acc.c[3][i]) + (acc.c[0][i] + acc.c[2][i]);
+    // rows j12 = 16 mt + g (+8): j1 = 2 mt (+1), j2 = g
+    float* dst = dP2 + acc.p * C::QP + 2 * mt * C::QA + g * C::QB + 8 * nt + 2 * t;
+    *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
+    *reinterpret_cast<float2*>(dst + C::QA) = make_float2(v[2], v[3]);
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc.c[u][i] = 0.f;
+}
+
+// (2) over the pairs of one batch.
+__device__ __forceinline__ void mma_bwd_dp2(const MmaBwd::Meta& m, const float* __restrict__ Ss,
+                                            const float* __restrict__ G3s, float* __restrict__ dP2,
+                                            DP2Acc& acc, int warp, int lane) {
+  using C = MmaBwd;
+  const int g = lane >> 2, t = lane & 3;
+  const int mt = warp & 1, nt = warp >> 1;
+  const int npairs = m.npairs;
+  for (int q = 0; q < npairs; ++q) {
+    const int e = m.pair[q];
+    const int r0 = e & 255, has2 = (e >> 8) & 1, p = e >> 9;
+    if (p != acc.p) {
+      dp2_flush(acc, dP2, mt, nt, lane);
+      acc.p = p;
+    }
+    // A[j12][(row of pair, j3)] = S[row][j12][j3]; B[(row, j3)][r2] = G3[i3_row][r2][j3]
+    const float* s0 = Ss + r0 * C::SS + (16 * mt + g) * 4 + t;
+    const float* s1 = s0 + C::SS;
+    FragA a;
+    a.v[0] = split_tf32(s0[0]);
+    a.v[1] = split_tf32(s0[32]);
+    a.v[2] = split_tf32(has2 ? s1[0] : 0.f);
+    a.v[3] = split_tf32(has2 ? s1[32] : 0.f);
+    const float* g0 = G3s + r0 * C::GS + (8 * nt + g) * 4 + t;
+    FragB b;
+    b.v[0] = split_tf32(g0[0]);
+    b.v[1] = split_tf32(has2 ? g0[C::GS] : 0.f);
+    if (q & 1) mma_3xtf32_2(acc.c[2], acc.c[3], a, b);
+    else mma_3xtf32_2(acc.c[0], acc.c[1], a, b);
+  }
+}
+
+// (3) over the pairs of one batch: warp w takes m-tile w % 2 (r2 = 16 (w % 2) ..
+// +15) of a contiguous quarter of the pairs.
+__device__ __forceinline__ void mma_bwd_dg3(const MmaBwd::Meta& m, const float* __restrict__ P2,
+                                            const float* __restrict__ Ss, float* __restrict__ dG3,
+                                            int warp, int lane) {
+  using C = MmaBwd;
+  const int g = lane >> 2, t = lane & 3;
+  const int mt = warp & 1, quarter = warp >> 1;
+  const int npairs = m.npairs;
+  const int q0 = (npairs * quarter) >> 2, q1 = (npairs * (quarter + 1)) >> 2;
+  int cur_p = -1;
+  FragA af[4];
+  for (int q = q0; q < q1; ++q) {
+    const int e = m.pair[q];
+    const int r0 = e & 255, has2 = (e >> 8) & 1, p = e >> 9;
+    if (p != cur_p) {
+      cur_p = p;
+      // A[r2][j12] = P2[p][j1 = ks][j2][r2], column-major in (r2, j2)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) af[ks] = load_a_cm(P2 + p * C::QP + ks * C::QA + 16 * mt, C::QB, lane);
+    }
+    // B[j12][(row of pair, j3)] = S[row][j12][j3]
+    const float* sp = Ss + (r0 + (has2 ? (g >> 2) : 0)) * C::SS + (g & 3);
+    float big[2][4], small[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) big[h][i] = small[h][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      FragB b;
+      b.v[0] = split_tf32(sp[(8 * ks + t) * 4]);
+      b.v[1] = split_tf32(sp[(8 * ks + t + 4) * 4]);
+      mma_3xtf32_2(big[ks & 1], small[ks & 1], af[ks], b);
+    }
+    // C[r2][(row of pair, j3)]: this lane holds j3 = 2 (t % 2), +1 of row t / 2
+    if (t < 2 || has2) {
+      float* o = dG3 + (size_t)m.ri3[r0 + (t >> 1)] * (4 * C::R) + (16 * mt + g) * 4 + 2 * (t & 1);
+      red_add_f2(o, (small[0][0] + small[1][0]) + (big[0][0] + big[1][0]),
+                 (small[0][1] + small[1][1]) + (big[0][1] + big[1][1]));
+      red_add_f2(o + 32, (small[0][2] + small[1][2]) + (big[0][2] + big[1][2]),
+                 (small[0][3] + small[1][3]) + (big[0][3] + big[1][3]));
     }
   }
 }
 
-template <int N2, int R, int CP>
-__global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
-  using C = BwsCfg<N2, R, CP>;
-  using T = typename C::T;
-  using Meta = typename C::Meta;
-  constexpr int NC = T::NC, P2S = T::P2S, P2P = T::P2P, D = T::D;
+// (4): dG2[i2][r1][(j2, r2)] += sum over (p, j1) of G1[i1_p][j1][r1] dP2[p][j1][j2][r2];
+// warp w owns j2 = w.
+__device__ __forceinline__ void mma_bwd_dg2(const float* __restrict__ P1n, const float* __restrict__ dP2,
+                                            float* __restrict__ dG2i2, int np, int warp, int lane) {
+  using C = MmaBwd;
+  const int g = lane >> 2, t = lane & 3;
+  float acc[2][4][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
+  for (int ks = 0; 2 * ks < np; ++ks) {
+    const bool second = 2 * ks + 1 < np;        // k = t + 4 belongs to prefix 2 ks + 1
+    FragA af[2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      af[mt] = load_a_cm(P1n + 8 * ks * C::P1S + 16 * mt, C::P1S, lane);
+      if (!second) af[mt].v[2] = af[mt].v[3] = Tf32x2{0u, 0u};
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float* bp = dP2 + 2 * ks * C::QP + t * C::QA + warp * C::QB + 8 * nt + g;
+      FragB b;
+      b.v[0] = split_tf32(bp[0]);
+      b.v[1] = split_tf32(second ? bp[C::QP] : 0.f);
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) mma_3xtf32(acc[mt][nt], af[mt], b);
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float* o = dG2i2 + (size_t)(16 * mt + g + 8 * h) * C::NC + 32 * warp + 2 * t;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) red_add_f2(o + 8 * nt, acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
+    }
+}
+
+// (5): dG1[i1_p][j1][r1] += sum over (j2, r2) of dP2[p][j1][j2][r2] G2[r1][(j2, r2)];
+// warp w takes the tile (p, j1) = 16 (w % 2) .. +15 x r1 = 8 (w / 2) .. +7.
+__device__ __forceinline__ void mma_bwd_dg1(const float* __restrict__ dP2, const float* __restrict__ G2s,
+                                            const int* __restrict__ pi1, float* __restrict__ dG1, int np,
+                                            int warp, int lane) {
+  using C = MmaBwd;
+  const int g = lane >> 2, t = lane & 3;
+  const int mt = warp & 1, nt = warp >> 1;
+  if (16 * mt >= 4 * np) return;
+  // rows (p, j1) = 16 mt + g and + 8
+  const int ra = 16 * mt + g, rb = ra + 8;
+  const float* a0 = dP2 + (ra >> 2) * C::QP + (ra & 3) * C::QA + t;
+  const float* a1 = dP2 + (rb >> 2) * C::QP + (rb & 3) * C::QA + t;
+  const float* bp = G2s + (8 * nt + g) * C::G2S + t;
+  float c[4][4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[u][i] = 0.f;
+#pragma unroll 4
+  for (int ks = 0; ks < C::NC / 8; ++ks) {
+    const int ko = (ks >> 2) * C::QB + 8 * (ks & 3);   // (j2, r2) = 8 ks + t
+    FragA a;
+    a.v[0] = split_tf32(a0[ko]);
+    a.v[1] = split_tf32(a1[ko]);
+    a.v[2] = split_tf32(a0[ko + 4]);
+    a.v[3] = split_tf32(a1[ko + 4]);
+    FragB b;
+    b.v[0] = split_tf32(bp[8 * ks]);
+    b.v[1] = split_tf32(bp[8 * ks + 4]);
+    mma_3xtf32_2(c[2 * (ks & 1)], c[2 * (ks & 1) + 1], a, b);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int row = 16 * mt + g + 8 * h, p = row >> 2;
+    if (p < np) {
+      float* o = dG1 + ((size_t)pi1[p] * 4 + (row & 3)) * C::R + 8 * nt + 2 * t;
+      red_add_f2(o, (c[1][2 * h] + c[3][2 * h]) + (c[0][2 * h] + c[2][2 * h]),
+                 (c[1][2 * h + 1] + c[3][2 * h + 1]) + (c[0][2 * h + 1] + c[2][2 * h + 1]));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
+  using C = MmaBwd;
+  using Meta = C::Meta;
   extern __shared__ float4 sm4[];
   float* base = reinterpret_cast<float*>(sm4);
   float* P2 = base + 2 * C::STAGE_F;
-  float* dP2 = P2 + T::F_P2;
-  float* P1t = dP2;     // transposed G1 rows live in the dP2 area until stage 2 is done
-  Meta* meta = reinterpret_cast<Meta*>(dP2 + T::F_P2);
+  float* dP2 = P2 + C::F_Q;
+  Meta* meta = reinterpret_cast<Meta*>(dP2 + C::F_Q);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
   uint64_t* empty = full + 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    mbar_init(&full[0], 33);
+    mbar_init(&full[1], 33);
     mbar_init(&empty[0], 1);
     mbar_init(&empty[1], 1);
     mbar_init_fence();
@@ -444,8 +660,7 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
   const int n_chunks = a.w.ctl->n_chunks;
 
   if (warp == 8) {
-    // ---------------- producer: claims one chunk ahead (see the forward kernel);
-    // chunks holding a later piece of a hot prefix are skipped
+    // ---------------- producer (claims one chunk ahead)
     auto next_chunk = [&](ChunkDesc& d) {
       for (;;) {
         const int c = claim_chunk(&a.w.ctl->bwd_chunk_ctr);
@@ -462,57 +677,80 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
       Meta& m = meta[s];
       if (c >= n_chunks) {
         if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
-        if (lane == 0) {
-          m.end = 1;
-          mbar_arrive(&full[s]);
-        }
+        if (lane == 0) m.end = 1;
+        __syncwarp();
+        cp_async_arrive_noinc(&full[s]);
+        if (lane == 0) mbar_arrive(&full[s]);
         break;
       }
       const int x0 = d.x0, p0 = d.p0, p1 = d.p1;
       const int x1 = p1 == p0 ? a.w.pair_row_start[p0 + 1] : d.x1;   // a whole hot prefix
-      const int np = p1 - p0 + 1;
-      const int nst = min(x1 - x0, C::RB);
-      int rp = 0, g3 = 0, gi1 = 0;
-      if (lane < nst) {
-        rp = a.w.row_pair[x0 + lane] - p0;
-        g3 = a.w.row_i3[x0 + lane];
+      const int np = p1 - p0 + 1, rows = x1 - x0;
+      const int nb = min(rows, C::RB);
+      int g3 = 0, gi1 = 0, rs = rows;
+      if (lane < nb) g3 = a.w.row_i3[x0 + lane];
+      if (lane < np) {
+        gi1 = a.w.pair_i1[p0 + lane];
+        rs = max(a.w.pair_row_start[p0 + lane], x0) - x0;
       }
-      if (lane < np) gi1 = a.w.pair_i1[p0 + lane];
       const int i2 = a.w.pair_i2[p0];
       ChunkDesc dn{};
       const int cn = next_chunk(dn);
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
       float* G2s = base + s * C::STAGE_F;
-      float* P1n = G2s + T::F_G2;
+      float* P1n = G2s + C::F_G2;
       float* Ss = P1n + C::F_P1;
-      float* G3s = Ss + C::RB * C::SS;
-      if (lane < nst) {
-        m.rp[lane] = rp;
-        m.ri3[lane] = g3;
+      float* G3s = Ss + C::F_S;
+      const float* g2src = a.G2 + (size_t)i2 * C::R * C::NC;
+#pragma unroll 8
+      for (int i = 0; i < C::R * C::NC / 128; ++i) {
+        const int e = i * 32 + lane, row = e >> 6, q = e & 63;
+        cp_async16(G2s + row * C::G2S + 4 * q, g2src + row * C::NC + 4 * q);
       }
-      if (lane < np) m.pi1[lane] = gi1;
+#pragma unroll
+      for (int pp = 0; pp < C::CP; ++pp) {
+        const int i1 = __shfl_sync(0xffffffffu, gi1, pp);
+        const int j1 = lane >> 3, q = lane & 7;
+        if (pp < np)
+          cp_async16(P1n + (4 * pp + j1) * C::P1S + 4 * q, a.G1 + ((size_t)i1 * 4 + j1) * C::R + 4 * q);
+      }
+      for (int r0 = 0; r0 < nb; r0 += 8) {
+        int i3v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) i3v[u] = __shfl_sync(0xffffffffu, g3, (r0 + u) & 31);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (r0 + u < nb) {
+            cp_async16(Ss + (r0 + u) * C::SS + 4 * lane, a.w.rowbuf + (size_t)(x0 + r0 + u) * C::D + 4 * lane);
+            cp_async16(G3s + (r0 + u) * C::GS + 4 * lane, a.G3 + (size_t)i3v[u] * 4 * C::R + 4 * lane);
+          }
+      }
+      cp_async_arrive_noinc(&full[s]);
+      if (lane < C::CP) {
+        m.rs[lane] = rs;
+        m.pi1[lane] = gi1;
+      }
+      if (lane < nb) m.ri3[lane] = g3;
+      int rsq[C::CP];
+#pragma unroll
+      for (int j = 0; j < C::CP; ++j) rsq[j] = __shfl_sync(0xffffffffu, rs, j);
+      const int npairs = bwd_pairs(0, nb, rows, rsq, m.pair, lane);
       __syncwarp();
       if (lane == 0) {
         m.x0 = x0;
         m.x1 = x1;
         m.p0 = p0;
         m.np = np;
-        m.nst = nst;
         m.i2 = i2;
+        m.nb = nb;
+        m.npairs = npairs;
         m.end = 0;
-        const uint32_t bytes = 4u * (T::F_G2 + np * 4 * R + nst * (D + 4 * R));
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(G2s, a.G2 + (size_t)i2 * T::F_G2, 4u * T::F_G2, &full[s]);
-      }
-      __syncwarp();
-      if (lane < np) bulk_g2s(P1n + lane * 4 * R, a.G1 + (size_t)gi1 * 4 * R, 16u * R, &full[s]);
-      if (lane < nst) {
-        bulk_g2s(Ss + lane * C::SS, a.w.rowbuf + (size_t)(x0 + lane) * D, 4u * D, &full[s]);
-        bulk_g2s(G3s + lane * C::GS, a.G3 + (size_t)g3 * 4 * R, 16u * R, &full[s]);
+        mbar_arrive(&full[s]);
       }
       c = cn;
       d = dn;
     }
+    cp_async_wait_all();
     return;
   }
 
@@ -522,224 +760,48 @@ __global__ void __launch_bounds__(288, 1) k_bwd_ws(BwdArgs a) {
     if (!mbar_wait(&full[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
     Meta& m = meta[s];
     if (m.end) break;
-    const int x0 = m.x0, x1 = m.x1, p0 = m.p0, np = m.np;
+    const int x0 = m.x0, x1 = m.x1, np = m.np, rows = x1 - x0;
     const float* G2s = base + s * C::STAGE_F;
-    const float* P1n = G2s + T::F_G2;
+    const float* P1n = G2s + C::F_G2;
     float* Ss = const_cast<float*>(P1n) + C::F_P1;
-    float* G3s = Ss + C::RB * C::SS;
-    stage2_natural<T>(G2s, P1n, P1t, P2, np);
-    for (int e = tid; e < np * P2P; e += 256) dP2[e] = 0.f;
-
-    for (int xb = x0; xb < x1; xb += C::RB) {
-      const int nb = min(C::RB, x1 - xb);
-      if (xb != x0) {
-        // later batches of a hot prefix: the consumers load them into the row area
-        named_sync(1, 256);
-        if (tid < nb) {
-          m.rp[tid] = a.w.row_pair[xb + tid] - p0;
-          m.ri3[tid] = a.w.row_i3[xb + tid];
-        }
-        for (int e = tid; e < nb * (D / 4); e += 256) {
-          const int r = e / (D / 4), q = e - r * (D / 4);
-          *reinterpret_cast<float4*>(Ss + r * C::SS + 4 * q) =
-              reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)(xb + r) * D)[q];
-        }
-        // G3 rows straight into the transposed [j3][b] layout
-        for (int e = tid; e < nb * R; e += 256) {
-          const int r = e / R, b = e - r * R;
-          const float4 v = __ldg(
-              reinterpret_cast<const float4*>(a.G3 + (size_t)a.w.row_i3[xb + r] * 4 * R) + b);
-          float* g = G3s + r * C::GS + b;
-          g[0] = v.x;
-          g[R] = v.y;
-          g[2 * R] = v.z;
-          g[3 * R] = v.w;
-        }
-        named_sync(1, 256);
-      } else {
-        // the staged G3 rows, in place from [b][j3] to [j3][b] (so that the dP2 tiles read
-        // 4 consecutive b per 128-bit load)
-        float4 v[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int e = tid + 256 * q;
-          if (e < nb * R) v[q] = *reinterpret_cast<const float4*>(G3s + (e / R) * C::GS + 4 * (e % R));
-        }
-        named_sync(1, 256);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int e = tid + 256 * q;
-          if (e < nb * R) {
-            float* g = G3s + (e / R) * C::GS + (e % R);
-            g[0] = v[q].x;
-            g[R] = v[q].y;
-            g[2 * R] = v[q].z;
-            g[3 * R] = v[q].w;
-          }
-        }
-        named_sync(1, 256);
-      }
-      // dG3[i3][b][j3] += sum_j12 P2[j12][b] S[j12][j3]: warp = block of 4 b, lane = row
-      // (batches of <= 16 / <= 8 rows: 2 / 4 lanes per row split the j12 sum)
-      if (nb <= 8) bwd_dg3<T, C, 4>(P2, Ss, m.rp, m.ri3, a.dG3, nb, warp, lane);
-      else if (nb <= 16) bwd_dg3<T, C, 2>(P2, Ss, m.rp, m.ri3, a.dG3, nb, warp, lane);
-      else bwd_dg3<T, C, 1>(P2, Ss, m.rp, m.ri3, a.dG3, nb, warp, lane);
-      // dP2[p][j12][b] += sum_j3 S[j12][j3] G3[b][j3]: tile (4 j12 x 4 b) per thread,
-      // row groups walk their rows and flush at every change of prefix
-      {
-        const int tile = tid % C::TILES, rg = tid / C::TILES;
-        const int jb = tile / (R / 4), bq = tile - jb * (R / 4);
-        const int r0 = (rg * nb) / C::RG, r1 = ((rg + 1) * nb) / C::RG;
-        float acc[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-        int cur = -1;
-        for (int r = r0; r < r1; ++r) {
-          const int pl = m.rp[r];
-          if (pl != cur) {
-            if (cur >= 0) {
-              float* d = dP2 + cur * P2P + (4 * jb) * P2S + 4 * bq;
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  atomicAdd(d + i * P2S + j, acc[i][j]);
-                  acc[i][j] = 0.f;
-                }
-            }
-            cur = pl;
-          }
-          float4 sv[4], gv[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            sv[i] = *reinterpret_cast<const float4*>(Ss + r * C::SS + (4 * jb + i) * 4);
-#pragma unroll
-          for (int j3 = 0; j3 < 4; ++j3)
-            gv[j3] = *reinterpret_cast<const float4*>(G3s + r * C::GS + j3 * R + 4 * bq);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float s4[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};
-#pragma unroll
-            for (int j3 = 0; j3 < 4; ++j3) {
-              acc[i][0] = fmaf(s4[j3], gv[j3].x, acc[i][0]);
-              acc[i][1] = fmaf(s4[j3], gv[j3].y, acc[i][1]);
-              acc[i][2] = fmaf(s4[j3], gv[j3].z, acc[i][2]);
-              acc[i][3] = fmaf(s4[j3], gv[j3].w, acc[i][3]);
-            }
-          }
-        }
-        if (cur >= 0) {
-          float* d = dP2 + cur * P2P + (4 * jb) * P2S + 4 * bq;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) atomicAdd(d + i * P2S + j, acc[i][j]);
-        }
-      }
-    }
+    float* G3s = Ss + C::F_S;
+    if (np > 4) mma_bwd_p2<2>(G2s, P1n, P2, warp, lane);
+    else mma_bwd_p2<1>(G2s, P1n, P2, warp, lane);
     named_sync(1, 256);
-    // dG2[i2][a][n] += sum_{p, j1} P1[p][j1][a] dP2[p][j1][n]: warp = block of 4 a,
-    // lane = 4-column groups at stride 128
-    const int i2 = m.i2;
-    {
-      constexpr int Q = NC / 128;
-      for (int ab = warp; ab < R / 4; ab += 8) {
-        float acc[4][4 * Q];
+    DP2Acc acc;
+    acc.p = -1;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
-          for (int j = 0; j < 4 * Q; ++j) acc[i][j] = 0.f;
-        for (int p = 0; p < np; ++p) {
-#pragma unroll
-          for (int j1 = 0; j1 < 4; ++j1) {
-            const float4 a4 = *reinterpret_cast<const float4*>(P1n + p * 4 * R + j1 * R + 4 * ab);
-            const float aw[4] = {a4.x, a4.y, a4.z, a4.w};
-            float bv[4 * Q];
-#pragma unroll
-            for (int q = 0; q < Q; ++q) {
-              const int n = q * 128 + 4 * lane;
-              const int j2 = n / R, b = n - j2 * R;
-              const float4 v = *reinterpret_cast<const float4*>(
-                  dP2 + p * P2P + (j1 * N2 + j2) * P2S + b);
-              bv[4 * q] = v.x; bv[4 * q + 1] = v.y; bv[4 * q + 2] = v.z; bv[4 * q + 3] = v.w;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int j = 0; j < 4 * Q; ++j) acc[i][j] = fmaf(aw[i], bv[j], acc[i][j]);
-          }
+      for (int i = 0; i < 4; ++i) acc.c[u][i] = 0.f;
+    for (int b0 = 0; b0 < rows; b0 += C::RB) {
+      if (b0 > 0) {
+        // later batches (rows of a hot prefix beyond the first RB): loaded here
+        const int nb = min(C::RB, rows - b0);
+        named_sync(1, 256);                      // previous batch fully consumed
+        for (int e = tid; e < nb * 32; e += 256) {
+          const int r = e >> 5, q = e & 31;
+          const int x = x0 + b0 + r;
+          const int i3 = __ldg(a.w.row_i3 + x);
+          *reinterpret_cast<float4*>(Ss + r * C::SS + 4 * q) =
+              reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)x * C::D)[q];
+          *reinterpret_cast<float4*>(G3s + r * C::GS + 4 * q) =
+              __ldg(reinterpret_cast<const float4*>(a.G3 + (size_t)i3 * 4 * C::R) + q);
+          if (q == 0) m.ri3[r] = i3;
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int q = 0; q < Q; ++q) {
-            float4* dst = reinterpret_cast<float4*>(
-                a.dG2 + (size_t)i2 * T::F_G2 + (size_t)(4 * ab + i) * NC + q * 128 + 4 * lane);
-            atomicAdd(dst, make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2],
-                                       acc[i][4 * q + 3]));
-          }
+        if (warp == 0) {
+          const int npairs = bwd_pairs(b0, b0 + nb, rows, m.rs, m.pair, lane);
+          if (lane == 0) m.npairs = npairs;
+        }
+        named_sync(1, 256);
       }
+      mma_bwd_dg3(m, P2, Ss, a.dG3, warp, lane);
+      mma_bwd_dp2(m, Ss, G3s, dP2, acc, warp, lane);
     }
-    // dG1[i1_p][j1][a] += sum_n dP2[p][j1][n] G2[a][n]: item = (prefix, 4 a, n-slice);
-    // the 8 n-slices of an item sit in 8 adjacent lanes and are summed by shuffles
-    {
-      constexpr int AQ = R / 4;
-      const int items = np * AQ * 8;
-      for (int b0 = 0; b0 < items; b0 += 256) {
-        const int item = b0 + tid;
-        const bool valid = item < items;
-        const int ns = item & 7, g = item >> 3;
-        const int p = g / AQ, aq = g - p * AQ;
-        float acc[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-        if (valid) {
-          for (int sgrp = 0; sgrp < NC / 32; ++sgrp) {
-            const int n = 32 * sgrp + 4 * ns;
-            const int j2 = n / R, b = n - j2 * R;
-            float4 dv[4], gv[4];
-#pragma unroll
-            for (int j1 = 0; j1 < 4; ++j1)
-              dv[j1] = *reinterpret_cast<const float4*>(dP2 + p * P2P + (j1 * N2 + j2) * P2S + b);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              gv[i] = *reinterpret_cast<const float4*>(G2s + (4 * aq + i) * NC + n);
-#pragma unroll
-            for (int j1 = 0; j1 < 4; ++j1)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                float v = acc[j1][i];
-                v = fmaf(dv[j1].x, gv[i].x, v);
-                v = fmaf(dv[j1].y, gv[i].y, v);
-                v = fmaf(dv[j1].z, gv[i].z, v);
-                v = fmaf(dv[j1].w, gv[i].w, v);
-                acc[j1][i] = v;
-              }
-          }
-        }
-#pragma unroll
-        for (int j1 = 0; j1 < 4; ++j1)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float v = acc[j1][i];
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            v += __shfl_xor_sync(0xffffffffu, v, 4);
-            acc[j1][i] = v;
-          }
-        if (valid && ns == 0) {
-          const int i1 = m.pi1[p];
-#pragma unroll
-          for (int j1 = 0; j1 < 4; ++j1)
-            atomicAdd(reinterpret_cast<float4*>(a.dG1 + ((size_t)i1 * 4 + j1) * R + 4 * aq),
-                      make_float4(acc[j1][0], acc[j1][1], acc[j1][2], acc[j1][3]));
-        }
-      }
-    }
+    dp2_flush(acc, dP2, warp & 1, warp >> 1, lane);
+    named_sync(1, 256);
+    mma_bwd_dg2(P1n, dP2, a.dG2 + (size_t)m.i2 * C::R * C::NC, np, warp, lane);
+    mma_bwd_dg1(dP2, G2s, m.pi1, a.dG1, np, warp, lane);
     named_sync(1, 256);
     if (tid == 0) mbar_arrive(&empty[s]);
   }
@@ -819,14 +881,12 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   ba.dG2 = core_grads[1];
   ba.dG3 = core_grads[2];
   if (s.n1 == 4 && s.n3 == 4 && s.n2 == 8 && s.R1 == 32 && s.R2 == 32) {
-    using C = BwsCfg<8, 32, kCP_8_32>;
     static int grid = 0;
     if (grid == 0) {
-      cudaFuncSetAttribute(k_bwd_ws<8, 32, kCP_8_32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::SMEM);
-      grid = persistent_grid_bwd((const void*)k_bwd_ws<8, 32, kCP_8_32>, 288, C::SMEM);
+      cudaFuncSetAttribute(k_bwd_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, MmaBwd::SMEM);
+      grid = persistent_grid_bwd((const void*)k_bwd_mma, MmaBwd::THREADS, MmaBwd::SMEM);
     }
-    TT_TIMED("k_bwd_ws", st, (k_bwd_ws<8, 32, kCP_8_32><<<grid, 288, C::SMEM, st>>>(ba)));
+    TT_TIMED("k_bwd_mma", st, (k_bwd_mma<<<grid, MmaBwd::THREADS, MmaBwd::SMEM, st>>>(ba)));
   } else {
     const size_t g2n = (size_t)s.R1 * s.n2 * s.R2;
     const size_t base = g2n + (size_t)s.n1 * s.R1 + 2 * (size_t)s.n1 * s.n2 * s.R2;

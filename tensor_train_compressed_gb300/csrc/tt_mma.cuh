@@ -74,11 +74,38 @@ __device__ __forceinline__ FragB load_b(const float* B, int ldb, int lane) {
   return f;
 }
 
+// A[m][k] at A[m + k * ldk] (column-major), rows 0 .. 15, columns 0 .. 7.
+__device__ __forceinline__ FragA load_a_cm(const float* A, int ldk, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const float* c0 = A + g + t * ldk;
+  const float* c4 = A + g + (t + 4) * ldk;
+  FragA f;
+  f.v[0] = split_tf32(c0[0]);
+  f.v[1] = split_tf32(c0[8]);
+  f.v[2] = split_tf32(c4[0]);
+  f.v[3] = split_tf32(c4[8]);
+  return f;
+}
+
 // c += a.b with the three-term split (small terms first).
 __device__ __forceinline__ void mma_3xtf32(float c[4], const FragA& a, const FragB& b) {
   mma_tf32(c, a.v[0].lo, a.v[1].lo, a.v[2].lo, a.v[3].lo, b.v[0].hi, b.v[1].hi);
   mma_tf32(c, a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].lo, b.v[1].lo);
   mma_tf32(c, a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].hi, b.v[1].hi);
+}
+
+// Same product with the hi.hi term and the two small terms in separate
+// accumulators (two independent dependency chains).
+__device__ __forceinline__ void mma_3xtf32_2(float big[4], float small[4], const FragA& a,
+                                             const FragB& b) {
+  mma_tf32(small, a.v[0].lo, a.v[1].lo, a.v[2].lo, a.v[3].lo, b.v[0].hi, b.v[1].hi);
+  mma_tf32(big, a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].hi, b.v[1].hi);
+  mma_tf32(small, a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].lo, b.v[1].lo);
+}
+
+// Float pair atomically added to global memory (no return value).
+__device__ __forceinline__ void red_add_f2(float* p, float x, float y) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(x), "f"(y) : "memory");
 }
 
 }  // namespace tt
