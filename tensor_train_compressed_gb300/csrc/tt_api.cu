@@ -91,6 +91,13 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
   L.coop = take(coop_scratch_bytes());
   // one extra row, kept at zero, that out-of-range lookups point at while pooling
   L.rowbuf = take(sizeof(float) * ((size_t)L.rowbuf_rows + 1) * (size_t)s.D);
+  if (tc_shape(s)) {
+    const size_t n1 = (size_t)s.m1 * s.n1 * s.R1, n2 = (size_t)s.m2 * s.R1 * s.n2 * s.R2;
+    L.g1h = take(2 * n1);
+    L.g1l = take(2 * n1);
+    L.g2h = take(2 * n2);
+    L.g2l = take(2 * n2);
+  }
   L.total = off;
   return L;
 }
@@ -118,6 +125,11 @@ WS make_ws(void* base, const Layout& L) {
   w.chunk_status = reinterpret_cast<uint32_t*>(b + L.chunk_status);
   w.coop = b + L.coop;
   w.rowbuf = reinterpret_cast<float*>(b + L.rowbuf);
+  const bool split = L.g2l != 0;
+  w.g1h = split ? reinterpret_cast<uint16_t*>(b + L.g1h) : nullptr;
+  w.g1l = split ? reinterpret_cast<uint16_t*>(b + L.g1l) : nullptr;
+  w.g2h = split ? reinterpret_cast<uint16_t*>(b + L.g2h) : nullptr;
+  w.g2l = split ? reinterpret_cast<uint16_t*>(b + L.g2l) : nullptr;
   return w;
 }
 

@@ -362,18 +362,22 @@ __global__ void __launch_bounds__(256) k_bwd_generic(BwdArgs a) {
 // Core gradients are accumulated with vector float reductions.
 struct MmaBwd {
   static constexpr int CP = kCP_8_32, R = 32, NC = 256, D = 128;
-  static constexpr int RB = 24;                     // rows per batch
+  static constexpr int RB = 32;                     // rows per batch
   static constexpr int MAXPAIRS = RB / 2 + CP;      // pairs of one batch
-  static constexpr int G2S = NC + 4;                // G2 row (r1) stride
-  static constexpr int P1S = R + 4;                 // G1 row ((p, j1)) stride
+  // G2 and G1 staged as bf16 hi / lo planes: G2 rows (r1) of 264 bf16 (528 B),
+  // G1 rows ((p, j1)) of 40 bf16 (80 B); dP2 as bf16 planes [(p, j1)][(j2, r2)]
+  static constexpr int G2LD = NC + 8, G1LD = R + 8, DPLD = NC + 8;
+  static constexpr int G2PLANE = R * G2LD * 2, G1PLANE = 4 * CP * G1LD * 2, DPPLANE = 4 * CP * DPLD * 2;
   static constexpr int SS = D + 16;                 // S row stride (rows of a pair 16 banks apart)
   static constexpr int GS = 4 * R + 16;             // G3 row stride
-  static constexpr int QB = R + 8;                  // P2 / dP2 [p][j1][j2][r2]: j2 stride
+  static constexpr int QB = R + 8;                  // P2 [p][j1][j2][r2] (fp32): j2 stride
   static constexpr int QA = 8 * QB + 8;             //   j1 stride
   static constexpr int QP = 4 * QA + 4;             //   p stride
-  static constexpr int F_G2 = R * G2S, F_P1 = CP * 4 * P1S, F_S = (RB + 1) * SS, F_G3 = (RB + 1) * GS;
+  static constexpr int F_G2 = G2PLANE / 2, F_P1 = G1PLANE / 2;          // floats (two planes)
+  static constexpr int F_S = (RB + 1) * SS, F_G3 = (RB + 1) * GS;
   static constexpr int STAGE_F = F_G2 + F_P1 + F_S + F_G3;
-  static constexpr int F_Q = CP * QP;
+  static constexpr int F_Q = CP * QP;                // P2
+  static constexpr int F_DP = DPPLANE / 2;           // dP2 (two planes)
   struct Meta {
     int x0, x1, p0, np, i2, nb, npairs, end;
     int rs[CP];          // chunk-local first row of each prefix
@@ -382,7 +386,7 @@ struct MmaBwd {
     int pair[MAXPAIRS];  // batch-local first row | (second row valid) << 8 | prefix << 9
   };
   static constexpr int THREADS = 288;
-  static constexpr int SMEM = 4 * (2 * STAGE_F + 2 * F_Q) + 2 * (int)sizeof(Meta) + 4 * 8;
+  static constexpr int SMEM = 4 * (2 * STAGE_F + F_Q + F_DP) + 2 * (int)sizeof(Meta) + 4 * 8;
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(RB <= 32 && CP <= 8, "one row per producer lane; pair encoding");
 };
@@ -414,12 +418,15 @@ __device__ __forceinline__ int bwd_pairs(int b0, int b1, int rows, const int* rs
   return n;
 }
 
-// (1): P2 rows (p, j1) = 16 MT tiles x 256 columns; warp w owns j2 = w.
+// (1): P2 rows (p, j1) = 16 MT tiles x 256 columns; warp w owns j2 = w.  bf16
+// three-term tiles: A = G1 rows (plain ldmatrix), B = G2 [r1][(j2, r2)] (transposed).
 template <int MT>
 __device__ __forceinline__ void mma_bwd_p2(const float* __restrict__ G2s, const float* __restrict__ P1n,
                                            float* __restrict__ P2, int warp, int lane) {
   using C = MmaBwd;
   const int g = lane >> 2, t = lane & 3;
+  const uint32_t g2h = smem_addr(G2s), g2l = g2h + C::G2PLANE;
+  const uint32_t g1h = smem_addr(P1n), g1l = g1h + C::G1PLANE;
   float acc[MT][4][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
@@ -428,15 +435,23 @@ __device__ __forceinline__ void mma_bwd_p2(const float* __restrict__ G2s, const 
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
 #pragma unroll
-  for (int ks = 0; ks < 4; ++ks) {
-    FragA af[MT];
+  for (int ks = 0; ks < C::R / 16; ++ks) {
+    uint32_t ah[MT][4], al[MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) af[mt] = load_a(P1n + 16 * mt * C::P1S + 8 * ks, C::P1S, 8 * C::P1S, lane);
+    for (int mt = 0; mt < MT; ++mt) {
+      ldsm_x4(ah[mt], a_addr_mk(g1h, C::G1LD, 16 * mt, 16 * ks, lane));
+      ldsm_x4(al[mt], a_addr_mk(g1l, C::G1LD, 16 * mt, 16 * ks, lane));
+    }
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const FragB bf = load_b(G2s + 8 * ks * C::G2S + 32 * warp + 8 * nt, C::G2S, lane);
+    for (int np2 = 0; np2 < 2; ++np2) {
+      uint32_t bh[4], bl[4];
+      ldsm_x4_t(bh, b2_addr_kn(g2h, C::G2LD, 16 * ks, 32 * warp + 16 * np2, lane));
+      ldsm_x4_t(bl, b2_addr_kn(g2l, C::G2LD, 16 * ks, 32 * warp + 16 * np2, lane));
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) mma_3xtf32(acc[mt][nt], af[mt], bf);
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+          mma_bf16x3(acc[mt][2 * np2 + h], ah[mt], al[mt], bh[2 * h], bh[2 * h + 1], bl[2 * h], bl[2 * h + 1]);
     }
   }
 #pragma unroll
@@ -465,10 +480,16 @@ __device__ __forceinline__ void dp2_flush(DP2Acc& acc, float* __restrict__ dP2, 
     float v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = (acc.c[1][i] + acc.c[3][i]) + (acc.c[0][i] + acc.c[2][i]);
-    // rows j12 = 16 mt + g (+8): j1 = 2 mt (+1), j2 = g
-    float* dst = dP2 + acc.p * C::QP + 2 * mt * C::QA + g * C::QB + 8 * nt + 2 * t;
-    *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
-    *reinterpret_cast<float2*>(dst + C::QA) = make_float2(v[2], v[3]);
+    // rows j12 = 16 mt + g (+8): j1 = 2 mt (+1), j2 = g; plane row (p, j1), column (j2, r2)
+    char* hi = reinterpret_cast<char*>(dP2) +
+               2 * (((4 * acc.p + 2 * mt) * C::DPLD) + g * C::R + 8 * nt + 2 * t);
+    uint32_t h0, l0, h1, l1;
+    split_bf16x2(v[0], v[1], h0, l0);
+    split_bf16x2(v[2], v[3], h1, l1);
+    *reinterpret_cast<uint32_t*>(hi) = h0;
+    *reinterpret_cast<uint32_t*>(hi + C::DPPLANE) = l0;
+    *reinterpret_cast<uint32_t*>(hi + 2 * C::DPLD) = h1;
+    *reinterpret_cast<uint32_t*>(hi + 2 * C::DPLD + C::DPPLANE) = l1;
   }
 #pragma unroll
   for (int u = 0; u < 4; ++u)
@@ -555,11 +576,15 @@ __device__ __forceinline__ void mma_bwd_dg3(const MmaBwd::Meta& m, const float* 
 }
 
 // (4): dG2[i2][r1][(j2, r2)] += sum over (p, j1) of G1[i1_p][j1][r1] dP2[p][j1][j2][r2];
-// warp w owns j2 = w.
+// warp w owns columns 32 w .. 32 w + 31.  bf16 tiles: A = G1 rows read transposed
+// ([k = (p, j1)][m = r1]), B = dP2 planes [k = (p, j1)][n] (transposed); the k range
+// is padded to 16 with rows that the caller has zeroed in both operands.
 __device__ __forceinline__ void mma_bwd_dg2(const float* __restrict__ P1n, const float* __restrict__ dP2,
                                             float* __restrict__ dG2i2, int np, int warp, int lane) {
   using C = MmaBwd;
   const int g = lane >> 2, t = lane & 3;
+  const uint32_t g1h = smem_addr(P1n), g1l = g1h + C::G1PLANE;
+  const uint32_t dph = smem_addr(dP2), dpl = dph + C::DPPLANE;
   float acc[2][4][4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt)
@@ -567,22 +592,24 @@ __device__ __forceinline__ void mma_bwd_dg2(const float* __restrict__ P1n, const
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
-  for (int ks = 0; 2 * ks < np; ++ks) {
-    const bool second = 2 * ks + 1 < np;        // k = t + 4 belongs to prefix 2 ks + 1
-    FragA af[2];
+  const int kk = (np + 3) >> 2;
+  for (int ks = 0; ks < kk; ++ks) {
+    uint32_t ah[2][4], al[2][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      af[mt] = load_a_cm(P1n + 8 * ks * C::P1S + 16 * mt, C::P1S, lane);
-      if (!second) af[mt].v[2] = af[mt].v[3] = Tf32x2{0u, 0u};
+      ldsm_x4_t(ah[mt], a_addr_km(g1h, C::G1LD, 16 * mt, 16 * ks, lane));
+      ldsm_x4_t(al[mt], a_addr_km(g1l, C::G1LD, 16 * mt, 16 * ks, lane));
     }
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const float* bp = dP2 + 2 * ks * C::QP + t * C::QA + warp * C::QB + 8 * nt + g;
-      FragB b;
-      b.v[0] = split_tf32(bp[0]);
-      b.v[1] = split_tf32(second ? bp[C::QP] : 0.f);
+    for (int np2 = 0; np2 < 2; ++np2) {
+      uint32_t bh[4], bl[4];
+      ldsm_x4_t(bh, b2_addr_kn(dph, C::DPLD, 16 * ks, 32 * warp + 16 * np2, lane));
+      ldsm_x4_t(bl, b2_addr_kn(dpl, C::DPLD, 16 * ks, 32 * warp + 16 * np2, lane));
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) mma_3xtf32(acc[mt][nt], af[mt], b);
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+          mma_bf16x3(acc[mt][2 * np2 + h], ah[mt], al[mt], bh[2 * h], bh[2 * h + 1], bl[2 * h], bl[2 * h + 1]);
     }
   }
 #pragma unroll
@@ -596,7 +623,8 @@ __device__ __forceinline__ void mma_bwd_dg2(const float* __restrict__ P1n, const
 }
 
 // (5): dG1[i1_p][j1][r1] += sum over (j2, r2) of dP2[p][j1][j2][r2] G2[r1][(j2, r2)];
-// warp w takes the tile (p, j1) = 16 (w % 2) .. +15 x r1 = 8 (w / 2) .. +7.
+// warp w takes the tile (p, j1) = 16 (w % 2) .. +15 x r1 = 8 (w / 2) .. +7.  bf16 tiles:
+// A = dP2 planes [m = (p, j1)][k] (plain), B = G2 [n = r1][k = (j2, r2)] (plain).
 __device__ __forceinline__ void mma_bwd_dg1(const float* __restrict__ dP2, const float* __restrict__ G2s,
                                             const int* __restrict__ pi1, float* __restrict__ dG1, int np,
                                             int warp, int lane) {
@@ -604,36 +632,28 @@ __device__ __forceinline__ void mma_bwd_dg1(const float* __restrict__ dP2, const
   const int g = lane >> 2, t = lane & 3;
   const int mt = warp & 1, nt = warp >> 1;
   if (16 * mt >= 4 * np) return;
-  // rows (p, j1) = 16 mt + g and + 8
-  const int ra = 16 * mt + g, rb = ra + 8;
-  const float* a0 = dP2 + (ra >> 2) * C::QP + (ra & 3) * C::QA + t;
-  const float* a1 = dP2 + (rb >> 2) * C::QP + (rb & 3) * C::QA + t;
-  const float* bp = G2s + (8 * nt + g) * C::G2S + t;
-  float c[4][4];
+  const uint32_t dph = smem_addr(dP2), dpl = dph + C::DPPLANE;
+  const uint32_t g2h = smem_addr(G2s), g2l = g2h + C::G2PLANE;
+  float c[2][4];
 #pragma unroll
-  for (int u = 0; u < 4; ++u)
+  for (int u = 0; u < 2; ++u)
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[u][i] = 0.f;
-#pragma unroll 4
-  for (int ks = 0; ks < C::NC / 8; ++ks) {
-    const int ko = (ks >> 2) * C::QB + 8 * (ks & 3);   // (j2, r2) = 8 ks + t
-    FragA a;
-    a.v[0] = split_tf32(a0[ko]);
-    a.v[1] = split_tf32(a1[ko]);
-    a.v[2] = split_tf32(a0[ko + 4]);
-    a.v[3] = split_tf32(a1[ko + 4]);
-    FragB b;
-    b.v[0] = split_tf32(bp[8 * ks]);
-    b.v[1] = split_tf32(bp[8 * ks + 4]);
-    mma_3xtf32_2(c[2 * (ks & 1)], c[2 * (ks & 1) + 1], a, b);
+#pragma unroll
+  for (int ks = 0; ks < C::NC / 16; ++ks) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    ldsm_x4(ah, a_addr_mk(dph, C::DPLD, 16 * mt, 16 * ks, lane));
+    ldsm_x4(al, a_addr_mk(dpl, C::DPLD, 16 * mt, 16 * ks, lane));
+    ldsm_x2(bh, b1_addr_nk(g2h, C::G2LD, 16 * ks, 8 * nt, lane));
+    ldsm_x2(bl, b1_addr_nk(g2l, C::G2LD, 16 * ks, 8 * nt, lane));
+    mma_bf16x3(c[ks & 1], ah, al, bh[0], bh[1], bl[0], bl[1]);
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int row = 16 * mt + g + 8 * h, p = row >> 2;
     if (p < np) {
       float* o = dG1 + ((size_t)pi1[p] * 4 + (row & 3)) * C::R + 8 * nt + 2 * t;
-      red_add_f2(o, (c[1][2 * h] + c[3][2 * h]) + (c[0][2 * h] + c[2][2 * h]),
-                 (c[1][2 * h + 1] + c[3][2 * h + 1]) + (c[0][2 * h + 1] + c[2][2 * h + 1]));
+      red_add_f2(o, c[0][2 * h] + c[1][2 * h], c[0][2 * h + 1] + c[1][2 * h + 1]);
     }
   }
 }
@@ -644,8 +664,8 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
   extern __shared__ float4 sm4[];
   float* base = reinterpret_cast<float*>(sm4);
   float* P2 = base + 2 * C::STAGE_F;
-  float* dP2 = P2 + C::F_Q;
-  Meta* meta = reinterpret_cast<Meta*>(dP2 + C::F_Q);
+  float* dP2 = P2 + C::F_Q;                         // bf16 planes
+  Meta* meta = reinterpret_cast<Meta*>(dP2 + C::F_DP);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
   uint64_t* empty = full + 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -701,18 +721,24 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
       float* P1n = G2s + C::F_G2;
       float* Ss = P1n + C::F_P1;
       float* G3s = Ss + C::F_S;
-      const float* g2src = a.G2 + (size_t)i2 * C::R * C::NC;
+      {
+        const uint16_t* h2 = a.w.g2h + (size_t)i2 * C::R * C::NC;
+        const uint16_t* l2 = a.w.g2l + (size_t)i2 * C::R * C::NC;
+        char* dst = reinterpret_cast<char*>(G2s);
 #pragma unroll 8
-      for (int i = 0; i < C::R * C::NC / 128; ++i) {
-        const int e = i * 32 + lane, row = e >> 6, q = e & 63;
-        cp_async16(G2s + row * C::G2S + 4 * q, g2src + row * C::NC + 4 * q);
+        for (int i = 0; i < 2 * C::R * C::NC / 256; ++i) {
+          const int e = i * 32 + lane, plane = e >> 10, row = (e >> 5) & 31, q = e & 31;
+          cp_async16(dst + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * q,
+                     (plane ? l2 : h2) + row * C::NC + 8 * q);
+        }
       }
 #pragma unroll
       for (int pp = 0; pp < C::CP; ++pp) {
         const int i1 = __shfl_sync(0xffffffffu, gi1, pp);
-        const int j1 = lane >> 3, q = lane & 7;
+        const int plane = lane >> 4, j1 = (lane >> 2) & 3, q = lane & 3;
         if (pp < np)
-          cp_async16(P1n + (4 * pp + j1) * C::P1S + 4 * q, a.G1 + ((size_t)i1 * 4 + j1) * C::R + 4 * q);
+          cp_async16(reinterpret_cast<char*>(P1n) + plane * C::G1PLANE + (4 * pp + j1) * (2 * C::G1LD) + 16 * q,
+                     (plane ? a.w.g1l : a.w.g1h) + ((size_t)i1 * 4 + j1) * C::R + 8 * q);
       }
       for (int r0 = 0; r0 < nb; r0 += 8) {
         int i3v[8];
@@ -767,6 +793,23 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
     float* G3s = Ss + C::F_S;
     if (np > 4) mma_bwd_p2<2>(G2s, P1n, P2, warp, lane);
     else mma_bwd_p2<1>(G2s, P1n, P2, warp, lane);
+    {
+      // rows (p, j1) from 4 np up to the next multiple of 16 enter the k range of (4):
+      // zero them in both bf16 operands (G1 rows: 5 pieces of 16 B per plane row;
+      // dP2 rows: 33 pieces)
+      const int r0 = 4 * np, r1 = 16 * ((np + 3) >> 2);
+      const int nz = (r1 - r0) * 2;            // plane rows
+      for (int e = tid; e < nz * 38; e += 256) {
+        const int pr = e / 38, q = e - pr * 38, plane = pr & 1, row = r0 + (pr >> 1);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        if (q < 5)
+          *reinterpret_cast<uint4*>(reinterpret_cast<char*>(const_cast<float*>(P1n)) + plane * C::G1PLANE +
+                                    row * (2 * C::G1LD) + 16 * q) = z;
+        else
+          *reinterpret_cast<uint4*>(reinterpret_cast<char*>(dP2) + plane * C::DPPLANE + row * (2 * C::DPLD) +
+                                    16 * (q - 5)) = z;
+      }
+    }
     named_sync(1, 256);
     DP2Acc acc;
     acc.p = -1;
@@ -880,7 +923,9 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   ba.dG1 = core_grads[0];
   ba.dG2 = core_grads[1];
   ba.dG3 = core_grads[2];
-  if (s.n1 == 4 && s.n3 == 4 && s.n2 == 8 && s.R1 == 32 && s.R2 == 32) {
+  if (tc_shape(s)) {
+    const int rc = launch_split(s, w, cores, st);
+    if (rc) return rc;
     static int grid = 0;
     if (grid == 0) {
       cudaFuncSetAttribute(k_bwd_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, MmaBwd::SMEM);

@@ -180,13 +180,15 @@ struct MmaFwd {
   static constexpr int ROWMAX = 64;                  // G3 rows staged per chunk
   static constexpr int MAXROWS = CP * 32;            // rows of one chunk (CP prefixes x 32)
   static constexpr int MAXPAIRS = MAXROWS / 2 + CP;
-  static constexpr int G2S = NC + 8;                 // G2 row (r1) stride
-  static constexpr int P1S = R + 4;                  // G1 row ((p, j1)) stride
-  static constexpr int G3S = 4 * R + 16;             // staged G3 row stride
+  // G2 and G1 are staged as bf16 hi / lo planes (k_split_cores): G2 rows (r1)
+  // of 264 bf16 (528 B), G1 rows ((p, j1)) of 40 bf16 (80 B)
+  static constexpr int G2LD = NC + 8, G1LD = R + 8;
+  static constexpr int G2PLANE = R * G2LD * 2, G1PLANE = 4 * CP * G1LD * 2;   // bytes
+  static constexpr int G3S = 4 * R + 16;             // staged G3 row stride (floats)
   static constexpr int P2B = R + 4;                  // P2[p][j1][j2][r2]: j2 stride
   static constexpr int P2A = 8 * P2B + 8;            //   j1 stride
   static constexpr int P2P = 4 * P2A;                //   p stride
-  static constexpr int F_G2 = R * G2S, F_P1 = CP * 4 * P1S, F_G3 = (ROWMAX + 1) * G3S;
+  static constexpr int F_G2 = G2PLANE / 2, F_P1 = G1PLANE / 2, F_G3 = (ROWMAX + 1) * G3S;   // floats
   static constexpr int STAGE_F = F_G2 + F_P1 + F_G3;
   static constexpr int F_P2 = CP * P2P;
   struct Meta {
@@ -202,33 +204,43 @@ struct MmaFwd {
 };
 
 // P2 rows (p, j1) = 16 MT tiles x 256 columns (j2, r2); consumer warp w owns
-// columns NCW w .. NCW (w+1) - 1.
+// columns 32 w .. 32 w + 31.  bf16 three-term tiles from the staged planes:
+// A = G1 rows [(p, j1)][r1] (plain ldmatrix), B = G2 [r1][(j2, r2)] (transposed).
 template <int CW, int MT>
 __device__ __forceinline__ void mma_fwd_stage2(const float* __restrict__ G2s,
                                                const float* __restrict__ P1n,
                                                float* __restrict__ P2, int warp, int lane) {
   using C = MmaFwd<CW>;
-  constexpr int NT = C::NCW / 8;
+  static_assert(C::NCW == 32, "eight consumer warps");
   const int g = lane >> 2, t = lane & 3;
-  float acc[MT][NT][4];
+  const uint32_t g2h = smem_addr(G2s), g2l = g2h + C::G2PLANE;
+  const uint32_t g1h = smem_addr(P1n), g1l = g1h + C::G1PLANE;
+  float acc[MT][4][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
   const int col0 = warp * C::NCW;
 #pragma unroll
-  for (int ks = 0; ks < 4; ++ks) {
-    FragA af[MT];
+  for (int ks = 0; ks < C::R / 16; ++ks) {
+    uint32_t ah[MT][4], al[MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-      af[mt] = load_a(P1n + 16 * mt * C::P1S + 8 * ks, C::P1S, 8 * C::P1S, lane);
+    for (int mt = 0; mt < MT; ++mt) {
+      ldsm_x4(ah[mt], a_addr_mk(g1h, C::G1LD, 16 * mt, 16 * ks, lane));
+      ldsm_x4(al[mt], a_addr_mk(g1l, C::G1LD, 16 * mt, 16 * ks, lane));
+    }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const FragB bf = load_b(G2s + 8 * ks * C::G2S + col0 + 8 * nt, C::G2S, lane);
+    for (int np2 = 0; np2 < 2; ++np2) {
+      uint32_t bh[4], bl[4];
+      ldsm_x4_t(bh, b2_addr_kn(g2h, C::G2LD, 16 * ks, col0 + 16 * np2, lane));
+      ldsm_x4_t(bl, b2_addr_kn(g2l, C::G2LD, 16 * ks, col0 + 16 * np2, lane));
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) mma_3xtf32(acc[mt][nt], af[mt], bf);
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+          mma_bf16x3(acc[mt][2 * np2 + h], ah[mt], al[mt], bh[2 * h], bh[2 * h + 1], bl[2 * h], bl[2 * h + 1]);
     }
   }
 #pragma unroll
@@ -238,7 +250,7 @@ __device__ __forceinline__ void mma_fwd_stage2(const float* __restrict__ G2s,
       const int row = 16 * mt + g + 8 * h;          // (p, j1)
       float* dst = P2 + (row >> 2) * C::P2P + (row & 3) * C::P2A + 2 * t;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+      for (int nt = 0; nt < 4; ++nt) {
         const int n0 = col0 + 8 * nt;               // (j2, r2) = (n0 / 32, n0 % 32 + 2t)
         *reinterpret_cast<float2*>(dst + (n0 >> 5) * C::P2B + (n0 & 31)) =
             make_float2(acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
@@ -391,20 +403,26 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
       float* G2s = base + s * C::STAGE_F;
       float* P1n = G2s + C::F_G2;
       float* G3s = P1n + C::F_P1;
-      // G2[i2]: 32 rows of 64 16-byte pieces
-      const float* g2src = a.G2 + (size_t)cur.i2 * C::R * C::NC;
+      // G2[i2] planes: 32 rows x 32 16-byte pieces each
+      {
+        const uint16_t* h2 = a.w.g2h + (size_t)cur.i2 * C::R * C::NC;
+        const uint16_t* l2 = a.w.g2l + (size_t)cur.i2 * C::R * C::NC;
+        char* dst = reinterpret_cast<char*>(G2s);
 #pragma unroll 8
-      for (int i = 0; i < C::R * C::NC / 128; ++i) {
-        const int e = i * 32 + lane, row = e >> 6, q = e & 63;
-        cp_async16(G2s + row * C::G2S + 4 * q, g2src + row * C::NC + 4 * q);
+        for (int i = 0; i < 2 * C::R * C::NC / 256; ++i) {
+          const int e = i * 32 + lane, plane = e >> 10, row = (e >> 5) & 31, q = e & 31;
+          cp_async16(dst + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * q,
+                     (plane ? l2 : h2) + row * C::NC + 8 * q);
+        }
       }
-      // G1[i1_p]: 4 rows of 8 pieces per prefix
+      // G1[i1_p] planes: per prefix, lane = plane | j1 | piece
 #pragma unroll
       for (int pp = 0; pp < C::CP; ++pp) {
         const int i1 = __shfl_sync(0xffffffffu, cur.gi1, pp);
-        const int j1 = lane >> 3, q = lane & 7;
+        const int plane = lane >> 4, j1 = (lane >> 2) & 3, q = lane & 3;
         if (pp < cur.np)
-          cp_async16(P1n + (4 * pp + j1) * C::P1S + 4 * q, a.G1 + ((size_t)i1 * 4 + j1) * C::R + 4 * q);
+          cp_async16(reinterpret_cast<char*>(P1n) + plane * C::G1PLANE + (4 * pp + j1) * (2 * C::G1LD) + 16 * q,
+                     (plane ? a.w.g1l : a.w.g1h) + ((size_t)i1 * 4 + j1) * C::R + 8 * q);
       }
       // G3[i3_x]: 32 pieces per row, 8 rows per batch of independent shuffles
       for (int r0 = 0; r0 < cur.nst; r0 += 8) {
@@ -579,8 +597,8 @@ static size_t fwd_generic_smem(const Shape& s, int CP) {
 enum FwdKind { kFwdGeneric = 0, kFwdTiled_8_32, kFwdTiled_8_64, kFwdTiled_4_16 };
 
 static FwdKind fwd_kind(const Shape& s) {
+  if (tc_shape(s)) return kFwdTiled_8_32;
   if (s.n1 != 4 || s.n3 != 4 || s.R1 != s.R2) return kFwdGeneric;
-  if (s.n2 == 8 && s.R1 == 32) return kFwdTiled_8_32;
   if (s.n2 == 8 && s.R1 == 64) return kFwdTiled_8_64;
   if (s.n2 == 4 && s.R1 == 16) return kFwdTiled_4_16;
   return kFwdGeneric;
@@ -648,7 +666,11 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
   fa.G2 = cores[1];
   fa.G3 = cores[2];
   switch (fwd_kind(s)) {
-    case kFwdTiled_8_32: launch_fwd_mma<16>(fa, st); break;
+    case kFwdTiled_8_32:
+      rc = launch_split(s, w, cores, st);
+      if (rc) return rc;
+      launch_fwd_mma<8>(fa, st);
+      break;
     case kFwdTiled_8_64: launch_tiled<8, 64, kCP_8_64>(fa, st); break;
     case kFwdTiled_4_16: launch_tiled<4, 16, kCP_4_16>(fa, st); break;
     default: {

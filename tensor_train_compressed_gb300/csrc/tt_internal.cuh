@@ -65,6 +65,7 @@ struct Layout {
   size_t ctl, hist, sort_status, keysA, keysB, bag_of, uid, perm;
   size_t row_start, row_i3, row_pair, pair_row_start, pair_i1, pair_i2;
   size_t seg_status, chunk_start, chunk_desc, chunk_status, coop, rowbuf, total;
+  size_t g1h, g1l, g2h, g2l;   // bf16 split planes of G1 and G2 (tensor-core shape only)
   int key_bits, passes, n_sort_tiles, n_scan_tiles;
   int64_t rowbuf_rows;
 };
@@ -91,7 +92,16 @@ struct WS {
   uint32_t* chunk_status;           // [n_scan_tiles]
   void* coop;                       // scratch of the cooperative grouping
   float* rowbuf;                    // [rowbuf_rows + 1][D]; the last row stays zero
+  uint16_t* g1h;                    // bf16 planes hi / lo of G1 [m1][n1][R1] and G2
+  uint16_t* g1l;                    // [m2][R1][n2 R2] (x = hi + lo + O(2^-18 |x|)), written
+  uint16_t* g2h;                    // per call by k_split_cores; null unless the shape
+  uint16_t* g2l;                    // runs the tensor-core chunk kernels
 };
+
+// Shapes served by the tensor-core chunk kernels (n1 = n3 = 4, n2 = 8, R1 = R2 = 32).
+inline bool tc_shape(const Shape& s) {
+  return s.n1 == 4 && s.n2 == 8 && s.n3 == 4 && s.R1 == 32 && s.R2 == 32;
+}
 
 // ---------------------------------------------------------------- device helpers
 
@@ -259,6 +269,7 @@ int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chu
 int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out,
                     const float* const cores[3], const int64_t* offsets, int64_t nnz,
                     int64_t num_bags, float* const core_grads[3], cudaStream_t st);
+int launch_split(const Shape& s, const WS& w, const float* const cores[3], cudaStream_t st);
 int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, float lr,
                int zero_grads, cudaStream_t st);
 

@@ -19,6 +19,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 
 namespace tt {
 
@@ -101,6 +102,84 @@ __device__ __forceinline__ void mma_3xtf32_2(float big[4], float small[4], const
   mma_tf32(small, a.v[0].lo, a.v[1].lo, a.v[2].lo, a.v[3].lo, b.v[0].hi, b.v[1].hi);
   mma_tf32(big, a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].hi, b.v[1].hi);
   mma_tf32(small, a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].lo, b.v[1].lo);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 three-term tiles for the prefix-level products.  Operands are stored as
+// two bf16 planes, hi = x rounded to bf16 and lo = (x - hi) rounded to bf16
+// (|x - hi - lo| <= 2^-18 |x|), and multiplied as a_lo.b_hi + a_hi.b_lo +
+// a_hi.b_hi with mma.m16n8k16 (fp32 accumulate): relative error about 1e-5
+// per product against fp32's 6e-8, at twice the multiply-adds per tensor
+// instruction of TF32 and with no per-use splitting.  Fragments come straight
+// from shared memory by ldmatrix (8 x 8 b16 matrices, one 16-byte row address
+// per lane), with .trans for an operand stored along the other axis, so one
+// plane layout serves both products that read it.  Rows of every plane are
+// padded to an odd multiple of 16 bytes (conflict-free ldmatrix).
+
+__device__ __forceinline__ void ldsm_x4(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t r[2], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+
+// Byte address of this lane's row for the 16 x 16 A fragment (rows m0.., k0..):
+// of a [m][k] plane (plain load) or a [k][m] plane (transposed load); ld in
+// bf16 elements, base a shared-memory byte address.
+__device__ __forceinline__ uint32_t a_addr_mk(uint32_t base, int ld, int m0, int k0, int lane) {
+  const int i = lane >> 3, r = lane & 7;
+  return base + 2u * (uint32_t)((m0 + 8 * (i & 1) + r) * ld + k0 + 8 * (i >> 1));
+}
+__device__ __forceinline__ uint32_t a_addr_km(uint32_t base, int ld, int m0, int k0, int lane) {
+  const int i = lane >> 3, r = lane & 7;
+  return base + 2u * (uint32_t)((k0 + 8 * (i >> 1) + r) * ld + m0 + 8 * (i & 1));
+}
+// B fragments of the two n-tiles n0.., n0+8.. (k0 .. k0+15): regs {0,1} and {2,3};
+// of a [k][n] plane (transposed load) or a [n][k] plane (plain load).
+__device__ __forceinline__ uint32_t b2_addr_kn(uint32_t base, int ld, int k0, int n0, int lane) {
+  const int i = lane >> 3, r = lane & 7;
+  return base + 2u * (uint32_t)((k0 + 8 * (i & 1) + r) * ld + n0 + 8 * (i >> 1));
+}
+__device__ __forceinline__ uint32_t b2_addr_nk(uint32_t base, int ld, int k0, int n0, int lane) {
+  const int i = lane >> 3, r = lane & 7;
+  return base + 2u * (uint32_t)((n0 + 8 * (i >> 1) + r) * ld + k0 + 8 * (i & 1));
+}
+// B fragment of one n-tile of a [n][k] plane (x2 load: lanes 0-15 give the rows).
+__device__ __forceinline__ uint32_t b1_addr_nk(uint32_t base, int ld, int k0, int n0, int lane) {
+  const int i = (lane >> 3) & 1, r = lane & 7;
+  return base + 2u * (uint32_t)((n0 + r) * ld + k0 + 8 * i);
+}
+
+__device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// c += a.b, three-term bf16 split (small terms first)
+__device__ __forceinline__ void mma_bf16x3(float c[4], const uint32_t ah[4], const uint32_t al[4],
+                                           uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
+  mma_bf16(c, al, bh0, bh1);
+  mma_bf16(c, ah, bl0, bl1);
+  mma_bf16(c, ah, bh0, bh1);
+}
+
+// (x, y) -> packed bf16x2 words of the hi and lo planes
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // Float pair atomically added to global memory (no return value).

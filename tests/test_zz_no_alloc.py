@@ -42,7 +42,10 @@ def test_static_forward_matches_workspace_forward_twice():
         pytest.skip("needs a GPU")
     from tensor_train_compressed_gb300 import build
     build.build()
-    first = make_inputs(3, num_bags=1000)                     # 20k lookups, 12M-row table
+    # 15k lookups into a 720,000-row table of the benchmark tables' factor shape (its
+    # bf16 split planes fit the array with the rest of the scratch)
+    first = make_custom((100, 60, 120), (4, 8, 4), (1, 32, 32, 1), num_bags=1000, max_len=30,
+                        seed=71)
     second = make_custom((5, 6, 7), (4, 8, 4), (1, 32, 32, 1), num_bags=700, max_len=9,
                          seed=77, empty_frac=0.1)             # a different shape right after
     for x in (first, second):
@@ -56,7 +59,7 @@ def test_static_forward_matches_workspace_forward_twice():
 def test_static_forward_rejects_sizes_beyond_its_array():
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
-    x = make_inputs(3, num_bags=3000)                         # ~60k lookups: > 16 MiB of scratch
+    x = make_inputs(3, num_bags=3000)                         # ~60k lookups, 12M rows: > 16 MiB
     assert tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags) > 16 << 20
     cores = [_dev(c) for c in x.cores]
     out = torch.empty((x.num_bags, x.D), dtype=torch.float32, device="cuda")
