@@ -196,8 +196,8 @@ struct MmaFwd {
     int pair[MAXPAIRS];   // first row | (second row valid) << 8 | chunk-local prefix << 9
   };
   static constexpr int NCW = NC / CW;                // stage-2 columns per consumer warp
-  static constexpr int THREADS = 32 * CW + 32;
-  static constexpr int SMEM = 4 * (2 * STAGE_F + F_P2) + 2 * (int)sizeof(Meta) + 4 * 8;
+  static constexpr int THREADS = 32 * CW + 64;       // consumers, lead producer, G2 copier
+  static constexpr int SMEM = 4 * (2 * STAGE_F + F_P2) + 2 * (int)sizeof(Meta) + 6 * 8 + 16;
   static_assert(CW == 8 || CW == 16, "8 or 16 consumer warps");
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(MAXROWS <= 256 && CP <= 8 && 4 * CP <= 32, "pair encoding and G1 staging");
@@ -341,21 +341,58 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
   Meta* meta = reinterpret_cast<Meta*>(P2 + C::F_P2);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
   uint64_t* empty = full + 2;
+  uint64_t* go = empty + 2;                          // lead producer -> G2 copier, per stage
+  volatile int* slot = reinterpret_cast<volatile int*>(go + 2);   // the stage's i2, or -1: stop
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    // full: 32 producer lanes' copy arrivals + the producer's metadata arrival
-    mbar_init(&full[0], 33);
-    mbar_init(&full[1], 33);
+    // full: the copy arrivals of both producer warps' 64 lanes + the lead's metadata arrival
+    mbar_init(&full[0], 65);
+    mbar_init(&full[1], 65);
     mbar_init(&empty[0], 1);
     mbar_init(&empty[1], 1);
+    mbar_init(&go[0], 1);
+    mbar_init(&go[1], 1);
     mbar_init_fence();
   }
   __syncthreads();
   const int n_chunks = a.w.ctl->n_chunks;
 
+  if (warp == CW + 1) {
+    // ---------------- G2 copier: stages the G2 planes of the chunks the lead
+    // producer hands over, one stage at a time
+    for (int it = 0;; ++it) {
+      const int s = it & 1;
+      if (!mbar_wait(&go[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
+      const int i2 = slot[s];
+      if (i2 >= 0) {
+        const uint16_t* h2 = a.w.g2h + (size_t)i2 * C::R * C::NC;
+        const uint16_t* l2 = a.w.g2l + (size_t)i2 * C::R * C::NC;
+        char* dst = reinterpret_cast<char*>(base + s * C::STAGE_F);
+#pragma unroll 8
+        for (int i = 0; i < 2 * C::R * C::NC / 256; ++i) {
+          const int e = i * 32 + lane, plane = e >> 10, row = (e >> 5) & 31, q = e & 31;
+          cp_async16(dst + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * q,
+                     (plane ? l2 : h2) + row * C::NC + 8 * q);
+        }
+      }
+      cp_async_arrive_noinc(&full[s]);
+      if (i2 < 0) break;
+    }
+    cp_async_wait_all();
+    return;
+  }
+
   if (warp == CW) {
-    // ---------------- producer.  Software-pipelined: while chunk i is staged,
+    // ---------------- lead producer.  Software-pipelined: while chunk i is staged,
     // the metadata loads of chunk i+1 and the claim of chunk i+2 are in flight.
+    // The G2 copier is released for a stage only once that stage is free.
+    auto release = [&](int s, int i2) {
+      __syncwarp();
+      if (lane == 0) {
+        slot[s] = i2;
+        mbar_arrive(&go[s]);
+      }
+    };
     struct PMeta {
       int x0, x1, p0, np, nst, i2;
       int g30, g31;    // i3 of staged rows lane, lane + 32
@@ -390,7 +427,9 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
       const uint32_t use = (uint32_t)it >> 1;
       Meta& m = meta[s];
       if (c >= n_chunks) {
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
+        const bool ok = use == 0 || mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl);
+        release(s, -1);
+        if (!ok) break;
         if (lane == 0) m.end = 1;
         __syncwarp();
         cp_async_arrive_noinc(&full[s]);
@@ -399,22 +438,14 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
       }
       if (cn < n_chunks) load_meta(dn, nxt);
       const int cnn = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
-      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
+      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) {
+        release(s, -1);
+        break;
+      }
+      release(s, cur.i2);
       float* G2s = base + s * C::STAGE_F;
       float* P1n = G2s + C::F_G2;
       float* G3s = P1n + C::F_P1;
-      // G2[i2] planes: 32 rows x 32 16-byte pieces each
-      {
-        const uint16_t* h2 = a.w.g2h + (size_t)cur.i2 * C::R * C::NC;
-        const uint16_t* l2 = a.w.g2l + (size_t)cur.i2 * C::R * C::NC;
-        char* dst = reinterpret_cast<char*>(G2s);
-#pragma unroll 8
-        for (int i = 0; i < 2 * C::R * C::NC / 256; ++i) {
-          const int e = i * 32 + lane, plane = e >> 10, row = (e >> 5) & 31, q = e & 31;
-          cp_async16(dst + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * q,
-                     (plane ? l2 : h2) + row * C::NC + 8 * q);
-        }
-      }
       // G1[i1_p] planes: per prefix, lane = plane | j1 | piece
 #pragma unroll
       for (int pp = 0; pp < C::CP; ++pp) {
