@@ -497,35 +497,50 @@ __device__ __forceinline__ void dp2_flush(DP2Acc& acc, float* __restrict__ dP2, 
     for (int i = 0; i < 4; ++i) acc.c[u][i] = 0.f;
 }
 
-// (2) over the pairs of one batch.
+// (2) over the pairs of one batch, four pairs per step: the pair entries and
+// the split operands of all four are loaded before their products, so that one
+// round of shared-memory latency covers four pairs.
 __device__ __forceinline__ void mma_bwd_dp2(const MmaBwd::Meta& m, const float* __restrict__ Ss,
                                             const float* __restrict__ G3s, float* __restrict__ dP2,
                                             DP2Acc& acc, int warp, int lane) {
   using C = MmaBwd;
+  constexpr int U = 4;
   const int g = lane >> 2, t = lane & 3;
   const int mt = warp & 1, nt = warp >> 1;
   const int npairs = m.npairs;
-  for (int q = 0; q < npairs; ++q) {
-    const int e = m.pair[q];
-    const int r0 = e & 255, has2 = (e >> 8) & 1, p = e >> 9;
-    if (p != acc.p) {
-      dp2_flush(acc, dP2, mt, nt, lane);
-      acc.p = p;
+  for (int q0 = 0; q0 < npairs; q0 += U) {
+    int e[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) e[u] = q0 + u < npairs ? m.pair[q0 + u] : -1;
+    FragA a[U];
+    FragB b[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      // past the last pair: reload the first (in bounds), no product
+      const int eu = e[u] < 0 ? e[0] : e[u];
+      const int r0 = eu & 255, has2 = (eu >> 8) & 1;
+      // A[j12][(row of pair, j3)] = S[row][j12][j3]; B[(row, j3)][r2] = G3[i3_row][r2][j3]
+      const float* s0 = Ss + r0 * C::SS + (16 * mt + g) * 4 + t;
+      const float* s1 = s0 + C::SS;
+      a[u].v[0] = split_tf32(s0[0]);
+      a[u].v[1] = split_tf32(s0[32]);
+      a[u].v[2] = split_tf32(has2 ? s1[0] : 0.f);
+      a[u].v[3] = split_tf32(has2 ? s1[32] : 0.f);
+      const float* g0 = G3s + r0 * C::GS + (8 * nt + g) * 4 + t;
+      b[u].v[0] = split_tf32(g0[0]);
+      b[u].v[1] = split_tf32(has2 ? g0[C::GS] : 0.f);
     }
-    // A[j12][(row of pair, j3)] = S[row][j12][j3]; B[(row, j3)][r2] = G3[i3_row][r2][j3]
-    const float* s0 = Ss + r0 * C::SS + (16 * mt + g) * 4 + t;
-    const float* s1 = s0 + C::SS;
-    FragA a;
-    a.v[0] = split_tf32(s0[0]);
-    a.v[1] = split_tf32(s0[32]);
-    a.v[2] = split_tf32(has2 ? s1[0] : 0.f);
-    a.v[3] = split_tf32(has2 ? s1[32] : 0.f);
-    const float* g0 = G3s + r0 * C::GS + (8 * nt + g) * 4 + t;
-    FragB b;
-    b.v[0] = split_tf32(g0[0]);
-    b.v[1] = split_tf32(has2 ? g0[C::GS] : 0.f);
-    if (q & 1) mma_3xtf32_2(acc.c[2], acc.c[3], a, b);
-    else mma_3xtf32_2(acc.c[0], acc.c[1], a, b);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (e[u] < 0) break;
+      const int p = e[u] >> 9;
+      if (p != acc.p) {
+        dp2_flush(acc, dP2, mt, nt, lane);
+        acc.p = p;
+      }
+      if (u & 1) mma_3xtf32_2(acc.c[2], acc.c[3], a[u], b[u]);
+      else mma_3xtf32_2(acc.c[0], acc.c[1], a[u], b[u]);
+    }
   }
 }
 
