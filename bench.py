@@ -42,15 +42,51 @@ FLUSH_BYTES = 512 << 20
 
 
 def peaks():
-    """Measured HBM bandwidth and SM clock of this machine, else the recipe's fallback."""
-    p = {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+    """Measured HBM bandwidth, bf16 tensor rate and SM clock of this machine, else the
+    recipe's fallback."""
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "source": "fallback"}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
         p.update(hbm_gbs=float(d.get("hbm_gbs", p["hbm_gbs"])),
+                 bf16_tflops=float(d.get("bf16_tflops", p["bf16_tflops"])),
                  sm_max_mhz=float(d.get("sm_max_mhz", p["sm_max_mhz"])), source="measured")
     return p
+
+
+# Kernels whose fp32-accurate contractions run as three-term split products on
+# the tensor cores (three tensor products per fp32-accurate product).
+TENSOR_SPLIT_KERNELS = ("k_fwd_mma", "k_bwd_mma")
+
+
+def kernel_sources_hash() -> str:
+    """Hash of the CUDA sources, to tell whether a stored ncu capture is current."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_train_compressed_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+    `kernel` on `workload` from the committed ncu summary, or None when that
+    capture was taken on other kernel sources than these."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_sources_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload and parts[3] == src:
+                return int(parts[2])
+    return None
 
 
 def fp32_peak_tflops(sm_count: int, mhz: float) -> float:
@@ -390,8 +426,8 @@ def run_ours(args, rank, world, dist):
         launches_per_step = {k: v[1] for k, v in r["kern"].items()}
         reps = max(3, min(args.steps, 10))
         flops = {"k_fwd_generic": a["fwd_contract"], "k_fwd_tiled": a["fwd_contract"],
-                 "k_fwd_ws": a["fwd_contract"], "k_fwd_mma": a["fwd_contract"], "k_bwd_generic": a["bwd_contract"],
-                 "k_bwd_ws": a["bwd_contract"], "k_bwd_mma": a["bwd_contract"], "k_pool": a["pool"], "k_s_gather": a["s_gather"]}
+                 "k_fwd_mma": a["fwd_contract"], "k_bwd_generic": a["bwd_contract"],
+                 "k_bwd_mma": a["bwd_contract"], "k_pool": a["pool"], "k_s_gather": a["s_gather"]}
         per_launch_ms = kms[dom] / max(1, launches_per_step[dom] / reps)
         out = {"kernel": dom, "share": round(kms[dom] / sum(kms.values()), 4)}
         # algorithmic bytes of the non-contraction kernels (DRAM-level minimum)
@@ -406,17 +442,25 @@ def run_ours(args, rank, world, dist):
         if dom in nbytes and dom not in flops:
             ach = nbytes[dom] / (per_launch_ms * 1e-3) / 1e9
             out.update(bound="hbm", achieved=round(ach, 1), peak=pk["hbm_gbs"], unit="GB/s",
-                       frac=round(ach / pk["hbm_gbs"], 4), traffic=None,
+                       frac=round(ach / pk["hbm_gbs"], 4), traffic=stored_traffic(dom, which),
                        algorithmic_bytes_per_launch=nbytes[dom],
                        avg_launch_ms=round(per_launch_ms, 5))
         elif dom in flops:
             ach = flops[dom] / (per_launch_ms * 1e-3) / 1e12
             out.update(bound="alu", achieved=round(ach, 3), peak=round(p_fp32, 2),
-                       unit="TFLOP/s", frac=round(ach / p_fp32, 4), traffic=None,
+                       unit="TFLOP/s", frac=round(ach / p_fp32, 4),
+                       traffic=stored_traffic(dom, which),
                        algorithmic_flop_per_launch=flops[dom],
                        avg_launch_ms=round(per_launch_ms, 5),
                        peak_source=f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x "
-                                   f"{pk['sm_max_mhz']:.0f} MHz")
+                                   f"{pk['sm_max_mhz']:.0f} MHz (fp32-accurate arithmetic)")
+            if dom in TENSOR_SPLIT_KERNELS:
+                pt = pk["bf16_tflops"] / 3.0
+                out["roofline_tensor"] = {
+                    "bound": "tensor", "achieved": round(ach, 3), "peak": round(pt, 1),
+                    "unit": "TFLOP/s", "frac": round(ach / pt, 4),
+                    "peak_source": f"measured bf16 dense burst {pk['bf16_tflops']:.1f} TFLOP/s / 3 "
+                                   "tensor products per fp32-accurate product (three-term split)"}
         else:
             out.update(bound="hbm", achieved=None, peak=pk["hbm_gbs"], unit="GB/s", frac=None,
                        traffic=None, avg_launch_ms=round(per_launch_ms, 5))
