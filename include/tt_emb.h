@@ -93,7 +93,9 @@ int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_
  * ACCUMULATED (+=) with d<grad_out, out>/dG_k; the caller zeroes them.
  * grad_out is float32 [num_bags][D].  With reuse_grouping != 0 the grouping
  * left in the workspace by the last tt_emb_forward / tt_emb_group on the SAME
- * indices, offsets and shape is reused (the caller guarantees that);
+ * indices, offsets and shape is reused (the caller guarantees that, and that
+ * the cores' contents did not change since that call: the bf16 split of the
+ * cores made by that forward is reused too when the core addresses match);
  * otherwise it is rebuilt.  The accumulation uses float atomics, so the
  * summation order (and the last bits) may differ from call to call. */
 int tt_emb_backward(const float* grad_out, const float* const cores[3], const int64_t m[3],

@@ -97,6 +97,11 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
     L.g1l = take(2 * n1);
     L.g2h = take(2 * n2);
     L.g2l = take(2 * n2);
+    const size_t n3 = (size_t)s.m3 * s.R2 * s.n3;
+    L.g3h = take(2 * n3);
+    L.g3l = take(2 * n3);
+    L.g3th = take(2 * n3);
+    L.g3tl = take(2 * n3);
   }
   L.total = off;
   return L;
@@ -130,6 +135,10 @@ WS make_ws(void* base, const Layout& L) {
   w.g1l = split ? reinterpret_cast<uint16_t*>(b + L.g1l) : nullptr;
   w.g2h = split ? reinterpret_cast<uint16_t*>(b + L.g2h) : nullptr;
   w.g2l = split ? reinterpret_cast<uint16_t*>(b + L.g2l) : nullptr;
+  w.g3h = split ? reinterpret_cast<uint16_t*>(b + L.g3h) : nullptr;
+  w.g3l = split ? reinterpret_cast<uint16_t*>(b + L.g3l) : nullptr;
+  w.g3th = split ? reinterpret_cast<uint16_t*>(b + L.g3th) : nullptr;
+  w.g3tl = split ? reinterpret_cast<uint16_t*>(b + L.g3tl) : nullptr;
   return w;
 }
 
@@ -243,7 +252,8 @@ int tt_emb_backward(const float* grad_out, const float* const cores[3], const in
     rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, st);
     if (rc) return rc;
   }
-  return launch_backward(s, L, w, grad_out, cores, offsets, nnz, num_bags, core_grads, st);
+  return launch_backward(s, L, w, grad_out, reuse_grouping ? 1 : 0, cores, offsets, nnz, num_bags,
+                         core_grads, st);
 }
 
 int tt_emb_sgd(float* const cores[3], float* const core_grads[3], const int64_t m[3],

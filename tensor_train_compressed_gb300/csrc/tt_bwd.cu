@@ -348,36 +348,38 @@ __global__ void __launch_bounds__(256) k_bwd_generic(BwdArgs a) {
 // Warp 8 is a producer: it claims the next chunk (skipping chunks that hold a
 // later piece of a hot prefix: the chunk that starts such a prefix takes all of
 // its rows, so that its prefix-level products are formed once), lists the row
-// pairs of the first batch and stages the G2 slice, the G1 rows and the first
-// batch's S and G3 rows with 16-byte cp.async copies (per-lane mbarrier
-// arrivals), double-buffered.  Warps 0-7 consume with m16n8k8 TF32 tiles
-// (three-term split, fp32 accuracy; tt_mma.cuh):
-//   (1) P2 = [G1 rows] . G2[i2]                     (4 np) x 256 x 32
+// pairs of the first batch and stages the chunk's operands into the free one of
+// two stage buffers, all as bf16 hi / lo planes: G2 and G1 (copies of the
+// per-call split planes), the first batch's G3 rows (copies of the split G3
+// planes, [r2][j3] per row) and its S rows (converted here from the fp32
+// unique-row buffer into [j3][(j1, j2)] per row).  Warps 0-7 consume with
+// three-term bf16 tensor-core tiles (tt_mma.cuh), fragments by ldmatrix:
+//   (1) P2 = [G1 rows] . G2[i2]                     (4 np) x 256 x 32, m16n8k16
 //   per batch of RB rows, by pairs of rows of one prefix:
-//   (2) dP2[p] += S[x] . G3[i3_x]^T                  32 x 32 x (4 per row)
-//   (3) dG3[i3_x] += P2[p]^T . S[x]                  32 x (4 per row) x 32
+//   (2) dP2[p] += S[x] . G3[i3_x]^T                  32 x 32 x (4 per row), m16n8k8
+//   (3) dG3[i3_x] += P2[p]^T . S[x]                  32 x (4 per row) x 32, m16n8k16
 //   then
 //   (4) dG2[i2] += [G1 rows]^T . dP2                 32 x 256 x (4 np)
 //   (5) dG1[i1_p] += dP2[p] . G2[i2]^T               (4 np) x 32 x 256
-// Core gradients are accumulated with vector float reductions.
+// A pair's missing second row reads a zero row.  Core gradients are
+// accumulated with vector float reductions.
 struct MmaBwd {
   static constexpr int CP = kCP_8_32, R = 32, NC = 256, D = 128;
-  static constexpr int RB = 32;                     // rows per batch
+  static constexpr int RB = 24;                     // rows per batch (row RB of a stage stays zero)
   static constexpr int MAXPAIRS = RB / 2 + CP;      // pairs of one batch
-  // G2 and G1 staged as bf16 hi / lo planes: G2 rows (r1) of 264 bf16 (528 B),
-  // G1 rows ((p, j1)) of 40 bf16 (80 B); dP2 as bf16 planes [(p, j1)][(j2, r2)]
+  // bf16 plane geometry (elements / bytes)
   static constexpr int G2LD = NC + 8, G1LD = R + 8, DPLD = NC + 8;
   static constexpr int G2PLANE = R * G2LD * 2, G1PLANE = 4 * CP * G1LD * 2, DPPLANE = 4 * CP * DPLD * 2;
-  static constexpr int SS = D + 16;                 // S row stride (rows of a pair 16 banks apart)
-  static constexpr int GS = 4 * R + 16;             // G3 row stride
-  static constexpr int QB = R + 8;                  // P2 [p][j1][j2][r2] (fp32): j2 stride
-  static constexpr int QA = 8 * QB + 8;             //   j1 stride
-  static constexpr int QP = 4 * QA + 4;             //   p stride
-  static constexpr int F_G2 = G2PLANE / 2, F_P1 = G1PLANE / 2;          // floats (two planes)
-  static constexpr int F_S = (RB + 1) * SS, F_G3 = (RB + 1) * GS;
-  static constexpr int STAGE_F = F_G2 + F_P1 + F_S + F_G3;
-  static constexpr int F_Q = CP * QP;                // P2
-  static constexpr int F_DP = DPPLANE / 2;           // dP2 (two planes)
+  static constexpr int SROW = 4 * (32 + 8) * 2;     // S plane row: [j3][(j1, j2)], 80-byte j3 rows
+  static constexpr int GROW = (4 * R + 32) * 2;     // G3 plane row: [r2][j3], 320 bytes
+  static constexpr int SPLANE = (RB + 1) * SROW, GPLANE = (RB + 1) * GROW;
+  // P2 planes [p][j1][j2][r2]: j2 rows of 80 B, j1 blocks of 656 B, prefixes 2624 B apart
+  static constexpr int PB = 80, PA = 8 * PB + 16, PPB = 4 * PA;
+  static constexpr int P2PLANE = CP * PPB;
+  // stage layout (bytes)
+  static constexpr int OFF_G1 = 2 * G2PLANE, OFF_S = OFF_G1 + 2 * G1PLANE, OFF_G3 = OFF_S + 2 * SPLANE;
+  static constexpr int STAGE_B = OFF_G3 + 2 * GPLANE;
+  static constexpr int OFF_P2 = 2 * STAGE_B, OFF_DP = OFF_P2 + 2 * P2PLANE, OFF_META = OFF_DP + 2 * DPPLANE;
   struct Meta {
     int x0, x1, p0, np, i2, nb, npairs, end;
     int rs[CP];          // chunk-local first row of each prefix
@@ -386,8 +388,9 @@ struct MmaBwd {
     int pair[MAXPAIRS];  // batch-local first row | (second row valid) << 8 | prefix << 9
   };
   static constexpr int THREADS = 288;
-  static constexpr int SMEM = 4 * (2 * STAGE_F + F_Q + F_DP) + 2 * (int)sizeof(Meta) + 4 * 8;
+  static constexpr int SMEM = OFF_META + 2 * (int)sizeof(Meta) + 4 * 8;
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(STAGE_B % 16 == 0 && OFF_S % 16 == 0 && OFF_G3 % 16 == 0 && OFF_META % 16 == 0, "alignment");
   static_assert(RB <= 32 && CP <= 8, "one row per producer lane; pair encoding");
 };
 
@@ -418,15 +421,30 @@ __device__ __forceinline__ int bwd_pairs(int b0, int b1, int rows, const int* rs
   return n;
 }
 
+// S row x (fp32 [(j1, j2)][j3], lane l's float4 = (j1, j2) = l, j3 = 0..3) -> bf16
+// planes [j3][(j1, j2)] of stage row r: eight 2-byte stores.
+__device__ __forceinline__ void bwd_store_s(char* Sp, int r, float4 v, int l) {
+  using C = MmaBwd;
+  const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x[c]);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(x[c] - __bfloat162float(h));
+    char* o = Sp + r * C::SROW + c * 80 + 2 * l;
+    *reinterpret_cast<__nv_bfloat16*>(o) = h;
+    *reinterpret_cast<__nv_bfloat16*>(o + C::SPLANE) = lo;
+  }
+}
+
 // (1): P2 rows (p, j1) = 16 MT tiles x 256 columns; warp w owns j2 = w.  bf16
-// three-term tiles: A = G1 rows (plain ldmatrix), B = G2 [r1][(j2, r2)] (transposed).
+// three-term tiles: A = G1 rows (plain ldmatrix), B = G2 [r1][(j2, r2)]
+// (transposed).  P2 is kept as bf16 planes for (3).
 template <int MT>
-__device__ __forceinline__ void mma_bwd_p2(const float* __restrict__ G2s, const float* __restrict__ P1n,
-                                           float* __restrict__ P2, int warp, int lane) {
+__device__ __forceinline__ void mma_bwd_p2(uint32_t g2h, uint32_t g1h, char* __restrict__ P2, int warp,
+                                           int lane) {
   using C = MmaBwd;
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t g2h = smem_addr(G2s), g2l = g2h + C::G2PLANE;
-  const uint32_t g1h = smem_addr(P1n), g1l = g1h + C::G1PLANE;
+  const uint32_t g2l = g2h + C::G2PLANE, g1l = g1h + C::G1PLANE;
   float acc[MT][4][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
@@ -454,15 +472,20 @@ __device__ __forceinline__ void mma_bwd_p2(const float* __restrict__ G2s, const 
           mma_bf16x3(acc[mt][2 * np2 + h], ah[mt], al[mt], bh[2 * h], bh[2 * h + 1], bl[2 * h], bl[2 * h + 1]);
     }
   }
+  // row (p, j1) = 16 mt + g (+8), columns j2 = warp, r2 = 8 nt + 2t (+1)
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = 16 * mt + g + 8 * h;
-      float* dst = P2 + (row >> 2) * C::QP + (row & 3) * C::QA + warp * C::QB + 2 * t;
+      char* dst = P2 + (row >> 2) * C::PPB + (row & 3) * C::PA + warp * C::PB + 4 * t;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-        *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
+      for (int nt = 0; nt < 4; ++nt) {
+        uint32_t hi, lo;
+        split_bf16x2(acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1], hi, lo);
+        *reinterpret_cast<uint32_t*>(dst + 16 * nt) = hi;
+        *reinterpret_cast<uint32_t*>(dst + 16 * nt + C::P2PLANE) = lo;
+      }
     }
 }
 
@@ -473,7 +496,7 @@ struct DP2Acc {
   int p;
 };
 
-__device__ __forceinline__ void dp2_flush(DP2Acc& acc, float* __restrict__ dP2, int mt, int nt, int lane) {
+__device__ __forceinline__ void dp2_flush(DP2Acc& acc, char* __restrict__ dP2, int mt, int nt, int lane) {
   using C = MmaBwd;
   const int g = lane >> 2, t = lane & 3;
   if (acc.p >= 0) {
@@ -481,8 +504,7 @@ __device__ __forceinline__ void dp2_flush(DP2Acc& acc, float* __restrict__ dP2, 
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = (acc.c[1][i] + acc.c[3][i]) + (acc.c[0][i] + acc.c[2][i]);
     // rows j12 = 16 mt + g (+8): j1 = 2 mt (+1), j2 = g; plane row (p, j1), column (j2, r2)
-    char* hi = reinterpret_cast<char*>(dP2) +
-               2 * (((4 * acc.p + 2 * mt) * C::DPLD) + g * C::R + 8 * nt + 2 * t);
+    char* hi = dP2 + 2 * (((4 * acc.p + 2 * mt) * C::DPLD) + g * C::R + 8 * nt + 2 * t);
     uint32_t h0, l0, h1, l1;
     split_bf16x2(v[0], v[1], h0, l0);
     split_bf16x2(v[2], v[3], h1, l1);
@@ -497,38 +519,36 @@ __device__ __forceinline__ void dp2_flush(DP2Acc& acc, float* __restrict__ dP2, 
     for (int i = 0; i < 4; ++i) acc.c[u][i] = 0.f;
 }
 
-// (2) over the pairs of one batch, four pairs per step: the pair entries and
-// the split operands of all four are loaded before their products, so that one
-// round of shared-memory latency covers four pairs.
-__device__ __forceinline__ void mma_bwd_dp2(const MmaBwd::Meta& m, const float* __restrict__ Ss,
-                                            const float* __restrict__ G3s, float* __restrict__ dP2,
-                                            DP2Acc& acc, int warp, int lane) {
+// (2) over the pairs of one batch, four pairs per step, bf16 m16n8k8 tiles:
+// A[j12][(row of pair, j3)] from the S planes (transposed ldmatrix, rows
+// (row, j3)), B[(row, j3)][r2] = G3[i3_row][r2][j3] (32-bit loads of j3 pairs).
+__device__ __forceinline__ void mma_bwd_dp2(const MmaBwd::Meta& m, uint32_t Sh, const char* __restrict__ G3p,
+                                            char* __restrict__ dP2, DP2Acc& acc, int warp, int lane) {
   using C = MmaBwd;
   constexpr int U = 4;
   const int g = lane >> 2, t = lane & 3;
   const int mt = warp & 1, nt = warp >> 1;
   const int npairs = m.npairs;
+  const int lr = lane & 7, lj = (lane >> 3) & 1;
   for (int q0 = 0; q0 < npairs; q0 += U) {
     int e[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) e[u] = q0 + u < npairs ? m.pair[q0 + u] : -1;
-    FragA a[U];
-    FragB b[U];
+    uint32_t ah[U][2], al[U][2], bh[U], bl[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      // past the last pair: reload the first (in bounds), no product
       const int eu = e[u] < 0 ? e[0] : e[u];
       const int r0 = eu & 255, has2 = (eu >> 8) & 1;
-      // A[j12][(row of pair, j3)] = S[row][j12][j3]; B[(row, j3)][r2] = G3[i3_row][r2][j3]
-      const float* s0 = Ss + r0 * C::SS + (16 * mt + g) * 4 + t;
-      const float* s1 = s0 + C::SS;
-      a[u].v[0] = split_tf32(s0[0]);
-      a[u].v[1] = split_tf32(s0[32]);
-      a[u].v[2] = split_tf32(has2 ? s1[0] : 0.f);
-      a[u].v[3] = split_tf32(has2 ? s1[32] : 0.f);
-      const float* g0 = G3s + r0 * C::GS + (8 * nt + g) * 4 + t;
-      b[u].v[0] = split_tf32(g0[0]);
-      b[u].v[1] = split_tf32(has2 ? g0[C::GS] : 0.f);
+      // ldmatrix rows k = (row of pair, j3): lanes 0-7 (and 8-15) give row lr
+      const int xr = (lr >> 2) == 0 ? r0 : (has2 ? r0 + 1 : C::RB);
+      const uint32_t aa = Sh + xr * C::SROW + (lr & 3) * 80 + 2 * (16 * mt + 8 * lj);
+      ldsm_x2_t(ah[u], aa);
+      ldsm_x2_t(al[u], aa + C::SPLANE);
+      // B: k = (t / 2, j3 = 2 (t % 2)), n = r2 = 8 nt + g
+      const int xb = (t >> 1) == 0 ? r0 : (has2 ? r0 + 1 : C::RB);
+      const char* bp = G3p + xb * C::GROW + (8 * nt + g) * 8 + 4 * (t & 1);
+      bh[u] = *reinterpret_cast<const uint32_t*>(bp);
+      bl[u] = *reinterpret_cast<const uint32_t*>(bp + C::GPLANE);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -538,54 +558,62 @@ __device__ __forceinline__ void mma_bwd_dp2(const MmaBwd::Meta& m, const float* 
         dp2_flush(acc, dP2, mt, nt, lane);
         acc.p = p;
       }
-      if (u & 1) mma_3xtf32_2(acc.c[2], acc.c[3], a[u], b[u]);
-      else mma_3xtf32_2(acc.c[0], acc.c[1], a[u], b[u]);
+      float* big = acc.c[(u & 1) ? 2 : 0];
+      float* small = acc.c[(u & 1) ? 3 : 1];
+      mma_bf16_k8(small, al[u][0], al[u][1], bh[u]);
+      mma_bf16_k8(big, ah[u][0], ah[u][1], bh[u]);
+      mma_bf16_k8(small, ah[u][0], ah[u][1], bl[u]);
     }
   }
 }
 
 // (3) over the pairs of one batch: warp w takes m-tile w % 2 (r2 = 16 (w % 2) ..
-// +15) of a contiguous quarter of the pairs.
-__device__ __forceinline__ void mma_bwd_dg3(const MmaBwd::Meta& m, const float* __restrict__ P2,
-                                            const float* __restrict__ Ss, float* __restrict__ dG3,
-                                            int warp, int lane) {
+// +15) of a contiguous quarter of the pairs.  bf16 m16n8k16 tiles:
+// A[r2][j12] = P2[p][j12][r2] (transposed ldmatrix, cached per prefix),
+// B[j12][(row of pair, j3)] from the S planes (plain ldmatrix, rows (row, j3)).
+__device__ __forceinline__ void mma_bwd_dg3(const MmaBwd::Meta& m, uint32_t P2h, uint32_t Sh,
+                                            float* __restrict__ dG3, int warp, int lane) {
   using C = MmaBwd;
   const int g = lane >> 2, t = lane & 3;
   const int mt = warp & 1, quarter = warp >> 1;
   const int npairs = m.npairs;
   const int q0 = (npairs * quarter) >> 2, q1 = (npairs * (quarter + 1)) >> 2;
+  const int li = lane >> 3, lr = lane & 7;
   int cur_p = -1;
-  FragA af[4];
+  uint32_t ah[2][4], al[2][4];
   for (int q = q0; q < q1; ++q) {
     const int e = m.pair[q];
     const int r0 = e & 255, has2 = (e >> 8) & 1, p = e >> 9;
     if (p != cur_p) {
       cur_p = p;
-      // A[r2][j12] = P2[p][j1 = ks][j2][r2], column-major in (r2, j2)
+      // matrix li: k rows j12 = 16 ks + 8 (li >> 1) + lr (j1 = 2 ks + (li >> 1), j2 = lr),
+      // m columns r2 = 16 mt + 8 (li & 1)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) af[ks] = load_a_cm(P2 + p * C::QP + ks * C::QA + 16 * mt, C::QB, lane);
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t aa = P2h + p * C::PPB + (2 * ks + (li >> 1)) * C::PA + lr * C::PB +
+                            2 * (16 * mt + 8 * (li & 1));
+        ldsm_x4_t(ah[ks], aa);
+        ldsm_x4_t(al[ks], aa + C::P2PLANE);
+      }
     }
-    // B[j12][(row of pair, j3)] = S[row][j12][j3]
-    const float* sp = Ss + (r0 + (has2 ? (g >> 2) : 0)) * C::SS + (g & 3);
-    float big[2][4], small[2][4];
+    // B rows n = (row of pair, j3) = lr, k columns j12 = 16 ks + 8 ((lane >> 3) & 1)
+    const int xr = (lr >> 2) == 0 ? r0 : (has2 ? r0 + 1 : C::RB);
+    const uint32_t bb = Sh + xr * C::SROW + (lr & 3) * 80 + 16 * (li & 1);
+    float big[4] = {0.f, 0.f, 0.f, 0.f}, small[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) big[h][i] = small[h][i] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      FragB b;
-      b.v[0] = split_tf32(sp[(8 * ks + t) * 4]);
-      b.v[1] = split_tf32(sp[(8 * ks + t + 4) * 4]);
-      mma_3xtf32_2(big[ks & 1], small[ks & 1], af[ks], b);
+    for (int ks = 0; ks < 2; ++ks) {
+      uint32_t bh[2], bl[2];
+      ldsm_x2(bh, bb + 32 * ks);
+      ldsm_x2(bl, bb + 32 * ks + C::SPLANE);
+      mma_bf16(small, al[ks], bh[0], bh[1]);
+      mma_bf16(big, ah[ks], bh[0], bh[1]);
+      mma_bf16(small, ah[ks], bl[0], bl[1]);
     }
     // C[r2][(row of pair, j3)]: this lane holds j3 = 2 (t % 2), +1 of row t / 2
     if (t < 2 || has2) {
       float* o = dG3 + (size_t)m.ri3[r0 + (t >> 1)] * (4 * C::R) + (16 * mt + g) * 4 + 2 * (t & 1);
-      red_add_f2(o, (small[0][0] + small[1][0]) + (big[0][0] + big[1][0]),
-                 (small[0][1] + small[1][1]) + (big[0][1] + big[1][1]));
-      red_add_f2(o + 32, (small[0][2] + small[1][2]) + (big[0][2] + big[1][2]),
-                 (small[0][3] + small[1][3]) + (big[0][3] + big[1][3]));
+      red_add_f2(o, small[0] + big[0], small[1] + big[1]);
+      red_add_f2(o + 32, small[2] + big[2], small[3] + big[3]);
     }
   }
 }
@@ -594,12 +622,11 @@ __device__ __forceinline__ void mma_bwd_dg3(const MmaBwd::Meta& m, const float* 
 // warp w owns columns 32 w .. 32 w + 31.  bf16 tiles: A = G1 rows read transposed
 // ([k = (p, j1)][m = r1]), B = dP2 planes [k = (p, j1)][n] (transposed); the k range
 // is padded to 16 with rows that the caller has zeroed in both operands.
-__device__ __forceinline__ void mma_bwd_dg2(const float* __restrict__ P1n, const float* __restrict__ dP2,
-                                            float* __restrict__ dG2i2, int np, int warp, int lane) {
+__device__ __forceinline__ void mma_bwd_dg2(uint32_t g1h, uint32_t dph, float* __restrict__ dG2i2, int np,
+                                            int warp, int lane) {
   using C = MmaBwd;
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t g1h = smem_addr(P1n), g1l = g1h + C::G1PLANE;
-  const uint32_t dph = smem_addr(dP2), dpl = dph + C::DPPLANE;
+  const uint32_t g1l = g1h + C::G1PLANE, dpl = dph + C::DPPLANE;
   float acc[2][4][4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt)
@@ -640,15 +667,13 @@ __device__ __forceinline__ void mma_bwd_dg2(const float* __restrict__ P1n, const
 // (5): dG1[i1_p][j1][r1] += sum over (j2, r2) of dP2[p][j1][j2][r2] G2[r1][(j2, r2)];
 // warp w takes the tile (p, j1) = 16 (w % 2) .. +15 x r1 = 8 (w / 2) .. +7.  bf16 tiles:
 // A = dP2 planes [m = (p, j1)][k] (plain), B = G2 [n = r1][k = (j2, r2)] (plain).
-__device__ __forceinline__ void mma_bwd_dg1(const float* __restrict__ dP2, const float* __restrict__ G2s,
-                                            const int* __restrict__ pi1, float* __restrict__ dG1, int np,
-                                            int warp, int lane) {
+__device__ __forceinline__ void mma_bwd_dg1(uint32_t dph, uint32_t g2h, const int* __restrict__ pi1,
+                                            float* __restrict__ dG1, int np, int warp, int lane) {
   using C = MmaBwd;
   const int g = lane >> 2, t = lane & 3;
   const int mt = warp & 1, nt = warp >> 1;
   if (16 * mt >= 4 * np) return;
-  const uint32_t dph = smem_addr(dP2), dpl = dph + C::DPPLANE;
-  const uint32_t g2h = smem_addr(G2s), g2l = g2h + C::G2PLANE;
+  const uint32_t dpl = dph + C::DPPLANE, g2l = g2h + C::G2PLANE;
   float c[2][4];
 #pragma unroll
   for (int u = 0; u < 2; ++u)
@@ -677,10 +702,10 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
   using C = MmaBwd;
   using Meta = C::Meta;
   extern __shared__ float4 sm4[];
-  float* base = reinterpret_cast<float*>(sm4);
-  float* P2 = base + 2 * C::STAGE_F;
-  float* dP2 = P2 + C::F_Q;                         // bf16 planes
-  Meta* meta = reinterpret_cast<Meta*>(dP2 + C::F_DP);
+  char* base = reinterpret_cast<char*>(sm4);
+  char* P2 = base + C::OFF_P2;                      // bf16 planes
+  char* dP2 = base + C::OFF_DP;                     // bf16 planes
+  Meta* meta = reinterpret_cast<Meta*>(base + C::OFF_META);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
   uint64_t* empty = full + 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -690,6 +715,16 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
     mbar_init(&empty[0], 1);
     mbar_init(&empty[1], 1);
     mbar_init_fence();
+    if (blockIdx.x == 0) mark_split(a.w.ctl, a.G1, a.G2, a.G3);
+  }
+  // the zero row (row RB) of the S and G3 planes of both stages
+  for (int e = tid; e < 2 * 4 * (C::SROW / 16); e += C::THREADS) {
+    const int st = e / (4 * (C::SROW / 16)), rem = e - st * 4 * (C::SROW / 16);
+    const int which = rem / (C::SROW / 16), q = rem - which * (C::SROW / 16);
+    char* st0 = base + st * C::STAGE_B;
+    char* row = which < 2 ? st0 + C::OFF_S + which * C::SPLANE + C::RB * C::SROW
+                          : st0 + C::OFF_G3 + (which - 2) * C::GPLANE + C::RB * C::GROW;
+    *reinterpret_cast<uint4*>(row + 16 * q) = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
   const int n_chunks = a.w.ctl->n_chunks;
@@ -732,18 +767,14 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
       ChunkDesc dn{};
       const int cn = next_chunk(dn);
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
-      float* G2s = base + s * C::STAGE_F;
-      float* P1n = G2s + C::F_G2;
-      float* Ss = P1n + C::F_P1;
-      float* G3s = Ss + C::F_S;
+      char* st = base + s * C::STAGE_B;
       {
         const uint16_t* h2 = a.w.g2h + (size_t)i2 * C::R * C::NC;
         const uint16_t* l2 = a.w.g2l + (size_t)i2 * C::R * C::NC;
-        char* dst = reinterpret_cast<char*>(G2s);
 #pragma unroll 8
         for (int i = 0; i < 2 * C::R * C::NC / 256; ++i) {
           const int e = i * 32 + lane, plane = e >> 10, row = (e >> 5) & 31, q = e & 31;
-          cp_async16(dst + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * q,
+          cp_async16(st + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * q,
                      (plane ? l2 : h2) + row * C::NC + 8 * q);
         }
       }
@@ -752,21 +783,28 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
         const int i1 = __shfl_sync(0xffffffffu, gi1, pp);
         const int plane = lane >> 4, j1 = (lane >> 2) & 3, q = lane & 3;
         if (pp < np)
-          cp_async16(reinterpret_cast<char*>(P1n) + plane * C::G1PLANE + (4 * pp + j1) * (2 * C::G1LD) + 16 * q,
+          cp_async16(st + C::OFF_G1 + plane * C::G1PLANE + (4 * pp + j1) * (2 * C::G1LD) + 16 * q,
                      (plane ? a.w.g1l : a.w.g1h) + ((size_t)i1 * 4 + j1) * C::R + 8 * q);
       }
-      for (int r0 = 0; r0 < nb; r0 += 8) {
-        int i3v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) i3v[u] = __shfl_sync(0xffffffffu, g3, (r0 + u) & 31);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (r0 + u < nb) {
-            cp_async16(Ss + (r0 + u) * C::SS + 4 * lane, a.w.rowbuf + (size_t)(x0 + r0 + u) * C::D + 4 * lane);
-            cp_async16(G3s + (r0 + u) * C::GS + 4 * lane, a.G3 + (size_t)i3v[u] * 4 * C::R + 4 * lane);
-          }
+      // G3 rows: lane = plane | 16-byte piece
+      for (int r = 0; r < nb; ++r) {
+        const int i3 = __shfl_sync(0xffffffffu, g3, r);
+        const int plane = lane >> 4, q = lane & 15;
+        cp_async16(st + C::OFF_G3 + plane * C::GPLANE + r * C::GROW + 16 * q,
+                   (plane ? a.w.g3l : a.w.g3h) + (size_t)i3 * 4 * C::R + 8 * q);
       }
       cp_async_arrive_noinc(&full[s]);
+      // S rows, converted: lane = (j1, j2); eight rows' loads in flight
+      for (int r0 = 0; r0 < nb; r0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (r0 + u < nb)
+            v[u] = __ldg(reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)(x0 + r0 + u) * C::D) + lane);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (r0 + u < nb) bwd_store_s(st + C::OFF_S, r0 + u, v[u], lane);
+      }
       if (lane < C::CP) {
         m.rs[lane] = rs;
         m.pi1[lane] = gi1;
@@ -802,12 +840,12 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
     Meta& m = meta[s];
     if (m.end) break;
     const int x0 = m.x0, x1 = m.x1, np = m.np, rows = x1 - x0;
-    const float* G2s = base + s * C::STAGE_F;
-    const float* P1n = G2s + C::F_G2;
-    float* Ss = const_cast<float*>(P1n) + C::F_P1;
-    float* G3s = Ss + C::F_S;
-    if (np > 4) mma_bwd_p2<2>(G2s, P1n, P2, warp, lane);
-    else mma_bwd_p2<1>(G2s, P1n, P2, warp, lane);
+    char* st = base + s * C::STAGE_B;
+    const uint32_t g2h = smem_addr(st), g1h = smem_addr(st + C::OFF_G1);
+    const uint32_t Sh = smem_addr(st + C::OFF_S), P2h = smem_addr(P2), dph = smem_addr(dP2);
+    const char* G3p = st + C::OFF_G3;
+    if (np > 4) mma_bwd_p2<2>(g2h, g1h, P2, warp, lane);
+    else mma_bwd_p2<1>(g2h, g1h, P2, warp, lane);
     {
       // rows (p, j1) from 4 np up to the next multiple of 16 enter the k range of (4):
       // zero them in both bf16 operands (G1 rows: 5 pieces of 16 B per plane row;
@@ -818,11 +856,9 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
         const int pr = e / 38, q = e - pr * 38, plane = pr & 1, row = r0 + (pr >> 1);
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
         if (q < 5)
-          *reinterpret_cast<uint4*>(reinterpret_cast<char*>(const_cast<float*>(P1n)) + plane * C::G1PLANE +
-                                    row * (2 * C::G1LD) + 16 * q) = z;
+          *reinterpret_cast<uint4*>(st + C::OFF_G1 + plane * C::G1PLANE + row * (2 * C::G1LD) + 16 * q) = z;
         else
-          *reinterpret_cast<uint4*>(reinterpret_cast<char*>(dP2) + plane * C::DPPLANE + row * (2 * C::DPLD) +
-                                    16 * (q - 5)) = z;
+          *reinterpret_cast<uint4*>(dP2 + plane * C::DPPLANE + row * (2 * C::DPLD) + 16 * (q - 5)) = z;
       }
     }
     named_sync(1, 256);
@@ -840,11 +876,11 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
         for (int e = tid; e < nb * 32; e += 256) {
           const int r = e >> 5, q = e & 31;
           const int x = x0 + b0 + r;
+          bwd_store_s(st + C::OFF_S, r, __ldg(reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)x * C::D) + q), q);
           const int i3 = __ldg(a.w.row_i3 + x);
-          *reinterpret_cast<float4*>(Ss + r * C::SS + 4 * q) =
-              reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)x * C::D)[q];
-          *reinterpret_cast<float4*>(G3s + r * C::GS + 4 * q) =
-              __ldg(reinterpret_cast<const float4*>(a.G3 + (size_t)i3 * 4 * C::R) + q);
+          const int plane = q >> 4, pc = q & 15;
+          *reinterpret_cast<uint4*>(const_cast<char*>(G3p) + plane * C::GPLANE + r * C::GROW + 16 * pc) =
+              *reinterpret_cast<const uint4*>((plane ? a.w.g3l : a.w.g3h) + (size_t)i3 * 4 * C::R + 8 * pc);
           if (q == 0) m.ri3[r] = i3;
         }
         if (warp == 0) {
@@ -853,13 +889,13 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
         }
         named_sync(1, 256);
       }
-      mma_bwd_dg3(m, P2, Ss, a.dG3, warp, lane);
-      mma_bwd_dp2(m, Ss, G3s, dP2, acc, warp, lane);
+      mma_bwd_dg3(m, P2h, Sh, a.dG3, warp, lane);
+      mma_bwd_dp2(m, Sh, G3p, dP2, acc, warp, lane);
     }
     dp2_flush(acc, dP2, warp & 1, warp >> 1, lane);
     named_sync(1, 256);
-    mma_bwd_dg2(P1n, dP2, a.dG2 + (size_t)m.i2 * C::R * C::NC, np, warp, lane);
-    mma_bwd_dg1(dP2, G2s, m.pi1, a.dG1, np, warp, lane);
+    mma_bwd_dg2(g1h, dph, a.dG2 + (size_t)m.i2 * C::R * C::NC, np, warp, lane);
+    mma_bwd_dg1(dph, g2h, m.pi1, a.dG1, np, warp, lane);
     named_sync(1, 256);
     if (tid == 0) mbar_arrive(&empty[s]);
   }
@@ -910,7 +946,7 @@ static int persistent_grid_bwd(const void* fn, int threads, size_t smem) {
   return per_sm * sm_count();
 }
 
-int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out,
+int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out, int reuse,
                     const float* const cores[3], const int64_t* offsets, int64_t nnz,
                     int64_t num_bags, float* const core_grads[3], cudaStream_t st) {
   if (nnz == 0) return TT_EMB_OK;
@@ -939,7 +975,7 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   ba.dG2 = core_grads[1];
   ba.dG3 = core_grads[2];
   if (tc_shape(s)) {
-    const int rc = launch_split(s, w, cores, st);
+    const int rc = launch_split(s, w, cores, reuse, st);
     if (rc) return rc;
     static int grid = 0;
     if (grid == 0) {

@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
     mbar_init(&go[0], 1);
     mbar_init(&go[1], 1);
     mbar_init_fence();
+    if (blockIdx.x == 0) mark_split(a.w.ctl, a.G1, a.G2, a.G3);
   }
   __syncthreads();
   const int n_chunks = a.w.ctl->n_chunks;
@@ -698,7 +699,7 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
   fa.G3 = cores[2];
   switch (fwd_kind(s)) {
     case kFwdTiled_8_32:
-      rc = launch_split(s, w, cores, st);
+      rc = launch_split(s, w, cores, 0, st);
       if (rc) return rc;
       launch_fwd_mma<8>(fa, st);
       break;

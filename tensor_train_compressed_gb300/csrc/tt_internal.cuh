@@ -50,7 +50,10 @@ struct Ctl {
   uint32_t chunk_tile_ctr;
   uint32_t fwd_chunk_ctr;
   uint32_t bwd_chunk_ctr;
-  uint32_t pad[51];
+  uint32_t split_valid;   // the bf16 split planes hold the cores split_src (reset by every grouping)
+  uint32_t pad0[2];
+  unsigned long long split_src[3];   // G1, G2, G3 addresses the planes were split from
+  uint32_t pad[42];
 };
 static_assert(sizeof(Ctl) == 256, "control block is 256 bytes");
 
@@ -66,6 +69,7 @@ struct Layout {
   size_t row_start, row_i3, row_pair, pair_row_start, pair_i1, pair_i2;
   size_t seg_status, chunk_start, chunk_desc, chunk_status, coop, rowbuf, total;
   size_t g1h, g1l, g2h, g2l;   // bf16 split planes of G1 and G2 (tensor-core shape only)
+  size_t g3h, g3l, g3th, g3tl; // bf16 split planes of G3 [m3][R2][n3] and of its transpose [m3][n3][R2]
   int key_bits, passes, n_sort_tiles, n_scan_tiles;
   int64_t rowbuf_rows;
 };
@@ -96,6 +100,10 @@ struct WS {
   uint16_t* g1l;                    // [m2][R1][n2 R2] (x = hi + lo + O(2^-18 |x|)), written
   uint16_t* g2h;                    // per call by k_split_cores; null unless the shape
   uint16_t* g2l;                    // runs the tensor-core chunk kernels
+  uint16_t* g3h;                    // G3 [m3][R2][n3] planes and the planes of its
+  uint16_t* g3l;                    // per-i3 transpose [m3][n3][R2], likewise
+  uint16_t* g3th;
+  uint16_t* g3tl;
 };
 
 // Shapes served by the tensor-core chunk kernels (n1 = n3 = 4, n2 = 8, R1 = R2 = 32).
@@ -266,10 +274,18 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
                    cudaStream_t st);
 int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chunk);
 // backward (tt_bwd.cu)
-int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out,
+int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out, int reuse,
                     const float* const cores[3], const int64_t* offsets, int64_t nnz,
                     int64_t num_bags, float* const core_grads[3], cudaStream_t st);
-int launch_split(const Shape& s, const WS& w, const float* const cores[3], cudaStream_t st);
+int launch_split(const Shape& s, const WS& w, const float* const cores[3], int reuse, cudaStream_t st);
+// Called by one thread of a kernel that runs after k_split_cores in the same
+// stream: the split planes now hold the cores at g1, g2, g3.
+__device__ __forceinline__ void mark_split(Ctl* ctl, const float* g1, const float* g2, const float* g3) {
+  ctl->split_src[0] = (unsigned long long)g1;
+  ctl->split_src[1] = (unsigned long long)g2;
+  ctl->split_src[2] = (unsigned long long)g3;
+  ctl->split_valid = 1;
+}
 int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, float lr,
                int zero_grads, cudaStream_t st);
 

@@ -306,6 +306,33 @@ def test_backward_rebuilds_grouping_when_not_reused():
         assert _rel_err(grads[k].cpu().numpy(), dref[k]) <= BWD_TOL
 
 
+def test_reused_grouping_resplits_other_or_regrouped_cores():
+    """The backward reuses the forward's bf16 split of the cores only when the
+    core addresses match and no grouping ran since; both other cases must split
+    again (else the gradients would use another table's cores)."""
+    x = make_inputs(5, num_bags=600)
+    rng = np.random.default_rng(5)
+    other = [rng.normal(0.0, 1.0 / np.sqrt(32), c.shape).astype(np.float32) for c in x.cores]
+    _, rc, bits, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK, bits
+    # (a) a reusing backward on different cores
+    cores_b = [_dev(c) for c in other]
+    grads = [torch.zeros_like(c) for c in cores_b]
+    tte.tt_emb_backward(_dev(x.grad_out), cores_b, x.m, x.n, x.R, st["idx"], st["off"], grads,
+                        st["ws"], reuse_grouping=True)
+    dref = oracle.backward(x.grad_out, other, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(grads[k].cpu().numpy(), dref[k]) <= BWD_TOL, k
+    # (b) the forward's cores again, after a grouping-only call on the workspace
+    tte.tt_emb_group(x.m, x.n, x.R, st["idx"], st["off"], st["ws"])
+    grads = [torch.zeros_like(c) for c in st["cores"]]
+    tte.tt_emb_backward(_dev(x.grad_out), st["cores"], x.m, x.n, x.R, st["idx"], st["off"], grads,
+                        st["ws"], reuse_grouping=True)
+    dref = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(grads[k].cpu().numpy(), dref[k]) <= BWD_TOL, k
+
+
 def test_owner_object_host_inputs():
     x = make_inputs(5, num_bags=500)
     emb = tte.TTEmbeddingBag(x.cores, x.m, x.n, x.R)
