@@ -184,13 +184,14 @@ struct MmaFwd {
   // of 264 bf16 (528 B), G1 rows ((p, j1)) of 40 bf16 (80 B)
   static constexpr int G2LD = NC + 8, G1LD = R + 8;
   static constexpr int G2PLANE = R * G2LD * 2, G1PLANE = 4 * CP * G1LD * 2;   // bytes
-  static constexpr int G3S = 4 * R + 16;             // staged G3 row stride (floats)
-  static constexpr int P2B = R + 4;                  // P2[p][j1][j2][r2]: j2 stride
-  static constexpr int P2A = 8 * P2B + 8;            //   j1 stride
-  static constexpr int P2P = 4 * P2A;                //   p stride
-  static constexpr int F_G2 = G2PLANE / 2, F_P1 = G1PLANE / 2, F_G3 = (ROWMAX + 1) * G3S;   // floats
+  // staged G3 rows as bf16 planes of G3 transposed per row: [j3][r2], 80-byte
+  // j3 rows (row ROWMAX stays zero); P2 as bf16 planes [p][j1][j2][r2]: j2 rows
+  // of 80 B, j1 blocks of 656 B, prefixes 2624 B apart
+  static constexpr int GTROW = 4 * (R + 8) * 2, GTPLANE = (ROWMAX + 1) * GTROW;
+  static constexpr int PB = 80, PA = 8 * PB + 16, PPB = 4 * PA, P2PLANE = CP * PPB;
+  static constexpr int F_G2 = G2PLANE / 2, F_P1 = G1PLANE / 2, F_G3 = GTPLANE / 2;   // floats
   static constexpr int STAGE_F = F_G2 + F_P1 + F_G3;
-  static constexpr int F_P2 = CP * P2P;
+  static constexpr int F_P2 = P2PLANE / 2;
   struct Meta {
     int x0, x1, p0, np, npairs, end, pad[2];
     int pair[MAXPAIRS];   // first row | (second row valid) << 8 | chunk-local prefix << 9
@@ -243,28 +244,34 @@ __device__ __forceinline__ void mma_fwd_stage2(const float* __restrict__ G2s,
           mma_bf16x3(acc[mt][2 * np2 + h], ah[mt], al[mt], bh[2 * h], bh[2 * h + 1], bl[2 * h], bl[2 * h + 1]);
     }
   }
+  // row (p, j1) = 16 mt + g (+8), columns (j2, r2) = (warp, 8 nt + 2t (+1))
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int row = 16 * mt + g + 8 * h;          // (p, j1)
-      float* dst = P2 + (row >> 2) * C::P2P + (row & 3) * C::P2A + 2 * t;
+      const int row = 16 * mt + g + 8 * h;
+      char* dst = reinterpret_cast<char*>(P2) + (row >> 2) * C::PPB + (row & 3) * C::PA + warp * C::PB + 4 * t;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
-        const int n0 = col0 + 8 * nt;               // (j2, r2) = (n0 / 32, n0 % 32 + 2t)
-        *reinterpret_cast<float2*>(dst + (n0 >> 5) * C::P2B + (n0 & 31)) =
-            make_float2(acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
+        uint32_t hi, lo;
+        split_bf16x2(acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1], hi, lo);
+        *reinterpret_cast<uint32_t*>(dst + 16 * nt) = hi;
+        *reinterpret_cast<uint32_t*>(dst + 16 * nt + C::P2PLANE) = lo;
       }
     }
 }
 
 // Rows of the chunk, by pairs.  Consumer warp w takes m-tile w % 2 (j12 =
 // 16 (w % 2) .. +15) of a contiguous share of the pairs, so that consecutive
-// pairs of one prefix reuse the warp's split P2 fragments.
+// pairs of one prefix reuse the warp's P2 fragments.  bf16 m16n8k16 tiles:
+// A[j12][r2] = P2 planes (plain ldmatrix), B[r2][(row of pair, j3)] from the
+// staged G3 planes [j3][r2] per row (plain ldmatrix, rows (row, j3); a missing
+// second row reads the zero row), or, for rows past the first ROWMAX, 32-bit
+// pairs loaded from the global split planes.
 template <int CW>
-__device__ __forceinline__ void mma_fwd_stage3(const typename MmaFwd<CW>::Meta& m,
-                                               const float* __restrict__ P2,
-                                               const float* __restrict__ G3s, const float* __restrict__ G3,
+__device__ __forceinline__ void mma_fwd_stage3(const typename MmaFwd<CW>::Meta& m, uint32_t P2h,
+                                               uint32_t G3h, const uint16_t* __restrict__ g3th,
+                                               const uint16_t* __restrict__ g3tl,
                                                const int32_t* __restrict__ row_i3, float* __restrict__ rowbuf,
                                                int warp, int lane) {
   using C = MmaFwd<CW>;
@@ -273,60 +280,60 @@ __device__ __forceinline__ void mma_fwd_stage3(const typename MmaFwd<CW>::Meta& 
   const int mt = warp & 1, share = warp >> 1;
   const int npairs = m.npairs, x0 = m.x0;
   const int q0 = npairs * share / SH, q1 = npairs * (share + 1) / SH;
+  const int li = lane >> 3, lr = lane & 7;
   int cur_p = -1;
-  FragA af[4];
+  uint32_t ah[2][4], al[2][4];
   for (int q = q0; q < q1; ++q) {
     const int e = m.pair[q];
     const int r0 = e & 255, has2 = (e >> 8) & 1, p = e >> 9;
     if (p != cur_p) {
       cur_p = p;
-      // A[j12][r2] = P2[p][j1 = 2 mt (+1 for rows 8..15)][j2 = row % 8][r2]
-      const float* pa = P2 + p * C::P2P + 2 * mt * C::P2A;
+      // matrix li: rows j12 = 16 mt + 8 (li & 1) + lr (j1 = 2 mt + (li & 1), j2 = lr),
+      // columns r2 = 16 ks + 8 (li >> 1)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) af[ks] = load_a(pa + 8 * ks, C::P2B, C::P2A, lane);
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t aa = P2h + p * C::PPB + (2 * mt + (li & 1)) * C::PA + lr * C::PB +
+                            2 * (16 * ks + 8 * (li >> 1));
+        ldsm_x4(ah[ks], aa);
+        ldsm_x4(al[ks], aa + C::P2PLANE);
+      }
     }
-    // B[r2][(row of pair, j3)] = G3[i3_row][r2][j3]
-    const int rb = r0 + (has2 ? (g >> 2) : 0);
-    FragB bf[4];
+    float big[4] = {0.f, 0.f, 0.f, 0.f}, small[4] = {0.f, 0.f, 0.f, 0.f};
     if (r0 + 1 < C::ROWMAX) {
-      const float* gp = G3s + rb * C::G3S + (g & 3);
+      // B rows n = (row of pair, j3) = lr, k columns r2 = 16 ks + 8 ((lane >> 3) & 1)
+      const int xr = (lr >> 2) == 0 ? r0 : (has2 ? r0 + 1 : C::ROWMAX);
+      const uint32_t bb = G3h + xr * C::GTROW + (lr & 3) * 80 + 16 * (li & 1);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        bf[ks].v[0] = split_tf32(gp[(8 * ks + t) * 4]);
-        bf[ks].v[1] = split_tf32(gp[(8 * ks + t + 4) * 4]);
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t bh[2], bl[2];
+        ldsm_x2(bh, bb + 32 * ks);
+        ldsm_x2(bl, bb + 32 * ks + C::GTPLANE);
+        mma_bf16(small, al[ks], bh[0], bh[1]);
+        mma_bf16(big, ah[ks], bh[0], bh[1]);
+        mma_bf16(small, ah[ks], bl[0], bl[1]);
       }
     } else {
-      const float* gp = rb < C::ROWMAX ? G3s + rb * C::G3S
-                                       : G3 + (size_t)__ldg(row_i3 + x0 + rb) * (4 * C::R);
-      gp += g & 3;
+      // b0 = {B[k = 2t][n = g], B[2t+1][g]}, b1 = same at k + 8; n = (row g / 4, j3 = g % 4)
+      const int xr = r0 + (g >> 2);
+      const bool live = (g >> 2) == 0 || has2;
+      const size_t base = live ? ((size_t)__ldg(row_i3 + x0 + xr) * 4 + (g & 3)) * C::R : 0;
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        bf[ks].v[0] = split_tf32(gp[(8 * ks + t) * 4]);
-        bf[ks].v[1] = split_tf32(gp[(8 * ks + t + 4) * 4]);
+      for (int ks = 0; ks < 2; ++ks) {
+        const size_t k0 = base + 16 * ks + 2 * t;
+        const uint32_t bh0 = live ? __ldg(reinterpret_cast<const uint32_t*>(g3th + k0)) : 0u;
+        const uint32_t bh1 = live ? __ldg(reinterpret_cast<const uint32_t*>(g3th + k0 + 8)) : 0u;
+        const uint32_t bl0 = live ? __ldg(reinterpret_cast<const uint32_t*>(g3tl + k0)) : 0u;
+        const uint32_t bl1 = live ? __ldg(reinterpret_cast<const uint32_t*>(g3tl + k0 + 8)) : 0u;
+        mma_bf16(small, al[ks], bh0, bh1);
+        mma_bf16(big, ah[ks], bh0, bh1);
+        mma_bf16(small, ah[ks], bl0, bl1);
       }
-    }
-    // four accumulator chains: k parity x {hi.hi, the two small terms}
-    float big[2][4], small[2][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) big[h][i] = small[h][i] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const FragA& a = af[ks];
-      const FragB& b = bf[ks];
-      mma_tf32(small[ks & 1], a.v[0].lo, a.v[1].lo, a.v[2].lo, a.v[3].lo, b.v[0].hi, b.v[1].hi);
-      mma_tf32(big[ks & 1], a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].hi, b.v[1].hi);
-      mma_tf32(small[ks & 1], a.v[0].hi, a.v[1].hi, a.v[2].hi, a.v[3].hi, b.v[0].lo, b.v[1].lo);
     }
     // C[j12][(row of pair, j3)]: this lane holds j3 = 2 (t % 2), +1 of row t / 2
     if (t < 2 || has2) {
       float* o = rowbuf + (size_t)(x0 + r0 + (t >> 1)) * C::D + (16 * mt + g) * 4 + 2 * (t & 1);
-      float v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = (small[0][i] + small[1][i]) + (big[0][i] + big[1][i]);
-      *reinterpret_cast<float2*>(o) = make_float2(v[0], v[1]);
-      *reinterpret_cast<float2*>(o + 32) = make_float2(v[2], v[3]);
+      *reinterpret_cast<float2*>(o) = make_float2(small[0] + big[0], small[1] + big[1]);
+      *reinterpret_cast<float2*>(o + 32) = make_float2(small[2] + big[2], small[3] + big[3]);
     }
   }
 }
@@ -354,6 +361,14 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
     mbar_init(&go[1], 1);
     mbar_init_fence();
     if (blockIdx.x == 0) mark_split(a.w.ctl, a.G1, a.G2, a.G3);
+  }
+  // the zero row (row ROWMAX) of the staged G3 planes of both stages
+  for (int e = tid; e < 2 * 2 * (C::GTROW / 16); e += C::THREADS) {
+    const int st = e / (2 * (C::GTROW / 16)), rem = e - st * 2 * (C::GTROW / 16);
+    const int plane = rem / (C::GTROW / 16), q = rem - plane * (C::GTROW / 16);
+    char* row = reinterpret_cast<char*>(base + st * C::STAGE_F + C::F_G2 + C::F_P1) + plane * C::GTPLANE +
+                C::ROWMAX * C::GTROW;
+    *reinterpret_cast<uint4*>(row + 16 * q) = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
   const int n_chunks = a.w.ctl->n_chunks;
@@ -456,16 +471,18 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
           cp_async16(reinterpret_cast<char*>(P1n) + plane * C::G1PLANE + (4 * pp + j1) * (2 * C::G1LD) + 16 * q,
                      (plane ? a.w.g1l : a.w.g1h) + ((size_t)i1 * 4 + j1) * C::R + 8 * q);
       }
-      // G3[i3_x]: 32 pieces per row, 8 rows per batch of independent shuffles
+      // G3 rows: transposed split planes, per row lane = plane | j3 | 16-byte piece
       for (int r0 = 0; r0 < cur.nst; r0 += 8) {
         const int src = r0 < 32 ? cur.g30 : cur.g31;
         int i3v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) i3v[u] = __shfl_sync(0xffffffffu, src, (r0 & 31) + u);
+        const int plane = lane >> 4, j3 = (lane >> 2) & 3, q = lane & 3;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           if (r0 + u < cur.nst)
-            cp_async16(G3s + (r0 + u) * C::G3S + 4 * lane, a.G3 + (size_t)i3v[u] * 4 * C::R + 4 * lane);
+            cp_async16(reinterpret_cast<char*>(G3s) + plane * C::GTPLANE + (r0 + u) * C::GTROW + j3 * 80 + 16 * q,
+                       (plane ? a.w.g3tl : a.w.g3th) + ((size_t)i3v[u] * 4 + j3) * C::R + 8 * q);
       }
       cp_async_arrive_noinc(&full[s]);
       // pairs: a row starts a pair when its offset within its prefix is even;
@@ -526,7 +543,7 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
     if (m.np > 4) mma_fwd_stage2<CW, 2>(G2s, P1n, P2, warp, lane);
     else mma_fwd_stage2<CW, 1>(G2s, P1n, P2, warp, lane);
     named_sync(1, 32 * CW);
-    mma_fwd_stage3<CW>(m, P2, G3s, a.G3, a.w.row_i3, a.w.rowbuf, warp, lane);
+    mma_fwd_stage3<CW>(m, smem_addr(P2), smem_addr(G3s), a.w.g3th, a.w.g3tl, a.w.row_i3, a.w.rowbuf, warp, lane);
     named_sync(1, 32 * CW);
     if (tid == 0) mbar_arrive(&empty[s]);
   }
