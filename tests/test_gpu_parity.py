@@ -306,6 +306,28 @@ def test_backward_rebuilds_grouping_when_not_reused():
         assert _rel_err(grads[k].cpu().numpy(), dref[k]) <= BWD_TOL
 
 
+def test_wide_dynamic_range_cores():
+    """The contractions run as three-term bf16 split products; cores whose
+    slices span six orders of magnitude (log-uniform scale per i_k slice, and a
+    tenth of the entries with their sign flipped against their neighbours) must
+    still meet the forward and gradient tolerances against the fp64 oracle."""
+    x = make_custom((23, 17, 29), (4, 8, 4), (1, 32, 32, 1), num_bags=900, max_len=24,
+                    seed=314, dist=("zipf", 1.1, "identity"))
+    rng = np.random.default_rng(2718)
+    for k, c in enumerate(x.cores):
+        scale = 10.0 ** rng.uniform(-3.0, 3.0, size=(c.shape[0],) + (1,) * (c.ndim - 1))
+        flip = np.where(rng.random(c.shape) < 0.1, -1.0, 1.0)
+        x.cores[k] = (c * scale * flip).astype(np.float32)
+    out, rc, bits, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK, bits
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    assert _rel_err(out, ref) <= FWD_TOL
+    dG = _gpu_backward(x, st)
+    dref = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(dG[k], dref[k]) <= BWD_TOL, k
+
+
 def test_reused_grouping_resplits_other_or_regrouped_cores():
     """The backward reuses the forward's bf16 split of the cores only when the
     core addresses match and no grouping ran since; both other cases must split
