@@ -21,27 +21,31 @@
 namespace tt {
 
 // Zero the S rows that more than one gather slice will add into, write the bag
-// of every lookup (CSR offsets, one warp per bag, clamped so that bad offsets
-// stay in bounds) and reset the backward chunk counter.
+// of every lookup (CSR offsets, clamped so that bad offsets stay in bounds) and
+// reset the backward chunk counter.  One thread per unique row (coalesced row
+// starts; a crossing row, one per slice boundary at most, is zeroed by its
+// thread) and one thread per bag (its lookups written in a loop).
 __global__ void __launch_bounds__(256) k_s_zero(WS w, int D, const int64_t* __restrict__ offsets,
                                                 int64_t B, int64_t nnz, int span) {
   if (blockIdx.x == 0 && threadIdx.x == 0) w.ctl->bwd_chunk_ctr = 0;
-  const int U = w.ctl->U_r;
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  for (int64_t u = gw; u < U; u += warps) {
+  const int64_t U = w.ctl->U_r;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < U; u += stride) {
     const int32_t s0 = w.row_start[u], s1 = w.row_start[u + 1];
     if (s0 / span != (s1 - 1) / span) {
       float* r = w.rowbuf + u * (int64_t)D;
-      for (int j = lane; j < D; j += 32) r[j] = 0.f;
+      if ((D & 3) == 0) {
+        for (int j = 0; j < D; j += 4) *reinterpret_cast<float4*>(r + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        for (int j = 0; j < D; ++j) r[j] = 0.f;
+      }
     }
   }
-  for (int64_t b = gw; b < B; b += warps) {
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < B; b += stride) {
     int64_t l0 = offsets[b], l1 = offsets[b + 1];
     l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
     l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
-    for (int64_t l = l0 + lane; l < l1; l += 32) w.bag_of[l] = (int32_t)b;
+    for (int64_t l = l0; l < l1; ++l) w.bag_of[l] = (int32_t)b;
   }
 }
 
@@ -913,26 +917,53 @@ struct SgdArgs {
 };
 
 __global__ void __launch_bounds__(256) k_sgd(SgdArgs a) {
+  // four float4 per thread and step, all loads issued before the stores (the
+  // cores and their gradients never alias); segment pointers chosen by selects
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.start[3]; i += stride) {
-    const int k = i < a.start[1] ? 0 : (i < a.start[2] ? 1 : 2);
-    const int64_t e = (i - a.start[k]) * 4;
-    float* G = a.G[k];
-    float* dG = a.dG[k];
-    const int64_t n = a.count[k];
-    if (e + 4 <= n) {
-      float4 g = *reinterpret_cast<float4*>(G + e);
-      const float4 d = *reinterpret_cast<const float4*>(dG + e);
-      g.x = fmaf(-a.lr, d.x, g.x);
-      g.y = fmaf(-a.lr, d.y, g.y);
-      g.z = fmaf(-a.lr, d.z, g.z);
-      g.w = fmaf(-a.lr, d.w, g.w);
-      *reinterpret_cast<float4*>(G + e) = g;
-      if (a.zero) *reinterpret_cast<float4*>(dG + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      for (int64_t t = e; t < n; ++t) {
-        G[t] = fmaf(-a.lr, dG[t], G[t]);
-        if (a.zero) dG[t] = 0.f;
+  auto seg_g = [&](int k) { return k == 0 ? a.G[0] : (k == 1 ? a.G[1] : a.G[2]); };
+  auto seg_d = [&](int k) { return k == 0 ? a.dG[0] : (k == 1 ? a.dG[1] : a.dG[2]); };
+  auto seg_n = [&](int k) { return k == 0 ? a.count[0] : (k == 1 ? a.count[1] : a.count[2]); };
+  auto seg_s = [&](int k) { return k == 0 ? a.start[0] : (k == 1 ? a.start[1] : a.start[2]); };
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < a.start[3]; i0 += 4 * stride) {
+    float4 g[4], d[4];
+    int ks[4];
+    int64_t es[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      ks[u] = -1;
+      es[u] = 0;
+      if (i < a.start[3]) {
+        const int k = i < a.start[1] ? 0 : (i < a.start[2] ? 1 : 2);
+        const int64_t e = (i - seg_s(k)) * 4;
+        ks[u] = k;
+        es[u] = e;
+        if (e + 4 <= seg_n(k)) {
+          g[u] = *reinterpret_cast<const float4*>(seg_g(k) + e);
+          d[u] = *reinterpret_cast<const float4*>(seg_d(k) + e);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = ks[u];
+      if (k < 0) continue;
+      float* G = seg_g(k);
+      float* dG = seg_d(k);
+      const int64_t e = es[u], n = seg_n(k);
+      if (e + 4 <= n) {
+        float4 v = g[u];
+        v.x = fmaf(-a.lr, d[u].x, v.x);
+        v.y = fmaf(-a.lr, d[u].y, v.y);
+        v.z = fmaf(-a.lr, d[u].z, v.z);
+        v.w = fmaf(-a.lr, d[u].w, v.w);
+        *reinterpret_cast<float4*>(G + e) = v;
+        if (a.zero) *reinterpret_cast<float4*>(dG + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        for (int64_t t = e; t < n; ++t) {
+          G[t] = fmaf(-a.lr, dG[t], G[t]);
+          if (a.zero) dG[t] = 0.f;
+        }
       }
     }
   }
@@ -951,8 +982,8 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
                     int64_t num_bags, float* const core_grads[3], cudaStream_t st) {
   if (nnz == 0) return TT_EMB_OK;
   const int sms = sm_count();
-  int grid = (int)ceil_div(L.rowbuf_rows > num_bags ? L.rowbuf_rows : num_bags, 8);
-  if (grid > sms * 16) grid = sms * 16;
+  int grid = (int)ceil_div(L.rowbuf_rows > num_bags ? L.rowbuf_rows : num_bags, 256);
+  if (grid > sms * 8) grid = sms * 8;
   if (grid < 1) grid = 1;
   const bool cta_gather = s.D == 128;
   TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D, offsets, num_bags, nnz,
@@ -1012,8 +1043,8 @@ int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, flo
   }
   a.lr = lr;
   a.zero = zero_grads ? 1 : 0;
-  int grid = (int)ceil_div(a.start[3], 256);
-  if (grid > sm_count() * 8) grid = sm_count() * 8;
+  int grid = (int)ceil_div(a.start[3], 4 * 256);
+  if (grid > sm_count() * 4) grid = sm_count() * 4;
   if (grid < 1) grid = 1;
   TT_TIMED("k_sgd", st, (k_sgd<<<grid, 256, 0, st>>>(a)));
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
