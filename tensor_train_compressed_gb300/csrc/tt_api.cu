@@ -37,6 +37,9 @@ int shape_from_args(const int64_t m[3], const int32_t n[3], const int32_t R[4], 
   if (D > (1 << 20)) return TT_EMB_ERR_UNSUPPORTED;
   s->m1 = m[0];
   s->m2 = m[1];
+  s->fm1 = make_fastdiv((uint32_t)m[0]);
+  s->fm2 = make_fastdiv((uint32_t)m[1]);
+  s->fm3 = make_fastdiv((uint32_t)m[2]);
   s->m3 = m[2];
   s->M = (int64_t)M;
   s->n1 = n[0];

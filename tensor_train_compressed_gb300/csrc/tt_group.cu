@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kScanThreads) k_segment(SegArgs a) {
       const uint64_t pk = prev >> 32;
       const bool first = (k == 0);
       if (first || key != pk) rflag |= 1u << i;
-      if (first || (uint32_t)key / m3 != (uint32_t)pk / m3) pflag |= 1u << i;
+      if (first || fdiv((uint32_t)key, a.s.fm3) != fdiv((uint32_t)pk, a.s.fm3)) pflag |= 1u << i;
     }
     prev = wv;
   }
@@ -281,9 +281,9 @@ __global__ void __launch_bounds__(kScanThreads) k_segment(SegArgs a) {
       }
       continue;
     }
-    const uint32_t q = (uint32_t)key / m3;
+    const uint32_t q = fdiv((uint32_t)key, a.s.fm3);
     if (pflag & (1u << i)) {
-      const uint32_t q2 = q / (uint32_t)a.s.m1;
+      const uint32_t q2 = fdiv(q, a.s.fm1);
       a.w.pair_row_start[pp] = rr;
       a.w.pair_i1[pp] = (int32_t)(q - q2 * (uint32_t)a.s.m1);
       a.w.pair_i2[pp] = (int32_t)q2;

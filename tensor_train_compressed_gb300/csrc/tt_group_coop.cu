@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       const uint64_t key = wv >> 32, pk = pv >> 32;
       const bool valid = live && key < M;
       const bool rf = valid && (i == 0 || key != pk);
-      const bool pf = valid && (i == 0 || (uint32_t)key / m3 != (uint32_t)pk / m3);
+      const bool pf = valid && (i == 0 || fdiv((uint32_t)key, a.s.fm3) != fdiv((uint32_t)pk, a.s.fm3));
       rbits[it] = __ballot_sync(0xffffffffu, rf);
       pbits[it] = __ballot_sync(0xffffffffu, pf);
       wr += __popc(rbits[it]);
@@ -360,9 +360,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
           if (key >= M) {
             a.w.uid[l] = -1;
           } else {
-            const uint32_t q = (uint32_t)key / m3;
+            const uint32_t q = fdiv((uint32_t)key, a.s.fm3);
             if (pf) {
-              const uint32_t q2 = q / (uint32_t)a.s.m1;
+              const uint32_t q2 = fdiv(q, a.s.fm1);
               a.w.pair_row_start[pi - 1] = ri - 1;
               a.w.pair_i1[pi - 1] = (int32_t)(q - q2 * (uint32_t)a.s.m1);
               a.w.pair_i2[pi - 1] = (int32_t)q2;

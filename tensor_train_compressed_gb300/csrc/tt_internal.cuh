@@ -58,9 +58,33 @@ struct Ctl {
 static_assert(sizeof(Ctl) == 256, "control block is 256 bytes");
 
 // Shape of one TT table as the kernels see it.
+// Unsigned 32-bit division by a divisor fixed per shape (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994,
+// section 4, for all 32-bit dividends): with l = ceil(log2 d) and
+// mul = floor(2^32 (2^l - d) / d) + 1, n / d = (t + ((n - t) >> s1)) >> s2 where
+// t = umulhi(mul, n), s1 = min(l, 1), s2 = max(l - 1, 0).
+struct FastDiv {
+  uint32_t mul, s1, s2, pad;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while (l < 32 && ((uint64_t)1 << l) < (uint64_t)d) ++l;
+  FastDiv f;
+  f.mul = (uint32_t)(((((uint64_t)1) << 32) * ((((uint64_t)1) << l) - d)) / d + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l > 0 ? l - 1 : 0;
+  f.pad = 0;
+  return f;
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(f.mul, n);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 struct Shape {
   int64_t m1, m2, m3, M;
   int n1, n2, n3, R1, R2, D;
+  FastDiv fm1, fm2, fm3;     // division by m1, m2, m3
 };
 
 // Workspace layout (byte offsets from the workspace base; 256-aligned).
@@ -150,8 +174,8 @@ __device__ __forceinline__ void f4add(float4& a, const float4& b) {
 // (i1, i2) prefixes come out grouped by the G2 slice they read.
 __device__ __forceinline__ uint32_t group_key(int64_t r, const Shape& s) {
   const uint32_t ru = (uint32_t)r, m1 = (uint32_t)s.m1, m2 = (uint32_t)s.m2, m3 = (uint32_t)s.m3;
-  const uint32_t q = ru / m3, i3 = ru - q * m3;
-  const uint32_t i1 = q / m2, i2 = q - i1 * m2;
+  const uint32_t q = fdiv(ru, s.fm3), i3 = ru - q * m3;
+  const uint32_t i1 = fdiv(q, s.fm2), i2 = q - i1 * m2;
   return (i2 * m1 + i1) * m3 + i3;
 }
 
