@@ -11,9 +11,11 @@ through ctypes.
 
 Pins (tests/test_oracle_pins.py): a hand-worked example (tests/golden/),
 exact reconstruction of a dense table through a TT-SVD, Kronecker rows for
-rank-1 cores, a materialised table + torch embedding_bag, multilinearity,
-the adjoint identity and torch autograd for the backward, and numpy
-lexsort/unique for the grouping.  No function here is "parity unpinned".
+rank-1 cores, a materialised table + torch embedding_bag (sum, mean and
+per-sample weights), multilinearity, integer weights against repeated
+lookups, the adjoint identity, central differences and torch autograd for the
+backward (core and weight gradients), and numpy lexsort/unique for the
+grouping.  No function here is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -63,6 +65,12 @@ def _load():
             lib.tto_backward.argtypes = [P, P, P, P, P, P, P, P, I64, P, I64, P, P, P,
                                          ctypes.c_int, I64, ctypes.c_int]
             lib.tto_backward.restype = ctypes.c_int
+            lib.tto_forward_ex.argtypes = [P, P, P, P, P, P, P, I64, P, I64, P, ctypes.c_int, P,
+                                           ctypes.c_int]
+            lib.tto_forward_ex.restype = ctypes.c_int
+            lib.tto_backward_ex.argtypes = [P, P, P, P, P, P, P, P, I64, P, I64, P, ctypes.c_int,
+                                            P, P, P, P, ctypes.c_int, I64, ctypes.c_int]
+            lib.tto_backward_ex.restype = ctypes.c_int
             lib.tto_sgd.argtypes = [P, P, I64, ctypes.c_double, P]
             lib.tto_sgd.restype = None
             lib.tto_group.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P]
@@ -86,40 +94,62 @@ def _cores(cores):
     return [np.ascontiguousarray(c, dtype=np.float32) for c in cores]
 
 
-def forward(cores, m, n, R, indices, offsets, threads: int = 1, strict: bool = True):
-    """fp64 pooled output [B][D] (naive chained contraction per lookup, then sum)."""
+_MODES = {"sum": 0, "mean": 1}
+
+
+def _weights(weights, nnz):
+    if weights is None:
+        return None
+    w = np.ascontiguousarray(weights, dtype=np.float32)
+    if w.shape != (nnz,):
+        raise ValueError(f"weights must have shape ({nnz},)")
+    return w
+
+
+def forward(cores, m, n, R, indices, offsets, threads: int = 1, strict: bool = True,
+            weights=None, mode: str = "sum"):
+    """fp64 pooled output [B][D] (naive chained contraction per lookup, then the bag's sum;
+    ``weights`` scale each lookup's row, ``mode="mean"`` divides by the bag length)."""
     lib = _load()
     G = _cores(cores)
     m_a, n_a, R_a = _shape_args(m, n, R)
     idx = np.ascontiguousarray(indices, dtype=np.int64)
     off = np.ascontiguousarray(offsets, dtype=np.int64)
+    w = _weights(weights, idx.shape[0])
     B = off.shape[0] - 1
     D = int(n_a.prod())
     out = np.zeros((max(B, 0), D), dtype=np.float64)
-    rc = lib.tto_forward(_p(G[0]), _p(G[1]), _p(G[2]), _p(m_a), _p(n_a), _p(R_a), _p(idx),
-                         idx.shape[0], _p(off), B, _p(out), int(threads))
+    rc = lib.tto_forward_ex(_p(G[0]), _p(G[1]), _p(G[2]), _p(m_a), _p(n_a), _p(R_a), _p(idx),
+                            idx.shape[0], _p(off), B, None if w is None else _p(w),
+                            _MODES[mode], _p(out), int(threads))
     if rc != TTO_OK and (strict or rc != TTO_ERR_INDEX):
-        raise OracleError(rc, "tto_forward")
+        raise OracleError(rc, "tto_forward_ex")
     return out
 
 
 def backward(grad_out, cores, m, n, R, indices, offsets, threads: int = 1,
-             filter_core: int = 0, filter_value: int = 0, strict: bool = True):
-    """fp64 core gradients [dG1, dG2, dG3] of <grad_out, out> (fresh zeros, then +=)."""
+             filter_core: int = 0, filter_value: int = 0, strict: bool = True,
+             weights=None, mode: str = "sum", want_dw: bool = False):
+    """fp64 core gradients [dG1, dG2, dG3] of <grad_out, out> (fresh zeros, then +=); with
+    ``want_dw`` also the gradient of the per-sample weights, fp64 [nnz]."""
     lib = _load()
     G = _cores(cores)
     m_a, n_a, R_a = _shape_args(m, n, R)
     idx = np.ascontiguousarray(indices, dtype=np.int64)
     off = np.ascontiguousarray(offsets, dtype=np.int64)
     g = np.ascontiguousarray(grad_out, dtype=np.float32)
+    w = _weights(weights, idx.shape[0])
     B = off.shape[0] - 1
     dG = [np.zeros(c.shape, dtype=np.float64) for c in G]
-    rc = lib.tto_backward(_p(g), _p(G[0]), _p(G[1]), _p(G[2]), _p(m_a), _p(n_a), _p(R_a),
-                          _p(idx), idx.shape[0], _p(off), B, _p(dG[0]), _p(dG[1]), _p(dG[2]),
-                          int(filter_core), int(filter_value), int(threads))
+    dW = np.zeros(idx.shape[0], dtype=np.float64) if want_dw else None
+    rc = lib.tto_backward_ex(_p(g), _p(G[0]), _p(G[1]), _p(G[2]), _p(m_a), _p(n_a), _p(R_a),
+                             _p(idx), idx.shape[0], _p(off), B, None if w is None else _p(w),
+                             _MODES[mode], _p(dG[0]), _p(dG[1]), _p(dG[2]),
+                             None if dW is None else _p(dW), int(filter_core), int(filter_value),
+                             int(threads))
     if rc != TTO_OK and (strict or rc != TTO_ERR_INDEX):
-        raise OracleError(rc, "tto_backward")
-    return dG
+        raise OracleError(rc, "tto_backward_ex")
+    return (dG, dW) if want_dw else dG
 
 
 def sgd(core, dcore, lr: float):

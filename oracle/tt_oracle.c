@@ -22,6 +22,11 @@
  *  - Bags are CSR offsets (B+1 entries); out[b] = sum of the rows of the
  *    lookups offsets[b] .. offsets[b+1]-1 (the "EmbeddingBag" of TT-Rec,
  *    abstract).  Empty bags give zero rows.
+ *  - The two other pooling rules of an embedding bag: a weighted sum, each
+ *    row scaled by its lookup's per-sample weight w[l], and the mean, the sum
+ *    divided by the bag's number of lookups (an empty bag stays zero).  The
+ *    weights go with the sum only.  For the weighted sum the gradient of
+ *    <grad_out, out> with respect to w[l] is <grad_out[bag(l)], row(r_l)>.
  *  - Backward: the exact gradient of <grad_out, out> with respect to each
  *    core, accumulated lookup by lookup (training latency, FlowTT abstract).
  *  - SGD: G <- G - lr*dG.
@@ -152,6 +157,8 @@ static int tto_parallel(void (*fn)(tto_job *, int64_t, int64_t), const void *ctx
 typedef struct {
   tto_tt t;
   const int64_t *indices, *offsets;
+  const float *weights;     /* per-sample weights [nnz], or NULL */
+  int mean;                 /* 1: divide each bag's sum by its length */
   double *out;
 } tto_fwd_ctx;
 
@@ -173,27 +180,42 @@ static void tto_fwd_bags(tto_job *job, int64_t b0, int64_t b1) {
       tto_split(t, r, &i1, &i2, &i3);
       tto_prefix(t, i1, i2, T12);
       tto_row(t, T12, i3, row);
-      for (int j = 0; j < D; ++j) o[j] += row[j];
+      double w = c->weights ? (double)c->weights[l] : 1.0;
+      for (int j = 0; j < D; ++j) o[j] += w * row[j];
     }
+    int64_t len = c->offsets[b + 1] - c->offsets[b];
+    if (c->mean && len > 0)
+      for (int j = 0; j < D; ++j) o[j] /= (double)len;
   }
   free(T12);
   free(row);
 }
 
 /* out: double [B][D], overwritten.  Out-of-range indices contribute nothing
- * and make the call return TTO_ERR_INDEX. */
-int tto_forward(const float *G1, const float *G2, const float *G3, const int64_t *m,
-                const int32_t *n, const int32_t *R, const int64_t *indices, int64_t nnz,
-                const int64_t *offsets, int64_t B, double *out, int threads) {
+ * and make the call return TTO_ERR_INDEX.  weights: float [nnz] or NULL;
+ * mean != 0 divides every non-empty bag by its length (not with weights). */
+int tto_forward_ex(const float *G1, const float *G2, const float *G3, const int64_t *m,
+                   const int32_t *n, const int32_t *R, const int64_t *indices, int64_t nnz,
+                   const int64_t *offsets, int64_t B, const float *weights, int mean,
+                   double *out, int threads) {
   tto_fwd_ctx c;
   int e = tto_init(&c.t, G1, G2, G3, m, n, R);
   if (e) return e;
   if (nnz < 0 || (nnz > 0 && !indices) || (B > 0 && !out)) return TTO_ERR_ARG;
+  if (mean && weights) return TTO_ERR_ARG;
   e = tto_check_offsets(offsets, B, nnz);
   if (e) return e;
   c.indices = indices; c.offsets = offsets; c.out = out;
+  c.weights = weights; c.mean = mean != 0;
   tto_job jobs[256];
   return tto_parallel(tto_fwd_bags, &c, B, threads, jobs);
+}
+
+/* Plain sum pooling. */
+int tto_forward(const float *G1, const float *G2, const float *G3, const int64_t *m,
+                const int32_t *n, const int32_t *R, const int64_t *indices, int64_t nnz,
+                const int64_t *offsets, int64_t B, double *out, int threads) {
+  return tto_forward_ex(G1, G2, G3, m, n, R, indices, nnz, offsets, B, NULL, 0, out, threads);
 }
 
 /* ---------------- backward ---------------- */
@@ -202,6 +224,9 @@ typedef struct {
   tto_tt t;
   const int64_t *indices, *offsets;
   const float *grad_out;
+  const float *weights;     /* per-sample weights [nnz], or NULL */
+  int mean;                 /* 1: bags were divided by their length */
+  double *dW;               /* [nnz] gradient of the weights, or NULL */
   int filter_core;          /* 0: all lookups; k in 1..3: only lookups with i_k == filter_value */
   int64_t filter_value;
   size_t n1g, n2g, n3g;     /* element counts of the three core gradients */
@@ -216,31 +241,49 @@ static void tto_bwd_bags(tto_job *job, int64_t b0, int64_t b1) {
   double *dG1 = job->scratch, *dG2 = dG1 + c->n1g, *dG3 = dG2 + c->n2g;
   double *T12 = (double *)malloc(sizeof(double) * n1 * n2 * R2);
   double *dT12 = (double *)malloc(sizeof(double) * n1 * n2 * R2);
-  if (!T12 || !dT12) { job->err = TTO_ERR_NOMEM; free(T12); free(dT12); return; }
+  double *g = (double *)malloc(sizeof(double) * D);
+  double *row = (double *)malloc(sizeof(double) * D);
+  if (!T12 || !dT12 || !g || !row) {
+    job->err = TTO_ERR_NOMEM; free(T12); free(dT12); free(g); free(row); return;
+  }
   for (int64_t b = b0; b < b1; ++b) {
-    const float *g = c->grad_out + b * D;
+    const float *gb = c->grad_out + b * D;
+    int64_t len = c->offsets[b + 1] - c->offsets[b];
     for (int64_t l = c->offsets[b]; l < c->offsets[b + 1]; ++l) {
       int64_t r = c->indices[l];
+      if (c->dW) c->dW[l] = 0.0;
       if (r < 0 || r >= M) { job->err = TTO_ERR_INDEX; continue; }
       int64_t i1, i2, i3;
       tto_split(t, r, &i1, &i2, &i3);
+      if (c->dW) {
+        /* d<grad_out, out>/dw_l = <grad_out[b], row(r)> */
+        tto_prefix(t, i1, i2, T12);
+        tto_row(t, T12, i3, row);
+        double s = 0.0;
+        for (int j = 0; j < D; ++j) s += (double)gb[j] * row[j];
+        c->dW[l] = s;
+      }
       if (c->filter_core == 1 && i1 != c->filter_value) continue;
       if (c->filter_core == 2 && i2 != c->filter_value) continue;
       if (c->filter_core == 3 && i3 != c->filter_value) continue;
+      /* the lookup's row enters out[b] with the factor w_l (weighted sum),
+       * 1/len (mean) or 1 (sum): its share of grad_out[b] is that factor times it */
+      double f = c->weights ? (double)c->weights[l] : (c->mean ? 1.0 / (double)len : 1.0);
+      for (int j = 0; j < D; ++j) g[j] = f * (double)gb[j];
       tto_prefix(t, i1, i2, T12);
       /* dG3[i3][b][j3] += sum_{j12} T12[j12][b] * g[j12][j3] */
       for (int bb = 0; bb < R2; ++bb)
         for (int j3 = 0; j3 < n3; ++j3) {
           double s = 0.0;
           for (int j12 = 0; j12 < n1 * n2; ++j12)
-            s += T12[j12 * R2 + bb] * (double)g[j12 * n3 + j3];
+            s += T12[j12 * R2 + bb] * g[j12 * n3 + j3];
           dG3[(i3 * R2 + bb) * n3 + j3] += s;
         }
       /* dT12[j12][b] = sum_{j3} g[j12][j3] * G3[i3][b][j3] */
       for (int j12 = 0; j12 < n1 * n2; ++j12)
         for (int bb = 0; bb < R2; ++bb) {
           double s = 0.0;
-          for (int j3 = 0; j3 < n3; ++j3) s += (double)g[j12 * n3 + j3] * g3(t, i3, bb, j3);
+          for (int j3 = 0; j3 < n3; ++j3) s += g[j12 * n3 + j3] * g3(t, i3, bb, j3);
           dT12[j12 * R2 + bb] = s;
         }
       /* dG2[i2][a][j2][b] += sum_{j1} G1[i1][j1][a] * dT12[j1][j2][b] */
@@ -264,24 +307,31 @@ static void tto_bwd_bags(tto_job *job, int64_t b0, int64_t b1) {
   }
   free(T12);
   free(dT12);
+  free(g);
+  free(row);
 }
 
 /* dG1, dG2, dG3: double, same layouts as the cores, ACCUMULATED (+=).
  * filter_core in 1..3 restricts the sum to lookups whose i_k equals
  * filter_value, which gives slice filter_value of dG_k exactly at a fraction
- * of the cost (the other slices then hold partial sums). */
-int tto_backward(const float *grad_out, const float *G1, const float *G2, const float *G3,
-                 const int64_t *m, const int32_t *n, const int32_t *R, const int64_t *indices,
-                 int64_t nnz, const int64_t *offsets, int64_t B, double *dG1, double *dG2,
-                 double *dG3, int filter_core, int64_t filter_value, int threads) {
+ * of the cost (the other slices then hold partial sums).  weights / mean as
+ * for tto_forward_ex; dW (double [nnz], overwritten; needs weights and no
+ * filter) receives the gradient of the weights, 0 for out-of-range lookups. */
+int tto_backward_ex(const float *grad_out, const float *G1, const float *G2, const float *G3,
+                    const int64_t *m, const int32_t *n, const int32_t *R, const int64_t *indices,
+                    int64_t nnz, const int64_t *offsets, int64_t B, const float *weights,
+                    int mean, double *dG1, double *dG2, double *dG3, double *dW,
+                    int filter_core, int64_t filter_value, int threads) {
   tto_bwd_ctx c;
   int e = tto_init(&c.t, G1, G2, G3, m, n, R);
   if (e) return e;
   if (nnz < 0 || (nnz > 0 && !indices) || (B > 0 && !grad_out)) return TTO_ERR_ARG;
   if (!dG1 || !dG2 || !dG3 || filter_core < 0 || filter_core > 3) return TTO_ERR_ARG;
+  if ((mean && weights) || (dW && (!weights || filter_core != 0))) return TTO_ERR_ARG;
   e = tto_check_offsets(offsets, B, nnz);
   if (e) return e;
   c.indices = indices; c.offsets = offsets; c.grad_out = grad_out;
+  c.weights = weights; c.mean = mean != 0; c.dW = dW;
   c.filter_core = filter_core; c.filter_value = filter_value;
   c.n1g = (size_t)m[0] * n[0] * R[1];
   c.n2g = (size_t)m[1] * R[1] * n[1] * R[2];
@@ -303,6 +353,15 @@ int tto_backward(const float *grad_out, const float *G1, const float *G2, const 
   }
   free(scratch);
   return e;
+}
+
+/* Plain sum pooling. */
+int tto_backward(const float *grad_out, const float *G1, const float *G2, const float *G3,
+                 const int64_t *m, const int32_t *n, const int32_t *R, const int64_t *indices,
+                 int64_t nnz, const int64_t *offsets, int64_t B, double *dG1, double *dG2,
+                 double *dG3, int filter_core, int64_t filter_value, int threads) {
+  return tto_backward_ex(grad_out, G1, G2, G3, m, n, R, indices, nnz, offsets, B, NULL, 0, dG1,
+                         dG2, dG3, NULL, filter_core, filter_value, threads);
 }
 
 /* out[i] = G[i] - lr * dG[i] in fp64. */

@@ -200,3 +200,10 @@ def make_custom(m, n, R, num_bags: int, max_len: int, seed: int, dist=("uniform"
             (num_bags, n[0] * n[1] * n[2]), dtype=np.float32)
     return TTInputs(m=m, n=n, R=R, cores=cores, indices=indices, offsets=offsets,
                     grad_out=grad, N=M)
+
+
+def make_sample_weights(nnz: int, seed: int, low: float = 0.0, high: float = 2.0) -> np.ndarray:
+    """Seeded per-sample weights of the weighted-sum pooling: float32 [nnz], uniform on
+    [low, high)."""
+    rng = np.random.default_rng(seed)
+    return rng.uniform(low, high, size=int(nnz)).astype(np.float32)

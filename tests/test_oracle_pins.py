@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from tensor_train_compressed_gb300.inputs import make_custom, make_inputs
+from tensor_train_compressed_gb300.inputs import make_custom, make_inputs, make_sample_weights
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -26,12 +26,14 @@ def _materialize(cores, m, n):
     return T.reshape(m[0] * m[1] * m[2], n[0] * n[1] * n[2])
 
 
-def _embedding_bag(table, indices, offsets):
-    """torch.nn.functional.embedding_bag (sum), fp64 on CPU."""
+def _embedding_bag(table, indices, offsets, mode="sum", weights=None):
+    """torch.nn.functional.embedding_bag, fp64 on CPU."""
     W = torch.from_numpy(np.ascontiguousarray(table, dtype=np.float64))
     idx = torch.from_numpy(np.asarray(indices, dtype=np.int64))
     off = torch.from_numpy(np.asarray(offsets[:-1], dtype=np.int64))
-    return torch.nn.functional.embedding_bag(idx, W, off, mode="sum").numpy()
+    psw = None if weights is None else torch.from_numpy(np.asarray(weights, dtype=np.float64))
+    return torch.nn.functional.embedding_bag(idx, W, off, mode=mode,
+                                             per_sample_weights=psw).numpy()
 
 
 def _tt_svd(W, m, n):
@@ -262,6 +264,110 @@ def test_backward_threads_and_sgd():
         assert np.allclose(a[k], b[k], rtol=1e-13, atol=1e-13)
         upd = oracle.sgd(x.cores[k], a[k], 0.01)
         assert np.array_equal(upd, x.cores[k].astype(np.float64) - 0.01 * a[k])
+
+
+# ------------------------------------------------- mean and weighted pooling
+
+
+def _pool_case():
+    return make_custom((3, 4, 5), (2, 3, 2), (1, 3, 2, 1), num_bags=41, max_len=9, seed=17,
+                       empty_frac=0.15)
+
+
+@pytest.mark.parametrize("mode", ["mean", "weighted"])
+def test_pooling_variants_match_torch_embedding_bag(mode):
+    x = _pool_case()
+    table = _materialize(x.cores, x.m, x.n)
+    if mode == "mean":
+        out = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, mode="mean")
+        ref = _embedding_bag(table, x.indices, x.offsets, mode="mean")
+    else:
+        w = make_sample_weights(len(x.indices), 5, -1.0, 2.0)
+        out = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, weights=w)
+        ref = _embedding_bag(table, x.indices, x.offsets, weights=w)
+    assert np.abs(np.diff(x.offsets)).min() == 0          # the case holds empty bags
+    assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_integer_weights_equal_repeated_lookups():
+    """A weight k in {0, 1, 2, 3} gives the bag with that lookup repeated k times
+    (dyadic cores: every sum is exact, so the two agree bit for bit)."""
+    m, n, R = (3, 4, 5), (2, 3, 2), (1, 3, 2, 1)
+    cores = _dyadic_cores(m, n, R, 40)
+    x = make_custom(m, n, R, num_bags=25, max_len=6, seed=41)
+    k = np.random.default_rng(42).integers(0, 4, size=len(x.indices))
+    out = oracle.forward(cores, m, n, R, x.indices, x.offsets, weights=k.astype(np.float32))
+    idx2 = np.repeat(x.indices, k)
+    lens = [int(k[x.offsets[b]:x.offsets[b + 1]].sum()) for b in range(25)]
+    off2 = np.concatenate([[0], np.cumsum(lens)])
+    assert np.array_equal(out, oracle.forward(cores, m, n, R, idx2, off2))
+
+
+def test_unit_weights_and_unit_bags_leave_the_sum():
+    x = _pool_case()
+    s = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets)
+    ones = np.ones(len(x.indices), np.float32)
+    assert np.array_equal(oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets,
+                                         weights=ones), s)
+    single = np.arange(len(x.indices) + 1)
+    assert np.array_equal(oracle.forward(x.cores, x.m, x.n, x.R, x.indices, single, mode="mean"),
+                          oracle.forward(x.cores, x.m, x.n, x.R, x.indices, single))
+
+
+@pytest.mark.parametrize("mode", ["mean", "weighted"])
+def test_pooling_variants_backward_match_torch_autograd(mode):
+    x = _pool_case()
+    w = make_sample_weights(len(x.indices), 6, -1.0, 2.0) if mode == "weighted" else None
+    if w is None:
+        dG = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets,
+                             mode="mean")
+    else:
+        dG, dW = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets,
+                                 weights=w, want_dw=True)
+    G = [torch.tensor(c, dtype=torch.float64, requires_grad=True) for c in x.cores]
+    G23 = torch.einsum("yaqb,zbr->yzaqr", G[1], G[2][:, :, :, 0])
+    T = torch.einsum("xpa,yzaqr->xyzpqr", G[0][:, 0], G23).reshape(60, 12)
+    psw = None if w is None else torch.tensor(w, dtype=torch.float64, requires_grad=True)
+    out = torch.nn.functional.embedding_bag(torch.from_numpy(x.indices), T,
+                                            torch.from_numpy(x.offsets[:-1]),
+                                            mode="mean" if w is None else "sum",
+                                            per_sample_weights=psw)
+    (out * torch.from_numpy(x.grad_out.astype(np.float64))).sum().backward()
+    for k in range(3):
+        ref = G[k].grad.numpy()
+        assert np.abs(dG[k] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+    if w is not None:
+        ref = psw.grad.numpy()
+        assert np.abs(dW - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_weight_gradient_central_differences():
+    """out is linear in every weight, so a central difference is exact (dyadic data)."""
+    m, n, R = (3, 4, 5), (2, 3, 2), (1, 3, 2, 1)
+    cores = _dyadic_cores(m, n, R, 50)
+    x = make_custom(m, n, R, num_bags=12, max_len=5, seed=51)
+    g = (np.random.default_rng(52).integers(-3, 4, size=x.grad_out.shape) / 2.0).astype(
+        np.float32)
+    w = (np.random.default_rng(53).integers(-4, 5, size=len(x.indices)) / 4.0).astype(np.float32)
+    _, dW = oracle.backward(g, cores, m, n, R, x.indices, x.offsets, weights=w, want_dw=True)
+    for l in range(0, len(x.indices), 3):
+        up, dn = w.copy(), w.copy()
+        up[l] += 0.5
+        dn[l] -= 0.5
+        fu = (oracle.forward(cores, m, n, R, x.indices, x.offsets, weights=up) * g).sum()
+        fd = (oracle.forward(cores, m, n, R, x.indices, x.offsets, weights=dn) * g).sum()
+        assert fu - fd == dW[l]
+
+
+def test_pooling_variant_errors():
+    x = _pool_case()
+    w = np.ones(len(x.indices), np.float32)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, weights=w, mode="mean")
+    assert e.value.code == oracle.TTO_ERR_ARG
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, want_dw=True)
+    assert e.value.code == oracle.TTO_ERR_ARG
 
 
 # ---------------------------------------------------------------- grouping
