@@ -89,6 +89,25 @@ int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_
                    const int64_t* offsets, int64_t num_bags, float* out, void* workspace,
                    size_t ws_bytes, void* stream);
 
+/* Pooling rules of tt_emb_forward_ex / tt_emb_backward_ex. */
+#define TT_EMB_POOL_SUM 0    /* out[b] = sum of the bag's rows (optionally weighted)   */
+#define TT_EMB_POOL_MEAN 1   /* out[b] = that sum / number of the bag's lookups        */
+
+/* Forward with the other pooling rules of an embedding bag (the TT-Rec
+ * abstract names its operator after the EmbeddingBag; the pages themselves
+ * only sum).  Same arguments and contract as tt_emb_forward, plus:
+ *  - per_sample_weights: NULL, or float32 [nnz] (device, 4-byte aligned):
+ *    out[b] = sum over the bag's lookups l of per_sample_weights[l] * row(indices[l]).
+ *    Only with pooling = TT_EMB_POOL_SUM (TT_EMB_ERR_ARG otherwise).
+ *  - pooling: TT_EMB_POOL_SUM, or TT_EMB_POOL_MEAN: every non-empty bag's sum
+ *    is divided by its number of lookups (out-of-range lookups included in
+ *    the count); empty bags give zeros.
+ * tt_emb_forward is tt_emb_forward_ex(..., NULL, TT_EMB_POOL_SUM, ...). */
+int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int32_t n[3],
+                      const int32_t R[4], const int64_t* indices, int64_t nnz,
+                      const int64_t* offsets, int64_t num_bags, const float* per_sample_weights,
+                      int pooling, float* out, void* workspace, size_t ws_bytes, void* stream);
+
 /* Backward into the cores: core_grads[k] (same layout as cores[k]) are
  * ACCUMULATED (+=) with d<grad_out, out>/dG_k; the caller zeroes them.
  * grad_out is float32 [num_bags][D].  With reuse_grouping != 0 the grouping
@@ -102,6 +121,20 @@ int tt_emb_backward(const float* grad_out, const float* const cores[3], const in
                     const int32_t n[3], const int32_t R[4], const int64_t* indices, int64_t nnz,
                     const int64_t* offsets, int64_t num_bags, float* const core_grads[3],
                     void* workspace, size_t ws_bytes, int reuse_grouping, void* stream);
+
+/* Backward of tt_emb_forward_ex: per_sample_weights and pooling as given to
+ * that forward; core_grads accumulated as in tt_emb_backward.
+ *  - grad_weights: NULL, or float32 [nnz] (device, 4-byte aligned; requires
+ *    per_sample_weights): OVERWRITTEN with d<grad_out, out>/d per_sample_weights[l]
+ *    = <grad_out[bag(l)], row(indices[l])>, 0 for out-of-range lookups.  The
+ *    rows are recomputed inside this call (one extra pass of the row kernels).
+ * tt_emb_backward is tt_emb_backward_ex(..., NULL, TT_EMB_POOL_SUM, core_grads, NULL, ...). */
+int tt_emb_backward_ex(const float* grad_out, const float* const cores[3], const int64_t m[3],
+                       const int32_t n[3], const int32_t R[4], const int64_t* indices,
+                       int64_t nnz, const int64_t* offsets, int64_t num_bags,
+                       const float* per_sample_weights, int pooling, float* const core_grads[3],
+                       float* grad_weights, void* workspace, size_t ws_bytes, int reuse_grouping,
+                       void* stream);
 
 /* Plain SGD on the three cores, one launch: G_k <- G_k - lr * dG_k
  * (element-wise, fp32).  With zero_grads != 0 the same pass also resets every

@@ -12,14 +12,16 @@ import numpy as np
 import torch
 
 from ._binding import (EXPORTED, TTEmbError, library_path, lib, tt_emb_backward,
-                       tt_emb_forward, tt_emb_get_error, tt_emb_group, tt_emb_grouping_view,
+                       tt_emb_backward_ex, tt_emb_forward, tt_emb_forward_ex, tt_emb_get_error, tt_emb_group, tt_emb_grouping_view,
                        tt_emb_forward_static, tt_emb_profile_read, tt_emb_profile_start,
                        tt_emb_profile_stop,
                        tt_emb_sgd, tt_emb_version, tt_emb_workspace_bytes)
 from ._binding import (TT_EMB_ERR_ARG, TT_EMB_ERR_CUDA, TT_EMB_ERR_INDEX, TT_EMB_ERR_OFFSETS,
-                       TT_EMB_ERR_TIMEOUT, TT_EMB_ERR_UNSUPPORTED, TT_EMB_ERR_WORKSPACE, TT_EMB_OK)
+                       TT_EMB_ERR_TIMEOUT, TT_EMB_ERR_UNSUPPORTED, TT_EMB_ERR_WORKSPACE, TT_EMB_OK,
+                       TT_EMB_POOL_MEAN, TT_EMB_POOL_SUM)
 
 __all__ = ["TTEmbeddingBag", "TTEmbError", "tt_emb_forward", "tt_emb_forward_static", "tt_emb_backward", "tt_emb_sgd",
+           "tt_emb_forward_ex", "tt_emb_backward_ex",
            "tt_emb_group", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_workspace_bytes",
            "tt_emb_version", "tt_emb_profile_start", "tt_emb_profile_stop", "tt_emb_profile_read",
            "read_grouping", "lib", "library_path", "EXPORTED"]
@@ -48,15 +50,19 @@ def read_grouping(m, n, R, nnz: int, num_bags: int, workspace: torch.Tensor) -> 
 
 
 class TTEmbeddingBag:
-    """A TT-compressed embedding table with sum pooling, resident on one GPU.
+    """A TT-compressed embedding table resident on one GPU.
 
     ``cores`` are float32 arrays [m_k][R_{k-1}][n_k][R_k].  ``forward`` takes
     int64 indices and CSR offsets (host or device tensors / numpy arrays; host
-    inputs are copied in on the current stream) and returns the pooled
-    float32 [num_bags][D] output on the device.
+    inputs are copied in on the current stream), optionally per-sample weights
+    (sum pooling), and returns the pooled float32 [num_bags][D] output on the
+    device.  ``mode`` is "sum" or "mean".
     """
 
-    def __init__(self, cores, m, n, R, device="cuda"):
+    def __init__(self, cores, m, n, R, device="cuda", mode: str = "sum"):
+        if mode not in ("sum", "mean"):
+            raise ValueError("mode must be 'sum' or 'mean'")
+        self.mode = mode
         self.m, self.n, self.R = tuple(int(v) for v in m), tuple(int(v) for v in n), \
             tuple(int(v) for v in R)
         self.D = self.n[0] * self.n[1] * self.n[2]
@@ -77,24 +83,40 @@ class TTEmbeddingBag:
         t = torch.as_tensor(x)
         return t.to(self.device, torch.int64, non_blocking=True).contiguous()
 
-    def forward(self, indices, offsets, out=None, stream=None):
+    def forward(self, indices, offsets, per_sample_weights=None, out=None, stream=None):
         idx, off = self._to_dev(indices), self._to_dev(offsets)
         B = off.numel() - 1
         self._ensure_ws(idx.numel(), B)
         if out is None:
             out = torch.empty((B, self.D), dtype=torch.float32, device=self.device)
-        tt_emb_forward(self.cores, self.m, self.n, self.R, idx, off, out, self.workspace, stream)
-        self._batch = (idx, off)
+        psw = None
+        if per_sample_weights is not None:
+            psw = torch.as_tensor(per_sample_weights).to(self.device, torch.float32,
+                                                         non_blocking=True).contiguous()
+        if psw is None and self.mode == "sum":
+            tt_emb_forward(self.cores, self.m, self.n, self.R, idx, off, out, self.workspace,
+                           stream)
+        else:
+            tt_emb_forward_ex(self.cores, self.m, self.n, self.R, idx, off, psw, self.mode, out,
+                              self.workspace, stream)
+        self._batch = (idx, off, psw)
         return out
 
-    def backward(self, grad_out, stream=None):
-        """Accumulate d<grad_out, out>/dG into self.grads, reusing the last forward's grouping."""
+    def backward(self, grad_out, grad_weights=None, stream=None):
+        """Accumulate d<grad_out, out>/dG into self.grads, reusing the last forward's grouping.
+        With per-sample weights in that forward and ``grad_weights`` (a float32 CUDA tensor
+        [nnz]), the weights' gradient is written there too."""
         if self._batch is None:
             raise RuntimeError("backward needs a forward on the same batch first")
-        idx, off = self._batch
+        idx, off, psw = self._batch
         g = torch.as_tensor(grad_out).to(self.device, torch.float32, non_blocking=True)
-        tt_emb_backward(g.contiguous(), self.cores, self.m, self.n, self.R, idx, off, self.grads,
-                        self.workspace, reuse_grouping=True, stream=stream)
+        if psw is None and self.mode == "sum" and grad_weights is None:
+            tt_emb_backward(g.contiguous(), self.cores, self.m, self.n, self.R, idx, off,
+                            self.grads, self.workspace, reuse_grouping=True, stream=stream)
+        else:
+            tt_emb_backward_ex(g.contiguous(), self.cores, self.m, self.n, self.R, idx, off, psw,
+                               self.mode, self.grads, grad_weights, self.workspace,
+                               reuse_grouping=True, stream=stream)
         return self.grads
 
     def zero_grad(self):

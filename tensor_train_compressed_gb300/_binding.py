@@ -25,8 +25,12 @@ TT_EMB_ERR_OFFSETS = -5
 TT_EMB_ERR_TIMEOUT = -6
 TT_EMB_ERR_UNSUPPORTED = -7
 _NAMES = {v: k for k, v in list(globals().items()) if k.startswith("TT_EMB_")}
+TT_EMB_POOL_SUM = 0
+TT_EMB_POOL_MEAN = 1
+_POOLING = {"sum": TT_EMB_POOL_SUM, "mean": TT_EMB_POOL_MEAN}
 
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
+            "tt_emb_forward_ex", "tt_emb_backward_ex",
             "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_profile_start",
             "tt_emb_profile_stop", "tt_emb_profile_read", "tt_emb_forward_static",
             "tt_emb_version")
@@ -65,6 +69,9 @@ def lib():
         L.tt_emb_group.argtypes = [P, P, P, P, I64, P, I64, P, SZ, P]
         L.tt_emb_forward.argtypes = [P, P, P, P, P, I64, P, I64, P, P, SZ, P]
         L.tt_emb_backward.argtypes = [P, P, P, P, P, P, I64, P, I64, P, P, SZ, ctypes.c_int, P]
+        L.tt_emb_forward_ex.argtypes = [P, P, P, P, P, I64, P, I64, P, ctypes.c_int, P, P, SZ, P]
+        L.tt_emb_backward_ex.argtypes = [P, P, P, P, P, P, I64, P, I64, P, ctypes.c_int, P, P, P,
+                                         SZ, ctypes.c_int, P]
         L.tt_emb_sgd.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, P]
         L.tt_emb_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
         L.tt_emb_grouping_view.argtypes = [P, P, P, I64, I64, P, ctypes.POINTER(Grouping)]
@@ -143,6 +150,40 @@ def tt_emb_backward(grad_out, cores, m, n, R, indices, offsets, core_grads, work
                                  _ptrs3(core_grads, "core_grads"),
                                  _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
                                  int(bool(reuse_grouping)), _stream(stream)), "tt_emb_backward")
+
+
+def _opt(t, dtype, name):
+    return None if t is None else _dev(t, dtype, name)
+
+
+def tt_emb_forward_ex(cores, m, n, R, indices, offsets, per_sample_weights, pooling, out,
+                      workspace, stream=None):
+    """pooling: "sum" / "mean" (or the TT_EMB_POOL_* value); per_sample_weights: None or a
+    float32 CUDA tensor [nnz] (sum only)."""
+    _check(lib().tt_emb_forward_ex(_ptrs3(cores, "cores"), *_shape(m, n, R),
+                                   _dev(indices, torch.int64, "indices"), indices.numel(),
+                                   _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
+                                   _opt(per_sample_weights, torch.float32, "per_sample_weights"),
+                                   int(_POOLING.get(pooling, pooling)),
+                                   _dev(out, torch.float32, "out"),
+                                   _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                   _stream(stream)), "tt_emb_forward_ex")
+
+
+def tt_emb_backward_ex(grad_out, cores, m, n, R, indices, offsets, per_sample_weights, pooling,
+                       core_grads, grad_weights, workspace, reuse_grouping: bool = True,
+                       stream=None):
+    _check(lib().tt_emb_backward_ex(_dev(grad_out, torch.float32, "grad_out"),
+                                    _ptrs3(cores, "cores"), *_shape(m, n, R),
+                                    _dev(indices, torch.int64, "indices"), indices.numel(),
+                                    _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
+                                    _opt(per_sample_weights, torch.float32, "per_sample_weights"),
+                                    int(_POOLING.get(pooling, pooling)),
+                                    _ptrs3(core_grads, "core_grads"),
+                                    _opt(grad_weights, torch.float32, "grad_weights"),
+                                    _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                    int(bool(reuse_grouping)), _stream(stream)),
+           "tt_emb_backward_ex")
 
 
 def tt_emb_sgd(cores, core_grads, m, n, R, lr: float, zero_grads: bool = False, stream=None):

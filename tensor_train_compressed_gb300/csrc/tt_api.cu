@@ -161,6 +161,16 @@ static int check_batch(const Shape& s, const int64_t* indices, int64_t nnz, cons
   return TT_EMB_OK;
 }
 
+// Pooling rule and per-sample weights (float32 [nnz], 4-byte aligned; only
+// with the sum).
+static int check_pooling(const float* psw, int pooling, Pooling* p) {
+  if (pooling != TT_EMB_POOL_SUM && pooling != TT_EMB_POOL_MEAN) return TT_EMB_ERR_ARG;
+  if (psw && (pooling != TT_EMB_POOL_SUM || !aligned(psw, 4))) return TT_EMB_ERR_ARG;
+  p->mode = psw ? kPoolWeighted : (pooling == TT_EMB_POOL_MEAN ? kPoolMean : kPoolSum);
+  p->psw = psw;
+  return TT_EMB_OK;
+}
+
 static int check_cores(const float* const cores[3]) {
   if (!cores) return TT_EMB_ERR_ARG;
   for (int k = 0; k < 3; ++k)
@@ -174,7 +184,7 @@ using namespace tt;
 
 extern "C" {
 
-int tt_emb_version(void) { return 100; }
+int tt_emb_version(void) { return 200; }
 
 int tt_emb_workspace_bytes(const int64_t m[3], const int32_t n[3], const int32_t R[4], int64_t nnz,
                            int64_t num_bags, size_t* bytes) {
@@ -202,14 +212,17 @@ int tt_emb_group(const int64_t m[3], const int32_t n[3], const int32_t R[4], con
                       (cudaStream_t)stream);
 }
 
-int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_t n[3],
-                   const int32_t R[4], const int64_t* indices, int64_t nnz,
-                   const int64_t* offsets, int64_t num_bags, float* out, void* workspace,
-                   size_t ws_bytes, void* stream) {
+int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int32_t n[3],
+                      const int32_t R[4], const int64_t* indices, int64_t nnz,
+                      const int64_t* offsets, int64_t num_bags, const float* per_sample_weights,
+                      int pooling, float* out, void* workspace, size_t ws_bytes, void* stream) {
   Shape s;
   int rc = shape_from_args(m, n, R, &s);
   if (rc) return rc;
   rc = check_cores(cores);
+  if (rc) return rc;
+  Pooling pool;
+  rc = check_pooling(per_sample_weights, pooling, &pool);
   if (rc) return rc;
   Layout L;
   rc = check_batch(s, indices, nnz, offsets, num_bags, workspace, ws_bytes, &L);
@@ -228,13 +241,23 @@ int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_
       return TT_EMB_ERR_CUDA;
     return TT_EMB_OK;
   }
-  return launch_forward(s, L, w, cores, offsets, nnz, num_bags, out, st);
+  return launch_forward(s, L, w, cores, offsets, nnz, num_bags, pool, out, st);
 }
 
-int tt_emb_backward(const float* grad_out, const float* const cores[3], const int64_t m[3],
-                    const int32_t n[3], const int32_t R[4], const int64_t* indices, int64_t nnz,
-                    const int64_t* offsets, int64_t num_bags, float* const core_grads[3],
-                    void* workspace, size_t ws_bytes, int reuse_grouping, void* stream) {
+int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_t n[3],
+                   const int32_t R[4], const int64_t* indices, int64_t nnz,
+                   const int64_t* offsets, int64_t num_bags, float* out, void* workspace,
+                   size_t ws_bytes, void* stream) {
+  return tt_emb_forward_ex(cores, m, n, R, indices, nnz, offsets, num_bags, nullptr,
+                           TT_EMB_POOL_SUM, out, workspace, ws_bytes, stream);
+}
+
+int tt_emb_backward_ex(const float* grad_out, const float* const cores[3], const int64_t m[3],
+                       const int32_t n[3], const int32_t R[4], const int64_t* indices,
+                       int64_t nnz, const int64_t* offsets, int64_t num_bags,
+                       const float* per_sample_weights, int pooling, float* const core_grads[3],
+                       float* grad_weights, void* workspace, size_t ws_bytes, int reuse_grouping,
+                       void* stream) {
   Shape s;
   int rc = shape_from_args(m, n, R, &s);
   if (rc) return rc;
@@ -242,6 +265,10 @@ int tt_emb_backward(const float* grad_out, const float* const cores[3], const in
   if (rc) return rc;
   rc = check_cores(core_grads);
   if (rc) return rc;
+  Pooling pool;
+  rc = check_pooling(per_sample_weights, pooling, &pool);
+  if (rc) return rc;
+  if (grad_weights && (!per_sample_weights || !aligned(grad_weights, 4))) return TT_EMB_ERR_ARG;
   Layout L;
   rc = check_batch(s, indices, nnz, offsets, num_bags, workspace, ws_bytes, &L);
   if (rc) return rc;
@@ -256,7 +283,16 @@ int tt_emb_backward(const float* grad_out, const float* const cores[3], const in
     if (rc) return rc;
   }
   return launch_backward(s, L, w, grad_out, reuse_grouping ? 1 : 0, cores, offsets, nnz, num_bags,
-                         core_grads, st);
+                         pool, core_grads, grad_weights, st);
+}
+
+int tt_emb_backward(const float* grad_out, const float* const cores[3], const int64_t m[3],
+                    const int32_t n[3], const int32_t R[4], const int64_t* indices, int64_t nnz,
+                    const int64_t* offsets, int64_t num_bags, float* const core_grads[3],
+                    void* workspace, size_t ws_bytes, int reuse_grouping, void* stream) {
+  return tt_emb_backward_ex(grad_out, cores, m, n, R, indices, nnz, offsets, num_bags, nullptr,
+                            TT_EMB_POOL_SUM, core_grads, nullptr, workspace, ws_bytes,
+                            reuse_grouping, stream);
 }
 
 int tt_emb_sgd(float* const cores[3], float* const core_grads[3], const int64_t m[3],

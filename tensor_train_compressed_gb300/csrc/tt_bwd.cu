@@ -64,12 +64,31 @@ __device__ __forceinline__ void s_flush(const WS& w, int32_t u, int64_t k0, int 
   }
 }
 
+// The factor with which lookup l's row enters its bag b (PoolMode): its
+// per-sample weight, 1 / (length of b), or 1.  S[x] sums grad_out[b] times
+// that factor.
+template <int MODE>
+__device__ __forceinline__ float lookup_factor(const float* __restrict__ psw,
+                                               const int64_t* __restrict__ offsets, int64_t nnz,
+                                               int32_t l, int32_t b) {
+  if (MODE == kPoolWeighted) return psw[l];
+  if (MODE == kPoolMean) {
+    int64_t l0 = offsets[b], l1 = offsets[b + 1];
+    l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
+    l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
+    return l1 > l0 ? 1.f / (float)(l1 - l0) : 0.f;
+  }
+  return 1.f;
+}
+
 // S[x] for every unique row: one warp per slice of kSSlice sorted lookups.  The
-// lanes fetch the slice's (unique row, bag) pairs in parallel, 32 at a time; the
-// output-gradient rows are then summed with 8 loads in flight, flushing at every
-// change of unique row.
+// lanes fetch the slice's (unique row, bag, factor) triples in parallel, 32 at a
+// time; the output-gradient rows are then summed with 8 loads in flight,
+// flushing at every change of unique row.
+template <int MODE>
 __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict__ grad_out,
-                                                  int64_t B, int D) {
+                                                  int64_t B, int D, const float* __restrict__ psw,
+                                                  const int64_t* __restrict__ offsets, int64_t nnz) {
   const int lane = threadIdx.x & 31;
   const int64_t nv = w.ctl->n_valid;
   const int64_t k0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kSSlice;
@@ -87,21 +106,24 @@ __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict_
     for (int64_t kb = k0; kb < k1; kb += 32) {
       const int cnt = (int)(k1 - kb < 32 ? k1 - kb : 32);
       int32_t my_u = -1, my_b = 0;
+      float my_c = 1.f;
       if (lane < cnt) {
         const int32_t l = w.perm[kb + lane];
         my_u = w.uid[l];
         const int32_t bb = w.bag_of[l];
         my_b = bb < 0 ? 0 : (bb >= B ? (int32_t)(B - 1) : bb);
+        my_c = lookup_factor<MODE>(psw, offsets, nnz, l, my_b);
       }
       for (int j = 0; j < cnt; j += 8) {
         int32_t uj[8];
         float4 g[8];
-        float gs[8];
+        float gs[8], cf[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const int jj = (j + t) & 31;
           uj[t] = __shfl_sync(0xffffffffu, my_u, jj);
           const int32_t bj = __shfl_sync(0xffffffffu, my_b, jj);
+          cf[t] = __shfl_sync(0xffffffffu, my_c, jj);
           const bool use = live && (j + t) < cnt;
           g[t] = z4;
           gs[t] = 0.f;
@@ -119,8 +141,13 @@ __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict_
             accs = 0.f;
             cur = uj[t];
           }
-          acc.x += g[t].x; acc.y += g[t].y; acc.z += g[t].z; acc.w += g[t].w;
-          accs += gs[t];
+          if (MODE == kPoolSum) {
+            f4add(acc, g[t]);
+            accs += gs[t];
+          } else {
+            f4fma(acc, cf[t], g[t]);
+            accs = fmaf(cf[t], gs[t], accs);
+          }
         }
       }
     }
@@ -146,8 +173,11 @@ __device__ __forceinline__ void s_merge_flush(const WS& w, int32_t u, int64_t K0
 }
 
 // D = 128: every lane owns one float4 column of the rows.
+template <int MODE>
 __global__ void __launch_bounds__(256) k_s_gather_cta(WS w, const float* __restrict__ grad_out,
-                                                      int64_t B) {
+                                                      int64_t B, const float* __restrict__ psw,
+                                                      const int64_t* __restrict__ offsets,
+                                                      int64_t nnz) {
   __shared__ float4 part[8][2][32];
   __shared__ int part_u[8][2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -176,11 +206,13 @@ __global__ void __launch_bounds__(256) k_s_gather_cta(WS w, const float* __restr
   for (int64_t kb = k0; kb < k1; kb += 32) {
     const int cnt = (int)(k1 - kb < 32 ? k1 - kb : 32);
     int32_t my_u = -1, my_b = 0;
+    float my_c = 1.f;
     if (lane < cnt) {
       const int32_t l = w.perm[kb + lane];
       my_u = w.uid[l];
       const int32_t bb = w.bag_of[l];
       my_b = bb < 0 ? 0 : (bb >= B ? (int32_t)(B - 1) : bb);
+      my_c = lookup_factor<MODE>(psw, offsets, nnz, l, my_b);
     }
     int j = 0;
     for (; j + 8 <= cnt; j += 8) {
@@ -198,18 +230,21 @@ __global__ void __launch_bounds__(256) k_s_gather_cta(WS w, const float* __restr
           acc = z4;
           cur = uj[t];
         }
-        f4add(acc, g[t]);
+        if (MODE == kPoolSum) f4add(acc, g[t]);
+        else f4fma(acc, __shfl_sync(0xffffffffu, my_c, j + t), g[t]);
       }
     }
     for (; j < cnt; ++j) {
       const int32_t u = __shfl_sync(0xffffffffu, my_u, j);
       const float4 g = __ldg(g4 + (int64_t)__shfl_sync(0xffffffffu, my_b, j) * 32 + lane);
+      const float cj = __shfl_sync(0xffffffffu, my_c, j);
       if (u != cur) {
         close_run();
         acc = z4;
         cur = u;
       }
-      f4add(acc, g);
+      if (MODE == kPoolSum) f4add(acc, g);
+      else f4fma(acc, cj, g);
     }
   }
   // the last run (or the only one)
@@ -239,6 +274,65 @@ __global__ void __launch_bounds__(256) k_s_gather_cta(WS w, const float* __restr
         f4add(m, part[ww][e][lane]);
       }
     if (mu >= 0) s_merge_flush(w, mu, K0, m, lane);
+  }
+}
+
+// Gradient of the per-sample weights: dW[l] = <grad_out[bag(l)], row(r_l)>,
+// read from the unique rows in the row buffer (filled by the row kernels just
+// before); one warp per bag, 4 lookups per step, each lane a float4 column of
+// the rows; out-of-range lookups get 0.  Stores are one coalesced write per
+// 32 lookups.
+__global__ void __launch_bounds__(256) k_psw_grad(const int64_t* __restrict__ offsets, int64_t B,
+                                                  int64_t nnz, const int32_t* __restrict__ uid,
+                                                  const float* __restrict__ rowbuf, int D,
+                                                  const float* __restrict__ grad_out,
+                                                  float* __restrict__ dW) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const bool vec = (D & 3) == 0;
+  const int cols = vec ? (D >> 2) : D;
+  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < B; b += warps) {
+    int64_t l0 = offsets[b], l1 = offsets[b + 1];
+    l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
+    l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
+    for (int64_t lb = l0; lb < l1; lb += 32) {
+      const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
+      const int32_t my_u = lane < cnt ? uid[lb + lane] : -1;
+      float my_dw = 0.f;
+      for (int j = 0; j < cnt; j += 4) {
+        int32_t u[4];
+        float part[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          u[t] = __shfl_sync(0xffffffffu, my_u, (j + t) & 31);
+          if (j + t >= cnt) u[t] = -1;
+          part[t] = 0.f;
+        }
+        for (int c = lane; c < cols; c += 32) {
+          if (vec) {
+            const float4 g = reinterpret_cast<const float4*>(grad_out + b * (int64_t)D)[c];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              if (u[t] >= 0) {
+                const float4 v = reinterpret_cast<const float4*>(rowbuf + (int64_t)u[t] * D)[c];
+                part[t] = fmaf(g.x, v.x, fmaf(g.y, v.y, fmaf(g.z, v.z, fmaf(g.w, v.w, part[t]))));
+              }
+          } else {
+            const float g = grad_out[b * (int64_t)D + c];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              if (u[t] >= 0) part[t] = fmaf(g, rowbuf[(int64_t)u[t] * D + c], part[t]);
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) part[t] += __shfl_xor_sync(0xffffffffu, part[t], o);
+          if (lane == j + t) my_dw = part[t];
+        }
+      }
+      if (lane < cnt) dW[lb + lane] = my_dw;
+    }
   }
 }
 
@@ -977,23 +1071,53 @@ static int persistent_grid_bwd(const void* fn, int threads, size_t smem) {
   return per_sm * sm_count();
 }
 
+template <int MODE>
+static void launch_s_gather(const Shape& s, const WS& w, const float* grad_out, int64_t nnz,
+                            int64_t num_bags, const int64_t* offsets, const float* psw,
+                            cudaStream_t st) {
+  if (s.D == 128) {
+    TT_TIMED("k_s_gather", st, (k_s_gather_cta<MODE><<<(int)ceil_div(nnz, kSCta), 256, 0, st>>>(
+                                   w, grad_out, num_bags, psw, offsets, nnz)));
+  } else {
+    const int64_t slices = ceil_div(nnz, kSSlice);
+    TT_TIMED("k_s_gather", st, (k_s_gather<MODE><<<(int)ceil_div(slices, 8), 256, 0, st>>>(
+                                   w, grad_out, num_bags, s.D, psw, offsets, nnz)));
+  }
+}
+
 int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out, int reuse,
                     const float* const cores[3], const int64_t* offsets, int64_t nnz,
-                    int64_t num_bags, float* const core_grads[3], cudaStream_t st) {
+                    int64_t num_bags, const Pooling& pool, float* const core_grads[3],
+                    float* grad_weights, cudaStream_t st) {
   if (nnz == 0) return TT_EMB_OK;
   const int sms = sm_count();
+  if (grad_weights) {
+    // the unique rows (the row buffer is free until S takes it), then one dot
+    // product per lookup; the forward chunk counter is re-armed first
+    if (cudaMemsetAsync(&w.ctl->fwd_chunk_ctr, 0, sizeof(uint32_t), st) != cudaSuccess)
+      return TT_EMB_ERR_CUDA;
+    const int rc = launch_rows(s, w, cores, st);
+    if (rc) return rc;
+    int grid = (int)ceil_div(num_bags, 8);
+    if (grid > sms * 16) grid = sms * 16;
+    TT_TIMED("k_psw_grad", st, (k_psw_grad<<<grid, 256, 0, st>>>(offsets, num_bags, nnz, w.uid,
+                                                                  w.rowbuf, s.D, grad_out,
+                                                                  grad_weights)));
+  }
   int grid = (int)ceil_div(L.rowbuf_rows > num_bags ? L.rowbuf_rows : num_bags, 256);
   if (grid > sms * 8) grid = sms * 8;
   if (grid < 1) grid = 1;
   const bool cta_gather = s.D == 128;
   TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D, offsets, num_bags, nnz,
                                                              cta_gather ? kSCta : kSSlice)));
-  const int64_t slices = ceil_div(nnz, kSSlice);
-  if (cta_gather) {
-    TT_TIMED("k_s_gather", st, (k_s_gather_cta<<<(int)ceil_div(nnz, kSCta), 256, 0, st>>>(
-                                   w, grad_out, num_bags)));
-  } else {
-    TT_TIMED("k_s_gather", st, (k_s_gather<<<(int)ceil_div(slices, 8), 256, 0, st>>>(w, grad_out, num_bags, s.D)));
+  switch (pool.mode) {
+    case kPoolWeighted:
+      launch_s_gather<kPoolWeighted>(s, w, grad_out, nnz, num_bags, offsets, pool.psw, st);
+      break;
+    case kPoolMean:
+      launch_s_gather<kPoolMean>(s, w, grad_out, nnz, num_bags, offsets, nullptr, st);
+      break;
+    default: launch_s_gather<kPoolSum>(s, w, grad_out, nnz, num_bags, offsets, nullptr, st);
   }
 
   BwdArgs ba;

@@ -549,12 +549,30 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
   }
 }
 
-// out[b] = sum of the unique rows of bag b's lookups; one warp per bag.  The
-// lanes fetch up to 32 of the bag's unique-row ids at once; each lane then sums
-// its float4 column of those rows, 8 loads in flight.
+// out[b] = pooled unique rows of bag b's lookups; one warp per bag.  The
+// lanes fetch up to 32 of the bag's unique-row ids (and weights) at once; each
+// lane then sums its float4 column of those rows, 8 loads in flight.  MODE
+// (PoolMode): plain sum, sum with each row scaled by its lookup's per-sample
+// weight, or the sum divided by the bag's length (empty bags give zeros).
 
+// The weight of lookup l (MODE kPoolWeighted), 0 for an out-of-range lookup.
+template <int MODE>
+__device__ __forceinline__ float pool_weight(const float* __restrict__ psw, int64_t l, int32_t u) {
+  return (MODE == kPoolWeighted && u >= 0) ? psw[l] : 1.f;
+}
+
+template <int MODE>
+__device__ __forceinline__ void pool_mean(float4& acc, int64_t len) {
+  if (MODE == kPoolMean && len > 0) {
+    const float f = (float)len;
+    acc.x /= f; acc.y /= f; acc.z /= f; acc.w /= f;
+  }
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offsets, int64_t B,
                                               int64_t nnz, const int32_t* __restrict__ uid,
+                                              const float* __restrict__ psw,
                                               const float* __restrict__ rowbuf, int D,
                                               float* __restrict__ out) {
   const int lane = threadIdx.x & 31;
@@ -574,22 +592,33 @@ __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offset
         for (int64_t lb = l0; lb < l1; lb += 32) {
           const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
           const int32_t my_u = lane < cnt ? uid[lb + lane] : -1;
+          const float my_w = lane < cnt ? pool_weight<MODE>(psw, lb + lane, my_u) : 0.f;
           int j = 0;
           for (; j + 8 <= cnt; j += 8) {
             float4 v[8];
+            float wt[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               const int32_t u = __shfl_sync(0xffffffffu, my_u, j + t);
+              wt[t] = __shfl_sync(0xffffffffu, my_w, j + t);
               v[t] = (live && u >= 0) ? rb4[(int64_t)u * cols + c] : z4;
             }
 #pragma unroll
-            for (int t = 0; t < 8; ++t) f4add(acc, v[t]);
+            for (int t = 0; t < 8; ++t) {
+              if (MODE == kPoolWeighted) f4fma(acc, wt[t], v[t]);
+              else f4add(acc, v[t]);
+            }
           }
           for (; j < cnt; ++j) {
             const int32_t u = __shfl_sync(0xffffffffu, my_u, j);
-            if (live && u >= 0) f4add(acc, rb4[(int64_t)u * cols + c]);
+            const float wj = __shfl_sync(0xffffffffu, my_w, j);
+            if (live && u >= 0) {
+              if (MODE == kPoolWeighted) f4fma(acc, wj, rb4[(int64_t)u * cols + c]);
+              else f4add(acc, rb4[(int64_t)u * cols + c]);
+            }
           }
         }
+        pool_mean<MODE>(acc, l1 - l0);
         if (live) reinterpret_cast<float4*>(out + b * (int64_t)D)[c] = acc;
       }
     } else {
@@ -597,8 +626,12 @@ __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offset
         float acc = 0.f;
         for (int64_t l = l0; l < l1; ++l) {
           const int u = uid[l];
-          if (u >= 0) acc += rowbuf[(int64_t)u * D + j];
+          if (u >= 0) {
+            if (MODE == kPoolWeighted) acc = fmaf(psw[l], rowbuf[(int64_t)u * D + j], acc);
+            else acc += rowbuf[(int64_t)u * D + j];
+          }
         }
+        if (MODE == kPoolMean && l1 > l0) acc /= (float)(l1 - l0);
         out[b * (int64_t)D + j] = acc;
       }
     }
@@ -607,9 +640,11 @@ __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offset
 
 // Pooling for D = 128: every lane owns one float4 column, so the inner loop
 // needs no column checks; lookups with an out-of-range index point at the zero
-// row `zrow`; full batches of 8 row loads run unpredicated.
+// row `zrow` (weight 0); full batches of 8 row loads run unpredicated.
+template <int MODE>
 __global__ void __launch_bounds__(256) k_pool128(const int64_t* __restrict__ offsets, int64_t B,
                                                  int64_t nnz, const int32_t* __restrict__ uid,
+                                                 const float* __restrict__ psw,
                                                  const float4* __restrict__ rb4, int32_t zrow,
                                                  float4* __restrict__ out) {
   const int lane = threadIdx.x & 31;
@@ -622,6 +657,8 @@ __global__ void __launch_bounds__(256) k_pool128(const int64_t* __restrict__ off
     for (int64_t lb = l0; lb < l1; lb += 32) {
       const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
       int32_t my_u = lane < cnt ? uid[lb + lane] : zrow;
+      float my_w = 0.f;
+      if (MODE == kPoolWeighted) my_w = (lane < cnt && my_u >= 0) ? psw[lb + lane] : 0.f;
       my_u = my_u < 0 ? zrow : my_u;
       int j = 0;
       for (; j + 8 <= cnt; j += 8) {
@@ -629,10 +666,18 @@ __global__ void __launch_bounds__(256) k_pool128(const int64_t* __restrict__ off
 #pragma unroll
         for (int t = 0; t < 8; ++t) v[t] = rb4[(int64_t)__shfl_sync(0xffffffffu, my_u, j + t) * 32 + lane];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) f4add(acc, v[t]);
+        for (int t = 0; t < 8; ++t) {
+          if (MODE == kPoolWeighted) f4fma(acc, __shfl_sync(0xffffffffu, my_w, j + t), v[t]);
+          else f4add(acc, v[t]);
+        }
       }
-      for (; j < cnt; ++j) f4add(acc, rb4[(int64_t)__shfl_sync(0xffffffffu, my_u, j) * 32 + lane]);
+      for (; j < cnt; ++j) {
+        const float4 v = rb4[(int64_t)__shfl_sync(0xffffffffu, my_u, j) * 32 + lane];
+        if (MODE == kPoolWeighted) f4fma(acc, __shfl_sync(0xffffffffu, my_w, j), v);
+        else f4add(acc, v);
+      }
     }
+    pool_mean<MODE>(acc, l1 - l0);
     out[b * 32 + lane] = acc;
   }
 }
@@ -702,9 +747,7 @@ static void launch_tiled(const FwdArgs& fa, cudaStream_t st) {
   TT_TIMED("k_fwd_tiled", st, (k_fwd_tiled<N2, R, CP><<<grid, 256, T::SMEM, st>>>(fa)));
 }
 
-int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* const cores[3],
-                   const int64_t* offsets, int64_t nnz, int64_t num_bags, float* out,
-                   cudaStream_t st) {
+int launch_rows(const Shape& s, const WS& w, const float* const cores[3], cudaStream_t st) {
   int CP = 0, CR = 0;
   int rc = forward_chunk_params(s, &CP, &CR);
   if (rc) return rc;
@@ -733,16 +776,41 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
       TT_TIMED("k_fwd_generic", st, (k_fwd_generic<<<grid, 256, smem, st>>>(fa)));
     }
   }
+  return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
+}
+
+template <int MODE>
+static void launch_pool_mode(const Shape& s, const Layout& L, const WS& w, const int64_t* offsets,
+                             int64_t nnz, int64_t num_bags, const float* psw, float* out,
+                             cudaStream_t st) {
+  int grid = (int)ceil_div(num_bags, 8);
+  const int cap = sm_count() * 16;
+  if (grid > cap) grid = cap;
+  if (s.D == 128) {
+    TT_TIMED("k_pool", st, (k_pool128<MODE><<<grid, 256, 0, st>>>(
+                               offsets, num_bags, nnz, w.uid, psw,
+                               reinterpret_cast<const float4*>(w.rowbuf), (int32_t)L.rowbuf_rows,
+                               reinterpret_cast<float4*>(out))));
+  } else {
+    TT_TIMED("k_pool", st, (k_pool<MODE><<<grid, 256, 0, st>>>(offsets, num_bags, nnz, w.uid, psw,
+                                                                w.rowbuf, s.D, out)));
+  }
+}
+
+int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* const cores[3],
+                   const int64_t* offsets, int64_t nnz, int64_t num_bags, const Pooling& pool,
+                   float* out, cudaStream_t st) {
+  int rc = launch_rows(s, w, cores, st);
+  if (rc) return rc;
   if (num_bags > 0) {
-    int grid = (int)ceil_div(num_bags, 8);
-    const int cap = sm_count() * 16;
-    if (grid > cap) grid = cap;
-    if (s.D == 128) {
-      TT_TIMED("k_pool", st, (k_pool128<<<grid, 256, 0, st>>>(
-                                 offsets, num_bags, nnz, w.uid, reinterpret_cast<const float4*>(w.rowbuf),
-                                 (int32_t)L.rowbuf_rows, reinterpret_cast<float4*>(out))));
-    } else {
-      TT_TIMED("k_pool", st, (k_pool<<<grid, 256, 0, st>>>(offsets, num_bags, nnz, w.uid, w.rowbuf, s.D, out)));
+    switch (pool.mode) {
+      case kPoolWeighted:
+        launch_pool_mode<kPoolWeighted>(s, L, w, offsets, nnz, num_bags, pool.psw, out, st);
+        break;
+      case kPoolMean:
+        launch_pool_mode<kPoolMean>(s, L, w, offsets, nnz, num_bags, nullptr, out, st);
+        break;
+      default: launch_pool_mode<kPoolSum>(s, L, w, offsets, nnz, num_bags, nullptr, out, st);
     }
   }
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;

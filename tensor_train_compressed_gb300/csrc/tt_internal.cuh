@@ -169,6 +169,23 @@ __device__ __forceinline__ void f4add(float4& a, const float4& b) {
   a.w += b.w;
 }
 
+// a += c * b, component-wise
+__device__ __forceinline__ void f4fma(float4& a, float c, const float4& b) {
+  a.x = fmaf(c, b.x, a.x);
+  a.y = fmaf(c, b.y, a.y);
+  a.z = fmaf(c, b.z, a.z);
+  a.w = fmaf(c, b.w, a.w);
+}
+
+// Pooling rule of a bag: the plain sum of its rows, the sum with each row
+// scaled by its lookup's per-sample weight, or the sum divided by the bag's
+// number of lookups.
+enum PoolMode { kPoolSum = 0, kPoolWeighted = 1, kPoolMean = 2 };
+struct Pooling {
+  int mode;            // PoolMode
+  const float* psw;    // [nnz] per-sample weights (kPoolWeighted), else null
+};
+
 // Grouping key of an in-range row index (r < M <= 2^32 - 2, so 32-bit
 // arithmetic is exact): (i2, i1, i3) with i3 least significant, so that unique
 // (i1, i2) prefixes come out grouped by the G2 slice they read.
@@ -292,15 +309,17 @@ int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratc
 int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                  int rows_per_chunk, cudaStream_t st);
-// forward (tt_fwd.cu)
+// forward (tt_fwd.cu): the unique rows into the row buffer, then the pooling
+int launch_rows(const Shape& s, const WS& w, const float* const cores[3], cudaStream_t st);
 int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* const cores[3],
-                   const int64_t* offsets, int64_t nnz, int64_t num_bags, float* out,
-                   cudaStream_t st);
+                   const int64_t* offsets, int64_t nnz, int64_t num_bags, const Pooling& pool,
+                   float* out, cudaStream_t st);
 int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chunk);
 // backward (tt_bwd.cu)
 int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out, int reuse,
                     const float* const cores[3], const int64_t* offsets, int64_t nnz,
-                    int64_t num_bags, float* const core_grads[3], cudaStream_t st);
+                    int64_t num_bags, const Pooling& pool, float* const core_grads[3],
+                    float* grad_weights, cudaStream_t st);
 int launch_split(const Shape& s, const WS& w, const float* const cores[3], int reuse, cudaStream_t st);
 // Called by one thread of a kernel that runs after k_split_cores in the same
 // stream: the split planes now hold the cores at g1, g2, g3.

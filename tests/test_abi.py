@@ -94,6 +94,29 @@ def test_forward_host_side_argument_checks(L):
     assert rc == tte.TT_EMB_ERR_ARG
 
 
+def test_pooling_variant_argument_checks(L):
+    """Weights go with the sum only; the weight gradient needs weights; unknown rules fail."""
+    m, n, R = (10, 10, 10), (2, 4, 2), (1, 4, 4, 1)
+    fake = 1 << 20
+    cores = (ctypes.c_void_p * 3)(fake, fake, fake)
+    P = ctypes.c_void_p
+    need = tte.tt_emb_workspace_bytes(m, n, R, 100, 10)
+    fwd = lambda psw, pooling, ws=need: L.tt_emb_forward_ex(
+        cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, psw, pooling, P(fake), P(fake), ws,
+        None)
+    assert fwd(P(fake), tte.TT_EMB_POOL_MEAN) == tte.TT_EMB_ERR_ARG     # weights with the mean
+    assert fwd(None, 7) == tte.TT_EMB_ERR_ARG                           # unknown pooling
+    assert fwd(P(fake + 2), tte.TT_EMB_POOL_SUM) == tte.TT_EMB_ERR_ARG  # misaligned weights
+    assert fwd(None, tte.TT_EMB_POOL_MEAN, need - 1) == tte.TT_EMB_ERR_WORKSPACE
+    bwd = lambda psw, pooling, gw: L.tt_emb_backward_ex(
+        P(fake), cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, psw, pooling, cores, gw,
+        P(fake), need - 1, 1, None)
+    assert bwd(None, tte.TT_EMB_POOL_SUM, P(fake)) == tte.TT_EMB_ERR_ARG   # no weights
+    assert bwd(P(fake), tte.TT_EMB_POOL_MEAN, None) == tte.TT_EMB_ERR_ARG
+    assert bwd(P(fake), tte.TT_EMB_POOL_SUM, P(fake + 1)) == tte.TT_EMB_ERR_ARG
+    assert bwd(P(fake), tte.TT_EMB_POOL_SUM, P(fake)) == tte.TT_EMB_ERR_WORKSPACE
+
+
 def test_product_path_has_no_oracle_dependency():
     """The package never imports the oracle."""
     pkg = os.path.join(ROOT, "tensor_train_compressed_gb300")
