@@ -17,20 +17,28 @@
 #include "tt_internal.cuh"
 #include "tt_tile.cuh"
 #include "tt_mma.cuh"
+#include "tt_split.cuh"
 
 namespace tt {
 
-// Zero the S rows that more than one gather slice will add into, write the bag
-// of every lookup (CSR offsets, clamped so that bad offsets stay in bounds) and
-// reset the backward chunk counter.  One thread per unique row (coalesced row
-// starts; a crossing row, one per slice boundary at most, is zeroed by its
-// thread) and one thread per bag (its lookups written in a loop).
+// Preparation of the backward, one launch:
+//  - zero the S rows that more than one gather slice will add into (one thread
+//    per unique row; a crossing row, one per slice boundary at most, is zeroed
+//    by its thread),
+//  - write the bag of every lookup (CSR offsets, clamped so that bad offsets
+//    stay in bounds): one warp per 32 bags, whose lanes read the 32 bags'
+//    bounds and then write each bag's lookups with consecutive lanes,
+//  - reset the backward chunk counter,
+//  - split the cores into their bf16 planes unless they already hold them
+//    (tensor-core shapes; sp.g2l is null otherwise).
 __global__ void __launch_bounds__(256) k_s_zero(WS w, int D, const int64_t* __restrict__ offsets,
-                                                int64_t B, int64_t nnz, int span) {
+                                                int64_t B, int64_t nnz, int span, SplitArgs sp,
+                                                int reuse) {
   if (blockIdx.x == 0 && threadIdx.x == 0) w.ctl->bwd_chunk_ctr = 0;
   const int64_t U = w.ctl->U_r;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < U; u += stride) {
+  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t u = gtid; u < U; u += stride) {
     const int32_t s0 = w.row_start[u], s1 = w.row_start[u + 1];
     if (s0 / span != (s1 - 1) / span) {
       float* r = w.rowbuf + u * (int64_t)D;
@@ -41,12 +49,23 @@ __global__ void __launch_bounds__(256) k_s_zero(WS w, int D, const int64_t* __re
       }
     }
   }
-  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < B; b += stride) {
-    int64_t l0 = offsets[b], l1 = offsets[b + 1];
-    l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
-    l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
-    for (int64_t l = l0; l < l1; ++l) w.bag_of[l] = (int32_t)b;
+  const int lane = threadIdx.x & 31;
+  for (int64_t b0 = (gtid >> 5) << 5; b0 < B; b0 += stride) {
+    const int64_t b = b0 + lane;
+    int64_t l0 = 0, l1 = 0;
+    if (b < B) {
+      l0 = offsets[b];
+      l1 = offsets[b + 1];
+      l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
+      l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
+    }
+    const int nb = B - b0 < 32 ? (int)(B - b0) : 32;
+    for (int k = 0; k < nb; ++k) {
+      const int64_t s0 = __shfl_sync(0xffffffffu, l0, k), s1 = __shfl_sync(0xffffffffu, l1, k);
+      for (int64_t l = s0 + lane; l < s1; l += 32) w.bag_of[l] = (int32_t)(b0 + k);
+    }
   }
+  if (sp.g2l && !(reuse && split_current(sp, w.ctl))) split_cores_body(sp);
 }
 
 __device__ __forceinline__ void s_flush(const WS& w, int32_t u, int64_t k0, int c, int D,
@@ -1104,12 +1123,17 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
                                                                   w.rowbuf, s.D, grad_out,
                                                                   grad_weights)));
   }
-  int grid = (int)ceil_div(L.rowbuf_rows > num_bags ? L.rowbuf_rows : num_bags, 256);
+  // one thread per unique row, one warp per 32 bags, and the split's own grid
+  const SplitArgs sp = make_split_args(s, w, cores);
+  int64_t want = L.rowbuf_rows > num_bags ? L.rowbuf_rows : num_bags;
+  int grid = (int)ceil_div(want, 256);
   if (grid > sms * 8) grid = sms * 8;
+  if (grid < split_grid(sp)) grid = split_grid(sp);
   if (grid < 1) grid = 1;
   const bool cta_gather = s.D == 128;
   TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D, offsets, num_bags, nnz,
-                                                             cta_gather ? kSCta : kSSlice)));
+                                                             cta_gather ? kSCta : kSSlice, sp,
+                                                             reuse)));
   switch (pool.mode) {
     case kPoolWeighted:
       launch_s_gather<kPoolWeighted>(s, w, grad_out, nnz, num_bags, offsets, pool.psw, st);
@@ -1130,8 +1154,6 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   ba.dG2 = core_grads[1];
   ba.dG3 = core_grads[2];
   if (tc_shape(s)) {
-    const int rc = launch_split(s, w, cores, reuse, st);
-    if (rc) return rc;
     static int grid = 0;
     if (grid == 0) {
       cudaFuncSetAttribute(k_bwd_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, MmaBwd::SMEM);

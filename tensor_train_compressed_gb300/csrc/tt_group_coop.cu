@@ -10,9 +10,8 @@
 // preceding barrier made complete (no look-back chains):
 //
 //   phase 0    keys, offsets check, per-CTA digit counts of pass 0
-//   pass p     CTA prefix + digit totals from the counts, stable rank within
-//              the CTA, scatter; the counts of pass p+1 are accumulated per
-//              destination CTA as the items land
+//   pass p     stable rank within the CTA and its digit counts | CTA prefix +
+//              digit totals from all CTAs' counts, scatter
 //   segment    run flags and per-CTA run counts | prefix, CSR arrays, uid
 //   chunks     chunk flags over the unique rows, per-CTA counts | prefix, chunks
 //
@@ -37,8 +36,7 @@ struct CoopArgs {
   int L;                  // sorted positions per CTA segment
   int CP, CR;             // chunking parameters
   WS w;
-  uint32_t* counts;       // [kMaxPasses][kRadix][Gp] per-CTA digit counts, Gp = G rounded to 4
-  int Gp;
+  uint32_t* counts;       // [kMaxPasses][G][kRadix / 2] per-CTA digit counts, two uint16 a word
   int4* seg_counts;       // [G] (rows, prefixes, valid lookups, 0) per CTA
   int* chunk_counts;      // [G] chunk starts per CTA
   uint32_t* bar;          // grid barrier words (zeroed before the launch)
@@ -144,7 +142,7 @@ __device__ __forceinline__ uint4 coop_sum4(uint4 v, uint4* sm) {
 template <int ITEMS>
 __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
   __shared__ uint32_t whist[kCoopWarps][kRadix];   // per-warp digit counts, then offsets
-  __shared__ uint32_t red[4][kRadix];              // partial (pre, tot) of the two halves
+  __shared__ __align__(16) uint32_t red[kCoopWarps][kRadix];   // per-warp partial digit sums
   __shared__ uint32_t scan_sm[kCoopWarps];
   __shared__ int2 wcnt[kCoopWarps];                 // per-warp (rows, prefixes)
   __shared__ uint4 sum_sm[kCoopWarps];
@@ -165,13 +163,24 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
 
   // ------------------------------------------------------------------ phase 0
   {
+    // every load of the phase is issued before any arithmetic: the CTA's
+    // indices and the bounds of the bag this thread checks
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+      const int64_t i = seg0 + warp * kSpan + it * 32 + lane;
+      word[it] = i < seg1 ? (uint64_t)__ldg(a.indices + i) : 0ull;
+    }
+    const int64_t bt = (int64_t)c * kCoopThreads + tid;
+    int64_t o0 = 0, o1 = 0;
+    if (bt <= a.B) o0 = __ldg(a.offsets + bt);
+    if (bt < a.B) o1 = __ldg(a.offsets + bt + 1);
     bool bad = false;
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
       const int64_t i = seg0 + warp * kSpan + it * 32 + lane;
       uint64_t wv = ~0ull;
       if (i < seg1) {
-        const int64_t r = a.indices[i];
+        const int64_t r = (int64_t)word[it];
         uint32_t key = a.sentinel;
         if (r >= 0 && r < a.s.M) key = group_key(r, a.s);
         else bad = true;
@@ -181,17 +190,18 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     }
     if (bad) set_status(a.w.ctl, kStIndex);
     bool bad_off = false;
-    for (int64_t b = (int64_t)c * kCoopThreads + tid; b <= a.B; b += (int64_t)G * kCoopThreads) {
-      const int64_t v = a.offsets[b];
+    for (int64_t b = bt; b <= a.B; b += (int64_t)G * kCoopThreads) {
+      int64_t v = o0, v1 = o1;
+      if (b != bt) {                       // batches of more than G * 512 bags
+        v = a.offsets[b];
+        v1 = b < a.B ? a.offsets[b + 1] : 0;
+      }
       if (v < 0 || v > a.nnz) bad_off = true;
       if (b == 0 && v != 0) bad_off = true;
       if (b == a.B && v != a.nnz) bad_off = true;
-      if (b < a.B && a.offsets[b + 1] < v) bad_off = true;
+      if (b < a.B && v1 < v) bad_off = true;
     }
     if (bad_off) set_status(a.w.ctl, kStOffsets);
-    if (c == 0)   // the padding columns of the counts stay zero
-      for (int e = tid; e < a.passes * kRadix; e += kCoopThreads)
-        for (int cc = G; cc < a.Gp; ++cc) a.counts[(size_t)e * a.Gp + cc] = 0;
   }
 
   // ------------------------------------------------------------------ radix passes
@@ -228,41 +238,64 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       __syncwarp();
     }
     __syncthreads();
-    uint32_t* cnt = a.counts + (size_t)p * kRadix * a.Gp;
-    if (tid < kRadix) {
-      uint32_t n = 0;
+    // this CTA's digit counts (at most L <= 512 ITEMS < 2^16 each), one 512-byte row
+    uint32_t* cnt = a.counts + (size_t)p * G * (kRadix / 2);
+    if (tid < kRadix / 2) {
+      uint32_t n0 = 0, n1 = 0;
 #pragma unroll
-      for (int w = 0; w < kCoopWarps; ++w) n += whist[w][tid];
-      cnt[(size_t)tid * a.Gp + c] = n;
+      for (int w = 0; w < kCoopWarps; ++w) {
+        n0 += whist[w][2 * tid];
+        n1 += whist[w][2 * tid + 1];
+      }
+      cnt[(size_t)c * (kRadix / 2) + tid] = n0 | (n1 << 16);
     }
     grid_barrier(a.bar, a.w.ctl);
     stamp();
-    // CTA prefix and total of every digit: two threads per digit, 128-bit loads
+    // CTA prefix and total of every digit from all CTAs' rows: warp w reads rows
+    // w, w + 16, ..., lane l the 16 bytes of digits 8 l .. 8 l + 7 (a warp load
+    // is one whole 512-byte row); the 16 warps' partial sums meet in shared memory
+    uint32_t my_pre = 0, my_tot = 0;
     {
-      const int d = tid & (kRadix - 1), h = tid >> 8;
-      const uint4* row = reinterpret_cast<const uint4*>(cnt + (size_t)d * a.Gp);
-      const int q4 = a.Gp / 4, q0 = h ? q4 / 2 : 0, q1 = h ? q4 : q4 / 2;
-      uint32_t pre = 0, tot = 0;
-#pragma unroll 8
-      for (int q = q0; q < q1; ++q) {
-        const uint4 v = __ldcg(row + q);
-        const int cc = 4 * q;
-        tot += v.x + v.y + v.z + v.w;
-        pre += (cc < c ? v.x : 0u) + (cc + 1 < c ? v.y : 0u) + (cc + 2 < c ? v.z : 0u) +
-               (cc + 3 < c ? v.w : 0u);
+      uint32_t pre[8], tot[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pre[k] = tot[k] = 0u;
+      const uint4* rows = reinterpret_cast<const uint4*>(cnt);
+#pragma unroll 5
+      for (int cc = warp; cc < G; cc += kCoopWarps) {
+        const uint4 v = __ldcg(rows + (size_t)cc * (kRadix / 8) + lane);
+        const bool before = cc < c;
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t lo = wv[j] & 0xffffu, hi = wv[j] >> 16;
+          tot[2 * j] += lo;
+          tot[2 * j + 1] += hi;
+          pre[2 * j] += before ? lo : 0u;
+          pre[2 * j + 1] += before ? hi : 0u;
+        }
       }
-      red[2 * h][d] = pre;
-      red[2 * h + 1][d] = tot;
+      uint4* mine = reinterpret_cast<uint4*>(&red[warp][8 * lane]);
+      mine[0] = make_uint4(pre[0], pre[1], pre[2], pre[3]);
+      mine[1] = make_uint4(pre[4], pre[5], pre[6], pre[7]);
+      __syncthreads();
+      if (tid < kRadix)
+#pragma unroll
+        for (int w = 0; w < kCoopWarps; ++w) my_pre += red[w][tid];
+      __syncthreads();
+      mine[0] = make_uint4(tot[0], tot[1], tot[2], tot[3]);
+      mine[1] = make_uint4(tot[4], tot[5], tot[6], tot[7]);
+      __syncthreads();
+      if (tid < kRadix)
+#pragma unroll
+        for (int w = 0; w < kCoopWarps; ++w) my_tot += red[w][tid];
     }
-    __syncthreads();
     // absolute start of every (warp, digit): bucket base + CTA prefix + warp prefix
     {
-      const uint32_t tot_d = tid < kRadix ? red[1][tid] + red[3][tid] : 0u;
       uint32_t all;
-      const uint32_t bucket = coop_scan(tot_d, &all, scan_sm);
+      const uint32_t bucket = coop_scan(tid < kRadix ? my_tot : 0u, &all, scan_sm);
       if (tid < kRadix) {
         const int d = tid;
-        uint32_t run = bucket + red[0][d] + red[2][d];
+        uint32_t run = bucket + my_pre;
 #pragma unroll
         for (int w = 0; w < kCoopWarps; ++w) {
           const uint32_t n = whist[w][d];
@@ -293,13 +326,26 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
   uint32_t rbits[ITEMS], pbits[ITEMS];
   {
     uint32_t wr = 0, wp = 0, wv_cnt = 0;
+    // one load per position; the word before a position comes from the lane
+    // before, from lane 31 of the item before, or (first position of the warp)
+    // from one more load
+    const int64_t wbase = seg0 + warp * kSpan;
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
-      const int64_t i = seg0 + warp * kSpan + it * 32 + lane;
+      const int64_t i = wbase + it * 32 + lane;
+      word[it] = i < seg1 ? __ldcg(sorted + i) : ~0ull;
+    }
+    const uint64_t before_warp = (wbase > 0 && wbase < seg1) ? __ldcg(sorted + wbase - 1) : ~0ull;
+    uint64_t carry = before_warp;          // the word before this item's lane 0
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+      const int64_t i = wbase + it * 32 + lane;
       const bool live = i < seg1;
-      const uint64_t wv = live ? __ldcg(sorted + i) : ~0ull;
-      const uint64_t pv = (live && i > 0) ? __ldcg(sorted + i - 1) : ~0ull;
-      word[it] = wv;
+      const uint64_t wv = word[it];
+      const uint64_t up = __shfl_up_sync(0xffffffffu, wv, 1);
+      uint64_t pv = lane > 0 ? up : carry;
+      carry = __shfl_sync(0xffffffffu, wv, 31);
+      if (!live || i == 0) pv = ~0ull;
       const uint64_t key = wv >> 32, pk = pv >> 32;
       const bool valid = live && key < M;
       const bool rf = valid && (i == 0 || key != pk);
@@ -317,6 +363,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
   }
   grid_barrier(a.bar, a.w.ctl);
   stamp();
+  int u_rows = 0, u_pairs = 0;   // unique rows and prefixes (every CTA has the totals)
   {
     uint4 mine_pre = make_uint4(0, 0, 0, 0), mine_tot = make_uint4(0, 0, 0, 0);
     for (int cc = tid; cc < G; cc += kCoopThreads) {
@@ -332,6 +379,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     const uint4 pre = coop_sum4(mine_pre, sum_sm);
     const uint4 tot = coop_sum4(mine_tot, sum_sm);
     const int64_t nv = (int64_t)tot.z;     // valid lookups (they sort first)
+    u_rows = (int)tot.x;
+    u_pairs = (int)tot.y;
     if (c == 0 && tid == 0) {
       a.w.ctl->n_valid = (int32_t)nv;
       a.w.ctl->U_r = (int32_t)tot.x;
@@ -384,36 +433,44 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
   stamp();
 
   // ------------------------------------------------------------------ chunks
+  // Chunk starts, enumerated per unique prefix p (rows f0 .. f1-1 of the
+  // prefix, nr = f1 - f0): its first row f0 starts a chunk when p is 0 or a
+  // multiple of CP, its i2 differs from prefix p-1's, or p or p-1 holds more
+  // than CR rows; rows f0 + k CR (k >= 1) start the CR-row pieces of a hot
+  // prefix.  Each thread owns Pt consecutive prefixes of the CTA's range and
+  // issues all their loads at once.
   {
-    const int U = __ldcg(&a.w.ctl->U_r);
-    const int Lr = (U + G - 1) / G;
-    const int x0 = c * Lr, x1 = min(x0 + Lr, U);
-    // each thread owns Rt consecutive rows of the CTA's range (Lr <= L <= 512 * ITEMS)
-    const int Rt = (Lr + kCoopThreads - 1) / kCoopThreads;
-    const int xt = x0 + tid * Rt;
-    uint32_t fl = 0, mine = 0;
+    const int U = u_rows, P = u_pairs;
+    const int Lp = (P + G - 1) / G;
+    const int y0 = c * Lp, y1 = min(y0 + Lp, P);
+    const int Pt = (Lp + kCoopThreads - 1) / kCoopThreads;   // <= ITEMS (P <= nnz)
+    const int yt = y0 + tid * Pt;
+    int f0s[ITEMS], nrs[ITEMS];
+    uint32_t firsts = 0, mine = 0;
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
-      const int x = xt + k;
-      bool f = false;
-      if (k < Rt && x < x1) {
-        const int32_t p = __ldcg(a.w.row_pair + x);
-        const int32_t f0 = __ldcg(a.w.pair_row_start + p);
-        const int32_t nr = __ldcg(a.w.pair_row_start + p + 1) - f0;
-        const int32_t pf = p > 0 ? __ldcg(a.w.pair_row_start + p - 1) : 0;
-        const int32_t i2 = __ldcg(a.w.pair_i2 + p);
-        const int32_t i2p = p > 0 ? __ldcg(a.w.pair_i2 + p - 1) : -1;
-        if (x != f0) f = ((x - f0) % a.CR) == 0;
-        else f = p == 0 || (p % a.CP) == 0 || i2 != i2p || nr > a.CR || (f0 - pf) > a.CR;
+      const int pp = yt + k;
+      f0s[k] = 0;
+      nrs[k] = 0;
+      if (k < Pt && pp < y1) {
+        const int32_t f0 = __ldcg(a.w.pair_row_start + pp);
+        const int32_t f1 = __ldcg(a.w.pair_row_start + pp + 1);
+        const int32_t pf = pp > 0 ? __ldcg(a.w.pair_row_start + pp - 1) : 0;
+        const int32_t i2 = __ldcg(a.w.pair_i2 + pp);
+        const int32_t i2p = pp > 0 ? __ldcg(a.w.pair_i2 + pp - 1) : -1;
+        const int32_t nr = f1 - f0;
+        const bool f = pp == 0 || (pp % a.CP) == 0 || i2 != i2p || nr > a.CR || (f0 - pf) > a.CR;
+        f0s[k] = f0;
+        nrs[k] = nr;
+        firsts |= (f ? 1u : 0u) << k;
+        mine += (f ? 1u : 0u) + (uint32_t)((nr - 1) / a.CR);
       }
-      fl |= (f ? 1u : 0u) << k;
     }
-    mine = __popc(fl);
     uint32_t tot;
     const uint32_t ex = coop_scan(mine, &tot, scan_sm);
     if (tid == 0) a.chunk_counts[c] = (int)tot;
     grid_barrier(a.bar, a.w.ctl);
-  stamp();
+    stamp();
     uint4 pr = make_uint4(0, 0, 0, 0);
     for (int cc = tid; cc < G; cc += kCoopThreads) {
       const uint32_t v = (uint32_t)__ldcg(a.chunk_counts + cc);
@@ -424,13 +481,18 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     int ci = (int)(ps.x + ex);
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
-      if ((fl >> k) & 1u) {
-        const int x = xt + k;
-        const int32_t p = __ldcg(a.w.row_pair + x);
-        const bool first = __ldcg(a.w.pair_row_start + p) == x;
-        a.w.chunk_start[ci] = x;
-        a.w.chunk_desc[ci] = make_int2(x, p | (first ? (int32_t)0x80000000 : 0));
-        ++ci;
+      const int pp = yt + k;
+      if (k < Pt && pp < y1) {
+        if ((firsts >> k) & 1u) {
+          a.w.chunk_start[ci] = f0s[k];
+          a.w.chunk_desc[ci] = make_int2(f0s[k], pp | (int32_t)0x80000000);
+          ++ci;
+        }
+        for (int x = f0s[k] + a.CR; x < f0s[k] + nrs[k]; x += a.CR) {
+          a.w.chunk_start[ci] = x;
+          a.w.chunk_desc[ci] = make_int2(x, pp);
+          ++ci;
+        }
       }
     }
     stamp();
@@ -438,7 +500,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
       const int n = (int)ps.y;
       a.w.ctl->n_chunks = n;
       a.w.chunk_start[n] = U;
-      a.w.chunk_desc[n] = make_int2(U, __ldcg(&a.w.ctl->U_12) | (int32_t)0x80000000);
+      a.w.chunk_desc[n] = make_int2(U, P | (int32_t)0x80000000);
     }
   }
 }
@@ -481,7 +543,7 @@ int coop_grid() {
 }
 
 size_t coop_scratch_bytes() {
-  return sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * kRadix + sizeof(int4) * kCoopMaxGrid +
+  return sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * (kRadix / 2) + sizeof(int4) * kCoopMaxGrid +
          sizeof(int) * kCoopMaxGrid + 16 * sizeof(unsigned long long);
 }
 
@@ -509,12 +571,11 @@ int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratc
   ca.CR = rows_per_chunk;
   ca.w = w;
   char* sc = static_cast<char*>(scratch);
-  ca.Gp = (G + 3) & ~3;
   // barrier words: the digit-histogram area, zeroed by the grouping's memset and
   // otherwise unused on this path (18 words 128 bytes apart = 2.3 KB)
   ca.bar = w.hist;
   ca.counts = reinterpret_cast<uint32_t*>(sc);
-  ca.seg_counts = reinterpret_cast<int4*>(sc + sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * kRadix);
+  ca.seg_counts = reinterpret_cast<int4*>(sc + sizeof(uint32_t) * kMaxPasses * kCoopMaxGrid * (kRadix / 2));
   ca.chunk_counts = reinterpret_cast<int*>(reinterpret_cast<char*>(ca.seg_counts) +
                                            sizeof(int4) * kCoopMaxGrid);
   ca.trace = reinterpret_cast<unsigned long long*>(ca.chunk_counts + kCoopMaxGrid);
