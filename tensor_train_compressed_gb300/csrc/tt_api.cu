@@ -208,8 +208,10 @@ int tt_emb_group(const int64_t m[3], const int32_t n[3], const int32_t R[4], con
   int CP, CR;
   rc = forward_chunk_params(s, &CP, &CR);
   if (rc) return rc;
-  return launch_group(s, L, make_ws(workspace, L), indices, nnz, offsets, num_bags, CP, CR,
-                      (cudaStream_t)stream);
+  const WS w = make_ws(workspace, L);
+  rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, (cudaStream_t)stream);
+  if (rc) return rc;
+  return launch_bag_ids(w, offsets, num_bags, nnz, (cudaStream_t)stream);
 }
 
 int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int32_t n[3],
@@ -280,6 +282,8 @@ int tt_emb_backward_ex(const float* grad_out, const float* const cores[3], const
     rc = forward_chunk_params(s, &CP, &CR);
     if (rc) return rc;
     rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, st);
+    if (rc) return rc;
+    rc = launch_bag_ids(w, offsets, num_bags, nnz, st);
     if (rc) return rc;
   }
   return launch_backward(s, L, w, grad_out, reuse_grouping ? 1 : 0, cores, offsets, nnz, num_bags,

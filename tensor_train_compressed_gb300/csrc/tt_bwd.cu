@@ -21,25 +21,31 @@
 
 namespace tt {
 
-// Preparation of the backward, one launch:
+// Preparation of the backward, one launch of one wave:
 //  - zero the S rows that more than one gather slice will add into (one thread
 //    per unique row; a crossing row, one per slice boundary at most, is zeroed
 //    by its thread),
-//  - write the bag of every lookup (CSR offsets, clamped so that bad offsets
-//    stay in bounds): one warp per 32 bags, whose lanes read the 32 bags'
-//    bounds and then write each bag's lookups with consecutive lanes,
 //  - reset the backward chunk counter,
 //  - split the cores into their bf16 planes unless they already hold them
 //    (tensor-core shapes; sp.g2l is null otherwise).
-__global__ void __launch_bounds__(256) k_s_zero(WS w, int D, const int64_t* __restrict__ offsets,
-                                                int64_t B, int64_t nnz, int span, SplitArgs sp,
-                                                int reuse) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) w.ctl->bwd_chunk_ctr = 0;
-  const int64_t U = w.ctl->U_r;
+// (The bag of every lookup is written by the grouping.)
+__global__ void __launch_bounds__(256) k_s_zero(WS w, int D, int span, int64_t rows_cap,
+                                                SplitArgs sp, int reuse) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t U = w.ctl->U_r;
+  int32_t s0 = 0, s1 = 0;
+  if (gtid < rows_cap) {               // row_start holds rows_cap + 1 entries at least
+    s0 = w.row_start[gtid];
+    s1 = w.row_start[gtid + 1];
+  }
+  const bool need_split = sp.g2l && !(reuse && split_current(sp, w.ctl));
+  if (blockIdx.x == 0 && threadIdx.x == 0) w.ctl->bwd_chunk_ctr = 0;
   for (int64_t u = gtid; u < U; u += stride) {
-    const int32_t s0 = w.row_start[u], s1 = w.row_start[u + 1];
+    if (u != gtid) {
+      s0 = w.row_start[u];
+      s1 = w.row_start[u + 1];
+    }
     if (s0 / span != (s1 - 1) / span) {
       float* r = w.rowbuf + u * (int64_t)D;
       if ((D & 3) == 0) {
@@ -49,23 +55,7 @@ __global__ void __launch_bounds__(256) k_s_zero(WS w, int D, const int64_t* __re
       }
     }
   }
-  const int lane = threadIdx.x & 31;
-  for (int64_t b0 = (gtid >> 5) << 5; b0 < B; b0 += stride) {
-    const int64_t b = b0 + lane;
-    int64_t l0 = 0, l1 = 0;
-    if (b < B) {
-      l0 = offsets[b];
-      l1 = offsets[b + 1];
-      l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
-      l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
-    }
-    const int nb = B - b0 < 32 ? (int)(B - b0) : 32;
-    for (int k = 0; k < nb; ++k) {
-      const int64_t s0 = __shfl_sync(0xffffffffu, l0, k), s1 = __shfl_sync(0xffffffffu, l1, k);
-      for (int64_t l = s0 + lane; l < s1; l += 32) w.bag_of[l] = (int32_t)(b0 + k);
-    }
-  }
-  if (sp.g2l && !(reuse && split_current(sp, w.ctl))) split_cores_body(sp);
+  if (need_split) split_cores_body(sp);
 }
 
 __device__ __forceinline__ void s_flush(const WS& w, int32_t u, int64_t k0, int c, int D,
@@ -180,9 +170,7 @@ __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict_
 // the runs that start and end inside its range, and leaves its first and last
 // run in shared memory; one warp then merges those in position order and
 // stores each merged row, or adds it with float atomics (into a row zeroed by
-// k_s_zero) when the row also crosses the CTA's range.  D % 4 == 0.
-constexpr int kSCta = 8 * kSSlice;
-
+// k_s_zero) when the row also crosses the CTA's range.  D = 128.
 __device__ __forceinline__ void s_merge_flush(const WS& w, int32_t u, int64_t K0, const float4& m,
                                               int lane) {
   const int32_t s0 = w.row_start[u], s1 = w.row_start[u + 1];
@@ -193,10 +181,10 @@ __device__ __forceinline__ void s_merge_flush(const WS& w, int32_t u, int64_t K0
 
 // D = 128: every lane owns one float4 column of the rows.
 template <int MODE>
-__global__ void __launch_bounds__(256) k_s_gather_cta(WS w, const float* __restrict__ grad_out,
-                                                      int64_t B, const float* __restrict__ psw,
-                                                      const int64_t* __restrict__ offsets,
-                                                      int64_t nnz) {
+__global__ void __launch_bounds__(256, MODE == kPoolSum ? 4 : 3) k_s_gather_cta(WS w, const float* __restrict__ grad_out,
+                                                         int64_t B, const float* __restrict__ psw,
+                                                         const int64_t* __restrict__ offsets,
+                                                         int64_t nnz) {
   __shared__ float4 part[8][2][32];
   __shared__ int part_u[8][2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -222,17 +210,32 @@ __global__ void __launch_bounds__(256) k_s_gather_cta(WS w, const float* __restr
       reinterpret_cast<float4*>(w.rowbuf)[(int64_t)cur * 32 + lane] = acc;
     }
   };
-  for (int64_t kb = k0; kb < k1; kb += 32) {
-    const int cnt = (int)(k1 - kb < 32 ? k1 - kb : 32);
-    int32_t my_u = -1, my_b = 0;
-    float my_c = 1.f;
-    if (lane < cnt) {
-      const int32_t l = w.perm[kb + lane];
-      my_u = w.uid[l];
-      const int32_t bb = w.bag_of[l];
-      my_b = bb < 0 ? 0 : (bb >= B ? (int32_t)(B - 1) : bb);
-      my_c = lookup_factor<MODE>(psw, offsets, nnz, l, my_b);
+  // the (unique row, bag, factor) of both 32-position batches of the slice,
+  // loaded together: two dependent round trips for the whole slice
+  static_assert(kSSlice == 64, "two batches of 32 sorted positions per warp");
+  int32_t bu[2] = {-1, -1}, bbag[2] = {0, 0}, bl[2] = {-1, -1};
+  float bc[2] = {1.f, 1.f};
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (k0 + 32 * h + lane < k1) bl[h] = w.perm[k0 + 32 * h + lane];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (bl[h] >= 0) {
+      bu[h] = w.uid[bl[h]];
+      bbag[h] = w.bag_of[bl[h]];
     }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    bbag[h] = bbag[h] < 0 ? 0 : (bbag[h] >= B ? (int32_t)(B - 1) : bbag[h]);
+    if (bl[h] >= 0) bc[h] = lookup_factor<MODE>(psw, offsets, nnz, bl[h], bbag[h]);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int64_t kb = k0 + 32 * h;
+    if (kb >= k1) break;
+    const int cnt = (int)(k1 - kb < 32 ? k1 - kb : 32);
+    const int32_t my_u = bu[h], my_b = bbag[h];
+    const float my_c = bc[h];
     int j = 0;
     for (; j + 8 <= cnt; j += 8) {
       int32_t uj[8];
@@ -294,6 +297,29 @@ __global__ void __launch_bounds__(256) k_s_gather_cta(WS w, const float* __restr
       }
     if (mu >= 0) s_merge_flush(w, mu, K0, m, lane);
   }
+}
+
+// The bag of every lookup, one warp per 32 bags (the forward's pooling writes
+// the same array; this serves a grouping that no forward followed).
+__global__ void __launch_bounds__(256) k_bag_ids(int32_t* __restrict__ bag_of,
+                                                 const int64_t* __restrict__ offsets, int64_t B,
+                                                 int64_t nnz) {
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t wb = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); wb < B; wb += stride) {
+    const int64_t b = wb + lane;
+    const int64_t o0 = b < B ? offsets[b] : 0, o1 = b < B ? offsets[b + 1] : 0;
+    write_bag_ids(bag_of, wb, B, nnz, o0, o1, lane);
+  }
+}
+
+int launch_bag_ids(const WS& w, const int64_t* offsets, int64_t num_bags, int64_t nnz,
+                   cudaStream_t st) {
+  if (num_bags <= 0 || nnz <= 0) return TT_EMB_OK;
+  int grid = (int)ceil_div(num_bags, 256);
+  if (grid > sm_count() * 8) grid = sm_count() * 8;
+  TT_TIMED("k_bag_ids", st, (k_bag_ids<<<grid, 256, 0, st>>>(w.bag_of, offsets, num_bags, nnz)));
+  return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }
 
 // Gradient of the per-sample weights: dW[l] = <grad_out[bag(l)], row(r_l)>,
@@ -1091,10 +1117,25 @@ static int persistent_grid_bwd(const void* fn, int threads, size_t smem) {
 }
 
 template <int MODE>
-static void launch_s_gather(const Shape& s, const WS& w, const float* grad_out, int64_t nnz,
-                            int64_t num_bags, const int64_t* offsets, const float* psw,
-                            cudaStream_t st) {
-  if (s.D == 128) {
+static void launch_s_gather(const Shape& s, const Layout& L, const WS& w, const float* grad_out,
+                            int64_t nnz, int64_t num_bags, const int64_t* offsets, const float* psw,
+                            const SplitArgs& sp, int reuse, cudaStream_t st) {
+  const bool cta_gather = s.D == 128;
+  static int zero_wave = 0;
+  if (zero_wave == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_s_zero, 256, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    zero_wave = per_sm * sm_count();
+  }
+  const int64_t want = ceil_div(L.rowbuf_rows, 256);
+  int grid = want < zero_wave ? (int)want : zero_wave;
+  if (grid < split_grid(sp)) grid = split_grid(sp);
+  if (grid < 1) grid = 1;
+  TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D, cta_gather ? kSCta : kSSlice,
+                                                             L.rowbuf_rows, sp, reuse)));
+  if (cta_gather) {
     TT_TIMED("k_s_gather", st, (k_s_gather_cta<MODE><<<(int)ceil_div(nnz, kSCta), 256, 0, st>>>(
                                    w, grad_out, num_bags, psw, offsets, nnz)));
   } else {
@@ -1123,25 +1164,17 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
                                                                   w.rowbuf, s.D, grad_out,
                                                                   grad_weights)));
   }
-  // one thread per unique row, one warp per 32 bags, and the split's own grid
   const SplitArgs sp = make_split_args(s, w, cores);
-  int64_t want = L.rowbuf_rows > num_bags ? L.rowbuf_rows : num_bags;
-  int grid = (int)ceil_div(want, 256);
-  if (grid > sms * 8) grid = sms * 8;
-  if (grid < split_grid(sp)) grid = split_grid(sp);
-  if (grid < 1) grid = 1;
-  const bool cta_gather = s.D == 128;
-  TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D, offsets, num_bags, nnz,
-                                                             cta_gather ? kSCta : kSSlice, sp,
-                                                             reuse)));
   switch (pool.mode) {
     case kPoolWeighted:
-      launch_s_gather<kPoolWeighted>(s, w, grad_out, nnz, num_bags, offsets, pool.psw, st);
+      launch_s_gather<kPoolWeighted>(s, L, w, grad_out, nnz, num_bags, offsets, pool.psw, sp, reuse,
+                                     st);
       break;
     case kPoolMean:
-      launch_s_gather<kPoolMean>(s, w, grad_out, nnz, num_bags, offsets, nullptr, st);
+      launch_s_gather<kPoolMean>(s, L, w, grad_out, nnz, num_bags, offsets, nullptr, sp, reuse, st);
       break;
-    default: launch_s_gather<kPoolSum>(s, w, grad_out, nnz, num_bags, offsets, nullptr, st);
+    default:
+      launch_s_gather<kPoolSum>(s, L, w, grad_out, nnz, num_bags, offsets, nullptr, sp, reuse, st);
   }
 
   BwdArgs ba;

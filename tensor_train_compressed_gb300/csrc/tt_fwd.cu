@@ -554,6 +554,7 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
 // lane then sums its float4 column of those rows, 8 loads in flight.  MODE
 // (PoolMode): plain sum, sum with each row scaled by its lookup's per-sample
 // weight, or the sum divided by the bag's length (empty bags give zeros).
+// The bag of every lookup is written on the way (bag_of, for the backward).
 
 // The weight of lookup l (MODE kPoolWeighted), 0 for an out-of-range lookup.
 template <int MODE>
@@ -574,7 +575,7 @@ __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offset
                                               int64_t nnz, const int32_t* __restrict__ uid,
                                               const float* __restrict__ psw,
                                               const float* __restrict__ rowbuf, int D,
-                                              float* __restrict__ out) {
+                                              float* __restrict__ out, int32_t* __restrict__ bag_of) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -582,6 +583,7 @@ __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offset
     int64_t l0 = offsets[b], l1 = offsets[b + 1];
     l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
     l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
+    for (int64_t l = l0 + lane; l < l1; l += 32) bag_of[l] = (int32_t)b;
     if ((D & 3) == 0) {
       const int cols = D >> 2;
       const float4* rb4 = reinterpret_cast<const float4*>(rowbuf);
@@ -646,7 +648,8 @@ __global__ void __launch_bounds__(256) k_pool128(const int64_t* __restrict__ off
                                                  int64_t nnz, const int32_t* __restrict__ uid,
                                                  const float* __restrict__ psw,
                                                  const float4* __restrict__ rb4, int32_t zrow,
-                                                 float4* __restrict__ out) {
+                                                 float4* __restrict__ out,
+                                                 int32_t* __restrict__ bag_of) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < B; b += warps) {
@@ -657,6 +660,7 @@ __global__ void __launch_bounds__(256) k_pool128(const int64_t* __restrict__ off
     for (int64_t lb = l0; lb < l1; lb += 32) {
       const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
       int32_t my_u = lane < cnt ? uid[lb + lane] : zrow;
+      if (lane < cnt) bag_of[lb + lane] = (int32_t)b;
       float my_w = 0.f;
       if (MODE == kPoolWeighted) my_w = (lane < cnt && my_u >= 0) ? psw[lb + lane] : 0.f;
       my_u = my_u < 0 ? zrow : my_u;
@@ -790,10 +794,10 @@ static void launch_pool_mode(const Shape& s, const Layout& L, const WS& w, const
     TT_TIMED("k_pool", st, (k_pool128<MODE><<<grid, 256, 0, st>>>(
                                offsets, num_bags, nnz, w.uid, psw,
                                reinterpret_cast<const float4*>(w.rowbuf), (int32_t)L.rowbuf_rows,
-                               reinterpret_cast<float4*>(out))));
+                               reinterpret_cast<float4*>(out), w.bag_of)));
   } else {
     TT_TIMED("k_pool", st, (k_pool<MODE><<<grid, 256, 0, st>>>(offsets, num_bags, nnz, w.uid, psw,
-                                                                w.rowbuf, s.D, out)));
+                                                                w.rowbuf, s.D, out, w.bag_of)));
   }
 }
 

@@ -24,6 +24,7 @@ constexpr int kScanThreads = 256;
 constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;
 constexpr int kSSlice = 64;                 // sorted positions per warp in the grad gather
+constexpr int kSCta = 8 * kSSlice;          // sorted positions per CTA in the D = 128 grad gather
 constexpr int kMaxSmemFloats = 53248;       // 208 KB of shared memory per CTA
 
 // status word bits
@@ -177,6 +178,22 @@ __device__ __forceinline__ void f4fma(float4& a, float c, const float4& b) {
   a.w = fmaf(c, b.w, a.w);
 }
 
+// Bag ids of the lookups of the 32 consecutive bags wb .. wb+31 (whole warp,
+// warp-uniform wb; lane k holds bag wb+k's bounds o0 = offsets[wb+k],
+// o1 = offsets[wb+k+1]): bag_of[l] = bag for every lookup l of each bag,
+// consecutive lanes writing consecutive lookups.  Bounds are clamped to
+// [0, nnz] so that bad offsets stay in bounds.
+__device__ __forceinline__ void write_bag_ids(int32_t* bag_of, int64_t wb, int64_t B, int64_t nnz,
+                                              int64_t o0, int64_t o1, int lane) {
+  const int64_t l0 = o0 < 0 ? 0 : (o0 > nnz ? nnz : o0);
+  const int64_t l1 = o1 < l0 ? l0 : (o1 > nnz ? nnz : o1);
+  const int nb = B - wb < 32 ? (int)(B - wb) : 32;
+  for (int k = 0; k < nb; ++k) {
+    const int64_t t0 = __shfl_sync(0xffffffffu, l0, k), t1 = __shfl_sync(0xffffffffu, l1, k);
+    for (int64_t l = t0 + lane; l < t1; l += 32) bag_of[l] = (int32_t)(wb + k);
+  }
+}
+
 // Pooling rule of a bag: the plain sum of its rows, the sum with each row
 // scaled by its lookup's per-sample weight, or the sum divided by the bag's
 // number of lookups.
@@ -309,6 +326,10 @@ int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratc
 int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                  int rows_per_chunk, cudaStream_t st);
+// bag of every lookup into the workspace (tt_bwd.cu); the forward's pooling
+// writes it too
+int launch_bag_ids(const WS& w, const int64_t* offsets, int64_t num_bags, int64_t nnz,
+                   cudaStream_t st);
 // forward (tt_fwd.cu): the unique rows into the row buffer, then the pooling
 int launch_rows(const Shape& s, const WS& w, const float* const cores[3], cudaStream_t st);
 int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* const cores[3],
