@@ -742,21 +742,22 @@ __device__ __forceinline__ void mma_bwd_dg3(const MmaBwd::Meta& m, uint32_t P2h,
     // B rows n = (row of pair, j3) = lr, k columns j12 = 16 ks + 8 ((lane >> 3) & 1)
     const int xr = (lr >> 2) == 0 ? r0 : (has2 ? r0 + 1 : C::RB);
     const uint32_t bb = Sh + xr * C::SROW + (lr & 3) * 80 + 16 * (li & 1);
-    float big[4] = {0.f, 0.f, 0.f, 0.f}, small[4] = {0.f, 0.f, 0.f, 0.f};
+    // hi.hi and the two small products in three accumulators (chains of two)
+    float big[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
       uint32_t bh[2], bl[2];
       ldsm_x2(bh, bb + 32 * ks);
       ldsm_x2(bl, bb + 32 * ks + C::SPLANE);
-      mma_bf16(small, al[ks], bh[0], bh[1]);
+      mma_bf16(sa, al[ks], bh[0], bh[1]);
+      mma_bf16(sb, ah[ks], bl[0], bl[1]);
       mma_bf16(big, ah[ks], bh[0], bh[1]);
-      mma_bf16(small, ah[ks], bl[0], bl[1]);
     }
     // C[r2][(row of pair, j3)]: this lane holds j3 = 2 (t % 2), +1 of row t / 2
     if (t < 2 || has2) {
       float* o = dG3 + (size_t)m.ri3[r0 + (t >> 1)] * (4 * C::R) + (16 * mt + g) * 4 + 2 * (t & 1);
-      red_add_f2(o, small[0] + big[0], small[1] + big[1]);
-      red_add_f2(o + 32, small[2] + big[2], small[3] + big[3]);
+      red_add_f2(o, (sa[0] + sb[0]) + big[0], (sa[1] + sb[1]) + big[1]);
+      red_add_f2(o + 32, (sa[2] + sb[2]) + big[2], (sa[3] + sb[3]) + big[3]);
     }
   }
 }
