@@ -252,19 +252,27 @@ class Workload:
         ws = tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.ws_bytes = ws
+        # the bf16 split of the cores is kept in the workspace: made here once
+        # (as when a model is loaded), then rewritten by every SGD step
+        tte.tt_emb_split(self.cores, x.m, x.n, x.R, self.ws)
 
     def step(self):
-        """forward, backward into the (zero) core gradients, SGD that also resets them"""
+        """forward on the kept split of the cores, backward into the (zero) core
+        gradients, SGD that also resets them and splits the updated cores"""
         t, x = self.tte, self.x
-        t.tt_emb_forward(self.cores, x.m, x.n, x.R, self.idx, self.off, self.out, self.ws)
+        t.tt_emb_forward_ex(self.cores, x.m, x.n, x.R, self.idx, self.off, None, "sum", self.out,
+                            self.ws, flags=t.TT_EMB_CORES_SPLIT)
         if self.train:
             t.tt_emb_backward(self.gout, self.cores, x.m, x.n, x.R, self.idx, self.off,
                               self.grads, self.ws, reuse_grouping=True)
-            t.tt_emb_sgd(self.cores, self.grads, x.m, x.n, x.R, LR, zero_grads=True)
+            t.tt_emb_sgd_ex(self.cores, self.grads, x.m, x.n, x.R, LR, True, self.ws)
 
     def restore(self):
+        """the cores of step 0 again, and their split (outside the timed region,
+        before the L2 flush: cores and planes start every step cold)"""
         for c, c0 in zip(self.cores, self.cores0):
             c.copy_(c0)
+        self.tte.tt_emb_split(self.cores, self.x.m, self.x.n, self.x.R, self.ws)
 
     def capture(self, profile: bool = False):
         torch = self.torch
@@ -289,8 +297,8 @@ def time_replays(torch, wl, graph, steps, flush, profile_n=0):
     times, per_kernel = [], {}
     for _ in range(steps):
         with torch.cuda.stream(s):
-            flush.zero_()
             wl.restore()
+            flush.zero_()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(s)
@@ -386,18 +394,19 @@ def run_ours(args, rank, world, dist):
     e2e_times = []
     for it in range(max(args.warmup, 3) + args.steps):
         with torch.cuda.stream(stream):
-            flush.zero_()
             wl.restore()
+            flush.zero_()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             idx_d.copy_(idx_h, non_blocking=True)
             off_d.copy_(off_h, non_blocking=True)
             g_d.copy_(g_h, non_blocking=True)
-            tte.tt_emb_forward(wl.cores, x.m, x.n, x.R, idx_d, off_d, wl.out, wl.ws)
+            tte.tt_emb_forward_ex(wl.cores, x.m, x.n, x.R, idx_d, off_d, None, "sum", wl.out,
+                                  wl.ws, flags=tte.TT_EMB_CORES_SPLIT)
             tte.tt_emb_backward(g_d, wl.cores, x.m, x.n, x.R, idx_d, off_d, wl.grads, wl.ws,
                                 reuse_grouping=True)
-            tte.tt_emb_sgd(wl.cores, wl.grads, x.m, x.n, x.R, LR, zero_grads=True)
+            tte.tt_emb_sgd_ex(wl.cores, wl.grads, x.m, x.n, x.R, LR, True, wl.ws)
             out_h.copy_(wl.out, non_blocking=True)
             e1.record(stream)
         stream.synchronize()
@@ -494,11 +503,13 @@ def run_ours(args, rank, world, dist):
         "config": {
             "workload": "training step: 47,952,000 rows = 360x360x370, D=128=4x8x4, "
                         "R1=R2=32, 32768 bags of U{10..30} Zipf(1.2) lookups, "
-                        "forward + backward + SGD(lr=0.01)",
+                        "forward + backward + SGD(lr=0.01) that also rewrites the kept "
+                        "bf16 split of the cores",
             "global_batch": 32768 * world, "lookups_per_gpu": nnz_tr,
             "unique_rows": at["U_r"], "unique_prefixes": at["U_12"],
             "parallelism": f"replicas x{world}",
-            "l2": "flushed between timed steps (512 MB write outside the timed events)",
+            "l2": "flushed between timed steps (512 MB write outside the timed events, "
+                  "after the cores and their split are restored)",
             "timing": "one CUDA graph replay per step, CUDA events on its stream",
         },
         "bags_per_s": round(32768 * world / (ms_train * 1e-3), 1),
@@ -506,7 +517,8 @@ def run_ours(args, rank, world, dist):
         "kernels_ms_per_step": kms_tr,
         "forward": {
             "workload": "12,000,000 rows = 200x240x250, D=128=4x8x4, R1=R2=32, 32768 bags x "
-                        "20 Zipf(1.2) lookups, forward only",
+                        "20 Zipf(1.2) lookups, forward only, on the bf16 split of the cores "
+                        "made once when they were loaded",
             "lookups_per_s": round(fw["wl"].x.nnz * world / (ms_fwd * 1e-3), 1),
             "bags_per_s": round(32768 * world / (ms_fwd * 1e-3), 1),
             "ms_per_call": round(ms_fwd, 5),
@@ -519,8 +531,9 @@ def run_ours(args, rank, world, dist):
         "e2e": {"value": round(nnz_tr * world / (ms_e2e * 1e-3), 1), "unit": "lookups/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 5),
-                "path": "pinned host indices/offsets/grad_out -> device, tt_emb_forward, "
-                        "tt_emb_backward, tt_emb_sgd, pooled output -> pinned host"},
+                "path": "pinned host indices/offsets/grad_out -> device, tt_emb_forward_ex "
+                        "(kept core split), tt_emb_backward, tt_emb_sgd_ex (SGD + split), "
+                        "pooled output -> pinned host"},
         "gpu_launches": tr["n_launch"] * args.steps,
         "clocks": tr["clocks"],
         "workspace_bytes": tr["wl"].ws_bytes,

@@ -93,6 +93,10 @@ int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_
 #define TT_EMB_POOL_SUM 0    /* out[b] = sum of the bag's rows (optionally weighted)   */
 #define TT_EMB_POOL_MEAN 1   /* out[b] = that sum / number of the bag's lookups        */
 
+/* Flags of tt_emb_forward_ex. */
+#define TT_EMB_CORES_SPLIT 1 /* the workspace already holds the bf16 split of these
+                                cores (see tt_emb_split): the forward skips the split */
+
 /* Forward with the other pooling rules of an embedding bag (the TT-Rec
  * abstract names its operator after the EmbeddingBag; the pages themselves
  * only sum).  Same arguments and contract as tt_emb_forward, plus:
@@ -102,11 +106,17 @@ int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_
  *  - pooling: TT_EMB_POOL_SUM, or TT_EMB_POOL_MEAN: every non-empty bag's sum
  *    is divided by its number of lookups (out-of-range lookups included in
  *    the count); empty bags give zeros.
- * tt_emb_forward is tt_emb_forward_ex(..., NULL, TT_EMB_POOL_SUM, ...). */
+ *  - flags: 0, or TT_EMB_CORES_SPLIT when the caller guarantees that the
+ *    workspace holds the bf16 split of exactly these core values, made by the
+ *    last tt_emb_split, tt_emb_sgd_ex or forward on this workspace with the
+ *    cores unchanged since (a serving loop with fixed cores; a training loop
+ *    that updates them with tt_emb_sgd_ex).  Other bits: TT_EMB_ERR_ARG.
+ * tt_emb_forward is tt_emb_forward_ex(..., NULL, TT_EMB_POOL_SUM, 0, ...). */
 int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int32_t n[3],
                       const int32_t R[4], const int64_t* indices, int64_t nnz,
                       const int64_t* offsets, int64_t num_bags, const float* per_sample_weights,
-                      int pooling, float* out, void* workspace, size_t ws_bytes, void* stream);
+                      int pooling, int flags, float* out, void* workspace, size_t ws_bytes,
+                      void* stream);
 
 /* Backward into the cores: core_grads[k] (same layout as cores[k]) are
  * ACCUMULATED (+=) with d<grad_out, out>/dG_k; the caller zeroes them.
@@ -141,6 +151,25 @@ int tt_emb_backward_ex(const float* grad_out, const float* const cores[3], const
  * dG_k to zero, ready for the next accumulating tt_emb_backward. */
 int tt_emb_sgd(float* const cores[3], float* const core_grads[3], const int64_t m[3],
                const int32_t n[3], const int32_t R[4], float lr, int zero_grads, void* stream);
+
+/* The bf16 split of the cores (hi = bf16(x), lo = bf16(x - hi), the operands
+ * of the three-term tensor-core products) into the workspace, where it stays
+ * until the cores are split again: later forwards on this workspace may pass
+ * TT_EMB_CORES_SPLIT while the core values do not change.  The planes sit at
+ * offsets that depend on the shape alone, so any workspace sized for this
+ * shape (any batch) holds them; a smaller one returns TT_EMB_ERR_WORKSPACE.
+ * Shapes without tensor-core kernels have no planes: the call does nothing.
+ * (The pages have no counterpart: the split is this implementation's operand
+ * format.) */
+int tt_emb_split(const float* const cores[3], const int64_t m[3], const int32_t n[3],
+                 const int32_t R[4], void* workspace, size_t ws_bytes, void* stream);
+
+/* tt_emb_sgd, and in the same pass the split of the updated cores into the
+ * workspace (as tt_emb_split would make it), so that the next forward may pass
+ * TT_EMB_CORES_SPLIT.  Workspace requirements as for tt_emb_split. */
+int tt_emb_sgd_ex(float* const cores[3], float* const core_grads[3], const int64_t m[3],
+                  const int32_t n[3], const int32_t R[4], float lr, int zero_grads,
+                  void* workspace, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, then reads the workspace status word written by the
  * kernels of the calls enqueued so far.  *device_status receives the raw

@@ -27,10 +27,11 @@ TT_EMB_ERR_UNSUPPORTED = -7
 _NAMES = {v: k for k, v in list(globals().items()) if k.startswith("TT_EMB_")}
 TT_EMB_POOL_SUM = 0
 TT_EMB_POOL_MEAN = 1
+TT_EMB_CORES_SPLIT = 1
 _POOLING = {"sum": TT_EMB_POOL_SUM, "mean": TT_EMB_POOL_MEAN}
 
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
-            "tt_emb_forward_ex", "tt_emb_backward_ex",
+            "tt_emb_forward_ex", "tt_emb_backward_ex", "tt_emb_split", "tt_emb_sgd_ex",
             "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_profile_start",
             "tt_emb_profile_stop", "tt_emb_profile_read", "tt_emb_forward_static",
             "tt_emb_version")
@@ -69,7 +70,10 @@ def lib():
         L.tt_emb_group.argtypes = [P, P, P, P, I64, P, I64, P, SZ, P]
         L.tt_emb_forward.argtypes = [P, P, P, P, P, I64, P, I64, P, P, SZ, P]
         L.tt_emb_backward.argtypes = [P, P, P, P, P, P, I64, P, I64, P, P, SZ, ctypes.c_int, P]
-        L.tt_emb_forward_ex.argtypes = [P, P, P, P, P, I64, P, I64, P, ctypes.c_int, P, P, SZ, P]
+        L.tt_emb_forward_ex.argtypes = [P, P, P, P, P, I64, P, I64, P, ctypes.c_int, ctypes.c_int,
+                                        P, P, SZ, P]
+        L.tt_emb_split.argtypes = [P, P, P, P, P, SZ, P]
+        L.tt_emb_sgd_ex.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, P, SZ, P]
         L.tt_emb_backward_ex.argtypes = [P, P, P, P, P, P, I64, P, I64, P, ctypes.c_int, P, P, P,
                                          SZ, ctypes.c_int, P]
         L.tt_emb_sgd.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, P]
@@ -157,14 +161,14 @@ def _opt(t, dtype, name):
 
 
 def tt_emb_forward_ex(cores, m, n, R, indices, offsets, per_sample_weights, pooling, out,
-                      workspace, stream=None):
+                      workspace, stream=None, flags: int = 0):
     """pooling: "sum" / "mean" (or the TT_EMB_POOL_* value); per_sample_weights: None or a
-    float32 CUDA tensor [nnz] (sum only)."""
+    float32 CUDA tensor [nnz] (sum only); flags: 0 or TT_EMB_CORES_SPLIT."""
     _check(lib().tt_emb_forward_ex(_ptrs3(cores, "cores"), *_shape(m, n, R),
                                    _dev(indices, torch.int64, "indices"), indices.numel(),
                                    _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
                                    _opt(per_sample_weights, torch.float32, "per_sample_weights"),
-                                   int(_POOLING.get(pooling, pooling)),
+                                   int(_POOLING.get(pooling, pooling)), int(flags),
                                    _dev(out, torch.float32, "out"),
                                    _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
                                    _stream(stream)), "tt_emb_forward_ex")
@@ -190,6 +194,19 @@ def tt_emb_sgd(cores, core_grads, m, n, R, lr: float, zero_grads: bool = False, 
     _check(lib().tt_emb_sgd(_ptrs3(cores, "cores"), _ptrs3(core_grads, "core_grads"),
                             *_shape(m, n, R), ctypes.c_float(lr), int(bool(zero_grads)),
                             _stream(stream)), "tt_emb_sgd")
+
+
+def tt_emb_split(cores, m, n, R, workspace, stream=None):
+    _check(lib().tt_emb_split(_ptrs3(cores, "cores"), *_shape(m, n, R),
+                              _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                              _stream(stream)), "tt_emb_split")
+
+
+def tt_emb_sgd_ex(cores, core_grads, m, n, R, lr: float, zero_grads: bool, workspace, stream=None):
+    _check(lib().tt_emb_sgd_ex(_ptrs3(cores, "cores"), _ptrs3(core_grads, "core_grads"),
+                               *_shape(m, n, R), ctypes.c_float(lr), int(bool(zero_grads)),
+                               _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                               _stream(stream)), "tt_emb_sgd_ex")
 
 
 def tt_emb_get_error(workspace, stream=None) -> tuple[int, int]:

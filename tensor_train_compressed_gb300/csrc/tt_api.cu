@@ -75,6 +75,21 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
   };
   L.ctl = take(sizeof(Ctl));
   L.hist = take(sizeof(uint32_t) * kHistCopies * kMaxPasses * kRadix);
+  L.zero_end = off;   // every grouping zeroes [ctl, zero_end)
+  // bf16 split planes of the cores, at offsets fixed by the shape: a split made
+  // by tt_emb_split or tt_emb_sgd_ex outlives the groupings of later batches
+  if (tc_shape(s)) {
+    const size_t n1 = (size_t)s.m1 * s.n1 * s.R1, n2 = (size_t)s.m2 * s.R1 * s.n2 * s.R2;
+    const size_t n3 = (size_t)s.m3 * s.R2 * s.n3;
+    L.g1h = take(2 * n1);
+    L.g1l = take(2 * n1);
+    L.g2h = take(2 * n2);
+    L.g2l = take(2 * n2);
+    L.g3h = take(2 * n3);
+    L.g3l = take(2 * n3);
+    L.g3th = take(2 * n3);
+    L.g3tl = take(2 * n3);
+  }
   L.sort_status = take(sizeof(uint32_t) * kMaxPasses * (size_t)L.n_sort_tiles * kRadix);
   L.keysA = take(sizeof(uint64_t) * (size_t)n);
   L.keysB = take(sizeof(uint64_t) * (size_t)n);
@@ -94,18 +109,6 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
   L.coop = take(coop_scratch_bytes());
   // one extra row, kept at zero, that out-of-range lookups point at while pooling
   L.rowbuf = take(sizeof(float) * ((size_t)L.rowbuf_rows + 1) * (size_t)s.D);
-  if (tc_shape(s)) {
-    const size_t n1 = (size_t)s.m1 * s.n1 * s.R1, n2 = (size_t)s.m2 * s.R1 * s.n2 * s.R2;
-    L.g1h = take(2 * n1);
-    L.g1l = take(2 * n1);
-    L.g2h = take(2 * n2);
-    L.g2l = take(2 * n2);
-    const size_t n3 = (size_t)s.m3 * s.R2 * s.n3;
-    L.g3h = take(2 * n3);
-    L.g3l = take(2 * n3);
-    L.g3th = take(2 * n3);
-    L.g3tl = take(2 * n3);
-  }
   L.total = off;
   return L;
 }
@@ -184,7 +187,7 @@ using namespace tt;
 
 extern "C" {
 
-int tt_emb_version(void) { return 200; }
+int tt_emb_version(void) { return 300; }
 
 int tt_emb_workspace_bytes(const int64_t m[3], const int32_t n[3], const int32_t R[4], int64_t nnz,
                            int64_t num_bags, size_t* bytes) {
@@ -217,12 +220,14 @@ int tt_emb_group(const int64_t m[3], const int32_t n[3], const int32_t R[4], con
 int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int32_t n[3],
                       const int32_t R[4], const int64_t* indices, int64_t nnz,
                       const int64_t* offsets, int64_t num_bags, const float* per_sample_weights,
-                      int pooling, float* out, void* workspace, size_t ws_bytes, void* stream) {
+                      int pooling, int flags, float* out, void* workspace, size_t ws_bytes,
+                      void* stream) {
   Shape s;
   int rc = shape_from_args(m, n, R, &s);
   if (rc) return rc;
   rc = check_cores(cores);
   if (rc) return rc;
+  if (flags & ~TT_EMB_CORES_SPLIT) return TT_EMB_ERR_ARG;
   Pooling pool;
   rc = check_pooling(per_sample_weights, pooling, &pool);
   if (rc) return rc;
@@ -243,7 +248,8 @@ int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int
       return TT_EMB_ERR_CUDA;
     return TT_EMB_OK;
   }
-  return launch_forward(s, L, w, cores, offsets, nnz, num_bags, pool, out, st);
+  return launch_forward(s, L, w, cores, offsets, nnz, num_bags, pool,
+                        (flags & TT_EMB_CORES_SPLIT) ? 1 : 0, out, st);
 }
 
 int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_t n[3],
@@ -251,7 +257,7 @@ int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_
                    const int64_t* offsets, int64_t num_bags, float* out, void* workspace,
                    size_t ws_bytes, void* stream) {
   return tt_emb_forward_ex(cores, m, n, R, indices, nnz, offsets, num_bags, nullptr,
-                           TT_EMB_POOL_SUM, out, workspace, ws_bytes, stream);
+                           TT_EMB_POOL_SUM, 0, out, workspace, ws_bytes, stream);
 }
 
 int tt_emb_backward_ex(const float* grad_out, const float* const cores[3], const int64_t m[3],
@@ -308,7 +314,46 @@ int tt_emb_sgd(float* const cores[3], float* const core_grads[3], const int64_t 
   if (rc) return rc;
   rc = check_cores(core_grads);
   if (rc) return rc;
-  return launch_sgd(cores, core_grads, s, lr, zero_grads, (cudaStream_t)stream);
+  return launch_sgd(cores, core_grads, s, lr, zero_grads, nullptr, (cudaStream_t)stream);
+}
+
+// The workspace part that holds the split planes (its offsets depend on the
+// shape alone): a workspace sized for any batch of this shape holds it.
+static int check_split_ws(const Shape& s, const void* workspace, size_t ws_bytes, Layout* L) {
+  if (!workspace || !aligned(workspace, 256)) return TT_EMB_ERR_ARG;
+  *L = make_layout(s, 0, 0);
+  if (ws_bytes < L->sort_status) return TT_EMB_ERR_WORKSPACE;
+  return TT_EMB_OK;
+}
+
+int tt_emb_split(const float* const cores[3], const int64_t m[3], const int32_t n[3],
+                 const int32_t R[4], void* workspace, size_t ws_bytes, void* stream) {
+  Shape s;
+  int rc = shape_from_args(m, n, R, &s);
+  if (rc) return rc;
+  rc = check_cores(cores);
+  if (rc) return rc;
+  Layout L;
+  rc = check_split_ws(s, workspace, ws_bytes, &L);
+  if (rc) return rc;
+  return launch_split(s, make_ws(workspace, L), cores, 0, (cudaStream_t)stream);
+}
+
+int tt_emb_sgd_ex(float* const cores[3], float* const core_grads[3], const int64_t m[3],
+                  const int32_t n[3], const int32_t R[4], float lr, int zero_grads,
+                  void* workspace, size_t ws_bytes, void* stream) {
+  Shape s;
+  int rc = shape_from_args(m, n, R, &s);
+  if (rc) return rc;
+  rc = check_cores(cores);
+  if (rc) return rc;
+  rc = check_cores(core_grads);
+  if (rc) return rc;
+  Layout L;
+  rc = check_split_ws(s, workspace, ws_bytes, &L);
+  if (rc) return rc;
+  const WS w = make_ws(workspace, L);
+  return launch_sgd(cores, core_grads, s, lr, zero_grads, &w, (cudaStream_t)stream);
 }
 
 int tt_emb_get_error(const void* workspace, void* stream, int* device_status) {

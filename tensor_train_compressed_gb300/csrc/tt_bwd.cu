@@ -1054,11 +1054,21 @@ struct SgdArgs {
   int64_t start[4];   // prefix of the float4 counts of the segments
   float lr;
   int zero;
+  // SPLIT: bf16 planes of the updated cores (tensor-core shape: every count is a
+  // multiple of 4 and a float4 of G3 is one (i3, r2) row of its n3 = 4 values)
+  uint2* hi[3];
+  uint2* lo[3];
+  uint16_t* g3th;
+  uint16_t* g3tl;
+  int R2;
 };
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(256) k_sgd(SgdArgs a) {
   // four float4 per thread and step, all loads issued before the stores (the
-  // cores and their gradients never alias); segment pointers chosen by selects
+  // cores and their gradients never alias); segment pointers chosen by selects.
+  // With SPLIT the updated values also go to the bf16 planes of the chunk
+  // kernels (the split of tt_split.cuh, element for element)
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   auto seg_g = [&](int k) { return k == 0 ? a.G[0] : (k == 1 ? a.G[1] : a.G[2]); };
   auto seg_d = [&](int k) { return k == 0 ? a.dG[0] : (k == 1 ? a.dG[1] : a.dG[2]); };
@@ -1099,6 +1109,26 @@ __global__ void __launch_bounds__(256) k_sgd(SgdArgs a) {
         v.w = fmaf(-a.lr, d[u].w, v.w);
         *reinterpret_cast<float4*>(G + e) = v;
         if (a.zero) *reinterpret_cast<float4*>(dG + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (SPLIT) {
+          uint32_t h0, l0, h1, l1;
+          split_bf16x2(v.x, v.y, h0, l0);
+          split_bf16x2(v.z, v.w, h1, l1);
+          const int64_t j = e >> 2;
+          (k == 0 ? a.hi[0] : (k == 1 ? a.hi[1] : a.hi[2]))[j] = make_uint2(h0, h1);
+          (k == 0 ? a.lo[0] : (k == 1 ? a.lo[1] : a.lo[2]))[j] = make_uint2(l0, l1);
+          if (k == 2) {   // row j = i3 R2 + r2 -> transposed (i3 n3 + j3) R2 + r2
+            const int64_t i3 = j / a.R2, r2 = j - i3 * a.R2;
+            const int64_t t0 = i3 * 4 * a.R2 + r2;
+            a.g3th[t0] = (uint16_t)(h0 & 0xffffu);
+            a.g3th[t0 + a.R2] = (uint16_t)(h0 >> 16);
+            a.g3th[t0 + 2 * a.R2] = (uint16_t)(h1 & 0xffffu);
+            a.g3th[t0 + 3 * a.R2] = (uint16_t)(h1 >> 16);
+            a.g3tl[t0] = (uint16_t)(l0 & 0xffffu);
+            a.g3tl[t0 + a.R2] = (uint16_t)(l0 >> 16);
+            a.g3tl[t0 + 2 * a.R2] = (uint16_t)(l1 & 0xffffu);
+            a.g3tl[t0 + 3 * a.R2] = (uint16_t)(l1 >> 16);
+          }
+        }
       } else {
         for (int64_t t = e; t < n; ++t) {
           G[t] = fmaf(-a.lr, dG[t], G[t]);
@@ -1157,7 +1187,7 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
     // product per lookup; the forward chunk counter is re-armed first
     if (cudaMemsetAsync(&w.ctl->fwd_chunk_ctr, 0, sizeof(uint32_t), st) != cudaSuccess)
       return TT_EMB_ERR_CUDA;
-    const int rc = launch_rows(s, w, cores, st);
+    const int rc = launch_rows(s, w, cores, 0, st);
     if (rc) return rc;
     int grid = (int)ceil_div(num_bags, 8);
     if (grid > sms * 16) grid = sms * 16;
@@ -1211,7 +1241,7 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
 }
 
 int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, float lr,
-               int zero_grads, cudaStream_t st) {
+               int zero_grads, const WS* ws, cudaStream_t st) {
   SgdArgs a;
   const int64_t counts[3] = {s.m1 * s.n1 * s.R1, s.m2 * s.R1 * s.n2 * s.R2, s.m3 * s.R2 * s.n3};
   a.start[0] = 0;
@@ -1223,10 +1253,24 @@ int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, flo
   }
   a.lr = lr;
   a.zero = zero_grads ? 1 : 0;
+  const bool split = ws && ws->g2l;
+  a.hi[0] = split ? reinterpret_cast<uint2*>(ws->g1h) : nullptr;
+  a.lo[0] = split ? reinterpret_cast<uint2*>(ws->g1l) : nullptr;
+  a.hi[1] = split ? reinterpret_cast<uint2*>(ws->g2h) : nullptr;
+  a.lo[1] = split ? reinterpret_cast<uint2*>(ws->g2l) : nullptr;
+  a.hi[2] = split ? reinterpret_cast<uint2*>(ws->g3h) : nullptr;
+  a.lo[2] = split ? reinterpret_cast<uint2*>(ws->g3l) : nullptr;
+  a.g3th = split ? ws->g3th : nullptr;
+  a.g3tl = split ? ws->g3tl : nullptr;
+  a.R2 = s.R2;
   int grid = (int)ceil_div(a.start[3], 4 * 256);
   if (grid > sm_count() * 4) grid = sm_count() * 4;
   if (grid < 1) grid = 1;
-  TT_TIMED("k_sgd", st, (k_sgd<<<grid, 256, 0, st>>>(a)));
+  if (split) {
+    TT_TIMED("k_sgd", st, (k_sgd<true><<<grid, 256, 0, st>>>(a)));
+  } else {
+    TT_TIMED("k_sgd", st, (k_sgd<false><<<grid, 256, 0, st>>>(a)));
+  }
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }
 

@@ -751,7 +751,8 @@ static void launch_tiled(const FwdArgs& fa, cudaStream_t st) {
   TT_TIMED("k_fwd_tiled", st, (k_fwd_tiled<N2, R, CP><<<grid, 256, T::SMEM, st>>>(fa)));
 }
 
-int launch_rows(const Shape& s, const WS& w, const float* const cores[3], cudaStream_t st) {
+int launch_rows(const Shape& s, const WS& w, const float* const cores[3], int presplit,
+                cudaStream_t st) {
   int CP = 0, CR = 0;
   int rc = forward_chunk_params(s, &CP, &CR);
   if (rc) return rc;
@@ -763,8 +764,10 @@ int launch_rows(const Shape& s, const WS& w, const float* const cores[3], cudaSt
   fa.G3 = cores[2];
   switch (fwd_kind(s)) {
     case kFwdTiled_8_32:
-      rc = launch_split(s, w, cores, 0, st);
-      if (rc) return rc;
+      if (!presplit) {
+        rc = launch_split(s, w, cores, 0, st);
+        if (rc) return rc;
+      }
       launch_fwd_mma<8>(fa, st);
       break;
     case kFwdTiled_8_64: launch_tiled<8, 64, kCP_8_64>(fa, st); break;
@@ -803,8 +806,8 @@ static void launch_pool_mode(const Shape& s, const Layout& L, const WS& w, const
 
 int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* const cores[3],
                    const int64_t* offsets, int64_t nnz, int64_t num_bags, const Pooling& pool,
-                   float* out, cudaStream_t st) {
-  int rc = launch_rows(s, w, cores, st);
+                   int presplit, float* out, cudaStream_t st) {
+  int rc = launch_rows(s, w, cores, presplit, st);
   if (rc) return rc;
   if (num_bags > 0) {
     switch (pool.mode) {

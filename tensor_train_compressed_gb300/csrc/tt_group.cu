@@ -380,7 +380,7 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                  int rows_per_chunk, cudaStream_t st) {
   // control block + digit histograms start from zero
-  if (cudaMemsetAsync(w.ctl, 0, L.sort_status - L.ctl, st) != cudaSuccess) return TT_EMB_ERR_CUDA;
+  if (cudaMemsetAsync(w.ctl, 0, L.zero_end - L.ctl, st) != cudaSuccess) return TT_EMB_ERR_CUDA;
   // the zero row after the unique rows (pooling points out-of-range lookups at it)
   if (cudaMemsetAsync(w.rowbuf + (size_t)L.rowbuf_rows * s.D, 0, sizeof(float) * (size_t)s.D, st) !=
       cudaSuccess)

@@ -90,10 +90,11 @@ struct Shape {
 
 // Workspace layout (byte offsets from the workspace base; 256-aligned).
 struct Layout {
-  size_t ctl, hist, sort_status, keysA, keysB, bag_of, uid, perm;
+  size_t ctl, hist, zero_end, sort_status, keysA, keysB, bag_of, uid, perm;
   size_t row_start, row_i3, row_pair, pair_row_start, pair_i1, pair_i2;
   size_t seg_status, chunk_start, chunk_desc, chunk_status, coop, rowbuf, total;
-  size_t g1h, g1l, g2h, g2l;   // bf16 split planes of G1 and G2 (tensor-core shape only)
+  size_t g1h, g1l, g2h, g2l;   // bf16 split planes of G1 and G2 (tensor-core shape only; their
+                               // offsets depend on the shape alone, not on the batch)
   size_t g3h, g3l, g3th, g3tl; // bf16 split planes of G3 [m3][R2][n3] and of its transpose [m3][n3][R2]
   int key_bits, passes, n_sort_tiles, n_scan_tiles;
   int64_t rowbuf_rows;
@@ -331,10 +332,12 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
 int launch_bag_ids(const WS& w, const int64_t* offsets, int64_t num_bags, int64_t nnz,
                    cudaStream_t st);
 // forward (tt_fwd.cu): the unique rows into the row buffer, then the pooling
-int launch_rows(const Shape& s, const WS& w, const float* const cores[3], cudaStream_t st);
+// presplit != 0: the workspace's split planes already hold these cores
+int launch_rows(const Shape& s, const WS& w, const float* const cores[3], int presplit,
+                cudaStream_t st);
 int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* const cores[3],
                    const int64_t* offsets, int64_t nnz, int64_t num_bags, const Pooling& pool,
-                   float* out, cudaStream_t st);
+                   int presplit, float* out, cudaStream_t st);
 int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chunk);
 // backward (tt_bwd.cu)
 int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out, int reuse,
@@ -350,7 +353,8 @@ __device__ __forceinline__ void mark_split(Ctl* ctl, const float* g1, const floa
   ctl->split_src[2] = (unsigned long long)g3;
   ctl->split_valid = 1;
 }
+// ws non-null: the updated cores are also split into the planes of that workspace
 int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, float lr,
-               int zero_grads, cudaStream_t st);
+               int zero_grads, const WS* ws, cudaStream_t st);
 
 }  // namespace tt

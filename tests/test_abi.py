@@ -101,13 +101,14 @@ def test_pooling_variant_argument_checks(L):
     cores = (ctypes.c_void_p * 3)(fake, fake, fake)
     P = ctypes.c_void_p
     need = tte.tt_emb_workspace_bytes(m, n, R, 100, 10)
-    fwd = lambda psw, pooling, ws=need: L.tt_emb_forward_ex(
-        cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, psw, pooling, P(fake), P(fake), ws,
-        None)
+    fwd = lambda psw, pooling, ws=need, flags=0: L.tt_emb_forward_ex(
+        cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, psw, pooling, flags, P(fake),
+        P(fake), ws, None)
     assert fwd(P(fake), tte.TT_EMB_POOL_MEAN) == tte.TT_EMB_ERR_ARG     # weights with the mean
     assert fwd(None, 7) == tte.TT_EMB_ERR_ARG                           # unknown pooling
     assert fwd(P(fake + 2), tte.TT_EMB_POOL_SUM) == tte.TT_EMB_ERR_ARG  # misaligned weights
     assert fwd(None, tte.TT_EMB_POOL_MEAN, need - 1) == tte.TT_EMB_ERR_WORKSPACE
+    assert fwd(None, tte.TT_EMB_POOL_SUM, need, 2) == tte.TT_EMB_ERR_ARG    # unknown flag
     bwd = lambda psw, pooling, gw: L.tt_emb_backward_ex(
         P(fake), cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, psw, pooling, cores, gw,
         P(fake), need - 1, 1, None)
@@ -125,3 +126,21 @@ def test_product_path_has_no_oracle_dependency():
             src = open(path).read()
             assert "import oracle" not in src and "from oracle" not in src, path
             assert "tt_oracle" not in src, path
+
+
+def test_split_and_fused_sgd_argument_checks(L):
+    """The planes' workspace part depends on the shape alone; too small or misaligned
+    workspaces are refused before any launch."""
+    m, n, R = (200, 240, 250), (4, 8, 4), (1, 32, 32, 1)
+    fake = 1 << 20
+    cores = (ctypes.c_void_p * 3)(fake, fake, fake)
+    P = ctypes.c_void_p
+    small = tte.tt_emb_workspace_bytes(m, n, R, 0, 0)
+    # any batch's workspace holds the planes
+    assert tte.tt_emb_workspace_bytes(m, n, R, 1000, 10) >= small
+    assert L.tt_emb_split(cores, *_shape(m, n, R), P(fake), 1024, None) == tte.TT_EMB_ERR_WORKSPACE
+    assert L.tt_emb_split(cores, *_shape(m, n, R), P(fake + 16), small, None) == tte.TT_EMB_ERR_ARG
+    assert L.tt_emb_sgd_ex(cores, cores, *_shape(m, n, R), ctypes.c_float(0.1), 0, P(fake), 1024,
+                           None) == tte.TT_EMB_ERR_WORKSPACE
+    assert L.tt_emb_sgd_ex(cores, None, *_shape(m, n, R), ctypes.c_float(0.1), 0, P(fake), small,
+                           None) == tte.TT_EMB_ERR_ARG
