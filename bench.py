@@ -36,7 +36,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "TT embedding-bag lookups/s at batch 32768 (fwd, fwd+bwd); % of roofline"
-TRAIN_CFG, FWD_CFG = 5, 3
+TRAIN_CFG, FWD_CFG, MULTI_CFG = 5, 3, 4
 LR = 0.01
 FLUSH_BYTES = 512 << 20
 
@@ -290,6 +290,49 @@ class Workload:
         return g["U_12"], g["U_r"], g["n_valid"], g["status"]
 
 
+class MultiTableWorkload(Workload):
+    """The eight-table forward workload: one forward call per table, all on one
+    stream in one captured graph, one workspace sized for the largest batch
+    (each call groups its own batch).  The R = 64 tables run the tiled FP32
+    chunk kernel (no tensor-core split)."""
+
+    def __init__(self, cfg: int, torch, tte, stream):
+        from tensor_train_compressed_gb300.inputs import CONFIGS, make_inputs
+        self.torch, self.tte, self.stream = torch, tte, stream
+        self.train = False
+        dev = torch.device("cuda")
+        self.xs = [make_inputs(cfg, table=t) for t in range(len(CONFIGS[cfg]["tables"]))]
+        self.x = self.xs[0]
+        self.tables = []
+        need = 0
+        for x in self.xs:
+            self.tables.append(dict(
+                cores=[torch.from_numpy(c).to(dev) for c in x.cores],
+                idx=torch.from_numpy(x.indices).to(dev), off=torch.from_numpy(x.offsets).to(dev),
+                out=torch.empty((x.num_bags, x.D), dtype=torch.float32, device=dev)))
+            need = max(need, tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags))
+        self.ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        self.ws_bytes = need
+
+    def step(self):
+        for x, t in zip(self.xs, self.tables):
+            self.tte.tt_emb_forward(t["cores"], x.m, x.n, x.R, t["idx"], t["off"], t["out"],
+                                    self.ws)
+
+    def restore(self):
+        pass                                # the cores never change
+
+    def table_counts(self):
+        """(U_12, U_r, n_valid, status) of every table, one forward each."""
+        res = []
+        for x, t in zip(self.xs, self.tables):
+            self.tte.tt_emb_forward(t["cores"], x.m, x.n, x.R, t["idx"], t["off"], t["out"],
+                                    self.ws)
+            g = self.tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, self.ws)
+            res.append((g["U_12"], g["U_r"], g["n_valid"], g["status"]))
+        return res
+
+
 def time_replays(torch, wl, graph, steps, flush, profile_n=0):
     """Per-replay device ms (events on the replay stream); flush + restore outside the events."""
     tte = wl.tte
@@ -332,11 +375,13 @@ def run_ours(args, rank, world, dist):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
     result = {}
-    todo = (("train", TRAIN_CFG, True), ("forward", FWD_CFG, False))
+    todo = (("train", TRAIN_CFG, True), ("forward", FWD_CFG, False),
+            ("forward8", MULTI_CFG, False))
     if args.only:
         todo = tuple(t for t in todo if t[0] == args.only)
     for name, cfg, train in todo:
-        wl = Workload(cfg, train, torch, tte, stream)
+        wl = (MultiTableWorkload(cfg, torch, tte, stream) if name == "forward8"
+              else Workload(cfg, train, torch, tte, stream))
         with torch.cuda.stream(stream):
             for _ in range(2):          # eager warm-up (also settles the library's caches)
                 wl.restore()
@@ -345,8 +390,18 @@ def run_ours(args, rank, world, dist):
         rc, bits = tte.tt_emb_get_error(wl.ws, stream)
         if rc != 0:
             raise RuntimeError(f"device status {bits} on workload {name}")
-        U_12, U_r, nv, _ = wl.counts()
-        alg = algorithmic(wl.x, U_12, U_r)
+        if name == "forward8":
+            alg = {}
+            nv = 0
+            for x, (u12, ur, v, _) in zip(wl.xs, wl.table_counts()):
+                a1 = algorithmic(x, u12, ur)
+                for k in ("U_12", "U_r", "nnz", "B", "fwd_contract", "pool", "fwd_bytes"):
+                    alg[k] = alg.get(k, 0) + a1[k]
+                nv += v
+            stream.synchronize()
+        else:
+            U_12, U_r, nv, _ = wl.counts()
+            alg = algorithmic(wl.x, U_12, U_r)
         with torch.cuda.stream(stream):   # creates the timing events before any capture
             tte.tt_emb_profile_start()
             wl.restore()
@@ -379,7 +434,7 @@ def run_ours(args, rank, world, dist):
         ms = rank_max(dist, r["ms"])
         if rank == 0:
             return {"only": args.only, "ms_per_step": round(ms, 5),
-                    "lookups_per_s": round(weak_throughput(r["wl"].x.nnz, world, ms), 1),
+                    "lookups_per_s": round(weak_throughput(r["alg"]["nnz"], world, ms), 1),
                     "kernels": {k: round(v[0] / max(1, v[1]), 5) for k, v in r["kern"].items()}}
         return None
 
@@ -415,9 +470,10 @@ def run_ours(args, rank, world, dist):
     h2d = idx_h.numel() * 8 + off_h.numel() * 8 + g_h.numel() * 4
     d2h = out_h.numel() * 4
 
-    tr, fw = result["train"], result["forward"]
+    tr, fw, f8 = result["train"], result["forward"], result["forward8"]
     ms_train = rank_max(dist, tr["ms"])
     ms_fwd = rank_max(dist, fw["ms"])
+    ms_f8 = rank_max(dist, f8["ms"])
     ms_e2e = rank_max(dist, float(np.mean(e2e_times)))
     if rank != 0:
         return None
@@ -483,6 +539,34 @@ def run_ours(args, rank, world, dist):
     fwd_call = {"T_roof_us": round(t_roof * 1e6, 3), "T_call_us": round(ms_fwd * 1e3, 3),
                 "frac": round(t_roof / (ms_fwd * 1e-3), 4),
                 "F_unique_flop": F_fwd, "bytes": a["fwd_bytes"]}
+    # eight tables: every kernel launches once per table; the contraction
+    # kernel's achieved rate is the tables' unique-prefix FLOPs over its time
+    a8 = f8["alg"]
+    kms_f8, _ = per_step_kernel_ms(f8)
+    F8 = a8["fwd_contract"] + a8["pool"]
+    t_roof8 = max(F8 / (p_fp32 * 1e12), a8["fwd_bytes"] / (pk["hbm_gbs"] * 1e9))
+    dom8 = max(kms_f8, key=kms_f8.get)
+    contract8 = next((k for k in ("k_fwd_mma", "k_fwd_tiled", "k_fwd_generic") if k in kms_f8), None)
+    f8_line = {
+        "workload": "8 tables of 1e5, 1e6, 4e6, 1e7, 2e7, 3e7, 4e7, 4e7 rows (3 near-equal "
+                    "factors each), D=128=4x8x4, R1=R2=64, 32768 bags each of max(Poisson(20),1) "
+                    "Zipf(1.4) lookups, forward, one call per table on one stream",
+        "lookups_per_s": round(weak_throughput(a8["nnz"], world, ms_f8), 1),
+        "bags_per_s": round(a8["B"] * world / (ms_f8 * 1e-3), 1),
+        "ms_per_batch": round(ms_f8, 5),
+        "lookups": a8["nnz"], "unique_rows": a8["U_r"], "unique_prefixes": a8["U_12"],
+        "roofline_call": {"T_roof_us": round(t_roof8 * 1e6, 3), "T_call_us": round(ms_f8 * 1e3, 3),
+                          "frac": round(t_roof8 / (ms_f8 * 1e-3), 4), "F_unique_flop": F8,
+                          "bytes": a8["fwd_bytes"]},
+        "dominant_kernel": dom8,
+        "kernels_ms_per_batch": {k: round(v, 5) for k, v in sorted(kms_f8.items(),
+                                                                     key=lambda kv: -kv[1])},
+    }
+    if contract8:
+        ach8 = a8["fwd_contract"] / (kms_f8[contract8] * 1e-3) / 1e12
+        f8_line["contraction"] = {"kernel": contract8, "bound": "alu", "achieved": round(ach8, 3),
+                                  "peak": round(p_fp32, 2), "unit": "TFLOP/s",
+                                  "frac": round(ach8 / p_fp32, 4)}
     at = tr["alg"]
     nnz_tr = tr["wl"].x.nnz
     value = weak_throughput(nnz_tr, world, ms_train)
@@ -528,6 +612,7 @@ def run_ours(args, rank, world, dist):
             "kernels_ms_per_call": kms_fw,
             "clocks": fw["clocks"],
         },
+        "forward_8_tables": f8_line,
         "e2e": {"value": round(nnz_tr * world / (ms_e2e * 1e-3), 1), "unit": "lookups/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 5),
@@ -635,7 +720,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["train", "forward"], default=None,
+    ap.add_argument("--only", choices=["train", "forward", "forward8"], default=None,
                     help="time one workload only (short report; used to drive ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
