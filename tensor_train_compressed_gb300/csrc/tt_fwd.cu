@@ -112,12 +112,12 @@ __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_til
       const int nb = min(T::RB, x1 - xb);
       __syncthreads();   // P2 complete (first batch) / G3s free (later batches)
       constexpr int Q = R;   // float4 per G3 slice (R*4 floats)
-      for (int e = tid; e < nb * Q; e += 256) {
+      for (int e = tid; e < nb * Q; e += 256) {   // asynchronous 16-byte copies, all in flight
         const int r = e / Q, q = e - r * Q;
-        const float4 v = __ldg(reinterpret_cast<const float4*>(
-                                   a.G3 + (size_t)a.w.row_i3[xb + r] * (R * 4)) + q);
-        *reinterpret_cast<float4*>(G3s + r * T::G3S + 4 * q) = v;
+        cp_async16(G3s + r * T::G3S + 4 * q,
+                   reinterpret_cast<const float4*>(a.G3 + (size_t)a.w.row_i3[xb + r] * (R * 4)) + q);
       }
+      cp_async_wait_all();
       __syncthreads();
       const int r = rgrp * 32 + lane;
       if (r < nb) {

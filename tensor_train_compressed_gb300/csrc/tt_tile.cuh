@@ -120,25 +120,6 @@ __device__ __forceinline__ void tiled_stage2_any(const float* __restrict__ G2s,
   else tiled_stage2<T, 16>(G2s, P1t, P2, np);
 }
 
-// Stage the chunk's G2 slice and the transposed G1 rows of its prefixes.
-template <class T>
-__device__ __forceinline__ void tiled_load_g2_p1(const float* __restrict__ G1,
-                                                 const float* __restrict__ G2,
-                                                 const int32_t* __restrict__ pair_i1, int i2,
-                                                 int p0, int np, float* G2s, float* P1t) {
-  constexpr int R = T::kR;
-  const int tid = threadIdx.x;
-  const float4* g2 = reinterpret_cast<const float4*>(G2 + (size_t)i2 * T::F_G2);
-  float4* d = reinterpret_cast<float4*>(G2s);
-#pragma unroll 4
-  for (int e = tid; e < T::F_G2 / 4; e += 256) d[e] = __ldg(g2 + e);
-  for (int e = tid; e < np * R * 4; e += 256) {
-    const int p = e / (R * 4), rem = e - p * (R * 4);
-    const int j1 = rem / R, k = rem - j1 * R;        // coalesced read of G1[i1][0][j1][k]
-    P1t[p * (R * 4) + k * 4 + j1] = __ldg(G1 + (size_t)pair_i1[p0 + p] * (R * 4) + rem);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // mbarrier + bulk-copy (TMA, 1-D) helpers.  Every wait is capped: after
 // kWaitCap polls it sets the timeout bit and gives up.
@@ -176,6 +157,27 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Stage the chunk's G2 slice and the transposed G1 rows of its prefixes.
+template <class T>
+__device__ __forceinline__ void tiled_load_g2_p1(const float* __restrict__ G1,
+                                                 const float* __restrict__ G2,
+                                                 const int32_t* __restrict__ pair_i1, int i2,
+                                                 int p0, int np, float* G2s, float* P1t) {
+  constexpr int R = T::kR;
+  const int tid = threadIdx.x;
+  const float4* g2 = reinterpret_cast<const float4*>(G2 + (size_t)i2 * T::F_G2);
+  float4* d = reinterpret_cast<float4*>(G2s);
+  // the G2 slice by 16-byte asynchronous copies, all in flight at once, while
+  // the G1 rows (transposed on the way) take the register path
+  for (int e = tid; e < T::F_G2 / 4; e += 256) cp_async16(d + e, g2 + e);
+  for (int e = tid; e < np * R * 4; e += 256) {
+    const int p = e / (R * 4), rem = e - p * (R * 4);
+    const int j1 = rem / R, k = rem - j1 * R;        // coalesced read of G1[i1][0][j1][k]
+    P1t[p * (R * 4) + k * 4 + j1] = __ldg(G1 + (size_t)pair_i1[p0 + p] * (R * 4) + rem);
+  }
+  cp_async_wait_all();
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
