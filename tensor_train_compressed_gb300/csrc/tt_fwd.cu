@@ -83,6 +83,27 @@ __global__ void __launch_bounds__(256) k_fwd_generic(FwdArgs a) {
   }
 }
 
+// Chunk metadata from the descriptors the grouping writes: rows x0 .. x1-1,
+// prefixes p0 .. p0+np-1, their i2.  Two dependent round trips (descriptors,
+// then i2); c >= n_chunks gives x0 = x1 (the end).
+struct TiledMeta {
+  int c, x0, x1, p0, np, i2;
+};
+__device__ __forceinline__ TiledMeta tiled_meta(const WS& w, int c, int n_chunks) {
+  TiledMeta m{c, 0, 0, 0, 0, 0};
+  if (c >= n_chunks) return m;
+  const int2 d0 = w.chunk_desc[c], d1 = w.chunk_desc[c + 1];
+  m.x0 = d0.x;
+  m.x1 = d1.x;
+  m.p0 = d0.y & 0x7fffffff;
+  // the chunk's last prefix: the next chunk's, unless that one starts a new prefix
+  const int pn = d1.y & 0x7fffffff;
+  const int p1 = (d1.y < 0) ? pn - 1 : pn;
+  m.np = p1 - m.p0 + 1;
+  m.i2 = w.pair_i2[m.p0];
+  return m;
+}
+
 template <int N2, int R, int CP>
 __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_tiled(FwdArgs a) {
   using T = TileCfg<N2, R, CP>;
@@ -91,19 +112,22 @@ __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_til
   float* P1t = G2s + T::F_G2;
   float* P2 = P1t + T::F_P1;
   float* G3s = P2 + T::F_P2;
-  __shared__ int c_sh;
+  __shared__ TiledMeta meta[2];
+  __shared__ int rp_sh[T::RB];          // prefix of every row of the stage-3 batch
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_chunks = a.w.ctl->n_chunks;
-  for (;;) {
-    if (tid == 0) c_sh = (int)atomicAdd(&a.w.ctl->fwd_chunk_ctr, 1u);
-    __syncthreads();
-    const int c = c_sh;
-    if (c >= n_chunks) break;
-    const int x0 = a.w.chunk_start[c], x1 = a.w.chunk_start[c + 1];
-    const int p0 = a.w.row_pair[x0], p1 = a.w.row_pair[x1 - 1];
-    const int np = p1 - p0 + 1;
-    const int i2 = a.w.pair_i2[p0];
-    tiled_load_g2_p1<T>(a.G1, a.G2, a.w.pair_i1, i2, p0, np, G2s, P1t);
+  if (tid == 0) meta[0] = tiled_meta(a.w, (int)atomicAdd(&a.w.ctl->fwd_chunk_ctr, 1u), n_chunks);
+  __syncthreads();
+  for (int it = 0;; ++it) {
+    const TiledMeta m = meta[it & 1];
+    if (m.c >= n_chunks) break;
+    const int x0 = m.x0, x1 = m.x1, p0 = m.p0, np = m.np;
+    // the G2 slice and G1 rows of this chunk; thread 0 claims the next chunk and
+    // loads its metadata while the copies are in flight
+    tiled_load_g2_p1<T>(a.G1, a.G2, a.w.pair_i1, m.i2, p0, np, G2s, P1t, [&]() {
+      if (tid == 0)
+        meta[(it + 1) & 1] = tiled_meta(a.w, (int)atomicAdd(&a.w.ctl->fwd_chunk_ctr, 1u), n_chunks);
+    });
     __syncthreads();
     tiled_stage2_any<T>(G2s, P1t, P2, np);
     // stage 3 in batches of RB rows
@@ -117,12 +141,13 @@ __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_til
         cp_async16(G3s + r * T::G3S + 4 * q,
                    reinterpret_cast<const float4*>(a.G3 + (size_t)a.w.row_i3[xb + r] * (R * 4)) + q);
       }
+      if (tid < nb) rp_sh[tid] = a.w.row_pair[xb + tid] - p0;
       cp_async_wait_all();
       __syncthreads();
       const int r = rgrp * 32 + lane;
       if (r < nb) {
         const int x = xb + r;
-        const float* pp = P2 + (a.w.row_pair[x] - p0) * T::P2P + (blk * 4) * T::P2S;
+        const float* pp = P2 + rp_sh[r] * T::P2P + (blk * 4) * T::P2S;
         const float* gg = G3s + r * T::G3S;
         float acc[4][4];
 #pragma unroll

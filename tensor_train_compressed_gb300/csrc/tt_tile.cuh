@@ -159,12 +159,14 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Stage the chunk's G2 slice and the transposed G1 rows of its prefixes.
-template <class T>
+// Stage the chunk's G2 slice and the transposed G1 rows of its prefixes;
+// `while_in_flight` runs once the slice's copies are issued.
+template <class T, class F = void (*)()>
 __device__ __forceinline__ void tiled_load_g2_p1(const float* __restrict__ G1,
                                                  const float* __restrict__ G2,
                                                  const int32_t* __restrict__ pair_i1, int i2,
-                                                 int p0, int np, float* G2s, float* P1t) {
+                                                 int p0, int np, float* G2s, float* P1t,
+                                                 F while_in_flight = [] {}) {
   constexpr int R = T::kR;
   const int tid = threadIdx.x;
   const float4* g2 = reinterpret_cast<const float4*>(G2 + (size_t)i2 * T::F_G2);
@@ -172,6 +174,7 @@ __device__ __forceinline__ void tiled_load_g2_p1(const float* __restrict__ G1,
   // the G2 slice by 16-byte asynchronous copies, all in flight at once, while
   // the G1 rows (transposed on the way) take the register path
   for (int e = tid; e < T::F_G2 / 4; e += 256) cp_async16(d + e, g2 + e);
+  while_in_flight();
   for (int e = tid; e < np * R * 4; e += 256) {
     const int p = e / (R * 4), rem = e - p * (R * 4);
     const int j1 = rem / R, k = rem - j1 * R;        // coalesced read of G1[i1][0][j1][k]
