@@ -89,6 +89,35 @@ int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_
                    const int64_t* offsets, int64_t num_bags, float* out, void* workspace,
                    size_t ws_bytes, void* stream);
 
+/* One table of tt_emb_forward_tables: the arguments of tt_emb_forward. */
+typedef struct {
+  const float* cores[3];
+  int64_t m[3];
+  int32_t n[3];
+  int32_t R[4];
+  const int64_t* indices;
+  int64_t nnz;
+  const int64_t* offsets;
+  int64_t num_bags;
+  float* out;
+  void* workspace;          /* this table's own workspace (no two tables share one) */
+  size_t ws_bytes;
+} tt_emb_table;
+
+/* Forward of up to 8 tables in one call (a recommendation model looks up
+ * several embedding tables per batch; the pages have no counterpart of this
+ * entry point).  Every table's `out` receives exactly what tt_emb_forward would
+ * write for it
+ * (sum pooling).  All tables share n and R (TT_EMB_ERR_ARG otherwise); their m,
+ * batches and workspaces are their own, and workspaces must not overlap.
+ * Each table is grouped into its own workspace; for shapes served by the
+ * tiled chunk kernel (n = (4, 8, 4) with R1 = R2 = 64, n = (4, 4, 4) with
+ * R1 = R2 = 16) one persistent launch of that kernel then works through the
+ * chunks of all tables (one counter, chunks numbered across the tables), so
+ * the tables share the grid instead of each draining it; other shapes run
+ * table by table.  num_tables in [1, 8]. */
+int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stream);
+
 /* Pooling rules of tt_emb_forward_ex / tt_emb_backward_ex. */
 #define TT_EMB_POOL_SUM 0    /* out[b] = sum of the bag's rows (optionally weighted)   */
 #define TT_EMB_POOL_MEAN 1   /* out[b] = that sum / number of the bag's lookups        */

@@ -32,6 +32,7 @@ _POOLING = {"sum": TT_EMB_POOL_SUM, "mean": TT_EMB_POOL_MEAN}
 
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
             "tt_emb_forward_ex", "tt_emb_backward_ex", "tt_emb_split", "tt_emb_sgd_ex",
+            "tt_emb_forward_tables",
             "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_profile_start",
             "tt_emb_profile_stop", "tt_emb_profile_read", "tt_emb_forward_static",
             "tt_emb_version")
@@ -41,6 +42,15 @@ class TTEmbError(RuntimeError):
     def __init__(self, code: int, what: str):
         super().__init__(f"{what}: {_NAMES.get(code, code)}")
         self.code = code
+
+
+class Table(ctypes.Structure):
+    """tt_emb_table of include/tt_emb.h."""
+    _fields_ = [("cores", ctypes.c_void_p * 3), ("m", ctypes.c_int64 * 3), ("n", ctypes.c_int32 * 3),
+                ("R", ctypes.c_int32 * 4), ("indices", ctypes.c_void_p), ("nnz", ctypes.c_int64),
+                ("offsets", ctypes.c_void_p), ("num_bags", ctypes.c_int64),
+                ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("ws_bytes", ctypes.c_size_t)]
 
 
 class Grouping(ctypes.Structure):
@@ -73,6 +83,7 @@ def lib():
         L.tt_emb_forward_ex.argtypes = [P, P, P, P, P, I64, P, I64, P, ctypes.c_int, ctypes.c_int,
                                         P, P, SZ, P]
         L.tt_emb_split.argtypes = [P, P, P, P, P, SZ, P]
+        L.tt_emb_forward_tables.argtypes = [ctypes.c_int, P, P]
         L.tt_emb_sgd_ex.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, P, SZ, P]
         L.tt_emb_backward_ex.argtypes = [P, P, P, P, P, P, I64, P, I64, P, ctypes.c_int, P, P, P,
                                          SZ, ctypes.c_int, P]
@@ -194,6 +205,27 @@ def tt_emb_sgd(cores, core_grads, m, n, R, lr: float, zero_grads: bool = False, 
     _check(lib().tt_emb_sgd(_ptrs3(cores, "cores"), _ptrs3(core_grads, "core_grads"),
                             *_shape(m, n, R), ctypes.c_float(lr), int(bool(zero_grads)),
                             _stream(stream)), "tt_emb_sgd")
+
+
+def tt_emb_forward_tables(tables, stream=None):
+    """tables: sequence of dicts with the tt_emb_forward arguments (cores, m, n, R, indices,
+    offsets, out, workspace); every table needs its own workspace."""
+    arr = (Table * len(tables))()
+    for k, t in enumerate(tables):
+        e = arr[k]
+        for j, c in enumerate(t["cores"]):
+            e.cores[j] = _dev(c, torch.float32, f"tables[{k}].cores[{j}]").value
+        m, n, R = _shape(t["m"], t["n"], t["R"])
+        e.m[:], e.n[:], e.R[:] = list(m), list(n), list(R)
+        e.indices = _dev(t["indices"], torch.int64, "indices")
+        e.nnz = t["indices"].numel()
+        e.offsets = _dev(t["offsets"], torch.int64, "offsets")
+        e.num_bags = t["offsets"].numel() - 1
+        e.out = _dev(t["out"], torch.float32, "out")
+        e.workspace = _dev(t["workspace"], torch.uint8, "workspace")
+        e.ws_bytes = t["workspace"].numel()
+    _check(lib().tt_emb_forward_tables(len(tables), ctypes.cast(arr, ctypes.c_void_p),
+                                       _stream(stream)), "tt_emb_forward_tables")
 
 
 def tt_emb_split(cores, m, n, R, workspace, stream=None):

@@ -260,6 +260,56 @@ int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_
                            TT_EMB_POOL_SUM, 0, out, workspace, ws_bytes, stream);
 }
 
+int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stream) {
+  if (num_tables < 1 || num_tables > kMaxTables || !tables) return TT_EMB_ERR_ARG;
+  Shape s[kMaxTables];
+  Layout L[kMaxTables];
+  WS w[kMaxTables];
+  const float* const* cores[kMaxTables];
+  const int64_t* offsets[kMaxTables];
+  int64_t nnz[kMaxTables], bags[kMaxTables];
+  float* out[kMaxTables];
+  for (int t = 0; t < num_tables; ++t) {
+    const tt_emb_table& tb = tables[t];
+    int rc = shape_from_args(tb.m, tb.n, tb.R, &s[t]);
+    if (rc) return rc;
+    for (int k = 0; k < 3; ++k)
+      if (tb.n[k] != tables[0].n[k]) return TT_EMB_ERR_ARG;
+    for (int k = 0; k < 4; ++k)
+      if (tb.R[k] != tables[0].R[k]) return TT_EMB_ERR_ARG;
+    rc = check_cores(tb.cores);
+    if (rc) return rc;
+    rc = check_batch(s[t], tb.indices, tb.nnz, tb.offsets, tb.num_bags, tb.workspace, tb.ws_bytes,
+                     &L[t]);
+    if (rc) return rc;
+    if (tb.num_bags > 0 && (!tb.out || !aligned(tb.out, 16))) return TT_EMB_ERR_ARG;
+    // every table groups into its own workspace
+    for (int u = 0; u < t; ++u) {
+      const char* a0 = static_cast<const char*>(tb.workspace);
+      const char* b0 = static_cast<const char*>(tables[u].workspace);
+      if (a0 < b0 + tables[u].ws_bytes && b0 < a0 + tb.ws_bytes) return TT_EMB_ERR_ARG;
+    }
+    w[t] = make_ws(tb.workspace, L[t]);
+    cores[t] = tb.cores;
+    offsets[t] = tb.offsets;
+    nnz[t] = tb.nnz;
+    bags[t] = tb.num_bags;
+    out[t] = tb.out;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  for (int t = 0; t < num_tables; ++t) {
+    int CP, CR;
+    int rc = forward_chunk_params(s[t], &CP, &CR);
+    if (rc) return rc;
+    rc = launch_group(s[t], L[t], w[t], tables[t].indices, nnz[t], offsets[t], bags[t], CP, CR, st);
+    if (rc) return rc;
+    if (nnz[t] == 0 && bags[t] > 0 &&
+        cudaMemsetAsync(out[t], 0, sizeof(float) * (size_t)bags[t] * s[t].D, st) != cudaSuccess)
+      return TT_EMB_ERR_CUDA;
+  }
+  return launch_forward_tables(num_tables, s, L, w, cores, offsets, nnz, bags, out, st);
+}
+
 int tt_emb_backward_ex(const float* grad_out, const float* const cores[3], const int64_t m[3],
                        const int32_t n[3], const int32_t R[4], const int64_t* indices,
                        int64_t nnz, const int64_t* offsets, int64_t num_bags,

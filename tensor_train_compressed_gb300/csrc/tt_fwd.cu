@@ -87,10 +87,10 @@ __global__ void __launch_bounds__(256) k_fwd_generic(FwdArgs a) {
 // prefixes p0 .. p0+np-1, their i2.  Two dependent round trips (descriptors,
 // then i2); c >= n_chunks gives x0 = x1 (the end).
 struct TiledMeta {
-  int c, x0, x1, p0, np, i2;
+  int c, x0, x1, p0, np, i2, tab;
 };
 __device__ __forceinline__ TiledMeta tiled_meta(const WS& w, int c, int n_chunks) {
-  TiledMeta m{c, 0, 0, 0, 0, 0};
+  TiledMeta m{c, 0, 0, 0, 0, 0, 0};
   if (c >= n_chunks) return m;
   const int2 d0 = w.chunk_desc[c], d1 = w.chunk_desc[c + 1];
   m.x0 = d0.x;
@@ -104,8 +104,34 @@ __device__ __forceinline__ TiledMeta tiled_meta(const WS& w, int c, int n_chunks
   return m;
 }
 
+// The tables of one launch of the tiled chunk kernel (one table for a plain
+// forward; up to kMaxTables for tt_emb_forward_tables, all of one (n, R)).
+// Chunks are claimed from the first table's counter and numbered across the
+// tables in order, so that one persistent grid balances all of them.
+struct TiledTables {
+  FwdArgs t[kMaxTables];
+  int T;
+};
+
+// Table and table-local metadata of global chunk cg (cbase: first global chunk
+// of every table, cbase[T] = all chunks).
+__device__ __forceinline__ TiledMeta tiled_meta_tables(const TiledTables& tabs, const int* cbase,
+                                                       int cg) {
+  int t = 0;
+  while (t + 1 < tabs.T && cg >= cbase[t + 1]) ++t;
+  if (cg >= cbase[tabs.T]) {
+    TiledMeta m{cg, 0, 0, 0, 0, 0, 0};
+    return m;
+  }
+  TiledMeta m = tiled_meta(tabs.t[t].w, cg - cbase[t], cbase[t + 1] - cbase[t]);
+  m.c = cg;
+  m.tab = t;
+  return m;
+}
+
 template <int N2, int R, int CP>
-__global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_tiled(FwdArgs a) {
+__global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS)
+    k_fwd_tiled(const __grid_constant__ TiledTables tabs) {
   using T = TileCfg<N2, R, CP>;
   extern __shared__ float4 sm4[];
   float* G2s = reinterpret_cast<float*>(sm4);
@@ -114,19 +140,29 @@ __global__ void __launch_bounds__(256, TileCfg<N2, R, CP>::MIN_BLOCKS) k_fwd_til
   float* G3s = P2 + T::F_P2;
   __shared__ TiledMeta meta[2];
   __shared__ int rp_sh[T::RB];          // prefix of every row of the stage-3 batch
+  __shared__ int cbase[kMaxTables + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_chunks = a.w.ctl->n_chunks;
-  if (tid == 0) meta[0] = tiled_meta(a.w, (int)atomicAdd(&a.w.ctl->fwd_chunk_ctr, 1u), n_chunks);
+  uint32_t* ctr = &tabs.t[0].w.ctl->fwd_chunk_ctr;
+  if (tid == 0) {
+    int acc = 0;
+    for (int t = 0; t < tabs.T; ++t) {
+      cbase[t] = acc;
+      acc += tabs.t[t].w.ctl->n_chunks;
+    }
+    cbase[tabs.T] = acc;
+    meta[0] = tiled_meta_tables(tabs, cbase, (int)atomicAdd(ctr, 1u));
+  }
   __syncthreads();
+  const int n_chunks = cbase[tabs.T];
   for (int it = 0;; ++it) {
     const TiledMeta m = meta[it & 1];
     if (m.c >= n_chunks) break;
+    const FwdArgs& a = tabs.t[m.tab];
     const int x0 = m.x0, x1 = m.x1, p0 = m.p0, np = m.np;
     // the G2 slice and G1 rows of this chunk; thread 0 claims the next chunk and
     // loads its metadata while the copies are in flight
     tiled_load_g2_p1<T>(a.G1, a.G2, a.w.pair_i1, m.i2, p0, np, G2s, P1t, [&]() {
-      if (tid == 0)
-        meta[(it + 1) & 1] = tiled_meta(a.w, (int)atomicAdd(&a.w.ctl->fwd_chunk_ctr, 1u), n_chunks);
+      if (tid == 0) meta[(it + 1) & 1] = tiled_meta_tables(tabs, cbase, (int)atomicAdd(ctr, 1u));
     });
     __syncthreads();
     tiled_stage2_any<T>(G2s, P1t, P2, np);
@@ -765,7 +801,7 @@ static void launch_fwd_mma(const FwdArgs& fa, cudaStream_t st) {
 }
 
 template <int N2, int R, int CP>
-static void launch_tiled(const FwdArgs& fa, cudaStream_t st) {
+static void launch_tiled(const TiledTables& tt, cudaStream_t st) {
   using T = TileCfg<N2, R, CP>;
   static int grid = 0;
   if (grid == 0) {
@@ -773,7 +809,12 @@ static void launch_tiled(const FwdArgs& fa, cudaStream_t st) {
                          T::SMEM);
     grid = persistent_grid((const void*)k_fwd_tiled<N2, R, CP>, 256, T::SMEM);
   }
-  TT_TIMED("k_fwd_tiled", st, (k_fwd_tiled<N2, R, CP><<<grid, 256, T::SMEM, st>>>(fa)));
+  TT_TIMED("k_fwd_tiled", st, (k_fwd_tiled<N2, R, CP><<<grid, 256, T::SMEM, st>>>(tt)));
+}
+
+static void launch_tiled_kind(FwdKind kind, const TiledTables& tt, cudaStream_t st) {
+  if (kind == kFwdTiled_8_64) launch_tiled<8, 64, kCP_8_64>(tt, st);
+  else launch_tiled<4, 16, kCP_4_16>(tt, st);
 }
 
 int launch_rows(const Shape& s, const WS& w, const float* const cores[3], int presplit,
@@ -795,8 +836,14 @@ int launch_rows(const Shape& s, const WS& w, const float* const cores[3], int pr
       }
       launch_fwd_mma<8>(fa, st);
       break;
-    case kFwdTiled_8_64: launch_tiled<8, 64, kCP_8_64>(fa, st); break;
-    case kFwdTiled_4_16: launch_tiled<4, 16, kCP_4_16>(fa, st); break;
+    case kFwdTiled_8_64:
+    case kFwdTiled_4_16: {
+      TiledTables tt;
+      tt.t[0] = fa;
+      tt.T = 1;
+      launch_tiled_kind(fwd_kind(s), tt, st);
+      break;
+    }
     default: {
       const size_t smem = fwd_generic_smem(s, CP);
       static int grid = 0;
@@ -845,6 +892,40 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
       default: launch_pool_mode<kPoolSum>(s, L, w, offsets, nnz, num_bags, nullptr, out, st);
     }
   }
+  return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
+}
+
+int launch_forward_tables(int T, const Shape* s, const Layout* L, const WS* w,
+                          const float* const* const* cores, const int64_t* const* offsets,
+                          const int64_t* nnz, const int64_t* num_bags, float* const* out,
+                          cudaStream_t st) {
+  const FwdKind kind = fwd_kind(s[0]);
+  if (kind != kFwdTiled_8_64 && kind != kFwdTiled_4_16) {
+    for (int t = 0; t < T; ++t) {
+      if (nnz[t] == 0) continue;
+      const Pooling pool{kPoolSum, nullptr};
+      const int rc = launch_forward(s[t], L[t], w[t], cores[t], offsets[t], nnz[t], num_bags[t],
+                                    pool, 0, out[t], st);
+      if (rc) return rc;
+    }
+    return TT_EMB_OK;
+  }
+  TiledTables tt;
+  tt.T = 0;
+  for (int t = 0; t < T; ++t) {
+    if (nnz[t] == 0) continue;
+    FwdArgs& fa = tt.t[tt.T++];
+    fa.s = s[t];
+    fa.w = w[t];
+    fa.G1 = cores[t][0];
+    fa.G2 = cores[t][1];
+    fa.G3 = cores[t][2];
+  }
+  if (tt.T > 0) launch_tiled_kind(kind, tt, st);
+  for (int t = 0; t < T; ++t)
+    if (nnz[t] > 0 && num_bags[t] > 0)
+      launch_pool_mode<kPoolSum>(s[t], L[t], w[t], offsets[t], nnz[t], num_bags[t], nullptr, out[t],
+                                 st);
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }
 

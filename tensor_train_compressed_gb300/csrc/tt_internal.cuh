@@ -26,6 +26,7 @@ constexpr int kScanTile = kScanThreads * kScanItems;
 constexpr int kSSlice = 64;                 // sorted positions per warp in the grad gather
 constexpr int kSCta = 8 * kSSlice;          // sorted positions per CTA in the D = 128 grad gather
 constexpr int kMaxSmemFloats = 53248;       // 208 KB of shared memory per CTA
+constexpr int kMaxTables = 8;               // tables of one tt_emb_forward_tables call
 
 // status word bits
 constexpr uint32_t kStIndex = 1u;
@@ -339,6 +340,13 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
                    const int64_t* offsets, int64_t nnz, int64_t num_bags, const Pooling& pool,
                    int presplit, float* out, cudaStream_t st);
 int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chunk);
+// forward of T tables already grouped into their workspaces, sum pooling: one
+// launch of the chunk kernel for all tables where the shape runs the tiled
+// kernel, table by table otherwise
+int launch_forward_tables(int T, const Shape* s, const Layout* L, const WS* w,
+                          const float* const* const* cores, const int64_t* const* offsets,
+                          const int64_t* nnz, const int64_t* num_bags, float* const* out,
+                          cudaStream_t st);
 // backward (tt_bwd.cu)
 int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out, int reuse,
                     const float* const cores[3], const int64_t* offsets, int64_t nnz,

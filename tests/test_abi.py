@@ -144,3 +144,26 @@ def test_split_and_fused_sgd_argument_checks(L):
                            None) == tte.TT_EMB_ERR_WORKSPACE
     assert L.tt_emb_sgd_ex(cores, None, *_shape(m, n, R), ctypes.c_float(0.1), 0, P(fake), small,
                            None) == tte.TT_EMB_ERR_ARG
+
+
+def test_forward_tables_argument_checks(L):
+    """Table counts outside 1..8 and tables that share a workspace are refused before any
+    launch."""
+    from tensor_train_compressed_gb300._binding import Table
+    fake = 1 << 20
+    m, n, R = (10, 10, 10), (2, 4, 2), (1, 4, 4, 1)
+    need = tte.tt_emb_workspace_bytes(m, n, R, 100, 10)
+    arr = (Table * 9)()
+    for t in arr:
+        t.cores[:] = [fake, fake, fake]
+        t.m[:], t.n[:], t.R[:] = list(m), list(n), list(R)
+        t.indices, t.nnz, t.offsets, t.num_bags = fake, 100, fake, 10
+        t.out, t.workspace, t.ws_bytes = fake, fake, need
+    P = ctypes.c_void_p
+    ptr = ctypes.cast(arr, P)
+    assert L.tt_emb_forward_tables(0, ptr, None) == tte.TT_EMB_ERR_ARG
+    assert L.tt_emb_forward_tables(9, ptr, None) == tte.TT_EMB_ERR_ARG
+    assert L.tt_emb_forward_tables(2, ptr, None) == tte.TT_EMB_ERR_ARG   # shared workspace
+    arr[1].workspace = fake + need + 256
+    arr[1].n[1] = 8
+    assert L.tt_emb_forward_tables(2, ptr, None) == tte.TT_EMB_ERR_ARG   # other n
