@@ -13,7 +13,7 @@ Pins (tests/test_oracle_pins.py): a hand-worked example (tests/golden/),
 exact reconstruction of a dense table through a TT-SVD, Kronecker rows for
 rank-1 cores, a materialised table + torch embedding_bag (sum, mean and
 per-sample weights), multilinearity, integer weights against repeated
-lookups, the adjoint identity, central differences and torch autograd for the
+lookups, exact TT-SVD reconstruction and torch autograd for chains of d cores, the adjoint identity, central differences and torch autograd for the
 backward (core and weight gradients), and numpy lexsort/unique for the
 grouping.  No function here is "parity unpinned".
 """
@@ -71,6 +71,10 @@ def _load():
             lib.tto_backward_ex.argtypes = [P, P, P, P, P, P, P, P, I64, P, I64, P, ctypes.c_int,
                                             P, P, P, P, ctypes.c_int, I64, ctypes.c_int]
             lib.tto_backward_ex.restype = ctypes.c_int
+            lib.tto_forward_d.argtypes = [ctypes.c_int, P, P, P, P, P, I64, P, I64, P]
+            lib.tto_forward_d.restype = ctypes.c_int
+            lib.tto_backward_d.argtypes = [ctypes.c_int, P, P, P, P, P, P, I64, P, I64, P]
+            lib.tto_backward_d.restype = ctypes.c_int
             lib.tto_sgd.argtypes = [P, P, I64, ctypes.c_double, P]
             lib.tto_sgd.restype = None
             lib.tto_group.argtypes = [P, I64, P, P, P, P, P, P, P, P, P, P]
@@ -150,6 +154,50 @@ def backward(grad_out, cores, m, n, R, indices, offsets, threads: int = 1,
     if rc != TTO_OK and (strict or rc != TTO_ERR_INDEX):
         raise OracleError(rc, "tto_backward_ex")
     return (dG, dW) if want_dw else dG
+
+
+def _ptr_array(arrs):
+    return (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+
+
+def forward_d(cores, m, n, R, indices, offsets, strict: bool = True):
+    """fp64 pooled output [B][D] of a chain of d = len(cores) cores (sum pooling)."""
+    lib = _load()
+    G = [np.ascontiguousarray(c, dtype=np.float32) for c in cores]
+    d = len(G)
+    m_a = np.ascontiguousarray(m, dtype=np.int64)
+    n_a = np.ascontiguousarray(n, dtype=np.int32)
+    R_a = np.ascontiguousarray(R, dtype=np.int32)
+    idx = np.ascontiguousarray(indices, dtype=np.int64)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    B = off.shape[0] - 1
+    out = np.zeros((max(B, 0), int(n_a.prod())), dtype=np.float64)
+    gp = _ptr_array(G)
+    rc = lib.tto_forward_d(d, gp, _p(m_a), _p(n_a), _p(R_a), _p(idx), idx.shape[0], _p(off), B,
+                           _p(out))
+    if rc != TTO_OK and (strict or rc != TTO_ERR_INDEX):
+        raise OracleError(rc, "tto_forward_d")
+    return out
+
+
+def backward_d(grad_out, cores, m, n, R, indices, offsets, strict: bool = True):
+    """fp64 gradients of <grad_out, out> for every core of a d-core chain (fresh zeros, +=)."""
+    lib = _load()
+    G = [np.ascontiguousarray(c, dtype=np.float32) for c in cores]
+    d = len(G)
+    m_a = np.ascontiguousarray(m, dtype=np.int64)
+    n_a = np.ascontiguousarray(n, dtype=np.int32)
+    R_a = np.ascontiguousarray(R, dtype=np.int32)
+    idx = np.ascontiguousarray(indices, dtype=np.int64)
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    g = np.ascontiguousarray(grad_out, dtype=np.float32)
+    B = off.shape[0] - 1
+    dG = [np.zeros(c.shape, dtype=np.float64) for c in G]
+    rc = lib.tto_backward_d(d, _p(g), _ptr_array(G), _p(m_a), _p(n_a), _p(R_a), _p(idx),
+                            idx.shape[0], _p(off), B, _ptr_array(dG))
+    if rc != TTO_OK and (strict or rc != TTO_ERR_INDEX):
+        raise OracleError(rc, "tto_backward_d")
+    return dG
 
 
 def sgd(core, dcore, lr: float):

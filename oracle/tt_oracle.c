@@ -443,3 +443,181 @@ int tto_group(const int64_t *indices, int64_t nnz, const int64_t *m, int32_t *pe
   free(kl);
   return err;
 }
+
+/* ---------------- d cores ----------------
+ *
+ * The same definitions for a chain of d >= 2 cores (the pages contract "a
+ * chain of small TT cores", FlowTT summary card, problem statement; three
+ * cores is the case above).  Core k (0-based) is float32
+ * [m_k][R_k][n_k][R_{k+1}] with R_0 = R_d = 1; the row index splits
+ * mixed-radix with i_0 most significant, the output position likewise with
+ * j_0 most significant.  Per lookup the chain T_0 = G_0[i_0] (n_0 x R_1),
+ * T_k = T_{k-1} . G_k[i_k] ((n_0..n_{k-1}) x R_k times R_k x (n_k R_{k+1}),
+ * viewed as (n_0..n_k) x R_{k+1}), row = T_{d-1}; bags are summed.  The
+ * backward keeps the chain and walks it back: dG_k[i_k] += T_{k-1}^T . dT_k,
+ * dT_{k-1} = dT_k . G_k[i_k]^T, dG_0[i_0] += dT_0. */
+
+#define TTO_MAXD 8
+
+typedef struct {
+  int d;
+  const float *G[TTO_MAXD];
+  int64_t m[TTO_MAXD];
+  int n[TTO_MAXD], R[TTO_MAXD + 1];
+  int64_t M;
+  int D;
+} tto_ttd;
+
+static int tto_initd(tto_ttd *t, int d, const float *const *G, const int64_t *m, const int32_t *n,
+                     const int32_t *R) {
+  if (d < 2 || d > TTO_MAXD || !G || !m || !n || !R) return TTO_ERR_ARG;
+  if (R[0] != 1 || R[d] != 1) return TTO_ERR_ARG;
+  t->d = d;
+  t->M = 1;
+  t->D = 1;
+  t->R[0] = 1;
+  for (int k = 0; k < d; ++k) {
+    if (!G[k] || m[k] < 1 || n[k] < 1 || R[k + 1] < 1) return TTO_ERR_ARG;
+    t->G[k] = G[k];
+    t->m[k] = m[k];
+    t->n[k] = n[k];
+    t->R[k + 1] = R[k + 1];
+    t->M *= m[k];
+    t->D *= n[k];
+  }
+  return TTO_OK;
+}
+
+/* digits of r, i_0 most significant */
+static void tto_splitd(const tto_ttd *t, int64_t r, int64_t *ik) {
+  for (int k = t->d - 1; k >= 0; --k) {
+    ik[k] = r % t->m[k];
+    r /= t->m[k];
+  }
+}
+
+/* chain T_0 .. T_{d-1} of one lookup into T (T_k at offset off[k]; N_k = n_0..n_k rows) */
+static void tto_chaind(const tto_ttd *t, const int64_t *ik, double *T, const size_t *off) {
+  int N = t->n[0];
+  const float *g0 = t->G[0] + ik[0] * (int64_t)t->n[0] * t->R[1];
+  for (int e = 0; e < N * t->R[1]; ++e) T[off[0] + e] = (double)g0[e];
+  for (int k = 1; k < t->d; ++k) {
+    const int Ra = t->R[k], nk = t->n[k], Rb = t->R[k + 1];
+    const float *gk = t->G[k] + ik[k] * (int64_t)Ra * nk * Rb;
+    const double *A = T + off[k - 1];
+    double *C = T + off[k];
+    for (int J = 0; J < N; ++J)
+      for (int j = 0; j < nk; ++j)
+        for (int b = 0; b < Rb; ++b) {
+          double s = 0.0;
+          for (int a = 0; a < Ra; ++a) s += A[J * Ra + a] * (double)gk[(a * nk + j) * Rb + b];
+          C[(J * nk + j) * Rb + b] = s;
+        }
+    N *= nk;
+  }
+}
+
+static size_t tto_chain_offsets(const tto_ttd *t, size_t *off) {
+  size_t o = 0;
+  int N = 1;
+  for (int k = 0; k < t->d; ++k) {
+    N *= t->n[k];
+    off[k] = o;
+    o += (size_t)N * t->R[k + 1];
+  }
+  return o;
+}
+
+/* out: double [B][D], overwritten; as tto_forward for d cores (sum pooling). */
+int tto_forward_d(int d, const float *const *G, const int64_t *m, const int32_t *n,
+                  const int32_t *R, const int64_t *indices, int64_t nnz, const int64_t *offsets,
+                  int64_t B, double *out) {
+  tto_ttd t;
+  int e = tto_initd(&t, d, G, m, n, R);
+  if (e) return e;
+  if (nnz < 0 || (nnz > 0 && !indices) || (B > 0 && !out)) return TTO_ERR_ARG;
+  e = tto_check_offsets(offsets, B, nnz);
+  if (e) return e;
+  size_t off[TTO_MAXD];
+  const size_t tot = tto_chain_offsets(&t, off);
+  double *T = (double *)malloc(sizeof(double) * tot);
+  if (!T) return TTO_ERR_NOMEM;
+  int err = TTO_OK;
+  int64_t ik[TTO_MAXD];
+  for (int64_t b = 0; b < B; ++b) {
+    double *o = out + b * t.D;
+    for (int j = 0; j < t.D; ++j) o[j] = 0.0;
+    for (int64_t l = offsets[b]; l < offsets[b + 1]; ++l) {
+      const int64_t r = indices[l];
+      if (r < 0 || r >= t.M) { err = TTO_ERR_INDEX; continue; }
+      tto_splitd(&t, r, ik);
+      tto_chaind(&t, ik, T, off);
+      const double *row = T + off[d - 1];
+      for (int j = 0; j < t.D; ++j) o[j] += row[j];
+    }
+  }
+  free(T);
+  return err;
+}
+
+/* dG[k]: double, same layouts as the cores, ACCUMULATED (+=). */
+int tto_backward_d(int d, const float *grad_out, const float *const *G, const int64_t *m,
+                   const int32_t *n, const int32_t *R, const int64_t *indices, int64_t nnz,
+                   const int64_t *offsets, int64_t B, double *const *dG) {
+  tto_ttd t;
+  int e = tto_initd(&t, d, G, m, n, R);
+  if (e) return e;
+  if (nnz < 0 || (nnz > 0 && !indices) || (B > 0 && !grad_out) || !dG) return TTO_ERR_ARG;
+  for (int k = 0; k < d; ++k)
+    if (!dG[k]) return TTO_ERR_ARG;
+  e = tto_check_offsets(offsets, B, nnz);
+  if (e) return e;
+  size_t off[TTO_MAXD];
+  const size_t tot = tto_chain_offsets(&t, off);
+  double *T = (double *)malloc(sizeof(double) * tot);
+  double *dT = (double *)malloc(sizeof(double) * tot);
+  if (!T || !dT) { free(T); free(dT); return TTO_ERR_NOMEM; }
+  int err = TTO_OK;
+  int64_t ik[TTO_MAXD];
+  for (int64_t b = 0; b < B; ++b) {
+    const float *g = grad_out + b * t.D;
+    for (int64_t l = offsets[b]; l < offsets[b + 1]; ++l) {
+      const int64_t r = indices[l];
+      if (r < 0 || r >= t.M) { err = TTO_ERR_INDEX; continue; }
+      tto_splitd(&t, r, ik);
+      tto_chaind(&t, ik, T, off);
+      for (int j = 0; j < t.D; ++j) dT[off[d - 1] + j] = (double)g[j];
+      int N = t.D;
+      for (int k = d - 1; k >= 1; --k) {
+        const int Ra = t.R[k], nk = t.n[k], Rb = t.R[k + 1];
+        N /= nk;                                   /* rows of T_{k-1} */
+        const float *gk = t.G[k] + ik[k] * (int64_t)Ra * nk * Rb;
+        double *dgk = dG[k] + ik[k] * (int64_t)Ra * nk * Rb;
+        const double *A = T + off[k - 1], *dC = dT + off[k];
+        double *dA = dT + off[k - 1];
+        /* dG_k[i_k][a][j][b] += sum_J A[J][a] dC[(J, j)][b] */
+        for (int a = 0; a < Ra; ++a)
+          for (int j = 0; j < nk; ++j)
+            for (int bb = 0; bb < Rb; ++bb) {
+              double s = 0.0;
+              for (int J = 0; J < N; ++J) s += A[J * Ra + a] * dC[(J * nk + j) * Rb + bb];
+              dgk[(a * nk + j) * Rb + bb] += s;
+            }
+        /* dA[J][a] = sum_{j, b} dC[(J, j)][b] G_k[i_k][a][j][b] */
+        for (int J = 0; J < N; ++J)
+          for (int a = 0; a < Ra; ++a) {
+            double s = 0.0;
+            for (int j = 0; j < nk; ++j)
+              for (int bb = 0; bb < Rb; ++bb)
+                s += dC[(J * nk + j) * Rb + bb] * (double)gk[(a * nk + j) * Rb + bb];
+            dA[J * Ra + a] = s;
+          }
+      }
+      double *dg0 = dG[0] + ik[0] * (int64_t)t.n[0] * t.R[1];
+      for (int e2 = 0; e2 < t.n[0] * t.R[1]; ++e2) dg0[e2] += dT[off[0] + e2];
+    }
+  }
+  free(T);
+  free(dT);
+  return err;
+}

@@ -103,7 +103,7 @@ class TTInputs:
 
     @property
     def D(self) -> int:
-        return int(self.n[0] * self.n[1] * self.n[2])
+        return int(np.prod(self.n))
 
     @property
     def nnz(self) -> int:
@@ -143,9 +143,13 @@ def _draw_rows(rng: np.random.Generator, spec: tuple, N: int, nnz: int) -> np.nd
 
 
 def make_cores(m, n, R, seed: int, std: float) -> list:
+    """Seeded Gaussian cores [m_k][R_k][n_k][R_{k+1}] of a chain of len(m) cores
+    (R: the len(m) + 1 ranks, or one inner rank for three cores)."""
     rng = np.random.default_rng(seed)
-    Rf = (1, R[1], R[2], 1) if len(R) == 4 else (1, R, R, 1)
-    shapes = [(m[k], Rf[k], n[k], Rf[k + 1]) for k in range(3)]
+    d = len(m)
+    Rf = tuple(R) if not np.isscalar(R) else (1, R, R, 1)
+    assert len(Rf) == d + 1
+    shapes = [(m[k], Rf[k], n[k], Rf[k + 1]) for k in range(d)]
     return [(rng.standard_normal(s, dtype=np.float32) * np.float32(std)).astype(np.float32)
             for s in shapes]
 
@@ -180,7 +184,8 @@ def make_inputs(cfg: int, table: int = 0, num_bags: int | None = None,
 
 def make_custom(m, n, R, num_bags: int, max_len: int, seed: int, dist=("uniform",),
                 std: float = 0.5, with_grad: bool = True, empty_frac: float = 0.0) -> TTInputs:
-    """Seeded inputs of an arbitrary shape (edge cases, ragged tails, tiny pins)."""
+    """Seeded inputs of an arbitrary shape (edge cases, ragged tails, tiny pins); any number
+    of cores (len(m) = len(n) = len(R) - 1)."""
     m = tuple(int(v) for v in m)
     n = tuple(int(v) for v in n)
     R = tuple(int(v) for v in R)
@@ -192,12 +197,12 @@ def make_custom(m, n, R, num_bags: int, max_len: int, seed: int, dist=("uniform"
         lengths[rng.random(num_bags) < empty_frac] = 0
     offsets = np.zeros(num_bags + 1, dtype=np.int64)
     np.cumsum(lengths, out=offsets[1:])
-    M = m[0] * m[1] * m[2]
+    M = int(np.prod(m))
     indices = _draw_rows(rng, dist, M, int(offsets[-1]))
     grad = None
     if with_grad:
         grad = np.random.default_rng(seed + 2).standard_normal(
-            (num_bags, n[0] * n[1] * n[2]), dtype=np.float32)
+            (num_bags, int(np.prod(n))), dtype=np.float32)
     return TTInputs(m=m, n=n, R=R, cores=cores, indices=indices, offsets=offsets,
                     grad_out=grad, N=M)
 

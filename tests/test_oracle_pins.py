@@ -370,6 +370,82 @@ def test_pooling_variant_errors():
     assert e.value.code == oracle.TTO_ERR_ARG
 
 
+# ---------------------------------------------------------------- chains of d cores
+
+
+def _tt_svd_d(W, m, n):
+    """Exact (full-rank) TT-SVD of W viewed as modes (m_k*n_k), k = 1..d."""
+    d = len(m)
+    X = W.reshape(*m, *n)
+    X = X.transpose([a for k in range(d) for a in (k, d + k)])     # (m1, n1, m2, n2, ...)
+    cores, Rprev, rest = [], 1, X.reshape(m[0] * n[0], -1)
+    for k in range(d - 1):
+        U, S, Vt = np.linalg.svd(rest.reshape(Rprev * m[k] * n[k], -1), full_matrices=False)
+        Rk = U.shape[1]
+        cores.append(U.reshape(Rprev, m[k], n[k], Rk).transpose(1, 0, 2, 3))
+        rest = S[:, None] * Vt
+        Rprev = Rk
+    cores.append(rest.reshape(Rprev, m[-1], n[-1], 1).transpose(1, 0, 2, 3))
+    return cores, tuple([1] + [c.shape[3] for c in cores])
+
+
+def _materialize_d(cores, m, n):
+    """Dense table, contracting the chain from the last core backwards (the oracle goes
+    forwards)."""
+    G = [torch.tensor(np.asarray(c, dtype=np.float64)) for c in cores]
+    T = G[-1][:, :, :, 0]                       # [m_d][R][n_d]
+    for k in range(len(G) - 2, -1, -1):
+        T = torch.einsum("xaqb,ybr->xyaqr", G[k], T)
+        T = T.reshape(T.shape[0] * T.shape[1], T.shape[2], T.shape[3] * T.shape[4])
+    return T[:, 0, :]
+
+
+@pytest.mark.parametrize("m,n", [((2, 3, 2, 3), (2, 2, 1, 2)), ((3, 2, 2, 2, 2), (1, 2, 2, 1, 2))])
+def test_tt_svd_reconstructs_dense_table_d_cores(m, n):
+    rng = np.random.default_rng(61)
+    M, D = int(np.prod(m)), int(np.prod(n))
+    W = rng.standard_normal((M, D))
+    cores, R = _tt_svd_d(W, m, n)
+    out = oracle.forward_d([c.astype(np.float32) for c in cores], m, n, R, np.arange(M),
+                           np.arange(M + 1))
+    # the cores are rounded to fp32 on the way in: compare at fp32 resolution
+    assert np.abs(out - W).max() <= 1e-5 * np.abs(W).max()
+
+
+@pytest.mark.parametrize("shape", [((3, 2, 4, 2), (2, 3, 1, 2), (1, 3, 2, 4, 1)),
+                                   ((2, 2, 3, 2, 3), (1, 2, 2, 2, 1), (1, 2, 3, 2, 2, 1)),
+                                   ((5, 7), (3, 2), (1, 4, 1))])
+def test_d_cores_materialized_table_and_torch_autograd(shape):
+    m, n, R = shape
+    x = make_custom(m, n, R, num_bags=31, max_len=7, seed=63, empty_frac=0.15)
+    out = oracle.forward_d(x.cores, m, n, R, x.indices, x.offsets)
+    T = _materialize_d(x.cores, m, n).numpy()
+    ref = _embedding_bag(T, x.indices, x.offsets)
+    assert np.abs(out - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+    dG = oracle.backward_d(x.grad_out, x.cores, m, n, R, x.indices, x.offsets)
+    G = [torch.tensor(c, dtype=torch.float64, requires_grad=True) for c in x.cores]
+    Tt = G[-1][:, :, :, 0]
+    for k in range(len(G) - 2, -1, -1):
+        Tt = torch.einsum("xaqb,ybr->xyaqr", G[k], Tt)
+        Tt = Tt.reshape(Tt.shape[0] * Tt.shape[1], Tt.shape[2], Tt.shape[3] * Tt.shape[4])
+    o = torch.nn.functional.embedding_bag(torch.from_numpy(x.indices), Tt[:, 0, :],
+                                          torch.from_numpy(x.offsets[:-1]), mode="sum")
+    (o * torch.from_numpy(x.grad_out.astype(np.float64))).sum().backward()
+    for k in range(len(G)):
+        gr = G[k].grad.numpy()
+        assert np.abs(dG[k] - gr).max() <= 1e-12 * max(1.0, np.abs(gr).max()), k
+
+
+def test_three_cores_of_the_chain_equal_the_three_core_oracle():
+    x = _bwd_case()
+    a = oracle.forward_d(x.cores, x.m, x.n, x.R, x.indices, x.offsets)
+    assert np.array_equal(a, oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets))
+    b = oracle.backward_d(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets)
+    c = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets)
+    for k in range(3):
+        assert np.allclose(b[k], c[k], rtol=1e-13, atol=1e-13)
+
+
 # ---------------------------------------------------------------- grouping
 
 
