@@ -200,6 +200,32 @@ int tt_emb_sgd_ex(float* const cores[3], float* const core_grads[3], const int64
                   const int32_t n[3], const int32_t R[4], float lr, int zero_grads,
                   void* workspace, size_t ws_bytes, void* stream);
 
+/* Chains of d cores, 3 <= d <= 8 (tt_emb_sgd_d: 2 <= d <= 8): core k is
+ * float32 [m[k]][R[k]][n[k]][R[k+1]], R has d + 1 entries with R[0] = R[d] = 1,
+ * the row index splits mixed-radix over m (m[0] most significant) and the
+ * output position over n likewise; otherwise the contracts of tt_emb_forward,
+ * tt_emb_backward and tt_emb_sgd (`cores` and `core_grads` point to d HOST
+ * arrays of device pointers).  d = 3 is the three-core call.  For d >= 4 the
+ * leading d - 2 cores are contracted once per call into one core over all
+ * their index combinations (its (m[0]..m[d-3]) (n[0]..n[d-3]) R[d-2] floats
+ * live in the workspace; more than 2^28 of them, or m[0]..m[d-3] >= 2^31,
+ * return TT_EMB_ERR_UNSUPPORTED) and the three-core path runs on that core
+ * and the last two; the backward carries the merged core's gradient back to
+ * the leading cores.  With reuse_grouping != 0 the merged core of the last
+ * tt_emb_forward_d on this workspace is reused too (the cores are unchanged
+ * under that contract).  Size the workspace with tt_emb_workspace_bytes_d. */
+int tt_emb_workspace_bytes_d(int d, const int64_t* m, const int32_t* n, const int32_t* R,
+                             int64_t nnz, int64_t num_bags, size_t* bytes);
+int tt_emb_forward_d(int d, const float* const* cores, const int64_t* m, const int32_t* n,
+                     const int32_t* R, const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                     int64_t num_bags, float* out, void* workspace, size_t ws_bytes, void* stream);
+int tt_emb_backward_d(int d, const float* grad_out, const float* const* cores, const int64_t* m,
+                      const int32_t* n, const int32_t* R, const int64_t* indices, int64_t nnz,
+                      const int64_t* offsets, int64_t num_bags, float* const* core_grads,
+                      void* workspace, size_t ws_bytes, int reuse_grouping, void* stream);
+int tt_emb_sgd_d(int d, float* const* cores, float* const* core_grads, const int64_t* m,
+                 const int32_t* n, const int32_t* R, float lr, int zero_grads, void* stream);
+
 /* Synchronises `stream`, then reads the workspace status word written by the
  * kernels of the calls enqueued so far.  *device_status receives the raw
  * bit set (1 = index out of range, 2 = bad offsets, 4 = timeout).  Returns

@@ -32,7 +32,8 @@ _POOLING = {"sum": TT_EMB_POOL_SUM, "mean": TT_EMB_POOL_MEAN}
 
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
             "tt_emb_forward_ex", "tt_emb_backward_ex", "tt_emb_split", "tt_emb_sgd_ex",
-            "tt_emb_forward_tables",
+            "tt_emb_forward_tables", "tt_emb_workspace_bytes_d", "tt_emb_forward_d",
+            "tt_emb_backward_d", "tt_emb_sgd_d",
             "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_profile_start",
             "tt_emb_profile_stop", "tt_emb_profile_read", "tt_emb_forward_static",
             "tt_emb_version")
@@ -84,6 +85,11 @@ def lib():
                                         P, P, SZ, P]
         L.tt_emb_split.argtypes = [P, P, P, P, P, SZ, P]
         L.tt_emb_forward_tables.argtypes = [ctypes.c_int, P, P]
+        C = ctypes.c_int
+        L.tt_emb_workspace_bytes_d.argtypes = [C, P, P, P, I64, I64, ctypes.POINTER(SZ)]
+        L.tt_emb_forward_d.argtypes = [C, P, P, P, P, P, I64, P, I64, P, P, SZ, P]
+        L.tt_emb_backward_d.argtypes = [C, P, P, P, P, P, P, I64, P, I64, P, P, SZ, C, P]
+        L.tt_emb_sgd_d.argtypes = [C, P, P, P, P, P, ctypes.c_float, C, P]
         L.tt_emb_sgd_ex.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, P, SZ, P]
         L.tt_emb_backward_ex.argtypes = [P, P, P, P, P, P, I64, P, I64, P, ctypes.c_int, P, P, P,
                                          SZ, ctypes.c_int, P]
@@ -226,6 +232,56 @@ def tt_emb_forward_tables(tables, stream=None):
         e.ws_bytes = t["workspace"].numel()
     _check(lib().tt_emb_forward_tables(len(tables), ctypes.cast(arr, ctypes.c_void_p),
                                        _stream(stream)), "tt_emb_forward_tables")
+
+
+def _shape_d(m, n, R):
+    d = len(m)
+    if len(n) != d or len(R) != d + 1:
+        raise ValueError("a chain of d cores needs d row factors, d output factors, d + 1 ranks")
+    return (d, (ctypes.c_int64 * d)(*[int(v) for v in m]), (ctypes.c_int32 * d)(*[int(v) for v in n]),
+            (ctypes.c_int32 * (d + 1))(*[int(v) for v in R]))
+
+
+def _ptrs_d(ts, name):
+    return (ctypes.c_void_p * len(ts))(*[_dev(t, torch.float32, f"{name}[{k}]").value
+                                         for k, t in enumerate(ts)])
+
+
+def tt_emb_workspace_bytes_d(m, n, R, nnz: int, num_bags: int) -> int:
+    out = ctypes.c_size_t(0)
+    d, m_, n_, R_ = _shape_d(m, n, R)
+    _check(lib().tt_emb_workspace_bytes_d(d, m_, n_, R_, int(nnz), int(num_bags), ctypes.byref(out)),
+           "tt_emb_workspace_bytes_d")
+    return int(out.value)
+
+
+def tt_emb_forward_d(cores, m, n, R, indices, offsets, out, workspace, stream=None):
+    d, m_, n_, R_ = _shape_d(m, n, R)
+    _check(lib().tt_emb_forward_d(d, _ptrs_d(cores, "cores"), m_, n_, R_,
+                                  _dev(indices, torch.int64, "indices"), indices.numel(),
+                                  _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
+                                  _dev(out, torch.float32, "out"),
+                                  _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                  _stream(stream)), "tt_emb_forward_d")
+
+
+def tt_emb_backward_d(grad_out, cores, m, n, R, indices, offsets, core_grads, workspace,
+                      reuse_grouping: bool = True, stream=None):
+    d, m_, n_, R_ = _shape_d(m, n, R)
+    _check(lib().tt_emb_backward_d(d, _dev(grad_out, torch.float32, "grad_out"),
+                                   _ptrs_d(cores, "cores"), m_, n_, R_,
+                                   _dev(indices, torch.int64, "indices"), indices.numel(),
+                                   _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
+                                   _ptrs_d(core_grads, "core_grads"),
+                                   _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                   int(bool(reuse_grouping)), _stream(stream)), "tt_emb_backward_d")
+
+
+def tt_emb_sgd_d(cores, core_grads, m, n, R, lr: float, zero_grads: bool = False, stream=None):
+    d, m_, n_, R_ = _shape_d(m, n, R)
+    _check(lib().tt_emb_sgd_d(d, _ptrs_d(cores, "cores"), _ptrs_d(core_grads, "core_grads"), m_, n_,
+                              R_, ctypes.c_float(lr), int(bool(zero_grads)), _stream(stream)),
+           "tt_emb_sgd_d")
 
 
 def tt_emb_split(cores, m, n, R, workspace, stream=None):

@@ -181,6 +181,77 @@ static int check_cores(const float* const cores[3]) {
   return TT_EMB_OK;
 }
 
+
+// A chain of 4 <= d <= 8 cores, its three-core view (the leading d - 2 cores
+// merged: m' = m_0 .. m_{d-3}, n' likewise, rank R_{d-2}) and the byte offsets
+// of its workspace parts: the three-core workspace first (its control block,
+// and so the status word, at the workspace base), then the merged cores
+// C_1 .. C_{d-3} and their gradients.
+struct ChainPlan {
+  ChainShape c;
+  int64_t m3[3];
+  int32_t n3[3], R3[4];
+  size_t merged[kMaxCores], dmerged[kMaxCores], count[kMaxCores], ws3, total;
+};
+
+static int chain_plan(int d, const int64_t* m, const int32_t* n, const int32_t* R, int64_t nnz,
+                      int64_t num_bags, ChainPlan* p) {
+  if (d < 4 || d > kMaxCores || !m || !n || !R) return TT_EMB_ERR_ARG;
+  if (R[0] != 1 || R[d] != 1) return TT_EMB_ERR_ARG;
+  ChainShape& c = p->c;
+  c.d = d;
+  c.R[0] = 1;
+  for (int k = 0; k < d; ++k) {
+    if (m[k] < 1 || m[k] >= (1ll << 31) || n[k] < 1 || R[k + 1] < 1) return TT_EMB_ERR_ARG;
+    c.m[k] = m[k];
+    c.n[k] = n[k];
+    c.R[k + 1] = R[k + 1];
+  }
+  // merged cores: C_k holds (m_0 .. m_k)(n_0 .. n_k) R_{k+1} floats, at most 2^28
+  unsigned __int128 mm = (unsigned __int128)m[0];
+  int64_t nn = n[0];
+  for (int k = 1; k <= d - 3; ++k) {
+    mm *= (unsigned __int128)m[k];
+    nn *= n[k];
+    if (mm >= ((unsigned __int128)1 << 31) || nn > (1 << 20)) return TT_EMB_ERR_UNSUPPORTED;
+    const unsigned __int128 cnt = mm * (unsigned __int128)nn * (unsigned __int128)R[k + 1];
+    if (cnt > ((unsigned __int128)1 << 28)) return TT_EMB_ERR_UNSUPPORTED;
+    p->count[k] = (size_t)cnt;
+  }
+  p->m3[0] = (int64_t)mm;
+  p->m3[1] = m[d - 2];
+  p->m3[2] = m[d - 1];
+  p->n3[0] = (int32_t)nn;
+  p->n3[1] = n[d - 2];
+  p->n3[2] = n[d - 1];
+  p->R3[0] = 1;
+  p->R3[1] = R[d - 2];
+  p->R3[2] = R[d - 1];
+  p->R3[3] = 1;
+  size_t b3 = 0;
+  const int rc = tt_emb_workspace_bytes(p->m3, p->n3, p->R3, nnz, num_bags, &b3);
+  if (rc) return rc;
+  p->ws3 = b3;
+  size_t off = align_up(b3, 256);
+  for (int k = 1; k <= d - 3; ++k) {
+    p->merged[k] = off;
+    off = align_up(off + 4 * p->count[k], 256);
+  }
+  for (int k = 1; k <= d - 3; ++k) {
+    p->dmerged[k] = off;
+    off = align_up(off + 4 * p->count[k], 256);
+  }
+  p->total = off;
+  return TT_EMB_OK;
+}
+
+static int check_cores_d(int d, const float* const* cores) {
+  if (!cores) return TT_EMB_ERR_ARG;
+  for (int k = 0; k < d; ++k)
+    if (!cores[k] || !aligned(cores[k], 16)) return TT_EMB_ERR_ARG;
+  return TT_EMB_OK;
+}
+
 }  // namespace tt
 
 using namespace tt;
@@ -404,6 +475,122 @@ int tt_emb_sgd_ex(float* const cores[3], float* const core_grads[3], const int64
   if (rc) return rc;
   const WS w = make_ws(workspace, L);
   return launch_sgd(cores, core_grads, s, lr, zero_grads, &w, (cudaStream_t)stream);
+}
+
+int tt_emb_workspace_bytes_d(int d, const int64_t* m, const int32_t* n, const int32_t* R,
+                             int64_t nnz, int64_t num_bags, size_t* bytes) {
+  if (d == 3) return tt_emb_workspace_bytes(m, n, R, nnz, num_bags, bytes);
+  if (!bytes) return TT_EMB_ERR_ARG;
+  ChainPlan p;
+  const int rc = chain_plan(d, m, n, R, nnz, num_bags, &p);
+  if (rc) return rc;
+  *bytes = p.total;
+  return TT_EMB_OK;
+}
+
+int tt_emb_forward_d(int d, const float* const* cores, const int64_t* m, const int32_t* n,
+                     const int32_t* R, const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                     int64_t num_bags, float* out, void* workspace, size_t ws_bytes, void* stream) {
+  if (d == 3)
+    return tt_emb_forward(cores, m, n, R, indices, nnz, offsets, num_bags, out, workspace, ws_bytes,
+                          stream);
+  if (nnz < 0 || nnz >= (1ll << 30) || num_bags < 0) return TT_EMB_ERR_ARG;
+  ChainPlan p;
+  int rc = chain_plan(d, m, n, R, nnz, num_bags, &p);
+  if (rc) return rc;
+  rc = check_cores_d(d, cores);
+  if (rc) return rc;
+  if (!workspace || !aligned(workspace, 256)) return TT_EMB_ERR_ARG;
+  if (ws_bytes < p.total) return TT_EMB_ERR_WORKSPACE;
+  char* b = static_cast<char*>(workspace);
+  float* merged[kMaxCores] = {nullptr};
+  for (int k = 1; k <= d - 3; ++k) merged[k] = reinterpret_cast<float*>(b + p.merged[k]);
+  const float* cores3[3] = {merged[d - 3], cores[d - 2], cores[d - 1]};
+  // argument checks of the three-core call first (nothing is enqueued on error)
+  Shape s3;
+  rc = shape_from_args(p.m3, p.n3, p.R3, &s3);
+  if (rc) return rc;
+  Layout L;
+  rc = check_batch(s3, indices, nnz, offsets, num_bags, b, p.ws3, &L);
+  if (rc) return rc;
+  rc = launch_merge_chain(p.c, cores, merged, (cudaStream_t)stream);
+  if (rc) return rc;
+  return tt_emb_forward(cores3, p.m3, p.n3, p.R3, indices, nnz, offsets, num_bags, out, b, p.ws3,
+                        stream);
+}
+
+int tt_emb_backward_d(int d, const float* grad_out, const float* const* cores, const int64_t* m,
+                      const int32_t* n, const int32_t* R, const int64_t* indices, int64_t nnz,
+                      const int64_t* offsets, int64_t num_bags, float* const* core_grads,
+                      void* workspace, size_t ws_bytes, int reuse_grouping, void* stream) {
+  if (d == 3)
+    return tt_emb_backward(grad_out, cores, m, n, R, indices, nnz, offsets, num_bags, core_grads,
+                           workspace, ws_bytes, reuse_grouping, stream);
+  if (nnz < 0 || nnz >= (1ll << 30) || num_bags < 0) return TT_EMB_ERR_ARG;
+  ChainPlan p;
+  int rc = chain_plan(d, m, n, R, nnz, num_bags, &p);
+  if (rc) return rc;
+  rc = check_cores_d(d, cores);
+  if (rc) return rc;
+  rc = check_cores_d(d, core_grads);
+  if (rc) return rc;
+  if (!workspace || !aligned(workspace, 256)) return TT_EMB_ERR_ARG;
+  if (ws_bytes < p.total) return TT_EMB_ERR_WORKSPACE;
+  char* b = static_cast<char*>(workspace);
+  float* merged[kMaxCores] = {nullptr};
+  float* dmerged[kMaxCores] = {nullptr};
+  for (int k = 1; k <= d - 3; ++k) {
+    merged[k] = reinterpret_cast<float*>(b + p.merged[k]);
+    dmerged[k] = reinterpret_cast<float*>(b + p.dmerged[k]);
+  }
+  Shape s3;
+  rc = shape_from_args(p.m3, p.n3, p.R3, &s3);
+  if (rc) return rc;
+  Layout L;
+  rc = check_batch(s3, indices, nnz, offsets, num_bags, b, p.ws3, &L);
+  if (rc) return rc;
+  if (num_bags > 0 && (!grad_out || !aligned(grad_out, 16))) return TT_EMB_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the merged cores of the forward stand when the grouping is reused (the
+  // cores are unchanged under that contract); otherwise merge again
+  if (!reuse_grouping) {
+    rc = launch_merge_chain(p.c, cores, merged, st);
+    if (rc) return rc;
+  }
+  for (int k = 1; k <= d - 3; ++k)
+    if (cudaMemsetAsync(dmerged[k], 0, 4 * p.count[k], st) != cudaSuccess) return TT_EMB_ERR_CUDA;
+  const float* cores3[3] = {merged[d - 3], cores[d - 2], cores[d - 1]};
+  float* grads3[3] = {dmerged[d - 3], core_grads[d - 2], core_grads[d - 1]};
+  rc = tt_emb_backward(grad_out, cores3, p.m3, p.n3, p.R3, indices, nnz, offsets, num_bags, grads3,
+                       b, p.ws3, reuse_grouping, stream);
+  if (rc) return rc;
+  return launch_unmerge_chain(p.c, cores, merged, dmerged, core_grads, st);
+}
+
+int tt_emb_sgd_d(int d, float* const* cores, float* const* core_grads, const int64_t* m,
+                 const int32_t* n, const int32_t* R, float lr, int zero_grads, void* stream) {
+  if (d < 2 || d > kMaxCores || !m || !n || !R || !cores || !core_grads) return TT_EMB_ERR_ARG;
+  if (R[0] != 1 || R[d] != 1) return TT_EMB_ERR_ARG;
+  int rc = check_cores_d(d, cores);
+  if (rc) return rc;
+  rc = check_cores_d(d, core_grads);
+  if (rc) return rc;
+  for (int k = 0; k < d; ++k)
+    if (m[k] < 1 || n[k] < 1 || R[k + 1] < 1) return TT_EMB_ERR_ARG;
+  for (int k0 = 0; k0 < d; k0 += 3) {
+    float* G[3];
+    float* dG[3];
+    int64_t cnt[3];
+    for (int u = 0; u < 3; ++u) {
+      const int k = k0 + u < d ? k0 + u : k0;
+      G[u] = cores[k];
+      dG[u] = core_grads[k];
+      cnt[u] = k0 + u < d ? m[k] * (int64_t)R[k] * n[k] * R[k + 1] : 0;
+    }
+    rc = launch_sgd_counts(G, dG, cnt, lr, zero_grads, (cudaStream_t)stream);
+    if (rc) return rc;
+  }
+  return TT_EMB_OK;
 }
 
 int tt_emb_get_error(const void* workspace, void* stream, int* device_status) {

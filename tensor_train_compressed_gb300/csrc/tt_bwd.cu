@@ -1240,6 +1240,31 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
   return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
 }
 
+// Plain SGD over three arrays of the given lengths (the cores of a chain are
+// updated three at a time).
+int launch_sgd_counts(float* const G[3], float* const dG[3], const int64_t counts[3], float lr,
+                      int zero_grads, cudaStream_t st) {
+  SgdArgs a;
+  a.start[0] = 0;
+  for (int k = 0; k < 3; ++k) {
+    a.G[k] = G[k];
+    a.dG[k] = dG[k];
+    a.count[k] = counts[k];
+    a.start[k + 1] = a.start[k] + ceil_div(counts[k], 4);
+    a.hi[k] = a.lo[k] = nullptr;
+  }
+  a.lr = lr;
+  a.zero = zero_grads ? 1 : 0;
+  a.g3th = a.g3tl = nullptr;
+  a.R2 = 1;
+  if (a.start[3] == 0) return TT_EMB_OK;
+  int grid = (int)ceil_div(a.start[3], 4 * 256);
+  if (grid > sm_count() * 4) grid = sm_count() * 4;
+  if (grid < 1) grid = 1;
+  TT_TIMED("k_sgd", st, (k_sgd<false><<<grid, 256, 0, st>>>(a)));
+  return cudaGetLastError() == cudaSuccess ? TT_EMB_OK : TT_EMB_ERR_CUDA;
+}
+
 int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, float lr,
                int zero_grads, const WS* ws, cudaStream_t st) {
   SgdArgs a;

@@ -27,6 +27,7 @@ constexpr int kSSlice = 64;                 // sorted positions per warp in the 
 constexpr int kSCta = 8 * kSSlice;          // sorted positions per CTA in the D = 128 grad gather
 constexpr int kMaxSmemFloats = 53248;       // 208 KB of shared memory per CTA
 constexpr int kMaxTables = 8;               // tables of one tt_emb_forward_tables call
+constexpr int kMaxCores = 8;                // cores of one chain (tt_emb_*_d)
 
 // status word bits
 constexpr uint32_t kStIndex = 1u;
@@ -328,6 +329,22 @@ int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratc
 int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                  int rows_per_chunk, cudaStream_t st);
+// chains of d > 3 cores (tt_chain.cu): the leading d - 2 cores merged into one
+struct ChainShape {
+  int d;
+  int64_t m[kMaxCores];
+  int n[kMaxCores];
+  int R[kMaxCores + 1];
+};
+// merged[k] = C_k = C_{k-1} (x) G_k for k = 1 .. d-3 (C_0 = cores[0])
+int launch_merge_chain(const ChainShape& c, const float* const* cores, float* const* merged,
+                       cudaStream_t st);
+// from dmerged[d-3] (gradient of the merged core) back into dmerged[k] (zeroed
+// by the caller) and core_grads[0 .. d-3] (accumulated)
+int launch_unmerge_chain(const ChainShape& c, const float* const* cores, const float* const* merged,
+                         float* const* dmerged, float* const* core_grads, cudaStream_t st);
+int launch_sgd_counts(float* const G[3], float* const dG[3], const int64_t counts[3], float lr,
+                      int zero_grads, cudaStream_t st);
 // bag of every lookup into the workspace (tt_bwd.cu); the forward's pooling
 // writes it too
 int launch_bag_ids(const WS& w, const int64_t* offsets, int64_t num_bags, int64_t nnz,

@@ -167,3 +167,23 @@ def test_forward_tables_argument_checks(L):
     arr[1].workspace = fake + need + 256
     arr[1].n[1] = 8
     assert L.tt_emb_forward_tables(2, ptr, None) == tte.TT_EMB_ERR_ARG   # other n
+
+
+def test_chain_workspace_and_shape_checks(L):
+    # four cores: the three-core view of (10, 12, 20, 30) x (2, 2, 8, 4) is (120, 20, 30) x (4, 8, 4)
+    m, n, R = (10, 12, 20, 30), (2, 2, 8, 4), (1, 16, 32, 32, 1)
+    b4 = tte.tt_emb_workspace_bytes_d(m, n, R, 1000, 100)
+    b3 = tte.tt_emb_workspace_bytes((120, 20, 30), (4, 8, 4), (1, 32, 32, 1), 1000, 100)
+    # the merged core (120 x 4 x 32 floats) and its gradient come on top
+    assert b4 >= b3 + 2 * 120 * 4 * 32 * 4
+    assert tte.tt_emb_workspace_bytes_d((10, 20, 30), (4, 8, 4), (1, 32, 32, 1), 10, 2) == \
+        tte.tt_emb_workspace_bytes((10, 20, 30), (4, 8, 4), (1, 32, 32, 1), 10, 2)
+    with pytest.raises(tte.TTEmbError) as e:      # R[0] != 1
+        tte.tt_emb_workspace_bytes_d(m, n, (2, 16, 32, 32, 1), 10, 1)
+    assert e.value.code == tte.TT_EMB_ERR_ARG
+    with pytest.raises(tte.TTEmbError) as e:      # merged core beyond 2^28 floats
+        tte.tt_emb_workspace_bytes_d((1000, 1000, 100, 10, 10), (4, 4, 4, 2, 2),
+                                     (1, 32, 32, 32, 32, 1), 10, 1)
+    assert e.value.code == tte.TT_EMB_ERR_UNSUPPORTED
+    with pytest.raises(ValueError):
+        tte.tt_emb_workspace_bytes_d(m, n, R[:-1], 10, 1)
