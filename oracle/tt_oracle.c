@@ -6,22 +6,21 @@
  * What it computes (plain definitions, evaluated naively in fp64):
  *
  *  - A table of M = m1*m2*m3 rows of width D = n1*n2*n3 is stored as three
- *    TT cores ("a sequence of smaller tensor cores", FlowTT summary card,
- *    problem statement; "a sequence of matrix products", TT-Rec press article,
- *    method paragraph).  Core k is float32 [m_k][R_{k-1}][n_k][R_k] with
+ *    TT cores (a table replaced by a series of small tensor cores whose
+ *    product gives the rows: FlowTT summary card, problem statement; TT-Rec
+ *    press article, method paragraph).  Core k is float32 [m_k][R_{k-1}][n_k][R_k] with
  *    R_0 = R_3 = 1.
  *  - Row index r is split mixed-radix with i1 most significant:
  *    r = (i1*m2 + i2)*m3 + i3.  Output position j = (j1*n2 + j2)*n3 + j3.
- *  - A lookup is the chain of contractions over the cores ("an input index is
- *    processed by sequentially contracting a chain of small TT cores", FlowTT
- *    summary card, problem statement):
+ *  - A lookup is the chain of contractions over the cores, one core after
+ *    the other (FlowTT summary card, problem statement):
  *        T1  = G1[i1]                (n1 x R1)
  *        T12 = T1 . G2[i2]           (n1 x n2*R2)  ==  (n1*n2 x R2)
  *        row = T12 . G3[i3]          (n1*n2 x n3)  ==  D values
  *    i.e. row(r)[j] = sum_{a,b} G1[i1][0][j1][a] G2[i2][a][j2][b] G3[i3][b][j3][0].
  *  - Bags are CSR offsets (B+1 entries); out[b] = sum of the rows of the
- *    lookups offsets[b] .. offsets[b+1]-1 (the "EmbeddingBag" of TT-Rec,
- *    abstract).  Empty bags give zero rows.
+ *    lookups offsets[b] .. offsets[b+1]-1 (the embedding-bag operator of
+ *    TT-Rec, abstract).  Empty bags give zero rows.
  *  - The two other pooling rules of an embedding bag: a weighted sum, each
  *    row scaled by its lookup's per-sample weight w[l], and the mean, the sum
  *    divided by the bag's number of lookups (an empty bag stays zero).  The
@@ -31,9 +30,9 @@
  *    core, accumulated lookup by lookup (training latency, FlowTT abstract).
  *  - SGD: G <- G - lr*dG.
  *  - Grouping reference: lookups stably sorted by the key (i2, i1, i3), then
- *    unique runs of rows and of (i1, i2) prefixes ("prefix-based index
- *    grouping ... inputs sharing high-order TT core indices", FlowTT summary
- *    card, key innovations).
+ *    unique runs of rows and of (i1, i2) prefixes (lookups that share the
+ *    leading core indices grouped together, FlowTT summary card, key
+ *    innovations).
  */
 #include <pthread.h>
 #include <stdint.h>
@@ -446,9 +445,9 @@ int tto_group(const int64_t *indices, int64_t nnz, const int64_t *m, int32_t *pe
 
 /* ---------------- d cores ----------------
  *
- * The same definitions for a chain of d >= 2 cores (the pages contract "a
- * chain of small TT cores", FlowTT summary card, problem statement; three
- * cores is the case above).  Core k (0-based) is float32
+ * The same definitions for a chain of d >= 2 cores (the pages contract a
+ * chain of cores without fixing their number, FlowTT summary card, problem
+ * statement; three cores is the case above).  Core k (0-based) is float32
  * [m_k][R_k][n_k][R_{k+1}] with R_0 = R_d = 1; the row index splits
  * mixed-radix with i_0 most significant, the output position likewise with
  * j_0 most significant.  Per lookup the chain T_0 = G_0[i_0] (n_0 x R_1),

@@ -1,9 +1,9 @@
 // Chains of d > 3 cores.
 //
-// A chain of d cores (a lookup contracts "a chain of small TT cores", FlowTT
-// summary card, problem statement) is run as a three-core table: the leading
-// d - 2 cores are contracted once per call into one core over all their index
-// combinations, C[(i_0 .. i_{d-3})][(j_0 .. j_{d-3})][r] (mixed radix, i_0 and
+// A chain of d cores (a lookup contracts one core after the other, their
+// number left open: FlowTT summary card, problem statement) is run as a
+// three-core table: the leading d - 2 cores are contracted once per call into
+// one core over all their index combinations, C[(i_0 .. i_{d-3})][(j_0 .. j_{d-3})][r] (mixed radix, i_0 and
 // j_0 most significant, so the row index and the output position are those of
 // the chain), and the three-core path (grouping, tensor-core chunk kernels,
 // pooling) takes (C, G_{d-2}, G_{d-1}).  The backward walks the merge back:
@@ -126,7 +126,7 @@ int launch_unmerge_chain(const ChainShape& c, const float* const* cores, const f
   int nas[kMaxCores];
   mas[0] = c.m[0];
   nas[0] = c.n[0];
-  for (int k = 1; k < c.d; ++k) {
+  for (int k = 1; k <= c.d - 3; ++k) {   // bounded by the merged core's limits
     mas[k] = mas[k - 1] * c.m[k];
     nas[k] = nas[k - 1] * c.n[k];
   }
