@@ -165,35 +165,39 @@ __global__ void __launch_bounds__(256) k_s_gather(WS w, const float* __restrict_
 }
 
 // S[x] with the partial sums of rows that cross warp boundaries merged inside
-// the CTA: a CTA covers kSCta = 8 x kSSlice sorted positions; each warp sums
-// the runs of its kSSlice positions (8 output-gradient rows in flight), stores
+// the CTA: a CTA covers 8 x span sorted positions (span, at most 32 x
+// kGatherBatches, chosen per batch so that the grid fills whole waves); each
+// warp sums the runs of its span positions (8 output-gradient rows in flight), stores
 // the runs that start and end inside its range, and leaves its first and last
 // run in shared memory; one warp then merges those in position order and
 // stores each merged row, or adds it with float atomics (into a row zeroed by
 // k_s_zero) when the row also crosses the CTA's range.  D = 128.
-__device__ __forceinline__ void s_merge_flush(const WS& w, int32_t u, int64_t K0, const float4& m,
-                                              int lane) {
+__device__ __forceinline__ void s_merge_flush(const WS& w, int32_t u, int64_t K0, int64_t K1,
+                                              const float4& m, int lane) {
   const int32_t s0 = w.row_start[u], s1 = w.row_start[u + 1];
   float4* dst = reinterpret_cast<float4*>(w.rowbuf) + (int64_t)u * 32 + lane;
-  if (s0 < K0 || s1 > K0 + kSCta) atomicAdd(dst, m);
+  if (s0 < K0 || s1 > K1) atomicAdd(dst, m);
   else *dst = m;
 }
+
+constexpr int kGatherBatches = 3;   // batches of 32 sorted positions per warp, at most
 
 // D = 128: every lane owns one float4 column of the rows.
 template <int MODE>
 __global__ void __launch_bounds__(256, MODE == kPoolSum ? 4 : 3) k_s_gather_cta(WS w, const float* __restrict__ grad_out,
                                                          int64_t B, const float* __restrict__ psw,
                                                          const int64_t* __restrict__ offsets,
-                                                         int64_t nnz) {
+                                                         int64_t nnz, int span) {
   __shared__ float4 part[8][2][32];
   __shared__ int part_u[8][2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nv = w.ctl->n_valid;
-  const int64_t K0 = (int64_t)blockIdx.x * kSCta;
+  const int64_t cspan = 8 * (int64_t)span;
+  const int64_t K0 = (int64_t)blockIdx.x * cspan;
   if (K0 >= nv) return;                                // uniform over the CTA
-  const int64_t K1 = K0 + kSCta < nv ? K0 + kSCta : nv;
-  const int64_t k0 = K0 + (int64_t)warp * kSSlice;
-  const int64_t k1 = k0 + kSSlice < K1 ? k0 + kSSlice : K1;
+  const int64_t K1 = K0 + cspan < nv ? K0 + cspan : nv;
+  const int64_t k0 = K0 + (int64_t)warp * span;
+  const int64_t k1 = k0 + span < K1 ? k0 + span : K1;
   const float4* g4 = reinterpret_cast<const float4*>(grad_out);
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   float4 acc = z4;
@@ -210,27 +214,31 @@ __global__ void __launch_bounds__(256, MODE == kPoolSum ? 4 : 3) k_s_gather_cta(
       reinterpret_cast<float4*>(w.rowbuf)[(int64_t)cur * 32 + lane] = acc;
     }
   };
-  // the (unique row, bag, factor) of both 32-position batches of the slice,
+  // the (unique row, bag, factor) of all 32-position batches of the slice,
   // loaded together: two dependent round trips for the whole slice
-  static_assert(kSSlice == 64, "two batches of 32 sorted positions per warp");
-  int32_t bu[2] = {-1, -1}, bbag[2] = {0, 0}, bl[2] = {-1, -1};
-  float bc[2] = {1.f, 1.f};
+  int32_t bu[kGatherBatches], bbag[kGatherBatches], bl[kGatherBatches];
+  float bc[kGatherBatches];
 #pragma unroll
-  for (int h = 0; h < 2; ++h)
+  for (int h = 0; h < kGatherBatches; ++h) {
+    bu[h] = -1;
+    bbag[h] = 0;
+    bl[h] = -1;
+    bc[h] = 1.f;
     if (k0 + 32 * h + lane < k1) bl[h] = w.perm[k0 + 32 * h + lane];
+  }
 #pragma unroll
-  for (int h = 0; h < 2; ++h)
+  for (int h = 0; h < kGatherBatches; ++h)
     if (bl[h] >= 0) {
       bu[h] = w.uid[bl[h]];
       bbag[h] = w.bag_of[bl[h]];
     }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < kGatherBatches; ++h) {
     bbag[h] = bbag[h] < 0 ? 0 : (bbag[h] >= B ? (int32_t)(B - 1) : bbag[h]);
     if (bl[h] >= 0) bc[h] = lookup_factor<MODE>(psw, offsets, nnz, bl[h], bbag[h]);
   }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < kGatherBatches; ++h) {
     const int64_t kb = k0 + 32 * h;
     if (kb >= k1) break;
     const int cnt = (int)(k1 - kb < 32 ? k1 - kb : 32);
@@ -289,13 +297,13 @@ __global__ void __launch_bounds__(256, MODE == kPoolSum ? 4 : 3) k_s_gather_cta(
         const int32_t u = part_u[ww][e];
         if (u < 0) continue;
         if (u != mu) {
-          if (mu >= 0) s_merge_flush(w, mu, K0, m, lane);
+          if (mu >= 0) s_merge_flush(w, mu, K0, K0 + cspan, m, lane);
           mu = u;
           m = z4;
         }
         f4add(m, part[ww][e][lane]);
       }
-    if (mu >= 0) s_merge_flush(w, mu, K0, m, lane);
+    if (mu >= 0) s_merge_flush(w, mu, K0, K0 + cspan, m, lane);
   }
 }
 
@@ -1152,6 +1160,20 @@ static void launch_s_gather(const Shape& s, const Layout& L, const WS& w, const 
                             int64_t nnz, int64_t num_bags, const int64_t* offsets, const float* psw,
                             const SplitArgs& sp, int reuse, cudaStream_t st) {
   const bool cta_gather = s.D == 128;
+  // CTA gather: positions per warp so that the grid fills whole waves of the
+  // resident CTAs (a partial last wave would run a few CTAs on an idle GPU)
+  static int gather_res = 0;
+  if (gather_res == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_s_gather_cta<MODE>, 256, 0) !=
+            cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    gather_res = per_sm * sm_count();
+  }
+  const int64_t per_wave = 8ll * 32 * kGatherBatches * gather_res;
+  const int64_t waves = nnz > per_wave ? ceil_div(nnz, per_wave) : 1;
+  int span = (int)ceil_div(nnz, 8ll * gather_res * waves);
+  if (span < 1) span = 1;
   static int zero_wave = 0;
   if (zero_wave == 0) {
     int per_sm = 0;
@@ -1164,11 +1186,11 @@ static void launch_s_gather(const Shape& s, const Layout& L, const WS& w, const 
   int grid = want < zero_wave ? (int)want : zero_wave;
   if (grid < split_grid(sp)) grid = split_grid(sp);
   if (grid < 1) grid = 1;
-  TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D, cta_gather ? kSCta : kSSlice,
+  TT_TIMED("k_s_zero", st, (k_s_zero<<<grid, 256, 0, st>>>(w, s.D, cta_gather ? 8 * span : kSSlice,
                                                              L.rowbuf_rows, sp, reuse)));
   if (cta_gather) {
-    TT_TIMED("k_s_gather", st, (k_s_gather_cta<MODE><<<(int)ceil_div(nnz, kSCta), 256, 0, st>>>(
-                                   w, grad_out, num_bags, psw, offsets, nnz)));
+    TT_TIMED("k_s_gather", st, (k_s_gather_cta<MODE><<<(int)ceil_div(nnz, 8ll * span), 256, 0, st>>>(
+                                   w, grad_out, num_bags, psw, offsets, nnz, span)));
   } else {
     const int64_t slices = ceil_div(nnz, kSSlice);
     TT_TIMED("k_s_gather", st, (k_s_gather<MODE><<<(int)ceil_div(slices, 8), 256, 0, st>>>(

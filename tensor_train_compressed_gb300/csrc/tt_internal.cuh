@@ -24,7 +24,6 @@ constexpr int kScanThreads = 256;
 constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;
 constexpr int kSSlice = 64;                 // sorted positions per warp in the grad gather
-constexpr int kSCta = 8 * kSSlice;          // sorted positions per CTA in the D = 128 grad gather
 constexpr int kMaxSmemFloats = 53248;       // 208 KB of shared memory per CTA
 constexpr int kMaxTables = 8;               // tables of one tt_emb_forward_tables call
 constexpr int kMaxCores = 8;                // cores of one chain (tt_emb_*_d)
