@@ -1311,7 +1311,7 @@ int launch_sgd(float* const cores[3], float* const grads[3], const Shape& s, flo
   a.g3tl = split ? ws->g3tl : nullptr;
   a.R2 = s.R2;
   int grid = (int)ceil_div(a.start[3], 4 * 256);
-  if (grid > sm_count() * 4) grid = sm_count() * 4;
+  if (grid > sm_count() * 8) grid = sm_count() * 8;   // one pass of four float4 per thread
   if (grid < 1) grid = 1;
   if (split) {
     TT_TIMED("k_sgd", st, (k_sgd<true><<<grid, 256, 0, st>>>(a)));
