@@ -916,6 +916,13 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
         rs = max(a.w.pair_row_start[p0 + lane], x0) - x0;
       }
       const int i2 = a.w.pair_i2[p0];
+      // the first batch's S rows: every load issued now, into registers (lane =
+      // (j1, j2) float4), stored once the stage is free
+      float4 sv[C::RB];
+#pragma unroll
+      for (int u = 0; u < C::RB; ++u)
+        sv[u] = u < nb ? __ldg(reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)(x0 + u) * C::D) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
       ChunkDesc dn{};
       const int cn = next_chunk(dn);
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
@@ -946,17 +953,10 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
                    (plane ? a.w.g3l : a.w.g3h) + (size_t)i3 * 4 * C::R + 8 * q);
       }
       cp_async_arrive_noinc(&full[s]);
-      // S rows, converted: lane = (j1, j2); eight rows' loads in flight
-      for (int r0 = 0; r0 < nb; r0 += 8) {
-        float4 v[8];
+      // S rows, converted: lane = (j1, j2)
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (r0 + u < nb)
-            v[u] = __ldg(reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)(x0 + r0 + u) * C::D) + lane);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (r0 + u < nb) bwd_store_s(st + C::OFF_S, r0 + u, v[u], lane);
-      }
+      for (int u = 0; u < C::RB; ++u)
+        if (u < nb) bwd_store_s(st + C::OFF_S, u, sv[u], lane);
       if (lane < C::CP) {
         m.rs[lane] = rs;
         m.pi1[lane] = gi1;
