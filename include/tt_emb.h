@@ -277,8 +277,9 @@ int tt_emb_profile_read(int i, char* name, int name_len, float* ms);
  * scratch is one file-scope device array of TT_EMB_STATIC_WORKSPACE_BYTES
  * (16 MiB) that every GPU loading this library holds until the process exits.
  *  - Sizes whose tt_emb_workspace_bytes exceed that capacity return
- *    TT_EMB_ERR_WORKSPACE before anything is enqueued (about 29k lookups at
- *    D = 128).
+ *    TT_EMB_ERR_WORKSPACE before anything is enqueued (for D = 128 with
+ *    R1 = R2 = 32 about 21k lookups at m = (100, 60, 120) and 11k at
+ *    m = (200, 240, 250): the bf16 split of the cores takes part of it).
  *  - The first call on a device looks up the array's device address with
  *    that device current; make that first call before any stream capture.
  *  - Every call shares the one array, which keeps the last call's contents;
