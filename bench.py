@@ -445,6 +445,7 @@ def run_ours(args, rank, world, dist):
     g_h = torch.from_numpy(x.grad_out).pin_memory()
     out_h = torch.empty((x.num_bags, x.D), dtype=torch.float32).pin_memory()
     idx_d, off_d, g_d = torch.empty_like(wl.idx), torch.empty_like(wl.off), torch.empty_like(wl.gout)
+    copy_stream = torch.cuda.Stream()
     e2e_times = []
     for it in range(max(args.warmup, 3) + args.steps):
         with torch.cuda.stream(stream):
@@ -453,15 +454,12 @@ def run_ours(args, rank, world, dist):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            idx_d.copy_(idx_h, non_blocking=True)
-            off_d.copy_(off_h, non_blocking=True)
-            g_d.copy_(g_h, non_blocking=True)
-            tte.tt_emb_forward_ex(wl.cores, x.m, x.n, x.R, idx_d, off_d, None, "sum", wl.out,
-                                  wl.ws, flags=tte.TT_EMB_CORES_SPLIT)
-            tte.tt_emb_backward(g_d, wl.cores, x.m, x.n, x.R, idx_d, off_d, wl.grads, wl.ws,
-                                reuse_grouping=True)
-            tte.tt_emb_sgd_ex(wl.cores, wl.grads, x.m, x.n, x.R, LR, True, wl.ws)
-            out_h.copy_(wl.out, non_blocking=True)
+            # one C-ABI call: copies in on the copy stream, forward, backward and
+            # SGD on `stream`, the pooled output copied back during the backward
+            tte.tt_emb_step_host(wl.cores, wl.grads, x.m, x.n, x.R, idx_h, off_h, g_h, out_h,
+                                 idx_d, off_d, g_d, wl.out, LR, wl.ws,
+                                 flags=tte.TT_EMB_CORES_SPLIT, stream=stream,
+                                 copy_stream=copy_stream)
             e1.record(stream)
         stream.synchronize()
         if it >= max(args.warmup, 3):
@@ -615,9 +613,10 @@ def run_ours(args, rank, world, dist):
         "e2e": {"value": round(nnz_tr * world / (ms_e2e * 1e-3), 1), "unit": "lookups/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 5),
-                "path": "pinned host indices/offsets/grad_out -> device, tt_emb_forward_ex "
-                        "(kept core split), tt_emb_backward, tt_emb_sgd_ex (SGD + split), "
-                        "pooled output -> pinned host"},
+                "path": "one tt_emb_step_host call per step: pinned host indices/offsets/"
+                        "grad_out -> device on a copy stream, forward on the kept core split "
+                        "as soon as the lookups are in, backward, SGD + split; the pooled "
+                        "output -> pinned host while the backward runs"},
         "gpu_launches": tr["n_launch"] * args.steps,
         "clocks": tr["clocks"],
         "workspace_bytes": tr["wl"].ws_bytes,

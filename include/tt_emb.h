@@ -27,8 +27,9 @@
  *
  * Conventions for every entry point:
  *  - All array arguments are DEVICE pointers owned by the caller (CUDA
- *    global memory of the current device).  The library allocates nothing
- *    and keeps no state between calls beyond the caller's workspace.
+ *    global memory of the current device), except the host arrays of
+ *    tt_emb_step_host.  The library allocates no memory and keeps no state
+ *    between calls beyond the caller's workspace.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *    call only enqueues work on it and returns; none synchronises except
  *    tt_emb_get_error.
@@ -200,6 +201,44 @@ int tt_emb_sgd_ex(float* const cores[3], float* const core_grads[3], const int64
                   const int32_t n[3], const int32_t R[4], float lr, int zero_grads,
                   void* workspace, size_t ws_bytes, void* stream);
 
+/* The host-side arrays of one batch for tt_emb_step_host (the one entry
+ * point that takes HOST arrays) and the caller's device arrays they are
+ * copied to and from.  Host arrays should be page-locked (cudaHostAlloc /
+ * cudaHostRegister): copies from or to pageable memory are correct but block
+ * the calling thread and do not overlap. */
+typedef struct {
+  const int64_t* h_indices;  /* host, nnz entries (any alignment)                      */
+  const int64_t* h_offsets;  /* host, num_bags + 1 entries (CSR, as above)             */
+  const float* h_grad_out;   /* host, float32 [num_bags][D], or NULL: forward only      */
+  float* h_out;              /* host, float32 [num_bags][D], or NULL: not copied back   */
+  int64_t* d_indices;        /* device, nnz entries                                     */
+  int64_t* d_offsets;        /* device, num_bags + 1 entries                            */
+  float* d_grad_out;         /* device, [num_bags][D], 16-byte aligned (training only)  */
+  float* d_out;              /* device, [num_bags][D], 16-byte aligned                  */
+  int64_t nnz;
+  int64_t num_bags;
+} tt_emb_host_batch;
+
+/* One step from host memory (a training step when batch->h_grad_out is not
+ * NULL, else a forward): indices and offsets are copied in, the forward
+ * (tt_emb_forward_ex with sum pooling and `flags`) runs into d_out, and for a
+ * training step the output gradient is copied in, tt_emb_backward reuses the
+ * forward's grouping and tt_emb_sgd_ex(lr, zero_grads = 1) updates the cores
+ * (so the next step may pass TT_EMB_CORES_SPLIT); h_out receives the pooled
+ * output.  The copies run on `copy_stream`, the kernels on `stream`, ordered
+ * by events: the copies start after the work enqueued on `stream` before the
+ * call, the forward waits only for indices and offsets (the output gradient
+ * arrives while it runs), and the output is copied back while the backward
+ * runs.  Everything the call does is complete when `stream` reaches the end
+ * of what it enqueued, h_out included.  copy_stream may equal stream (no
+ * overlap).  core_grads may be NULL for a forward; otherwise they are
+ * overwritten with zeros after the SGD.  Argument errors return before
+ * anything is enqueued; device-side conditions as for the calls named. */
+int tt_emb_step_host(float* const cores[3], float* const core_grads[3], const int64_t m[3],
+                     const int32_t n[3], const int32_t R[4], const tt_emb_host_batch* batch,
+                     float lr, int flags, void* workspace, size_t ws_bytes, void* stream,
+                     void* copy_stream);
+
 /* Chains of d cores, 3 <= d <= 8 (tt_emb_sgd_d: 2 <= d <= 8): core k is
  * float32 [m[k]][R[k]][n[k]][R[k+1]], R has d + 1 entries with R[0] = R[d] = 1,
  * the row index splits mixed-radix over m (m[0] most significant) and the
@@ -267,7 +306,7 @@ int tt_emb_profile_start(void);
 int tt_emb_profile_stop(void);
 int tt_emb_profile_read(int i, char* name, int name_len, float* ms);
 
-/* Forward for callers that cannot allocate device memory.  (The paper has no
+/* Forward for callers that cannot allocate device memory.  (None of the TT embedding designs has a
  * counterpart of this entry point.)  Some callers cannot call cudaMalloc at
  * all -- an allocator-less runtime that only hands out input and output
  * buffers, a plugin whose host framework owns every device allocation, code

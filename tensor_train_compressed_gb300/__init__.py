@@ -17,7 +17,7 @@ from ._binding import (EXPORTED, TTEmbError, library_path, lib, tt_emb_backward,
                        tt_emb_workspace_bytes_d, tt_emb_forward_d, tt_emb_backward_d, tt_emb_sgd_d, tt_emb_group, tt_emb_grouping_view,
                        tt_emb_forward_static, tt_emb_profile_read, tt_emb_profile_start,
                        tt_emb_profile_stop,
-                       tt_emb_sgd, tt_emb_version, tt_emb_workspace_bytes)
+                       tt_emb_sgd, tt_emb_step_host, tt_emb_version, tt_emb_workspace_bytes)
 from ._binding import (TT_EMB_ERR_ARG, TT_EMB_ERR_CUDA, TT_EMB_ERR_INDEX, TT_EMB_ERR_OFFSETS,
                        TT_EMB_ERR_TIMEOUT, TT_EMB_ERR_UNSUPPORTED, TT_EMB_ERR_WORKSPACE, TT_EMB_OK,
                        TT_EMB_CORES_SPLIT, TT_EMB_POOL_MEAN, TT_EMB_POOL_SUM)
@@ -25,7 +25,7 @@ from ._binding import (TT_EMB_ERR_ARG, TT_EMB_ERR_CUDA, TT_EMB_ERR_INDEX, TT_EMB
 __all__ = ["TTEmbeddingBag", "TTEmbError", "tt_emb_forward", "tt_emb_forward_static", "tt_emb_backward", "tt_emb_sgd",
            "tt_emb_forward_ex", "tt_emb_backward_ex", "tt_emb_split", "tt_emb_sgd_ex",
            "tt_emb_forward_tables", "tt_emb_workspace_bytes_d", "tt_emb_forward_d",
-           "tt_emb_backward_d", "tt_emb_sgd_d",
+           "tt_emb_backward_d", "tt_emb_sgd_d", "tt_emb_step_host",
            "tt_emb_group", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_workspace_bytes",
            "tt_emb_version", "tt_emb_profile_start", "tt_emb_profile_stop", "tt_emb_profile_read",
            "read_grouping", "lib", "library_path", "EXPORTED"]

@@ -33,7 +33,7 @@ _POOLING = {"sum": TT_EMB_POOL_SUM, "mean": TT_EMB_POOL_MEAN}
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
             "tt_emb_forward_ex", "tt_emb_backward_ex", "tt_emb_split", "tt_emb_sgd_ex",
             "tt_emb_forward_tables", "tt_emb_workspace_bytes_d", "tt_emb_forward_d",
-            "tt_emb_backward_d", "tt_emb_sgd_d",
+            "tt_emb_backward_d", "tt_emb_sgd_d", "tt_emb_step_host",
             "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_profile_start",
             "tt_emb_profile_stop", "tt_emb_profile_read", "tt_emb_forward_static",
             "tt_emb_version")
@@ -52,6 +52,13 @@ class Table(ctypes.Structure):
                 ("offsets", ctypes.c_void_p), ("num_bags", ctypes.c_int64),
                 ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
                 ("ws_bytes", ctypes.c_size_t)]
+
+
+class HostBatch(ctypes.Structure):
+    """tt_emb_host_batch of include/tt_emb.h."""
+    _fields_ = [(name, ctypes.c_void_p) for name in (
+        "h_indices", "h_offsets", "h_grad_out", "h_out", "d_indices", "d_offsets", "d_grad_out",
+        "d_out")] + [("nnz", ctypes.c_int64), ("num_bags", ctypes.c_int64)]
 
 
 class Grouping(ctypes.Structure):
@@ -295,6 +302,56 @@ def tt_emb_sgd_ex(cores, core_grads, m, n, R, lr: float, zero_grads: bool, works
                                *_shape(m, n, R), ctypes.c_float(lr), int(bool(zero_grads)),
                                _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
                                _stream(stream)), "tt_emb_sgd_ex")
+
+
+def _host(t, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_copy_streams = {}
+
+
+def tt_emb_step_host(cores, core_grads, m, n, R, h_indices, h_offsets, h_grad_out, h_out,
+                     d_indices, d_offsets, d_grad_out, d_out, lr: float, workspace, flags: int = 0,
+                     stream=None, copy_stream=None):
+    """One step from host tensors (pinned for the copies to overlap): h_grad_out None runs a
+    forward only, h_out None leaves the output on the device.  Without copy_stream a copy
+    stream of this module (one per device) is used."""
+    if copy_stream is None:
+        dev = torch.cuda.current_device()
+        if dev not in _copy_streams:
+            _copy_streams[dev] = torch.cuda.Stream(device=dev)
+        copy_stream = _copy_streams[dev]
+    train = h_grad_out is not None
+    b = HostBatch()
+    b.h_indices = _host(h_indices, torch.int64, "h_indices")
+    b.h_offsets = _host(h_offsets, torch.int64, "h_offsets")
+    b.h_grad_out = _host(h_grad_out, torch.float32, "h_grad_out") if train else None
+    b.h_out = None if h_out is None else _host(h_out, torch.float32, "h_out")
+    b.d_indices = _dev(d_indices, torch.int64, "d_indices")
+    b.d_offsets = _dev(d_offsets, torch.int64, "d_offsets")
+    b.d_grad_out = _dev(d_grad_out, torch.float32, "d_grad_out") if train else None
+    b.d_out = _dev(d_out, torch.float32, "d_out")
+    b.nnz = h_indices.numel()
+    b.num_bags = h_offsets.numel() - 1
+    if d_indices.numel() < b.nnz or d_offsets.numel() < b.num_bags + 1:
+        raise ValueError("device staging tensors smaller than the host batch")
+    D = int(n[0]) * int(n[1]) * int(n[2])
+    for name, t in (("h_grad_out", h_grad_out), ("h_out", h_out), ("d_grad_out", d_grad_out),
+                    ("d_out", d_out)):
+        if t is not None and (name != "d_grad_out" or train) and t.numel() < b.num_bags * D:
+            raise ValueError(f"{name} holds fewer than num_bags * D floats")
+    grads = _ptrs3(core_grads, "core_grads") if train else None
+    _check(lib().tt_emb_step_host(_ptrs3(cores, "cores"), grads, *_shape(m, n, R),
+                                  ctypes.byref(b), ctypes.c_float(lr), int(flags),
+                                  _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                  _stream(stream), _stream(copy_stream)), "tt_emb_step_host")
 
 
 def tt_emb_get_error(workspace, stream=None) -> tuple[int, int]:

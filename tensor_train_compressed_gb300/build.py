@@ -1,6 +1,6 @@
 """Build the CUDA library libtt_emb.so in-tree (nvcc, sm_103a only).
 
-Each translation unit under csrc/ is compiled in parallel, then linked into
+Each translation unit under csrc/ (CUDA sources and host-only C++) is compiled in parallel, then linked into
 tensor_train_compressed_gb300/_build/libtt_emb.so against the shared CUDA
 runtime.  No torch headers or libraries are involved.
 """
@@ -30,7 +30,7 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
@@ -53,7 +53,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

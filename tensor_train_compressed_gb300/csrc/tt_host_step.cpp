@@ -1,0 +1,126 @@
+// One step from host memory (tt_emb_step_host): the batch is copied in on a
+// copy stream, the pooled output copied back, and the kernels of the step run
+// on the caller's stream in between, ordered by events so that the copies of
+// the output gradient and of the pooled output overlap with the forward and
+// with the backward.  Host code only: every kernel is launched through the
+// other entry points of the library.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/tt_emb.h"
+
+namespace {
+
+enum { kEvStart, kEvIn, kEvGrad, kEvFwd, kEvDone, kNumEv };
+
+// Events of this thread on the current device, created once and reused: a
+// wait enqueued on a stream refers to the record that preceded it, so a later
+// call may record the same events again.
+int step_events(cudaEvent_t** ev) {
+  thread_local std::vector<std::vector<cudaEvent_t>> per_device;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return TT_EMB_ERR_CUDA;
+  if ((size_t)dev >= per_device.size()) per_device.resize(dev + 1);
+  std::vector<cudaEvent_t>& e = per_device[dev];
+  if (e.empty()) {
+    e.assign(kNumEv, nullptr);
+    for (int i = 0; i < kNumEv; ++i)
+      if (cudaEventCreateWithFlags(&e[i], cudaEventDisableTiming) != cudaSuccess) {
+        for (int j = 0; j < i; ++j) cudaEventDestroy(e[j]);
+        e.clear();
+        return TT_EMB_ERR_CUDA;
+      }
+  }
+  *ev = e.data();
+  return TT_EMB_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool cores_ok(const void* const* c) {
+  if (!c) return false;
+  for (int k = 0; k < 3; ++k)
+    if (!c[k] || !aligned(c[k], 16)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" int tt_emb_step_host(float* const cores[3], float* const core_grads[3],
+                                const int64_t m[3], const int32_t n[3], const int32_t R[4],
+                                const tt_emb_host_batch* batch, float lr, int flags,
+                                void* workspace, size_t ws_bytes, void* stream,
+                                void* copy_stream) {
+  // Every check of the calls below is made here first, so that an argument
+  // error returns before any copy is enqueued.
+  if (!batch) return TT_EMB_ERR_ARG;
+  const tt_emb_host_batch& b = *batch;
+  size_t need = 0;
+  int rc = tt_emb_workspace_bytes(m, n, R, b.nnz, b.num_bags, &need);
+  if (rc) return rc;
+  const bool train = b.h_grad_out != nullptr;
+  if (flags & ~TT_EMB_CORES_SPLIT) return TT_EMB_ERR_ARG;
+  if (!cores_ok((const void* const*)cores) || (train && !cores_ok((const void* const*)core_grads)))
+    return TT_EMB_ERR_ARG;
+  if (b.nnz > 0 && (b.num_bags == 0 || !b.h_indices || !b.d_indices)) return TT_EMB_ERR_ARG;
+  if (b.num_bags >= (1ll << 31)) return TT_EMB_ERR_ARG;
+  if (!b.h_offsets || !b.d_offsets) return TT_EMB_ERR_ARG;
+  if (b.num_bags > 0 && (!b.d_out || !aligned(b.d_out, 16))) return TT_EMB_ERR_ARG;
+  if (train && b.num_bags > 0 && (!b.d_grad_out || !aligned(b.d_grad_out, 16)))
+    return TT_EMB_ERR_ARG;
+  if (!workspace || !aligned(workspace, 256)) return TT_EMB_ERR_ARG;
+  if (ws_bytes < need) return TT_EMB_ERR_WORKSPACE;
+
+  const int64_t D = (int64_t)n[0] * n[1] * n[2];
+  const size_t out_bytes = sizeof(float) * (size_t)b.num_bags * (size_t)D;
+  cudaStream_t st = (cudaStream_t)stream, cs = (cudaStream_t)copy_stream;
+  cudaEvent_t* ev = nullptr;
+  rc = step_events(&ev);
+  if (rc) return rc;
+  bool ok = true;
+  auto cuda = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
+
+  // the copies in start after the work the caller ordered before this call
+  cuda(cudaEventRecord(ev[kEvStart], st));
+  cuda(cudaStreamWaitEvent(cs, ev[kEvStart], 0));
+  if (b.nnz > 0)
+    cuda(cudaMemcpyAsync(b.d_indices, b.h_indices, sizeof(int64_t) * (size_t)b.nnz,
+                         cudaMemcpyHostToDevice, cs));
+  cuda(cudaMemcpyAsync(b.d_offsets, b.h_offsets, sizeof(int64_t) * (size_t)(b.num_bags + 1),
+                       cudaMemcpyHostToDevice, cs));
+  cuda(cudaEventRecord(ev[kEvIn], cs));
+  if (train && out_bytes > 0)
+    cuda(cudaMemcpyAsync(b.d_grad_out, b.h_grad_out, out_bytes, cudaMemcpyHostToDevice, cs));
+  cuda(cudaEventRecord(ev[kEvGrad], cs));
+  if (!ok) return TT_EMB_ERR_CUDA;
+
+  // forward as soon as the lookups are in (the output gradient still copying)
+  cuda(cudaStreamWaitEvent(st, ev[kEvIn], 0));
+  if (!ok) return TT_EMB_ERR_CUDA;
+  const float* const* cc = (const float* const*)cores;
+  rc = tt_emb_forward_ex(cc, m, n, R, b.d_indices, b.nnz, b.d_offsets, b.num_bags, nullptr,
+                         TT_EMB_POOL_SUM, flags, b.d_out, workspace, ws_bytes, stream);
+  if (rc) return rc;
+  cuda(cudaEventRecord(ev[kEvFwd], st));
+  if (train) {
+    // backward on the forward's grouping and split, then SGD that resets the
+    // gradients and leaves the split of the updated cores
+    cuda(cudaStreamWaitEvent(st, ev[kEvGrad], 0));
+    if (!ok) return TT_EMB_ERR_CUDA;
+    rc = tt_emb_backward(b.d_grad_out, cc, m, n, R, b.d_indices, b.nnz, b.d_offsets, b.num_bags,
+                         core_grads, workspace, ws_bytes, 1, stream);
+    if (rc) return rc;
+    rc = tt_emb_sgd_ex(cores, core_grads, m, n, R, lr, 1, workspace, ws_bytes, stream);
+    if (rc) return rc;
+  }
+  // the pooled output goes back while the backward runs; enqueued after the
+  // kernels, since a copy into pageable host memory blocks the host
+  cuda(cudaStreamWaitEvent(cs, ev[kEvFwd], 0));
+  if (b.h_out && out_bytes > 0)
+    cuda(cudaMemcpyAsync(b.h_out, b.d_out, out_bytes, cudaMemcpyDeviceToHost, cs));
+  cuda(cudaEventRecord(ev[kEvDone], cs));
+  cuda(cudaStreamWaitEvent(st, ev[kEvDone], 0));
+  return ok ? TT_EMB_OK : TT_EMB_ERR_CUDA;
+}

@@ -187,3 +187,44 @@ def test_chain_workspace_and_shape_checks(L):
     assert e.value.code == tte.TT_EMB_ERR_UNSUPPORTED
     with pytest.raises(ValueError):
         tte.tt_emb_workspace_bytes_d(m, n, R[:-1], 10, 1)
+
+
+def test_step_host_argument_checks(L):
+    """The host-buffer step checks every argument of the calls it makes before it
+    enqueues its first copy."""
+    m, n, R = (10, 10, 10), (2, 4, 2), (1, 4, 4, 1)
+    fake = 1 << 20
+    cores = (ctypes.c_void_p * 3)(fake, fake, fake)
+    P = ctypes.c_void_p
+    need = tte.tt_emb_workspace_bytes(m, n, R, 100, 10)
+
+    def batch(**kw):
+        b = B.HostBatch()
+        for name in ("h_indices", "h_offsets", "h_grad_out", "h_out", "d_indices", "d_offsets",
+                     "d_grad_out", "d_out"):
+            setattr(b, name, fake)
+        b.nnz, b.num_bags = 100, 10
+        for k, v in kw.items():
+            setattr(b, k, v)
+        return b
+
+    def call(b, grads=cores, flags=0, ws=fake, ws_bytes=need):
+        return L.tt_emb_step_host(cores, grads, *_shape(m, n, R),
+                                  None if b is None else ctypes.byref(b), ctypes.c_float(0.1),
+                                  flags, P(ws), ws_bytes, None, None)
+
+    assert call(None) == tte.TT_EMB_ERR_ARG
+    assert call(batch(), ws_bytes=need - 1) == tte.TT_EMB_ERR_WORKSPACE
+    assert call(batch(), ws=fake + 8) == tte.TT_EMB_ERR_ARG          # workspace alignment
+    assert call(batch(), flags=2) == tte.TT_EMB_ERR_ARG              # unknown flag
+    assert call(batch(), grads=None) == tte.TT_EMB_ERR_ARG           # training needs gradients
+    assert call(batch(d_grad_out=None)) == tte.TT_EMB_ERR_ARG
+    assert call(batch(d_out=fake + 4)) == tte.TT_EMB_ERR_ARG         # out alignment
+    assert call(batch(h_indices=None)) == tte.TT_EMB_ERR_ARG
+    assert call(batch(d_offsets=None)) == tte.TT_EMB_ERR_ARG
+    assert call(batch(num_bags=0)) == tte.TT_EMB_ERR_ARG             # lookups without bags
+    assert call(batch(nnz=-1)) == tte.TT_EMB_ERR_ARG
+    bad_shape = (ctypes.c_int32 * 4)(2, 4, 4, 1)
+    assert L.tt_emb_step_host(cores, cores, _shape(m, n, R)[0], _shape(m, n, R)[1], bad_shape,
+                              ctypes.byref(batch()), ctypes.c_float(0.1), 0, P(fake), need, None,
+                              None) == tte.TT_EMB_ERR_ARG
