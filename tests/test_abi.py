@@ -228,3 +228,19 @@ def test_step_host_argument_checks(L):
     assert L.tt_emb_step_host(cores, cores, _shape(m, n, R)[0], _shape(m, n, R)[1], bad_shape,
                               ctypes.byref(batch()), ctypes.c_float(0.1), 0, P(fake), need, None,
                               None) == tte.TT_EMB_ERR_ARG
+
+
+def test_step_host_binding_checks_tensor_kinds(L):
+    """The binding refuses host tensors of the wrong type and device staging that is not on
+    the GPU before it calls the library."""
+    import torch
+    m, n, R = (10, 10, 10), (2, 4, 2), (1, 4, 4, 1)
+    cores = [torch.zeros(4) for _ in range(3)]
+    h_idx, h_off = torch.zeros(5, dtype=torch.int64), torch.tensor([0, 5], dtype=torch.int64)
+    h_g, h_out = torch.zeros(1, 16), torch.zeros(1, 16)
+    with pytest.raises(TypeError):                 # indices must be int64
+        tte.tt_emb_step_host(cores, cores, m, n, R, h_idx.int(), h_off, h_g, h_out, h_idx, h_off,
+                             h_g, h_out, 0.1, torch.zeros(8, dtype=torch.uint8), copy_stream=0)
+    with pytest.raises(TypeError):                 # device staging must be CUDA tensors
+        tte.tt_emb_step_host(cores, cores, m, n, R, h_idx, h_off, h_g, h_out, h_idx, h_off, h_g,
+                             h_out, 0.1, torch.zeros(8, dtype=torch.uint8), copy_stream=0)
