@@ -704,24 +704,31 @@ __global__ void __launch_bounds__(256) k_pool(const int64_t* __restrict__ offset
 // Pooling for D = 128: every lane owns one float4 column, so the inner loop
 // needs no column checks; lookups with an out-of-range index point at the zero
 // row `zrow` (weight 0); full batches of 8 row loads run unpredicated.
+constexpr int kPoolThreads = 128, kPoolCtasPerSm = 9;
 template <int MODE>
-__global__ void __launch_bounds__(256) k_pool128(const int64_t* __restrict__ offsets, int64_t B,
-                                                 int64_t nnz, const int32_t* __restrict__ uid,
-                                                 const float* __restrict__ psw,
-                                                 const float4* __restrict__ rb4, int32_t zrow,
-                                                 float4* __restrict__ out,
-                                                 int32_t* __restrict__ bag_of) {
+__global__ void __launch_bounds__(kPoolThreads, MODE == kPoolWeighted ? 1 : kPoolCtasPerSm) k_pool128(const int64_t* __restrict__ offsets, int64_t B64,
+                                                    int64_t nnz64, const int32_t* __restrict__ uid,
+                                                    const float* __restrict__ psw,
+                                                    const float4* __restrict__ rb4, int32_t zrow,
+                                                    float4* __restrict__ out,
+                                                    int32_t* __restrict__ bag_of) {
+  // bags < 2^31 and lookups < 2^30, so positions fit in 32 bits (fewer
+  // registers: 36 warps per SM instead of 32); an offset is read by its low word
+  // (little-endian) and clamped to [0, nnz], which keeps every access in
+  // bounds even for offsets the grouping reported as bad
+  const int B = (int)B64, nnz = (int)nnz64;
+  const int32_t* __restrict__ off32 = reinterpret_cast<const int32_t*>(offsets);
   const int lane = threadIdx.x & 31;
-  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < B; b += warps) {
-    int64_t l0 = offsets[b], l1 = offsets[b + 1];
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < B; b += warps) {
+    int l0 = off32[2 * (int64_t)b], l1 = off32[2 * (int64_t)b + 2];
     l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
     l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t lb = l0; lb < l1; lb += 32) {
-      const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
+    for (int lb = l0; lb < l1; lb += 32) {
+      const int cnt = l1 - lb < 32 ? l1 - lb : 32;
       int32_t my_u = lane < cnt ? uid[lb + lane] : zrow;
-      if (lane < cnt) bag_of[lb + lane] = (int32_t)b;
+      if (lane < cnt) bag_of[lb + lane] = b;
       float my_w = 0.f;
       if (MODE == kPoolWeighted) my_w = (lane < cnt && my_u >= 0) ? psw[lb + lane] : 0.f;
       my_u = my_u < 0 ? zrow : my_u;
@@ -743,7 +750,7 @@ __global__ void __launch_bounds__(256) k_pool128(const int64_t* __restrict__ off
       }
     }
     pool_mean<MODE>(acc, l1 - l0);
-    out[b * 32 + lane] = acc;
+    out[(int64_t)b * 32 + lane] = acc;
   }
 }
 
@@ -866,7 +873,11 @@ static void launch_pool_mode(const Shape& s, const Layout& L, const WS& w, const
   const int cap = sm_count() * 16;
   if (grid > cap) grid = cap;
   if (s.D == 128) {
-    TT_TIMED("k_pool", st, (k_pool128<MODE><<<grid, 256, 0, st>>>(
+    // two full waves of 4-warp CTAs, each warp taking bags by grid stride
+    grid = (int)ceil_div(num_bags, kPoolThreads / 32);
+    const int cap128 = sm_count() * kPoolCtasPerSm * 2;
+    if (grid > cap128) grid = cap128;
+    TT_TIMED("k_pool", st, (k_pool128<MODE><<<grid, kPoolThreads, 0, st>>>(
                                offsets, num_bags, nnz, w.uid, psw,
                                reinterpret_cast<const float4*>(w.rowbuf), (int32_t)L.rowbuf_rows,
                                reinterpret_cast<float4*>(out), w.bag_of)));
