@@ -77,6 +77,7 @@ class TTEmbeddingBag:
         self.grads = [torch.zeros_like(c) for c in self.cores]
         self.workspace = torch.empty(0, dtype=torch.uint8, device=self.device)
         self._batch = None
+        self._staging = None
 
     def _ensure_ws(self, nnz, num_bags):
         need = tt_emb_workspace_bytes(self.m, self.n, self.R, nnz, num_bags)
@@ -122,6 +123,31 @@ class TTEmbeddingBag:
                                self.mode, self.grads, grad_weights, self.workspace,
                                reuse_grouping=True, stream=stream)
         return self.grads
+
+    def train_step_host(self, h_indices, h_offsets, h_grad_out, lr: float, h_out=None,
+                        stream=None):
+        """One training step (sum pooling) from host tensors through tt_emb_step_host: the
+        batch is copied in on a copy stream while the kernels run, the cores take an SGD
+        step and the gradients are reset; the pooled output lands in ``h_out`` (a float32
+        host tensor [num_bags][D]) if given, and is returned on the device.  Page-locked
+        host tensors (``.pin_memory()``) let the copies overlap the kernels."""
+        if self.mode != "sum":
+            raise ValueError("train_step_host pools by sum")
+        nnz, B = h_indices.numel(), h_offsets.numel() - 1
+        self._ensure_ws(nnz, B)
+        st = self._staging
+        if st is None or st[0].numel() < nnz or st[1].numel() < B + 1 or st[2].shape[0] < B:
+            st = (torch.empty(max(nnz, 1), dtype=torch.int64, device=self.device),
+                  torch.empty(B + 1, dtype=torch.int64, device=self.device),
+                  torch.empty((max(B, 1), self.D), dtype=torch.float32, device=self.device),
+                  torch.empty((max(B, 1), self.D), dtype=torch.float32, device=self.device))
+            self._staging = st
+        d_idx, d_off, d_g, d_out = st[0][:nnz], st[1][:B + 1], st[2][:B], st[3][:B]
+        tt_emb_step_host(self.cores, self.grads, self.m, self.n, self.R, h_indices, h_offsets,
+                         h_grad_out, h_out, d_idx, d_off, d_g, d_out, lr, self.workspace,
+                         stream=stream)
+        self._batch = None          # the grouping now belongs to this step's batch
+        return d_out
 
     def zero_grad(self):
         for g in self.grads:

@@ -132,3 +132,24 @@ def test_step_with_no_lookups():
     assert not s.h_out.any()
     for k in range(3):
         assert torch.equal(cores[k], plain[k])
+
+
+def test_class_train_step_from_host_matches_the_device_calls():
+    x = make_inputs(5, num_bags=600)
+    a = tte.TTEmbeddingBag(x.cores, x.m, x.n, x.R)
+    b = tte.TTEmbeddingBag(x.cores, x.m, x.n, x.R)
+    h_out = torch.full((x.num_bags, x.D), float("nan")).pin_memory()
+    d_out = a.train_step_host(_pinned(x.indices), _pinned(x.offsets), _pinned(x.grad_out), 0.5,
+                              h_out=h_out)
+    out_b = b.forward(x.indices, x.offsets)
+    b.backward(x.grad_out)
+    dg = [g.clone() for g in b.grads]
+    b.sgd_step(0.5, zero_grads=True)
+    torch.cuda.synchronize()
+    a.check()
+    assert torch.equal(h_out, out_b.cpu()) and torch.equal(d_out, out_b)
+    for k in range(3):
+        # the two gradients differ only in the order of their float atomics
+        tol = 0.5 * 1e-3 * dg[k].abs().max().item()
+        assert (a.cores[k] - b.cores[k]).abs().max().item() <= tol, k
+        assert not a.grads[k].any()
