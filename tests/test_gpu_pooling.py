@@ -119,12 +119,11 @@ def test_weighted_full_size_sampled():
     sel = np.concatenate([np.arange(x.offsets[b], x.offsets[b + 1]) for b in bags])
     off = np.concatenate([[0], np.cumsum(np.diff(x.offsets)[bags])])
     ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices[sel], off, threads=8, weights=w[sel])
-    scale = max(np.abs(run.out).max(), np.abs(ref).max())
-    assert np.abs(run.out[bags] - ref).max() <= FWD_TOL * scale
+    # tolerance scales: the oracle's own largest values over the sampled bags
+    assert np.abs(run.out[bags] - ref).max() <= FWD_TOL * np.abs(ref).max()
     _, dwref = oracle.backward(x.grad_out[bags], x.cores, x.m, x.n, x.R, x.indices[sel], off,
                                threads=8, weights=w[sel], want_dw=True)
-    assert np.abs(run.dW[sel] - dwref).max() <= DW_TOL * max(np.abs(run.dW).max(),
-                                                             np.abs(dwref).max())
+    assert np.abs(run.dW[sel] - dwref).max() <= DW_TOL * np.abs(dwref).max()
     r = x.indices
     i1, i2, i3 = r // (x.m[1] * x.m[2]), (r // x.m[2]) % x.m[1], r % x.m[2]
     for core, v in [(1, int(i1[3])), (2, int(i2[9])), (3, int(i3[0])), (3, int(i3[4242]))]:

@@ -256,14 +256,36 @@ def test_backward_filter_gives_the_exact_slice(k):
     assert np.allclose(part[k - 1][v], full[k - 1][v], rtol=1e-13, atol=1e-13)
 
 
-def test_backward_threads_and_sgd():
+def test_backward_threads():
     x = _bwd_case()
     a = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=1)
     b = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=3)
     for k in range(3):
         assert np.allclose(a[k], b[k], rtol=1e-13, atol=1e-13)
-        upd = oracle.sgd(x.cores[k], a[k], 0.01)
-        assert np.array_equal(upd, x.cores[k].astype(np.float64) - 0.01 * a[k])
+
+
+@pytest.mark.parametrize("lr", [1.0 / 64, 0.25])
+def test_sgd_step_is_the_exact_descent_of_the_loss(lr):
+    """L(G) = <g, out(G)> is linear in each core on its own (the row is a product of one
+    slice of every core), so L(G_k + delta) = L(G_k) + <dL/dG_k, delta> exactly.  One SGD
+    step on core k alone must therefore change L by exactly -lr * ||dL/dG_k||^2, with L
+    evaluated by the forward oracle.  Dyadic cores, output gradient and step keep every
+    value exact, so a sign, a scale, a dropped lr or a misplaced element fails."""
+    m, n, R = (3, 4, 5), (2, 3, 2), (1, 3, 2, 1)
+    cores = _dyadic_cores(m, n, R, 21)
+    x = make_custom(m, n, R, num_bags=15, max_len=5, seed=22)
+    g = (np.random.default_rng(23).integers(-3, 4, size=x.grad_out.shape) / 2.0).astype(
+        np.float32)
+    dG = oracle.backward(g, cores, m, n, R, x.indices, x.offsets)
+    L0 = (oracle.forward(cores, m, n, R, x.indices, x.offsets) * g).sum()
+    for k in range(3):
+        assert np.abs(dG[k]).max() > 0
+        upd = oracle.sgd(cores[k], dG[k], lr)
+        assert np.array_equal(upd.astype(np.float32).astype(np.float64), upd)   # exact in fp32
+        stepped = [c.copy() for c in cores]
+        stepped[k] = upd.astype(np.float32)
+        L1 = (oracle.forward(stepped, m, n, R, x.indices, x.offsets) * g).sum()
+        assert L1 - L0 == -lr * float((dG[k] ** 2).sum()), k
 
 
 # ------------------------------------------------- mean and weighted pooling
