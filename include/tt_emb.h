@@ -29,7 +29,12 @@
  *  - All array arguments are DEVICE pointers owned by the caller (CUDA
  *    global memory of the current device), except the host arrays of
  *    tt_emb_step_host.  The library allocates no memory and keeps no state
- *    between calls beyond the caller's workspace.
+ *    between calls beyond the caller's workspace, with three exceptions,
+ *    each described at its declaration: the fixed device array of
+ *    tt_emb_forward_static (shared by every call of that entry point), the
+ *    per-thread, per-device CUDA events of tt_emb_step_host (created on a
+ *    thread's first call on a device, kept until the process exits), and the
+ *    opt-in launch records of tt_emb_profile_start.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *    call only enqueues work on it and returns; none synchronises except
  *    tt_emb_get_error.
@@ -233,7 +238,10 @@ typedef struct {
  * of what it enqueued, h_out included.  copy_stream may equal stream (no
  * overlap).  core_grads may be NULL for a forward; otherwise they are
  * overwritten with zeros after the SGD.  Argument errors return before
- * anything is enqueued; device-side conditions as for the calls named. */
+ * anything is enqueued; device-side conditions as for the calls named.  If a
+ * call fails after its copies were enqueued (a CUDA error, or an error code
+ * of one of the calls named), `stream` is still made to wait for every copy
+ * the call enqueued, so the host buffers may be reused once `stream` drains. */
 int tt_emb_step_host(float* const cores[3], float* const core_grads[3], const int64_t m[3],
                      const int32_t n[3], const int32_t R[4], const tt_emb_host_batch* batch,
                      float lr, int flags, void* workspace, size_t ws_bytes, void* stream,
@@ -321,6 +329,9 @@ int tt_emb_profile_read(int i, char* name, int name_len, float* ms);
  *    m = (200, 240, 250): the bf16 split of the cores takes part of it).
  *  - The first call on a device looks up the array's device address with
  *    that device current; make that first call before any stream capture.
+ *    The address is kept per device id for the life of the process: after a
+ *    cudaDeviceReset the array is gone and so is its cached address, so this
+ *    entry point must not be called again in that process.
  *  - Every call shares the one array, which keeps the last call's contents;
  *    the call clears what must start at zero itself.  Calls whose work
  *    overlaps on the GPU (other streams or threads) race on the array: the

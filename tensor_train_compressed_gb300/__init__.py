@@ -82,6 +82,10 @@ class TTEmbeddingBag:
     def _ensure_ws(self, nnz, num_bags):
         need = tt_emb_workspace_bytes(self.m, self.n, self.R, nnz, num_bags)
         if self.workspace.numel() < need:
+            # the old workspace may still be in use by work enqueued on another stream
+            # (a caller's stream, the host step's copy stream); growth is rare, so wait
+            # for the device before handing its memory back to torch's allocator
+            torch.cuda.synchronize(self.device)
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
 
     def _to_dev(self, x):
@@ -130,13 +134,19 @@ class TTEmbeddingBag:
         batch is copied in on a copy stream while the kernels run, the cores take an SGD
         step and the gradients are reset; the pooled output lands in ``h_out`` (a float32
         host tensor [num_bags][D]) if given, and is returned on the device.  Page-locked
-        host tensors (``.pin_memory()``) let the copies overlap the kernels."""
+        host tensors (``.pin_memory()``) let the copies overlap the kernels.
+
+        The returned device tensor is a view of this module's staging buffer: it is
+        valid until the next ``train_step_host`` call, which overwrites it (clone it to
+        keep it)."""
         if self.mode != "sum":
             raise ValueError("train_step_host pools by sum")
         nnz, B = h_indices.numel(), h_offsets.numel() - 1
         self._ensure_ws(nnz, B)
         st = self._staging
         if st is None or st[0].numel() < nnz or st[1].numel() < B + 1 or st[2].shape[0] < B:
+            if st is not None:
+                torch.cuda.synchronize(self.device)     # old staging may still be in use
             st = (torch.empty(max(nnz, 1), dtype=torch.int64, device=self.device),
                   torch.empty(B + 1, dtype=torch.int64, device=self.device),
                   torch.empty((max(B, 1), self.D), dtype=torch.float32, device=self.device),

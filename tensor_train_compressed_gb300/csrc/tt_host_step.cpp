@@ -82,9 +82,21 @@ extern "C" int tt_emb_step_host(float* const cores[3], float* const core_grads[3
   bool ok = true;
   auto cuda = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
 
+  // Once a copy is enqueued, every return goes through `finish`: it still
+  // records kEvDone on the copy stream and makes `stream` wait for it, so
+  // that the caller's host buffers are free to reuse once `stream` drains,
+  // whatever failed on the way.
+  auto finish = [&](int code) {
+    cudaError_t e1 = cudaEventRecord(ev[kEvDone], cs);
+    cudaError_t e2 = cudaStreamWaitEvent(st, ev[kEvDone], 0);
+    if (code) return code;
+    return (ok && e1 == cudaSuccess && e2 == cudaSuccess) ? TT_EMB_OK : TT_EMB_ERR_CUDA;
+  };
+
   // the copies in start after the work the caller ordered before this call
   cuda(cudaEventRecord(ev[kEvStart], st));
   cuda(cudaStreamWaitEvent(cs, ev[kEvStart], 0));
+  if (!ok) return TT_EMB_ERR_CUDA;            // nothing enqueued on the copy stream yet
   if (b.nnz > 0)
     cuda(cudaMemcpyAsync(b.d_indices, b.h_indices, sizeof(int64_t) * (size_t)b.nnz,
                          cudaMemcpyHostToDevice, cs));
@@ -94,33 +106,31 @@ extern "C" int tt_emb_step_host(float* const cores[3], float* const core_grads[3
   if (train && out_bytes > 0)
     cuda(cudaMemcpyAsync(b.d_grad_out, b.h_grad_out, out_bytes, cudaMemcpyHostToDevice, cs));
   cuda(cudaEventRecord(ev[kEvGrad], cs));
-  if (!ok) return TT_EMB_ERR_CUDA;
+  if (!ok) return finish(TT_EMB_ERR_CUDA);
 
   // forward as soon as the lookups are in (the output gradient still copying)
   cuda(cudaStreamWaitEvent(st, ev[kEvIn], 0));
-  if (!ok) return TT_EMB_ERR_CUDA;
+  if (!ok) return finish(TT_EMB_ERR_CUDA);
   const float* const* cc = (const float* const*)cores;
   rc = tt_emb_forward_ex(cc, m, n, R, b.d_indices, b.nnz, b.d_offsets, b.num_bags, nullptr,
                          TT_EMB_POOL_SUM, flags, b.d_out, workspace, ws_bytes, stream);
-  if (rc) return rc;
+  if (rc) return finish(rc);
   cuda(cudaEventRecord(ev[kEvFwd], st));
   if (train) {
     // backward on the forward's grouping and split, then SGD that resets the
     // gradients and leaves the split of the updated cores
     cuda(cudaStreamWaitEvent(st, ev[kEvGrad], 0));
-    if (!ok) return TT_EMB_ERR_CUDA;
+    if (!ok) return finish(TT_EMB_ERR_CUDA);
     rc = tt_emb_backward(b.d_grad_out, cc, m, n, R, b.d_indices, b.nnz, b.d_offsets, b.num_bags,
                          core_grads, workspace, ws_bytes, 1, stream);
-    if (rc) return rc;
+    if (rc) return finish(rc);
     rc = tt_emb_sgd_ex(cores, core_grads, m, n, R, lr, 1, workspace, ws_bytes, stream);
-    if (rc) return rc;
+    if (rc) return finish(rc);
   }
   // the pooled output goes back while the backward runs; enqueued after the
   // kernels, since a copy into pageable host memory blocks the host
   cuda(cudaStreamWaitEvent(cs, ev[kEvFwd], 0));
-  if (b.h_out && out_bytes > 0)
+  if (b.h_out && out_bytes > 0 && ok)
     cuda(cudaMemcpyAsync(b.h_out, b.d_out, out_bytes, cudaMemcpyDeviceToHost, cs));
-  cuda(cudaEventRecord(ev[kEvDone], cs));
-  cuda(cudaStreamWaitEvent(st, ev[kEvDone], 0));
-  return ok ? TT_EMB_OK : TT_EMB_ERR_CUDA;
+  return finish(TT_EMB_OK);
 }
