@@ -260,8 +260,11 @@ class Workload:
         """forward on the kept split of the cores, backward into the (zero) core
         gradients, SGD that also resets them and splits the updated cores"""
         t, x = self.tte, self.x
+        # a training step's forward keeps the per-row lookup lists for the
+        # backward; an inference call does not need them
+        flags = t.TT_EMB_CORES_SPLIT | (0 if self.train else t.TT_EMB_FORWARD_ONLY)
         t.tt_emb_forward_ex(self.cores, x.m, x.n, x.R, self.idx, self.off, None, "sum", self.out,
-                            self.ws, flags=t.TT_EMB_CORES_SPLIT)
+                            self.ws, flags=flags)
         if self.train:
             t.tt_emb_backward(self.gout, self.cores, x.m, x.n, x.R, self.idx, self.off,
                               self.grads, self.ws, reuse_grouping=True)

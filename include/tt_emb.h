@@ -18,8 +18,9 @@
  *   out[b]    = sum over the bag's lookups of row(indices[l]); empty bag -> 0
  *
  * How it is computed (FlowTT, summary card, key innovations; FlowTT
- * abstract): lookups are grouped by their (i1, i2) prefix on the device
- * (radix sort + run segmentation), the prefix partial P2 = G1[i1].G2[i2] is
+ * abstract): lookups are grouped by their (i1, i2) prefix on the device (a
+ * presence bitmap over the row keys when the batch is dense in its table,
+ * else a radix sort + run segmentation), the prefix partial P2 = G1[i1].G2[i2] is
  * formed once per unique prefix and kept on chip, each unique row is formed
  * once from it, and rows are pooled per bag.  Persistent CTAs take work
  * chunks from an atomic queue so that Zipf-skewed prefixes do not stall the
@@ -70,6 +71,8 @@ extern "C" {
 #define TT_EMB_ERR_OFFSETS (-5)      /* device: offsets not CSR (see above)                  */
 #define TT_EMB_ERR_TIMEOUT (-6)      /* device: a capped inter-CTA wait gave up              */
 #define TT_EMB_ERR_UNSUPPORTED (-7)  /* shape beyond the limits above                        */
+#define TT_EMB_ERR_REUSE (-8)        /* device: a backward reused the grouping of a forward
+                                        called with TT_EMB_FORWARD_ONLY                      */
 
 /* Bytes of workspace that forward/backward/group need for this shape and
  * batch.  The workspace holds the prefix grouping (sorted lookups, unique
@@ -78,9 +81,14 @@ extern "C" {
 int tt_emb_workspace_bytes(const int64_t m[3], const int32_t n[3], const int32_t R[4],
                            int64_t nnz, int64_t num_bags, size_t* bytes);
 
-/* Prefix grouping only (index decomposition, radix sort by (i2, i1, i3),
- * unique rows / unique (i1,i2) prefixes, work chunks), written into the
- * workspace.  FlowTT summary card, key innovations ("prefix-based index
+/* Prefix grouping only (index decomposition, grouping by the (i2, i1, i3)
+ * key, unique rows / unique (i1,i2) prefixes, work chunks), written into the
+ * workspace.  Two methods give the same unique rows, prefixes, per-lookup
+ * unique row and chunks: a presence bitmap over the M keys when the batch is
+ * dense in its table (ceil(M / 32) <= 8 nnz, the bitmaps fit in the workspace's
+ * unique-row buffer, and at most 8192 lookups per SM), else a radix sort.  They
+ * differ only in the order of one row's lookups inside `perm` (see
+ * tt_emb_grouping_view).  FlowTT summary card, key innovations ("prefix-based index
  * grouping").  tt_emb_forward calls this itself. */
 int tt_emb_group(const int64_t m[3], const int32_t n[3], const int32_t R[4],
                  const int64_t* indices, int64_t nnz, const int64_t* offsets,
@@ -131,6 +139,12 @@ int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stre
 /* Flags of tt_emb_forward_ex. */
 #define TT_EMB_CORES_SPLIT 1 /* the workspace already holds the bf16 split of these
                                 cores (see tt_emb_split): the forward skips the split */
+#define TT_EMB_FORWARD_ONLY 2 /* no backward will reuse this call's grouping (inference):
+                                the grouping may leave out the per-row lookup lists
+                                that only the backward reads (perm and row_start of
+                                tt_emb_grouping_view).  A tt_emb_backward with
+                                reuse_grouping != 0 on such a grouping adds nothing
+                                and tt_emb_get_error returns TT_EMB_ERR_REUSE */
 
 /* Forward with the other pooling rules of an embedding bag (the TT-Rec
  * abstract names its operator after the EmbeddingBag; the pages themselves
@@ -141,11 +155,12 @@ int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stre
  *  - pooling: TT_EMB_POOL_SUM, or TT_EMB_POOL_MEAN: every non-empty bag's sum
  *    is divided by its number of lookups (out-of-range lookups included in
  *    the count); empty bags give zeros.
- *  - flags: 0, or TT_EMB_CORES_SPLIT when the caller guarantees that the
- *    workspace holds the bf16 split of exactly these core values, made by the
- *    last tt_emb_split, tt_emb_sgd_ex or forward on this workspace with the
- *    cores unchanged since (a serving loop with fixed cores; a training loop
- *    that updates them with tt_emb_sgd_ex).  Other bits: TT_EMB_ERR_ARG.
+ *  - flags: 0, or a combination of TT_EMB_CORES_SPLIT, when the caller
+ *    guarantees that the workspace holds the bf16 split of exactly these core
+ *    values, made by the last tt_emb_split, tt_emb_sgd_ex or forward on this
+ *    workspace with the cores unchanged since (a serving loop with fixed cores;
+ *    a training loop that updates them with tt_emb_sgd_ex), and
+ *    TT_EMB_FORWARD_ONLY (above).  Other bits: TT_EMB_ERR_ARG.
  * tt_emb_forward is tt_emb_forward_ex(..., NULL, TT_EMB_POOL_SUM, 0, ...). */
 int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int32_t n[3],
                       const int32_t R[4], const int64_t* indices, int64_t nnz,
@@ -236,7 +251,8 @@ typedef struct {
  * arrives while it runs), and the output is copied back while the backward
  * runs.  Everything the call does is complete when `stream` reaches the end
  * of what it enqueued, h_out included.  copy_stream may equal stream (no
- * overlap).  core_grads may be NULL for a forward; otherwise they are
+ * overlap).  `flags` as for tt_emb_forward_ex; TT_EMB_FORWARD_ONLY only for a
+ * forward (TT_EMB_ERR_ARG with h_grad_out).  core_grads may be NULL for a forward; otherwise they are
  * overwritten with zeros after the SGD.  Argument errors return before
  * anything is enqueued; device-side conditions as for the calls named.  If a
  * call fails after its copies were enqueued (a CUDA error, or an error code
@@ -275,18 +291,23 @@ int tt_emb_sgd_d(int d, float* const* cores, float* const* core_grads, const int
 
 /* Synchronises `stream`, then reads the workspace status word written by the
  * kernels of the calls enqueued so far.  *device_status receives the raw
- * bit set (1 = index out of range, 2 = bad offsets, 4 = timeout).  Returns
- * TT_EMB_OK or the code of the most severe condition found
- * (TIMEOUT > OFFSETS > INDEX), or TT_EMB_ERR_CUDA. */
+ * bit set (1 = index out of range, 2 = bad offsets, 4 = timeout, 8 = a
+ * backward reused a forward-only grouping).  Returns TT_EMB_OK or the code of
+ * the most severe condition found (TIMEOUT > REUSE > OFFSETS > INDEX), or
+ * TT_EMB_ERR_CUDA. */
 int tt_emb_get_error(const void* workspace, void* stream, int* device_status);
 
 /* Device pointers into a workspace holding a grouping (pure pointer
  * arithmetic; reads no device memory).  For inspection and tests. */
 typedef struct {
   const int32_t* counts;          /* [0] valid lookups, [1] U_r unique rows, [2] U_12 unique
-                                     (i1,i2) prefixes, [3] work chunks, [4] status bits     */
-  const int32_t* perm;            /* [nnz]   lookup positions sorted by (i2,i1,i3, position);
-                                              out-of-range lookups last                     */
+                                     (i1,i2) prefixes, [3] work chunks, [4] status bits,
+                                     [5] grouping method: 1 key bitmap, 2 one-launch radix
+                                     sort, 3 multi-launch radix sort                         */
+  const int32_t* perm;            /* [nnz]   lookup positions grouped by unique row in
+                                              (i2,i1,i3) order, out-of-range lookups last;
+                                              inside a row in position order after a radix
+                                              sort, in no fixed order after the key bitmap  */
   const int32_t* row_start;       /* [U_r+1] first sorted position of each unique row         */
   const int32_t* row_i3;          /* [U_r]   i3 digit of each unique row                       */
   const int32_t* row_pair;        /* [U_r]   unique prefix of each unique row                  */

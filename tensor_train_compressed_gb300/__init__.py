@@ -20,7 +20,8 @@ from ._binding import (EXPORTED, TTEmbError, library_path, lib, tt_emb_backward,
                        tt_emb_sgd, tt_emb_step_host, tt_emb_version, tt_emb_workspace_bytes)
 from ._binding import (TT_EMB_ERR_ARG, TT_EMB_ERR_CUDA, TT_EMB_ERR_INDEX, TT_EMB_ERR_OFFSETS,
                        TT_EMB_ERR_TIMEOUT, TT_EMB_ERR_UNSUPPORTED, TT_EMB_ERR_WORKSPACE, TT_EMB_OK,
-                       TT_EMB_CORES_SPLIT, TT_EMB_POOL_MEAN, TT_EMB_POOL_SUM)
+                       TT_EMB_CORES_SPLIT, TT_EMB_POOL_MEAN, TT_EMB_POOL_SUM,
+                       TT_EMB_FORWARD_ONLY, TT_EMB_ERR_REUSE)
 
 __all__ = ["TTEmbeddingBag", "TTEmbError", "tt_emb_forward", "tt_emb_forward_static", "tt_emb_backward", "tt_emb_sgd",
            "tt_emb_forward_ex", "tt_emb_backward_ex", "tt_emb_split", "tt_emb_sgd_ex",
@@ -41,10 +42,12 @@ def read_grouping(m, n, R, nnz: int, num_bags: int, workspace: torch.Tensor) -> 
         esz = torch.tensor([], dtype=dtype).element_size()
         return workspace[off:off + count * esz].view(dtype).cpu().numpy()
 
-    counts = arr("counts", 5)
+    counts = arr("counts", 6)
     nv, ur, up, nc = (int(v) for v in counts[:4])
     D = int(n[0] * n[1] * n[2])
-    return dict(n_valid=nv, U_r=ur, U_12=up, n_chunks=nc, status=int(counts[4]),
+    method = {1: "bitmap", 2: "coop_sort", 3: "multi_sort",
+              4: "bitmap_nolists"}.get(int(counts[5]), "none")
+    return dict(n_valid=nv, U_r=ur, U_12=up, n_chunks=nc, status=int(counts[4]), method=method,
                 perm=arr("perm", nnz), row_start=arr("row_start", ur + 1),
                 row_i3=arr("row_i3", ur), row_pair=arr("row_pair", ur),
                 pair_row_start=arr("pair_row_start", up + 1), pair_i1=arr("pair_i1", up),

@@ -24,10 +24,12 @@ TT_EMB_ERR_INDEX = -4
 TT_EMB_ERR_OFFSETS = -5
 TT_EMB_ERR_TIMEOUT = -6
 TT_EMB_ERR_UNSUPPORTED = -7
+TT_EMB_ERR_REUSE = -8
 _NAMES = {v: k for k, v in list(globals().items()) if k.startswith("TT_EMB_")}
 TT_EMB_POOL_SUM = 0
 TT_EMB_POOL_MEAN = 1
 TT_EMB_CORES_SPLIT = 1
+TT_EMB_FORWARD_ONLY = 2
 _POOLING = {"sum": TT_EMB_POOL_SUM, "mean": TT_EMB_POOL_MEAN}
 
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
@@ -187,7 +189,8 @@ def _opt(t, dtype, name):
 def tt_emb_forward_ex(cores, m, n, R, indices, offsets, per_sample_weights, pooling, out,
                       workspace, stream=None, flags: int = 0):
     """pooling: "sum" / "mean" (or the TT_EMB_POOL_* value); per_sample_weights: None or a
-    float32 CUDA tensor [nnz] (sum only); flags: 0 or TT_EMB_CORES_SPLIT."""
+    float32 CUDA tensor [nnz] (sum only); flags: 0, TT_EMB_CORES_SPLIT and/or
+    TT_EMB_FORWARD_ONLY."""
     _check(lib().tt_emb_forward_ex(_ptrs3(cores, "cores"), *_shape(m, n, R),
                                    _dev(indices, torch.int64, "indices"), indices.numel(),
                                    _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,

@@ -298,7 +298,7 @@ int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int
   if (rc) return rc;
   rc = check_cores(cores);
   if (rc) return rc;
-  if (flags & ~TT_EMB_CORES_SPLIT) return TT_EMB_ERR_ARG;
+  if (flags & ~(TT_EMB_CORES_SPLIT | TT_EMB_FORWARD_ONLY)) return TT_EMB_ERR_ARG;
   Pooling pool;
   rc = check_pooling(per_sample_weights, pooling, &pool);
   if (rc) return rc;
@@ -311,7 +311,8 @@ int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int
   int CP, CR;
   rc = forward_chunk_params(s, &CP, &CR);
   if (rc) return rc;
-  rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, st);
+  rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, st,
+                    (flags & TT_EMB_FORWARD_ONLY) ? 0 : 1);
   if (rc) return rc;
   if (nnz == 0) {
     if (num_bags > 0 &&
@@ -602,6 +603,7 @@ int tt_emb_get_error(const void* workspace, void* stream, int* device_status) {
     return TT_EMB_ERR_CUDA;
   *device_status = (int)st;
   if (st & kStTimeout) return TT_EMB_ERR_TIMEOUT;
+  if (st & kStNoLists) return TT_EMB_ERR_REUSE;
   if (st & kStOffsets) return TT_EMB_ERR_OFFSETS;
   if (st & kStIndex) return TT_EMB_ERR_INDEX;
   return TT_EMB_OK;

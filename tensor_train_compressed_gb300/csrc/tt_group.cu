@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(256) k_prepare(PrepArgs a) {
   __shared__ uint32_t sh[kMaxPasses * kRadix];
   const int tid = threadIdx.x, lane = tid & 31;
   for (int i = tid; i < a.passes * kRadix; i += blockDim.x) sh[i] = 0;
+  if (blockIdx.x == 0 && tid == 0) a.w.ctl->method = kGroupMulti;
   __syncthreads();
 
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(kScanThreads) k_chunks(ChunkArgs a) {
 
 int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
-                 int rows_per_chunk, cudaStream_t st) {
+                 int rows_per_chunk, cudaStream_t st, int lists) {
   // control block + digit histograms start from zero
   if (cudaMemsetAsync(w.ctl, 0, L.zero_end - L.ctl, st) != cudaSuccess) return TT_EMB_ERR_CUDA;
   // the zero row after the unique rows (pooling points out-of-range lookups at it)
@@ -386,6 +387,12 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
       cudaSuccess)
     return TT_EMB_ERR_CUDA;
   if (nnz == 0) return TT_EMB_OK;   // counts stay zero; row_start etc. are never read
+  {
+    // a batch dense in its table: bitmap of the keys, no sort
+    const int rc = launch_group_bitmap(s, L, w, indices, nnz, offsets, num_bags, pairs_per_chunk,
+                                       rows_per_chunk, lists, st);
+    if (rc != TT_EMB_ERR_UNSUPPORTED) return rc;
+  }
   {
     const int rc = launch_group_coop(s, L, w, w.coop, indices, nnz, offsets, num_bags,
                                      pairs_per_chunk, rows_per_chunk, st);

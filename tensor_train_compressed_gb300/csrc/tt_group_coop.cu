@@ -17,13 +17,9 @@
 //
 // Grid barriers are capped spins: after kSpinCap polls a CTA sets the timeout
 // bit and goes on, so a broken barrier cannot hang the GPU.
-#include "tt_internal.cuh"
+#include "tt_coop.cuh"
 
 namespace tt {
-
-constexpr int kCoopThreads = 512;
-constexpr int kCoopWarps = kCoopThreads / 32;
-constexpr int kCoopMaxGrid = 1024;
 
 struct CoopArgs {
   const int64_t* indices;
@@ -42,102 +38,6 @@ struct CoopArgs {
   uint32_t* bar;          // grid barrier words (zeroed before the launch)
   unsigned long long* trace;   // [16] phase timestamps of CTA 0 (ns, %globaltimer)
 };
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Grid barrier over the CTAs of a cooperative launch (capped).  One monotonic
-// counter per launch: the k-th arrival (k counted from 0 over the launch, one
-// per CTA and barrier) adds 1 with release semantics and waits, with acquire
-// loads and a short sleep, until the counter reaches (k / G + 1) G.  The block
-// barrier before the arrival orders the CTA's writes before the release; the
-// one after the wait orders the CTA's later reads after the acquire.  One
-// atomic per CTA and no reset or generation word: measured 1.2 us per barrier
-// at G = 152 against 3.2 us for a two-level counter tree with fences.  `bar`
-// must be zero before the launch.
-__device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ void grid_barrier(uint32_t* bar, Ctl* ctl) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t G = gridDim.x;
-    const uint32_t k = atom_add_release_u32(bar, 1u);
-    const uint32_t target = (k / G + 1) * G;
-    long long spins = 0;
-    while (ld_acquire_u32(bar) < target) {
-      __nanosleep(20);
-      if (++spins > kSpinCap) {
-        set_status(ctl, kStTimeout);
-        break;
-      }
-    }
-  }
-  __syncthreads();
-}
-
-// Block-wide exclusive scan of one uint32 per thread (kCoopThreads threads).
-__device__ __forceinline__ uint32_t coop_scan(uint32_t v, uint32_t* total, uint32_t* sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sm[warp] = x;
-  __syncthreads();
-  uint32_t pre = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kCoopWarps; ++w) {
-    const uint32_t c = sm[w];
-    if (w < warp) pre += c;
-    tot += c;
-  }
-  __syncthreads();
-  *total = tot;
-  return pre + x - v;
-}
-
-// Block-wide sums of four uint32 per thread (kCoopThreads threads).
-__device__ __forceinline__ uint4 coop_sum4(uint4 v, uint4* sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-    v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
-    v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
-  }
-  if (lane == 0) sm[warp] = v;
-  __syncthreads();
-  uint4 t = make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (int w = 0; w < kCoopWarps; ++w) {
-    const uint4 u = sm[w];
-    t.x += u.x;
-    t.y += u.y;
-    t.z += u.z;
-    t.w += u.w;
-  }
-  __syncthreads();
-  return t;
-}
 
 template <int ITEMS>
 __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
@@ -382,6 +282,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     u_rows = (int)tot.x;
     u_pairs = (int)tot.y;
     if (c == 0 && tid == 0) {
+      a.w.ctl->method = kGroupCoop;
       a.w.ctl->n_valid = (int32_t)nv;
       a.w.ctl->U_r = (int32_t)tot.x;
       a.w.ctl->U_12 = (int32_t)tot.y;

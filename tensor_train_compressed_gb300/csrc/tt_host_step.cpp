@@ -61,7 +61,8 @@ extern "C" int tt_emb_step_host(float* const cores[3], float* const core_grads[3
   int rc = tt_emb_workspace_bytes(m, n, R, b.nnz, b.num_bags, &need);
   if (rc) return rc;
   const bool train = b.h_grad_out != nullptr;
-  if (flags & ~TT_EMB_CORES_SPLIT) return TT_EMB_ERR_ARG;
+  if (flags & ~(TT_EMB_CORES_SPLIT | TT_EMB_FORWARD_ONLY)) return TT_EMB_ERR_ARG;
+  if (train && (flags & TT_EMB_FORWARD_ONLY)) return TT_EMB_ERR_ARG;   // the backward reuses it
   if (!cores_ok((const void* const*)cores) || (train && !cores_ok((const void* const*)core_grads)))
     return TT_EMB_ERR_ARG;
   if (b.nnz > 0 && (b.num_bags == 0 || !b.h_indices || !b.d_indices)) return TT_EMB_ERR_ARG;

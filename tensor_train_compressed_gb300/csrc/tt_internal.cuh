@@ -32,6 +32,7 @@ constexpr int kMaxCores = 8;                // cores of one chain (tt_emb_*_d)
 constexpr uint32_t kStIndex = 1u;
 constexpr uint32_t kStOffsets = 2u;
 constexpr uint32_t kStTimeout = 4u;
+constexpr uint32_t kStNoLists = 8u;         // a backward reused a forward-only grouping
 
 // decoupled look-back flags (top two bits of a 32-bit status word)
 constexpr uint32_t kFlagAgg = 1u << 30;
@@ -40,6 +41,13 @@ constexpr uint32_t kFlagMask = 3u << 30;
 constexpr uint32_t kValMask = (1u << 30) - 1u;
 constexpr long long kSpinCap = 1ll << 22;   // polls before a look-back gives up
 
+// Grouping methods (Ctl::method).
+constexpr int32_t kGroupBitmap = 1;   // key bitmap, one cooperative launch
+constexpr int32_t kGroupCoop = 2;     // radix sort, one cooperative launch
+constexpr int32_t kGroupMulti = 3;    // radix sort, one launch per phase
+constexpr int32_t kGroupBitmapNoLists = 4;   // key bitmap without the per-row lookup lists
+                                             // (perm, row_start): a forward-only grouping
+
 // The control block at the start of the workspace (256 bytes).
 struct Ctl {
   int32_t n_valid;        // lookups with an in-range index
@@ -47,13 +55,14 @@ struct Ctl {
   int32_t U_12;           // unique (i1, i2) prefixes
   int32_t n_chunks;       // work chunks
   uint32_t status;        // kSt* bits
+  int32_t method;         // grouping that ran: kGroupBitmap, kGroupCoop or kGroupMulti
   uint32_t sort_tile_ctr[kMaxPasses];
   uint32_t seg_tile_ctr;
   uint32_t chunk_tile_ctr;
   uint32_t fwd_chunk_ctr;
   uint32_t bwd_chunk_ctr;
   uint32_t split_valid;   // the bf16 split planes hold the cores split_src (reset by every grouping)
-  uint32_t pad0[2];
+  uint32_t pad0[1];
   unsigned long long split_src[3];   // G1, G2, G3 addresses the planes were split from
   uint32_t pad[42];
 };
@@ -321,13 +330,19 @@ int sm_count();
 
 // grouping in one cooperative launch (tt_group_coop.cu)
 size_t coop_scratch_bytes();
+int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
+                        int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
+                        int rows_per_chunk, int lists, cudaStream_t st);
+bool bitmap_grouping_applies(const Shape& s, const Layout& L, int64_t nnz);
 int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratch,
                       const int64_t* indices, int64_t nnz, const int64_t* offsets,
                       int64_t num_bags, int pairs_per_chunk, int rows_per_chunk, cudaStream_t st);
 // grouping (tt_group.cu)
+// lists = 0: the bitmap grouping may leave out the per-row lookup lists (perm,
+// row_start), which only a backward reads (a forward-only call)
 int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
-                 int rows_per_chunk, cudaStream_t st);
+                 int rows_per_chunk, cudaStream_t st, int lists = 1);
 // chains of d > 3 cores (tt_chain.cu): the leading d - 2 cores merged into one
 struct ChainShape {
   int d;

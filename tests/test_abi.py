@@ -108,7 +108,7 @@ def test_pooling_variant_argument_checks(L):
     assert fwd(None, 7) == tte.TT_EMB_ERR_ARG                           # unknown pooling
     assert fwd(P(fake + 2), tte.TT_EMB_POOL_SUM) == tte.TT_EMB_ERR_ARG  # misaligned weights
     assert fwd(None, tte.TT_EMB_POOL_MEAN, need - 1) == tte.TT_EMB_ERR_WORKSPACE
-    assert fwd(None, tte.TT_EMB_POOL_SUM, need, 2) == tte.TT_EMB_ERR_ARG    # unknown flag
+    assert fwd(None, tte.TT_EMB_POOL_SUM, need, 4) == tte.TT_EMB_ERR_ARG    # unknown flag
     bwd = lambda psw, pooling, gw: L.tt_emb_backward_ex(
         P(fake), cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, psw, pooling, cores, gw,
         P(fake), need - 1, 1, None)

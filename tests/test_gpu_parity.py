@@ -62,13 +62,26 @@ def _rel_err(a, ref):
     return float(np.abs(a.astype(np.float64) - ref).max() / max(np.abs(ref).max(), 1e-30))
 
 
-def _check_grouping(x, ws):
+def _check_grouping(x, ws, method=None):
+    """The grouping in ``ws`` against the oracle's: unique rows, prefixes, CSR offsets
+    and the unique row of every lookup bit for bit; the lookups of every unique row
+    exactly as a set, and in position order after a radix-sort grouping (the oracle
+    sorts stably); chunks valid.  ``method`` (if given) must be the one that ran."""
     ref = oracle.group(x.indices, x.m)
     g = tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, ws)
+    if method is not None:
+        assert g["method"] == method, g["method"]
     assert g["n_valid"] == ref["n_valid"] and g["U_r"] == ref["U_r"] and g["U_12"] == ref["U_12"]
     nv = ref["n_valid"]
-    assert np.array_equal(g["perm"][:nv], ref["perm"])
-    assert np.array_equal(g["row_start"], ref["row_start"])
+    if g["method"] != "bitmap_nolists":          # a forward-only grouping has no lookup lists
+        assert np.array_equal(g["row_start"], ref["row_start"])
+        rid = np.repeat(np.arange(g["U_r"]), np.diff(g["row_start"]))
+        perm = g["perm"][:nv]
+        assert np.array_equal(perm[np.lexsort((perm, rid))], ref["perm"])   # each row's lookup set
+        if g["method"] != "bitmap":
+            assert np.array_equal(perm, ref["perm"])                        # and in position order
+        assert np.array_equal(np.sort(g["perm"][nv:]),
+                              np.setdiff1d(np.arange(x.nnz), ref["perm"]))  # out-of-range last
     assert np.array_equal(g["row_pair"], ref["row_pair"])
     assert np.array_equal(g["pair_row_start"], ref["pair_row_start"])
     assert np.array_equal(g["pair_i1"], ref["pair_i1"])
@@ -144,24 +157,24 @@ def test_forward_full_size_sampled(cfg, table):
     assert g["U_r"] == np.unique(x.indices).size and g["n_valid"] == x.nnz
 
 
-def _coop_grid():
+def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-@pytest.mark.parametrize("items", [4, 8, 12, 16])
-def test_grouping_every_cooperative_variant_bit_exact(items):
-    """The one-launch grouping keeps ceil(nnz / grid) sorted positions per CTA in
-    registers, 4, 8, 12 or 16 per thread (512 threads); the batch size picks the
-    variant.  Each variant is driven here with the benchmark table's shape and index
-    distribution and compared with the oracle's grouping element by element."""
-    G = _coop_grid()
-    lo, hi = G * 512 * (items - 4), G * 512 * items          # nnz range of this variant
+@pytest.mark.parametrize("items", [4, 8, 16])
+def test_bitmap_grouping_every_variant(items):
+    """The key-bitmap grouping keeps ceil(nnz / SMs) lookups per CTA in registers, 4, 8
+    or 16 per thread (512 threads); the batch size picks the variant.  Each one runs here
+    on the benchmark table's shape and index distribution (dense in the table: at most
+    8 bitmap words per lookup) and is compared with the oracle's grouping."""
+    G = _sms()
+    lo, hi = G * 512 * {4: 0, 8: 4, 16: 8}[items], G * 512 * items
     target = (lo + hi) // 2 if items > 4 else hi - 1000
     x = make_inputs(3, num_bags=target // 20)                # fixed bag length 20
     assert lo < x.nnz <= hi
     out, rc, _, st = _gpu_forward(x)
     assert rc == tte.TT_EMB_OK
-    _check_grouping(x, st["ws"])
+    _check_grouping(x, st["ws"], method="bitmap")
     rng = np.random.default_rng(items)
     bags = np.sort(rng.choice(x.num_bags, size=200, replace=False))
     idx, off = _sample_bags(x, bags)
@@ -169,14 +182,79 @@ def test_grouping_every_cooperative_variant_bit_exact(items):
     assert np.abs(out[bags] - ref).max() <= FWD_TOL * np.abs(ref).max()
 
 
+@pytest.mark.parametrize("items", [4, 8, 12, 16])
+def test_sort_grouping_every_cooperative_variant(items):
+    """The one-launch radix-sort grouping (4, 8, 12 or 16 lookups per thread), which
+    serves batches sparse in their table: 343M rows = 700^3, so the key bitmap would
+    take more than 8 words per lookup.  Its grouping must equal the oracle's in every
+    array, the order of each row's lookups included."""
+    G = _sms()
+    lo, hi = G * 512 * (items - 4), G * 512 * items
+    target = (lo + hi) // 2 if items > 4 else hi - 1000
+    x = make_custom((700, 700, 700), (4, 8, 4), (1, 32, 32, 1), num_bags=target // 20,
+                    max_len=39, seed=800 + items, dist=("zipf", 1.2, "identity"))
+    assert lo < x.nnz <= hi and (700 ** 3 + 31) // 32 > 8 * x.nnz
+    out, rc, _, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK
+    _check_grouping(x, st["ws"], method="coop_sort")
+    rng = np.random.default_rng(items)
+    bags = np.sort(rng.choice(x.num_bags, size=200, replace=False))
+    idx, off = _sample_bags(x, bags)
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, idx, off, threads=8)
+    assert np.abs(out[bags] - ref).max() <= FWD_TOL * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("cfg", [3, 5])
+def test_forward_only_grouping_full_size(cfg):
+    """A forward-only call (TT_EMB_FORWARD_ONLY) groups without the per-row lookup
+    lists: its output equals the plain forward's bit for bit, and its grouping (unique
+    rows, prefixes, uid, chunks) equals the oracle's."""
+    x = make_inputs(cfg)
+    ref_out, rc, _, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK
+    out = torch.full((x.num_bags, x.D), float("nan"), dtype=torch.float32, device="cuda")
+    tte.tt_emb_forward_ex(st["cores"], x.m, x.n, x.R, st["idx"], st["off"], None, "sum", out,
+                          st["ws"], flags=tte.TT_EMB_FORWARD_ONLY)
+    rc, bits = tte.tt_emb_get_error(st["ws"])
+    assert rc == tte.TT_EMB_OK, bits
+    assert np.array_equal(out.cpu().numpy(), ref_out)
+    _check_grouping(x, st["ws"], method="bitmap_nolists")
+
+
+def test_backward_refuses_a_forward_only_grouping():
+    """A backward that reuses the grouping of a forward-only call reports
+    TT_EMB_ERR_REUSE and leaves the core gradients untouched; rebuilding the grouping
+    (reuse_grouping=False) then gives the right gradients."""
+    x = make_inputs(3, num_bags=3000, with_grad=True)     # dense in its table: key bitmap
+    cores = [_dev(c) for c in x.cores]
+    idx, off = _dev(x.indices), _dev(x.offsets)
+    ws = torch.empty(tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty((x.num_bags, x.D), dtype=torch.float32, device="cuda")
+    tte.tt_emb_forward_ex(cores, x.m, x.n, x.R, idx, off, None, "sum", out, ws,
+                          flags=tte.TT_EMB_FORWARD_ONLY)
+    assert tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, ws)["method"] == "bitmap_nolists"
+    grads = [torch.zeros_like(c) for c in cores]
+    tte.tt_emb_backward(_dev(x.grad_out), cores, x.m, x.n, x.R, idx, off, grads, ws,
+                        reuse_grouping=True)
+    rc, bits = tte.tt_emb_get_error(ws)
+    assert rc == tte.TT_EMB_ERR_REUSE and bits & 8
+    assert not any(g.any() for g in grads)
+    tte.tt_emb_backward(_dev(x.grad_out), cores, x.m, x.n, x.R, idx, off, grads, ws,
+                        reuse_grouping=False)
+    dref = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(grads[k].cpu().numpy(), dref[k]) <= BWD_TOL, k
+
+
 def test_large_batch_uses_the_multi_kernel_grouping():
     """1.3M lookups exceed the register-resident cooperative grouping: the multi-kernel
     grouping path must give the same bit-exact grouping and forward."""
     x = make_custom((5, 6, 7), (4, 8, 4), (1, 32, 32, 1), num_bags=70000, max_len=40, seed=19)
-    assert x.nnz > 152 * 512 * 16
+    assert x.nnz > _sms() * 512 * 16
     out, rc, _, st = _gpu_forward(x)
     assert rc == tte.TT_EMB_OK
-    _check_grouping(x, st["ws"])
+    _check_grouping(x, st["ws"], method="multi_sort")
     rng = np.random.default_rng(5)
     bags = np.sort(rng.choice(x.num_bags, size=400, replace=False))
     idx, off = _sample_bags(x, bags)
