@@ -303,7 +303,10 @@ typedef struct {
   const int32_t* counts;          /* [0] valid lookups, [1] U_r unique rows, [2] U_12 unique
                                      (i1,i2) prefixes, [3] work chunks, [4] status bits,
                                      [5] grouping method: 1 key bitmap, 2 one-launch radix
-                                     sort, 3 multi-launch radix sort                         */
+                                     sort, 3 multi-launch radix sort, 4 key bitmap without
+                                     perm / row_start (TT_EMB_FORWARD_ONLY), [6] work chunks
+                                     of the last forward that took their prefix partial from
+                                     the L2 checkpoint instead of forming it              */
   const int32_t* perm;            /* [nnz]   lookup positions grouped by unique row in
                                               (i2,i1,i3) order, out-of-range lookups last;
                                               inside a row in position order after a radix

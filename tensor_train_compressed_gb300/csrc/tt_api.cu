@@ -75,6 +75,7 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
   };
   L.ctl = take(sizeof(Ctl));
   L.hist = take(sizeof(uint32_t) * kHistCopies * kMaxPasses * kRadix);
+  L.ckpt = take(sizeof(uint32_t) * 2 * kCkptSlots);
   L.zero_end = off;   // every grouping zeroes [ctl, zero_end)
   // bf16 split planes of the cores, at offsets fixed by the shape: a split made
   // by tt_emb_split or tt_emb_sgd_ex outlives the groupings of later batches
@@ -118,6 +119,10 @@ WS make_ws(void* base, const Layout& L) {
   WS w;
   w.ctl = reinterpret_cast<Ctl*>(b + L.ctl);
   w.hist = reinterpret_cast<uint32_t*>(b + L.hist);
+  w.ckpt = reinterpret_cast<uint32_t*>(b + L.ckpt);
+  // the claim order of the chunks is written by the grouping's last phase, when
+  // the sort keys are no longer needed
+  w.chunk_order = reinterpret_cast<int32_t*>(b + L.keysB);
   w.sort_status = reinterpret_cast<uint32_t*>(b + L.sort_status);
   w.keysA = reinterpret_cast<uint64_t*>(b + L.keysA);
   w.keysB = reinterpret_cast<uint64_t*>(b + L.keysB);
@@ -136,6 +141,7 @@ WS make_ws(void* base, const Layout& L) {
   w.chunk_status = reinterpret_cast<uint32_t*>(b + L.chunk_status);
   w.coop = b + L.coop;
   w.rowbuf = reinterpret_cast<float*>(b + L.rowbuf);
+  w.rowbuf_rows = L.rowbuf_rows;
   const bool split = L.g2l != 0;
   w.g1h = split ? reinterpret_cast<uint16_t*>(b + L.g1h) : nullptr;
   w.g1l = split ? reinterpret_cast<uint16_t*>(b + L.g1l) : nullptr;

@@ -1220,6 +1220,10 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
     // product per lookup; the forward chunk counter is re-armed first
     if (cudaMemsetAsync(&w.ctl->fwd_chunk_ctr, 0, sizeof(uint32_t), st) != cudaSuccess)
       return TT_EMB_ERR_CUDA;
+    // and the prefix-partial checkpoints are emptied: these cores may not be
+    // the ones the forward checkpointed
+    if (cudaMemsetAsync(w.ckpt, 0, sizeof(uint32_t) * 2 * kCkptSlots, st) != cudaSuccess)
+      return TT_EMB_ERR_CUDA;
     const int rc = launch_rows(s, w, cores, 0, st);
     if (rc) return rc;
     int grid = (int)ceil_div(num_bags, 8);

@@ -253,8 +253,13 @@ struct MmaFwd {
   static constexpr int F_G2 = G2PLANE / 2, F_P1 = G1PLANE / 2, F_G3 = GTPLANE / 2;   // floats
   static constexpr int STAGE_F = F_G2 + F_P1 + F_G3;
   static constexpr int F_P2 = P2PLANE / 2;
+  // L2 checkpoint slot of one prefix partial: the hi and lo planes of its P2
+  // (one prefix of the P2 layout, padding included)
+  static constexpr int CKB = 2 * PPB;
   struct Meta {
-    int x0, x1, p0, np, npairs, end, pad[2];
+    int x0, x1, p0, np, npairs, end;
+    int ck;               // checkpoint role: s + 1 writes slot s, -(s + 1) reads it, 0 none
+    int pad;
     int pair[MAXPAIRS];   // first row | (second row valid) << 8 | chunk-local prefix << 9
   };
   static constexpr int NCW = NC / CW;                // stage-2 columns per consumer warp
@@ -433,6 +438,20 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
   }
   __syncthreads();
   const int n_chunks = a.w.ctl->n_chunks;
+  // L2 checkpoint of prefix partials: a hot prefix is split into CR-row pieces;
+  // its first piece writes its P2 planes to a slot (owner word: CAS from 0 to
+  // prefix + 1) and sets the slot's ready word to prefix + 1; a later piece that
+  // finds the ready word set loads P2 from the slot instead of forming it again,
+  // and recomputes it otherwise (nothing ever waits for a slot).  The claim
+  // order puts later pieces after all other chunks, so their first piece is
+  // usually done.  Slots lie in the unique-row buffer past the batch's unique
+  // rows (below its zero row); their words are zeroed by every grouping.
+  const int64_t U_r = a.w.ctl->U_r;
+  const int64_t ck_fit = (a.w.rowbuf_rows - U_r) * (int64_t)C::D * 4 / C::CKB;
+  const int n_slots = (int)(ck_fit < 0 ? 0 : (ck_fit > kCkptSlots ? kCkptSlots : ck_fit));
+  char* ck_data = reinterpret_cast<char*>(a.w.rowbuf + (size_t)U_r * C::D);
+  uint32_t* ck_owner = a.w.ckpt;
+  uint32_t* ck_ready = a.w.ckpt + kCkptSlots;
 
   if (warp == CW + 1) {
     // ---------------- G2 copier: stages the G2 planes of the chunks the lead
@@ -440,7 +459,7 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
     for (int it = 0;; ++it) {
       const int s = it & 1;
       if (!mbar_wait(&go[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
-      const int i2 = slot[s];
+      const int i2 = slot[s];        // the G2 slice, -1: stop, -2 - k: checkpoint slot k
       if (i2 >= 0) {
         const uint16_t* h2 = a.w.g2h + (size_t)i2 * C::R * C::NC;
         const uint16_t* l2 = a.w.g2l + (size_t)i2 * C::R * C::NC;
@@ -451,9 +470,18 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
           cp_async16(dst + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * q,
                      (plane ? l2 : h2) + row * C::NC + 8 * q);
         }
+      } else if (i2 <= -2) {
+        // a checkpointed P2 into the stage's G2 area, in the P2 layout (planes
+        // P2PLANE apart), where the consumers' stage 3 reads it
+        const char* src = ck_data + (size_t)(-2 - i2) * C::CKB;
+        char* dst = reinterpret_cast<char*>(base + s * C::STAGE_F);
+        for (int e = lane; e < C::CKB / 16; e += 32) {
+          const int plane = e / (C::PPB / 16), q = e - plane * (C::PPB / 16);
+          cp_async16(dst + plane * C::P2PLANE + 16 * q, src + plane * C::PPB + 16 * q);
+        }
       }
       cp_async_arrive_noinc(&full[s]);
-      if (i2 < 0) break;
+      if (i2 == -1) break;
     }
     cp_async_wait_all();
     return;
@@ -474,6 +502,8 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
       int x0, x1, p0, np, nst, i2;
       int g30, g31;    // i3 of staged rows lane, lane + 32
       int gi1, rs, re; // lane < np: i1 and chunk-local row range of prefix p0 + lane
+      int pe;          // lane < np: the first row after prefix p0 + lane
+      bool whole;      // the chunk starts at its first prefix's first row
     };
     auto load_meta = [&](const ChunkDesc& d, PMeta& pm) {
       pm.x0 = d.x0;
@@ -486,19 +516,24 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
       pm.g31 = lane + 32 < pm.nst ? a.w.row_i3[d.x0 + lane + 32] : 0;
       pm.gi1 = 0;
       pm.rs = pm.re = rows;
+      pm.pe = d.x1;
+      pm.whole = d.whole;
       if (lane < pm.np) {
         pm.gi1 = a.w.pair_i1[d.p0 + lane];
         pm.rs = max(a.w.pair_row_start[d.p0 + lane], d.x0) - d.x0;
-        pm.re = min(a.w.pair_row_start[d.p0 + lane + 1], d.x1) - d.x0;
+        pm.pe = a.w.pair_row_start[d.p0 + lane + 1];
+        pm.re = min(pm.pe, d.x1) - d.x0;
       }
       pm.i2 = a.w.pair_i2[d.p0];
     };
+    // the c-th claim takes chunk chunk_order[c]
+    const int32_t* order = a.w.chunk_order;
     PMeta cur{}, nxt{};
     int c = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
-    if (c < n_chunks) load_meta(load_chunk(a.w.chunk_desc, c), cur);
+    if (c < n_chunks) load_meta(load_chunk(a.w.chunk_desc, order[c]), cur);
     int cn = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
     ChunkDesc dn{};
-    if (cn < n_chunks) dn = load_chunk(a.w.chunk_desc, cn);
+    if (cn < n_chunks) dn = load_chunk(a.w.chunk_desc, order[cn]);
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t use = (uint32_t)it >> 1;
@@ -519,16 +554,33 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
         release(s, -1);
         break;
       }
-      release(s, cur.i2);
+      // checkpoint role of a one-prefix chunk of a hot prefix
+      int ck = 0;
+      if (n_slots > 0 && cur.np == 1) {
+        const int sl = cur.p0 % n_slots;
+        const int pe0 = __shfl_sync(0xffffffffu, cur.pe, 0);
+        uint32_t v = 0;
+        if (!cur.whole) {                 // a later piece: reuse the slot if it is ready
+          if (lane == 0) v = ld_acquire_u32(ck_ready + sl);
+          v = __shfl_sync(0xffffffffu, v, 0);
+          if (v == (uint32_t)cur.p0 + 1u) ck = -(sl + 1);
+        } else if (pe0 > cur.x1) {        // the first piece: checkpoint its P2
+          if (lane == 0) v = atomicCAS(ck_owner + sl, 0u, (uint32_t)cur.p0 + 1u);
+          v = __shfl_sync(0xffffffffu, v, 0);
+          if (v == 0u) ck = sl + 1;
+        }
+        if (ck < 0 && lane == 0) atomicAdd(&a.w.ctl->ckpt_reused, 1);
+      }
+      release(s, ck < 0 ? -1 + ck : cur.i2);   // -2 - slot: the copier loads the checkpoint
       float* G2s = base + s * C::STAGE_F;
       float* P1n = G2s + C::F_G2;
       float* G3s = P1n + C::F_P1;
-      // G1[i1_p] planes: per prefix, lane = plane | j1 | piece
+      // G1[i1_p] planes: per prefix, lane = plane | j1 | piece (not for a reused P2)
 #pragma unroll
       for (int pp = 0; pp < C::CP; ++pp) {
         const int i1 = __shfl_sync(0xffffffffu, cur.gi1, pp);
         const int plane = lane >> 4, j1 = (lane >> 2) & 3, q = lane & 3;
-        if (pp < cur.np)
+        if (pp < cur.np && ck >= 0)
           cp_async16(reinterpret_cast<char*>(P1n) + plane * C::G1PLANE + (4 * pp + j1) * (2 * C::G1LD) + 16 * q,
                      (plane ? a.w.g1l : a.w.g1h) + ((size_t)i1 * 4 + j1) * C::R + 8 * q);
       }
@@ -579,10 +631,11 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
         m.np = cur.np;
         m.npairs = npairs;
         m.end = 0;
+        m.ck = ck;
         mbar_arrive(&full[s]);
       }
       ChunkDesc dnn{};
-      if (cnn < n_chunks) dnn = load_chunk(a.w.chunk_desc, cnn);
+      if (cnn < n_chunks) dnn = load_chunk(a.w.chunk_desc, order[cnn]);
       c = cn;
       cur = nxt;
       cn = cnn;
@@ -601,11 +654,28 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
     const float* G2s = base + s * C::STAGE_F;
     const float* P1n = G2s + C::F_G2;
     const float* G3s = P1n + C::F_P1;
-    if (m.np > 4) mma_fwd_stage2<CW, 2>(G2s, P1n, P2, warp, lane);
-    else mma_fwd_stage2<CW, 1>(G2s, P1n, P2, warp, lane);
+    const int ck = m.ck;
+    if (ck >= 0) {
+      if (m.np > 4) mma_fwd_stage2<CW, 2>(G2s, P1n, P2, warp, lane);
+      else mma_fwd_stage2<CW, 1>(G2s, P1n, P2, warp, lane);
+      named_sync(1, 32 * CW);
+      if (ck > 0) {                 // checkpoint: the prefix's P2 planes to slot ck - 1
+        char* dst = ck_data + (size_t)(ck - 1) * C::CKB;
+        for (int e = tid; e < C::CKB / 16; e += 32 * CW) {
+          const int plane = e / (C::PPB / 16), q = e - plane * (C::PPB / 16);
+          *reinterpret_cast<uint4*>(dst + plane * C::PPB + 16 * q) =
+              *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(P2) + plane * C::P2PLANE + 16 * q);
+        }
+      }
+      mma_fwd_stage3<CW>(m, smem_addr(P2), smem_addr(G3s), a.w.g3th, a.w.g3tl, a.w.row_i3, a.w.rowbuf, warp, lane);
+    } else {                        // P2 from the checkpoint, staged in the G2 area
+      mma_fwd_stage3<CW>(m, smem_addr(G2s), smem_addr(G3s), a.w.g3th, a.w.g3tl, a.w.row_i3, a.w.rowbuf, warp, lane);
+    }
     named_sync(1, 32 * CW);
-    mma_fwd_stage3<CW>(m, smem_addr(P2), smem_addr(G3s), a.w.g3th, a.w.g3tl, a.w.row_i3, a.w.rowbuf, warp, lane);
-    named_sync(1, 32 * CW);
+    if (ck > 0 && tid == 0) {       // the slot's planes are written: publish them
+      __threadfence();
+      st_release_u32(ck_ready + ck - 1, (uint32_t)m.p0 + 1u);
+    }
     if (tid == 0) mbar_arrive(&empty[s]);
   }
 }

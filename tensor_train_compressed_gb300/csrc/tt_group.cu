@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(kScanThreads) k_chunks(ChunkArgs a) {
       const bool first = a.w.pair_row_start[p] == (int32_t)x;
       a.w.chunk_start[c] = (int32_t)x;
       a.w.chunk_desc[c] = make_int2((int32_t)x, p | (first ? (int32_t)0x80000000 : 0));
+      a.w.chunk_order[c] = c;          // claimed in row order on this path
       ++c;
     }
     if (x == U - 1) {

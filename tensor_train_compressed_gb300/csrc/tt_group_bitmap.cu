@@ -456,7 +456,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
     // (d) first row of every prefix and the chunk starts it makes: its first row
     // starts a chunk when it is prefix 0 or a multiple of CP, its i2 differs from
     // the prefix before, or it or the prefix before holds more than CR rows; rows
-    // f0 + k CR (k >= 1) start the CR-row pieces of a hot prefix
+    // f0 + k CR (k >= 1) start the CR-row pieces of a hot prefix.  Counted as
+    // (head chunks) | (later pieces) << 16: the claim order puts every later
+    // piece after all head chunks (at most 8192 of either per CTA)
     uint32_t mine = 0;
 #pragma unroll 1
     for (uint32_t k = 0; k < Pt; ++k) {
@@ -476,7 +478,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
       const bool f = p == 0 || (p % (uint32_t)a.CP) == 0 || i2 != i2p || nr > a.CR ||
                      (int)nrp > a.CR;
       firsts |= (f ? 1u : 0u) << k;
-      mine += (f ? 1u : 0u) + (uint32_t)((nr - 1) / a.CR);
+      mine += (f ? 1u : 0u) + ((uint32_t)((nr - 1) / a.CR) << 16);
     }
     uint32_t ctot;
     chunk_ex = coop_scan(mine, &ctot, scan_sm);
@@ -486,14 +488,21 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
 
   // ------------------------------------------------------------------ phase E
   {
+    // (head chunks, later pieces) before this CTA, and the totals
     uint4 pr = make_uint4(0, 0, 0, 0);
     for (int cc = tid; cc < G; cc += kCoopThreads) {
       const uint32_t v = (uint32_t)__ldcg(a.cta_chunks + cc);
-      pr.y += v;
-      if (cc < c) pr.x += v;
+      pr.z += v & 0xffffu;
+      pr.w += v >> 16;
+      if (cc < c) {
+        pr.x += v & 0xffffu;
+        pr.y += v >> 16;
+      }
     }
     const uint4 ps = coop_sum4(pr, sum_sm);
-    int ci = (int)(ps.x + chunk_ex);
+    const uint32_t H = ps.z;                          // head chunks of the whole batch
+    uint32_t hr = ps.x + (chunk_ex & 0xffffu), tr = H + ps.y + (chunk_ex >> 16);
+    int ci = (int)(hr + tr - H);                      // natural (row-order) chunk number
 #pragma unroll 1
     for (uint32_t k = 0; k < Pt; ++k) {
       const uint32_t p = yt + k;
@@ -502,16 +511,18 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
       if ((firsts >> k) & 1u) {
         a.w.chunk_start[ci] = f0;
         a.w.chunk_desc[ci] = make_int2(f0, (int)p | (int32_t)0x80000000);
+        a.w.chunk_order[hr++] = ci;
         ++ci;
       }
       for (int x = f0 + a.CR; x < f1; x += a.CR) {
         a.w.chunk_start[ci] = x;
         a.w.chunk_desc[ci] = make_int2(x, (int)p);
+        a.w.chunk_order[tr++] = ci;
         ++ci;
       }
     }
     if (c == 0 && tid == 0) {
-      const int n = (int)ps.y;
+      const int n = (int)(ps.z + ps.w);
       a.w.ctl->n_chunks = n;
       a.w.chunk_start[n] = (int)U;
       a.w.chunk_desc[n] = make_int2((int)U, (int)P | (int32_t)0x80000000);

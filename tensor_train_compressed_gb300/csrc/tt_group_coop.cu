@@ -339,7 +339,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
   // multiple of CP, its i2 differs from prefix p-1's, or p or p-1 holds more
   // than CR rows; rows f0 + k CR (k >= 1) start the CR-row pieces of a hot
   // prefix.  Each thread owns Pt consecutive prefixes of the CTA's range and
-  // issues all their loads at once.
+  // issues all their loads at once.  Counted as (head chunks) | (later pieces)
+  // << 16 (at most 8192 heads and 2^16 - 1 pieces per CTA for the batches this
+  // launch takes): the claim order puts every later piece after all heads.
   {
     const int U = u_rows, P = u_pairs;
     const int Lp = (P + G - 1) / G;
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
         f0s[k] = f0;
         nrs[k] = nr;
         firsts |= (f ? 1u : 0u) << k;
-        mine += (f ? 1u : 0u) + (uint32_t)((nr - 1) / a.CR);
+        mine += (f ? 1u : 0u) + ((uint32_t)((nr - 1) / a.CR) << 16);
       }
     }
     uint32_t tot;
@@ -375,11 +377,17 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
     uint4 pr = make_uint4(0, 0, 0, 0);
     for (int cc = tid; cc < G; cc += kCoopThreads) {
       const uint32_t v = (uint32_t)__ldcg(a.chunk_counts + cc);
-      pr.y += v;
-      if (cc < c) pr.x += v;
+      pr.z += v & 0xffffu;
+      pr.w += v >> 16;
+      if (cc < c) {
+        pr.x += v & 0xffffu;
+        pr.y += v >> 16;
+      }
     }
     const uint4 ps = coop_sum4(pr, sum_sm);
-    int ci = (int)(ps.x + ex);
+    const uint32_t H = ps.z;                          // head chunks of the whole batch
+    uint32_t hr = ps.x + (ex & 0xffffu), tr = H + ps.y + (ex >> 16);
+    int ci = (int)(hr + tr - H);                      // natural (row-order) chunk number
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
       const int pp = yt + k;
@@ -387,18 +395,20 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
         if ((firsts >> k) & 1u) {
           a.w.chunk_start[ci] = f0s[k];
           a.w.chunk_desc[ci] = make_int2(f0s[k], pp | (int32_t)0x80000000);
+          a.w.chunk_order[hr++] = ci;
           ++ci;
         }
         for (int x = f0s[k] + a.CR; x < f0s[k] + nrs[k]; x += a.CR) {
           a.w.chunk_start[ci] = x;
           a.w.chunk_desc[ci] = make_int2(x, pp);
+          a.w.chunk_order[tr++] = ci;
           ++ci;
         }
       }
     }
     stamp();
     if (c == 0 && tid == 0) {
-      const int n = (int)ps.y;
+      const int n = (int)(ps.z + ps.w);
       a.w.ctl->n_chunks = n;
       a.w.chunk_start[n] = U;
       a.w.chunk_desc[n] = make_int2(U, P | (int32_t)0x80000000);

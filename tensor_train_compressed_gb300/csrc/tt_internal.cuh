@@ -27,6 +27,7 @@ constexpr int kSSlice = 64;                 // sorted positions per warp in the 
 constexpr int kMaxSmemFloats = 53248;       // 208 KB of shared memory per CTA
 constexpr int kMaxTables = 8;               // tables of one tt_emb_forward_tables call
 constexpr int kMaxCores = 8;                // cores of one chain (tt_emb_*_d)
+constexpr int kCkptSlots = 1024;            // L2 checkpoint slots of prefix partials
 
 // status word bits
 constexpr uint32_t kStIndex = 1u;
@@ -56,13 +57,13 @@ struct Ctl {
   int32_t n_chunks;       // work chunks
   uint32_t status;        // kSt* bits
   int32_t method;         // grouping that ran: kGroupBitmap, kGroupCoop or kGroupMulti
+  int32_t ckpt_reused;    // chunks of the last forward that reused a checkpointed P2
   uint32_t sort_tile_ctr[kMaxPasses];
   uint32_t seg_tile_ctr;
   uint32_t chunk_tile_ctr;
   uint32_t fwd_chunk_ctr;
   uint32_t bwd_chunk_ctr;
   uint32_t split_valid;   // the bf16 split planes hold the cores split_src (reset by every grouping)
-  uint32_t pad0[1];
   unsigned long long split_src[3];   // G1, G2, G3 addresses the planes were split from
   uint32_t pad[42];
 };
@@ -100,7 +101,7 @@ struct Shape {
 
 // Workspace layout (byte offsets from the workspace base; 256-aligned).
 struct Layout {
-  size_t ctl, hist, zero_end, sort_status, keysA, keysB, bag_of, uid, perm;
+  size_t ctl, hist, ckpt, zero_end, sort_status, keysA, keysB, bag_of, uid, perm;
   size_t row_start, row_i3, row_pair, pair_row_start, pair_i1, pair_i2;
   size_t seg_status, chunk_start, chunk_desc, chunk_status, coop, rowbuf, total;
   size_t g1h, g1l, g2h, g2l;   // bf16 split planes of G1 and G2 (tensor-core shape only; their
@@ -114,6 +115,8 @@ struct Layout {
 struct WS {
   Ctl* ctl;
   uint32_t* hist;          // [kHistCopies][kMaxPasses][kRadix]
+  uint32_t* ckpt;          // [2][kCkptSlots] checkpoint slot owner / ready words (prefix + 1)
+  int32_t* chunk_order;    // [chunks] claim order of the work chunks (aliases keysB)
   uint32_t* sort_status;   // [kMaxPasses][n_sort_tiles][kRadix]
   uint64_t* keysA;
   uint64_t* keysB;
@@ -132,6 +135,7 @@ struct WS {
   uint32_t* chunk_status;           // [n_scan_tiles]
   void* coop;                       // scratch of the cooperative grouping
   float* rowbuf;                    // [rowbuf_rows + 1][D]; the last row stays zero
+  int64_t rowbuf_rows;
   uint16_t* g1h;                    // bf16 planes hi / lo of G1 [m1][n1][R1] and G2
   uint16_t* g1l;                    // [m2][R1][n2 R2] (x = hi + lo + O(2^-18 |x|)), written
   uint16_t* g2h;                    // per call by k_split_cores; null unless the shape
@@ -164,6 +168,15 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 }
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {

@@ -155,6 +155,13 @@ def test_forward_full_size_sampled(cfg, table):
     # against the oracle's, element by element
     g = _check_grouping(x, st["ws"])
     assert g["U_r"] == np.unique(x.indices).size and g["n_valid"] == x.nnz
+    if cfg in (3, 5):
+        # the later pieces of hot prefixes took their P2 from the L2 checkpoint (the
+        # sampled bags above include rows made that way: the hot rows are in most bags)
+        cs = g["chunk_start"]
+        pieces = sum(1 for c in range(g["n_chunks"])
+                     if g["pair_row_start"][g["row_pair"][cs[c]]] != cs[c])
+        assert 0 < g["ckpt_reused"] <= pieces, (g["ckpt_reused"], pieces)
 
 
 def _sms():
