@@ -236,10 +236,10 @@ def weak_throughput(units_per_rank: int, world: int, ms_max: float) -> float:
 class Workload:
     """Device-resident inputs of one workload plus its captured step graphs."""
 
-    def __init__(self, cfg: int, train: bool, torch, tte, stream):
+    def __init__(self, cfg: int, train: bool, torch, tte, stream, mapping=None):
         from tensor_train_compressed_gb300.inputs import make_inputs
         self.torch, self.tte, self.stream = torch, tte, stream
-        self.x = x = make_inputs(cfg, with_grad=train)
+        self.x = x = make_inputs(cfg, with_grad=train, mapping=mapping)
         self.train = train
         dev = torch.device("cuda")
         self.cores0 = [torch.from_numpy(c).to(dev) for c in x.cores]
@@ -287,10 +287,9 @@ class Workload:
         n = self.tte.tt_emb_profile_stop() if profile else 0
         return g, n
 
-    def counts(self):
-        g = self.tte.read_grouping(self.x.m, self.x.n, self.x.R, self.x.nnz, self.x.num_bags,
-                                   self.ws)
-        return g["U_12"], g["U_r"], g["n_valid"], g["status"]
+    def grouping(self):
+        return self.tte.read_grouping(self.x.m, self.x.n, self.x.R, self.x.nnz, self.x.num_bags,
+                                      self.ws)
 
 
 class MultiTableWorkload(Workload):
@@ -324,14 +323,9 @@ class MultiTableWorkload(Workload):
     def restore(self):
         pass                                # the cores never change
 
-    def table_counts(self):
-        """(U_12, U_r, n_valid, status) of every table after one call."""
-        self.tte.tt_emb_forward_tables(self.tables)
-        res = []
-        for x, t in zip(self.xs, self.tables):
-            g = self.tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, t["workspace"])
-            res.append((g["U_12"], g["U_r"], g["n_valid"], g["status"]))
-        return res
+    def groupings(self):
+        return [self.tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, t["workspace"])
+                for x, t in zip(self.xs, self.tables)]
 
 
 def time_replays(torch, wl, graph, steps, flush, profile_n=0):
@@ -358,6 +352,95 @@ def time_replays(torch, wl, graph, steps, flush, profile_n=0):
     return times, per_kernel
 
 
+# The workloads of one bench run: (name, config, training step, Zipf rank -> row mapping).
+# "train" is the step the headline value is measured on; the others are lines beside it.
+WORKLOADS = (("train", TRAIN_CFG, True, None), ("forward", FWD_CFG, False, None),
+             ("forward8", MULTI_CFG, False, None), ("config1", 1, False, None),
+             ("config2", 2, False, None), ("forward_permuted", FWD_CFG, False, "permuted"),
+             ("train_permuted", TRAIN_CFG, True, "permuted"))
+
+
+def counts_of(g, x) -> dict:
+    """Unique prefixes / rows / chunks of one grouping, and the algorithmic work of the batch."""
+    a = algorithmic(x, g["U_12"], g["U_r"])
+    a.update(n_chunks=g["n_chunks"], method=g["method"], n_valid=g["n_valid"],
+             ckpt_reused=g["ckpt_reused"])
+    return a
+
+
+def add_counts(alls):
+    tot = {}
+    for a in alls:
+        for k in ("U_12", "U_r", "nnz", "B", "fwd_contract", "pool", "fwd_bytes", "n_chunks"):
+            tot[k] = tot.get(k, 0) + a[k]
+    return tot
+
+
+def kernel_work(name: str, a: dict, x, train: bool):
+    """Algorithmic work of one launch of kernel `name` on a batch with counts `a`:
+    ("flop", F) for the contraction kernels (each unique prefix and unique row once),
+    ("bytes", B) for the others (the bytes the method itself must read and write once
+    at the DRAM level), or None."""
+    nnz, B, D, U_r, U_12 = a["nnz"], a["B"], x.D, a["U_r"], a["U_12"]
+    nc = a.get("n_chunks", 0)
+    if name in ("k_fwd_mma", "k_fwd_tiled", "k_fwd_generic"):
+        return "flop", a["fwd_contract"]
+    if name in ("k_bwd_mma", "k_bwd_generic"):
+        return "flop", a["bwd_contract"]
+    if name.startswith("k_group"):
+        lists = 8 * nnz + 4 * U_r if train else 0          # perm + row_start
+        return "bytes", (8 * nnz + 8 * (B + 1) + 4 * nnz + lists + 8 * U_r + 12 * U_12
+                         + 16 * nc)
+    if name == "k_pool":
+        return "bytes", 8 * (B + 1) + 4 * nnz + 4 * nnz + 4 * B * D
+    if name == "k_s_gather":
+        return "bytes", 12 * nnz + 4 * B * D + 4 * U_r * D
+    return None
+
+
+def kernel_roofline(name, per_launch_ms, a, x, train, p_fp32, pk, sms, which):
+    """Achieved rate of one kernel against the peak of what bounds it."""
+    work = kernel_work(name, a, x, train)
+    out = {"kernel": name, "avg_launch_ms": round(per_launch_ms, 5)}
+    if work is None:
+        out.update(bound="hbm", achieved=None, peak=pk["hbm_gbs"], unit="GB/s", frac=None,
+                   traffic=None)
+        return out
+    kind, amount = work
+    if kind == "bytes":
+        ach = amount / (per_launch_ms * 1e-3) / 1e9
+        out.update(bound="hbm", achieved=round(ach, 1), peak=pk["hbm_gbs"], unit="GB/s",
+                   frac=round(ach / pk["hbm_gbs"], 4), traffic=stored_traffic(name, which),
+                   algorithmic_bytes_per_launch=int(amount),
+                   peak_source="measured copy bandwidth (MEASURED_PEAKS.json)")
+        return out
+    ach = amount / (per_launch_ms * 1e-3) / 1e12
+    out.update(bound="alu", achieved=round(ach, 3), peak=round(p_fp32, 2), unit="TFLOP/s",
+               frac=round(ach / p_fp32, 4), traffic=stored_traffic(name, which),
+               algorithmic_flop_per_launch=int(amount),
+               peak_source=f"{sms} SMs x 128 FP32 lanes x 2 x {pk['sm_max_mhz']:.0f} MHz (nominal "
+                           "FFMA rate; a probe on this GPU measured 115 FFMA MAC/SM/clk, 90% "
+                           "of the nominal 128)")
+    if name in TENSOR_SPLIT_KERNELS:
+        pt = pk["bf16_tflops"] / 3.0
+        out["roofline_tensor"] = {
+            "bound": "tensor", "achieved": round(ach, 3), "peak": round(pt, 1), "unit": "TFLOP/s",
+            "frac": round(ach / pt, 4),
+            "peak_source": f"measured bf16 dense burst {pk['bf16_tflops']:.1f} TFLOP/s / 3 bf16 "
+                           "products per fp32-level product (three-term split)"}
+    return out
+
+
+def call_roofline(a, ms, p_fp32, pk):
+    """North-star roofline of a whole forward call: the larger of the unique-prefix FLOPs
+    at the FP32 peak and the index + offset + output bytes at the HBM peak."""
+    F = a["fwd_contract"] + a["pool"]
+    t_roof = max(F / (p_fp32 * 1e12), a["fwd_bytes"] / (pk["hbm_gbs"] * 1e9))
+    return {"T_roof_us": round(t_roof * 1e6, 3), "T_call_us": round(ms * 1e3, 3),
+            "frac": round(t_roof / (ms * 1e-3), 4), "F_unique_flop": int(F),
+            "bytes": int(a["fwd_bytes"])}
+
+
 def run_ours(args, rank, world, dist):
     import torch
 
@@ -371,18 +454,19 @@ def run_ours(args, rank, world, dist):
     uuid = str(getattr(props, "uuid", ""))
     gpu_id = uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local))
     pk = peaks()
-    p_fp32 = fp32_peak_tflops(props.multi_processor_count, pk["sm_max_mhz"])
+    sms = props.multi_processor_count
+    p_fp32 = fp32_peak_tflops(sms, pk["sm_max_mhz"])
     stream = torch.cuda.Stream()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
     result = {}
-    todo = (("train", TRAIN_CFG, True), ("forward", FWD_CFG, False),
-            ("forward8", MULTI_CFG, False))
+    todo = WORKLOADS
     if args.only:
         todo = tuple(t for t in todo if t[0] == args.only)
-    for name, cfg, train in todo:
+    for name, cfg, train, mapping in todo:
+        main = name == "train"
         wl = (MultiTableWorkload(cfg, torch, tte, stream) if name == "forward8"
-              else Workload(cfg, train, torch, tte, stream))
+              else Workload(cfg, train, torch, tte, stream, mapping))
         with torch.cuda.stream(stream):
             for _ in range(2):          # eager warm-up (also settles the library's caches)
                 wl.restore()
@@ -393,17 +477,9 @@ def run_ours(args, rank, world, dist):
             if rc != 0:
                 raise RuntimeError(f"device status {bits} on workload {name}")
         if name == "forward8":
-            alg = {}
-            nv = 0
-            for x, (u12, ur, v, _) in zip(wl.xs, wl.table_counts()):
-                a1 = algorithmic(x, u12, ur)
-                for k in ("U_12", "U_r", "nnz", "B", "fwd_contract", "pool", "fwd_bytes"):
-                    alg[k] = alg.get(k, 0) + a1[k]
-                nv += v
-            stream.synchronize()
+            alg = add_counts([counts_of(g, x) for g, x in zip(wl.groupings(), wl.xs)])
         else:
-            U_12, U_r, nv, _ = wl.counts()
-            alg = algorithmic(wl.x, U_12, U_r)
+            alg = counts_of(wl.grouping(), wl.x)
         with torch.cuda.stream(stream):   # creates the timing events before any capture
             tte.tt_emb_profile_start()
             wl.restore()
@@ -412,6 +488,7 @@ def run_ours(args, rank, world, dist):
         stream.synchronize()
         graph, _ = wl.capture()
         pgraph, n_launch = wl.capture(profile=True)
+        steps = args.steps if main or name in ("forward", "forward8") else max(3, args.steps // 2)
         time_replays(torch, wl, graph, max(args.warmup, 3), flush)
         if dist is not None:
             dist.barrier()
@@ -419,25 +496,30 @@ def run_ours(args, rank, world, dist):
         clocks = ClockSampler(gpu_id)
         clocks.start()
         t0 = time.perf_counter()
-        times, _ = time_replays(torch, wl, graph, args.steps, flush)
+        times, _ = time_replays(torch, wl, graph, steps, flush)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         clk = clocks.stop()
         if dist is not None:
             dist.barrier()
-        _, kern = time_replays(torch, wl, pgraph, max(3, min(args.steps, 10)), flush, n_launch)
-        ms = float(np.mean(times))
-        result[name] = dict(wl=wl, alg=alg, ms=ms, times=times, wall=wall, clocks=clk,
-                            kern=kern, n_launch=n_launch, n_valid=nv)
+        reps = max(3, min(steps, 10))
+        _, kern = time_replays(torch, wl, pgraph, reps, flush, n_launch)
+        if not main:                      # the last grouping of the timed replays
+            if name == "forward8":
+                alg["ckpt_reused"] = 0
+            else:
+                alg["ckpt_reused"] = wl.grouping()["ckpt_reused"]
+        result[name] = dict(wl=wl, alg=alg, ms=rank_max(dist, float(np.mean(times))),
+                            times=times, wall=wall, clocks=clk, kern=kern, reps=reps,
+                            n_launch=n_launch, steps=steps)
 
     if args.only:
         # single-workload run (profiling driver): a short report, no e2e / baseline
         r = result[args.only]
-        ms = rank_max(dist, r["ms"])
         if rank == 0:
-            return {"only": args.only, "ms_per_step": round(ms, 5),
-                    "lookups_per_s": round(weak_throughput(r["alg"]["nnz"], world, ms), 1),
-                    "kernels": {k: round(v[0] / max(1, v[1]), 5) for k, v in r["kern"].items()}}
+            return {"only": args.only, "ms_per_step": round(r["ms"], 5),
+                    "lookups_per_s": round(weak_throughput(r["alg"]["nnz"], world, r["ms"]), 1),
+                    "kernels": {k: round(v[0] / r["reps"], 5) for k, v in r["kern"].items()}}
         return None
 
     # ---- end to end through the public API from pinned host buffers (training step)
@@ -469,96 +551,66 @@ def run_ours(args, rank, world, dist):
             e2e_times.append(e0.elapsed_time(e1))
     h2d = idx_h.numel() * 8 + off_h.numel() * 8 + g_h.numel() * 4
     d2h = out_h.numel() * 4
-
-    tr, fw, f8 = result["train"], result["forward"], result["forward8"]
-    ms_train = rank_max(dist, tr["ms"])
-    ms_fwd = rank_max(dist, fw["ms"])
-    ms_f8 = rank_max(dist, f8["ms"])
     ms_e2e = rank_max(dist, float(np.mean(e2e_times)))
     if rank != 0:
         return None
 
-    def per_step_kernel_ms(r):
-        steps = max(1, min(len(r["times"]), 10))
-        reps = max(3, min(args.steps, 10))
-        return {k: v[0] / reps for k, v in r["kern"].items()}, steps
+    def kernels_ms(r):
+        return {k: v[0] / r["reps"] for k, v in r["kern"].items()}
 
-    def roofline_of(r, which):
-        """Dominant kernel of the step, its algorithmic FLOPs per launch and its live duration."""
-        kms, _ = per_step_kernel_ms(r)
+    def launches(r):
+        return {k: v[1] / r["reps"] for k, v in r["kern"].items()}
+
+    def dominant(r, which):
+        kms = kernels_ms(r)
         dom = max(kms, key=kms.get)
-        a = r["alg"]
-        launches_per_step = {k: v[1] for k, v in r["kern"].items()}
-        reps = max(3, min(args.steps, 10))
-        flops = {"k_fwd_generic": a["fwd_contract"], "k_fwd_tiled": a["fwd_contract"],
-                 "k_fwd_mma": a["fwd_contract"], "k_bwd_generic": a["bwd_contract"],
-                 "k_bwd_mma": a["bwd_contract"], "k_pool": a["pool"], "k_s_gather": a["s_gather"]}
-        per_launch_ms = kms[dom] / max(1, launches_per_step[dom] / reps)
-        out = {"kernel": dom, "share": round(kms[dom] / sum(kms.values()), 4)}
-        # algorithmic bytes of the non-contraction kernels (DRAM-level minimum)
-        nnz, B, D = a["nnz"], a["B"], r["wl"].x.D
-        npass = 3 if r["wl"].x.m[0] * r["wl"].x.m[1] * r["wl"].x.m[2] < (1 << 24) else 4
-        nbytes = {
-            "k_group_coop": 8 * nnz + 8 * (B + 1) + 16 * nnz * npass + 8 * nnz
-                            + 12 * a["U_r"] + 12 * a["U_12"],
-            "k_pool": 4 * nnz + 8 * (B + 1) + 4 * nnz * D + 4 * B * D,
-            "k_s_gather": 12 * nnz + 4 * nnz * D + 4 * a["U_r"] * D,
-        }
-        if dom in nbytes and dom not in flops:
-            ach = nbytes[dom] / (per_launch_ms * 1e-3) / 1e9
-            out.update(bound="hbm", achieved=round(ach, 1), peak=pk["hbm_gbs"], unit="GB/s",
-                       frac=round(ach / pk["hbm_gbs"], 4), traffic=stored_traffic(dom, which),
-                       algorithmic_bytes_per_launch=nbytes[dom],
-                       avg_launch_ms=round(per_launch_ms, 5))
-        elif dom in flops:
-            ach = flops[dom] / (per_launch_ms * 1e-3) / 1e12
-            out.update(bound="alu", achieved=round(ach, 3), peak=round(p_fp32, 2),
-                       unit="TFLOP/s", frac=round(ach / p_fp32, 4),
-                       traffic=stored_traffic(dom, which),
-                       algorithmic_flop_per_launch=flops[dom],
-                       avg_launch_ms=round(per_launch_ms, 5),
-                       peak_source=f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x "
-                                   f"{pk['sm_max_mhz']:.0f} MHz (fp32-accurate arithmetic)")
-            if dom in TENSOR_SPLIT_KERNELS:
-                pt = pk["bf16_tflops"] / 3.0
-                out["roofline_tensor"] = {
-                    "bound": "tensor", "achieved": round(ach, 3), "peak": round(pt, 1),
-                    "unit": "TFLOP/s", "frac": round(ach / pt, 4),
-                    "peak_source": f"measured bf16 dense burst {pk['bf16_tflops']:.1f} TFLOP/s / 3 "
-                                   "tensor products per fp32-accurate product (three-term split)"}
-        else:
-            out.update(bound="hbm", achieved=None, peak=pk["hbm_gbs"], unit="GB/s", frac=None,
-                       traffic=None, avg_launch_ms=round(per_launch_ms, 5))
-        return out, {k: round(v, 5) for k, v in sorted(kms.items(), key=lambda kv: -kv[1])}
+        per = kms[dom] / max(1.0, launches(r)[dom])
+        roof = kernel_roofline(dom, per, r["alg"], r["wl"].x, r["wl"].train, p_fp32, pk, sms,
+                               which)
+        roof["share"] = round(kms[dom] / sum(kms.values()), 4)
+        return roof, {k: round(v, 5) for k, v in sorted(kms.items(), key=lambda kv: -kv[1])}
 
-    roof_tr, kms_tr = roofline_of(tr, "train")
-    roof_fw, kms_fw = roofline_of(fw, "forward")
-    a = fw["alg"]
-    F_fwd = a["fwd_contract"] + a["pool"]
-    t_roof = max(F_fwd / (p_fp32 * 1e12), a["fwd_bytes"] / (pk["hbm_gbs"] * 1e9))
-    fwd_call = {"T_roof_us": round(t_roof * 1e6, 3), "T_call_us": round(ms_fwd * 1e3, 3),
-                "frac": round(t_roof / (ms_fwd * 1e-3), 4),
-                "F_unique_flop": F_fwd, "bytes": a["fwd_bytes"]}
-    # eight tables: every kernel launches once per table; the contraction
-    # kernel's achieved rate is the tables' unique-prefix FLOPs over its time
+    def grouping_roofline(r, which):
+        kms, nl = kernels_ms(r), launches(r)
+        g = next((k for k in kms if k.startswith("k_group")), None)
+        if g is None:
+            return None
+        return kernel_roofline(g, kms[g] / max(1.0, nl[g]), r["alg"], r["wl"].x, r["wl"].train,
+                               p_fp32, pk, sms, which)
+
+    def forward_line(r, workload, which):
+        a = r["alg"]
+        roof, kms = dominant(r, which)
+        return {
+            "workload": workload,
+            "lookups_per_s": round(weak_throughput(a["nnz"], world, r["ms"]), 1),
+            "bags_per_s": round(a["B"] * world / (r["ms"] * 1e-3), 1),
+            "ms_per_call": round(r["ms"], 5), "lookups": a["nnz"],
+            "unique_rows": a["U_r"], "unique_prefixes": a["U_12"], "chunks": a["n_chunks"],
+            "grouping_method": a.get("method"), "prefix_partials_reused": a.get("ckpt_reused"),
+            "roofline_call": call_roofline(a, r["ms"], p_fp32, pk),
+            "roofline": roof, "roofline_grouping": grouping_roofline(r, which),
+            "kernels_ms_per_call": kms, "clocks": r["clocks"],
+        }
+
+    tr, fw, f8 = result["train"], result["forward"], result["forward8"]
+    at = tr["alg"]
+    nnz_tr = tr["wl"].x.nnz
+    value = weak_throughput(nnz_tr, world, tr["ms"])
+    roof_tr, kms_tr = dominant(tr, "train")
     a8 = f8["alg"]
-    kms_f8, _ = per_step_kernel_ms(f8)
-    F8 = a8["fwd_contract"] + a8["pool"]
-    t_roof8 = max(F8 / (p_fp32 * 1e12), a8["fwd_bytes"] / (pk["hbm_gbs"] * 1e9))
-    dom8 = max(kms_f8, key=kms_f8.get)
+    kms_f8 = kernels_ms(f8)
     contract8 = next((k for k in ("k_fwd_mma", "k_fwd_tiled", "k_fwd_generic") if k in kms_f8), None)
     f8_line = {
         "workload": "8 tables of 1e5, 1e6, 4e6, 1e7, 2e7, 3e7, 4e7, 4e7 rows (3 near-equal "
                     "factors each), D=128=4x8x4, R1=R2=64, 32768 bags each of max(Poisson(20),1) "
                     "Zipf(1.4) lookups, forward, one tt_emb_forward_tables call",
-        "lookups_per_s": round(weak_throughput(a8["nnz"], world, ms_f8), 1),
-        "bags_per_s": round(a8["B"] * world / (ms_f8 * 1e-3), 1),
-        "ms_per_batch": round(ms_f8, 5),
+        "dtype": "f32 (FP32 FFMA chunk kernel; no tensor-core split at R=64)",
+        "lookups_per_s": round(weak_throughput(a8["nnz"], world, f8["ms"]), 1),
+        "bags_per_s": round(a8["B"] * world / (f8["ms"] * 1e-3), 1),
+        "ms_per_batch": round(f8["ms"], 5),
         "lookups": a8["nnz"], "unique_rows": a8["U_r"], "unique_prefixes": a8["U_12"],
-        "roofline_call": {"T_roof_us": round(t_roof8 * 1e6, 3), "T_call_us": round(ms_f8 * 1e3, 3),
-                          "frac": round(t_roof8 / (ms_f8 * 1e-3), 4), "F_unique_flop": F8,
-                          "bytes": a8["fwd_bytes"]},
-        "dominant_kernel": dom8,
+        "roofline_call": call_roofline(a8, f8["ms"], p_fp32, pk),
         "kernels_ms_per_batch": {k: round(v, 5) for k, v in sorted(kms_f8.items(),
                                                                      key=lambda kv: -kv[1])},
     }
@@ -567,9 +619,29 @@ def run_ours(args, rank, world, dist):
         f8_line["contraction"] = {"kernel": contract8, "bound": "alu", "achieved": round(ach8, 3),
                                   "peak": round(p_fp32, 2), "unit": "TFLOP/s",
                                   "frac": round(ach8 / p_fp32, 4)}
-    at = tr["alg"]
-    nnz_tr = tr["wl"].x.nnz
-    value = weak_throughput(nnz_tr, world, ms_train)
+    small = {}
+    for nm, cfg in (("config1", 1), ("config2", 2)):
+        r = result[nm]
+        ln = forward_line(r, CONFIG_NAMES[cfg] + ", forward only", nm)
+        ln["dtype"] = "f32 (FP32 FFMA chunk kernel)" if cfg == 1 else \
+            "f32 (FP32 FFMA tiled chunk kernel; no tensor-core split at R=16)"
+        small[nm] = ln
+    sens = {}
+    for nm, base in (("forward_permuted", fw), ("train_permuted", tr)):
+        r = result[nm]
+        a = r["alg"]
+        ln = {"workload": CONFIG_NAMES[r["wl"].x.cfg] + ", Zipf ranks mapped to rows through a "
+                          "seeded random permutation",
+              "lookups_per_s": round(weak_throughput(a["nnz"], world, r["ms"]), 1),
+              "ms_per_step": round(r["ms"], 5), "unique_rows": a["U_r"],
+              "unique_prefixes": a["U_12"], "grouping_method": a.get("method"),
+              "F_unique_flop": int(a["fwd_contract"] + a["pool"]),
+              "vs_identity_mapping_time": round(r["ms"] / base["ms"], 3),
+              "kernels_ms": {k: round(v, 5) for k, v in sorted(kernels_ms(r).items(),
+                                                                 key=lambda kv: -kv[1])}}
+        if nm == "forward_permuted":
+            ln["roofline_call"] = call_roofline(a, r["ms"], p_fp32, pk)
+        sens[nm] = ln
     cpu = cpu_baseline(args) if (world == 1 and not args.no_cpu_baseline) else None
     line = {
         "metric": METRIC,
@@ -578,12 +650,14 @@ def run_ours(args, rank, world, dist):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_train, 5),
+        "ms_per_step": round(tr["ms"], 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "f32 in/out; contractions as bf16x3 tensor-core products (hi/lo bf16 split, "
+                 "fp32 accumulate, ~4e-6 relative error per product)",
         "data": "synthetic (seeded cores, Zipf indices, Gaussian grad_out)",
+        "gpu_launches": tr["n_launch"] * args.steps,
         "config": {
             "workload": "training step: 47,952,000 rows = 360x360x370, D=128=4x8x4, "
                         "R1=R2=32, 32768 bags of U{10..30} Zipf(1.2) lookups, "
@@ -591,28 +665,22 @@ def run_ours(args, rank, world, dist):
                         "bf16 split of the cores",
             "global_batch": 32768 * world, "lookups_per_gpu": nnz_tr,
             "unique_rows": at["U_r"], "unique_prefixes": at["U_12"],
+            "grouping_method": at.get("method"),
             "parallelism": f"replicas x{world}",
             "l2": "flushed between timed steps (512 MB write outside the timed events, "
                   "after the cores and their split are restored)",
             "timing": "one CUDA graph replay per step, CUDA events on its stream",
         },
-        "bags_per_s": round(32768 * world / (ms_train * 1e-3), 1),
+        "bags_per_s": round(32768 * world / (tr["ms"] * 1e-3), 1),
         "roofline": roof_tr,
+        "roofline_grouping": grouping_roofline(tr, "train"),
         "kernels_ms_per_step": kms_tr,
-        "forward": {
-            "workload": "12,000,000 rows = 200x240x250, D=128=4x8x4, R1=R2=32, 32768 bags x "
-                        "20 Zipf(1.2) lookups, forward only, on the bf16 split of the cores "
-                        "made once when they were loaded",
-            "lookups_per_s": round(fw["wl"].x.nnz * world / (ms_fwd * 1e-3), 1),
-            "bags_per_s": round(32768 * world / (ms_fwd * 1e-3), 1),
-            "ms_per_call": round(ms_fwd, 5),
-            "unique_rows": a["U_r"], "unique_prefixes": a["U_12"],
-            "roofline_call": fwd_call,
-            "roofline": roof_fw,
-            "kernels_ms_per_call": kms_fw,
-            "clocks": fw["clocks"],
-        },
+        "forward": forward_line(fw, CONFIG_NAMES[FWD_CFG] + ", forward only (inference: "
+                                "TT_EMB_FORWARD_ONLY), on the bf16 split of the cores made "
+                                "once when they were loaded", "forward"),
         "forward_8_tables": f8_line,
+        "forward_small": small,
+        "sensitivity_permuted_zipf": sens,
         "e2e": {"value": round(nnz_tr * world / (ms_e2e * 1e-3), 1), "unit": "lookups/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 5),
@@ -620,35 +688,50 @@ def run_ours(args, rank, world, dist):
                         "grad_out -> device on a copy stream, forward on the kept core split "
                         "as soon as the lookups are in, backward, SGD + split; the pooled "
                         "output -> pinned host while the backward runs"},
-        "gpu_launches": tr["n_launch"] * args.steps,
         "clocks": tr["clocks"],
         "workspace_bytes": tr["wl"].ws_bytes,
         "wall_s_timed_region": round(tr["wall"], 4),
         "peaks": pk,
     }
+    line["forward"]["dtype"] = line["dtype"]
     if cpu is not None:
         line["cpu_baseline"] = cpu
+        if not args.no_oracle_matrix:
+            line["oracle_matrix"] = oracle_matrix()
     return line
+
+
+CONFIG_NAMES = {
+    1: "1000 rows = 10x10x10, D=16=2x4x2, R1=R2=4, 64 bags of U{1..4} uniform lookups",
+    2: "1,000,000 rows = 100^3, D=64=4x4x4, R1=R2=16, 4096 bags of 1 Zipf(1.05) lookup "
+       "over a random row permutation (a pure gather)",
+    3: "12,000,000 rows = 200x240x250, D=128=4x8x4, R1=R2=32, 32768 bags x 20 Zipf(1.2) lookups",
+    4: "8 tables, D=128, R1=R2=64, 32768 bags each of max(Poisson(20),1) Zipf(1.4) lookups",
+    5: "47,952,000 rows = 360x360x370, D=128=4x8x4, R1=R2=32, 32768 bags of U{10..30} "
+       "Zipf(1.2) lookups",
+}
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
 
 
-def _oracle_sample(bags: int):
+def _oracle_sample(bags: int, cfg: int = TRAIN_CFG, table: int = 0):
     from tensor_train_compressed_gb300.inputs import make_inputs
-    x = make_inputs(TRAIN_CFG, with_grad=True)
-    sel = np.arange(bags)
+    x = make_inputs(cfg, table=table, with_grad=cfg == TRAIN_CFG)
+    bags = min(bags, x.num_bags)
     idx = x.indices[:x.offsets[bags]]
     off = x.offsets[:bags + 1]
-    return x, idx, off, x.grad_out[sel]
+    g = x.grad_out[:bags] if x.grad_out is not None else None
+    return x, idx, off, g
 
 
 def oracle_step(x, idx, off, g, threads):
     import oracle
     oracle.forward(x.cores, x.m, x.n, x.R, idx, off, threads=threads)
-    dG = oracle.backward(g, x.cores, x.m, x.n, x.R, idx, off, threads=threads)
-    for k in range(3):
-        oracle.sgd(x.cores[k], dG[k], LR)
+    if g is not None:
+        dG = oracle.backward(g, x.cores, x.m, x.n, x.R, idx, off, threads=threads)
+        for k in range(3):
+            oracle.sgd(x.cores[k], dG[k], LR)
 
 
 def cpu_threads():
@@ -677,6 +760,40 @@ def cpu_baseline(args, target_s: float = 10.0) -> dict:
             "kind": "oracle",
             "sample": f"first {bags} bags ({len(idx)} lookups) of the training workload, "
                       f"fp64 forward + backward + SGD, {n} repetitions"}
+
+
+def oracle_rate(cfg: int, threads: int, target_s: float, table: int = 0) -> dict:
+    """Lookups/s of the oracle on the first bags of a workload, the sample grown until one
+    pass takes about target_s (forward; forward + backward + SGD for the training step)."""
+    bags = 16
+    while True:
+        x, idx, off, g = _oracle_sample(bags, cfg, table)
+        t0 = time.perf_counter()
+        oracle_step(x, idx, off, g, threads)
+        dt = time.perf_counter() - t0
+        full = x.offsets.shape[0] - 1
+        if dt >= target_s or bags >= full:
+            return {"lookups_per_s": round(len(idx) / dt, 1),
+                    "sample": f"first {min(bags, full)} bags ({len(idx)} lookups)"}
+        bags = min(full, max(bags * 2, int(bags * target_s / max(dt, 1e-4) * 1.1)))
+
+
+def oracle_matrix(target_s: float = 1.0) -> dict:
+    """The oracle at 1 thread and at every host thread on each workload (config 4: its
+    1e7-row table), forward; forward + backward + SGD for the training step."""
+    import oracle
+    oracle.build()
+    allt = cpu_threads()
+    res = {"cores": allt}
+    for cfg in (1, 2, 3, 4, 5):
+        table = 3 if cfg == 4 else 0
+        one = oracle_rate(cfg, 1, target_s, table)
+        many = oracle_rate(cfg, allt, target_s, table)
+        res[f"config{cfg}"] = {
+            "pass": "forward + backward + SGD" if cfg == TRAIN_CFG else "forward",
+            "threads_1": one["lookups_per_s"], f"threads_{allt}": many["lookups_per_s"],
+            "sample_threads_1": one["sample"], f"sample_threads_{allt}": many["sample"]}
+    return res
 
 
 def run_reference(args):
@@ -721,7 +838,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["train", "forward", "forward8"], default=None,
+    ap.add_argument("--no-oracle-matrix", action="store_true",
+                    help="skip the per-workload oracle timings (1 thread / all threads)")
+    ap.add_argument("--only", choices=[w[0] for w in WORKLOADS], default=None,
                     help="time one workload only (short report; used to drive ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

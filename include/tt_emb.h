@@ -19,8 +19,8 @@
  *
  * How it is computed (FlowTT, summary card, key innovations; FlowTT
  * abstract): lookups are grouped by their (i1, i2) prefix on the device (a
- * presence bitmap over the row keys when the batch is dense in its table,
- * else a radix sort + run segmentation), the prefix partial P2 = G1[i1].G2[i2] is
+ * radix sort + run segmentation, or for a forward-only call on a batch dense in
+ * its table a presence bitmap over the row keys), the prefix partial P2 = G1[i1].G2[i2] is
  * formed once per unique prefix and kept on chip, each unique row is formed
  * once from it, and rows are pooled per bag.  Persistent CTAs take work
  * chunks from an atomic queue so that Zipf-skewed prefixes do not stall the
@@ -83,12 +83,11 @@ int tt_emb_workspace_bytes(const int64_t m[3], const int32_t n[3], const int32_t
 
 /* Prefix grouping only (index decomposition, grouping by the (i2, i1, i3)
  * key, unique rows / unique (i1,i2) prefixes, work chunks), written into the
- * workspace.  Two methods give the same unique rows, prefixes, per-lookup
- * unique row and chunks: a presence bitmap over the M keys when the batch is
- * dense in its table (ceil(M / 32) <= 8 nnz, the bitmaps fit in the workspace's
- * unique-row buffer, and at most 8192 lookups per SM), else a radix sort.  They
- * differ only in the order of one row's lookups inside `perm` (see
- * tt_emb_grouping_view).  FlowTT summary card, key innovations ("prefix-based index
+ * workspace, by a radix sort.  (A forward called with TT_EMB_FORWARD_ONLY on a
+ * batch dense in its table -- ceil(M / 32) <= 8 nnz, at most 8192 lookups per
+ * SM -- groups by a presence bitmap over the M keys instead: the same unique
+ * rows, prefixes, per-lookup unique rows and chunks, without perm and
+ * row_start.)  FlowTT summary card, key innovations ("prefix-based index
  * grouping").  tt_emb_forward calls this itself. */
 int tt_emb_group(const int64_t m[3], const int32_t n[3], const int32_t R[4],
                  const int64_t* indices, int64_t nnz, const int64_t* offsets,
@@ -302,15 +301,13 @@ int tt_emb_get_error(const void* workspace, void* stream, int* device_status);
 typedef struct {
   const int32_t* counts;          /* [0] valid lookups, [1] U_r unique rows, [2] U_12 unique
                                      (i1,i2) prefixes, [3] work chunks, [4] status bits,
-                                     [5] grouping method: 1 key bitmap, 2 one-launch radix
-                                     sort, 3 multi-launch radix sort, 4 key bitmap without
-                                     perm / row_start (TT_EMB_FORWARD_ONLY), [6] work chunks
-                                     of the last forward that took their prefix partial from
-                                     the L2 checkpoint instead of forming it              */
-  const int32_t* perm;            /* [nnz]   lookup positions grouped by unique row in
-                                              (i2,i1,i3) order, out-of-range lookups last;
-                                              inside a row in position order after a radix
-                                              sort, in no fixed order after the key bitmap  */
+                                     [5] grouping method: 1 key bitmap (a forward-only
+                                     call: no perm, no row_start), 2 one-launch radix sort,
+                                     3 multi-launch radix sort, [6] work chunks of the last
+                                     forward that took their prefix partial from the L2
+                                     checkpoint instead of forming it                      */
+  const int32_t* perm;            /* [nnz]   lookup positions sorted by (i2,i1,i3, position);
+                                              out-of-range lookups last                     */
   const int32_t* row_start;       /* [U_r+1] first sorted position of each unique row         */
   const int32_t* row_i3;          /* [U_r]   i3 digit of each unique row                       */
   const int32_t* row_pair;        /* [U_r]   unique prefix of each unique row                  */
@@ -321,6 +318,8 @@ typedef struct {
   const int32_t* bag_of;          /* [nnz]   bag of each lookup (written by tt_emb_backward)   */
   const int32_t* chunk_start;     /* [chunks+1] first unique row of each work chunk             */
   const float* rowbuf;            /* [U_r][D] unique rows (after a forward)                    */
+  const int32_t* chunk_order;     /* [chunks]   the chunk each forward claim takes (a hot
+                                                prefix's later pieces after all other chunks)  */
 } tt_emb_grouping;
 
 int tt_emb_grouping_view(const int64_t m[3], const int32_t n[3], const int32_t R[4],

@@ -45,15 +45,14 @@ def read_grouping(m, n, R, nnz: int, num_bags: int, workspace: torch.Tensor) -> 
     counts = arr("counts", 7)
     nv, ur, up, nc = (int(v) for v in counts[:4])
     D = int(n[0] * n[1] * n[2])
-    method = {1: "bitmap", 2: "coop_sort", 3: "multi_sort",
-              4: "bitmap_nolists"}.get(int(counts[5]), "none")
+    method = {1: "bitmap", 2: "coop_sort", 3: "multi_sort"}.get(int(counts[5]), "none")
     return dict(n_valid=nv, U_r=ur, U_12=up, n_chunks=nc, status=int(counts[4]), method=method,
                 ckpt_reused=int(counts[6]),
                 perm=arr("perm", nnz), row_start=arr("row_start", ur + 1),
                 row_i3=arr("row_i3", ur), row_pair=arr("row_pair", ur),
                 pair_row_start=arr("pair_row_start", up + 1), pair_i1=arr("pair_i1", up),
                 pair_i2=arr("pair_i2", up), uid=arr("uid", nnz), bag_of=arr("bag_of", nnz),
-                chunk_start=arr("chunk_start", nc + 1),
+                chunk_start=arr("chunk_start", nc + 1), chunk_order=arr("chunk_order", nc),
                 rowbuf=arr("rowbuf", ur * D, torch.float32).reshape(ur, D))
 
 

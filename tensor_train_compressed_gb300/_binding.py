@@ -66,7 +66,7 @@ class HostBatch(ctypes.Structure):
 class Grouping(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "counts", "perm", "row_start", "row_i3", "row_pair", "pair_row_start", "pair_i1",
-        "pair_i2", "uid", "bag_of", "chunk_start", "rowbuf")]
+        "pair_i2", "uid", "bag_of", "chunk_start", "rowbuf", "chunk_order")]
 
 
 _lib = None

@@ -635,6 +635,7 @@ int tt_emb_grouping_view(const int64_t m[3], const int32_t n[3], const int32_t R
   view->bag_of = w.bag_of;
   view->chunk_start = w.chunk_start;
   view->rowbuf = w.rowbuf;
+  view->chunk_order = w.chunk_order;
   return TT_EMB_OK;
 }
 

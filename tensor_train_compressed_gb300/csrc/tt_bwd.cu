@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(256) k_s_zero(WS w, int D, int span, int64_t r
                                                 SplitArgs sp, int reuse) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (reuse && w.ctl->method == kGroupBitmapNoLists) {
+  if (reuse && w.ctl->method == kGroupBitmap) {
     // the grouping came from a forward-only call and has no per-row lookup
     // lists: report it, and leave the backward's later kernels no lookups and
     // no chunks, so that the core gradients stay as they are

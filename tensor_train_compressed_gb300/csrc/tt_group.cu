@@ -388,10 +388,10 @@ int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* in
       cudaSuccess)
     return TT_EMB_ERR_CUDA;
   if (nnz == 0) return TT_EMB_OK;   // counts stay zero; row_start etc. are never read
-  {
-    // a batch dense in its table: bitmap of the keys, no sort
+  if (!lists) {
+    // a forward-only call on a batch dense in its table: bitmap of the keys, no sort
     const int rc = launch_group_bitmap(s, L, w, indices, nnz, offsets, num_bags, pairs_per_chunk,
-                                       rows_per_chunk, lists, st);
+                                       rows_per_chunk, st);
     if (rc != TT_EMB_ERR_UNSUPPORTED) return rc;
   }
   {

@@ -1,32 +1,29 @@
-// Prefix grouping by a presence bitmap over the key space, in ONE cooperative
-// launch (FlowTT summary card, key innovations: prefix-based index grouping).
+// Prefix grouping of a forward-only call by a presence bitmap over the key
+// space, in ONE cooperative launch (FlowTT summary card, key innovations:
+// prefix-based index grouping).
 //
 // The radix-sort groupings (tt_group_coop.cu, tt_group.cu) move every lookup's
-// 64-bit (key, position) word through three or four passes.  When the batch is
-// dense in its table (at most kBmWordsPerLookup bitmap words per lookup), the
-// unique rows can instead be read off a bitmap of the M grouping keys: a key's
-// unique-row number is the number of set bits before it.  The lookups then
-// move once, into their row's segment of `perm`.  Phases (one grid barrier
-// after each; `|` marks it):
+// 64-bit (key, position) word through three or four passes, because the
+// backward wants each unique row's lookups listed in position order.  A
+// forward needs less: the unique rows and prefixes in key order, the unique
+// row of every lookup and the work chunks.  When the batch is dense in its
+// table (at most kBmWordsPerLookup bitmap words per lookup) those come off a
+// bitmap of the M grouping keys: a key's unique-row number is the number of
+// set bits before it.  Phases (one grid barrier after each; `|` marks it):
 //
 //   0  keys and checks; the row and prefix bitmaps are zeroed              |
-//   A  every CTA inserts its keys into a shared-memory table (one entry per
-//      distinct key, with its count in the CTA) and sets the bitmap bits of
-//      its distinct keys and prefixes, one global atomic per bitmap word      |
+//   A  every CTA puts its keys into a shared-memory table (one entry per
+//      distinct key) and sets the bitmap bits of its distinct keys and of
+//      their prefixes, one global atomic per bitmap word and 32-slot group   |
 //   B  set-bit counts of each CTA's range of bitmap words                    |
 //   C  rank of every bitmap word; unique rows (i3, prefix key) and unique
 //      prefixes (i1, i2) written in key order                                |
-//   D  unique row of every lookup (uid); row sizes accumulated with one
-//      atomic per distinct key and CTA; row -> prefix number; prefix -> first
-//      row; work-chunk counts                                                |
-//   E  work chunks; CTA-local prefix sums of the row sizes                   |
-//   F  row_start; every lookup placed in its row's segment of perm
+//   D  unique row of every lookup (uid); row -> prefix number; prefix ->
+//      first row; work-chunk counts                                          |
+//   E  work chunks and their claim order
 //
-// Unique rows, unique prefixes, uid, row_start and the chunks are exactly those
-// of the sorting groupings.  The order of the lookups INSIDE one row's segment
-// of perm is not position order: each CTA reserves its lookups' slots in the
-// row with an atomic, so the CTAs' blocks come in arrival order.  Only the
-// backward's per-row sums read that order, and they are sums.
+// Unique rows, unique prefixes, uid and the chunks are exactly those of the
+// sorting groupings; perm and row_start are not written.
 //
 // The bitmaps are built in the unique-row buffer, which no one reads until the
 // row kernels fill it after the grouping; the buffer's last row (the zero row
@@ -45,7 +42,8 @@ constexpr int kBmPSlots = 2048;         // per-CTA table of prefix-bitmap words
 constexpr uint32_t kBmEmpty = 0xffffffffu;   // no key (in-range keys are < M <= 2^32 - 2)
 constexpr int64_t kBmWordsPerLookup = 8;     // density bound of this path
 constexpr int kBmItemsMax = 16;
-constexpr size_t kBmSmem = sizeof(uint32_t) * 2 * (kBmSlots + kBmPSlots) + sizeof(uint16_t) * kBmSlots;
+constexpr size_t kBmSmem =
+    sizeof(uint32_t) * (kBmSlots + 2 * kBmPSlots) + sizeof(uint16_t) * kBmSlots;
 
 struct BitmapArgs {
   const int64_t* indices;
@@ -62,12 +60,8 @@ struct BitmapArgs {
   uint32_t zero_quads;    // 16-byte units covering both bitmaps (zeroed in phase 0)
   int4* cta;              // [G] per CTA: (row bits, prefix bits, valid lookups, 0)
   int* cta_chunks;        // [G] chunks of each CTA's prefixes
-  int* cta_lookups;       // [G] lookups of each CTA's rows
-  int32_t* row_loc;       // [U_r] row start within its CTA's range of rows
   uint32_t* bar;          // grid barrier word (zero before the launch)
-  uint32_t* spill;        // counter of out-of-range lookups placed after the valid ones
   unsigned long long* trace;   // [16] %globaltimer of CTA 0 at phase ends and barrier releases
-  int lists;              // 0: no per-row lookup lists (perm, row_start) -- a forward-only call
 };
 
 // 32-slot group of key k's bitmap word in the CTA table (multiplicative hash,
@@ -87,15 +81,13 @@ template <int ITEMS>
 __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) {
   extern __shared__ uint32_t bm_sm[];
   uint32_t* tag = bm_sm;                   // [kBmSlots] key (phases A-D), then its unique row
-  uint32_t* cnt = tag + kBmSlots;          // [kBmSlots] its lookups in this CTA, then their base
-  uint32_t* ptag = cnt + kBmSlots;         // [kBmPSlots] prefix-bitmap word
+  uint32_t* ptag = tag + kBmSlots;         // [kBmPSlots] prefix-bitmap word
   uint32_t* pbit = ptag + kBmPSlots;       // [kBmPSlots] bits of that word seen by this CTA
   uint16_t* occ_list = reinterpret_cast<uint16_t*>(pbit + kBmPSlots);   // [kBmSlots] occupied slots
   __shared__ uint32_t n_occ_sm;
   __shared__ uint32_t scan_sm[kCoopWarps];
   __shared__ uint4 sum_sm[kCoopWarps];
   __shared__ uint32_t wtot[2][kCoopWarps];  // set bits of each warp's bitmap words
-  __shared__ int base_of[kCoopMaxGrid];     // first sorted position of each CTA's rows
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x, G = gridDim.x;
@@ -133,10 +125,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
     uint4* z = reinterpret_cast<uint4*>(a.rbm);
     for (uint32_t q = (uint32_t)bt; q < a.zero_quads; q += (uint32_t)G * kCoopThreads)
       z[q] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = tid; i < kBmSlots; i += kCoopThreads) {
-      tag[i] = kBmEmpty;
-      cnt[i] = 0u;
-    }
+    for (int i = tid; i < kBmSlots; i += kCoopThreads) tag[i] = kBmEmpty;
     for (int i = tid; i < kBmPSlots; i += kCoopThreads) {
       ptag[i] = kBmEmpty;
       pbit[i] = 0u;
@@ -172,12 +161,11 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
   // Every lookup finds its key's slot in the CTA table: lane k mod 32 of the
   // 32-slot group that its bitmap word hashes to, else of one of the next
   // kBmProbes - 1 groups (a key with no free slot sets its bits in the global
-  // bitmaps directly); with per-row lists it also counts itself there.  The
-  // lookup that puts a key in the table records the key's prefix in the CTA's
-  // prefix table (a third or more of all lookups can share one prefix, whose
-  // shared-memory word would otherwise take one serialised atomic per lookup).
+  // bitmaps directly).  The lookup that puts a key in the table records the
+  // key's prefix in the CTA's prefix table (a third or more of all lookups can
+  // share one prefix, whose shared-memory word would otherwise take one
+  // serialised atomic per lookup).
   int32_t slot[ITEMS];     // table slot of the lookup's key (-1: its bits were set directly)
-  uint32_t lr[ITEMS];      // the lookup's rank among this CTA's lookups of its key
   uint32_t n_valid = 0;
   {
     volatile uint32_t* vtag = tag;
@@ -185,7 +173,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
       slot[it] = -1;
-      lr[it] = 0u;
       const uint32_t k = key[it];
       if (k == kBmEmpty) continue;
       ++n_valid;
@@ -211,7 +198,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
       const uint32_t q = fdiv(k, s.fm3);
       if (sl >= 0) {
         slot[it] = sl;
-        if (a.lists) lr[it] = atomicAdd(&cnt[sl], 1u);
         if (first) {
           const uint32_t pw = q >> 5, pb = 1u << (q & 31);
           const int ps = (int)(pw & (kBmPSlots - 1));
@@ -235,7 +221,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
   // Flush, one warp per 32-slot group.  Every key sits in the lane equal to its
   // low five bits, so the keys of one bitmap word in a group carry exactly the
   // bits of the lanes of their match group: one atomic per word and group.  The
-  // occupied slots are listed on the way (phases D and F visit only those).
+  // occupied slots are listed on the way (phase D visits only those).
   for (int s0 = warp * 32; s0 < kBmSlots; s0 += kCoopThreads) {
     const uint32_t k = tag[s0 + lane];
     const bool occ = k != kBmEmpty;
@@ -293,7 +279,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
   barrier();
 
   // ------------------------------------------------------------------ phase C
-  uint32_t U = 0, P = 0, NV = 0;
+  uint32_t U = 0, P = 0;
   {
     uint4 pre = make_uint4(0, 0, 0, 0), tot = make_uint4(0, 0, 0, 0);
     for (int cc = tid; cc < G; cc += kCoopThreads) {
@@ -310,13 +296,11 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
     tot = coop_sum4(tot, sum_sm);
     U = tot.x;
     P = tot.y;
-    NV = tot.z;
     if (c == 0 && tid == 0) {
-      a.w.ctl->method = a.lists ? kGroupBitmap : kGroupBitmapNoLists;
-      a.w.ctl->n_valid = (int32_t)NV;
+      a.w.ctl->method = kGroupBitmap;
+      a.w.ctl->n_valid = (int32_t)tot.z;
       a.w.ctl->U_r = (int32_t)U;
       a.w.ctl->U_12 = (int32_t)P;
-      a.w.row_start[U] = (int32_t)NV;
       a.w.pair_row_start[P] = (int32_t)U;
     }
     uint32_t rb = pre.x, pb = pre.y;       // set bits before this warp's words
@@ -379,16 +363,11 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
       }
       pb += run_tot;
     }
-    // row sizes start from zero (every CTA clears its share of the rows)
-    const uint32_t Lz = (U + G - 1) / G;
-    if (a.lists)
-      for (uint32_t u = (uint32_t)c * Lz + tid; u < min((uint32_t)c * Lz + Lz, U); u += kCoopThreads)
-        a.w.row_start[u] = 0;
   }
   barrier();
 
   // ------------------------------------------------------------------ phase D
-  // rows [c Lu, c Lu + Lu) belong to CTA c in phases D-F; prefixes [c Lp, c Lp + Lp)
+  // rows [c Lu, c Lu + Lu) belong to CTA c here; prefixes [c Lp, c Lp + Lp)
   const uint32_t Lu = (U + G - 1) / G, Ut = (Lu + kCoopThreads - 1) / kCoopThreads;
   const uint32_t x0 = min((uint32_t)c * Lu, U), x1 = min(x0 + Lu, U);
   const uint32_t xt = x0 + (uint32_t)tid * Ut;
@@ -397,9 +376,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
   const uint32_t yt = y0 + (uint32_t)tid * Pt;
   uint32_t firsts = 0, chunk_ex = 0;
   {
-    // (a) one atomic per distinct key of the CTA reserves its lookups' places in
-    // the key's row (the occupied slots, four per thread at a time: their rank
-    // loads in flight together)
+    // (a) unique row of every distinct key of the CTA (the occupied slots, four
+    // per thread at a time: their rank loads in flight together)
     const int n_occ = (int)n_occ_sm;
 #pragma unroll 1
     for (int e0 = 0; e0 < n_occ; e0 += 4 * kCoopThreads) {
@@ -414,36 +392,18 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
         e[j] = k[j] != kBmEmpty ? __ldcg(a.rbm + (k[j] >> 5)) : make_uint2(0u, 0u);
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (k[j] != kBmEmpty) {
-          const uint32_t u = e[j].y + __popc(e[j].x & ((1u << (k[j] & 31)) - 1u));
-          tag[sl[j]] = u;
-          if (a.lists)
-            cnt[sl[j]] = atomicAdd(reinterpret_cast<uint32_t*>(a.w.row_start) + u, cnt[sl[j]]);
-        }
-      }
+      for (int j = 0; j < 4; ++j)
+        if (k[j] != kBmEmpty) tag[sl[j]] = e[j].y + __popc(e[j].x & ((1u << (k[j] & 31)) - 1u));
     }
     __syncthreads();
-    // (b) the unique row of every lookup; a lookup whose key has no slot takes
-    // its place in the row with an atomic of its own (slot[] then holds -2 - u)
+    // (b) the unique row of every lookup (a key without a slot: its own rank load)
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
       const int64_t i = pos_of(it);
       const uint32_t k = key[it];
       if (i >= seg1) continue;
-      if (k == kBmEmpty) {
-        a.w.uid[i] = -1;
-        continue;
-      }
-      uint32_t u;
-      if (slot[it] >= 0) {
-        u = tag[slot[it]];
-      } else {
-        u = bm_rank(a.rbm, k);
-        if (a.lists) lr[it] = atomicAdd(reinterpret_cast<uint32_t*>(a.w.row_start) + u, 1u);
-        slot[it] = -2 - (int32_t)u;
-      }
-      a.w.uid[i] = (int32_t)u;
+      a.w.uid[i] = k == kBmEmpty ? -1
+                                 : (int32_t)(slot[it] >= 0 ? tag[slot[it]] : bm_rank(a.rbm, k));
     }
     // (c) prefix number of every unique row
 #pragma unroll 1
@@ -457,8 +417,9 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
     // starts a chunk when it is prefix 0 or a multiple of CP, its i2 differs from
     // the prefix before, or it or the prefix before holds more than CR rows; rows
     // f0 + k CR (k >= 1) start the CR-row pieces of a hot prefix.  Counted as
-    // (head chunks) | (later pieces) << 16: the claim order puts every later
-    // piece after all head chunks (at most 8192 of either per CTA)
+    // (head chunks) | (later pieces) << 16 (at most 8192 heads and 2^16 - 1
+    // pieces per CTA for the batches this launch takes): the claim order puts
+    // every later piece after all head chunks
     uint32_t mine = 0;
 #pragma unroll 1
     for (uint32_t k = 0; k < Pt; ++k) {
@@ -526,88 +487,6 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
       a.w.ctl->n_chunks = n;
       a.w.chunk_start[n] = (int)U;
       a.w.chunk_desc[n] = make_int2((int)U, (int)P | (int32_t)0x80000000);
-    }
-  }
-  if (!a.lists) {                           // no per-row lookup lists: done
-    stamp();
-    return;
-  }
-  {
-    // lookups of each of this CTA's rows -> CTA-local exclusive prefix
-    uint32_t mine = 0;
-#pragma unroll 1
-    for (uint32_t k = 0; k < Ut; ++k) {
-      const uint32_t u = xt + k;
-      if (u >= x1) break;
-      mine += (uint32_t)__ldcg(a.w.row_start + u);
-    }
-    uint32_t rtot;
-    uint32_t run = coop_scan(mine, &rtot, scan_sm);
-#pragma unroll 1
-    for (uint32_t k = 0; k < Ut; ++k) {
-      const uint32_t u = xt + k;
-      if (u >= x1) break;
-      a.row_loc[u] = (int32_t)run;
-      run += (uint32_t)__ldcg(a.w.row_start + u);
-    }
-    if (tid == 0) a.cta_lookups[c] = (int)rtot;
-  }
-  barrier();
-
-  // ------------------------------------------------------------------ phase F
-  {
-    // first sorted position of every CTA's rows (exclusive prefix over the CTAs,
-    // in rounds of 512)
-    uint32_t carry = 0;
-    for (int c0 = 0; c0 < G; c0 += kCoopThreads) {
-      const int cc = c0 + tid;
-      const uint32_t v = cc < G ? (uint32_t)__ldcg(a.cta_lookups + cc) : 0u;
-      uint32_t t;
-      const uint32_t ex = coop_scan(v, &t, scan_sm);
-      if (cc < G) base_of[cc] = (int)(carry + ex);
-      carry += t;
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (uint32_t k = 0; k < Ut; ++k) {
-      const uint32_t u = xt + k;
-      if (u >= x1) break;
-      a.w.row_start[u] = __ldcg(a.row_loc + u) + base_of[c];
-    }
-    // sorted position of each occupied slot's first lookup, then every lookup
-    const int n_occ = (int)n_occ_sm;
-#pragma unroll 1
-    for (int e0 = 0; e0 < n_occ; e0 += 4 * kCoopThreads) {
-      int sl[4];
-      uint32_t rl[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int x = e0 + j * kCoopThreads + tid;
-        sl[j] = x < n_occ ? (int)occ_list[x] : -1;
-        rl[j] = sl[j] >= 0 ? (uint32_t)__ldcg(a.row_loc + tag[sl[j]]) : 0u;
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (sl[j] >= 0) cnt[sl[j]] += rl[j] + (uint32_t)base_of[tag[sl[j]] / Lu];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-      const int64_t i = pos_of(it);
-      if (i >= seg1) continue;
-      if (key[it] == kBmEmpty) {
-        const uint32_t x = NV + atomicAdd(a.spill, 1u);
-        if (x < (uint64_t)a.nnz) a.w.perm[x] = (int32_t)i;
-        continue;
-      }
-      uint32_t at;
-      if (slot[it] >= 0) {
-        at = cnt[slot[it]] + lr[it];
-      } else {
-        const uint32_t u = (uint32_t)(-2 - slot[it]);
-        at = (uint32_t)__ldcg(a.row_loc + u) + (uint32_t)base_of[u / Lu] + lr[it];
-      }
-      if (at < (uint64_t)a.nnz) a.w.perm[at] = (int32_t)i;
     }
   }
   stamp();
@@ -682,7 +561,7 @@ bool bitmap_grouping_applies(const Shape& s, const Layout& L, int64_t nnz) {
 
 int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
                         int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
-                        int rows_per_chunk, int lists, cudaStream_t st) {
+                        int rows_per_chunk, cudaStream_t st) {
   if (!bitmap_grouping_applies(s, L, nnz)) return TT_EMB_ERR_UNSUPPORTED;
   const int G = bitmap_grid();
   const int64_t Lseg = ceil_div(nnz, G);
@@ -706,14 +585,10 @@ int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, const int6
   char* sc = static_cast<char*>(w.coop);
   ba.cta = reinterpret_cast<int4*>(sc);
   ba.cta_chunks = reinterpret_cast<int*>(sc + sizeof(int4) * kCoopMaxGrid);
-  ba.cta_lookups = ba.cta_chunks + kCoopMaxGrid;
-  ba.row_loc = reinterpret_cast<int32_t*>(w.keysA);
-  // grid barrier word and the out-of-range counter: the digit-histogram area,
-  // zeroed by the grouping's memset and otherwise unused on this path
+  // grid barrier word and phase trace: the digit-histogram area, zeroed by the
+  // grouping's memset and otherwise unused on this path
   ba.bar = w.hist;
-  ba.spill = w.hist + 64;
   ba.trace = reinterpret_cast<unsigned long long*>(w.hist + 128);
-  ba.lists = lists ? 1 : 0;
   if (Lseg <= kCoopThreads * 4) return launch_bitmap_items<4>(ba, G, st);
   if (Lseg <= kCoopThreads * 8) return launch_bitmap_items<8>(ba, G, st);
   return launch_bitmap_items<16>(ba, G, st);

@@ -43,11 +43,10 @@ constexpr uint32_t kValMask = (1u << 30) - 1u;
 constexpr long long kSpinCap = 1ll << 22;   // polls before a look-back gives up
 
 // Grouping methods (Ctl::method).
-constexpr int32_t kGroupBitmap = 1;   // key bitmap, one cooperative launch
+constexpr int32_t kGroupBitmap = 1;   // key bitmap, one cooperative launch, no per-row
+                                      // lookup lists (perm, row_start): forward-only calls
 constexpr int32_t kGroupCoop = 2;     // radix sort, one cooperative launch
 constexpr int32_t kGroupMulti = 3;    // radix sort, one launch per phase
-constexpr int32_t kGroupBitmapNoLists = 4;   // key bitmap without the per-row lookup lists
-                                             // (perm, row_start): a forward-only grouping
 
 // The control block at the start of the workspace (256 bytes).
 struct Ctl {
@@ -345,14 +344,15 @@ int sm_count();
 size_t coop_scratch_bytes();
 int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
                         int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
-                        int rows_per_chunk, int lists, cudaStream_t st);
+                        int rows_per_chunk, cudaStream_t st);
 bool bitmap_grouping_applies(const Shape& s, const Layout& L, int64_t nnz);
 int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratch,
                       const int64_t* indices, int64_t nnz, const int64_t* offsets,
                       int64_t num_bags, int pairs_per_chunk, int rows_per_chunk, cudaStream_t st);
 // grouping (tt_group.cu)
-// lists = 0: the bitmap grouping may leave out the per-row lookup lists (perm,
-// row_start), which only a backward reads (a forward-only call)
+// lists = 0: a forward-only call, whose grouping may leave out the per-row
+// lookup lists (perm, row_start) that only a backward reads: the key-bitmap
+// grouping then serves a batch dense in its table
 int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                  int rows_per_chunk, cudaStream_t st, int lists = 1);

@@ -155,11 +155,14 @@ def make_cores(m, n, R, seed: int, std: float) -> list:
 
 
 def make_inputs(cfg: int, table: int = 0, num_bags: int | None = None,
-                with_grad: bool | None = None) -> TTInputs:
+                with_grad: bool | None = None, mapping: str | None = None) -> TTInputs:
     """Seeded inputs of workload ``cfg`` (table ``table``).
 
-    ``num_bags`` overrides the batch size (the first ``num_bags`` bags of a
-    smaller draw; used for reduced-size parity cases).
+    ``num_bags`` overrides the batch size (a draw of that many bags from the
+    workload's seed: a different draw from the full batch's, not its first
+    bags; used for reduced-size parity cases).  ``mapping`` overrides how Zipf
+    ranks become rows: "identity" (rank k -> row k - 1) or "permuted" (through a
+    seeded random permutation of the rows), the sensitivity variant.
     """
     c = CONFIGS[cfg]
     m = tuple(int(v) for v in c["tables"][table])
@@ -173,7 +176,10 @@ def make_inputs(cfg: int, table: int = 0, num_bags: int | None = None,
     offsets = np.zeros(B + 1, dtype=np.int64)
     np.cumsum(lengths, out=offsets[1:])
     nnz = int(offsets[-1])
-    indices = _draw_rows(rng, c["dist"], N, nnz)
+    dist = c["dist"]
+    if mapping is not None and dist[0] == "zipf":
+        dist = (dist[0], dist[1], mapping)
+    indices = _draw_rows(rng, dist, N, nnz)
     grad = None
     if with_grad if with_grad is not None else c.get("train", False):
         g = np.random.default_rng(3000 * cfg + table)

@@ -33,7 +33,7 @@ def _dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
 
-def _gpu_forward(x, ws=None):
+def _gpu_forward(x, ws=None, flags=0):
     cores = [_dev(c) for c in x.cores]
     idx, off = _dev(x.indices.astype(np.int64)), _dev(x.offsets.astype(np.int64))
     B = x.num_bags
@@ -41,7 +41,10 @@ def _gpu_forward(x, ws=None):
     if ws is None:
         ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     out = torch.full((B, x.D), float("nan"), dtype=torch.float32, device="cuda")
-    tte.tt_emb_forward(cores, x.m, x.n, x.R, idx, off, out, ws)
+    if flags:
+        tte.tt_emb_forward_ex(cores, x.m, x.n, x.R, idx, off, None, "sum", out, ws, flags=flags)
+    else:
+        tte.tt_emb_forward(cores, x.m, x.n, x.R, idx, off, out, ws)
     rc, bits = tte.tt_emb_get_error(ws)
     return out.cpu().numpy(), rc, bits, dict(cores=cores, idx=idx, off=off, ws=ws)
 
@@ -63,25 +66,20 @@ def _rel_err(a, ref):
 
 
 def _check_grouping(x, ws, method=None):
-    """The grouping in ``ws`` against the oracle's: unique rows, prefixes, CSR offsets
-    and the unique row of every lookup bit for bit; the lookups of every unique row
-    exactly as a set, and in position order after a radix-sort grouping (the oracle
-    sorts stably); chunks valid.  ``method`` (if given) must be the one that ran."""
+    """The grouping in ``ws`` against the oracle's, bit for bit: unique rows, prefixes,
+    the unique row of every lookup and (except for a forward-only key-bitmap grouping,
+    which has none) the lookups of every row in position order with their CSR offsets;
+    chunks valid, each chunk's prefixes sharing one i2, the claim order a permutation of
+    the chunks.  ``method`` (if given) must be the one that ran."""
     ref = oracle.group(x.indices, x.m)
     g = tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, ws)
     if method is not None:
         assert g["method"] == method, g["method"]
     assert g["n_valid"] == ref["n_valid"] and g["U_r"] == ref["U_r"] and g["U_12"] == ref["U_12"]
     nv = ref["n_valid"]
-    if g["method"] != "bitmap_nolists":          # a forward-only grouping has no lookup lists
+    if g["method"] != "bitmap":                  # a forward-only grouping has no lookup lists
         assert np.array_equal(g["row_start"], ref["row_start"])
-        rid = np.repeat(np.arange(g["U_r"]), np.diff(g["row_start"]))
-        perm = g["perm"][:nv]
-        assert np.array_equal(perm[np.lexsort((perm, rid))], ref["perm"])   # each row's lookup set
-        if g["method"] != "bitmap":
-            assert np.array_equal(perm, ref["perm"])                        # and in position order
-        assert np.array_equal(np.sort(g["perm"][nv:]),
-                              np.setdiff1d(np.arange(x.nnz), ref["perm"]))  # out-of-range last
+        assert np.array_equal(g["perm"][:nv], ref["perm"])
     assert np.array_equal(g["row_pair"], ref["row_pair"])
     assert np.array_equal(g["pair_row_start"], ref["pair_row_start"])
     assert np.array_equal(g["pair_i1"], ref["pair_i1"])
@@ -97,6 +95,8 @@ def _check_grouping(x, ws, method=None):
     for c in range(g["n_chunks"]):
         p = g["row_pair"][cs[c]:cs[c + 1]]
         assert np.unique(g["pair_i2"][p]).size == 1
+    order = g["chunk_order"]
+    assert np.array_equal(np.sort(order), np.arange(g["n_chunks"]))
     return g
 
 
@@ -158,6 +158,7 @@ def test_forward_full_size_sampled(cfg, table):
     if cfg in (3, 5):
         # the later pieces of hot prefixes took their P2 from the L2 checkpoint (the
         # sampled bags above include rows made that way: the hot rows are in most bags)
+        assert g["method"] == "coop_sort"
         cs = g["chunk_start"]
         pieces = sum(1 for c in range(g["n_chunks"])
                      if g["pair_row_start"][g["row_pair"][cs[c]]] != cs[c])
@@ -170,18 +171,21 @@ def _sms():
 
 @pytest.mark.parametrize("items", [4, 8, 16])
 def test_bitmap_grouping_every_variant(items):
-    """The key-bitmap grouping keeps ceil(nnz / SMs) lookups per CTA in registers, 4, 8
-    or 16 per thread (512 threads); the batch size picks the variant.  Each one runs here
-    on the benchmark table's shape and index distribution (dense in the table: at most
-    8 bitmap words per lookup) and is compared with the oracle's grouping."""
+    """The key-bitmap grouping of a forward-only call keeps ceil(nnz / SMs) lookups per
+    CTA in registers, 4, 8 or 16 per thread (512 threads); the batch size picks the
+    variant.  Each one runs here on the benchmark table's shape and index distribution
+    (dense in the table: at most 8 bitmap words per lookup), is compared with the
+    oracle's grouping, and its output equals the sort-grouped forward's bit for bit."""
     G = _sms()
     lo, hi = G * 512 * {4: 0, 8: 4, 16: 8}[items], G * 512 * items
     target = (lo + hi) // 2 if items > 4 else hi - 1000
     x = make_inputs(3, num_bags=target // 20)                # fixed bag length 20
     assert lo < x.nnz <= hi
-    out, rc, _, st = _gpu_forward(x)
+    out, rc, _, st = _gpu_forward(x, flags=tte.TT_EMB_FORWARD_ONLY)
     assert rc == tte.TT_EMB_OK
     _check_grouping(x, st["ws"], method="bitmap")
+    ref_out, rc, _, _ = _gpu_forward(x)                      # the same batch, sort-grouped
+    assert rc == tte.TT_EMB_OK and np.array_equal(out, ref_out)
     rng = np.random.default_rng(items)
     bags = np.sort(rng.choice(x.num_bags, size=200, replace=False))
     idx, off = _sample_bags(x, bags)
@@ -225,7 +229,7 @@ def test_forward_only_grouping_full_size(cfg):
     rc, bits = tte.tt_emb_get_error(st["ws"])
     assert rc == tte.TT_EMB_OK, bits
     assert np.array_equal(out.cpu().numpy(), ref_out)
-    _check_grouping(x, st["ws"], method="bitmap_nolists")
+    _check_grouping(x, st["ws"], method="bitmap")
 
 
 def test_backward_refuses_a_forward_only_grouping():
@@ -240,7 +244,7 @@ def test_backward_refuses_a_forward_only_grouping():
     out = torch.empty((x.num_bags, x.D), dtype=torch.float32, device="cuda")
     tte.tt_emb_forward_ex(cores, x.m, x.n, x.R, idx, off, None, "sum", out, ws,
                           flags=tte.TT_EMB_FORWARD_ONLY)
-    assert tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, ws)["method"] == "bitmap_nolists"
+    assert tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, ws)["method"] == "bitmap"
     grads = [torch.zeros_like(c) for c in cores]
     tte.tt_emb_backward(_dev(x.grad_out), cores, x.m, x.n, x.R, idx, off, grads, ws,
                         reuse_grouping=True)
