@@ -123,7 +123,8 @@ typedef struct {
  * write for it
  * (sum pooling).  All tables share n and R (TT_EMB_ERR_ARG otherwise); their m,
  * batches and workspaces are their own, and workspaces must not overlap.
- * Each table is grouped into its own workspace; for shapes served by the
+ * Each table is grouped into its own workspace as by a forward-only call
+ * (TT_EMB_FORWARD_ONLY: a backward must not reuse these groupings); for shapes served by the
  * tiled chunk kernel (n = (4, 8, 4) with R1 = R2 = 64, n = (4, 4, 4) with
  * R1 = R2 = 16) one persistent launch of that kernel then works through the
  * chunks of all tables (one counter, chunks numbered across the tables), so

@@ -379,7 +379,9 @@ int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stre
     int CP, CR;
     int rc = forward_chunk_params(s[t], &CP, &CR);
     if (rc) return rc;
-    rc = launch_group(s[t], L[t], w[t], tables[t].indices, nnz[t], offsets[t], bags[t], CP, CR, st);
+    // forward-only groupings: no backward reuses them
+    rc = launch_group(s[t], L[t], w[t], tables[t].indices, nnz[t], offsets[t], bags[t], CP, CR, st,
+                      0);
     if (rc) return rc;
     if (nnz[t] == 0 && bags[t] > 0 &&
         cudaMemsetAsync(out[t], 0, sizeof(float) * (size_t)bags[t] * s[t].D, st) != cudaSuccess)

@@ -57,6 +57,12 @@ def test_eight_tables_of_the_multi_table_workload():
     xs = [make_inputs(4, table=k, num_bags=1500) for k in range(8)]
     tables = [_table(x) for x in xs]
     tte.tt_emb_forward_tables(tables)
+    # the tables dense in their rows (at most 8 bitmap words per lookup) are grouped by
+    # the key bitmap of a forward-only call, the others by the radix sort
+    for x, t in zip(xs, tables):
+        g = tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, t["workspace"])
+        dense = (int(np.prod(x.m)) + 31) // 32 <= 8 * x.nnz
+        assert g["method"] == ("bitmap" if dense else "coop_sort"), (x.m, g["method"])
     _check_all(xs, tables)
     rng = np.random.default_rng(3)
     for k in (0, 7):
