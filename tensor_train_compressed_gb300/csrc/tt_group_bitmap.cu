@@ -563,15 +563,7 @@ int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, const int6
                         int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                         int rows_per_chunk, cudaStream_t st) {
   if (!bitmap_grouping_applies(s, L, nnz)) return TT_EMB_ERR_UNSUPPORTED;
-  // as many CTAs as the batch needs (about 2048 lookups and 4096 bitmap words
-  // each), at most the resident grid: a small batch then pays for cheap grid
-  // barriers among a few CTAs, not for ones across the whole GPU
-  uint32_t Wr0, Wp0;
-  bitmap_bytes(s, &Wr0, &Wp0);
-  const int Gmax = bitmap_grid();
-  int64_t want = ceil_div(nnz, 2048);
-  if (ceil_div((int64_t)Wr0, 4096) > want) want = ceil_div((int64_t)Wr0, 4096);
-  const int G = (int)(want < 1 ? 1 : (want > Gmax ? Gmax : want));
+  const int G = bitmap_grid();
   const int64_t Lseg = ceil_div(nnz, G);
   BitmapArgs ba;
   ba.indices = indices;
