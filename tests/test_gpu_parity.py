@@ -337,6 +337,35 @@ def test_bad_offsets_are_reported():
     assert rc == tte.TT_EMB_ERR_OFFSETS and bits & 2
 
 
+def test_largest_table_32_bit_keys():
+    """The largest table the ABI takes: M = 65535 x 65535 x 1 = 4,294,836,225 rows, just
+    under the 2^32 - 2 limit, so the grouping keys use all 32 bits (four radix passes,
+    and the out-of-range sentinel is all ones).  Uniform indices plus the extremes
+    0, 1, M - 2, M - 1 and rows around 2^31; forward (whole output), grouping and every
+    core gradient (whole cores) against the oracle; then one index = M is reported and
+    contributes nothing."""
+    m, n, R = (65535, 65535, 1), (2, 2, 2), (1, 4, 4, 1)
+    M = 65535 * 65535
+    x = make_custom(m, n, R, num_bags=3000, max_len=6, seed=61)
+    x.indices[:6] = [0, 1, M - 2, M - 1, 2 ** 31 - 1, 2 ** 31]
+    x.indices[-3:] = [M - 1, 65535 * 7 + 65534, M - 65535]
+    out, rc, bits, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK, bits
+    ref = oracle.forward(x.cores, m, n, R, x.indices, x.offsets, threads=8)
+    assert _rel_err(out, ref) <= FWD_TOL
+    _check_grouping(x, st["ws"], method="coop_sort")
+    dG = _gpu_backward(x, st)
+    dref = oracle.backward(x.grad_out, x.cores, m, n, R, x.indices, x.offsets, threads=8)
+    for k in range(3):
+        assert _rel_err(dG[k], dref[k]) <= BWD_TOL, k
+    x.indices[100] = M                                       # one past the last row
+    out, rc, bits, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_ERR_INDEX and bits & 1
+    ref = oracle.forward(x.cores, m, n, R, x.indices, x.offsets, strict=False)
+    assert _rel_err(out, ref) <= FWD_TOL
+    _check_grouping(x, st["ws"], method="coop_sort")
+
+
 def test_single_hot_row_and_all_same_prefix():
     """Every lookup on one row (a 40k-lookup run) and one prefix with many rows."""
     m, n, R = (4, 5, 300), (4, 8, 4), (1, 32, 32, 1)
