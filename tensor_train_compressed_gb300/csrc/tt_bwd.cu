@@ -525,6 +525,9 @@ __global__ void __launch_bounds__(256) k_bwd_generic(BwdArgs a) {
 //   (5) dG1[i1_p] += dP2[p] . G2[i2]^T               (4 np) x 32 x 256
 // A pair's missing second row reads a zero row.  Core gradients are
 // accumulated with vector float reductions.
+// Longest run of consecutive chunks one claim of the backward chunk kernel takes.
+constexpr int kBwdRun = 8;
+
 struct MmaBwd {
   static constexpr int CP = kCP_8_32, R = 32, NC = 256, D = 128;
   static constexpr int RB = 24;                     // rows per batch (row RB of a stage stays zero)
@@ -544,6 +547,8 @@ struct MmaBwd {
   static constexpr int OFF_P2 = 2 * STAGE_B, OFF_DP = OFF_P2 + 2 * P2PLANE, OFF_META = OFF_DP + 2 * DPPLANE;
   struct Meta {
     int x0, x1, p0, np, i2, nb, npairs, end;
+    int flush;           // the CTA's next chunk has another i2: reduce dG2[i2] after this one
+    int pad[3];
     int rs[CP];          // chunk-local first row of each prefix
     int pi1[CP];
     int ri3[RB];         // i3 of the current batch's rows
@@ -781,22 +786,15 @@ __device__ __forceinline__ void mma_bwd_dg3(const MmaBwd::Meta& m, uint32_t P2h,
   }
 }
 
-// (4): dG2[i2][r1][(j2, r2)] += sum over (p, j1) of G1[i1_p][j1][r1] dP2[p][j1][j2][r2];
-// warp w owns columns 32 w .. 32 w + 31.  bf16 tiles: A = G1 rows read transposed
+// (4): dG2[i2][r1][(j2, r2)] += sum over (p, j1) of G1[i1_p][j1][r1] dP2[p][j1][j2][r2],
+// into the warp's accumulators (kept across the CTA's consecutive chunks of one
+// i2, reduced into dG2 by dg2_flush); warp w owns columns 32 w .. 32 w + 31.  bf16 tiles: A = G1 rows read transposed
 // ([k = (p, j1)][m = r1]), B = dP2 planes [k = (p, j1)][n] (transposed); the k range
 // is padded to 16 with rows that the caller has zeroed in both operands.
-__device__ __forceinline__ void mma_bwd_dg2(uint32_t g1h, uint32_t dph, float* __restrict__ dG2i2, int np,
+__device__ __forceinline__ void mma_bwd_dg2(uint32_t g1h, uint32_t dph, float (&acc)[2][4][4], int np,
                                             int warp, int lane) {
   using C = MmaBwd;
-  const int g = lane >> 2, t = lane & 3;
   const uint32_t g1l = g1h + C::G1PLANE, dpl = dph + C::DPPLANE;
-  float acc[2][4][4];
-#pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
   const int kk = (np + 3) >> 2;
   for (int ks = 0; ks < kk; ++ks) {
     uint32_t ah[2][4], al[2][4];
@@ -817,13 +815,24 @@ __device__ __forceinline__ void mma_bwd_dg2(uint32_t g1h, uint32_t dph, float* _
           mma_bf16x3(acc[mt][2 * np2 + h], ah[mt], al[mt], bh[2 * h], bh[2 * h + 1], bl[2 * h], bl[2 * h + 1]);
     }
   }
+}
+
+// dG2[i2] += the warp's accumulated part of (4) (vector float reductions), then
+// the accumulators start again from zero.
+__device__ __forceinline__ void dg2_flush(float (&acc)[2][4][4], float* __restrict__ dG2i2, int warp,
+                                          int lane) {
+  using C = MmaBwd;
+  const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       float* o = dG2i2 + (size_t)(16 * mt + g + 8 * h) * C::NC + 32 * warp + 2 * t;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) red_add_f2(o + 8 * nt, acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
+      for (int nt = 0; nt < 4; ++nt) {
+        red_add_f2(o + 8 * nt, acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
+        acc[mt][nt][2 * h] = acc[mt][nt][2 * h + 1] = 0.f;
+      }
     }
 }
 
@@ -893,10 +902,28 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
   const int n_chunks = a.w.ctl->n_chunks;
 
   if (warp == 8) {
-    // ---------------- producer (claims one chunk ahead)
+    // ---------------- producer (claims one chunk ahead).  Chunks are claimed in
+    // runs of consecutive ones, long while many remain and one at a time at the
+    // end (guided), so that this CTA's consecutive chunks often share i2 and the
+    // consumers keep dG2[i2] in registers across them.
+    int run_c = 0, run_end = 0;
+    auto claim_next = [&]() {
+      if (run_c >= run_end) {
+        int k = 1, c0 = 0;
+        if (lane == 0) {
+          const int seen = (int)ld_relaxed_u32(&a.w.ctl->bwd_chunk_ctr);
+          k = (n_chunks - seen) / (2 * (int)gridDim.x);
+          k = k < 1 ? 1 : (k > kBwdRun ? kBwdRun : k);
+          c0 = (int)atomicAdd(&a.w.ctl->bwd_chunk_ctr, (uint32_t)k);
+        }
+        run_c = __shfl_sync(0xffffffffu, c0, 0);
+        run_end = run_c + __shfl_sync(0xffffffffu, k, 0);
+      }
+      return run_c++;
+    };
     auto next_chunk = [&](ChunkDesc& d) {
       for (;;) {
-        const int c = claim_chunk(&a.w.ctl->bwd_chunk_ctr);
+        const int c = claim_next();
         if (c >= n_chunks) return c;
         d = load_chunk(a.w.chunk_desc, c);
         if (d.whole) return c;
@@ -936,6 +963,7 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
                        : make_float4(0.f, 0.f, 0.f, 0.f);
       ChunkDesc dn{};
       const int cn = next_chunk(dn);
+      const int flush = cn >= n_chunks || a.w.pair_i2[dn.p0] != i2;
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
       char* st = base + s * C::STAGE_B;
       {
@@ -987,6 +1015,7 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
         m.nb = nb;
         m.npairs = npairs;
         m.end = 0;
+        m.flush = flush;
         mbar_arrive(&full[s]);
       }
       c = cn;
@@ -997,6 +1026,13 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
   }
 
   // ---------------- consumers (warps 0-7)
+  float dg2[2][4][4];                    // (4) of the CTA's current run of chunks of one i2
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dg2[mt][nt][i] = 0.f;
   for (int it = 0;; ++it) {
     const int s = it & 1;
     if (!mbar_wait(&full[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
@@ -1057,7 +1093,8 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
     }
     dp2_flush(acc, dP2, warp & 1, warp >> 1, lane);
     named_sync(1, 256);
-    mma_bwd_dg2(g1h, dph, a.dG2 + (size_t)m.i2 * C::R * C::NC, np, warp, lane);
+    mma_bwd_dg2(g1h, dph, dg2, np, warp, lane);
+    if (m.flush) dg2_flush(dg2, a.dG2 + (size_t)m.i2 * C::R * C::NC, warp, lane);
     mma_bwd_dg1(dph, g2h, m.pi1, a.dG1, np, warp, lane);
     named_sync(1, 256);
     if (tid == 0) mbar_arrive(&empty[s]);
