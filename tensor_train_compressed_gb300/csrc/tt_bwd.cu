@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(256) k_bwd_generic(BwdArgs a) {
 // A pair's missing second row reads a zero row.  Core gradients are
 // accumulated with vector float reductions.
 // Longest run of consecutive chunks one claim of the backward chunk kernel takes.
-constexpr int kBwdRun = 8;
+constexpr int kBwdRun = 16;
 
 struct MmaBwd {
   static constexpr int CP = kCP_8_32, R = 32, NC = 256, D = 128;
@@ -931,6 +931,7 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
     };
     ChunkDesc d{};
     int c = next_chunk(d);
+    int held_i2[2] = {-1, -1};           // the i2 whose G2 slice each stage holds
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t use = (uint32_t)it >> 1;
@@ -966,7 +967,8 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
       const int flush = cn >= n_chunks || a.w.pair_i2[dn.p0] != i2;
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) break;
       char* st = base + s * C::STAGE_B;
-      {
+      if (held_i2[s] != i2) {           // (a run of one i2 finds it there already)
+        held_i2[s] = i2;
         const uint16_t* h2 = a.w.g2h + (size_t)i2 * C::R * C::NC;
         const uint16_t* l2 = a.w.g2l + (size_t)i2 * C::R * C::NC;
 #pragma unroll 8
