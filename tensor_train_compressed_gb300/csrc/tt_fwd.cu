@@ -259,12 +259,13 @@ struct MmaFwd {
   struct Meta {
     int x0, x1, p0, np, npairs, end;
     int ck;               // checkpoint role: s + 1 writes slot s, -(s + 1) reads it, 0 none
-    int pad;
+    int nst;              // G3 rows staged (the chunk's first ROWMAX rows)
     int pair[MAXPAIRS];   // first row | (second row valid) << 8 | chunk-local prefix << 9
+    int g3i[ROWMAX];      // i3 of the staged rows (read by the G3 stager)
   };
   static constexpr int NCW = NC / CW;                // stage-2 columns per consumer warp
-  static constexpr int THREADS = 32 * CW + 64;       // consumers, lead producer, G2 copier
-  static constexpr int SMEM = 4 * (2 * STAGE_F + F_P2) + 2 * (int)sizeof(Meta) + 6 * 8 + 16;
+  static constexpr int THREADS = 32 * CW + 96;       // consumers, lead producer, G2 copier, G3 stager
+  static constexpr int SMEM = 4 * (2 * STAGE_F + F_P2) + 2 * (int)sizeof(Meta) + 8 * 8 + 16;
   static_assert(CW == 8 || CW == 16, "8 or 16 consumer warps");
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(MAXROWS <= 256 && CP <= 8 && 4 * CP <= 32, "pair encoding and G1 staging");
@@ -415,16 +416,20 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 2);
   uint64_t* empty = full + 2;
   uint64_t* go = empty + 2;                          // lead producer -> G2 copier, per stage
-  volatile int* slot = reinterpret_cast<volatile int*>(go + 2);   // the stage's i2, or -1: stop
+  uint64_t* go3 = go + 2;                            // lead producer -> G3 stager, per stage
+  volatile int* slot = reinterpret_cast<volatile int*>(go3 + 2);  // the stage's i2, or -1: stop
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    // full: the copy arrivals of both producer warps' 64 lanes + the lead's metadata arrival
-    mbar_init(&full[0], 65);
-    mbar_init(&full[1], 65);
+    // full: the copy arrivals of the three producer warps' 96 lanes + the lead's
+    // metadata arrival
+    mbar_init(&full[0], 97);
+    mbar_init(&full[1], 97);
     mbar_init(&empty[0], 1);
     mbar_init(&empty[1], 1);
     mbar_init(&go[0], 1);
     mbar_init(&go[1], 1);
+    mbar_init(&go3[0], 1);
+    mbar_init(&go3[1], 1);
     mbar_init_fence();
     if (blockIdx.x == 0) mark_split(a.w.ctl, a.G1, a.G2, a.G3);
   }
@@ -452,6 +457,35 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
   char* ck_data = reinterpret_cast<char*>(a.w.rowbuf + (size_t)U_r * C::D);
   uint32_t* ck_owner = a.w.ckpt;
   uint32_t* ck_ready = a.w.ckpt + kCkptSlots;
+
+  if (warp == CW + 2) {
+    // ---------------- G3 stager: stages the chunk's first ROWMAX G3 rows (the
+    // transposed split planes; the lead producer lists their i3 in the stage's
+    // metadata), per row lane = plane | j3 | 16-byte piece
+    for (int it = 0;; ++it) {
+      const int s = it & 1;
+      if (!mbar_wait(&go3[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
+      const int i2 = slot[s];
+      if (i2 != -1) {
+        const Meta& mg = meta[s];
+        const int nst = mg.nst;
+        char* G3s = reinterpret_cast<char*>(base + s * C::STAGE_F + C::F_G2 + C::F_P1);
+        const int plane = lane >> 4, j3 = (lane >> 2) & 3, q = lane & 3;
+        const uint16_t* src = plane ? a.w.g3tl : a.w.g3th;
+        for (int r0 = 0; r0 < nst; r0 += 8) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (r0 + u < nst)
+              cp_async16(G3s + plane * C::GTPLANE + (r0 + u) * C::GTROW + j3 * 80 + 16 * q,
+                         src + ((size_t)mg.g3i[r0 + u] * 4 + j3) * C::R + 8 * q);
+        }
+      }
+      cp_async_arrive_noinc(&full[s]);
+      if (i2 == -1) break;
+    }
+    cp_async_wait_all();
+    return;
+  }
 
   if (warp == CW + 1) {
     // ---------------- G2 copier: stages the G2 planes of the chunks the lead
@@ -496,6 +530,7 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
       if (lane == 0) {
         slot[s] = i2;
         mbar_arrive(&go[s]);
+        mbar_arrive(&go3[s]);
       }
     };
     struct PMeta {
@@ -571,10 +606,13 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
         }
         if (ck < 0 && lane == 0) atomicAdd(&a.w.ctl->ckpt_reused, 1);
       }
+      // the i3 of the rows the G3 stager stages for this chunk
+      if (lane < cur.nst) m.g3i[lane] = cur.g30;
+      if (lane + 32 < cur.nst) m.g3i[lane + 32] = cur.g31;
+      if (lane == 0) m.nst = cur.nst;
       release(s, ck < 0 ? -1 + ck : cur.i2);   // -2 - slot: the copier loads the checkpoint
       float* G2s = base + s * C::STAGE_F;
       float* P1n = G2s + C::F_G2;
-      float* G3s = P1n + C::F_P1;
       // G1[i1_p] planes: per prefix, lane = plane | j1 | piece (not for a reused P2)
 #pragma unroll
       for (int pp = 0; pp < C::CP; ++pp) {
@@ -583,19 +621,6 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
         if (pp < cur.np && ck >= 0)
           cp_async16(reinterpret_cast<char*>(P1n) + plane * C::G1PLANE + (4 * pp + j1) * (2 * C::G1LD) + 16 * q,
                      (plane ? a.w.g1l : a.w.g1h) + ((size_t)i1 * 4 + j1) * C::R + 8 * q);
-      }
-      // G3 rows: transposed split planes, per row lane = plane | j3 | 16-byte piece
-      for (int r0 = 0; r0 < cur.nst; r0 += 8) {
-        const int src = r0 < 32 ? cur.g30 : cur.g31;
-        int i3v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) i3v[u] = __shfl_sync(0xffffffffu, src, (r0 & 31) + u);
-        const int plane = lane >> 4, j3 = (lane >> 2) & 3, q = lane & 3;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (r0 + u < cur.nst)
-            cp_async16(reinterpret_cast<char*>(G3s) + plane * C::GTPLANE + (r0 + u) * C::GTROW + j3 * 80 + 16 * q,
-                       (plane ? a.w.g3tl : a.w.g3th) + ((size_t)i3v[u] * 4 + j3) * C::R + 8 * q);
       }
       cp_async_arrive_noinc(&full[s]);
       // pairs: a row starts a pair when its offset within its prefix is even;
