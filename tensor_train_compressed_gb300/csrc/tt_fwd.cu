@@ -533,12 +533,12 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
         mbar_arrive(&go3[s]);
       }
     };
+    // The metadata of a chunk, as loaded (every field a plain load or
+    // register arithmetic, so that issuing them does not wait for any)
     struct PMeta {
       int x0, x1, p0, np, nst, i2;
       int g30, g31;    // i3 of staged rows lane, lane + 32
-      int gi1, rs, re; // lane < np: i1 and chunk-local row range of prefix p0 + lane
-      int pe;          // lane < np: the first row after prefix p0 + lane
-      bool whole;      // the chunk starts at its first prefix's first row
+      int gi1, prs;    // lane < np: i1 and first row of prefix p0 + lane (else prs = x1)
     };
     auto load_meta = [&](const ChunkDesc& d, PMeta& pm) {
       pm.x0 = d.x0;
@@ -550,25 +550,59 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
       pm.g30 = lane < pm.nst ? a.w.row_i3[d.x0 + lane] : 0;
       pm.g31 = lane + 32 < pm.nst ? a.w.row_i3[d.x0 + lane + 32] : 0;
       pm.gi1 = 0;
-      pm.rs = pm.re = rows;
-      pm.pe = d.x1;
-      pm.whole = d.whole;
+      pm.prs = d.x1;
       if (lane < pm.np) {
         pm.gi1 = a.w.pair_i1[d.p0 + lane];
-        pm.rs = max(a.w.pair_row_start[d.p0 + lane], d.x0) - d.x0;
-        pm.pe = a.w.pair_row_start[d.p0 + lane + 1];
-        pm.re = min(pm.pe, d.x1) - d.x0;
+        pm.prs = a.w.pair_row_start[d.p0 + lane];
       }
       pm.i2 = a.w.pair_i2[d.p0];
     };
-    // the c-th claim takes chunk chunk_order[c]
+    // The c-th claim takes chunk chunk_order[c].  Every dependent step of a
+    // chunk's bookkeeping gets one iteration of slack: the claim of chunk k + 3
+    // is issued at the start of iteration k and read at its end, when the load
+    // of its order entry is issued; chunk k + 2's descriptor is loaded late in
+    // iteration k from that entry, chunk k + 1's metadata at its start, and
+    // chunk k + 1's checkpoint role (ready check or slot claim) is decided from
+    // its descriptor during iteration k.
     const int32_t* order = a.w.chunk_order;
-    PMeta cur{}, nxt{};
-    int c = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
-    if (c < n_chunks) load_meta(load_chunk(a.w.chunk_desc, order[c]), cur);
-    int cn = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
-    ChunkDesc dn{};
+    uint32_t* ctr = &a.w.ctl->fwd_chunk_ctr;
+    int c = claim_chunk(ctr), cn = claim_chunk(ctr), cnn = claim_chunk(ctr);
+    ChunkDesc d0{}, dn{};
+    if (c < n_chunks) d0 = load_chunk(a.w.chunk_desc, order[c]);
     if (cn < n_chunks) dn = load_chunk(a.w.chunk_desc, order[cn]);
+    int onn = cnn < n_chunks ? order[cnn] : 0;
+    PMeta cur{}, nxt{};
+    if (c < n_chunks) load_meta(d0, cur);
+    // checkpoint role of one chunk: 0 none, s + 1 writes slot s, -(s + 1) reads it
+    // (lane 0 issues the check; `resolve` reads its result)
+    auto role_issue = [&](const ChunkDesc& d, int& kind, int& sl, uint32_t& v) {
+      kind = 0;
+      sl = 0;
+      v = 0;
+      if (n_slots > 0 && d.p1 == d.p0) {
+        sl = d.p0 % n_slots;
+        if (!d.whole) {                 // a later piece: reuse the slot if it is ready
+          kind = 1;
+          if (lane == 0) v = ld_acquire_u32(ck_ready + sl);
+        } else if (d.cont) {            // the first piece of a hot prefix: checkpoint its P2
+          kind = 2;
+          if (lane == 0) v = atomicCAS(ck_owner + sl, 0u, (uint32_t)d.p0 + 1u);
+        }
+      }
+    };
+    auto role_resolve = [&](const ChunkDesc& d, int kind, int sl, uint32_t v) {
+      v = __shfl_sync(0xffffffffu, v, 0);
+      if (kind == 1 && v == (uint32_t)d.p0 + 1u) return -(sl + 1);
+      if (kind == 2 && v == 0u) return sl + 1;
+      return 0;
+    };
+    int ck_cur = 0;
+    if (c < n_chunks) {
+      int kind, sl;
+      uint32_t v;
+      role_issue(d0, kind, sl, v);
+      ck_cur = role_resolve(d0, kind, sl, v);
+    }
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t use = (uint32_t)it >> 1;
@@ -584,28 +618,17 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
         break;
       }
       if (cn < n_chunks) load_meta(dn, nxt);
-      const int cnn = claim_chunk(&a.w.ctl->fwd_chunk_ctr);
+      uint32_t tk = 0;
+      if (lane == 0) tk = atomicAdd(ctr, 1u);
+      int kind_n = 0, sl_n = 0;
+      uint32_t v_n = 0;
+      if (cn < n_chunks) role_issue(dn, kind_n, sl_n, v_n);
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.w.ctl)) {
         release(s, -1);
         break;
       }
-      // checkpoint role of a one-prefix chunk of a hot prefix
-      int ck = 0;
-      if (n_slots > 0 && cur.np == 1) {
-        const int sl = cur.p0 % n_slots;
-        const int pe0 = __shfl_sync(0xffffffffu, cur.pe, 0);
-        uint32_t v = 0;
-        if (!cur.whole) {                 // a later piece: reuse the slot if it is ready
-          if (lane == 0) v = ld_acquire_u32(ck_ready + sl);
-          v = __shfl_sync(0xffffffffu, v, 0);
-          if (v == (uint32_t)cur.p0 + 1u) ck = -(sl + 1);
-        } else if (pe0 > cur.x1) {        // the first piece: checkpoint its P2
-          if (lane == 0) v = atomicCAS(ck_owner + sl, 0u, (uint32_t)cur.p0 + 1u);
-          v = __shfl_sync(0xffffffffu, v, 0);
-          if (v == 0u) ck = sl + 1;
-        }
-        if (ck < 0 && lane == 0) atomicAdd(&a.w.ctl->ckpt_reused, 1);
-      }
+      const int ck = ck_cur;
+      if (ck < 0 && lane == 0) atomicAdd(&a.w.ctl->ckpt_reused, 1);
       // the i3 of the rows the G3 stager stages for this chunk
       if (lane < cur.nst) m.g3i[lane] = cur.g30;
       if (lane + 32 < cur.nst) m.g3i[lane + 32] = cur.g31;
@@ -627,7 +650,8 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
       // the list follows row order (prefix after prefix)
       int rsq[C::CP];
 #pragma unroll
-      for (int j = 0; j < C::CP; ++j) rsq[j] = __shfl_sync(0xffffffffu, cur.rs, j);
+      for (int j = 0; j < C::CP; ++j)   // chunk-local first row of each prefix (rows past the last)
+        rsq[j] = max(__shfl_sync(0xffffffffu, cur.prs, j), cur.x0) - cur.x0;
       const int rows = cur.x1 - cur.x0;
       int npairs = 0;
       for (int rb = 0; rb < rows; rb += 32) {
@@ -660,11 +684,17 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
         mbar_arrive(&full[s]);
       }
       ChunkDesc dnn{};
-      if (cnn < n_chunks) dnn = load_chunk(a.w.chunk_desc, order[cnn]);
+      if (cnn < n_chunks) dnn = load_chunk(a.w.chunk_desc, onn);
+      const int ck_nxt = cn < n_chunks ? role_resolve(dn, kind_n, sl_n, v_n) : 0;
+      const int c3 = __shfl_sync(0xffffffffu, (int)tk, 0);
+      const int onew = c3 < n_chunks ? order[c3] : 0;
       c = cn;
       cur = nxt;
+      ck_cur = ck_nxt;
       cn = cnn;
       dn = dnn;
+      cnn = c3;
+      onn = onew;
     }
     cp_async_wait_all();
     return;

@@ -212,6 +212,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 struct ChunkDesc {
   int x0, x1, p0, p1;
   bool whole;
+  bool cont;   // the next chunk (row order) is a later piece of this chunk's last prefix
 };
 __device__ __forceinline__ ChunkDesc load_chunk(const int2* __restrict__ desc, int c) {
   const int2 a = desc[c], b = desc[c + 1];
@@ -222,6 +223,7 @@ __device__ __forceinline__ ChunkDesc load_chunk(const int2* __restrict__ desc, i
   d.whole = a.y < 0;
   // the next chunk starts a new prefix, or continues (a piece of) this one
   d.p1 = (b.y & 0x7fffffff) - (b.y < 0 ? 1 : 0);
+  d.cont = b.y >= 0;
   return d;
 }
 // Lane 0 of the calling warp claims the next work chunk; broadcast to the warp.
