@@ -124,13 +124,20 @@ typedef struct {
  * (sum pooling).  All tables share n and R (TT_EMB_ERR_ARG otherwise); their m,
  * batches and workspaces are their own, and workspaces must not overlap.
  * Each table is grouped into its own workspace as by a forward-only call
- * (TT_EMB_FORWARD_ONLY: a backward must not reuse these groupings); for shapes served by the
- * tiled chunk kernel (n = (4, 8, 4) with R1 = R2 = 64, n = (4, 4, 4) with
- * R1 = R2 = 16) one persistent launch of that kernel then works through the
- * chunks of all tables (one counter, chunks numbered across the tables), so
- * the tables share the grid instead of each draining it; other shapes run
- * table by table.  num_tables in [1, 8]. */
+ * (TT_EMB_FORWARD_ONLY: a backward must not reuse these groupings); for
+ * n = (4, 8, 4) with R1 = R2 = 64 (tensor-core chunk kernel) and n = (4, 4, 4)
+ * with R1 = R2 = 16 (tiled FP32 chunk kernel) one persistent launch then works
+ * through the chunks of all tables (one counter, chunks numbered across the
+ * tables), so the tables share the grid instead of each draining it; other
+ * shapes run table by table.  num_tables in [1, 8]. */
 int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stream);
+
+/* tt_emb_forward_tables with flags: 0 or TT_EMB_CORES_SPLIT, which promises
+ * that every table's workspace already holds the split of that table's cores
+ * (tt_emb_split or tt_emb_sgd_ex on that workspace, as for tt_emb_forward_ex);
+ * the per-call split of the cores is then skipped.  Other flag bits:
+ * TT_EMB_ERR_ARG. */
+int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int flags, void* stream);
 
 /* Pooling rules of tt_emb_forward_ex / tt_emb_backward_ex. */
 #define TT_EMB_POOL_SUM 0    /* out[b] = sum of the bag's rows (optionally weighted)   */

@@ -34,7 +34,7 @@ _POOLING = {"sum": TT_EMB_POOL_SUM, "mean": TT_EMB_POOL_MEAN}
 
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
             "tt_emb_forward_ex", "tt_emb_backward_ex", "tt_emb_split", "tt_emb_sgd_ex",
-            "tt_emb_forward_tables", "tt_emb_workspace_bytes_d", "tt_emb_forward_d",
+            "tt_emb_forward_tables", "tt_emb_forward_tables_ex", "tt_emb_workspace_bytes_d", "tt_emb_forward_d",
             "tt_emb_backward_d", "tt_emb_sgd_d", "tt_emb_step_host",
             "tt_emb_sgd", "tt_emb_get_error", "tt_emb_grouping_view", "tt_emb_profile_start",
             "tt_emb_profile_stop", "tt_emb_profile_read", "tt_emb_forward_static",
@@ -94,6 +94,7 @@ def lib():
                                         P, P, SZ, P]
         L.tt_emb_split.argtypes = [P, P, P, P, P, SZ, P]
         L.tt_emb_forward_tables.argtypes = [ctypes.c_int, P, P]
+        L.tt_emb_forward_tables_ex.argtypes = [ctypes.c_int, P, ctypes.c_int, P]
         C = ctypes.c_int
         L.tt_emb_workspace_bytes_d.argtypes = [C, P, P, P, I64, I64, ctypes.POINTER(SZ)]
         L.tt_emb_forward_d.argtypes = [C, P, P, P, P, P, I64, P, I64, P, P, SZ, P]
@@ -223,9 +224,10 @@ def tt_emb_sgd(cores, core_grads, m, n, R, lr: float, zero_grads: bool = False, 
                             _stream(stream)), "tt_emb_sgd")
 
 
-def tt_emb_forward_tables(tables, stream=None):
+def tt_emb_forward_tables(tables, stream=None, flags: int = 0):
     """tables: sequence of dicts with the tt_emb_forward arguments (cores, m, n, R, indices,
-    offsets, out, workspace); every table needs its own workspace."""
+    offsets, out, workspace); every table needs its own workspace.  flags != 0 calls
+    tt_emb_forward_tables_ex (TT_EMB_CORES_SPLIT: every workspace holds its table's split)."""
     arr = (Table * len(tables))()
     for k, t in enumerate(tables):
         e = arr[k]
@@ -240,8 +242,13 @@ def tt_emb_forward_tables(tables, stream=None):
         e.out = _dev(t["out"], torch.float32, "out")
         e.workspace = _dev(t["workspace"], torch.uint8, "workspace")
         e.ws_bytes = t["workspace"].numel()
-    _check(lib().tt_emb_forward_tables(len(tables), ctypes.cast(arr, ctypes.c_void_p),
-                                       _stream(stream)), "tt_emb_forward_tables")
+    if flags:
+        _check(lib().tt_emb_forward_tables_ex(len(tables), ctypes.cast(arr, ctypes.c_void_p),
+                                              int(flags), _stream(stream)),
+               "tt_emb_forward_tables_ex")
+    else:
+        _check(lib().tt_emb_forward_tables(len(tables), ctypes.cast(arr, ctypes.c_void_p),
+                                           _stream(stream)), "tt_emb_forward_tables")
 
 
 def _shape_d(m, n, R):

@@ -79,7 +79,7 @@ Layout make_layout(const Shape& s, int64_t nnz, int64_t num_bags) {
   L.zero_end = off;   // every grouping zeroes [ctl, zero_end)
   // bf16 split planes of the cores, at offsets fixed by the shape: a split made
   // by tt_emb_split or tt_emb_sgd_ex outlives the groupings of later batches
-  if (tc_shape(s)) {
+  if (split_shape(s)) {
     const size_t n1 = (size_t)s.m1 * s.n1 * s.R1, n2 = (size_t)s.m2 * s.R1 * s.n2 * s.R2;
     const size_t n3 = (size_t)s.m3 * s.R2 * s.n3;
     L.g1h = take(2 * n1);
@@ -339,7 +339,12 @@ int tt_emb_forward(const float* const cores[3], const int64_t m[3], const int32_
 }
 
 int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stream) {
+  return tt_emb_forward_tables_ex(num_tables, tables, 0, stream);
+}
+
+int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int flags, void* stream) {
   if (num_tables < 1 || num_tables > kMaxTables || !tables) return TT_EMB_ERR_ARG;
+  if (flags & ~TT_EMB_CORES_SPLIT) return TT_EMB_ERR_ARG;
   Shape s[kMaxTables];
   Layout L[kMaxTables];
   WS w[kMaxTables];
@@ -387,7 +392,8 @@ int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stre
         cudaMemsetAsync(out[t], 0, sizeof(float) * (size_t)bags[t] * s[t].D, st) != cudaSuccess)
       return TT_EMB_ERR_CUDA;
   }
-  return launch_forward_tables(num_tables, s, L, w, cores, offsets, nnz, bags, out, st);
+  return launch_forward_tables(num_tables, s, L, w, cores, offsets, nnz, bags, out,
+                               (flags & TT_EMB_CORES_SPLIT) ? 1 : 0, st);
 }
 
 int tt_emb_backward_ex(const float* grad_out, const float* const cores[3], const int64_t m[3],

@@ -1271,7 +1271,9 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
                                                                   w.rowbuf, s.D, grad_out,
                                                                   grad_weights)));
   }
-  const SplitArgs sp = make_split_args(s, w, cores);
+  // the split planes only where the backward's chunk kernel reads them
+  SplitArgs sp = make_split_args(s, w, cores);
+  if (!tc_shape(s)) sp.g2l = nullptr;
   switch (pool.mode) {
     case kPoolWeighted:
       launch_s_gather<kPoolWeighted>(s, L, w, grad_out, nnz, num_bags, offsets, pool.psw, sp, reuse,

@@ -885,13 +885,12 @@ static size_t fwd_generic_smem(const Shape& s, int CP) {
 }
 
 // Which chunk kernel serves a shape, and its chunking parameters.
-enum FwdKind { kFwdGeneric = 0, kFwdTiled_8_32, kFwdTiled_8_64, kFwdTiled_4_16 };
+enum FwdKind { kFwdGeneric = 0, kFwdMma_8_32, kFwdMma_8_64, kFwdTiled_4_16 };
 
 static FwdKind fwd_kind(const Shape& s) {
-  if (tc_shape(s)) return kFwdTiled_8_32;
-  if (s.n1 != 4 || s.n3 != 4 || s.R1 != s.R2) return kFwdGeneric;
-  if (s.n2 == 8 && s.R1 == 64) return kFwdTiled_8_64;
-  if (s.n2 == 4 && s.R1 == 16) return kFwdTiled_4_16;
+  if (tc_shape(s)) return kFwdMma_8_32;
+  if (tc64_shape(s)) return kFwdMma_8_64;
+  if (s.n1 == 4 && s.n3 == 4 && s.n2 == 4 && s.R1 == 16 && s.R2 == 16) return kFwdTiled_4_16;
   return kFwdGeneric;
 }
 
@@ -903,8 +902,8 @@ int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chu
   if (cp > 16) cp = 16;
   if (cp < 1) cp = 1;
   switch (fwd_kind(s)) {
-    case kFwdTiled_8_32: cp = kCP_8_32; break;
-    case kFwdTiled_8_64: cp = kCP_8_64; break;
+    case kFwdMma_8_32: cp = kCP_8_32; break;
+    case kFwdMma_8_64: cp = kCP_8_64; break;
     case kFwdTiled_4_16: cp = kCP_4_16; break;
     default: break;
   }
@@ -944,10 +943,6 @@ static void launch_tiled(const TiledTables& tt, cudaStream_t st) {
   TT_TIMED("k_fwd_tiled", st, (k_fwd_tiled<N2, R, CP><<<grid, 256, T::SMEM, st>>>(tt)));
 }
 
-static void launch_tiled_kind(FwdKind kind, const TiledTables& tt, cudaStream_t st) {
-  if (kind == kFwdTiled_8_64) launch_tiled<8, 64, kCP_8_64>(tt, st);
-  else launch_tiled<4, 16, kCP_4_16>(tt, st);
-}
 
 int launch_rows(const Shape& s, const WS& w, const float* const cores[3], int presplit,
                 cudaStream_t st) {
@@ -961,19 +956,26 @@ int launch_rows(const Shape& s, const WS& w, const float* const cores[3], int pr
   fa.G2 = cores[1];
   fa.G3 = cores[2];
   switch (fwd_kind(s)) {
-    case kFwdTiled_8_32:
+    case kFwdMma_8_32:
       if (!presplit) {
         rc = launch_split(s, w, cores, 0, st);
         if (rc) return rc;
       }
       launch_fwd_mma<8>(fa, st);
       break;
-    case kFwdTiled_8_64:
+    case kFwdMma_8_64: {
+      if (!presplit) {
+        rc = launch_split(s, w, cores, 0, st);
+        if (rc) return rc;
+      }
+      const float* const* c3 = cores;
+      return launch_fwd_mma64(1, &w, &c3, st);
+    }
     case kFwdTiled_4_16: {
       TiledTables tt;
       tt.t[0] = fa;
       tt.T = 1;
-      launch_tiled_kind(fwd_kind(s), tt, st);
+      launch_tiled<4, 16, kCP_4_16>(tt, st);
       break;
     }
     default: {
@@ -1084,30 +1086,50 @@ __global__ void __launch_bounds__(256) k_pool128_tables(const __grid_constant__ 
 int launch_forward_tables(int T, const Shape* s, const Layout* L, const WS* w,
                           const float* const* const* cores, const int64_t* const* offsets,
                           const int64_t* nnz, const int64_t* num_bags, float* const* out,
-                          cudaStream_t st) {
+                          int presplit, cudaStream_t st) {
   const FwdKind kind = fwd_kind(s[0]);
-  if (kind != kFwdTiled_8_64 && kind != kFwdTiled_4_16) {
+  if (kind != kFwdMma_8_64 && kind != kFwdTiled_4_16) {
     for (int t = 0; t < T; ++t) {
       if (nnz[t] == 0) continue;
       const Pooling pool{kPoolSum, nullptr};
       const int rc = launch_forward(s[t], L[t], w[t], cores[t], offsets[t], nnz[t], num_bags[t],
-                                    pool, 0, out[t], st);
+                                    pool, presplit, out[t], st);
       if (rc) return rc;
     }
     return TT_EMB_OK;
   }
-  TiledTables tt;
-  tt.T = 0;
-  for (int t = 0; t < T; ++t) {
-    if (nnz[t] == 0) continue;
-    FwdArgs& fa = tt.t[tt.T++];
-    fa.s = s[t];
-    fa.w = w[t];
-    fa.G1 = cores[t][0];
-    fa.G2 = cores[t][1];
-    fa.G3 = cores[t][2];
+  if (kind == kFwdMma_8_64) {
+    // the split of every table with lookups, then one launch over all their chunks
+    WS wt[kMaxTables];
+    const float* const* ct[kMaxTables];
+    int n = 0;
+    for (int t = 0; t < T; ++t) {
+      if (nnz[t] == 0) continue;
+      if (!presplit) {
+        const int rc = launch_split(s[t], w[t], cores[t], 0, st);
+        if (rc) return rc;
+      }
+      wt[n] = w[t];
+      ct[n++] = cores[t];
+    }
+    if (n > 0) {
+      const int rc = launch_fwd_mma64(n, wt, ct, st);
+      if (rc) return rc;
+    }
+  } else {
+    TiledTables tt;
+    tt.T = 0;
+    for (int t = 0; t < T; ++t) {
+      if (nnz[t] == 0) continue;
+      FwdArgs& fa = tt.t[tt.T++];
+      fa.s = s[t];
+      fa.w = w[t];
+      fa.G1 = cores[t][0];
+      fa.G2 = cores[t][1];
+      fa.G3 = cores[t][2];
+    }
+    if (tt.T > 0) launch_tiled<4, 16, kCP_4_16>(tt, st);
   }
-  if (tt.T > 0) launch_tiled_kind(kind, tt, st);
   if (s[0].D == 128) {
     // the pooling of every table with lookups in one launch
     PoolTables pt;

@@ -145,10 +145,18 @@ struct WS {
   uint16_t* g3tl;
 };
 
-// Shapes served by the tensor-core chunk kernels (n1 = n3 = 4, n2 = 8, R1 = R2 = 32).
+// Shapes served by the tensor-core chunk kernels of the forward and the
+// backward (n1 = n3 = 4, n2 = 8, R1 = R2 = 32).
 inline bool tc_shape(const Shape& s) {
   return s.n1 == 4 && s.n2 == 8 && s.n3 == 4 && s.R1 == 32 && s.R2 == 32;
 }
+// n1 = n3 = 4, n2 = 8, R1 = R2 = 64: forward rows on the tensor cores
+// (k_fwd_mma64), backward on the generic kernel.
+inline bool tc64_shape(const Shape& s) {
+  return s.n1 == 4 && s.n2 == 8 && s.n3 == 4 && s.R1 == 64 && s.R2 == 64;
+}
+// Shapes whose workspace holds the bf16 split planes of the cores.
+inline bool split_shape(const Shape& s) { return tc_shape(s) || tc64_shape(s); }
 
 // ---------------------------------------------------------------- device helpers
 
@@ -390,7 +398,10 @@ int forward_chunk_params(const Shape& s, int* pairs_per_chunk, int* rows_per_chu
 int launch_forward_tables(int T, const Shape* s, const Layout* L, const WS* w,
                           const float* const* const* cores, const int64_t* const* offsets,
                           const int64_t* nnz, const int64_t* num_bags, float* const* out,
-                          cudaStream_t st);
+                          int presplit, cudaStream_t st);
+// R = 64 tensor-core rows of T tables in one launch (tt_fwd64.cu); the split
+// planes of every table must hold its cores
+int launch_fwd_mma64(int T, const WS* w, const float* const* const* cores, cudaStream_t st);
 // backward (tt_bwd.cu)
 int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* grad_out, int reuse,
                     const float* const cores[3], const int64_t* offsets, int64_t nnz,
