@@ -129,7 +129,8 @@ typedef struct {
  * with R1 = R2 = 16 (tiled FP32 chunk kernel) one persistent launch then works
  * through the chunks of all tables (one counter, chunks numbered across the
  * tables), so the tables share the grid instead of each draining it; other
- * shapes run table by table.  num_tables in [1, 8]. */
+ * shapes run table by table.  num_tables in [1, 8]; the tables' bags together
+ * fewer than 2^31 (TT_EMB_ERR_ARG otherwise). */
 int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stream);
 
 /* tt_emb_forward_tables with flags: 0 or TT_EMB_CORES_SPLIT, which promises

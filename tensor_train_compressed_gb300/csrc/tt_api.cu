@@ -352,6 +352,7 @@ int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int fla
   const int64_t* offsets[kMaxTables];
   int64_t nnz[kMaxTables], bags[kMaxTables];
   float* out[kMaxTables];
+  int64_t total_bags = 0;
   for (int t = 0; t < num_tables; ++t) {
     const tt_emb_table& tb = tables[t];
     int rc = shape_from_args(tb.m, tb.n, tb.R, &s[t]);
@@ -373,6 +374,8 @@ int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int fla
       if (a0 < b0 + tables[u].ws_bytes && b0 < a0 + tb.ws_bytes) return TT_EMB_ERR_ARG;
     }
     w[t] = make_ws(tb.workspace, L[t]);
+    total_bags += tb.num_bags;
+    if (total_bags >= (1ll << 31)) return TT_EMB_ERR_ARG;   // bags are numbered in 32 bits
     cores[t] = tb.cores;
     offsets[t] = tb.offsets;
     nnz[t] = tb.nnz;

@@ -1035,39 +1035,42 @@ int launch_forward(const Shape& s, const Layout& L, const WS& w, const float* co
 
 // Sum pooling of several tables (D = 128) in one launch: bags are numbered
 // across the tables (bag_base[t] = first bag of table t), each warp takes bags
-// by grid stride and pools them as k_pool128<kPoolSum> does.
+// by grid stride and pools them as k_pool128<kPoolSum> does (4-warp CTAs,
+// 32-bit positions, offsets read by their low word and clamped).
 struct PoolTables {
   const int64_t* offsets[kMaxTables];
-  int64_t nnz[kMaxTables];
+  int32_t nnz[kMaxTables];
   const int32_t* uid[kMaxTables];
   const float4* rb4[kMaxTables];
   int32_t zrow[kMaxTables];
   float4* out[kMaxTables];
   int32_t* bag_of[kMaxTables];
-  int64_t bag_base[kMaxTables + 1];
+  int32_t bag_base[kMaxTables + 1];
   int T;
 };
 
-__global__ void __launch_bounds__(256) k_pool128_tables(const __grid_constant__ PoolTables pt) {
+__global__ void __launch_bounds__(kPoolThreads, kPoolCtasPerSm)
+    k_pool128_tables(const __grid_constant__ PoolTables pt) {
   const int lane = threadIdx.x & 31;
-  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const int64_t total = pt.bag_base[pt.T];
-  for (int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < total;
-       g += warps) {
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  const int total = pt.bag_base[pt.T];
+  for (int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < total; g += warps) {
     int t = 0;
     while (t + 1 < pt.T && g >= pt.bag_base[t + 1]) ++t;
-    const int64_t b = g - pt.bag_base[t], nnz = pt.nnz[t];
-    int64_t l0 = pt.offsets[t][b], l1 = pt.offsets[t][b + 1];
+    const int b = g - pt.bag_base[t], nnz = pt.nnz[t];
+    const int32_t* off32 = reinterpret_cast<const int32_t*>(pt.offsets[t]);
+    int l0 = off32[2 * (int64_t)b], l1 = off32[2 * (int64_t)b + 2];
     l0 = l0 < 0 ? 0 : (l0 > nnz ? nnz : l0);
     l1 = l1 < l0 ? l0 : (l1 > nnz ? nnz : l1);
     const int32_t* uid = pt.uid[t];
     const float4* rb4 = pt.rb4[t];
     const int32_t zrow = pt.zrow[t];
+    int32_t* bag_of = pt.bag_of[t];
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t lb = l0; lb < l1; lb += 32) {
-      const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
+    for (int lb = l0; lb < l1; lb += 32) {
+      const int cnt = l1 - lb < 32 ? l1 - lb : 32;
       int32_t my_u = lane < cnt ? uid[lb + lane] : zrow;
-      if (lane < cnt) pt.bag_of[t][lb + lane] = (int32_t)b;
+      if (lane < cnt) bag_of[lb + lane] = b;
       my_u = my_u < 0 ? zrow : my_u;
       int j = 0;
       for (; j + 8 <= cnt; j += 8) {
@@ -1079,7 +1082,7 @@ __global__ void __launch_bounds__(256) k_pool128_tables(const __grid_constant__ 
       }
       for (; j < cnt; ++j) f4add(acc, rb4[(int64_t)__shfl_sync(0xffffffffu, my_u, j) * 32 + lane]);
     }
-    pt.out[t][b * 32 + lane] = acc;
+    pt.out[t][(int64_t)b * 32 + lane] = acc;
   }
 }
 
@@ -1139,19 +1142,20 @@ int launch_forward_tables(int T, const Shape* s, const Layout* L, const WS* w,
       if (nnz[t] == 0 || num_bags[t] == 0) continue;
       const int k = pt.T++;
       pt.offsets[k] = offsets[t];
-      pt.nnz[k] = nnz[t];
+      pt.nnz[k] = (int32_t)nnz[t];
       pt.uid[k] = w[t].uid;
       pt.rb4[k] = reinterpret_cast<const float4*>(w[t].rowbuf);
       pt.zrow[k] = (int32_t)L[t].rowbuf_rows;
       pt.out[k] = reinterpret_cast<float4*>(out[t]);
       pt.bag_of[k] = w[t].bag_of;
-      pt.bag_base[k + 1] = pt.bag_base[k] + num_bags[t];
+      pt.bag_base[k + 1] = pt.bag_base[k] + (int32_t)num_bags[t];
     }
     if (pt.T > 0) {
-      int grid = (int)ceil_div(pt.bag_base[pt.T], 8);
-      const int cap = sm_count() * 16;
+      // two full waves of 4-warp CTAs, as for one table
+      int grid = (int)ceil_div(pt.bag_base[pt.T], kPoolThreads / 32);
+      const int cap = sm_count() * kPoolCtasPerSm * 2;
       if (grid > cap) grid = cap;
-      TT_TIMED("k_pool", st, (k_pool128_tables<<<grid, 256, 0, st>>>(pt)));
+      TT_TIMED("k_pool", st, (k_pool128_tables<<<grid, kPoolThreads, 0, st>>>(pt)));
     }
   } else {
     for (int t = 0; t < T; ++t)

@@ -106,8 +106,11 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
   const uint32_t M = (uint32_t)s.M, m1 = (uint32_t)s.m1, m3 = (uint32_t)s.m3;
   const int64_t seg0 = (int64_t)c * a.L;
   const int64_t seg1 = seg0 + a.L < a.nnz ? seg0 + a.L : a.nnz;
-  constexpr int kSpan = 32 * ITEMS;
-  auto pos_of = [&](int it) { return seg0 + warp * kSpan + it * 32 + lane; };
+  // item it of warp w: positions seg0 + 32 (it * warps + w) + lane, so that every
+  // warp holds lookups whatever the segment's length (the order of the items
+  // of a segment does not matter here)
+  const int64_t pos_base = seg0 + warp * 32 + lane;
+  auto pos_of = [&](int it) { return pos_base + it * (32 * kCoopWarps); };
 
   uint32_t key[ITEMS];
   // ------------------------------------------------------------------ phase 0
@@ -308,6 +311,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
       rb += wtot[0][w2];
       pb += wtot[1][w2];
     }
+    stamp();
     // eight runs' words loaded at a time
     for (uint32_t j0 = 0; j0 < Kr; j0 += 8) {
       uint32_t bw[8];
@@ -341,6 +345,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
         rb += run_tot;
       }
     }
+    stamp();
     for (uint32_t j = 0; j < Kp; ++j) {
       const uint32_t wd = pw0 + 32 * j + lane;
       const uint32_t bits = wd < p1 ? __ldcg(&a.pbm[wd].x) : 0u;
@@ -591,6 +596,7 @@ int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, const int6
   ba.trace = reinterpret_cast<unsigned long long*>(w.hist + 128);
   if (Lseg <= kCoopThreads * 4) return launch_bitmap_items<4>(ba, G, st);
   if (Lseg <= kCoopThreads * 8) return launch_bitmap_items<8>(ba, G, st);
+  if (Lseg <= kCoopThreads * 12) return launch_bitmap_items<12>(ba, G, st);
   return launch_bitmap_items<16>(ba, G, st);
 }
 

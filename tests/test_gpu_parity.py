@@ -169,15 +169,15 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-@pytest.mark.parametrize("items", [4, 8, 16])
+@pytest.mark.parametrize("items", [4, 8, 12, 16])
 def test_bitmap_grouping_every_variant(items):
     """The key-bitmap grouping of a forward-only call keeps ceil(nnz / SMs) lookups per
-    CTA in registers, 4, 8 or 16 per thread (512 threads); the batch size picks the
+    CTA in registers, 4, 8, 12 or 16 per thread (512 threads); the batch size picks the
     variant.  Each one runs here on the benchmark table's shape and index distribution
     (dense in the table: at most 8 bitmap words per lookup), is compared with the
     oracle's grouping, and its output equals the sort-grouped forward's bit for bit."""
     G = _sms()
-    lo, hi = G * 512 * {4: 0, 8: 4, 16: 8}[items], G * 512 * items
+    lo, hi = G * 512 * {4: 0, 8: 4, 12: 8, 16: 12}[items], G * 512 * items
     target = (lo + hi) // 2 if items > 4 else hi - 1000
     x = make_inputs(3, num_bags=target // 20)                # fixed bag length 20
     assert lo < x.nnz <= hi
