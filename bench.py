@@ -236,10 +236,10 @@ def weak_throughput(units_per_rank: int, world: int, ms_max: float) -> float:
 class Workload:
     """Device-resident inputs of one workload plus its captured step graphs."""
 
-    def __init__(self, cfg: int, train: bool, torch, tte, stream, mapping=None):
+    def __init__(self, cfg: int, train: bool, torch, tte, stream, mapping=None, bags=None):
         from tensor_train_compressed_gb300.inputs import make_inputs
         self.torch, self.tte, self.stream = torch, tte, stream
-        self.x = x = make_inputs(cfg, with_grad=train, mapping=mapping)
+        self.x = x = make_inputs(cfg, with_grad=train, mapping=mapping, num_bags=bags)
         self.train = train
         dev = torch.device("cuda")
         self.cores0 = [torch.from_numpy(c).to(dev) for c in x.cores]
@@ -299,12 +299,13 @@ class MultiTableWorkload(Workload):
     As for the single-table inference forward, every table's cores are split
     into its workspace once, at load time, and the calls pass TT_EMB_CORES_SPLIT."""
 
-    def __init__(self, cfg: int, torch, tte, stream):
+    def __init__(self, cfg: int, torch, tte, stream, bags=None):
         from tensor_train_compressed_gb300.inputs import CONFIGS, make_inputs
         self.torch, self.tte, self.stream = torch, tte, stream
         self.train = False
         dev = torch.device("cuda")
-        self.xs = [make_inputs(cfg, table=t) for t in range(len(CONFIGS[cfg]["tables"]))]
+        self.xs = [make_inputs(cfg, table=t, num_bags=bags)
+                   for t in range(len(CONFIGS[cfg]["tables"]))]
         self.x = self.xs[0]
         self.tables = []
         for x in self.xs:
@@ -468,8 +469,8 @@ def run_ours(args, rank, world, dist):
         todo = tuple(t for t in todo if t[0] == args.only)
     for name, cfg, train, mapping in todo:
         main = name == "train"
-        wl = (MultiTableWorkload(cfg, torch, tte, stream) if name == "forward8"
-              else Workload(cfg, train, torch, tte, stream, mapping))
+        wl = (MultiTableWorkload(cfg, torch, tte, stream, args.bags) if name == "forward8"
+              else Workload(cfg, train, torch, tte, stream, mapping, args.bags))
         with torch.cuda.stream(stream):
             for _ in range(2):          # eager warm-up (also settles the library's caches)
                 wl.restore()
@@ -624,7 +625,8 @@ def run_ours(args, rank, world, dist):
         ach8 = a8["fwd_contract"] / (kms_f8[contract8] * 1e-3) / 1e12
         f8_line["contraction"] = {"kernel": contract8, "bound": "alu", "achieved": round(ach8, 3),
                                   "peak": round(p_fp32, 2), "unit": "TFLOP/s",
-                                  "frac": round(ach8 / p_fp32, 4)}
+                                  "frac": round(ach8 / p_fp32, 4),
+                                  "traffic": stored_traffic(contract8, "forward8")}
         if contract8 in TENSOR_SPLIT_KERNELS:
             pt = pk["bf16_tflops"] / 3.0
             f8_line["contraction"]["roofline_tensor"] = {
@@ -853,7 +855,12 @@ def main(argv=None):
                     help="skip the per-workload oracle timings (1 thread / all threads)")
     ap.add_argument("--only", choices=[w[0] for w in WORKLOADS], default=None,
                     help="time one workload only (short report; used to drive ncu captures)")
+    ap.add_argument("--bags", type=int, default=None,
+                    help="with --only: that many bags per table instead of the workload's "
+                         "(a smaller case of the same shapes and distributions, for captures)")
     args = ap.parse_args(argv)
+    if args.bags is not None and not args.only:
+        ap.error("--bags needs --only")
     if args.warmup < 3:
         args.warmup = 3
 
