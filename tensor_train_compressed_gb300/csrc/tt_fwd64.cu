@@ -35,7 +35,7 @@ namespace tt {
 
 struct MmaFwd64 {
   static constexpr int CW = 8, CP = kCP_8_64, R = 64, NC = 256, H = 2, D = 128;
-  static constexpr int ROWMAX = 48;                  // G3 rows staged per chunk
+  static constexpr int ROWMAX = 32;                  // G3 rows staged per chunk
   static constexpr int MAXROWS = CP * 32;            // rows of one chunk
   static constexpr int MAXPAIRS = MAXROWS / 2 + CP;
   // G2 half planes: rows r1 of 256 columns (j2 - 4h, r2) + 8 bf16 of padding;
@@ -52,7 +52,7 @@ struct MmaFwd64 {
   // different bank groups.
   static constexpr int PB = (R + 8) * 2, PA = 4 * PB + 96, PPB = 4 * PA + 16, P2PLANE = CP * PPB;
   static constexpr int STAGE_B = 2 * G2PLANE + 2 * G1PLANE;
-  static constexpr int G3_B = 2 * GTPLANE, P2_B = 2 * P2PLANE;
+  static constexpr int G3_B = 2 * GTPLANE, P2_B = 4 * P2PLANE;   // P2: both halves, hi and lo
   static constexpr int CKB = H * 2 * PPB;            // checkpoint slot: [half][plane][PPB]
   struct Meta {
     int x0, p0, np, npairs, end, ck, tab, pad;
@@ -63,9 +63,12 @@ struct MmaFwd64 {
     int g3i[ROWMAX];
   };
   static constexpr int THREADS = 32 * CW + 96;
-  static constexpr int BAR_B = 10 * 8;               // full, empty, go (2 each), go3, g3full
-  static constexpr int SMEM = 2 * STAGE_B + G3_B + P2_B + 2 * (int)sizeof(Meta) +
-                              (int)sizeof(G3Meta) + BAR_B + 16;
+  // full, empty, go (2 each), go3, g3full, g3empty
+  static constexpr int BAR_B = 9 * 8;
+  // two stage metas, two G3 row lists (by chunk parity), the consumers' own copy
+  // of the chunk's metadata, barriers, stage slots
+  static constexpr int SMEM = 2 * STAGE_B + G3_B + P2_B + 3 * (int)sizeof(Meta) +
+                              2 * (int)sizeof(G3Meta) + BAR_B + 8 + 16;
   static_assert(CW == 8 && NC / CW == 32, "eight consumer warps of 32 stage-2 columns");
   static_assert((PB / 16) % 8 == 1 && (PA / 16) % 8 == 2 && (PPB / 16) % 8 == 1, "P2 banks");
   static_assert((G2LD * 2 / 16) % 2 == 1 && (G1LD * 2 / 16) % 2 == 1 && (GTJ / 16) % 2 == 1,
@@ -128,12 +131,14 @@ __device__ __forceinline__ void mma_fwd64_stage2(uint32_t g2h, uint32_t g1h, cha
   }
 }
 
-// Stage 3 of one half, by pairs of rows: consumer warp w takes a contiguous
-// share of the pairs.  One m16n8k16 tile per k step: A[m][r2] with the 16
-// rows m = (j1, j2 - 4h), rows 0-7 holding j1 in {0, 2} and rows 8-15 j1 in
-// {1, 3} (m = 8 (j1 & 1) + 4 (j1 >> 1) + (j2 - 4h)); B[r2][(row of pair, j3)].
-__device__ __forceinline__ void mma_fwd64_stage3(const MmaFwd64::Meta& m, int half, uint32_t P2h,
-                                                 uint32_t G3h, const uint16_t* __restrict__ g3th,
+// Stage 3 of both halves, by pairs of rows: consumer warp w takes a contiguous
+// share of the pairs.  Per half h one m16n8k16 tile per k step: A[m][r2] with
+// the 16 rows m = (j1, j2 - 4h), rows 0-7 holding j1 in {0, 2} and rows 8-15 j1
+// in {1, 3} (m = 8 (j1 & 1) + 4 (j1 >> 1) + (j2 - 4h)), from the half's P2
+// planes (P2a + 2 h P2PLANE); B[r2][(row of pair, j3)], the same for both
+// halves, loaded once.
+__device__ __forceinline__ void mma_fwd64_stage3(const MmaFwd64::Meta& m, uint32_t P2a, uint32_t G3h,
+                                                 const uint16_t* __restrict__ g3th,
                                                  const uint16_t* __restrict__ g3tl,
                                                  const int32_t* __restrict__ row_i3,
                                                  float* __restrict__ rowbuf, int warp, int lane) {
@@ -145,62 +150,70 @@ __device__ __forceinline__ void mma_fwd64_stage3(const MmaFwd64::Meta& m, int ha
   // this lane's A row: j1 = 2 (lr / 4) + (li & 1), j2 - 4h = lr % 4; k half li / 2
   const uint32_t a_off = (2 * (lr >> 2) + (li & 1)) * C::PA + (lr & 3) * C::PB + 16 * (li >> 1);
   int cur_p = -1;
-  uint32_t ah[4][4], al[4][4];
+  uint32_t ah[2][4][4], al[2][4][4];
   for (int q = q0; q < q1; ++q) {
     const int e = m.pair[q];
     const int r0 = e & 255, has2 = (e >> 8) & 1, p = e >> 9;
     if (p != cur_p) {
       cur_p = p;
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint32_t aa = P2h + p * C::PPB + a_off + 32 * ks;
-        ldsm_x4(ah[ks], aa);
-        ldsm_x4(al[ks], aa + C::P2PLANE);
-      }
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t aa = P2a + hh * 2 * C::P2PLANE + p * C::PPB + a_off + 32 * ks;
+          ldsm_x4(ah[hh][ks], aa);
+          ldsm_x4(al[hh][ks], aa + C::P2PLANE);
+        }
     }
-    float big[4] = {0.f, 0.f, 0.f, 0.f}, small[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t bh[4][2], bl[4][2];
     if (r0 + 1 < C::ROWMAX) {
       // B rows n = (row of pair, j3) = lr, k columns r2 = 16 ks + 8 (li & 1)
       const int xr = (lr >> 2) == 0 ? r0 : (has2 ? r0 + 1 : C::ROWMAX);
       const uint32_t bb = G3h + xr * C::GTROW + (lr & 3) * C::GTJ + 16 * (li & 1);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        uint32_t bh[2], bl[2];
-        ldsm_x2(bh, bb + 32 * ks);
-        ldsm_x2(bl, bb + 32 * ks + C::GTPLANE);
-        mma_bf16(small, al[ks], bh[0], bh[1]);
-        mma_bf16(big, ah[ks], bh[0], bh[1]);
-        mma_bf16(small, ah[ks], bl[0], bl[1]);
+        ldsm_x2(bh[ks], bb + 32 * ks);
+        ldsm_x2(bl[ks], bb + 32 * ks + C::GTPLANE);
       }
     } else {
       // b0 = {B[2t][g], B[2t+1][g]}, b1 = same at k + 8; n = g: row g / 4, j3 = g % 4
       const int xr = r0 + (g >> 2);
       const bool live = (g >> 2) == 0 || has2;
       const size_t base = live ? ((size_t)__ldg(row_i3 + x0 + xr) * 4 + (g & 3)) * C::R : 0;
-      uint32_t bh0[4], bh1[4], bl0[4], bl1[4];
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const size_t k0 = base + 16 * ks + 2 * t;
-        bh0[ks] = live ? __ldg(reinterpret_cast<const uint32_t*>(g3th + k0)) : 0u;
-        bh1[ks] = live ? __ldg(reinterpret_cast<const uint32_t*>(g3th + k0 + 8)) : 0u;
-        bl0[ks] = live ? __ldg(reinterpret_cast<const uint32_t*>(g3tl + k0)) : 0u;
-        bl1[ks] = live ? __ldg(reinterpret_cast<const uint32_t*>(g3tl + k0 + 8)) : 0u;
-      }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(small, al[ks], bh0[ks], bh1[ks]);
-        mma_bf16(big, ah[ks], bh0[ks], bh1[ks]);
-        mma_bf16(small, ah[ks], bl0[ks], bl1[ks]);
+        bh[ks][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(g3th + k0)) : 0u;
+        bh[ks][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(g3th + k0 + 8)) : 0u;
+        bl[ks][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(g3tl + k0)) : 0u;
+        bl[ks][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(g3tl + k0 + 8)) : 0u;
       }
     }
+    float big[2][4], small[2][4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) big[hh][i] = small[hh][i] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        mma_bf16(small[hh], al[hh][ks], bh[ks][0], bh[ks][1]);
+        mma_bf16(big[hh], ah[hh][ks], bh[ks][0], bh[ks][1]);
+        mma_bf16(small[hh], ah[hh][ks], bl[ks][0], bl[ks][1]);
+      }
     // C[m][(row of pair, j3)]: rows m = g (j1 = 2 (g / 4)) and g + 8 (j1 + 1),
     // j2 - 4h = g % 4; this lane holds j3 = 2 (t % 2), +1 of pair row t / 2.
     // Output column j1 * 32 + j2 * 4 + j3.
     if (t < 2 || has2) {
-      float* o = rowbuf + (size_t)(x0 + r0 + (t >> 1)) * C::D + (g >> 2) * 64 + 16 * half +
-                 (g & 3) * 4 + 2 * (t & 1);
-      *reinterpret_cast<float2*>(o) = make_float2(small[0] + big[0], small[1] + big[1]);
-      *reinterpret_cast<float2*>(o + 32) = make_float2(small[2] + big[2], small[3] + big[3]);
+      float* o = rowbuf + (size_t)(x0 + r0 + (t >> 1)) * C::D + (g >> 2) * 64 + (g & 3) * 4 + 2 * (t & 1);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        *reinterpret_cast<float2*>(o + 16 * hh) =
+            make_float2(small[hh][0] + big[hh][0], small[hh][1] + big[hh][1]);
+        *reinterpret_cast<float2*>(o + 16 * hh + 32) =
+            make_float2(small[hh][2] + big[hh][2], small[hh][3] + big[hh][3]);
+      }
     }
   }
 }
@@ -212,15 +225,17 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
   extern __shared__ float4 sm4[];
   char* base = reinterpret_cast<char*>(sm4);
   char* G3a = base + 2 * C::STAGE_B;                 // the chunk's staged G3 rows
-  char* P2 = G3a + C::G3_B;
+  char* P2 = G3a + C::G3_B;                          // both halves' P2: half h at 2 h P2PLANE
   Meta* meta = reinterpret_cast<Meta*>(P2 + C::P2_B);
-  C::G3Meta* g3m = reinterpret_cast<C::G3Meta*>(meta + 2);
-  uint64_t* full = reinterpret_cast<uint64_t*>(g3m + 1);
+  Meta* cmeta = meta + 2;                            // the consumers' copy of the chunk's metadata
+  C::G3Meta* g3ms = reinterpret_cast<C::G3Meta*>(meta + 3);   // G3 row lists by chunk parity
+  uint64_t* full = reinterpret_cast<uint64_t*>(g3ms + 2);
   uint64_t* empty = full + 2;
   uint64_t* go = empty + 2;
   uint64_t* go3 = go + 2;
   uint64_t* g3full = go3 + 1;
-  volatile int* slot = reinterpret_cast<volatile int*>(g3full + 1);  // the stage's i2, -1: stop, -2 - k: slot k
+  uint64_t* g3empty = g3full + 1;                    // consumers done with the G3 area
+  volatile int* slot = reinterpret_cast<volatile int*>(g3empty + 1);  // the stage's i2, -1: stop, -2 - k: slot k
   __shared__ int cbase[kMaxTables + 1];
   __shared__ int nslots[kMaxTables];
   __shared__ long long ckoff[kMaxTables];          // checkpoint slots: byte offset into rowbuf
@@ -236,6 +251,7 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
     mbar_init(&go[1], 1);
     mbar_init(go3, 1);
     mbar_init(g3full, 32);
+    mbar_init(g3empty, 1);
     mbar_init_fence();
     int acc = 0;
     for (int t = 0; t < T; ++t) {
@@ -261,16 +277,17 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
   const int total = cbase[T];
 
   if (warp == C::CW + 2) {
-    // ---------------- G3 stager: per chunk, its first ROWMAX G3 rows (listed by
-    // the lead in g3m) into the G3 area, once the consumers have finished the
-    // previous chunk's second half; per row lane = plane | j3 | 16-byte piece
-    // (two pieces: q and q + 4)
+    // ---------------- G3 stager: per chunk i, its first ROWMAX G3 rows (listed by
+    // the lead in the row list of parity i % 2) into the G3 area, once the
+    // consumers have finished the previous chunk's stage 3 (g3empty); per row
+    // lane = plane | j3 | 16-byte piece (two pieces: q and q + 4)
     for (int i = 0;; ++i) {
       if (!mbar_wait(go3, (uint32_t)i & 1, ctl0)) break;
-      if (g3m->stop) break;
-      if (i > 0 && !mbar_wait(&empty[1], (uint32_t)(i - 1) & 1, ctl0)) break;
-      const int nst = g3m->nst;
-      const WS& w = tabs.w[g3m->tab];
+      const C::G3Meta& gm = g3ms[i & 1];
+      if (gm.stop) break;
+      if (i > 0 && !mbar_wait(g3empty, (uint32_t)(i - 1) & 1, ctl0)) break;
+      const int nst = gm.nst;
+      const WS& w = tabs.w[gm.tab];
       const int plane = lane >> 4, j3 = (lane >> 2) & 3, q = lane & 3;
       const uint16_t* src = plane ? w.g3tl : w.g3th;
       char* dst = G3a + plane * C::GTPLANE + j3 * C::GTJ + 16 * q;
@@ -278,9 +295,9 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           if (r0 + u < nst) {
-            const uint16_t* s = src + ((size_t)g3m->g3i[r0 + u] * 4 + j3) * C::R + 8 * q;
-            cp_async16(dst + (r0 + u) * C::GTROW, s);
-            cp_async16(dst + (r0 + u) * C::GTROW + 64, s + 32);
+            const uint16_t* sp = src + ((size_t)gm.g3i[r0 + u] * 4 + j3) * C::R + 8 * q;
+            cp_async16(dst + (r0 + u) * C::GTROW, sp);
+            cp_async16(dst + (r0 + u) * C::GTROW + 64, sp + 32);
           }
       }
       cp_async_arrive_noinc(g3full);
@@ -328,11 +345,12 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
     // ---------------- lead producer: per chunk, half 0 into buffer 0 and half
     // 1 into buffer 1.  The claim of the chunk after next and the metadata of
     // the next chunk are in flight while the current chunk is handed over.
-    auto stop_all = [&](int s) {
+    // stop the copier (at stage s) and the stager (at its chunk ci)
+    auto stop_all = [&](int s, int ci) {
       __syncwarp();
       if (lane == 0) {
         slot[s] = -1;
-        g3m->stop = 1;
+        g3ms[ci & 1].stop = 1;
         mbar_arrive(&go[s]);
         mbar_arrive(go3);
       }
@@ -380,13 +398,18 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         const WS& w = tabs.w[t];
         sl = d.p0 % ns;
         if (!d.whole) {
-          kind = 1;
-          if (lane == 0) v = ld_acquire_u32(w.ckpt + kCkptSlots + sl);
+          kind = 1;                 // the ready flag is read later (ready_check)
         } else if (d.cont) {
           kind = 2;
           if (lane == 0) v = atomicCAS(w.ckpt + sl, 0u, (uint32_t)d.p0 + 1u);
         }
       }
+    };
+    // a piece's slot is read as late as the lead can still hide the load: after
+    // the current chunk's second buffer is handed over, one chunk ahead of use
+    auto ready_check = [&](const ChunkDesc& d, int t, int kind, int sl, uint32_t& v) {
+      if (kind == 1 && lane == 0) v = ld_acquire_u32(tabs.w[t].ckpt + kCkptSlots + sl);
+      (void)d;
     };
     auto role_resolve = [&](const ChunkDesc& d, int kind, int sl, uint32_t v) {
       v = __shfl_sync(0xffffffffu, v, 0);
@@ -418,20 +441,19 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
     if (g < total) d = desc_of(g, t);
     if (gn < total) dn = desc_of(gn, tn);
     PMeta cur{};
-    int ck_cur = 0;
+    int kind_c = 0, sl_c = 0;       // the current chunk's checkpoint role, resolved
+    uint32_t v_c = 0;               // once its first buffer is free
     if (g < total) {
       load_meta(d, t, cur);
-      int kind, sl;
-      uint32_t v;
-      role_issue(d, t, kind, sl, v);
-      ck_cur = role_resolve(d, kind, sl, v);
+      role_issue(d, t, kind_c, sl_c, v_c);
+      ready_check(d, t, kind_c, sl_c, v_c);
     }
     for (int i = 0;; ++i) {
       const uint32_t par = (uint32_t)(i - 1) & 1;
       if (g >= total) {
         const bool ok = i == 0 || mbar_wait(&empty[0], par, ctl0);
         if (lane == 0) meta[0].end = 1;
-        stop_all(0);
+        stop_all(0, i);
         if (!ok) break;
         cp_async_arrive_noinc(&full[0]);
         if (lane == 0) mbar_arrive(&full[0]);
@@ -444,20 +466,20 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
       int kind_n = 0, sl_n = 0;
       uint32_t v_n = 0;
       if (gn < total) role_issue(dn, tn, kind_n, sl_n, v_n);
-      const int ck = ck_cur;
       // ---- half 0
       if (i > 0 && !mbar_wait(&empty[0], par, ctl0)) {
-        stop_all(0);
+        stop_all(0, i);
         break;
       }
+      const int ck = role_resolve(d, kind_c, sl_c, v_c);
       if (ck < 0 && lane == 0) atomicAdd(&tabs.w[cur.tab].ctl->ckpt_reused, 1);
       Meta& m = meta[0];
-      if (lane < cur.nst) g3m->g3i[lane] = cur.g30;
-      if (lane + 32 < cur.nst) g3m->g3i[lane + 32] = cur.g31;
+      C::G3Meta& gm = g3ms[i & 1];
+      if (lane < cur.nst) gm.g3i[lane] = cur.g30;
       if (lane == 0) {
-        g3m->nst = cur.nst;
-        g3m->tab = cur.tab;
-        g3m->stop = 0;
+        gm.nst = cur.nst;
+        gm.tab = cur.tab;
+        gm.stop = 0;
         m.tab = cur.tab;
         slot[0] = ck < 0 ? -1 + ck : cur.i2;
       }
@@ -505,11 +527,11 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
       }
       // ---- half 1: the same metadata into buffer 1
       if (i > 0 && !mbar_wait(&empty[1], par, ctl0)) {
-        stop_all(1);
+        stop_all(1, i + 1);
         break;
       }
+      if (gn < total) ready_check(dn, tn, kind_n, sl_n, v_n);
       Meta& m1 = meta[1];
-      for (int e = lane; e < npairs; e += 32) m1.pair[e] = m.pair[e];
       if (lane == 0) {
         m1.tab = cur.tab;
         slot[1] = ck < 0 ? -1 + ck : cur.i2;
@@ -529,7 +551,6 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         mbar_arrive(&full[1]);
       }
       // ---- the next chunk
-      const int ck_nxt = gn < total ? role_resolve(dn, kind_n, sl_n, v_n) : 0;
       const int gnn = __shfl_sync(0xffffffffu, (int)tk, 0);
       ChunkDesc dnn{};
       int tnn = 0;
@@ -538,7 +559,9 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
       d = dn;
       t = tn;
       cur = nxt;
-      ck_cur = ck_nxt;
+      kind_c = kind_n;
+      sl_c = sl_n;
+      v_c = v_n;
       gn = gnn;
       dn = dnn;
       tn = tnn;
@@ -547,10 +570,15 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
     return;
   }
 
-  // ---------------- consumers: warps 0 .. 7, two stages (halves) per chunk
+  // ---------------- consumers: warps 0 .. 7.  Per chunk: stage 2 of half 0
+  // (buffer 0) and of half 1 (buffer 1) into the two P2 areas, each buffer
+  // released as soon as its stage 2 is done; then stage 3 of both halves at once
+  // on the chunk's G3 rows, after which the G3 area is released (g3empty).  The
+  // chunk's metadata is copied out of buffer 0's before that buffer is released.
   for (int i = 0;; ++i) {
     const uint32_t par = (uint32_t)i & 1;
     bool done = false;
+    int ck = 0, tab = 0;
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
       if (!mbar_wait(&full[h], par, ctl0)) {
@@ -562,38 +590,53 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         done = true;
         break;
       }
-      const WS& w = tabs.w[m.tab];
+      ck = m.ck;
+      tab = m.tab;
+      if (h == 0) {
+        for (int e = tid; e < m.npairs; e += 32 * C::CW) cmeta->pair[e] = m.pair[e];
+        if (tid == 0) {
+          cmeta->x0 = m.x0;
+          cmeta->p0 = m.p0;
+          cmeta->npairs = m.npairs;
+        }
+      }
+      const WS& w = tabs.w[tab];
       char* stage = base + h * C::STAGE_B;
-      const int ck = m.ck;
-      char* ck_data = reinterpret_cast<char*>(w.rowbuf) + ckoff[m.tab];
-      uint32_t p2a = smem_addr(P2);
+      char* P2h = P2 + h * 2 * C::P2PLANE;
+      char* ck_data = reinterpret_cast<char*>(w.rowbuf) + ckoff[tab];
       if (ck >= 0) {
-        mma_fwd64_stage2(smem_addr(stage), smem_addr(stage + 2 * C::G2PLANE), P2, warp, lane);
+        mma_fwd64_stage2(smem_addr(stage), smem_addr(stage + 2 * C::G2PLANE), P2h, warp, lane);
         named_sync(1, 32 * C::CW);
         if (ck > 0) {               // checkpoint: half h of the prefix's P2 planes
           char* dst = ck_data + (size_t)(ck - 1) * C::CKB + h * 2 * C::PPB;
           for (int e = tid; e < 2 * C::PPB / 16; e += 32 * C::CW) {
             const int plane = e / (C::PPB / 16), q = e - plane * (C::PPB / 16);
             *reinterpret_cast<uint4*>(dst + plane * C::PPB + 16 * q) =
-                *reinterpret_cast<const uint4*>(P2 + plane * C::P2PLANE + 16 * q);
+                *reinterpret_cast<const uint4*>(P2h + plane * C::P2PLANE + 16 * q);
           }
         }
       } else {
-        p2a = smem_addr(stage);     // P2 from the checkpoint, staged in the G2 area
-      }
-      if (h == 0 && !mbar_wait(g3full, par, ctl0)) {
-        done = true;
-        break;
-      }
-      mma_fwd64_stage3(m, h, p2a, smem_addr(G3a), w.g3th, w.g3tl, w.row_i3, w.rowbuf, warp, lane);
-      named_sync(1, 32 * C::CW);
-      if (h == 1 && ck > 0 && tid == 0) {   // both halves written: publish the slot
-        __threadfence();
-        st_release_u32(w.ckpt + kCkptSlots + ck - 1, (uint32_t)m.p0 + 1u);
+        // P2 of half h from the checkpoint, staged in the buffer's G2 area: into
+        // the half's P2 area (prefix 0), so that the buffer can be released
+        for (int e = tid; e < 2 * C::PPB / 16; e += 32 * C::CW) {
+          const int plane = e / (C::PPB / 16), q = e - plane * (C::PPB / 16);
+          *reinterpret_cast<uint4*>(P2h + plane * C::P2PLANE + 16 * q) =
+              *reinterpret_cast<const uint4*>(stage + plane * C::P2PLANE + 16 * q);
+        }
+        named_sync(1, 32 * C::CW);
       }
       if (tid == 0) mbar_arrive(&empty[h]);
     }
     if (done) break;
+    if (!mbar_wait(g3full, par, ctl0)) break;
+    const WS& w = tabs.w[tab];
+    mma_fwd64_stage3(*cmeta, smem_addr(P2), smem_addr(G3a), w.g3th, w.g3tl, w.row_i3, w.rowbuf, warp, lane);
+    named_sync(1, 32 * C::CW);
+    if (ck > 0 && tid == 0) {       // both halves written: publish the slot.  Done
+      __threadfence();              // here, not right after the writes, so that the
+      st_release_u32(w.ckpt + kCkptSlots + ck - 1, (uint32_t)cmeta->p0 + 1u);  // fence
+    }                               // finds them landed instead of waiting for them
+    if (tid == 0) mbar_arrive(g3empty);
   }
 }
 

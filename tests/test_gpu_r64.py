@@ -69,9 +69,11 @@ def test_chunks_with_more_rows_than_are_staged():
 
 
 def test_hot_prefixes_reuse_checkpointed_partials():
-    # 6 prefixes of about 2,600 rows each: 32-row pieces, later pieces reuse the
-    # first piece's P2 from its L2 slot (the buffer has spare rows for slots)
-    x = make_custom((3, 2, 5000), N, R, num_bags=3000, max_len=14, seed=22)
+    # 6 prefixes of about 15,000 rows each: 32-row pieces, later pieces reuse the
+    # first piece's P2 from its L2 slot (the buffer has spare rows for slots).  A
+    # piece reuses the slot only if its owner has published it by the time the
+    # piece is staged, so the batch gives each CTA many pieces to work
+    x = make_custom((3, 2, 5000), N, R, num_bags=12000, max_len=14, seed=22)
     ws = _ws(x)
     out = _forward(x, ws)
     g = tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, ws)
