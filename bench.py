@@ -366,7 +366,15 @@ WORKLOADS = (("train", TRAIN_CFG, True, None), ("forward", FWD_CFG, False, None)
 
 def counts_of(g, x) -> dict:
     """Unique prefixes / rows / chunks of one grouping, and the algorithmic work of the batch."""
-    a = algorithmic(x, g["U_12"], g["U_r"])
+    U_12, U_r = g["U_12"], g["U_r"]
+    if g["method"] == "direct":
+        # a per-lookup forward makes no grouping: the batch's unique rows and
+        # (i1, i2) prefixes (row // m3) are counted here
+        M = int(np.prod(x.m))
+        idx = x.indices[(x.indices >= 0) & (x.indices < M)]
+        U_r = int(np.unique(idx).size)
+        U_12 = int(np.unique(idx // x.m[2]).size)
+    a = algorithmic(x, U_12, U_r)
     a.update(n_chunks=g["n_chunks"], method=g["method"], n_valid=g["n_valid"],
              ckpt_reused=g["ckpt_reused"])
     return a
@@ -391,6 +399,10 @@ def kernel_work(name: str, a: dict, x, train: bool):
         return "flop", a["fwd_contract"]
     if name in ("k_bwd_mma", "k_bwd_generic"):
         return "flop", a["bwd_contract"]
+    if name == "k_fwd_direct":                             # every lookup's chain on its own
+        n1, n2, _ = x.n
+        R1, R2 = x.R[1], x.R[2]
+        return "flop", 2 * nnz * (n1 * n2 * R2 * R1 + D * R2)
     if name.startswith("k_group"):
         lists = 8 * nnz + 4 * U_r if train else 0          # perm + row_start
         return "bytes", (8 * nnz + 8 * (B + 1) + 4 * nnz + lists + 8 * U_r + 12 * U_12
@@ -636,8 +648,9 @@ def run_ours(args, rank, world, dist):
     for nm, cfg in (("config1", 1), ("config2", 2)):
         r = result[nm]
         ln = forward_line(r, CONFIG_NAMES[cfg] + ", forward only", nm)
-        ln["dtype"] = "f32 (FP32 FFMA chunk kernel)" if cfg == 1 else \
-            "f32 (FP32 FFMA tiled chunk kernel; no tensor-core split at R=16)"
+        ln["dtype"] = ("f32 (FP32 FFMA, one warp per bag forming each lookup's row on its own: "
+                       "a forward-only batch this small is not grouped)"
+                       if r["alg"].get("method") == "direct" else "f32 (FP32 FFMA chunk kernel)")
         small[nm] = ln
     sens = {}
     for nm, base in (("forward_permuted", fw), ("train_permuted", tr)):

@@ -150,9 +150,13 @@ int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int fla
 #define TT_EMB_FORWARD_ONLY 2 /* no backward will reuse this call's grouping (inference):
                                 the grouping may leave out the per-row lookup lists
                                 that only the backward reads (perm and row_start of
-                                tt_emb_grouping_view).  A tt_emb_backward with
-                                reuse_grouping != 0 on such a grouping adds nothing
-                                and tt_emb_get_error returns TT_EMB_ERR_REUSE */
+                                tt_emb_grouping_view), and a small batch (D <= 256 and
+                                nnz * (n1*n2*R2*R1 + D*R2) <= 2^27 multiply-adds) is
+                                not grouped at all: each lookup's row is formed on its
+                                own (TT-Rec's per-lookup chain) in one launch, and the
+                                workspace then holds no grouping.  A tt_emb_backward
+                                with reuse_grouping != 0 after such a call adds
+                                nothing and tt_emb_get_error returns TT_EMB_ERR_REUSE */
 
 /* Forward with the other pooling rules of an embedding bag (the TT-Rec
  * abstract names its operator after the EmbeddingBag; the pages themselves

@@ -45,7 +45,7 @@ def read_grouping(m, n, R, nnz: int, num_bags: int, workspace: torch.Tensor) -> 
     counts = arr("counts", 7)
     nv, ur, up, nc = (int(v) for v in counts[:4])
     D = int(n[0] * n[1] * n[2])
-    method = {1: "bitmap", 2: "coop_sort", 3: "multi_sort"}.get(int(counts[5]), "none")
+    method = {1: "bitmap", 2: "coop_sort", 3: "multi_sort", 4: "direct"}.get(int(counts[5]), "none")
     return dict(n_valid=nv, U_r=ur, U_12=up, n_chunks=nc, status=int(counts[4]), method=method,
                 ckpt_reused=int(counts[6]),
                 perm=arr("perm", nnz), row_start=arr("row_start", ur + 1),

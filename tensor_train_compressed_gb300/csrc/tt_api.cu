@@ -314,6 +314,15 @@ int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int
   if (num_bags > 0 && (!out || !aligned(out, 16))) return TT_EMB_ERR_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   const WS w = make_ws(workspace, L);
+  if ((flags & TT_EMB_FORWARD_ONLY) && direct_eligible(s, nnz)) {
+    // a small batch: each lookup's row formed on its own, no grouping
+    if (!(flags & TT_EMB_CORES_SPLIT)) {
+      // the split a forward leaves for later TT_EMB_CORES_SPLIT calls
+      rc = launch_split(s, w, cores, 0, st);
+      if (rc) return rc;
+    }
+    return launch_forward_direct(s, w, cores, indices, nnz, offsets, num_bags, pool, out, st);
+  }
   int CP, CR;
   rc = forward_chunk_params(s, &CP, &CR);
   if (rc) return rc;

@@ -33,10 +33,11 @@ __global__ void __launch_bounds__(256) k_s_zero(WS w, int D, int span, int64_t r
                                                 SplitArgs sp, int reuse) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (reuse && w.ctl->method == kGroupBitmap) {
+  if (reuse && (w.ctl->method == kGroupBitmap || w.ctl->method == kGroupDirect)) {
     // the grouping came from a forward-only call and has no per-row lookup
-    // lists: report it, and leave the backward's later kernels no lookups and
-    // no chunks, so that the core gradients stay as they are
+    // lists (or there is none: a per-lookup forward): report it, and leave the
+    // backward's later kernels no lookups and no chunks, so that the core
+    // gradients stay as they are
     if (gtid == 0) {
       set_status(w.ctl, kStNoLists);
       w.ctl->n_valid = 0;

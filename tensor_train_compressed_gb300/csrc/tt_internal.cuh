@@ -47,6 +47,16 @@ constexpr int32_t kGroupBitmap = 1;   // key bitmap, one cooperative launch, no 
                                       // lookup lists (perm, row_start): forward-only calls
 constexpr int32_t kGroupCoop = 2;     // radix sort, one cooperative launch
 constexpr int32_t kGroupMulti = 3;    // radix sort, one launch per phase
+constexpr int32_t kGroupDirect = 4;   // no grouping: a small forward-only batch whose rows
+                                      // were formed per lookup (k_fwd_direct)
+
+// A forward-only call takes the per-lookup kernel when the batch's arithmetic
+// in that form (nnz * direct_macs_per_lookup) is at most this, D <= kDirectMaxD
+// and one warp's shared memory (two lookups' core slices and the partial) fits
+// kDirectMaxSmem.
+constexpr int64_t kDirectMaxMacs = 1ll << 27;
+constexpr int kDirectMaxD = 256;
+constexpr int kDirectMaxSmem = 200 * 1024;
 
 // The control block at the start of the workspace (256 bytes).
 struct Ctl {
@@ -408,6 +418,11 @@ int launch_backward(const Shape& s, const Layout& L, const WS& w, const float* g
                     int64_t num_bags, const Pooling& pool, float* const core_grads[3],
                     float* grad_weights, cudaStream_t st);
 int launch_split(const Shape& s, const WS& w, const float* const cores[3], int reuse, cudaStream_t st);
+int64_t direct_macs_per_lookup(const Shape& s);
+bool direct_eligible(const Shape& s, int64_t nnz);
+int launch_forward_direct(const Shape& s, const WS& w, const float* const cores[3],
+                          const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                          int64_t num_bags, const Pooling& pool, float* out, cudaStream_t st);
 // Called by one thread of a kernel that runs after k_split_cores in the same
 // stream: the split planes now hold the cores at g1, g2, g3.
 __device__ __forceinline__ void mark_split(Ctl* ctl, const float* g1, const float* g2, const float* g3) {
