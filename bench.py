@@ -55,8 +55,8 @@ def peaks():
     return p
 
 
-# Kernels whose fp32-accurate contractions run as three-term split products on
-# the tensor cores (three tensor products per fp32-accurate product).
+# Kernels whose contractions run as three-term bf16 split products on the
+# tensor cores (three tensor products per fp32-level product).
 TENSOR_SPLIT_KERNELS = ("k_fwd_mma", "k_fwd_mma64", "k_bwd_mma")
 
 
