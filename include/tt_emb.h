@@ -257,11 +257,11 @@ typedef struct {
  * training step the output gradient is copied in, tt_emb_backward reuses the
  * forward's grouping and tt_emb_sgd_ex(lr, zero_grads = 1) updates the cores
  * (so the next step may pass TT_EMB_CORES_SPLIT); h_out receives the pooled
- * output.  The copies run on `copy_stream`, the kernels on `stream`, ordered
- * by events: the copies start after the work enqueued on `stream` before the
- * call, the forward waits only for indices and offsets (the output gradient
- * arrives while it runs), and the output is copied back while the backward
- * runs.  Everything the call does is complete when `stream` reaches the end
+ * output.  Indices and offsets are copied in on `stream`, after the work
+ * enqueued on it before the call, and the forward follows them there; the
+ * output gradient is copied in on `copy_stream` once they are in, while the
+ * forward runs, and the output is copied back on `copy_stream` while the
+ * backward runs, all ordered by events.  Everything the call does is complete when `stream` reaches the end
  * of what it enqueued, h_out included.  copy_stream may equal stream (no
  * overlap).  `flags` as for tt_emb_forward_ex; TT_EMB_FORWARD_ONLY only for a
  * forward (TT_EMB_ERR_ARG with h_grad_out).  core_grads may be NULL for a forward; otherwise they are

@@ -13,7 +13,7 @@
 
 namespace {
 
-enum { kEvStart, kEvIn, kEvGrad, kEvFwd, kEvDone, kNumEv };
+enum { kEvIn, kEvGrad, kEvFwd, kEvDone, kNumEv };
 
 // Events of this thread on the current device, created once and reused: a
 // wait enqueued on a stream refers to the record that preceded it, so a later
@@ -94,23 +94,21 @@ extern "C" int tt_emb_step_host(float* const cores[3], float* const core_grads[3
     return (ok && e1 == cudaSuccess && e2 == cudaSuccess) ? TT_EMB_OK : TT_EMB_ERR_CUDA;
   };
 
-  // the copies in start after the work the caller ordered before this call
-  cuda(cudaEventRecord(ev[kEvStart], st));
-  cuda(cudaStreamWaitEvent(cs, ev[kEvStart], 0));
-  if (!ok) return TT_EMB_ERR_CUDA;            // nothing enqueued on the copy stream yet
+  // The lookups come in on `stream` itself, after the work the caller ordered
+  // before this call, so the forward follows them with no wait across
+  // streams; the output gradient comes in on the copy stream once they are in
+  // (not competing with them for the copy bandwidth) while the forward runs.
   if (b.nnz > 0)
     cuda(cudaMemcpyAsync(b.d_indices, b.h_indices, sizeof(int64_t) * (size_t)b.nnz,
-                         cudaMemcpyHostToDevice, cs));
+                         cudaMemcpyHostToDevice, st));
   cuda(cudaMemcpyAsync(b.d_offsets, b.h_offsets, sizeof(int64_t) * (size_t)(b.num_bags + 1),
-                       cudaMemcpyHostToDevice, cs));
-  cuda(cudaEventRecord(ev[kEvIn], cs));
+                       cudaMemcpyHostToDevice, st));
+  cuda(cudaEventRecord(ev[kEvIn], st));
+  cuda(cudaStreamWaitEvent(cs, ev[kEvIn], 0));
+  if (!ok) return TT_EMB_ERR_CUDA;            // nothing enqueued on the copy stream yet
   if (train && out_bytes > 0)
     cuda(cudaMemcpyAsync(b.d_grad_out, b.h_grad_out, out_bytes, cudaMemcpyHostToDevice, cs));
   cuda(cudaEventRecord(ev[kEvGrad], cs));
-  if (!ok) return finish(TT_EMB_ERR_CUDA);
-
-  // forward as soon as the lookups are in (the output gradient still copying)
-  cuda(cudaStreamWaitEvent(st, ev[kEvIn], 0));
   if (!ok) return finish(TT_EMB_ERR_CUDA);
   const float* const* cc = (const float* const*)cores;
   rc = tt_emb_forward_ex(cc, m, n, R, b.d_indices, b.nnz, b.d_offsets, b.num_bags, nullptr,
