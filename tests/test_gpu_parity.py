@@ -7,6 +7,8 @@ fp32 rounding of the cores.  Full-size configurations are checked on sampled
 bags (forward) and on sampled core slices (backward), computed one by one by
 the oracle.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -163,6 +165,37 @@ def test_forward_full_size_sampled(cfg, table):
         pieces = sum(1 for c in range(g["n_chunks"])
                      if g["pair_row_start"][g["row_pair"][cs[c]]] != cs[c])
         assert 0 < g["ckpt_reused"] <= pieces, (g["ckpt_reused"], pieces)
+
+
+def _oracle_threads():
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+@pytest.mark.parametrize("cfg,table,mapping", [(3, 0, None), (5, 0, None), (4, 7, None),
+                                               (3, 0, "permuted")])
+def test_forward_full_size_every_output(cfg, table, mapping):
+    """The whole batch at full size (32,768 bags; config 4: its largest table, 4e7 rows;
+    the 12M-row batch also with its Zipf ranks mapped through a random row permutation)
+    in the launch configuration the bench times: every pooled output element against
+    the oracle, scaled by the oracle's largest value."""
+    x = make_inputs(cfg, table=table, mapping=mapping)
+    out, rc, _, _ = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=_oracle_threads())
+    assert np.abs(out - ref).max() <= FWD_TOL * np.abs(ref).max()
+
+
+def test_backward_full_size_every_gradient():
+    """The 48M-row training batch at full size: every element of the three core
+    gradients against the oracle's, each scaled by the oracle's largest value."""
+    x = make_inputs(5, with_grad=True)
+    _, rc, _, st = _gpu_forward(x)
+    assert rc == tte.TT_EMB_OK
+    dG = _gpu_backward(x, st)
+    dref = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets,
+                           threads=_oracle_threads())
+    for k in range(3):
+        assert np.abs(dG[k] - dref[k]).max() <= BWD_TOL * np.abs(dref[k]).max(), k
 
 
 def _sms():
