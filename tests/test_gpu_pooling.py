@@ -7,6 +7,8 @@ Bars as for the sum: outputs within 1e-4 * max|ref|, core gradients within
 gradient with a row per lookup) within 1e-4 * max|ref|.  Unit weights and
 one-lookup bags must leave the sum bit for bit.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -63,13 +65,13 @@ class _Run:
         self.dW = None if dw is None else dw.cpu().numpy()
 
 
-def _check_against_oracle(x, weights, mode, run, strict=True):
-    ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8,
+def _check_against_oracle(x, weights, mode, run, strict=True, threads=8):
+    ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=threads,
                          weights=weights, mode=mode, strict=strict)
     assert _rel_err(run.out, ref) <= FWD_TOL
-    res = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8,
-                          weights=weights, mode=mode, want_dw=weights is not None,
-                          strict=strict)
+    res = oracle.backward(x.grad_out, x.cores, x.m, x.n, x.R, x.indices, x.offsets,
+                          threads=threads, weights=weights, mode=mode,
+                          want_dw=weights is not None, strict=strict)
     dref, dwref = res if weights is not None else (res, None)
     for k in range(3):
         assert _rel_err(run.dG[k], dref[k]) <= BWD_TOL, k
@@ -131,6 +133,19 @@ def test_weighted_full_size_sampled():
                                threads=8, weights=w, filter_core=core,
                                filter_value=v)[core - 1][v]
         assert _rel_err(run.dG[core - 1][v], dref) <= BWD_TOL, (core, v)
+
+
+@pytest.mark.parametrize("mode", ["mean", "weighted"])
+def test_pooling_variants_full_size_every_element(mode):
+    """The full training table and batch (655,893 lookups): every pooled output, every
+    core-gradient element and (weighted) every weight-gradient element against the
+    oracle, threaded over the host's cores."""
+    x = make_inputs(5)
+    w = make_sample_weights(x.nnz, 9) if mode == "weighted" else None
+    m = "sum" if mode == "weighted" else "mean"
+    run = _Run(x, w, m)
+    assert run.rc_fwd == tte.TT_EMB_OK and run.rc_bwd == tte.TT_EMB_OK
+    _check_against_oracle(x, w, m, run, threads=max(1, min(16, os.cpu_count() or 1)))
 
 
 def test_unit_weights_and_single_lookup_bags_leave_the_sum_bitwise():
