@@ -9,8 +9,10 @@
 // cooperative launch with grid barriers, the chunk kernel, the pooling) is
 // most of the call.  Below a fixed amount of arithmetic (kDirectMaxMacs) a
 // forward-only call therefore takes this one kernel instead: one warp per bag,
-// its lookups one after another, each row's n1*n2 x R2 partial in shared
-// memory, the bag's sum in registers, one coalesced store per bag.
+// its lookups one after another, each lookup's three core slices copied into
+// the warp's shared memory with cp.async (the next lookup's while the current
+// one is worked), its n1*n2 x R2 partial formed there, the bag's sum in
+// registers, one coalesced store per bag.
 //
 // The workspace records that no grouping was made (Ctl::method = kGroupDirect),
 // so a backward that asks to reuse it reports TT_EMB_ERR_REUSE, as after the
