@@ -264,7 +264,10 @@ struct MmaFwd {
     int g3i[ROWMAX];      // i3 of the staged rows (read by the G3 stager)
   };
   static constexpr int NCW = NC / CW;                // stage-2 columns per consumer warp
-  static constexpr int THREADS = 32 * CW + 96;       // consumers, lead producer, G2 copier, G3 stager
+  // consumers, lead producer, NCOPY G2 copiers and NSTAGE G3 stagers sharing
+  // a stage's copies row by row (one warp issuing all of them paces the pipeline)
+  static constexpr int NCOPY = 2, NSTAGE = 2;
+  static constexpr int THREADS = 32 * (CW + 1 + NCOPY + NSTAGE);
   static constexpr int SMEM = 4 * (2 * STAGE_F + F_P2) + 2 * (int)sizeof(Meta) + 8 * 8 + 16;
   static_assert(CW == 8 || CW == 16, "8 or 16 consumer warps");
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -420,10 +423,10 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
   volatile int* slot = reinterpret_cast<volatile int*>(go3 + 2);  // the stage's i2, or -1: stop
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    // full: the copy arrivals of the three producer warps' 96 lanes + the lead's
-    // metadata arrival
-    mbar_init(&full[0], 97);
-    mbar_init(&full[1], 97);
+    // full: the copy arrivals of the producer warps' lanes + the lead's metadata
+    // arrival
+    mbar_init(&full[0], 32 * (1 + C::NCOPY + C::NSTAGE) + 1);
+    mbar_init(&full[1], 32 * (1 + C::NCOPY + C::NSTAGE) + 1);
     mbar_init(&empty[0], 1);
     mbar_init(&empty[1], 1);
     mbar_init(&go[0], 1);
@@ -458,10 +461,12 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
   uint32_t* ck_owner = a.w.ckpt;
   uint32_t* ck_ready = a.w.ckpt + kCkptSlots;
 
-  if (warp == CW + 2) {
-    // ---------------- G3 stager: stages the chunk's first ROWMAX G3 rows (the
+  if (warp >= CW + 1 + C::NCOPY) {
+    // ---------------- G3 stagers: stage the chunk's first ROWMAX G3 rows (the
     // transposed split planes; the lead producer lists their i3 in the stage's
-    // metadata), per row lane = plane | j3 | 16-byte piece
+    // metadata), stager h the rows h, h + NSTAGE, ..., per row lane = plane |
+    // j3 | 16-byte piece
+    const int h = warp - (CW + 1 + C::NCOPY);
     for (int it = 0;; ++it) {
       const int s = it & 1;
       if (!mbar_wait(&go3[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
@@ -472,9 +477,9 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
         char* G3s = reinterpret_cast<char*>(base + s * C::STAGE_F + C::F_G2 + C::F_P1);
         const int plane = lane >> 4, j3 = (lane >> 2) & 3, q = lane & 3;
         const uint16_t* src = plane ? a.w.g3tl : a.w.g3th;
-        for (int r0 = 0; r0 < nst; r0 += 8) {
+        for (int r0 = h; r0 < nst; r0 += 8 * C::NSTAGE) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
+          for (int u = 0; u < 8 * C::NSTAGE; u += C::NSTAGE)
             if (r0 + u < nst)
               cp_async16(G3s + plane * C::GTPLANE + (r0 + u) * C::GTROW + j3 * 80 + 16 * q,
                          src + ((size_t)mg.g3i[r0 + u] * 4 + j3) * C::R + 8 * q);
@@ -487,29 +492,30 @@ __global__ void __launch_bounds__(MmaFwd<CW>::THREADS, 1) k_fwd_mma(FwdArgs a) {
     return;
   }
 
-  if (warp == CW + 1) {
-    // ---------------- G2 copier: stages the G2 planes of the chunks the lead
-    // producer hands over, one stage at a time
+  if (warp >= CW + 1) {
+    // ---------------- G2 copiers: stage the G2 planes of the chunks the lead
+    // producer hands over, one stage at a time; the 64 rows of the two planes
+    // (hi, lo) are dealt to the copiers, copier h taking rows h, h + NCOPY, ...
+    const int h = warp - (CW + 1);
     for (int it = 0;; ++it) {
       const int s = it & 1;
       if (!mbar_wait(&go[s], ((uint32_t)it >> 1) & 1, a.w.ctl)) break;
       const int i2 = slot[s];        // the G2 slice, -1: stop, -2 - k: checkpoint slot k
       if (i2 >= 0) {
-        const uint16_t* h2 = a.w.g2h + (size_t)i2 * C::R * C::NC;
-        const uint16_t* l2 = a.w.g2l + (size_t)i2 * C::R * C::NC;
+        const size_t at = (size_t)i2 * C::R * C::NC;
         char* dst = reinterpret_cast<char*>(base + s * C::STAGE_F);
 #pragma unroll 8
-        for (int i = 0; i < 2 * C::R * C::NC / 256; ++i) {
-          const int e = i * 32 + lane, plane = e >> 10, row = (e >> 5) & 31, q = e & 31;
-          cp_async16(dst + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * q,
-                     (plane ? l2 : h2) + row * C::NC + 8 * q);
+        for (int pr = h; pr < 2 * C::R; pr += C::NCOPY) {   // lane: 16-byte piece of a 512-byte row
+          const int plane = pr / C::R, row = pr - plane * C::R;
+          cp_async16(dst + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * lane,
+                     (plane ? a.w.g2l : a.w.g2h) + at + row * C::NC + 8 * lane);
         }
       } else if (i2 <= -2) {
         // a checkpointed P2 into the stage's G2 area, in the P2 layout (planes
         // P2PLANE apart), where the consumers' stage 3 reads it
         const char* src = ck_data + (size_t)(-2 - i2) * C::CKB;
         char* dst = reinterpret_cast<char*>(base + s * C::STAGE_F);
-        for (int e = lane; e < C::CKB / 16; e += 32) {
+        for (int e = lane + 32 * h; e < C::CKB / 16; e += 32 * C::NCOPY) {
           const int plane = e / (C::PPB / 16), q = e - plane * (C::PPB / 16);
           cp_async16(dst + plane * C::P2PLANE + 16 * q, src + plane * C::PPB + 16 * q);
         }

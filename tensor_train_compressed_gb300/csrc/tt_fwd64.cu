@@ -62,7 +62,10 @@ struct MmaFwd64 {
     int nst, tab, stop, pad;
     int g3i[ROWMAX];
   };
-  static constexpr int THREADS = 32 * CW + 96;
+  // consumers, lead producer, NCOPY G2 copiers and NSTAGE G3 stagers sharing
+  // the copies row by row (one warp issuing all of them paces the pipeline)
+  static constexpr int NCOPY = 3, NSTAGE = 1;
+  static constexpr int THREADS = 32 * (CW + 1 + NCOPY + NSTAGE);
   // full, empty, go (2 each), go3, g3full, g3empty
   static constexpr int BAR_B = 9 * 8;
   // two stage metas, two G3 row lists (by chunk parity), the consumers' own copy
@@ -243,14 +246,15 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
   const int T = tabs.T;
   Ctl* ctl0 = tabs.w[0].ctl;
   if (tid == 0) {
-    mbar_init(&full[0], 65);      // copier lanes + lead lanes (noinc) + the lead's metadata arrival
-    mbar_init(&full[1], 65);
+    // copiers' and lead's lanes (noinc) + the lead's metadata arrival
+    mbar_init(&full[0], 32 * (C::NCOPY + 1) + 1);
+    mbar_init(&full[1], 32 * (C::NCOPY + 1) + 1);
     mbar_init(&empty[0], 1);
     mbar_init(&empty[1], 1);
     mbar_init(&go[0], 1);
     mbar_init(&go[1], 1);
     mbar_init(go3, 1);
-    mbar_init(g3full, 32);
+    mbar_init(g3full, 32 * C::NSTAGE);
     mbar_init(g3empty, 1);
     mbar_init_fence();
     int acc = 0;
@@ -276,11 +280,13 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
   __syncthreads();
   const int total = cbase[T];
 
-  if (warp == C::CW + 2) {
-    // ---------------- G3 stager: per chunk i, its first ROWMAX G3 rows (listed by
+  if (warp >= C::CW + 1 + C::NCOPY) {
+    // ---------------- G3 stagers: per chunk i, its first ROWMAX G3 rows (listed by
     // the lead in the row list of parity i % 2) into the G3 area, once the
-    // consumers have finished the previous chunk's stage 3 (g3empty); per row
-    // lane = plane | j3 | 16-byte piece (two pieces: q and q + 4)
+    // consumers have finished the previous chunk's stage 3 (g3empty); stager h
+    // the rows h, h + NSTAGE, ..., per row lane = plane | j3 | 16-byte piece
+    // (two pieces: q and q + 4)
+    const int h = warp - (C::CW + 1 + C::NCOPY);
     for (int i = 0;; ++i) {
       if (!mbar_wait(go3, (uint32_t)i & 1, ctl0)) break;
       const C::G3Meta& gm = g3ms[i & 1];
@@ -291,9 +297,9 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
       const int plane = lane >> 4, j3 = (lane >> 2) & 3, q = lane & 3;
       const uint16_t* src = plane ? w.g3tl : w.g3th;
       char* dst = G3a + plane * C::GTPLANE + j3 * C::GTJ + 16 * q;
-      for (int r0 = 0; r0 < nst; r0 += 8) {
+      for (int r0 = h; r0 < nst; r0 += 8 * C::NSTAGE) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < 8 * C::NSTAGE; u += C::NSTAGE)
           if (r0 + u < nst) {
             const uint16_t* sp = src + ((size_t)gm.g3i[r0 + u] * 4 + j3) * C::R + 8 * q;
             cp_async16(dst + (r0 + u) * C::GTROW, sp);
@@ -306,8 +312,11 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
     return;
   }
 
-  if (warp == C::CW + 1) {
-    // ---------------- G2 copier: stage k holds half k % 2 of a chunk
+  if (warp >= C::CW + 1) {
+    // ---------------- G2 copiers: stage k holds half k % 2 of a chunk; the
+    // 128 rows of its two planes are dealt to the copiers, copier h taking rows
+    // h, h + NCOPY, ...
+    const int h = warp - (C::CW + 1);
     for (int k = 0;; ++k) {
       const int s = k & 1;
       if (!mbar_wait(&go[s], ((uint32_t)k >> 1) & 1, ctl0)) break;
@@ -319,7 +328,7 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         const uint16_t* h2 = w.g2h + (size_t)v * C::R * (2 * C::NC) + C::NC * s;
         const uint16_t* l2 = w.g2l + (size_t)v * C::R * (2 * C::NC) + C::NC * s;
 #pragma unroll 8
-        for (int i = 0; i < 2 * C::R * C::NC / 256; ++i) {
+        for (int i = h; i < 2 * C::R * C::NC / 256; i += C::NCOPY) {
           const int e = i * 32 + lane, plane = e >> 11, row = (e >> 5) & 63, q = e & 31;
           cp_async16(dst + plane * C::G2PLANE + row * (2 * C::G2LD) + 16 * q,
                      (plane ? l2 : h2) + row * (2 * C::NC) + 8 * q);
@@ -329,7 +338,7 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         const WS& w = tabs.w[meta[s].tab];
         const char* src = reinterpret_cast<const char*>(w.rowbuf) + ckoff[meta[s].tab] +
                           (size_t)(-2 - v) * C::CKB + s * 2 * C::PPB;
-        for (int e = lane; e < 2 * C::PPB / 16; e += 32) {
+        for (int e = lane + 32 * h; e < 2 * C::PPB / 16; e += 32 * C::NCOPY) {
           const int plane = e / (C::PPB / 16), q = e - plane * (C::PPB / 16);
           cp_async16(dst + plane * C::P2PLANE + 16 * q, src + plane * C::PPB + 16 * q);
         }
