@@ -58,12 +58,12 @@ def _rel_err(a, ref):
 
 def test_chunks_with_more_rows_than_are_staged():
     # 32 prefixes of 30 rows each, four prefixes of one i2 per chunk: 120-row chunks,
-    # more than the 48 G3 rows a chunk stages
+    # more than the 32 G3 rows a chunk stages
     x = make_custom((8, 4, 30), N, R, num_bags=3000, max_len=12, seed=21)
     ws = _ws(x)
     out = _forward(x, ws)
     g = tte.read_grouping(x.m, x.n, x.R, x.nnz, x.num_bags, ws)
-    assert np.diff(g["chunk_start"]).max() > 48
+    assert np.diff(g["chunk_start"]).max() > 32
     ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
     assert _rel_err(out, ref) <= FWD_TOL
     grp = oracle.group(x.indices, x.m)
