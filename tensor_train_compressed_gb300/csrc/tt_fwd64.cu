@@ -27,11 +27,17 @@
 // One launch serves up to kMaxTables tables (chunks numbered across the
 // tables, claimed from the first table's counter).  The L2 checkpoint of prefix
 // partials works as in the R = 32 chunk kernel, one slot holding both halves.
+#include <climits>
+
 #include "tt_internal.cuh"
 #include "tt_tile.cuh"
 #include "tt_mma.cuh"
 
 namespace tt {
+
+constexpr int kFwd64Run = 16;          // longest run of consecutive chunks one claim takes
+constexpr int kKeepG2 = INT_MIN;      // slot value: the stage buffer keeps its G2 half
+                                      // (tested first: no i2, no checkpoint slot)
 
 struct MmaFwd64 {
   static constexpr int CW = 8, CP = kCP_8_64, R = 64, NC = 256, H = 2, D = 128;
@@ -238,7 +244,9 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
   uint64_t* go3 = go + 2;
   uint64_t* g3full = go3 + 1;
   uint64_t* g3empty = g3full + 1;                    // consumers done with the G3 area
-  volatile int* slot = reinterpret_cast<volatile int*>(g3empty + 1);  // the stage's i2, -1: stop, -2 - k: slot k
+  // the stage's i2, -1: stop, -2 - k: checkpoint slot k, kKeepG2: the buffer
+  // already holds the chunk's G2 half
+  volatile int* slot = reinterpret_cast<volatile int*>(g3empty + 1);
   __shared__ int cbase[kMaxTables + 1];
   __shared__ int nslots[kMaxTables];
   __shared__ long long ckoff[kMaxTables];          // checkpoint slots: byte offset into rowbuf
@@ -322,7 +330,9 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
       if (!mbar_wait(&go[s], ((uint32_t)k >> 1) & 1, ctl0)) break;
       const int v = slot[s];
       char* dst = base + s * C::STAGE_B;
-      if (v >= 0) {
+      if (v == kKeepG2) {
+        // the buffer holds this half of the chunk's G2 slice already
+      } else if (v >= 0) {
         // rows r1 of the half: columns 256 s .. 256 s + 255 of G2[i2][r1][.]
         const WS& w = tabs.w[meta[s].tab];
         const uint16_t* h2 = w.g2h + (size_t)v * C::R * (2 * C::NC) + C::NC * s;
@@ -443,8 +453,40 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         }
       }
     };
+    // Claims come in runs of consecutive claim-order positions (long while many
+    // chunks remain, one at a time at the end), so that a CTA's successive
+    // chunks mostly share i2 (heads are in row order; the later pieces of a hot
+    // prefix follow each other) and a buffer that holds the chunk's G2 half
+    // is not staged again.
     uint32_t* ctr = &ctl0->fwd_chunk_ctr;
-    int g = claim_chunk(ctr), gn = claim_chunk(ctr);
+    int run_c = 0, run_end = 0;
+    auto claim_next = [&]() {
+      if (run_c >= run_end) {
+        int k = 1, c0 = 0;
+        if (lane == 0) {
+          const int seen = (int)ld_relaxed_u32(ctr);
+          k = (total - seen) / (2 * (int)gridDim.x);
+          k = k < 1 ? 1 : (k > kFwd64Run ? kFwd64Run : k);
+          c0 = (int)atomicAdd(ctr, (uint32_t)k);
+        }
+        run_c = __shfl_sync(0xffffffffu, c0, 0);
+        run_end = run_c + __shfl_sync(0xffffffffu, k, 0);
+      }
+      return run_c++;
+    };
+    int held_tab[2] = {-1, -1}, held_i2[2] = {-1, -1};   // the G2 half each buffer holds
+    // the slot value of half h of the current chunk (and the buffer's new contents)
+    auto g2_slot = [&](int h, int ck, const PMeta& pm) {
+      if (ck < 0) {                       // the checkpointed P2 goes into the G2 area
+        held_i2[h] = -1;
+        return -1 + ck;
+      }
+      if (held_i2[h] == pm.i2 && held_tab[h] == pm.tab) return kKeepG2;
+      held_i2[h] = pm.i2;
+      held_tab[h] = pm.tab;
+      return pm.i2;
+    };
+    int g = claim_next(), gn = claim_next();
     ChunkDesc d{}, dn{};
     int t = 0, tn = 0;
     if (g < total) d = desc_of(g, t);
@@ -468,8 +510,6 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         if (lane == 0) mbar_arrive(&full[0]);
         break;
       }
-      uint32_t tk = 0;
-      if (lane == 0) tk = atomicAdd(ctr, 1u);
       PMeta nxt{};
       if (gn < total) load_meta(dn, tn, nxt);
       int kind_n = 0, sl_n = 0;
@@ -481,6 +521,7 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         break;
       }
       const int ck = role_resolve(d, kind_c, sl_c, v_c);
+      const int s0v = g2_slot(0, ck, cur), s1v = g2_slot(1, ck, cur);
       if (ck < 0 && lane == 0) atomicAdd(&tabs.w[cur.tab].ctl->ckpt_reused, 1);
       Meta& m = meta[0];
       C::G3Meta& gm = g3ms[i & 1];
@@ -490,7 +531,7 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         gm.tab = cur.tab;
         gm.stop = 0;
         m.tab = cur.tab;
-        slot[0] = ck < 0 ? -1 + ck : cur.i2;
+        slot[0] = s0v;
       }
       __syncwarp();
       if (lane == 0) {
@@ -543,7 +584,7 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
       Meta& m1 = meta[1];
       if (lane == 0) {
         m1.tab = cur.tab;
-        slot[1] = ck < 0 ? -1 + ck : cur.i2;
+        slot[1] = s1v;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&go[1]);
@@ -560,7 +601,7 @@ __global__ void __launch_bounds__(MmaFwd64::THREADS, 1)
         mbar_arrive(&full[1]);
       }
       // ---- the next chunk
-      const int gnn = __shfl_sync(0xffffffffu, (int)tk, 0);
+      const int gnn = claim_next();
       ChunkDesc dnn{};
       int tnn = 0;
       if (gnn < total) dnn = desc_of(gnn, tnn);
