@@ -27,8 +27,6 @@
 // One launch serves up to kMaxTables tables (chunks numbered across the
 // tables, claimed from the first table's counter).  The L2 checkpoint of prefix
 // partials works as in the R = 32 chunk kernel, one slot holding both halves.
-#include <climits>
-
 #include "tt_internal.cuh"
 #include "tt_tile.cuh"
 #include "tt_mma.cuh"
@@ -36,8 +34,6 @@
 namespace tt {
 
 constexpr int kFwd64Run = 16;          // longest run of consecutive chunks one claim takes
-constexpr int kKeepG2 = INT_MIN;      // slot value: the stage buffer keeps its G2 half
-                                      // (tested first: no i2, no checkpoint slot)
 
 struct MmaFwd64 {
   static constexpr int CW = 8, CP = kCP_8_64, R = 64, NC = 256, H = 2, D = 128;

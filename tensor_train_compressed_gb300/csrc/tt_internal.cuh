@@ -3,6 +3,7 @@
 // parameter structs and small device helpers.
 #pragma once
 
+#include <climits>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -28,6 +29,9 @@ constexpr int kMaxSmemFloats = 53248;       // 208 KB of shared memory per CTA
 constexpr int kMaxTables = 8;               // tables of one tt_emb_forward_tables call
 constexpr int kMaxCores = 8;                // cores of one chain (tt_emb_*_d)
 constexpr int kCkptSlots = 1024;            // L2 checkpoint slots of prefix partials
+// Stage slot value of the forward chunk kernels: the stage buffer already holds
+// the chunk's G2 slice (tested before the i2 and checkpoint-slot readings).
+constexpr int kKeepG2 = INT_MIN;
 
 // status word bits
 constexpr uint32_t kStIndex = 1u;
