@@ -1046,6 +1046,14 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
     const uint32_t g2h = smem_addr(st), g1h = smem_addr(st + C::OFF_G1);
     const uint32_t Sh = smem_addr(st + C::OFF_S), P2h = smem_addr(P2), dph = smem_addr(dP2);
     const char* G3p = st + C::OFF_G3;
+    // Later batches (rows of the chunk beyond the first RB: a hot prefix's) are
+    // staged by the consumers with their loads issued early: the S rows and
+    // row i3 of batch k + 1 before batch k is computed, so that only the G3
+    // plane pieces (addressed by i3) are loaded while the batch is stored;
+    // thread t handles the (row, 16-byte piece) elements t, t + 256 and
+    // t + 512 of a batch.
+    float4 ns[3];
+    int si3[3];
     if (np > 4) mma_bwd_p2<2>(g2h, g1h, P2, warp, lane);
     else mma_bwd_p2<1>(g2h, g1h, P2, warp, lane);
     {
@@ -1072,24 +1080,36 @@ __global__ void __launch_bounds__(MmaBwd::THREADS, 1) k_bwd_mma(BwdArgs a) {
       for (int i = 0; i < 4; ++i) acc.c[u][i] = 0.f;
     for (int b0 = 0; b0 < rows; b0 += C::RB) {
       if (b0 > 0) {
-        // later batches (rows of a hot prefix beyond the first RB): loaded here
+        // a later batch: store what was loaded during the previous one
         const int nb = min(C::RB, rows - b0);
         named_sync(1, 256);                      // previous batch fully consumed
-        for (int e = tid; e < nb * 32; e += 256) {
-          const int r = e >> 5, q = e & 31;
-          const int x = x0 + b0 + r;
-          bwd_store_s(st + C::OFF_S, r, __ldg(reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)x * C::D) + q), q);
-          const int i3 = __ldg(a.w.row_i3 + x);
-          const int plane = q >> 4, pc = q & 15;
-          *reinterpret_cast<uint4*>(const_cast<char*>(G3p) + plane * C::GPLANE + r * C::GROW + 16 * pc) =
-              *reinterpret_cast<const uint4*>((plane ? a.w.g3l : a.w.g3h) + (size_t)i3 * 4 * C::R + 8 * pc);
-          if (q == 0) m.ri3[r] = i3;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int e = tid + 256 * k, r = e >> 5, q = e & 31;
+          if (r < nb) {
+            bwd_store_s(st + C::OFF_S, r, ns[k], q);
+            const int plane = q >> 4, pc = q & 15;
+            *reinterpret_cast<uint4*>(const_cast<char*>(G3p) + plane * C::GPLANE + r * C::GROW + 16 * pc) =
+                __ldg(reinterpret_cast<const uint4*>((plane ? a.w.g3l : a.w.g3h) + (size_t)si3[k] * 4 * C::R + 8 * pc));
+            if (q == 0) m.ri3[r] = si3[k];
+          }
         }
         if (warp == 0) {
           const int npairs = bwd_pairs(b0, b0 + nb, rows, m.rs, m.pair, lane);
           if (lane == 0) m.npairs = npairs;
         }
         named_sync(1, 256);
+      }
+      if (b0 + C::RB < rows) {                   // the next batch's loads
+        const int nb0 = b0 + C::RB;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int e = tid + 256 * k, r = e >> 5, q = e & 31;
+          if (nb0 + r < rows) {
+            ns[k] = __ldg(reinterpret_cast<const float4*>(a.w.rowbuf + (size_t)(x0 + nb0 + r) * C::D) + q);
+            si3[k] = __ldg(a.w.row_i3 + x0 + nb0 + r);
+          }
+        }
       }
       mma_bwd_dg3(m, P2h, Sh, a.dG3, warp, lane);
       mma_bwd_dp2(m, Sh, G3p, dP2, acc, warp, lane);
