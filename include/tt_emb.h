@@ -133,11 +133,12 @@ typedef struct {
  * fewer than 2^31 (TT_EMB_ERR_ARG otherwise). */
 int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stream);
 
-/* tt_emb_forward_tables with flags: 0 or TT_EMB_CORES_SPLIT, which promises
- * that every table's workspace already holds the split of that table's cores
- * (tt_emb_split or tt_emb_sgd_ex on that workspace, as for tt_emb_forward_ex);
- * the per-call split of the cores is then skipped.  Other flag bits:
- * TT_EMB_ERR_ARG. */
+/* tt_emb_forward_tables with flags: 0 or a combination of TT_EMB_CORES_SPLIT,
+ * which promises that every table's workspace already holds the split of that
+ * table's cores (tt_emb_split or tt_emb_sgd_ex on that workspace, as for
+ * tt_emb_forward_ex; the per-call split of the cores is then skipped), and
+ * TT_EMB_INDICES_I32 (every table's indices are int32; defined below).  Other
+ * flag bits: TT_EMB_ERR_ARG. */
 int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int flags, void* stream);
 
 /* Pooling rules of tt_emb_forward_ex / tt_emb_backward_ex. */
@@ -157,6 +158,15 @@ int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int fla
                                 workspace then holds no grouping.  A tt_emb_backward
                                 with reuse_grouping != 0 after such a call adds
                                 nothing and tt_emb_get_error returns TT_EMB_ERR_REUSE */
+#define TT_EMB_INDICES_I32 4  /* `indices` points at nnz int32 values (4-byte aligned)
+                                instead of int64 ones (8-byte aligned); PyTorch's
+                                EmbeddingBag takes either.  Values are read as
+                                they are (a negative one is out of range).  Also a
+                                flag of tt_emb_forward_tables_ex (every table's
+                                indices) and tt_emb_step_host (h_indices and
+                                d_indices).  A tt_emb_backward that reuses the
+                                call's grouping does not read indices; one that
+                                regroups reads int64 */
 
 /* Forward with the other pooling rules of an embedding bag (the TT-Rec
  * abstract names its operator after the EmbeddingBag; the pages themselves
@@ -171,8 +181,9 @@ int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int fla
  *    guarantees that the workspace holds the bf16 split of exactly these core
  *    values, made by the last tt_emb_split, tt_emb_sgd_ex or forward on this
  *    workspace with the cores unchanged since (a serving loop with fixed cores;
- *    a training loop that updates them with tt_emb_sgd_ex), and
- *    TT_EMB_FORWARD_ONLY (above).  Other bits: TT_EMB_ERR_ARG.
+ *    a training loop that updates them with tt_emb_sgd_ex), TT_EMB_FORWARD_ONLY
+ *    and TT_EMB_INDICES_I32 (above).  Other bits: TT_EMB_ERR_ARG.
+ *  - indices must be aligned to its element size (TT_EMB_ERR_ARG otherwise).
  * tt_emb_forward is tt_emb_forward_ex(..., NULL, TT_EMB_POOL_SUM, 0, ...). */
 int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int32_t n[3],
                       const int32_t R[4], const int64_t* indices, int64_t nnz,
@@ -239,11 +250,11 @@ int tt_emb_sgd_ex(float* const cores[3], float* const core_grads[3], const int64
  * cudaHostRegister): copies from or to pageable memory are correct but block
  * the calling thread and do not overlap. */
 typedef struct {
-  const int64_t* h_indices;  /* host, nnz entries (any alignment)                      */
+  const int64_t* h_indices;  /* host, nnz entries (int32 with TT_EMB_INDICES_I32)       */
   const int64_t* h_offsets;  /* host, num_bags + 1 entries (CSR, as above)             */
   const float* h_grad_out;   /* host, float32 [num_bags][D], or NULL: forward only      */
   float* h_out;              /* host, float32 [num_bags][D], or NULL: not copied back   */
-  int64_t* d_indices;        /* device, nnz entries                                     */
+  int64_t* d_indices;        /* device, nnz entries, aligned to their size (likewise)   */
   int64_t* d_offsets;        /* device, num_bags + 1 entries                            */
   float* d_grad_out;         /* device, [num_bags][D], 16-byte aligned (training only)  */
   float* d_out;              /* device, [num_bags][D], 16-byte aligned                  */

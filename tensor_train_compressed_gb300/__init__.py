@@ -21,7 +21,7 @@ from ._binding import (EXPORTED, TTEmbError, library_path, lib, tt_emb_backward,
 from ._binding import (TT_EMB_ERR_ARG, TT_EMB_ERR_CUDA, TT_EMB_ERR_INDEX, TT_EMB_ERR_OFFSETS,
                        TT_EMB_ERR_TIMEOUT, TT_EMB_ERR_UNSUPPORTED, TT_EMB_ERR_WORKSPACE, TT_EMB_OK,
                        TT_EMB_CORES_SPLIT, TT_EMB_POOL_MEAN, TT_EMB_POOL_SUM,
-                       TT_EMB_FORWARD_ONLY, TT_EMB_ERR_REUSE)
+                       TT_EMB_FORWARD_ONLY, TT_EMB_INDICES_I32, TT_EMB_ERR_REUSE)
 
 __all__ = ["TTEmbeddingBag", "TTEmbError", "tt_emb_forward", "tt_emb_forward_static", "tt_emb_backward", "tt_emb_sgd",
            "tt_emb_forward_ex", "tt_emb_backward_ex", "tt_emb_split", "tt_emb_sgd_ex",
@@ -91,12 +91,14 @@ class TTEmbeddingBag:
             torch.cuda.synchronize(self.device)
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
 
-    def _to_dev(self, x):
+    def _to_dev(self, x, keep_int32=False):
         t = torch.as_tensor(x)
-        return t.to(self.device, torch.int64, non_blocking=True).contiguous()
+        dtype = torch.int32 if keep_int32 and t.dtype == torch.int32 else torch.int64
+        return t.to(self.device, dtype, non_blocking=True).contiguous()
 
     def forward(self, indices, offsets, per_sample_weights=None, out=None, stream=None):
-        idx, off = self._to_dev(indices), self._to_dev(offsets)
+        # int32 indices stay int32 (TT_EMB_INDICES_I32); offsets are int64
+        idx, off = self._to_dev(indices, keep_int32=True), self._to_dev(offsets)
         B = off.numel() - 1
         self._ensure_ws(idx.numel(), B)
         if out is None:
@@ -105,7 +107,7 @@ class TTEmbeddingBag:
         if per_sample_weights is not None:
             psw = torch.as_tensor(per_sample_weights).to(self.device, torch.float32,
                                                          non_blocking=True).contiguous()
-        if psw is None and self.mode == "sum":
+        if psw is None and self.mode == "sum" and idx.dtype == torch.int64:
             tt_emb_forward(self.cores, self.m, self.n, self.R, idx, off, out, self.workspace,
                            stream)
         else:
@@ -147,10 +149,11 @@ class TTEmbeddingBag:
         nnz, B = h_indices.numel(), h_offsets.numel() - 1
         self._ensure_ws(nnz, B)
         st = self._staging
-        if st is None or st[0].numel() < nnz or st[1].numel() < B + 1 or st[2].shape[0] < B:
+        if (st is None or st[0].numel() < nnz or st[0].dtype != h_indices.dtype
+                or st[1].numel() < B + 1 or st[2].shape[0] < B):
             if st is not None:
                 torch.cuda.synchronize(self.device)     # old staging may still be in use
-            st = (torch.empty(max(nnz, 1), dtype=torch.int64, device=self.device),
+            st = (torch.empty(max(nnz, 1), dtype=h_indices.dtype, device=self.device),
                   torch.empty(B + 1, dtype=torch.int64, device=self.device),
                   torch.empty((max(B, 1), self.D), dtype=torch.float32, device=self.device),
                   torch.empty((max(B, 1), self.D), dtype=torch.float32, device=self.device))

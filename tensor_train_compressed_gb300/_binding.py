@@ -30,6 +30,7 @@ TT_EMB_POOL_SUM = 0
 TT_EMB_POOL_MEAN = 1
 TT_EMB_CORES_SPLIT = 1
 TT_EMB_FORWARD_ONLY = 2
+TT_EMB_INDICES_I32 = 4
 _POOLING = {"sum": TT_EMB_POOL_SUM, "mean": TT_EMB_POOL_MEAN}
 
 EXPORTED = ("tt_emb_workspace_bytes", "tt_emb_group", "tt_emb_forward", "tt_emb_backward",
@@ -172,11 +173,19 @@ def tt_emb_forward(cores, m, n, R, indices, offsets, out, workspace, stream=None
                                 _stream(stream)), "tt_emb_forward")
 
 
+def _bwd_indices(indices, reuse_grouping):
+    """A backward that reuses the forward's grouping reads no index, so the forward's int32
+    indices may be passed; one that regroups reads int64."""
+    if reuse_grouping and isinstance(indices, torch.Tensor) and indices.dtype == torch.int32:
+        return _dev(indices, torch.int32, "indices")
+    return _dev(indices, torch.int64, "indices")
+
+
 def tt_emb_backward(grad_out, cores, m, n, R, indices, offsets, core_grads, workspace,
                     reuse_grouping: bool = True, stream=None):
     _check(lib().tt_emb_backward(_dev(grad_out, torch.float32, "grad_out"),
                                  _ptrs3(cores, "cores"), *_shape(m, n, R),
-                                 _dev(indices, torch.int64, "indices"), indices.numel(),
+                                 _bwd_indices(indices, reuse_grouping), indices.numel(),
                                  _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
                                  _ptrs3(core_grads, "core_grads"),
                                  _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
@@ -187,13 +196,25 @@ def _opt(t, dtype, name):
     return None if t is None else _dev(t, dtype, name)
 
 
+def _index_flag(t, name: str) -> int:
+    """TT_EMB_INDICES_I32 for an int32 index tensor, 0 for int64 (either dtype is accepted
+    by the calls that take flags)."""
+    if isinstance(t, torch.Tensor) and t.dtype == torch.int32:
+        return TT_EMB_INDICES_I32
+    if isinstance(t, torch.Tensor) and t.dtype == torch.int64:
+        return 0
+    raise TypeError(f"{name} must be an int64 or int32 tensor")
+
+
 def tt_emb_forward_ex(cores, m, n, R, indices, offsets, per_sample_weights, pooling, out,
                       workspace, stream=None, flags: int = 0):
     """pooling: "sum" / "mean" (or the TT_EMB_POOL_* value); per_sample_weights: None or a
     float32 CUDA tensor [nnz] (sum only); flags: 0, TT_EMB_CORES_SPLIT and/or
-    TT_EMB_FORWARD_ONLY."""
+    TT_EMB_FORWARD_ONLY.  indices: int64 or int32 (TT_EMB_INDICES_I32 is set for int32)."""
+    ixf = _index_flag(indices, "indices")
+    flags = int(flags) | ixf
     _check(lib().tt_emb_forward_ex(_ptrs3(cores, "cores"), *_shape(m, n, R),
-                                   _dev(indices, torch.int64, "indices"), indices.numel(),
+                                   _dev(indices, indices.dtype, "indices"), indices.numel(),
                                    _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
                                    _opt(per_sample_weights, torch.float32, "per_sample_weights"),
                                    int(_POOLING.get(pooling, pooling)), int(flags),
@@ -207,7 +228,7 @@ def tt_emb_backward_ex(grad_out, cores, m, n, R, indices, offsets, per_sample_we
                        stream=None):
     _check(lib().tt_emb_backward_ex(_dev(grad_out, torch.float32, "grad_out"),
                                     _ptrs3(cores, "cores"), *_shape(m, n, R),
-                                    _dev(indices, torch.int64, "indices"), indices.numel(),
+                                    _bwd_indices(indices, reuse_grouping), indices.numel(),
                                     _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,
                                     _opt(per_sample_weights, torch.float32, "per_sample_weights"),
                                     int(_POOLING.get(pooling, pooling)),
@@ -227,7 +248,12 @@ def tt_emb_sgd(cores, core_grads, m, n, R, lr: float, zero_grads: bool = False, 
 def tt_emb_forward_tables(tables, stream=None, flags: int = 0):
     """tables: sequence of dicts with the tt_emb_forward arguments (cores, m, n, R, indices,
     offsets, out, workspace); every table needs its own workspace.  flags != 0 calls
-    tt_emb_forward_tables_ex (TT_EMB_CORES_SPLIT: every workspace holds its table's split)."""
+    tt_emb_forward_tables_ex (TT_EMB_CORES_SPLIT: every workspace holds its table's split).
+    Index tensors: all int64 or all int32 (TT_EMB_INDICES_I32 is set for int32)."""
+    ixf = {_index_flag(t["indices"], f"tables[{k}].indices") for k, t in enumerate(tables)}
+    if len(ixf) > 1:
+        raise TypeError("the tables' index tensors must share one dtype")
+    flags = int(flags) | (ixf.pop() if ixf else 0)
     arr = (Table * len(tables))()
     for k, t in enumerate(tables):
         e = arr[k]
@@ -235,7 +261,7 @@ def tt_emb_forward_tables(tables, stream=None, flags: int = 0):
             e.cores[j] = _dev(c, torch.float32, f"tables[{k}].cores[{j}]").value
         m, n, R = _shape(t["m"], t["n"], t["R"])
         e.m[:], e.n[:], e.R[:] = list(m), list(n), list(R)
-        e.indices = _dev(t["indices"], torch.int64, "indices")
+        e.indices = _dev(t["indices"], t["indices"].dtype, "indices")
         e.nnz = t["indices"].numel()
         e.offsets = _dev(t["offsets"], torch.int64, "offsets")
         e.num_bags = t["offsets"].numel() - 1
@@ -332,7 +358,8 @@ def tt_emb_step_host(cores, core_grads, m, n, R, h_indices, h_offsets, h_grad_ou
                      stream=None, copy_stream=None):
     """One step from host tensors (pinned for the copies to overlap): h_grad_out None runs a
     forward only, h_out None leaves the output on the device.  Without copy_stream a copy
-    stream of this module (one per device) is used."""
+    stream of this module (one per device) is used.  h_indices and d_indices: both int64 or
+    both int32 (TT_EMB_INDICES_I32 is set for int32)."""
     if copy_stream is None:
         dev = torch.cuda.current_device()
         if dev not in _copy_streams:
@@ -340,11 +367,13 @@ def tt_emb_step_host(cores, core_grads, m, n, R, h_indices, h_offsets, h_grad_ou
         copy_stream = _copy_streams[dev]
     train = h_grad_out is not None
     b = HostBatch()
-    b.h_indices = _host(h_indices, torch.int64, "h_indices")
+    ixf = _index_flag(h_indices, "h_indices")
+    flags = int(flags) | ixf
+    b.h_indices = _host(h_indices, h_indices.dtype, "h_indices")
     b.h_offsets = _host(h_offsets, torch.int64, "h_offsets")
     b.h_grad_out = _host(h_grad_out, torch.float32, "h_grad_out") if train else None
     b.h_out = None if h_out is None else _host(h_out, torch.float32, "h_out")
-    b.d_indices = _dev(d_indices, torch.int64, "d_indices")
+    b.d_indices = _dev(d_indices, h_indices.dtype, "d_indices")
     b.d_offsets = _dev(d_offsets, torch.int64, "d_offsets")
     b.d_grad_out = _dev(d_grad_out, torch.float32, "d_grad_out") if train else None
     b.d_out = _dev(d_out, torch.float32, "d_out")

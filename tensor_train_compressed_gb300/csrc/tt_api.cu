@@ -158,11 +158,13 @@ static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 // Common checks of the batch arguments.
 static int check_batch(const Shape& s, const int64_t* indices, int64_t nnz, const int64_t* offsets,
-                       int64_t num_bags, const void* workspace, size_t ws_bytes, Layout* L) {
+                       int64_t num_bags, const void* workspace, size_t ws_bytes, Layout* L,
+                       size_t idx_align = 8) {
   (void)s;
   if (nnz < 0 || nnz >= (1ll << 30) || num_bags < 0 || num_bags >= (1ll << 31)) return TT_EMB_ERR_ARG;
   if (nnz > 0 && num_bags == 0) return TT_EMB_ERR_ARG;   // offsets[0] = 0 != offsets[B] = nnz
-  if (nnz > 0 && !indices) return TT_EMB_ERR_ARG;
+  // indices: aligned to the element size the call reads (1: not read)
+  if (nnz > 0 && (!indices || !aligned(indices, idx_align))) return TT_EMB_ERR_ARG;
   if (!offsets || !workspace) return TT_EMB_ERR_ARG;
   if (!aligned(workspace, 256)) return TT_EMB_ERR_ARG;
   *L = make_layout(s, nnz, num_bags);
@@ -289,7 +291,7 @@ int tt_emb_group(const int64_t m[3], const int32_t n[3], const int32_t R[4], con
   rc = forward_chunk_params(s, &CP, &CR);
   if (rc) return rc;
   const WS w = make_ws(workspace, L);
-  rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, (cudaStream_t)stream);
+  rc = launch_group(s, L, w, Idx{indices, 0}, nnz, offsets, num_bags, CP, CR, (cudaStream_t)stream);
   if (rc) return rc;
   return launch_bag_ids(w, offsets, num_bags, nnz, (cudaStream_t)stream);
 }
@@ -304,12 +306,13 @@ int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int
   if (rc) return rc;
   rc = check_cores(cores);
   if (rc) return rc;
-  if (flags & ~(TT_EMB_CORES_SPLIT | TT_EMB_FORWARD_ONLY)) return TT_EMB_ERR_ARG;
+  if (flags & ~(TT_EMB_CORES_SPLIT | TT_EMB_FORWARD_ONLY | TT_EMB_INDICES_I32)) return TT_EMB_ERR_ARG;
   Pooling pool;
   rc = check_pooling(per_sample_weights, pooling, &pool);
   if (rc) return rc;
+  const Idx idx{indices, (flags & TT_EMB_INDICES_I32) ? 1 : 0};
   Layout L;
-  rc = check_batch(s, indices, nnz, offsets, num_bags, workspace, ws_bytes, &L);
+  rc = check_batch(s, indices, nnz, offsets, num_bags, workspace, ws_bytes, &L, idx.i32 ? 4 : 8);
   if (rc) return rc;
   if (num_bags > 0 && (!out || !aligned(out, 16))) return TT_EMB_ERR_ARG;
   cudaStream_t st = (cudaStream_t)stream;
@@ -321,12 +324,12 @@ int tt_emb_forward_ex(const float* const cores[3], const int64_t m[3], const int
       rc = launch_split(s, w, cores, 0, st);
       if (rc) return rc;
     }
-    return launch_forward_direct(s, w, cores, indices, nnz, offsets, num_bags, pool, out, st);
+    return launch_forward_direct(s, w, cores, idx, nnz, offsets, num_bags, pool, out, st);
   }
   int CP, CR;
   rc = forward_chunk_params(s, &CP, &CR);
   if (rc) return rc;
-  rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, st,
+  rc = launch_group(s, L, w, idx, nnz, offsets, num_bags, CP, CR, st,
                     (flags & TT_EMB_FORWARD_ONLY) ? 0 : 1);
   if (rc) return rc;
   if (nnz == 0) {
@@ -353,7 +356,8 @@ int tt_emb_forward_tables(int num_tables, const tt_emb_table* tables, void* stre
 
 int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int flags, void* stream) {
   if (num_tables < 1 || num_tables > kMaxTables || !tables) return TT_EMB_ERR_ARG;
-  if (flags & ~TT_EMB_CORES_SPLIT) return TT_EMB_ERR_ARG;
+  if (flags & ~(TT_EMB_CORES_SPLIT | TT_EMB_INDICES_I32)) return TT_EMB_ERR_ARG;
+  const int idx32 = (flags & TT_EMB_INDICES_I32) ? 1 : 0;
   Shape s[kMaxTables];
   Layout L[kMaxTables];
   WS w[kMaxTables];
@@ -373,7 +377,7 @@ int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int fla
     rc = check_cores(tb.cores);
     if (rc) return rc;
     rc = check_batch(s[t], tb.indices, tb.nnz, tb.offsets, tb.num_bags, tb.workspace, tb.ws_bytes,
-                     &L[t]);
+                     &L[t], idx32 ? 4 : 8);
     if (rc) return rc;
     if (tb.num_bags > 0 && (!tb.out || !aligned(tb.out, 16))) return TT_EMB_ERR_ARG;
     // every table groups into its own workspace
@@ -397,8 +401,8 @@ int tt_emb_forward_tables_ex(int num_tables, const tt_emb_table* tables, int fla
     int rc = forward_chunk_params(s[t], &CP, &CR);
     if (rc) return rc;
     // forward-only groupings: no backward reuses them
-    rc = launch_group(s[t], L[t], w[t], tables[t].indices, nnz[t], offsets[t], bags[t], CP, CR, st,
-                      0);
+    rc = launch_group(s[t], L[t], w[t], Idx{tables[t].indices, idx32}, nnz[t], offsets[t], bags[t],
+                      CP, CR, st, 0);
     if (rc) return rc;
     if (nnz[t] == 0 && bags[t] > 0 &&
         cudaMemsetAsync(out[t], 0, sizeof(float) * (size_t)bags[t] * s[t].D, st) != cudaSuccess)
@@ -426,7 +430,8 @@ int tt_emb_backward_ex(const float* grad_out, const float* const cores[3], const
   if (rc) return rc;
   if (grad_weights && (!per_sample_weights || !aligned(grad_weights, 4))) return TT_EMB_ERR_ARG;
   Layout L;
-  rc = check_batch(s, indices, nnz, offsets, num_bags, workspace, ws_bytes, &L);
+  rc = check_batch(s, indices, nnz, offsets, num_bags, workspace, ws_bytes, &L,
+                   reuse_grouping ? 1 : 8);   // a reused grouping reads no index
   if (rc) return rc;
   if (num_bags > 0 && (!grad_out || !aligned(grad_out, 16))) return TT_EMB_ERR_ARG;
   cudaStream_t st = (cudaStream_t)stream;
@@ -435,7 +440,7 @@ int tt_emb_backward_ex(const float* grad_out, const float* const cores[3], const
     int CP, CR;
     rc = forward_chunk_params(s, &CP, &CR);
     if (rc) return rc;
-    rc = launch_group(s, L, w, indices, nnz, offsets, num_bags, CP, CR, st);
+    rc = launch_group(s, L, w, Idx{indices, 0}, nnz, offsets, num_bags, CP, CR, st);
     if (rc) return rc;
     rc = launch_bag_ids(w, offsets, num_bags, nnz, st);
     if (rc) return rc;

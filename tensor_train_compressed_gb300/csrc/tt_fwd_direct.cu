@@ -32,7 +32,7 @@ struct DirectArgs {
   const float* G1;
   const float* G2;
   const float* G3;
-  const int64_t* indices;
+  Idx indices;
   const int64_t* offsets;
   const float* psw;     // per-sample weights (kPoolWeighted), else null
   int64_t B, nnz;
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(32 * kDirectWarps) k_fwd_direct(const DirectAr
     for (int k = 0; k < DL; ++k) acc[k] = 0.f;
     for (int64_t lb = l0; lb < l1; lb += 32) {
       const int cnt = (int)(l1 - lb < 32 ? l1 - lb : 32);
-      int64_t my_r = lane < cnt ? a.indices[lb + lane] : 0;
+      int64_t my_r = lane < cnt ? a.indices.at(lb + lane) : 0;
       const float my_w = (MODE == kPoolWeighted && lane < cnt) ? a.psw[lb + lane] : 1.f;
       const bool bad = lane < cnt && (my_r < 0 || my_r >= s.M);
       if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(a.ctl, kStIndex);
@@ -227,7 +227,7 @@ bool direct_eligible(const Shape& s, int64_t nnz) {
 }
 
 int launch_forward_direct(const Shape& s, const WS& w, const float* const cores[3],
-                          const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                          Idx indices, int64_t nnz, const int64_t* offsets,
                           int64_t num_bags, const Pooling& pool, float* out, cudaStream_t st) {
   if (!direct_eligible(s, nnz)) return TT_EMB_ERR_UNSUPPORTED;
   // a fresh control block: no grouping, no status bits, the split planes unrecorded

@@ -26,7 +26,7 @@
 namespace tt {
 
 struct PrepArgs {
-  const int64_t* indices;
+  Idx indices;
   int64_t nnz;
   const int64_t* offsets;
   int64_t B;
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(256) k_prepare(PrepArgs a) {
     uint32_t key = a.sentinel;
     const bool live = l < a.nnz;
     if (live) {
-      const int64_t r = a.indices[l];
+      const int64_t r = a.indices.at(l);
       if (r >= 0 && r < a.s.M) key = group_key(r, a.s);
       else bad_index = true;
     }
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(256) k_prepare(PrepArgs a) {
 }
 
 struct ScatterArgs {
-  const int64_t* indices;   // pass 0 reads the indices directly
+  Idx indices;              // pass 0 reads the indices directly
   const uint64_t* in;
   uint64_t* out;
   int64_t nnz;
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kSortThreads) k_scatter(ScatterArgs a) {
     uint64_t wv = ~0ull;
     if (i < a.nnz) {
       if (a.pass == 0) {
-        const int64_t r = a.indices[i];
+        const int64_t r = a.indices.at(i);
         const uint32_t key = (r >= 0 && r < a.s.M) ? group_key(r, a.s) : a.sentinel;
         wv = ((uint64_t)key << 32) | (uint64_t)(uint32_t)i;
       } else {
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kScanThreads) k_chunks(ChunkArgs a) {
   }
 }
 
-int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
+int launch_group(const Shape& s, const Layout& L, const WS& w, Idx indices,
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                  int rows_per_chunk, cudaStream_t st, int lists) {
   // control block + digit histograms start from zero

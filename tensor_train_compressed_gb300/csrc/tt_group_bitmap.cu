@@ -46,7 +46,7 @@ constexpr size_t kBmSmem =
     sizeof(uint32_t) * (kBmSlots + 2 * kBmPSlots) + sizeof(uint16_t) * kBmSlots;
 
 struct BitmapArgs {
-  const int64_t* indices;
+  Idx indices;
   int64_t nnz;
   const int64_t* offsets;
   int64_t B;
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_bitmap(BitmapArgs a) 
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
       const int64_t i = pos_of(it);
-      r[it] = i < seg1 ? __ldg(a.indices + i) : -1;
+      r[it] = i < seg1 ? a.indices.at(i) : -1;
     }
     const int64_t bt = (int64_t)c * kCoopThreads + tid;
     int64_t o0 = 0, o1 = 0;
@@ -564,7 +564,7 @@ bool bitmap_grouping_applies(const Shape& s, const Layout& L, int64_t nnz) {
   return need <= sizeof(float) * (size_t)L.rowbuf_rows * (size_t)s.D;
 }
 
-int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
+int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, Idx indices,
                         int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                         int rows_per_chunk, cudaStream_t st) {
   if (!bitmap_grouping_applies(s, L, nnz)) return TT_EMB_ERR_UNSUPPORTED;

@@ -22,7 +22,7 @@
 namespace tt {
 
 struct CoopArgs {
-  const int64_t* indices;
+  Idx indices;
   int64_t nnz;
   const int64_t* offsets;
   int64_t B;
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_group_coop(CoopArgs a) {
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
       const int64_t i = seg0 + warp * kSpan + it * 32 + lane;
-      word[it] = i < seg1 ? (uint64_t)__ldg(a.indices + i) : 0ull;
+      word[it] = i < seg1 ? (uint64_t)a.indices.at(i) : 0ull;
     }
     const int64_t bt = (int64_t)c * kCoopThreads + tid;
     int64_t o0 = 0, o1 = 0;
@@ -462,7 +462,7 @@ size_t coop_scratch_bytes() {
 // register-resident segments; returns TT_EMB_ERR_UNSUPPORTED otherwise (the
 // caller then uses the multi-kernel path).
 int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratch,
-                      const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                      Idx indices, int64_t nnz, const int64_t* offsets,
                       int64_t num_bags, int pairs_per_chunk, int rows_per_chunk,
                       cudaStream_t st) {
   const int G = coop_grid();

@@ -61,11 +61,13 @@ extern "C" int tt_emb_step_host(float* const cores[3], float* const core_grads[3
   int rc = tt_emb_workspace_bytes(m, n, R, b.nnz, b.num_bags, &need);
   if (rc) return rc;
   const bool train = b.h_grad_out != nullptr;
-  if (flags & ~(TT_EMB_CORES_SPLIT | TT_EMB_FORWARD_ONLY)) return TT_EMB_ERR_ARG;
+  if (flags & ~(TT_EMB_CORES_SPLIT | TT_EMB_FORWARD_ONLY | TT_EMB_INDICES_I32)) return TT_EMB_ERR_ARG;
+  const size_t idx_bytes = (flags & TT_EMB_INDICES_I32) ? sizeof(int32_t) : sizeof(int64_t);
   if (train && (flags & TT_EMB_FORWARD_ONLY)) return TT_EMB_ERR_ARG;   // the backward reuses it
   if (!cores_ok((const void* const*)cores) || (train && !cores_ok((const void* const*)core_grads)))
     return TT_EMB_ERR_ARG;
-  if (b.nnz > 0 && (b.num_bags == 0 || !b.h_indices || !b.d_indices)) return TT_EMB_ERR_ARG;
+  if (b.nnz > 0 && (b.num_bags == 0 || !b.h_indices || !b.d_indices || !aligned(b.d_indices, idx_bytes)))
+    return TT_EMB_ERR_ARG;
   if (b.num_bags >= (1ll << 31)) return TT_EMB_ERR_ARG;
   if (!b.h_offsets || !b.d_offsets) return TT_EMB_ERR_ARG;
   if (b.num_bags > 0 && (!b.d_out || !aligned(b.d_out, 16))) return TT_EMB_ERR_ARG;
@@ -99,7 +101,7 @@ extern "C" int tt_emb_step_host(float* const cores[3], float* const core_grads[3
   // streams; the output gradient comes in on the copy stream once they are in
   // (not competing with them for the copy bandwidth) while the forward runs.
   if (b.nnz > 0)
-    cuda(cudaMemcpyAsync(b.d_indices, b.h_indices, sizeof(int64_t) * (size_t)b.nnz,
+    cuda(cudaMemcpyAsync(b.d_indices, b.h_indices, idx_bytes * (size_t)b.nnz,
                          cudaMemcpyHostToDevice, st));
   cuda(cudaMemcpyAsync(b.d_offsets, b.h_offsets, sizeof(int64_t) * (size_t)(b.num_bags + 1),
                        cudaMemcpyHostToDevice, st));

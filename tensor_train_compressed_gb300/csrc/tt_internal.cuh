@@ -362,20 +362,30 @@ WS make_ws(void* base, const Layout& L);
 int shape_from_args(const int64_t m[3], const int32_t n[3], const int32_t R[4], Shape* s);
 int sm_count();
 
+// The lookups' row indices, int64 or (TT_EMB_INDICES_I32) int32 values; a
+// negative int32 reads as the same negative int64, out of range either way.
+struct Idx {
+  const void* p;
+  int i32;
+  __device__ __forceinline__ int64_t at(int64_t i) const {
+    return i32 ? (int64_t)__ldg(static_cast<const int32_t*>(p) + i) : __ldg(static_cast<const int64_t*>(p) + i);
+  }
+};
+
 // grouping in one cooperative launch (tt_group_coop.cu)
 size_t coop_scratch_bytes();
-int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
+int launch_group_bitmap(const Shape& s, const Layout& L, const WS& w, Idx indices,
                         int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                         int rows_per_chunk, cudaStream_t st);
 bool bitmap_grouping_applies(const Shape& s, const Layout& L, int64_t nnz);
 int launch_group_coop(const Shape& s, const Layout& L, const WS& w, void* scratch,
-                      const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                      Idx indices, int64_t nnz, const int64_t* offsets,
                       int64_t num_bags, int pairs_per_chunk, int rows_per_chunk, cudaStream_t st);
 // grouping (tt_group.cu)
 // lists = 0: a forward-only call, whose grouping may leave out the per-row
 // lookup lists (perm, row_start) that only a backward reads: the key-bitmap
 // grouping then serves a batch dense in its table
-int launch_group(const Shape& s, const Layout& L, const WS& w, const int64_t* indices,
+int launch_group(const Shape& s, const Layout& L, const WS& w, Idx indices,
                  int64_t nnz, const int64_t* offsets, int64_t num_bags, int pairs_per_chunk,
                  int rows_per_chunk, cudaStream_t st, int lists = 1);
 // chains of d > 3 cores (tt_chain.cu): the leading d - 2 cores merged into one
@@ -425,7 +435,7 @@ int launch_split(const Shape& s, const WS& w, const float* const cores[3], int r
 int64_t direct_macs_per_lookup(const Shape& s);
 bool direct_eligible(const Shape& s, int64_t nnz);
 int launch_forward_direct(const Shape& s, const WS& w, const float* const cores[3],
-                          const int64_t* indices, int64_t nnz, const int64_t* offsets,
+                          Idx indices, int64_t nnz, const int64_t* offsets,
                           int64_t num_bags, const Pooling& pool, float* out, cudaStream_t st);
 // Called by one thread of a kernel that runs after k_split_cores in the same
 // stream: the split planes now hold the cores at g1, g2, g3.

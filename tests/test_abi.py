@@ -108,7 +108,7 @@ def test_pooling_variant_argument_checks(L):
     assert fwd(None, 7) == tte.TT_EMB_ERR_ARG                           # unknown pooling
     assert fwd(P(fake + 2), tte.TT_EMB_POOL_SUM) == tte.TT_EMB_ERR_ARG  # misaligned weights
     assert fwd(None, tte.TT_EMB_POOL_MEAN, need - 1) == tte.TT_EMB_ERR_WORKSPACE
-    assert fwd(None, tte.TT_EMB_POOL_SUM, need, 4) == tte.TT_EMB_ERR_ARG    # unknown flag
+    assert fwd(None, tte.TT_EMB_POOL_SUM, need, 8) == tte.TT_EMB_ERR_ARG    # unknown flag
     bwd = lambda psw, pooling, gw: L.tt_emb_backward_ex(
         P(fake), cores, *_shape(m, n, R), P(fake), 100, P(fake), 10, psw, pooling, cores, gw,
         P(fake), need - 1, 1, None)
@@ -116,6 +116,41 @@ def test_pooling_variant_argument_checks(L):
     assert bwd(P(fake), tte.TT_EMB_POOL_MEAN, None) == tte.TT_EMB_ERR_ARG
     assert bwd(P(fake), tte.TT_EMB_POOL_SUM, P(fake + 1)) == tte.TT_EMB_ERR_ARG
     assert bwd(P(fake), tte.TT_EMB_POOL_SUM, P(fake)) == tte.TT_EMB_ERR_WORKSPACE
+
+
+def test_index_width_argument_checks(L):
+    """Indices are int64 (8-byte aligned) or, with TT_EMB_INDICES_I32, int32 (4-byte
+    aligned); the flag is known to the three calls that take flags."""
+    m, n, R = (10, 10, 10), (2, 4, 2), (1, 4, 4, 1)
+    fake = 1 << 20
+    cores = (ctypes.c_void_p * 3)(fake, fake, fake)
+    P = ctypes.c_void_p
+    need = tte.tt_emb_workspace_bytes(m, n, R, 100, 10)
+    fwd = lambda idx, flags: L.tt_emb_forward_ex(
+        cores, *_shape(m, n, R), P(idx), 100, P(fake), 10, None, tte.TT_EMB_POOL_SUM, flags,
+        P(fake), P(fake), need, None)
+    assert fwd(fake + 4, 0) == tte.TT_EMB_ERR_ARG                        # int64 at 4 bytes
+    assert fwd(fake + 2, tte.TT_EMB_INDICES_I32) == tte.TT_EMB_ERR_ARG   # int32 at 2 bytes
+    assert tte.TT_EMB_INDICES_I32 == 4
+    from tensor_train_compressed_gb300._binding import Table
+    arr = (Table * 1)()
+    arr[0].cores[:] = [fake, fake, fake]
+    arr[0].m[:], arr[0].n[:], arr[0].R[:] = list(m), list(n), list(R)
+    arr[0].indices, arr[0].nnz, arr[0].offsets, arr[0].num_bags = fake + 2, 100, fake, 10
+    arr[0].out, arr[0].workspace, arr[0].ws_bytes = fake, fake, need
+    ptr = ctypes.cast(arr, P)
+    assert L.tt_emb_forward_tables_ex(1, ptr, tte.TT_EMB_INDICES_I32, None) == tte.TT_EMB_ERR_ARG
+    assert L.tt_emb_forward_tables_ex(1, ptr, 8, None) == tte.TT_EMB_ERR_ARG   # unknown flag
+
+
+def test_index_dtype_binding_checks():
+    """The binding takes int64 or int32 index tensors and sets the flag from the dtype."""
+    import torch
+    assert B._index_flag(torch.zeros(3, dtype=torch.int64), "i") == 0
+    assert B._index_flag(torch.zeros(3, dtype=torch.int32), "i") == tte.TT_EMB_INDICES_I32
+    for bad in (torch.zeros(3, dtype=torch.int16), torch.zeros(3), [0, 1]):
+        with pytest.raises(TypeError):
+            B._index_flag(bad, "i")
 
 
 def test_product_path_has_no_oracle_dependency():
@@ -216,7 +251,10 @@ def test_step_host_argument_checks(L):
     assert call(None) == tte.TT_EMB_ERR_ARG
     assert call(batch(), ws_bytes=need - 1) == tte.TT_EMB_ERR_WORKSPACE
     assert call(batch(), ws=fake + 8) == tte.TT_EMB_ERR_ARG          # workspace alignment
-    assert call(batch(), flags=2) == tte.TT_EMB_ERR_ARG              # unknown flag
+    assert call(batch(), flags=2) == tte.TT_EMB_ERR_ARG              # forward-only with a gradient
+    assert call(batch(), flags=8) == tte.TT_EMB_ERR_ARG              # unknown flag
+    assert call(batch(d_indices=fake + 4)) == tte.TT_EMB_ERR_ARG     # int64 indices alignment
+    assert call(batch(d_indices=fake + 2), flags=tte.TT_EMB_INDICES_I32) == tte.TT_EMB_ERR_ARG
     assert call(batch(), grads=None) == tte.TT_EMB_ERR_ARG           # training needs gradients
     assert call(batch(d_grad_out=None)) == tte.TT_EMB_ERR_ARG
     assert call(batch(d_out=fake + 4)) == tte.TT_EMB_ERR_ARG         # out alignment
@@ -238,8 +276,8 @@ def test_step_host_binding_checks_tensor_kinds(L):
     cores = [torch.zeros(4) for _ in range(3)]
     h_idx, h_off = torch.zeros(5, dtype=torch.int64), torch.tensor([0, 5], dtype=torch.int64)
     h_g, h_out = torch.zeros(1, 16), torch.zeros(1, 16)
-    with pytest.raises(TypeError):                 # indices must be int64
-        tte.tt_emb_step_host(cores, cores, m, n, R, h_idx.int(), h_off, h_g, h_out, h_idx, h_off,
+    with pytest.raises(TypeError):                 # indices must be int64 or int32
+        tte.tt_emb_step_host(cores, cores, m, n, R, h_idx.short(), h_off, h_g, h_out, h_idx, h_off,
                              h_g, h_out, 0.1, torch.zeros(8, dtype=torch.uint8), copy_stream=0)
     with pytest.raises(TypeError):                 # device staging must be CUDA tensors
         tte.tt_emb_step_host(cores, cores, m, n, R, h_idx, h_off, h_g, h_out, h_idx, h_off, h_g,
