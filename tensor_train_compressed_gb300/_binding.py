@@ -165,6 +165,10 @@ def tt_emb_group(m, n, R, indices, offsets, workspace, stream=None):
 
 
 def tt_emb_forward(cores, m, n, R, indices, offsets, out, workspace, stream=None):
+    """Sum pooling; int32 indices go through tt_emb_forward_ex with TT_EMB_INDICES_I32."""
+    if isinstance(indices, torch.Tensor) and indices.dtype == torch.int32:
+        return tt_emb_forward_ex(cores, m, n, R, indices, offsets, None, "sum", out, workspace,
+                                 stream)
     _check(lib().tt_emb_forward(_ptrs3(cores, "cores"), *_shape(m, n, R),
                                 _dev(indices, torch.int64, "indices"), indices.numel(),
                                 _dev(offsets, torch.int64, "offsets"), offsets.numel() - 1,

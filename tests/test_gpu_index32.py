@@ -88,6 +88,11 @@ def test_forward_int32_equals_int64(case):
     assert rc64 == tte.TT_EMB_OK and rc32 == tte.TT_EMB_OK, bits
     assert _same_grouping(x, w64, w32) == case
     assert torch.equal(o32, o64)
+    if case == "coop_sort":                 # the plain entry point takes int32 too
+        o = torch.empty_like(o64)
+        tte.tt_emb_forward(cores, x.m, x.n, x.R, _dev(x.indices.astype(np.int32)),
+                           _dev(x.offsets), o, w32)
+        assert torch.equal(o, o64)
     if case in ("direct", "coop_sort"):
         ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets, threads=8)
         assert _rel_err(o32.cpu().numpy(), ref) <= FWD_TOL
