@@ -33,9 +33,9 @@
  *    between calls beyond the caller's workspace, with three exceptions,
  *    each described at its declaration: the fixed device array of
  *    tt_emb_forward_static (shared by every call of that entry point), the
- *    per-thread, per-device CUDA events of tt_emb_step_host (created on a
- *    thread's first call on a device, kept until the process exits), and the
- *    opt-in launch records of tt_emb_profile_start.
+ *    per-thread, per-device CUDA events and CUDA graphs of tt_emb_step_host
+ *    (created on a thread's first calls on a device, kept until the process
+ *    exits), and the opt-in launch records of tt_emb_profile_start.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *    call only enqueues work on it and returns; none synchronises except
  *    tt_emb_get_error.
@@ -280,7 +280,16 @@ typedef struct {
  * anything is enqueued; device-side conditions as for the calls named.  If a
  * call fails after its copies were enqueued (a CUDA error, or an error code
  * of one of the calls named), `stream` is still made to wait for every copy
- * the call enqueued, so the host buffers may be reused once `stream` drains. */
+ * the call enqueued, so the host buffers may be reused once `stream` drains.
+ * Graphs: the second call of a thread whose arguments (every pointer, size,
+ * lr, flags and both streams) equal an earlier call's captures the call's
+ * work into a CUDA graph, and later such calls launch that graph on `stream`
+ * (the same copies and kernels with the same dependencies, without their
+ * launch costs), after the work enqueued on either stream before the call and
+ * before the copy stream's later work.  A thread keeps the last four argument
+ * sets per device.  Calls with pageable host buffers, on the legacy or
+ * per-thread default stream, on a stream being captured, or with launch
+ * records on (tt_emb_profile_start) always run eagerly. */
 int tt_emb_step_host(float* const cores[3], float* const core_grads[3], const int64_t m[3],
                      const int32_t n[3], const int32_t R[4], const tt_emb_host_batch* batch,
                      float lr, int flags, void* workspace, size_t ws_bytes, void* stream,

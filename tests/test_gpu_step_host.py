@@ -153,3 +153,97 @@ def test_class_train_step_from_host_matches_the_device_calls():
         tol = 0.5 * 1e-3 * dg[k].abs().max().item()
         assert (a.cores[k] - b.cores[k]).abs().max().item() <= tol, k
         assert not a.grads[k].any()
+
+
+def test_repeated_forward_steps_replay_a_graph():
+    # the second call with the same arguments captures the work into a graph and
+    # later ones replay it: every call's output is the device forward's, bit for bit
+    x = make_inputs(3, num_bags=2000)
+    cores = [_dev(c) for c in x.cores]
+    ws = torch.empty(tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags),
+                     dtype=torch.uint8, device="cuda")
+    expect = _device_forward(x, cores, torch.empty_like(ws)).cpu()
+    f = Staging(x, train=False)
+    stream, copy_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for it in range(5):
+        f.h_out.fill_(float("nan"))
+        f.d_out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            f.step(x, cores, None, ws, 0.1, flags=tte.TT_EMB_FORWARD_ONLY, stream=stream,
+                   copy_stream=copy_stream)
+        stream.synchronize()
+        rc, bits = tte.tt_emb_get_error(ws, stream)
+        assert rc == tte.TT_EMB_OK, (it, bits)
+        assert torch.equal(f.h_out, expect), it
+        assert torch.equal(f.d_out.cpu(), expect), it
+
+
+def test_repeated_training_steps_replay_a_graph():
+    # five training steps with the same arguments (the last three replayed from
+    # a graph) against five steps of the device calls
+    x = make_inputs(5, num_bags=1500)
+    lr = 1e-3                # repeated steps on one fixed output gradient: kept small
+    ws_a = torch.empty(tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags),
+                       dtype=torch.uint8, device="cuda")
+    ws_b = torch.empty_like(ws_a)
+    a = [_dev(c) for c in x.cores]
+    b = [c.clone() for c in a]
+    ga = [torch.zeros_like(c) for c in a]
+    gb = [torch.zeros_like(c) for c in b]
+    tte.tt_emb_split(a, x.m, x.n, x.R, ws_a)
+    tte.tt_emb_split(b, x.m, x.n, x.R, ws_b)
+    s = Staging(x)
+    stream, copy_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    idx, off, g = _dev(x.indices), _dev(x.offsets), _dev(x.grad_out)
+    out_b = torch.empty((x.num_bags, x.D), device="cuda")
+    torch.cuda.synchronize()
+    for it in range(5):
+        with torch.cuda.stream(stream):
+            s.step(x, a, ga, ws_a, lr, flags=tte.TT_EMB_CORES_SPLIT, stream=stream,
+                   copy_stream=copy_stream)
+        stream.synchronize()
+        tte.tt_emb_forward_ex(b, x.m, x.n, x.R, idx, off, None, "sum", out_b, ws_b,
+                              flags=tte.TT_EMB_CORES_SPLIT)
+        tte.tt_emb_backward(g, b, x.m, x.n, x.R, idx, off, gb, ws_b, reuse_grouping=True)
+        tte.tt_emb_sgd_ex(b, gb, x.m, x.n, x.R, lr, True, ws_b)
+        torch.cuda.synchronize()
+        for ws in (ws_a, ws_b):
+            rc, bits = tte.tt_emb_get_error(ws)
+            assert rc == tte.TT_EMB_OK, (it, bits)
+        # outputs and cores differ only by the order of the backward's float atomics
+        ref = out_b.cpu()
+        assert (s.h_out - ref).abs().max().item() <= 1e-5 * ref.abs().max().item(), it
+        for k in range(3):
+            assert (a[k] - b[k]).abs().max().item() <= 1e-5 * b[k].abs().max().item(), (it, k)
+            assert not ga[k].any()
+
+
+def test_graph_replay_follows_changed_arguments():
+    # alternating output buffers and a pageable host output: every call writes
+    # where its own arguments say
+    x = make_inputs(3, num_bags=800)
+    cores = [_dev(c) for c in x.cores]
+    ws = torch.empty(tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags),
+                     dtype=torch.uint8, device="cuda")
+    expect = _device_forward(x, cores, torch.empty_like(ws)).cpu()
+    f = Staging(x, train=False)
+    outs = [torch.empty((x.num_bags, x.D), device="cuda") for _ in range(2)]
+    pageable = torch.empty((x.num_bags, x.D))
+    stream, copy_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for it in range(6):
+        d_out = outs[it % 2]
+        h_out = pageable if it == 4 else f.h_out
+        d_out.fill_(float("nan"))
+        h_out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            tte.tt_emb_step_host(cores, None, x.m, x.n, x.R, f.h_idx, f.h_off, None, h_out,
+                                 f.d_idx, f.d_off, None, d_out, 0.1, ws,
+                                 flags=tte.TT_EMB_FORWARD_ONLY, stream=stream,
+                                 copy_stream=copy_stream)
+        stream.synchronize()
+        assert torch.equal(d_out.cpu(), expect), it
+        assert torch.equal(h_out, expect), it
