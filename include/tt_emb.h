@@ -289,7 +289,9 @@ typedef struct {
  * before the copy stream's later work.  A thread keeps the last four argument
  * sets per device.  Calls with pageable host buffers, on the legacy or
  * per-thread default stream, on a stream being captured, or with launch
- * records on (tt_emb_profile_start) always run eagerly. */
+ * records on (tt_emb_profile_start) always run eagerly.  The events and
+ * graphs belong to the device's context: after cudaDeviceReset a thread's
+ * calls return TT_EMB_ERR_CUDA. */
 int tt_emb_step_host(float* const cores[3], float* const core_grads[3], const int64_t m[3],
                      const int32_t n[3], const int32_t R[4], const tt_emb_host_batch* batch,
                      float lr, int flags, void* workspace, size_t ws_bytes, void* stream,
