@@ -142,6 +142,27 @@ def test_forward_tables_int32():
         tte.tt_emb_forward_tables([dict(tables[0]), dict(tables[1], indices=tables[1]["indices"].long())])
 
 
+def test_forward_tables_int32_tiled_shape():
+    # n = (4, 4, 4), R = 16: the tables share the tiled FP32 chunk kernel
+    xs = [make_custom((30, 40, 50), (4, 4, 4), (1, 16, 16, 1), num_bags=900, max_len=25,
+                      seed=83 + t) for t in range(3)]
+    outs = {}
+    for dt in (np.int64, np.int32):
+        tables = [dict(cores=[_dev(c) for c in x.cores], m=x.m, n=x.n, R=x.R,
+                       indices=_dev(x.indices.astype(dt)), offsets=_dev(x.offsets),
+                       out=torch.empty((x.num_bags, x.D), device="cuda"), workspace=_ws(x))
+                  for x in xs]
+        tte.tt_emb_forward_tables(tables)
+        for t in tables:
+            rc, bits = tte.tt_emb_get_error(t["workspace"])
+            assert rc == tte.TT_EMB_OK, bits
+        outs[dt] = [t["out"] for t in tables]
+    for x, a, b in zip(xs, outs[np.int64], outs[np.int32]):
+        assert torch.equal(a, b)
+        ref = oracle.forward(x.cores, x.m, x.n, x.R, x.indices, x.offsets)
+        assert _rel_err(b.cpu().numpy(), ref) <= FWD_TOL
+
+
 def test_step_host_with_int32_indices():
     x = make_inputs(5, num_bags=1500)
     lr = 0.5

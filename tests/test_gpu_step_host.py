@@ -155,16 +155,19 @@ def test_class_train_step_from_host_matches_the_device_calls():
         assert not a.grads[k].any()
 
 
-def test_repeated_forward_steps_replay_a_graph():
+@pytest.mark.parametrize("same_stream", [False, True])
+def test_repeated_forward_steps_replay_a_graph(same_stream):
     # the second call with the same arguments captures the work into a graph and
     # later ones replay it: every call's output is the device forward's, bit for bit
+    # (also with the copy stream equal to the compute stream)
     x = make_inputs(3, num_bags=2000)
     cores = [_dev(c) for c in x.cores]
     ws = torch.empty(tte.tt_emb_workspace_bytes(x.m, x.n, x.R, x.nnz, x.num_bags),
                      dtype=torch.uint8, device="cuda")
     expect = _device_forward(x, cores, torch.empty_like(ws)).cpu()
     f = Staging(x, train=False)
-    stream, copy_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    stream = torch.cuda.Stream()
+    copy_stream = stream if same_stream else torch.cuda.Stream()
     torch.cuda.synchronize()
     for it in range(5):
         f.h_out.fill_(float("nan"))
