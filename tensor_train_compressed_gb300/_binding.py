@@ -363,7 +363,9 @@ def tt_emb_step_host(cores, core_grads, m, n, R, h_indices, h_offsets, h_grad_ou
     """One step from host tensors (pinned for the copies to overlap): h_grad_out None runs a
     forward only, h_out None leaves the output on the device.  Without copy_stream a copy
     stream of this module (one per device) is used.  h_indices and d_indices: both int64 or
-    both int32 (TT_EMB_INDICES_I32 is set for int32)."""
+    both int32 (TT_EMB_INDICES_I32 is set for int32).  From the second call with the same
+    tensors, sizes, lr, flags and streams the library replays a CUDA graph of the step
+    (page-locked host tensors and non-default streams only)."""
     if copy_stream is None:
         dev = torch.cuda.current_device()
         if dev not in _copy_streams:

@@ -98,7 +98,7 @@ bool pinned_or_absent(const void* p, bool needed) {
 // ordinary streams not already being captured, every host buffer is page-locked
 // (a copy from pageable memory cannot be captured), and launch records are off.
 bool graph_eligible(cudaStream_t st, cudaStream_t cs, const tt_emb_host_batch& b, bool train,
-                    size_t idx_bytes, size_t out_bytes) {
+                    size_t out_bytes) {
   if (tt::g_prof_on) return false;
   for (cudaStream_t x : {st, cs}) {
     if (x == nullptr || x == cudaStreamLegacy || x == cudaStreamPerThread) return false;
@@ -106,7 +106,6 @@ bool graph_eligible(cudaStream_t st, cudaStream_t cs, const tt_emb_host_batch& b
     if (cudaStreamIsCapturing(x, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
       return false;
   }
-  (void)idx_bytes;
   return pinned_or_absent(b.h_indices, b.nnz > 0) && pinned_or_absent(b.h_offsets, true) &&
          pinned_or_absent(b.h_grad_out, train && out_bytes > 0) &&
          pinned_or_absent(b.h_out, out_bytes > 0);
@@ -237,7 +236,7 @@ extern "C" int tt_emb_step_host(float* const cores[3], float* const core_grads[3
   // the CUDA graph of that work (captured the second time the arguments come):
   // the same copies and kernels in the same order, without their launch costs.
   StepGraphs* gs = step_graphs();
-  if (gs && graph_eligible(st, cs, b, train, idx_bytes, out_bytes)) {
+  if (gs && graph_eligible(st, cs, b, train, out_bytes)) {
     StepGraph* g = nullptr;
     for (StepGraph& e : gs->e)
       if (e.valid && memcmp(&e.key, &key, sizeof key) == 0) g = &e;
